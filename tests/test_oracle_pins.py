@@ -1,0 +1,365 @@
+"""Pins for the oracle: it is checked against things other than itself.
+
+- hand-derived byte/nibble vectors (tests/golden/packing_vectors.json);
+- brute force: codes drawn directly, the dense matrix expanded with numpy and
+  multiplied with numpy's matmul;
+- exact special cases (integer data, implicit == explicit zero point, partial
+  block == zero-padded K, doubling the scales doubles Y);
+- every binary16 / bfloat16 pattern widened against numpy / torch;
+- routing against numpy's lexsort / scipy's softmax and crafted ties;
+- the expert-sorted permutation against numpy's stable argsort;
+- a hand-built QMoE layer whose output has a closed form.
+"""
+import json
+import math
+import os
+import zlib
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import workloads as wl
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "packing_vectors.json")))
+
+
+def as_f64(x, dtype):
+    """Reference widening by library routines (numpy float16, torch bfloat16)."""
+    if dtype == "f32":
+        return np.asarray(x, np.float32).astype(np.float64)
+    if dtype == "f16":
+        return np.asarray(x, np.uint16).view(np.float16).astype(np.float64)
+    t = torch.from_numpy(np.ascontiguousarray(x, np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.double().numpy()
+
+
+# ------------------------------------------------------------- byte vectors
+
+@pytest.mark.parametrize("v", GOLD["int4"])
+def test_int4_nibble_vectors(v):
+    b = bytes.fromhex(v["bytes"])
+    packed = np.zeros((1, 16), np.uint8)
+    packed[0, :len(b)] = list(b)
+    K = 2 * len(b)
+    assert oracle.unpack_codes(packed, 1, K, 4, 32)[0].tolist() == v["codes"]
+    repacked = oracle.pack_codes(np.array([v["codes"]], np.uint8), 4, 32)
+    assert repacked[0, :len(b)].tobytes() == b and not repacked[0, len(b):].any()
+
+
+@pytest.mark.parametrize("v", GOLD["int3"])
+def test_int3_cross_byte_vectors(v):
+    b = bytes.fromhex(v["bytes"])
+    packed = np.zeros((1, 12), np.uint8)
+    packed[0, :3] = list(b)
+    assert oracle.unpack_codes(packed, 1, 8, 3, 32)[0].tolist() == v["codes"]
+    repacked = oracle.pack_codes(np.array([v["codes"]], np.uint8), 3, 32)
+    assert repacked[0, :3].tobytes() == b and not repacked[0, 3:].any()
+
+
+@pytest.mark.parametrize("v", GOLD["zero_points"])
+def test_zero_point_vectors(v):
+    codes = np.array([v["codes"]], np.uint8)
+    z = oracle.pack_zero_points(codes, v["bits"])
+    assert z[0].tobytes() == bytes.fromhex(v["bytes"])
+    assert oracle.unpack_zero_points(z, 1, len(v["codes"]), v["bits"])[0].tolist() == v["codes"]
+
+
+def test_int3_rows_restart_on_a_byte():
+    # K=32, bs=32: each row is one 12-byte blob; row 1 starts at byte 12.
+    codes = np.zeros((2, 32), np.uint8)
+    codes[1, 0] = 7
+    codes[0, 31] = 5  # last code of row 0 sits in bits 93..95 of the row stream
+    p = oracle.pack_codes(codes, 3, 32)
+    assert p.shape == (2, 12)
+    assert p[1, 0] == 0x07 and not p[1, 1:].any()
+    assert p[0, 11] == 5 << 5 and not p[0, :11].any()
+
+
+def test_int4_row_and_block_strides():
+    # Tiny-case shape: N=128, K=256, bs=32 -> 8 blobs of 16 bytes, row stride 128 bytes.
+    N, K, bs = 128, 256, 32
+    packed = np.zeros((N, 128), np.uint8)
+    for n in range(N):
+        for b in range(8):
+            packed[n, 16 * b:16 * (b + 1)] = (37 * n + 11 * b + 3) & 0xFF
+    codes = oracle.unpack_codes(packed, N, K, 4, bs)
+    for n in (0, 1, 77, 127):
+        for k in range(K):
+            v = (37 * n + 11 * (k // 32) + 3) & 0xFF
+            assert codes[n, k] == (v & 0xF if k % 2 == 0 else v >> 4)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_pack_unpack_roundtrip(bits, bs):
+    g = wl.rng(1)
+    K = 2 * bs + 13
+    codes = g.integers(0, 1 << bits, size=(7, K), dtype=np.uint8)
+    packed = oracle.pack_codes(codes, bits, bs)
+    assert packed.shape == (7, oracle.row_bytes(K, bits, bs))
+    assert np.array_equal(oracle.unpack_codes(packed, 7, K, bits, bs), codes)
+    # canonical bytes survive unpack -> pack
+    assert np.array_equal(oracle.pack_codes(oracle.unpack_codes(packed, 7, K, bits, bs), bits, bs), packed)
+
+
+# ------------------------------------------------------ widening of scalars
+
+def test_every_f16_pattern_widens_like_numpy():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    N = pats.size
+    codes = np.full((N, 32), 9, np.uint8)  # 9 - implicit zero point 8 = 1, so w = scale
+    packed = oracle.pack_codes(codes, 4, 32)
+    w = oracle.dequantize(packed, pats.reshape(N, 1), "f16", None, N, 32, 4, 32)[:, 0]
+    ref = pats.view(np.float16).astype(np.float64)
+    assert np.array_equal(w, ref, equal_nan=True)
+
+
+def test_every_bf16_pattern_widens_like_torch():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    N = pats.size
+    codes = np.full((N, 32), 5, np.uint8)  # INT3: 5 - implicit 4 = 1
+    packed = oracle.pack_codes(codes, 3, 32)
+    w = oracle.dequantize(packed, pats.reshape(N, 1), "bf16", None, N, 32, 3, 32)[:, 0]
+    assert np.array_equal(w, as_f64(pats, "bf16"), equal_nan=True)
+
+
+# ------------------------------------------------------------ brute force
+
+def _case(g, N, K, bits, bs, with_zp, s_dtype):
+    nb = oracle.n_blocks(K, bs)
+    codes = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    packed = oracle.pack_codes(codes, bits, bs)
+    scales = wl.uniform(g, (N, nb), 0.005, 0.02, s_dtype)
+    zc = g.integers(0, 1 << bits, size=(N, nb), dtype=np.uint8) if with_zp else None
+    zp = oracle.pack_zero_points(zc, bits) if with_zp else None
+    z = zc.astype(np.float64) if with_zp else np.full((N, nb), float(1 << (bits - 1)))
+    s = as_f64(scales, s_dtype)
+    W = np.repeat(s, bs, axis=1)[:, :K] * (codes.astype(np.float64) - np.repeat(z, bs, axis=1)[:, :K])
+    return packed, scales, zp, W
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("with_zp", [False, True])
+@pytest.mark.parametrize("a_dtype,s_dtype", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"), ("bf16", "f32")])
+def test_brute_force_expand_then_multiply(bits, bs, with_zp, a_dtype, s_dtype):
+    g = wl.rng(zlib.crc32(repr((bits, bs, with_zp, a_dtype, s_dtype)).encode()))
+    N, M = 6, 3
+    K = bs + 17  # one full block plus a partial one
+    packed, scales, zp, W = _case(g, N, K, bits, bs, with_zp, s_dtype)
+    assert np.array_equal(oracle.dequantize(packed, scales, s_dtype, zp, N, K, bits, bs), W)
+    A = wl.normal(g, (M, K), a_dtype)
+    Y = oracle.mnb_matmul(A, a_dtype, packed, scales, s_dtype, zp, N, K, bits, bs)
+    ref = as_f64(A, a_dtype).reshape(M, K) @ W.T
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_selected_rows_match_full_output():
+    g = wl.rng(5)
+    N, K, M = 9, 96, 11
+    packed, scales, _ = wl.quantized_weight(g, N, K, 4, 32)
+    A = wl.normal(g, (M, K))
+    full = oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, 4, 32, threads=3)
+    part = oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, 4, 32, mrows=[10, 0, 4])
+    assert np.array_equal(part, full[[10, 0, 4]])
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_integer_data_is_exact(bits):
+    g = wl.rng(7)
+    N, K, M, bs = 13, 2048, 2, 64
+    codes = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    packed = oracle.pack_codes(codes, bits, bs)
+    nb = K // bs
+    zp = oracle.pack_zero_points(np.zeros((N, nb), np.uint8), bits)
+    scales = np.ones((N, nb), np.float32)
+    A = g.integers(-4, 5, size=(M, K)).astype(np.float32)
+    Y = oracle.mnb_matmul(A, "f32", packed, scales, "f32", zp, N, K, bits, bs)
+    exact = A.astype(np.int64) @ codes.astype(np.int64).T
+    assert np.array_equal(Y, exact.astype(np.float64))
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_implicit_equals_explicit_midpoint(bits):
+    g = wl.rng(8)
+    N, K, bs = 10, 320, 32
+    packed, scales, _ = wl.quantized_weight(g, N, K, bits, bs)
+    nb = K // bs
+    zp = oracle.pack_zero_points(np.full((N, nb), 1 << (bits - 1), np.uint8), bits)
+    A = wl.normal(g, (2, K))
+    a = oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, bits, bs)
+    b = oracle.mnb_matmul(A, "f32", packed, scales, "f32", zp, N, K, bits, bs)
+    assert np.array_equal(a, b)
+
+
+def test_doubling_scales_doubles_output():
+    g = wl.rng(9)
+    N, K = 12, 200
+    packed, scales, zp = wl.quantized_weight(g, N, K, 3, 64, with_zp=True)
+    A = wl.normal(g, (3, K))
+    a = oracle.mnb_matmul(A, "f32", packed, scales, "f32", zp, N, K, 3, 64)
+    b = oracle.mnb_matmul(A, "f32", packed, scales * np.float32(2), "f32", zp, N, K, 3, 64)
+    assert np.array_equal(b, 2 * a)
+
+
+@pytest.mark.parametrize("K,Kpad,bs", [(2072, 2080, 32), (2080, 2112, 64), (2080, 2176, 128)])
+def test_partial_block_equals_zero_padded_k(K, Kpad, bs):
+    g = wl.rng(10)
+    N = 8
+    packed, scales, _ = wl.quantized_weight(g, N, K, 4, bs)
+    assert oracle.n_blocks(K, bs) == oracle.n_blocks(Kpad, bs)
+    A = wl.normal(g, (2, K))
+    Ap = np.zeros((2, Kpad), np.float32)
+    Ap[:, :K] = A
+    a = oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, 4, bs)
+    b = oracle.mnb_matmul(Ap, "f32", packed, scales, "f32", None, N, Kpad, 4, bs)
+    # the padded columns hold random (non-canonical) codes; they meet zero activations
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- routing
+
+def test_route_equal_logits():
+    idx, w = oracle.route(np.zeros((3, 16), np.float32), 4, True)
+    assert (idx == np.arange(4)).all() and (w == 0.25).all()
+    idx, w = oracle.route(np.zeros((2, 16), np.float32), 4, False)
+    assert (idx == np.arange(4)).all() and (w == 1 / 16).all()
+
+
+def test_route_ties_go_to_lower_index():
+    logits = np.array([[1, 3, 3, 2, 3], [0, 0, -1, 0, 5]], np.float32)
+    idx, _ = oracle.route(logits, 3, True)
+    assert idx.tolist() == [[1, 2, 4], [4, 0, 1]]
+    # -0.0 and +0.0 compare equal
+    idx, _ = oracle.route(np.array([[-0.0, 0.0, -1.0]], np.float32), 2, True)
+    assert idx.tolist() == [[0, 1]]
+
+
+def test_route_k_equals_e_is_a_stable_descending_sort():
+    g = wl.rng(11)
+    logits = np.round(g.standard_normal((20, 32)) * 2).astype(np.float32)  # many ties
+    idx, _ = oracle.route(logits, 32, True)
+    for t in range(20):
+        assert idx[t].tolist() == np.lexsort((np.arange(32), -logits[t])).tolist()
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_route_weights_against_scipy_softmax(normalize):
+    g = wl.rng(12)
+    logits = wl.router_logits(g, 50, 128, skew=True)
+    idx, w = oracle.route(logits, 8, normalize)
+    for t in range(50):
+        assert len(set(idx[t].tolist())) == 8
+        top = np.sort(logits[t])[::-1][:8]
+        assert np.array_equal(logits[t][idx[t]], top)
+        if normalize:
+            ref = scipy.special.softmax(logits[t][idx[t]].astype(np.float64))
+            assert abs(w[t].sum() - 1) < 1e-14
+        else:
+            ref = scipy.special.softmax(logits[t].astype(np.float64))[idx[t]]
+        assert np.allclose(w[t], ref, rtol=1e-13, atol=0)
+
+
+def test_permute_is_a_stable_expert_sort():
+    g = wl.rng(13)
+    T, k, E = 37, 8, 128
+    idx, _ = oracle.route(wl.router_logits(g, T, E, skew=True), k, True)
+    counts, offsets, perm = oracle.permute(idx, E)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert offsets[0] == 0 and offsets[-1] == T * k and np.array_equal(np.diff(offsets), counts)
+    assert np.array_equal(perm, np.argsort(idx.ravel(), kind="stable"))
+
+
+# ------------------------------------------------------------------- QMoE
+
+def _unit_rows(rows, K, bits, bs, col_of_row, value=1):
+    """Packed rows with code z+value at column col_of_row[r] and z elsewhere (z implicit)."""
+    z = 1 << (bits - 1)
+    codes = np.full((rows, K), z, np.uint8)
+    for r, c in enumerate(col_of_row):
+        if c is not None:
+            codes[r, c] = z + value
+    return oracle.pack_codes(codes, bits, bs)
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+@pytest.mark.parametrize("bits", [(3, 3), (4, 3), (3, 4), (4, 4)])
+def test_qmoe_hand_built_layer_closed_form(layout, bits):
+    """Expert 1's FC1 gate rows are unit vectors, its up rows are 2x unit vectors and its
+    FC2 is the identity, so y_n = w * silu(x_n) * 2 x_n; expert 0 (gate 1x, up 1x) adds
+    w' * silu(x_n) * x_n.  Scales are 1 (exact in fp16), X is exact in fp16."""
+    b1, b2 = bits
+    H = I = 32
+    bs = 32
+    E = 3
+    x = np.linspace(-3, 3, H).round(3)
+    X = wl.cast(x.reshape(1, H), "f16")
+    xv = X.view(np.float16).astype(np.float64)[0]
+    gate_row = (lambda i: 2 * i) if layout == "interleaved" else (lambda i: i)
+    up_row = (lambda i: 2 * i + 1) if layout == "interleaved" else (lambda i: I + i)
+    fc1 = np.zeros((E, 2 * I, oracle.row_bytes(H, b1, bs)), np.uint8)
+    fc2 = np.zeros((E, H, oracle.row_bytes(I, b2, bs)), np.uint8)
+    for e, up_val in ((0, 1), (1, 2), (2, 3)):
+        gcols = [None] * (2 * I)
+        for i in range(I):
+            gcols[gate_row(i)] = i
+        fc1[e] = _unit_rows(2 * I, H, b1, bs, gcols, 1)
+        ucodes = oracle.unpack_codes(fc1[e], 2 * I, H, b1, bs)
+        for i in range(I):
+            ucodes[up_row(i)] = 1 << (b1 - 1)
+            ucodes[up_row(i), i] += up_val
+        fc1[e] = oracle.pack_codes(ucodes, b1, bs)
+        fc2[e] = _unit_rows(H, I, b2, bs, list(range(H)), 1)
+    s1 = wl.cast(np.ones((E, 2 * I, 1)), "f16")
+    s2 = wl.cast(np.ones((E, H, 1)), "f16")
+    d = np.float32(math.log(3.0))
+    logits = np.array([[d, 0.0, -4.0]], np.float32)  # experts 0 and 1 selected, weights 3/4, 1/4
+    Y = oracle.qmoe(X, "f16", logits, 2, True, fc1, s1, None, b1, fc2, s2, None, b2, I, bs, layout)
+    e = math.exp(float(d))
+    w0, w1 = e / (e + 1), 1 / (e + 1)
+    silu = xv / (1 + np.exp(-xv))
+    ref = w0 * silu * xv + w1 * silu * 2 * xv
+    assert np.allclose(Y[0], ref, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+def test_qmoe_single_expert_is_two_matmuls(layout):
+    g = wl.rng(14)
+    T, H, I, bs = 3, 64, 64, 32
+    d = wl.moe_layer(g, T, H, I, 1, 3, 4, bs, "bf16", with_zp=True)
+    Y = oracle.qmoe(d["X"], "bf16", d["logits"], 1, True, d["fc1_w"], d["fc1_scales"], d["fc1_zp"],
+                    3, d["fc2_w"], d["fc2_scales"], d["fc2_zp"], 4, I, bs, layout)
+    GU = oracle.mnb_matmul(d["X"], "bf16", d["fc1_w"][0], d["fc1_scales"][0], "bf16", d["fc1_zp"][0],
+                           2 * I, H, 3, bs)
+    gate = GU[:, 0::2] if layout == "interleaved" else GU[:, :I]
+    up = GU[:, 1::2] if layout == "interleaved" else GU[:, I:]
+    h = gate / (1 + np.exp(-gate)) * up
+    W2 = oracle.dequantize(d["fc2_w"][0], d["fc2_scales"][0], "bf16", d["fc2_zp"][0], H, I, 4, bs)
+    assert np.allclose(Y, h @ W2.T, rtol=1e-12, atol=1e-12)
+
+
+def test_qmoe_token_subset_and_fc2_scale_doubling():
+    g = wl.rng(15)
+    T, H, I, E, bs = 5, 64, 32, 6, 32
+    d = wl.moe_layer(g, T, H, I, E, 4, 3, bs, "f16", skew=True)
+    args = lambda s2: (d["X"], "f16", d["logits"], 3, True, d["fc1_w"], d["fc1_scales"], None, 4,
+                       d["fc2_w"], s2, None, 3, I, bs)
+    full = oracle.qmoe(*args(d["fc2_scales"]), threads=2)
+    sub = oracle.qmoe(*args(d["fc2_scales"]), tokens=[4, 1])
+    assert np.array_equal(sub, full[[4, 1]])
+    s2x = wl.cast(d["fc2_scales"].view(np.float16).astype(np.float32) * 2, "f16")
+    assert np.array_equal(oracle.qmoe(*args(s2x)), 2 * full)
+
+
+def test_qmoe_unnormalised_weights_are_softmax_probabilities():
+    g = wl.rng(16)
+    T, H, I, E, bs = 2, 32, 32, 4, 32
+    d = wl.moe_layer(g, T, H, I, E, 4, 4, bs, "f16")
+    one = lambda k, norm: oracle.qmoe(d["X"], "f16", d["logits"], k, norm, d["fc1_w"], d["fc1_scales"],
+                                      None, 4, d["fc2_w"], d["fc2_scales"], None, 4, I, bs)
+    # with k = E and no renormalisation the weights are the full softmax, which sums to one,
+    # so the result equals the renormalised one up to rounding
+    assert np.allclose(one(E, False), one(E, True), rtol=1e-13, atol=1e-13)
