@@ -1,0 +1,168 @@
+/*
+ * mnb.h -- C ABI of the GB300 (sm_103a) library for block-quantized
+ * weight-only matmul (MatMulNBits) and the QMoE expert FFN built on it.
+ *
+ * Shared conventions
+ * ------------------
+ * Pointers.  Every tensor argument is a device pointer owned by the caller,
+ * except mnb_validate_host(), which reads host buffers.  The library keeps no
+ * state between calls and never repacks weights: packed weights are consumed
+ * in the layout below on every call ("Qwen3 Missing-Kernel Implementation
+ * Plan", PR sequence rows K01/K02: reuse constant packed weights, no repacking).
+ *
+ * Streams.  `stream` is a cudaStream_t (0 = the legacy default stream).  Calls
+ * enqueue asynchronous work on it and return without synchronising, except
+ * mnb_get_last_device_error(), which synchronises `stream`.
+ *
+ * Layouts (all dense, row-major, C order):
+ *   bs = block_size, nb = ceil(K / bs), blob = bs * bits / 8 bytes.
+ *   B_packed     uint8 [N, nb, blob].  Row n is one stream of K codes of width
+ *                `bits`: code k occupies stream bits bits*k .. bits*k+bits-1,
+ *                least significant bit first, stream bit i being bit i%8 of
+ *                byte i/8 (so an INT4 byte holds column 2j in its low nibble and
+ *                2j+1 in its high nibble, and 3-bit codes cross byte
+ *                boundaries).  Codes at k >= K in the last blob are padding and
+ *                are never read into a result ("INT3 QMoE CUDA correctness
+ *                baseline and Qwen experimental results", section "P0: Portable
+ *                Format and Numerical References": row-local LSB-first packing).
+ *   scales       [N, nb], dtype `scale_dtype`.
+ *   zero_points  uint8 [N, ceil(nb * bits / 8)]: one code of width `bits` per
+ *                block, packed per row by the same LSB-first rule ("packed
+ *                per-row block zero points", same section).  NULL selects the
+ *                implicit zero point 2^(bits-1): 8 for INT4, 4 for INT3 (the
+ *                offset-4 decoding (code - 4) * scale).
+ *   Dequantised weight: w[n, k] = scale[n, k/bs] * (code[n, k] - zp[n, k/bs]).
+ *
+ * Supported set.  bits in {3, 4}; block_size in {32, 64, 128}; activation and
+ * output dtypes f32 / f16 / bf16 for mnb_matmul (f16 / bf16 for QMoE); scale
+ * dtype f32 or equal to the activation dtype (QMoE: equal).  B_packed must be
+ * 16-byte aligned, the other tensors aligned to their element size.  Anything
+ * else returns MNB_ERR_UNSUPPORTED before any work is enqueued; no call ever
+ * falls back to a CPU path or to a different kernel family silently.
+ *
+ * Errors.  Metadata is validated on the host before any launch (payloads are
+ * never read on the host, except by mnb_validate_host).  Launch failures return
+ * MNB_ERR_CUDA.  Kernels that wait on on-chip barriers give up after a bounded
+ * time, record MNB_ERR_TIMEOUT in a device error word and return;
+ * mnb_get_last_device_error() reports and clears that word.
+ */
+#ifndef MNB_H_
+#define MNB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MNB_OK = 0,
+    MNB_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, k > E, ... */
+    MNB_ERR_UNSUPPORTED = 2,   /* valid request outside the supported set */
+    MNB_ERR_SIZE_OVERFLOW = 3, /* a byte count does not fit in 63 bits */
+    MNB_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    MNB_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    MNB_ERR_TIMEOUT = 6,       /* a bounded on-device wait gave up */
+    MNB_ERR_CONTENT = 7        /* mnb_validate_host found malformed content */
+} mnb_status;
+
+typedef enum { MNB_F32 = 0, MNB_F16 = 1, MNB_BF16 = 2 } mnb_dtype;
+
+/* Row order of a fused FC1 weight of 2I rows: INTERLEAVED puts gate_i at row 2i
+ * and up_i at row 2i+1 (the fused interleaved gate/up of "INT3 QMoE CUDA
+ * correctness baseline...", "P1: Compatible QMoE v1 Extension"); CONCAT puts
+ * gate_i at row i and up_i at row I+i. */
+typedef enum { MNB_FC1_INTERLEAVED = 0, MNB_FC1_CONCAT = 1 } mnb_fc1_layout;
+
+/* ABI-identical to cudaStream_t; declared here so that callers need no CUDA headers. */
+typedef struct CUstream_st* mnb_stream_t;
+
+/* ------------------------------------------------------------ MatMulNBits */
+
+/* Bytes of device workspace mnb_matmul needs for this problem (0 = none, in
+ * which case workspace may be NULL).  The bound depends only on the arguments. */
+mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, int block_size,
+                                     mnb_dtype a_dtype, size_t* bytes);
+
+/* Y[M, N] = A[M, K] . W^T with W[N, K] dequantised from B_packed/scales/
+ * zero_points on the fly ("Qwen3 Missing-Kernel Implementation Plan", rows
+ * K01 MatMulNBits contract, K02 M=1 decode GEMV, K03 small-M and prefill GEMM
+ * with partial blocks and output tails).  Any M >= 1, K >= 1, N >= 1.
+ * Accumulation is fp32; the dequantised weight is formed in fp32 (SIMT paths)
+ * or rounded to bf16/fp16 in shared memory before a tensor-core contraction
+ * (M >= 16 with f16/bf16 activations).  Y is written in y_dtype with
+ * round-to-nearest-even. */
+mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
+                      const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                      const uint8_t* zero_points, int64_t N, int bits, int block_size, void* Y,
+                      mnb_dtype y_dtype, void* workspace, size_t workspace_bytes,
+                      mnb_stream_t stream);
+
+/* ------------------------------------------------------------------- QMoE */
+
+/* Bytes of device workspace qmoe_forward needs (routing tables, the SwiGLU
+ * activations between FC1 and FC2, the FC2 outputs before the combine). */
+mnb_status qmoe_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int k,
+                               mnb_dtype act_dtype, size_t* bytes);
+
+/* One QMoE expert-FFN layer ("INT3 QMoE CUDA correctness baseline and Qwen
+ * experimental results", Summary and "P1: Compatible QMoE v1 Extension";
+ * routing as in "feat(qwen4): component kernels extracted from the brick PRs"):
+ *   route:   p = softmax(router_logits[t, :]) in fp32; the k experts with the
+ *            largest logits, ties to the lower index; weights p[idx] divided
+ *            by their sum when normalize_topk != 0, else p[idx].
+ *   FC1:     g, u = the gate and up rows of expert e applied to X[t]
+ *            (fc1_w [E, 2I, H/bs, bs*fc1_bits/8], fc1_scales [E, 2I, H/bs],
+ *            fc1_zp [E, 2I, ceil((H/bs)*fc1_bits/8)] or NULL).
+ *   SwiGLU:  h = silu(g) * u = g * sigmoid(g) * u.
+ *   FC2:     o = expert e's down projection of h (fc2_w [E, H, I/bs, bs*fc2_bits/8],
+ *            fc2_scales [E, H, I/bs], fc2_zp [E, H, ceil((I/bs)*fc2_bits/8)] or NULL).
+ *   combine: Y[t] = sum_{j<k} w[t, j] * o[t, j], ascending j, fp32, then act_dtype.
+ * X, Y and the scales have act_dtype (f16 or bf16); router_logits are fp32
+ * [T, E].  H and I must be multiples of block_size; 1 <= k <= E <= 1024.
+ * Never materialises a dequantised expert matrix in global memory. */
+mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H,
+                        const float* router_logits, int64_t E, int k, int normalize_topk,
+                        const uint8_t* fc1_w, const void* fc1_scales, const uint8_t* fc1_zp,
+                        int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                        const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
+                        mnb_fc1_layout fc1_layout, void* Y, void* workspace,
+                        size_t workspace_bytes, mnb_stream_t stream);
+
+/* The routing step alone: topk_idx int32 [T, k], topk_w fp32 [T, k]. */
+mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk,
+                      int32_t* topk_idx, float* topk_w, mnb_stream_t stream);
+
+/* Expert-sorted order of routed (token, slot) pairs: counts int32 [E];
+ * offsets int32 [E+1] = exclusive prefix sum of counts; perm int32 [T*k] lists
+ * the flat pair index t*k + j grouped by expert, ascending inside an expert. */
+mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, mnb_stream_t stream);
+
+/* ------------------------------------------------------ diagnostics, tools */
+
+/* codes uint8 [rows, K] = the raw codes of B_packed (layout above), bit-exact. */
+mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits,
+                            int block_size, uint8_t* codes, mnb_stream_t stream);
+
+/* Host-side content check of one packed projection (host buffers): exact
+ * sizes are implied by the arguments; scales must be finite and >= 0; every
+ * padding bit of the weights and of the zero points must be zero ("canonical
+ * padding" of "INT3 QMoE CUDA correctness baseline...", P0 and P1 sections).
+ * Returns MNB_OK or MNB_ERR_CONTENT.  Never called by the compute entry points. */
+mnb_status mnb_validate_host(const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                             const uint8_t* zero_points, int64_t N, int64_t K, int bits,
+                             int block_size);
+
+/* Synchronises `stream`, then returns and clears the device error word
+ * (MNB_OK when no kernel recorded an error). */
+mnb_status mnb_get_last_device_error(mnb_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* mnb_status_string(mnb_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MNB_H_ */

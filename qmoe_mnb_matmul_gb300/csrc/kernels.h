@@ -1,0 +1,53 @@
+// kernels.h -- host-side launchers of the sm_103a kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mnb {
+
+// ------------------------------------------------------------- SIMT GEMV
+// Y[M, N] = A[M, K] . W^T for small M, streaming packed rows through shared memory.
+struct GemvArgs {
+    const void* A;
+    int a_dtype;
+    int64_t M, K;
+    const uint8_t* B;
+    const void* scales;
+    const uint8_t* zp;
+    int64_t N;
+    int bits, bs, nb;
+    int64_t row_bytes;
+    int zp_row_bytes;
+    void* Y;
+    int y_dtype;
+    int64_t y_ld;          // row stride of Y in elements (N for a plain matmul)
+    int rows_per_block;    // RC: rows of B staged per pipeline stage
+    int n_blocks;          // ceil(N / RC)
+    int chunks;            // C = nb * bs / 32 (32 codes per chunk)
+};
+
+// Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
+// instantiation.  Returns cudaSuccess or the launch error; cudaErrorNotSupported
+// when the shape does not fit the kernel's shared-memory plan.
+cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl,
+                        cudaStream_t stream);
+
+// Shared memory the GEMV plan needs for (K, bits, bs, scale dtype, M); 0 if unsupported.
+size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype);
+
+// --------------------------------------------------------------- unpack
+cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
+                                uint8_t* codes, cudaStream_t stream);
+
+// ------------------------------------------------------------- routing
+cudaError_t launch_route(const float* logits, int64_t T, int64_t E, int k, int normalize,
+                         int32_t* idx, float* w, cudaStream_t stream);
+cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
+
+// Per-translation-unit device error words (read and cleared; 0 = none).
+cudaError_t gemv_take_error(unsigned int* out);
+cudaError_t qmoe_take_error(unsigned int* out);
+
+}  // namespace mnb

@@ -1,0 +1,302 @@
+// mnb_api.cu -- the extern "C" entry points declared in include/mnb.h:
+// host-side metadata validation (payloads are never read on the host), plan
+// selection and kernel launches on the caller's stream.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "qmoe.h"
+
+namespace mnb {
+
+namespace {
+
+bool valid_dtype(int d) { return d == MNB_F32 || d == MNB_F16 || d == MNB_BF16; }
+bool valid_bits(int b) { return b == 3 || b == 4; }
+bool valid_bs(int bs) { return bs == 32 || bs == 64 || bs == 128; }
+size_t dsize(int d) { return d == MNB_F32 ? 4 : 2; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a * b without overflow past 2^62 (the largest byte count we accept).
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > (int64_t(1) << 62) / a) return false;
+    *out = a * b;
+    return true;
+}
+
+int sm_count_current() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+mnb_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MNB_OK;
+    if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
+    return MNB_ERR_CUDA;
+}
+
+// Byte counts of one packed projection [N, K]; false on overflow.
+struct ProjBytes {
+    int64_t nb, row_bytes, weight, scales, zp_row, zp;
+};
+bool proj_bytes(int64_t N, int64_t K, int bits, int bs, int sdt, ProjBytes* p) {
+    p->nb = (K + bs - 1) / bs;
+    p->row_bytes = p->nb * bs * bits / 8;
+    p->zp_row = (p->nb * bits + 7) / 8;
+    return mul_ok(N, p->row_bytes, &p->weight) && mul_ok(N, p->nb * int64_t(dsize(sdt)), &p->scales) &&
+           mul_ok(N, p->zp_row, &p->zp);
+}
+
+}  // namespace
+}  // namespace mnb
+
+using namespace mnb;
+
+extern "C" {
+
+const char* mnb_status_string(mnb_status s) {
+    switch (s) {
+        case MNB_OK: return "MNB_OK";
+        case MNB_ERR_INVALID_ARG: return "MNB_ERR_INVALID_ARG";
+        case MNB_ERR_UNSUPPORTED: return "MNB_ERR_UNSUPPORTED";
+        case MNB_ERR_SIZE_OVERFLOW: return "MNB_ERR_SIZE_OVERFLOW";
+        case MNB_ERR_WORKSPACE: return "MNB_ERR_WORKSPACE";
+        case MNB_ERR_CUDA: return "MNB_ERR_CUDA";
+        case MNB_ERR_TIMEOUT: return "MNB_ERR_TIMEOUT";
+        case MNB_ERR_CONTENT: return "MNB_ERR_CONTENT";
+    }
+    return "MNB_ERR_UNKNOWN";
+}
+
+mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
+    unsigned int first = 0;
+    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error};
+    for (auto take : takers) {
+        unsigned int v = 0;
+        if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;
+        if (first == 0) first = v;
+    }
+    return static_cast<mnb_status>(first);
+}
+
+mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, int block_size,
+                                     mnb_dtype a_dtype, size_t* bytes) {
+    if (!bytes) return MNB_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || N < 1 || !valid_dtype(a_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    *bytes = 0;
+    return MNB_OK;
+}
+
+mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, const uint8_t* B_packed,
+                      const void* scales, mnb_dtype scale_dtype, const uint8_t* zero_points, int64_t N,
+                      int bits, int block_size, void* Y, mnb_dtype y_dtype, void* workspace,
+                      size_t workspace_bytes, mnb_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!A || !B_packed || !scales || !Y) return MNB_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || N < 1) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (scale_dtype != MNB_F32 && scale_dtype != a_dtype) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(B_packed, 16) || !aligned(scales, 16) || !aligned(A, dsize(a_dtype)) ||
+        !aligned(Y, dsize(y_dtype)))
+        return MNB_ERR_UNSUPPORTED;
+    ProjBytes pb;
+    int64_t tmp;
+    if (!proj_bytes(N, K, bits, block_size, scale_dtype, &pb) || !mul_ok(M, K * 4, &tmp) ||
+        !mul_ok(M, N * 4, &tmp))
+        return MNB_ERR_SIZE_OVERFLOW;
+    if (N > (int64_t(1) << 31)) return MNB_ERR_UNSUPPORTED;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+    if (gemv_smem_bytes(M, K, bits, block_size, scale_dtype) == 0) return MNB_ERR_UNSUPPORTED;
+
+    GemvArgs a = {};
+    a.A = A;
+    a.a_dtype = a_dtype;
+    a.M = M;
+    a.K = K;
+    a.B = B_packed;
+    a.scales = scales;
+    a.zp = zero_points;
+    a.N = N;
+    a.bits = bits;
+    a.bs = block_size;
+    a.nb = static_cast<int>(pb.nb);
+    a.row_bytes = pb.row_bytes;
+    a.zp_row_bytes = static_cast<int>(pb.zp_row);
+    a.Y = Y;
+    a.y_dtype = y_dtype;
+    a.y_ld = N;
+    a.chunks = static_cast<int>(pb.nb * block_size / 32);
+    return from_cuda(launch_gemv(a, scale_dtype, sms, /*pdl=*/true, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits, int block_size,
+                            uint8_t* codes, mnb_stream_t stream) {
+    if (!B_packed || !codes || rows < 1 || K < 1) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    ProjBytes pb;
+    int64_t tmp;
+    if (!proj_bytes(rows, K, bits, block_size, MNB_F32, &pb) || !mul_ok(rows, K, &tmp))
+        return MNB_ERR_SIZE_OVERFLOW;
+    return from_cuda(launch_unpack_codes(B_packed, rows, K, bits, block_size, codes,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk, int32_t* topk_idx,
+                      float* topk_w, mnb_stream_t stream) {
+    if (!logits || !topk_idx || !topk_w) return MNB_ERR_INVALID_ARG;
+    if (T < 1 || E < 1 || k < 1 || k > E) return MNB_ERR_INVALID_ARG;
+    if (E > 1024) return MNB_ERR_UNSUPPORTED;
+    int64_t tmp;
+    if (!mul_ok(T, E * 4, &tmp) || T > (int64_t(1) << 31)) return MNB_ERR_SIZE_OVERFLOW;
+    return from_cuda(launch_route(logits, T, E, k, normalize_topk ? 1 : 0, topk_idx, topk_w,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
+                        int32_t* perm, mnb_stream_t stream) {
+    if (!topk_idx || !counts || !offsets || !perm) return MNB_ERR_INVALID_ARG;
+    if (T < 1 || k < 1 || E < 1 || k > E) return MNB_ERR_INVALID_ARG;
+    if (E > 1024) return MNB_ERR_UNSUPPORTED;
+    if (T * int64_t(k) >= (int64_t(1) << 31)) return MNB_ERR_SIZE_OVERFLOW;
+    return from_cuda(
+        launch_permute(topk_idx, T, k, E, counts, offsets, perm, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------- QMoE
+
+mnb_status qmoe_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int k, mnb_dtype act_dtype,
+                               size_t* bytes) {
+    if (!bytes) return MNB_ERR_INVALID_ARG;
+    if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return MNB_ERR_INVALID_ARG;
+    if (act_dtype != MNB_F16 && act_dtype != MNB_BF16) return MNB_ERR_UNSUPPORTED;
+    if (E > 1024) return MNB_ERR_UNSUPPORTED;
+    int64_t b = 0;
+    if (!qmoe_workspace_bytes(T, H, I, E, k, &b)) return MNB_ERR_SIZE_OVERFLOW;
+    *bytes = static_cast<size_t>(b);
+    return MNB_OK;
+}
+
+mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H, const float* router_logits,
+                        int64_t E, int k, int normalize_topk, const uint8_t* fc1_w, const void* fc1_scales,
+                        const uint8_t* fc1_zp, int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                        const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
+                        mnb_fc1_layout fc1_layout, void* Y, void* workspace, size_t workspace_bytes,
+                        mnb_stream_t stream) {
+    if (!X || !router_logits || !fc1_w || !fc1_scales || !fc2_w || !fc2_scales || !Y) return MNB_ERR_INVALID_ARG;
+    if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return MNB_ERR_INVALID_ARG;
+    if (fc1_layout != MNB_FC1_INTERLEAVED && fc1_layout != MNB_FC1_CONCAT) return MNB_ERR_INVALID_ARG;
+    if (act_dtype != MNB_F16 && act_dtype != MNB_BF16) return MNB_ERR_UNSUPPORTED;
+    if (!valid_bits(fc1_bits) || !valid_bits(fc2_bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (H % block_size != 0 || I % block_size != 0 || E > 1024) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(fc1_w, 16) || !aligned(fc2_w, 16) || !aligned(fc1_scales, 16) || !aligned(fc2_scales, 16) ||
+        !aligned(X, 2) || !aligned(Y, 2) || !aligned(router_logits, 4))
+        return MNB_ERR_UNSUPPORTED;
+    ProjBytes p1, p2;
+    int64_t w1, w2, tmp;
+    if (!proj_bytes(2 * I, H, fc1_bits, block_size, act_dtype, &p1) ||
+        !proj_bytes(H, I, fc2_bits, block_size, act_dtype, &p2) || !mul_ok(E, p1.weight, &w1) ||
+        !mul_ok(E, p2.weight, &w2) || !mul_ok(T, H * 4, &tmp) || !mul_ok(T, E * 4, &tmp))
+        return MNB_ERR_SIZE_OVERFLOW;
+    int64_t need = 0;
+    if (!qmoe_workspace_bytes(T, H, I, E, k, &need)) return MNB_ERR_SIZE_OVERFLOW;
+    if (!workspace || int64_t(workspace_bytes) < need) return MNB_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MNB_ERR_UNSUPPORTED;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+
+    QmoeArgs q = {};
+    q.X = X;
+    q.act_dtype = act_dtype;
+    q.T = T;
+    q.H = H;
+    q.I = I;
+    q.E = E;
+    q.k = k;
+    q.normalize = normalize_topk ? 1 : 0;
+    q.logits = router_logits;
+    q.fc1_w = fc1_w;
+    q.fc1_s = fc1_scales;
+    q.fc1_zp = fc1_zp;
+    q.fc1_bits = fc1_bits;
+    q.fc2_w = fc2_w;
+    q.fc2_s = fc2_scales;
+    q.fc2_zp = fc2_zp;
+    q.fc2_bits = fc2_bits;
+    q.bs = block_size;
+    q.fc1_layout = fc1_layout;
+    q.Y = Y;
+    q.workspace = workspace;
+    q.fc1 = {p1.nb, p1.row_bytes, p1.zp_row};
+    q.fc2 = {p2.nb, p2.row_bytes, p2.zp_row};
+    return from_cuda(launch_qmoe(q, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------ host validation
+
+static double host_scale(const void* s, int dt, int64_t i, bool* finite, bool* negative) {
+    if (dt == MNB_F32) {
+        float f;
+        std::memcpy(&f, static_cast<const char*>(s) + 4 * i, 4);
+        *finite = std::isfinite(f);
+        *negative = f < 0.f;
+        return f;
+    }
+    uint16_t h;
+    std::memcpy(&h, static_cast<const char*>(s) + 2 * i, 2);
+    const bool neg_sign = (h >> 15) != 0;
+    if (dt == MNB_F16) {
+        *finite = ((h >> 10) & 0x1F) != 0x1F;
+        *negative = neg_sign && (h & 0x7FFF) != 0;
+    } else {
+        *finite = ((h >> 7) & 0xFF) != 0xFF;
+        *negative = neg_sign && (h & 0x7FFF) != 0;
+    }
+    return 0.0;
+}
+
+mnb_status mnb_validate_host(const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                             const uint8_t* zero_points, int64_t N, int64_t K, int bits, int block_size) {
+    if (!B_packed || !scales || N < 1 || K < 1) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(scale_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    ProjBytes pb;
+    if (!proj_bytes(N, K, bits, block_size, scale_dtype, &pb)) return MNB_ERR_SIZE_OVERFLOW;
+    for (int64_t i = 0; i < N * pb.nb; ++i) {
+        bool fin = true, neg = false;
+        host_scale(scales, scale_dtype, i, &fin, &neg);
+        if (!fin || neg) return MNB_ERR_CONTENT;
+    }
+    // padding: weight stream bits [K*bits, row_bytes*8) and zero-point stream bits [nb*bits, zp_row*8)
+    auto padding_clear = [](const uint8_t* row, int64_t first_bit, int64_t nbytes) {
+        for (int64_t bit = first_bit; bit < nbytes * 8; ++bit)
+            if ((row[bit >> 3] >> (bit & 7)) & 1) return false;
+        return true;
+    };
+    for (int64_t n = 0; n < N; ++n) {
+        if (!padding_clear(B_packed + n * pb.row_bytes, K * bits, pb.row_bytes)) return MNB_ERR_CONTENT;
+        if (zero_points && !padding_clear(zero_points + n * pb.zp_row, pb.nb * bits, pb.zp_row))
+            return MNB_ERR_CONTENT;
+    }
+    return MNB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,579 @@
+// qmoe.cu -- one QMoE expert-FFN layer ("INT3 QMoE CUDA correctness baseline
+// and Qwen experimental results", Summary and "P1: Compatible QMoE v1
+// Extension"): routing, FC1 (fused gate/up) with SwiGLU, FC2 (down
+// projection) and the weighted combine, on packed INT3/INT4 experts that are
+// dequantised while their rows are consumed -- no dequantised expert matrix is
+// ever written to global memory ("prohibit all-expert floating-weight
+// materialization").
+//
+// Two SIMT plans share the packed-row machinery of gemv_core.cuh:
+//  * decode (T <= 8, k <= 8): two kernels.  Every CTA routes its own token
+//    (one warp, a few hundred logits), so no routing kernel sits on the
+//    critical path.  FC1 runs over (token, slot) x row blocks of the selected
+//    expert and writes h = silu(gate) * up in fp32.  FC2 runs over tokens x
+//    row blocks, streams the block's rows of all k selected experts and folds
+//    the weighted combine into its epilogue (fixed slot order).  FC2 is
+//    launched as a programmatic dependent: its prologue routes and pulls its
+//    experts' rows into L2 while FC1 is still running.
+//  * tiled (any T): route -> expert-sorted permutation -> tiles of <= 4 pairs
+//    of one expert -> FC1 tiles (gathered activations) -> FC2 tiles -> combine
+//    by token in fixed slot order.
+#include <algorithm>
+
+#include "common.cuh"
+#include "gemv_core.cuh"
+#include "kernels.h"
+#include "qmoe.h"
+#include "route_core.cuh"
+
+namespace mnb {
+
+namespace {
+
+using namespace gemv;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int R = 4;            // rows per warp unit (two gate/up pairs in FC1)
+constexpr int kTileM = 4;       // pairs per tile in the tiled plan
+constexpr int kDecodeMaxT = 8;
+constexpr int kDecodeMaxK = 8;
+constexpr int kPairsPerBlock = 16;  // FC1 gate/up pairs per CTA (32 rows)
+constexpr int kRowsPerBlock2 = 16;  // FC2 rows per CTA
+
+__host__ __device__ inline int64_t a256(int64_t x) { return (x + 255) / 256 * 256; }
+
+struct Ws {
+    int64_t idx, wts, counts, offsets, perm, inv, tiles, ntiles, h, o, total;
+};
+
+__host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
+    const int64_t t = (P + kTileM - 1) / kTileM + E;
+    return P < t ? P : t;
+}
+
+__host__ __device__ inline Ws ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int k) {
+    const int64_t P = T * k;
+    Ws w;
+    int64_t off = 0;
+    w.idx = off; off += a256(P * 4);
+    w.wts = off; off += a256(P * 4);
+    w.counts = off; off += a256(E * 4);
+    w.offsets = off; off += a256((E + 1) * 4);
+    w.perm = off; off += a256(P * 4);
+    w.inv = off; off += a256(P * 4);
+    w.tiles = off; off += a256(max_tiles(P, E) * 8);
+    w.ntiles = off; off += 256;
+    w.h = off; off += a256(P * I * 4);
+    w.o = off; off += a256(P * H * 4);
+    w.total = off;
+    return w;
+}
+
+bool use_decode(const QmoeArgs& q) { return q.T <= kDecodeMaxT && q.k <= kDecodeMaxK; }
+
+// --------------------------------------------------------- shared memory
+
+struct Fc1Plan {
+    int64_t a4, asum, w, s, total;
+};
+__host__ __device__ inline Fc1Plan fc1_plan(int MT, int C, int64_t row_bytes, int nb, int ssize) {
+    Fc1Plan p;
+    p.a4 = int64_t(MT) * 8 * C * 16;
+    p.asum = round_up(int64_t(MT) * C * 4, 128);
+    p.w = round_up(int64_t(2 * kPairsPerBlock) * row_bytes, 128);
+    p.s = round_up(int64_t(2 * kPairsPerBlock) * nb * ssize, 128);
+    p.total = 256 + p.a4 + p.asum + p.w + p.s;
+    return p;
+}
+
+struct Fc2Plan {
+    int64_t a4, asum, w, s, total;
+};
+__host__ __device__ inline Fc2Plan fc2_plan(int ACT, int C, int64_t row_bytes, int nb, int ssize) {
+    Fc2Plan p;
+    p.a4 = int64_t(ACT) * 8 * C * 16;
+    p.asum = round_up(int64_t(ACT) * C * 4, 128);
+    p.w = round_up(int64_t(kRowsPerBlock2) * row_bytes, 128);  // per expert slot
+    p.s = round_up(int64_t(kRowsPerBlock2) * nb * ssize, 128);
+    p.total = 256 + p.a4 + p.asum + int64_t(ACT) * (p.w + p.s);
+    return p;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// ------------------------------------------------------------------ FC1
+
+// FC1 + SwiGLU for one (activation group, expert) x block of kPairsPerBlock
+// gate/up pairs.  DECODE: blockIdx.x is the slot p = t*k + j and the CTA
+// routes token t itself; h row = p.  Tiled: blockIdx.x is a tile of <= MT
+// sorted pairs of one expert; h rows = sorted positions.
+template <int BITS, int ST, int MT, bool DECODE>
+__global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ QmoeArgs q) {
+    using S = typename DType<ST>::T;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = static_cast<int>(q.fc1.nb * q.bs / 32);
+    const int nb = static_cast<int>(q.fc1.nb);
+    const int64_t rb = q.fc1.row_bytes;
+    const Fc1Plan plan = fc1_plan(MT, C, rb, nb, sizeof(S));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int* s_int = reinterpret_cast<int*>(smem + 16);          // [0]=expert [1]=s0 [2]=cnt, [4..4+MT) rows
+    float* s_w = reinterpret_cast<float*>(smem + 128);      // routing weights (decode)
+    int* s_idx = reinterpret_cast<int*>(smem + 192);        // routing experts (decode)
+    float4* A4 = reinterpret_cast<float4*>(smem + 256);
+    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
+    const S* Sst = reinterpret_cast<const S*>(Wst + plan.w);
+
+    char* ws = static_cast<char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    float* h = reinterpret_cast<float*>(ws + L.h);
+    const int64_t P = q.T * q.k;
+
+    grid_dependency_wait();
+    if (DECODE) {
+        const int64_t p = blockIdx.x;
+        const int64_t t = p / q.k;
+        if (warp == 0) warp_route(q.logits + t * q.E, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, 1);
+        __syncthreads();
+        if (tid == 0) {
+            s_int[0] = s_idx[p % q.k];
+            s_int[1] = static_cast<int>(p);
+            s_int[2] = 1;
+            s_int[4] = static_cast<int>(t);
+        }
+    } else {
+        const int tile = blockIdx.x;
+        const int ntiles = *reinterpret_cast<const int*>(ws + L.ntiles);
+        if (tile >= ntiles) return;
+        if (tid == 0) {
+            const int2 ti = reinterpret_cast<const int2*>(ws + L.tiles)[tile];
+            const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+            const int* perm = reinterpret_cast<const int*>(ws + L.perm);
+            const int cnt = min(MT, offsets[ti.x + 1] - ti.y);
+            s_int[0] = ti.x;
+            s_int[1] = ti.y;
+            s_int[2] = cnt;
+            for (int m = 0; m < MT; ++m) s_int[4 + m] = m < cnt ? perm[ti.y + m] / q.k : -1;
+        }
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int e = s_int[0], s0 = s_int[1], cnt = s_int[2];
+    const int64_t I = q.I;
+    const int64_t pair0 = int64_t(blockIdx.y) * kPairsPerBlock;
+    const int pc = static_cast<int>(std::min<int64_t>(kPairsPerBlock, I - pair0));
+    const uint8_t* W1 = q.fc1_w + int64_t(e) * 2 * I * rb;
+    const S* S1 = static_cast<const S*>(q.fc1_s) + int64_t(e) * 2 * I * nb;
+    const bool inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
+    if (tid == 0) {
+        const uint32_t wrow = static_cast<uint32_t>(rb), srow = static_cast<uint32_t>(nb * sizeof(S));
+        const uint32_t total = 2u * pc * (wrow + srow);
+        mbar_arrive_expect_tx(bar, total);
+        uint8_t* Sdst = Wst + plan.w;
+        if (inter) {
+            bulk_g2s(Wst, W1 + 2 * pair0 * rb, 2 * pc * wrow, bar);
+            bulk_g2s(Sdst, S1 + 2 * pair0 * nb, 2 * pc * srow, bar);
+        } else {
+            bulk_g2s(Wst, W1 + pair0 * rb, pc * wrow, bar);
+            bulk_g2s(Wst + kPairsPerBlock * rb, W1 + (I + pair0) * rb, pc * wrow, bar);
+            bulk_g2s(Sdst, S1 + pair0 * nb, pc * srow, bar);
+            bulk_g2s(Sdst + kPairsPerBlock * nb * sizeof(S), S1 + (I + pair0) * nb, pc * srow, bar);
+        }
+    }
+    stage_activations<MT>(
+        A4, Asum, C,
+        [&](int m, int64_t kk) -> float {
+            const int t = m < cnt ? s_int[4 + m] : -1;
+            return (t >= 0 && kk < q.H) ? load_as_f32(q.X, q.act_dtype, int64_t(t) * q.H + kk) : 0.f;
+        },
+        tid, kThreads);
+    grid_launch_dependents();
+    const bool ok = mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+        mbar_wait(bar, 0);
+        return;
+    }
+    const int bs_shift = __ffs(q.bs) - 1;
+    constexpr int kZImplicit = 1 << (BITS - 1);
+    const uint8_t* Z1 = q.fc1_zp ? q.fc1_zp + int64_t(e) * 2 * I * q.fc1.zp_row : nullptr;
+
+    // Warp unit: pairs 2g and 2g+1 -> logical rows (gate 2g, up 2g, gate 2g+1, up 2g+1).
+    for (int g = warp; 2 * g < pc; g += kWarps) {
+        float out[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) out[r][m] = 0.f;
+        int lrow[R];      // row inside the staged block
+        int64_t grow[R];  // row inside the expert's FC1 weight
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int pq = min(2 * g + (r >> 1), pc - 1);
+            const int up = r & 1;
+            lrow[r] = inter ? 2 * pq + up : up * kPairsPerBlock + pq;
+            grow[r] = inter ? 2 * (pair0 + pq) + up : up * I + pair0 + pq;
+        }
+        for (int c = lane; c < C; c += 32) {
+            const int b = (c * 32) >> bs_shift;
+            uint32_t w[R][BITS];
+            float sc[R], zz[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                load_chunk<BITS>(Wst + int64_t(lrow[r]) * rb, c, w[r]);
+                sc[r] = to_f32(Sst[lrow[r] * nb + b]);
+                zz[r] = float(Z1 ? zero_point_code<BITS>(Z1 + grow[r] * q.fc1.zp_row, b) : kZImplicit);
+            }
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Asum, C, c, out);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out[r][m]);
+        if (lane == 0) {
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                const int pq = 2 * g + pp;
+                if (pq >= pc) break;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (m < cnt) h[int64_t(s0 + m) * I + pair0 + pq] = silu_mul(out[2 * pp][m], out[2 * pp + 1][m]);
+            }
+        }
+    }
+    (void)P;
+}
+
+// ------------------------------------------------------- FC2 (decode)
+
+// FC2 + combine for token t = blockIdx.x over rows [n0, n0 + 16) of H: the
+// block's rows of all k selected experts are streamed, each multiplied with
+// that slot's h, and combined with the routing weights in slot order.
+template <int BITS, int ST>
+__global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_constant__ QmoeArgs q) {
+    using S = typename DType<ST>::T;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = q.k;
+    const int C = static_cast<int>(q.fc2.nb * q.bs / 32);
+    const int nb = static_cast<int>(q.fc2.nb);
+    const int64_t rb = q.fc2.row_bytes;
+    const Fc2Plan plan = fc2_plan(k, C, rb, nb, sizeof(S));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    float* s_w = reinterpret_cast<float*>(smem + 128);
+    int* s_idx = reinterpret_cast<int*>(smem + 192);
+    float4* A4 = reinterpret_cast<float4*>(smem + 256);
+    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
+    uint8_t* Sst = Wst + int64_t(k) * plan.w;
+
+    const int64_t t = blockIdx.x;
+    const int64_t H = q.H, I = q.I;
+    const int64_t n0 = int64_t(blockIdx.y) * kRowsPerBlock2;
+    const int rc = static_cast<int>(std::min<int64_t>(kRowsPerBlock2, H - n0));
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const float* h = reinterpret_cast<const float*>(static_cast<const char*>(q.workspace) + L.h);
+
+    // Prologue, overlapping the FC1 kernel: the router logits were complete
+    // before FC1 started, so this CTA may route its token and warm L2 with the
+    // selected experts' rows before waiting for h.
+    if (warp == 0) warp_route(q.logits + t * q.E, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, 1);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint32_t wbytes = static_cast<uint32_t>(rc * rb), sbytes = static_cast<uint32_t>(rc * nb * sizeof(S));
+    if (tid < k) {
+        const int e = s_idx[tid];
+        bulk_prefetch_l2(q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes);
+    }
+    grid_dependency_wait();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, k * (wbytes + sbytes));
+        for (int j = 0; j < k; ++j) {
+            const int e = s_idx[j];
+            bulk_g2s(Wst + j * plan.w, q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes, bar);
+            bulk_g2s(Sst + j * plan.s, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
+        }
+    }
+    for (int j = 0; j < k; ++j)
+        stage_activations<1>(
+            A4 + int64_t(j) * 8 * C, Asum + j * C, C,
+            [&](int, int64_t kk) -> float { return kk < I ? h[(t * k + j) * I + kk] : 0.f; }, tid, kThreads);
+    grid_launch_dependents();
+    const bool ok = mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+        mbar_wait(bar, 0);
+        return;
+    }
+    const int bs_shift = __ffs(q.bs) - 1;
+    constexpr int kZImplicit = 1 << (BITS - 1);
+
+    for (int g = warp; g * R < rc; g += kWarps) {
+        float acc[R] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const int e = s_idx[j];
+            const uint8_t* W = Wst + j * plan.w;
+            const S* Sc = reinterpret_cast<const S*>(Sst + j * plan.s);
+            const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
+            float out[R][1];
+#pragma unroll
+            for (int r = 0; r < R; ++r) out[r][0] = 0.f;
+            for (int c = lane; c < C; c += 32) {
+                const int b = (c * 32) >> bs_shift;
+                uint32_t w[R][BITS];
+                float sc[R], zz[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int rl = min(g * R + r, rc - 1);
+                    load_chunk<BITS>(W + int64_t(rl) * rb, c, w[r]);
+                    sc[r] = to_f32(Sc[rl * nb + b]);
+                    zz[r] = float(Z2 ? zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b) : kZImplicit);
+                }
+                chunk_accumulate<BITS, R, 1>(w, sc, zz, A4 + int64_t(j) * 8 * C, Asum + j * C, C, c, out);
+            }
+            const float wj = s_w[j];
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[r] = fmaf(wj, out[r][0], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = warp_sum(acc[r]);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int rl = g * R + r;
+                if (rl < rc) store_from_f32(q.Y, q.act_dtype, t * H + n0 + rl, acc[r]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------- FC2 (tiled)
+
+template <int BITS, int ST, int MT>
+__global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constant__ QmoeArgs q) {
+    using S = typename DType<ST>::T;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = static_cast<int>(q.fc2.nb * q.bs / 32);
+    const int nb = static_cast<int>(q.fc2.nb);
+    const int64_t rb = q.fc2.row_bytes;
+    const Fc2Plan plan = fc2_plan(MT, C, rb, nb, sizeof(S));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int* s_int = reinterpret_cast<int*>(smem + 16);
+    float4* A4 = reinterpret_cast<float4*>(smem + 256);
+    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
+    const S* Sc = reinterpret_cast<const S*>(Wst + plan.w);
+
+    char* ws = static_cast<char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const float* h = reinterpret_cast<const float*>(ws + L.h);
+    float* o = reinterpret_cast<float*>(ws + L.o);
+    const int64_t H = q.H, I = q.I;
+
+    grid_dependency_wait();
+    const int tile = blockIdx.x;
+    if (tile >= *reinterpret_cast<const int*>(ws + L.ntiles)) return;
+    if (tid == 0) {
+        const int2 ti = reinterpret_cast<const int2*>(ws + L.tiles)[tile];
+        s_int[0] = ti.x;
+        s_int[1] = ti.y;
+        s_int[2] = min(MT, reinterpret_cast<const int*>(ws + L.offsets)[ti.x + 1] - ti.y);
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int e = s_int[0], s0 = s_int[1], cnt = s_int[2];
+    const int64_t n0 = int64_t(blockIdx.y) * kRowsPerBlock2;
+    const int rc = static_cast<int>(std::min<int64_t>(kRowsPerBlock2, H - n0));
+    if (tid == 0) {
+        const uint32_t wbytes = static_cast<uint32_t>(rc * rb), sbytes = static_cast<uint32_t>(rc * nb * sizeof(S));
+        mbar_arrive_expect_tx(bar, wbytes + sbytes);
+        bulk_g2s(Wst, q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes, bar);
+        bulk_g2s(Wst + plan.w, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
+    }
+    stage_activations<MT>(
+        A4, Asum, C, [&](int m, int64_t kk) -> float { return (m < cnt && kk < I) ? h[(s0 + m) * I + kk] : 0.f; },
+        tid, kThreads);
+    grid_launch_dependents();
+    const bool ok = mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+        mbar_wait(bar, 0);
+        return;
+    }
+    const int bs_shift = __ffs(q.bs) - 1;
+    constexpr int kZImplicit = 1 << (BITS - 1);
+    const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
+    for (int g = warp; g * R < rc; g += kWarps) {
+        float out[R][MT];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) out[r][m] = 0.f;
+        for (int c = lane; c < C; c += 32) {
+            const int b = (c * 32) >> bs_shift;
+            uint32_t w[R][BITS];
+            float sc[R], zz[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int rl = min(g * R + r, rc - 1);
+                load_chunk<BITS>(Wst + int64_t(rl) * rb, c, w[r]);
+                sc[r] = to_f32(Sc[rl * nb + b]);
+                zz[r] = float(Z2 ? zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b) : kZImplicit);
+            }
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Asum, C, c, out);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out[r][m]);
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int rl = g * R + r;
+                if (rl >= rc) break;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (m < cnt) o[int64_t(s0 + m) * H + n0 + rl] = out[r][m];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------ tiles, combine
+
+// Tiles of <= kTileM consecutive sorted pairs of one expert.  One thread per
+// expert (E <= 1024): tile counts, an exclusive scan, then each expert writes
+// its tiles (expert, first sorted position).
+__global__ void __launch_bounds__(1024) tiles_kernel(char* ws, int64_t T, int64_t H, int64_t I, int64_t E, int k) {
+    const Ws L = ws_layout(T, H, I, E, k);
+    const int* counts = reinterpret_cast<const int*>(ws + L.counts);
+    const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+    int2* tiles = reinterpret_cast<int2*>(ws + L.tiles);
+    __shared__ int scan[1024];
+    grid_dependency_wait();
+    const int e = threadIdx.x;
+    const int n = e < E ? (counts[e] + kTileM - 1) / kTileM : 0;
+    scan[e] = n;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int v = e >= o ? scan[e - o] : 0;
+        __syncthreads();
+        scan[e] += v;
+        __syncthreads();
+    }
+    const int first = scan[e] - n;
+    for (int i = 0; i < n; ++i) tiles[first + i] = make_int2(e, offsets[e] + i * kTileM);
+    if (e == 1023) *reinterpret_cast<int*>(ws + L.ntiles) = scan[1023];
+    grid_launch_dependents();
+}
+
+// Y[t, n] = sum_j w[t, j] * o[position of (t, j), n], ascending j, fp32 -> act dtype.
+__global__ void combine_kernel(const __grid_constant__ QmoeArgs q) {
+    const char* ws = static_cast<const char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const float* o = reinterpret_cast<const float*>(ws + L.o);
+    const float* wts = reinterpret_cast<const float*>(ws + L.wts);
+    const int* inv = reinterpret_cast<const int*>(ws + L.inv);
+    grid_dependency_wait();
+    const int64_t total = q.T * q.H;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = i / q.H, n = i - t * q.H;
+        float acc = 0.f;
+        for (int j = 0; j < q.k; ++j) acc = fmaf(wts[t * q.k + j], o[int64_t(inv[t * q.k + j]) * q.H + n], acc);
+        store_from_f32(q.Y, q.act_dtype, i, acc);
+    }
+}
+
+// ------------------------------------------------------------ launching
+
+template <typename Kern>
+cudaError_t launch(Kern kern, dim3 grid, int64_t smem, cudaStream_t stream, const QmoeArgs& q) {
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, q);
+}
+
+template <int BITS, int ST, int MT, bool DECODE>
+cudaError_t launch_fc1(const QmoeArgs& q, unsigned gx, cudaStream_t stream) {
+    const int C = static_cast<int>(q.fc1.nb * q.bs / 32);
+    const Fc1Plan p = fc1_plan(MT, C, q.fc1.row_bytes, static_cast<int>(q.fc1.nb), ST == kF32 ? 4 : 2);
+    const unsigned gy = static_cast<unsigned>(cdiv<int64_t>(q.I, kPairsPerBlock));
+    return launch(fc1_kernel<BITS, ST, MT, DECODE>, dim3(gx, gy, 1), p.total, stream, q);
+}
+
+template <int B1, int B2, int ST>
+cudaError_t run_typed(const QmoeArgs& q, cudaStream_t stream) {
+    char* ws = static_cast<char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const int64_t P = q.T * q.k;
+    const int C2 = static_cast<int>(q.fc2.nb * q.bs / 32);
+    const unsigned gy2 = static_cast<unsigned>(cdiv<int64_t>(q.H, kRowsPerBlock2));
+    cudaError_t e;
+    if (use_decode(q)) {
+        e = launch_fc1<B1, ST, 1, true>(q, static_cast<unsigned>(P), stream);
+        if (e != cudaSuccess) return e;
+        const Fc2Plan p2 = fc2_plan(q.k, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
+        return launch(fc2_decode_kernel<B2, ST>, dim3(static_cast<unsigned>(q.T), gy2, 1), p2.total, stream, q);
+    }
+    int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
+    float* wts = reinterpret_cast<float*>(ws + L.wts);
+    if ((e = launch_route(q.logits, q.T, q.E, q.k, q.normalize, idx, wts, stream)) != cudaSuccess) return e;
+    if ((e = launch_permute(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.counts),
+                            reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
+                            reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
+        return e;
+    tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
+    if ((e = launch_fc1<B1, ST, kTileM, false>(q, gx, stream)) != cudaSuccess) return e;
+    const Fc2Plan p2 = fc2_plan(kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
+    if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q)) != cudaSuccess) return e;
+    const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), 152 * 16);
+    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
+    return cudaGetLastError();
+}
+
+template <int ST>
+cudaError_t run_bits(const QmoeArgs& q, cudaStream_t stream) {
+    if (q.fc1_bits == 3 && q.fc2_bits == 3) return run_typed<3, 3, ST>(q, stream);
+    if (q.fc1_bits == 3 && q.fc2_bits == 4) return run_typed<3, 4, ST>(q, stream);
+    if (q.fc1_bits == 4 && q.fc2_bits == 3) return run_typed<4, 3, ST>(q, stream);
+    return run_typed<4, 4, ST>(q, stream);
+}
+
+}  // namespace
+
+bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int64_t* bytes) {
+    if (T > (int64_t(1) << 24) || H > (int64_t(1) << 24) || I > (int64_t(1) << 24) || k > 1024) return false;
+    const int64_t P = T * k;
+    if (P >= (int64_t(1) << 31) || P * std::max(H, I) > (int64_t(1) << 40)) return false;
+    *bytes = ws_layout(T, H, I, E, k).total;
+    return true;
+}
+
+cudaError_t qmoe_take_error(unsigned int* out) { return take_unit_error(out); }
+
+cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, cudaStream_t stream) {
+    (void)sm_count;
+    return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, stream) : run_bits<kBF16>(q, stream);
+}
+
+}  // namespace mnb

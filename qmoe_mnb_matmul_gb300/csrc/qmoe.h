@@ -1,0 +1,41 @@
+// qmoe.h -- internal interface of the QMoE expert-FFN pipeline.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mnb {
+
+struct ProjGeom {
+    int64_t nb;         // blocks per row
+    int64_t row_bytes;  // packed bytes per row
+    int64_t zp_row;     // packed zero-point bytes per row
+};
+
+struct QmoeArgs {
+    const void* X;
+    int act_dtype;
+    int64_t T, H, I, E;
+    int k, normalize;
+    const float* logits;
+    const uint8_t* fc1_w;
+    const void* fc1_s;
+    const uint8_t* fc1_zp;
+    int fc1_bits;
+    const uint8_t* fc2_w;
+    const void* fc2_s;
+    const uint8_t* fc2_zp;
+    int fc2_bits;
+    int bs;
+    int fc1_layout;
+    void* Y;
+    void* workspace;
+    ProjGeom fc1, fc2;
+};
+
+// Workspace bytes for one qmoe_forward call; false on overflow.
+bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int64_t* bytes);
+
+cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, cudaStream_t stream);
+
+}  // namespace mnb

@@ -1,0 +1,174 @@
+// route.cu -- MoE routing (softmax + canonical top-k), the expert-sorted
+// permutation of routed pairs, and the raw-code unpack export.
+//
+// Routing semantics follow "feat(qwen4): component kernels extracted from the
+// brick PRs" (fp32 softmax, canonical top-k, optional renormalisation of the
+// selected probabilities) and the QMoE routing step of "INT3 QMoE CUDA
+// correctness baseline and Qwen experimental results".
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "route_core.cuh"
+
+namespace mnb {
+
+namespace {
+
+// ------------------------------------------------------------------ unpack
+
+// One thread per code: code k of a row is stream bits bits*k .. +bits-1 of the
+// row's bytes, least significant bit first.
+__global__ void unpack_kernel(const uint8_t* __restrict__ packed, int64_t rows, int64_t K, int bits,
+                              int64_t row_bytes, uint8_t* __restrict__ codes) {
+    const int64_t total = rows * K;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t n = i / K, k = i - n * K;
+        const uint8_t* row = packed + n * row_bytes;
+        const int64_t bit = k * bits;
+        const int64_t byte = bit >> 3;
+        const int sh = static_cast<int>(bit & 7);
+        uint32_t v = row[byte];
+        if (sh + bits > 8) v |= static_cast<uint32_t>(row[byte + 1]) << 8;
+        codes[i] = static_cast<uint8_t>((v >> sh) & ((1u << bits) - 1u));
+    }
+}
+
+// ----------------------------------------------------------------- routing
+
+// One warp per token (see route_core.cuh).
+__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int normalize,
+                             int32_t* __restrict__ idx, float* __restrict__ wout) {
+    const int64_t t = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5);
+    grid_dependency_wait();
+    if (t >= T) return;
+    warp_route(logits + t * E, E, k, normalize, idx + t * k, wout + t * k, 1);
+}
+
+// ------------------------------------------------------------- permutation
+
+// One CTA of 1024 threads.  Warp w owns the contiguous pair range
+// [w*seg, (w+1)*seg).  Pass 1 counts pairs per (warp, expert); a scan gives
+// every (warp, expert) its first output slot; pass 2 walks the same range in
+// order, 32 pairs at a time, ranking equal experts with match_any so that the
+// order inside an expert is the pair order (stable).
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ idx, int64_t P,
+                                                               int E, int32_t* __restrict__ counts,
+                                                               int32_t* __restrict__ offsets,
+                                                               int32_t* __restrict__ perm,
+                                                               int32_t* __restrict__ inv_perm) {
+    extern __shared__ int32_t cnt[];  // [kPermWarps][E], then tot[E+1]
+    int32_t* tot = cnt + kPermWarps * E;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependency_wait();
+    for (int i = tid; i < kPermWarps * E; i += kPermThreads) cnt[i] = 0;
+    __syncthreads();
+    const int64_t seg = (P + kPermWarps - 1) / kPermWarps;
+    const int64_t p0 = warp * seg, p1 = (P < p0 + seg) ? P : p0 + seg;
+    const uint32_t lt = (1u << lane) - 1u;
+    int32_t* mycnt = cnt + warp * E;
+    for (int64_t base = p0; base < p1; base += 32) {
+        const int64_t p = base + lane;
+        const bool valid = p < p1;
+        const int e = valid ? idx[p] : -1 - lane;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (valid && (same & lt) == 0) mycnt[e] += __popc(same);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per-expert totals and the exclusive scan over experts (E <= 1024, one thread each)
+    int32_t my_total = 0;
+    if (tid < E)
+        for (int w = 0; w < kPermWarps; ++w) my_total += cnt[w * E + tid];
+    // block-wide exclusive scan of my_total over tid < E
+    __shared__ int32_t warp_sums[kPermWarps];
+    int32_t x = (tid < E) ? my_total : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    const int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (tid < E) {
+        const int32_t excl = incl - my_total;
+        tot[tid] = excl;
+        counts[tid] = my_total;
+        offsets[tid] = excl;
+        if (tid == E - 1) offsets[E] = incl;
+        // first slot of each warp's pairs of expert tid, in warp order
+        int32_t run = excl;
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int32_t c = cnt[w * E + tid];
+            cnt[w * E + tid] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int64_t base = p0; base < p1; base += 32) {
+        const int64_t p = base + lane;
+        const bool valid = p < p1;
+        const int e = valid ? idx[p] : -1 - lane;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        int32_t slot = 0;
+        if (valid) slot = mycnt[e] + __popc(same & lt);
+        __syncwarp();
+        if (valid && (same & lt) == 0) mycnt[e] += __popc(same);
+        __syncwarp();
+        if (valid) {
+            perm[slot] = static_cast<int32_t>(p);
+            if (inv_perm) inv_perm[p] = slot;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
+                                uint8_t* codes, cudaStream_t stream) {
+    const int64_t nb = cdiv<int64_t>(K, bs);
+    const int64_t row_bytes = nb * bs * bits / 8;
+    const int64_t total = rows * K;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(total, threads), 65535 * 16);
+    unpack_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(
+        packed, rows, K, bits, row_bytes, codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route(const float* logits, int64_t T, int64_t E, int k, int normalize, int32_t* idx,
+                         float* w, cudaStream_t stream) {
+    const int warps = 8;
+    const int64_t blocks = cdiv<int64_t>(T, warps);
+    route_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(logits, T, static_cast<int>(E), k,
+                                                                            normalize, idx, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
+                           int32_t* perm, int32_t* inv_perm, cudaStream_t stream) {
+    const size_t smem = (size_t(kPermWarps) * E + E + 1) * sizeof(int32_t);
+    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    permute_kernel<<<1, kPermThreads, smem, stream>>>(idx, T * k, static_cast<int>(E), counts, offsets, perm,
+                                                     inv_perm);
+    return cudaGetLastError();
+}
+
+}  // namespace mnb
