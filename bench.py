@@ -1,0 +1,386 @@
+"""Benchmark: packed INT4 decode GEMV throughput on a Qwen3-1.7B-shaped model.
+
+One step is a full M=1 decode pass through every weight-only projection of a
+28-layer Qwen3-1.7B-shaped model -- per layer QKV 2048->4096, o_proj
+2048->2048, gate and up 2048->6144, down 6144->2048 -- plus the vocabulary head
+2048->151936: 141 mnb_matmul calls (INT4, block 32, fp32 scales, implicit zero
+point 8, fp32 activations and outputs) over 1.075 GB of packed weights and
+scales, captured once in a CUDA graph and replayed.  Every layer has its own
+weights, so each step streams > 8x the 129 MB L2 from HBM.
+
+metric: GB/s of algorithmic bytes (packed weights + scales + activations +
+outputs) per second, whole job.  `roofline` reports the vocabulary-head launch
+of the GEMV kernel (timed with CUDA events inside the timed region) against the
+measured HBM copy bandwidth; `e2e` repeats the step with the activations copied
+from pinned host memory and all outputs copied back inside the timed region.
+
+`--impl reference` times the oracle (plain fp64 C, test infrastructure) on the
+host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "INT4 decode GEMV throughput (packed weights + scales + activations + outputs)"
+UNIT = "GB/s"
+BITS, BS = 4, 32
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_int4_vocab_head_ncu.md")
+
+
+def suite():
+    layers = [(f"L{l}.{n}", K, N) for l in range(wl.QWEN3_1P7B_LAYERS) for n, K, N in wl.QWEN3_1P7B_PROJECTIONS]
+    return layers + [wl.QWEN3_1P7B_LM_HEAD]
+
+
+def proj_bytes(K, N):
+    nb = (K + BS - 1) // BS
+    return N * nb * BS * BITS // 8 + N * nb * 4 + K * 4 + N * 4
+
+
+def workload_config():
+    return {"workload": "qwen3-1.7b-shaped INT4 decode: 28 layers x (qkv 2048->4096, o 2048->2048, "
+                        "gate/up 2048->6144, down 6144->2048) + vocab head 2048->151936, M=1, bs=32, fp32 act/scales",
+            "M": 1, "bits": BITS, "block_size": BS, "layers": wl.QWEN3_1P7B_LAYERS, "calls_per_step": len(suite()),
+            "bytes_per_step": sum(proj_bytes(K, N) for _, K, N in suite()),
+            "l2": "inputs larger than L2 (1.075 GB of distinct weights per step, 129 MB L2)"}
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if len(r) >= 8 and num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if len(r) >= 8 and num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) < 8:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel_sha: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != kernel_sha:
+        return None
+    return float(t.group(1))
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemv.cu", "gemv_core.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "qmoe_mnb_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ the oracle arm
+
+def oracle_sample(seconds: float = 12.0):
+    """Time the oracle (fp64 C, all host cores) on whole projections of one
+    layer of the workload, repeated until about `seconds` have passed."""
+    import oracle
+    threads = os.cpu_count() or 1
+    g = wl.rng(1234)
+    layer = [(name, K, N, *wl.quantized_weight(g, N, K, BITS, BS)[:2], wl.normal(g, (1, K)))
+             for name, K, N in wl.QWEN3_1P7B_PROJECTIONS]
+    done_bytes, t_total, calls = 0, 0.0, 0
+    while t_total < seconds and calls < 5000:
+        name, K, N, packed, scales, A = layer[calls % len(layer)]
+        t0 = time.perf_counter()
+        oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, BITS, BS, threads=threads)
+        t_total += time.perf_counter() - t0
+        done_bytes += proj_bytes(K, N)
+        calls += 1
+    return {"value": done_bytes / t_total / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{calls} whole projections cycling through one Qwen3-1.7B-shaped layer "
+                      f"(qkv, o_proj, gate, up, down), M=1, {done_bytes / 1e6:.0f} MB in {t_total:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    """The oracle as the reference arm: each step is one o_proj-shaped projection
+    (2048 -> 2048, 2.6 MB), a bounded sample of the workload, on all host cores."""
+    if rank != 0:
+        return
+    import oracle
+    threads = os.cpu_count() or 1
+    g = wl.rng(99)
+    _, K, N = wl.QWEN3_1P7B_PROJECTIONS[1]
+    packed, scales, _ = wl.quantized_weight(g, N, K, BITS, BS)
+    A = wl.normal(g, (1, K))
+
+    def step():
+        oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, BITS, BS, threads=threads)
+        return proj_bytes(K, N)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    sample = f"one o_proj-shaped projection (2048 -> 2048, {proj_bytes(K, N) / 1e6:.2f} MB) per step, M=1"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ------------------------------------------------------------- our arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import qmoe_mnb_matmul_gb300 as mnb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    # ---- synthetic model weights (seeded; every layer distinct).  Activations and
+    # outputs are views into two flat buffers so that the end-to-end variant
+    # moves them with one copy each way.
+    g = wl.rng(2024 + rank)
+    plan = suite()
+    a_off, y_off, oa, oy = [], [], 0, 0
+    for _, K, N in plan:
+        a_off.append(oa)
+        y_off.append(oy)
+        oa += K
+        oy += N
+    A_all = torch.empty(oa, dtype=torch.float32, device=dev)
+    Y_all = torch.empty(oy, dtype=torch.float32, device=dev)
+    calls = []
+    for (name, K, N), ao, yo in zip(plan, a_off, y_off):
+        packed, scales, _ = wl.quantized_weight(g, N, K, BITS, BS)
+        A_all[ao:ao + K] = torch.from_numpy(wl.normal(g, (K,)))
+        calls.append(dict(name=name, K=K, N=N, B=torch.from_numpy(packed).to(dev),
+                          S=torch.from_numpy(scales).to(dev), A=A_all[ao:ao + K], Y=Y_all[yo:yo + N]))
+    bytes_step = sum(proj_bytes(c["K"], c["N"]) for c in calls)
+    head = calls[-1]
+    head_bytes = proj_bytes(head["K"], head["N"])
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(cs, s):
+        for c in cs:
+            mnb.mnb_matmul(c["A"], c["B"], c["S"], None, c["N"], BITS, BS, c["Y"], stream=s, K=c["K"], M=1)
+
+    def capture(fn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            gr.capture_begin()
+            fn()
+            gr.capture_end()
+        return gr
+
+    with torch.cuda.stream(stream):
+        launch(calls, stream)  # eager warm-up (module load, kernel attributes)
+    torch.cuda.synchronize(dev)
+    g_layers = capture(lambda: launch(calls[:-1], stream))
+    g_head = capture(lambda: launch([head], stream))
+    if mnb.mnb_get_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set after warm-up")
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def timed(step, steps):
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        clocks.stop()
+        ms = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, clocks.summary()
+
+    # One step = the 140 layer projections (one graph) then the vocabulary head
+    # (a second graph); CUDA events on the launching stream bracket the head.
+    n_ev = min(args.steps, 512)
+    hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    stride = max(1, args.steps // n_ev)
+
+    def step(i):
+        g_layers.replay()
+        j = i // stride
+        if i % stride == 0 and j < n_ev:
+            hev[j][0].record(stream)
+            g_head.replay()
+            hev[j][1].record(stream)
+        else:
+            g_head.replay()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            g_layers.replay()
+            g_head.replay()
+        ms, clocks = timed(step, args.steps)
+    used = [a.elapsed_time(b) * 1e3 for a, b in hev[:min(n_ev, (args.steps + stride - 1) // stride)]]
+    head_us = statistics.mean(used)
+
+    value = bytes_step * args.steps * ws / (ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    achieved = head_bytes / (head_us * 1e-6) / 1e9
+
+    # ---- end to end: activations from pinned host memory in, every output back out
+    h_in = A_all.cpu().pin_memory()
+    h_out = torch.empty(Y_all.numel(), dtype=torch.float32).pin_memory()
+    h2d, d2h = h_in.numel() * 4, h_out.numel() * 4
+
+    def e2e_body():
+        A_all.copy_(h_in, non_blocking=True)
+        launch(calls, stream)
+        h_out.copy_(Y_all, non_blocking=True)
+    g_e2e = capture(e2e_body)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_e2e.replay()
+        e2e_steps = max(3, args.steps // 4)
+        ms_e2e, _ = timed(lambda i: g_e2e.replay(), e2e_steps)
+    e2e_value = bytes_step * e2e_steps * ws / (ms_e2e / 1e3) / 1e9
+
+    if mnb.mnb_get_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded uniform packed bytes, U[0.005,0.02] scales, N(0,1) activations)",
+        "config": workload_config(),
+        "gpu_launches": len(calls) * args.steps,
+        "clocks": clocks,
+        "roofline": {"kernel": "gemv_kernel<INT4, fp32 scales, M=1>, vocabulary-head launch", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch": head_bytes,
+                     "launch_us": head_us, "traffic": ncu_traffic(kernel_source_sha()),
+                     "timing": "CUDA events around the head launch on its stream, inside the timed region",
+                     "step_frac": value / ws / peak},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e / e2e_steps},
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_sample()
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -6,27 +6,20 @@
 // consumed; no dequantised weight matrix is ever written to global memory.
 //
 // Design (HBM-bound: the packed weights and scales are the traffic):
-//  * A CTA owns contiguous blocks of RC weight rows.  Because rows are
-//    contiguous in the [N, nb, blob] layout, a block's packed bytes and its
-//    scales are two contiguous ranges; one thread moves each with a single
-//    bulk (TMA) copy into a 2-stage shared-memory ring tracked by mbarriers.
-//    The grid is persistent (<= resident CTAs), so the copy of block i+2 is in
-//    flight while block i is consumed.
-//  * The activations are staged once per CTA, pre-multiplied by 256 (exact),
-//    in a chunk-interleaved float4 layout that makes every lane's read
-//    conflict-free, together with per-chunk activation sums.
-//  * A chunk is 32 consecutive codes of one row (16 bytes of INT4, 12 of INT3).
-//    A code q is turned into a float with one byte-permute (INT4) or one
-//    shift + one mask (INT3) by placing it in mantissa bits 16.. under
-//    exponent 126: f = 0.5 + q/256.  With A' = 256 A this gives
-//    A' f = 128 A + A q, so over a chunk
-//        sum A (q - z) = sum A' f - (128 + z) sum A,
-//    and the scale of the chunk's block multiplies that once.  The products
-//    run as packed f32x2 FMAs.  Integer inputs stay exact (all partial sums
-//    are integers below 2^24).
-//  * A warp owns R rows at a time and walks their chunks with one chunk per
-//    lane; the R x MT sums are reduced with shuffles in a fixed order, so
+//  * A CTA owns contiguous blocks of RC = 8 * R weight rows.  Rows are
+//    contiguous in the [N, nb, blob] layout, so a block's packed bytes and its
+//    scales are two contiguous ranges, each moved by one bulk (TMA) copy.
+//  * Warp 8 is the producer: one lane keeps a ring of NST stages filled,
+//    waiting on per-stage "empty" mbarriers; the 8 consumer warps wait on the
+//    per-stage "full" mbarriers.  There is no block-wide barrier in the loop.
+//    The grid is persistent (<= resident CTAs).
+//  * The activations are staged once per CTA (gemv_core.cuh); each consumer
+//    warp owns R rows of a block and walks their 32-code chunks, one chunk
+//    per lane; the R x MT sums are reduced with shuffles in a fixed order, so
 //    results are deterministic.
+//  * Before the grid-dependency wait each CTA only warms L2 with its first
+//    blocks (a prefetch cannot observe stale data), so a programmatic
+//    dependent launch overlaps that traffic with the previous kernel.
 #include <algorithm>
 
 #include "common.cuh"
@@ -39,175 +32,227 @@ namespace {
 
 using namespace gemv;
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 2;
-constexpr int kRowsPerWarp = 4;                 // R
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int64_t kSmemBudget = 227 * 1024;
+
 struct Plan {
-    int64_t a4_bytes, asum_bytes, w_stage, s_stage, total;
+    int64_t a4, sums, w_stage, s_stage, fixed;
+    int stages;
+    int64_t total;
 };
 
-__host__ __device__ inline Plan make_plan(int MT, int C, int RC, int64_t row_bytes, int nb, int ssize) {
+__host__ __device__ inline Plan make_plan(int MT, int C, int RC, int64_t row_bytes, int nb, int ssize, int stages) {
     Plan p;
-    p.a4_bytes = int64_t(MT) * 8 * C * 16;
-    p.asum_bytes = round_up(int64_t(MT) * C * 4, 128);
+    p.a4 = int64_t(MT) * 8 * C * 16;
+    p.sums = round_up(int64_t(MT) * C * 16, 128);  // one float4 correction per (row, chunk)
     p.w_stage = round_up(int64_t(RC) * row_bytes, 128);
     p.s_stage = round_up(int64_t(RC) * nb * ssize, 128);
-    p.total = 128 + p.a4_bytes + p.asum_bytes + kStages * (p.w_stage + p.s_stage);
+    p.fixed = 256 + p.a4 + p.sums;
+    p.stages = stages;
+    p.total = p.fixed + int64_t(stages) * (p.w_stage + p.s_stage);
     return p;
 }
 
-template <int BITS, int ST, int MT>
+// Named barrier over the consumer warps only.
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+template <int BITS, int ST, int MT, int R>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using S = typename DType<ST>::T;
-    constexpr int R = kRowsPerWarp;
+    constexpr int RC = kConsumerWarps * R;
     extern __shared__ __align__(128) uint8_t smem[];
 
-    const int C = a.chunks, RC = a.rows_per_block, nb = a.nb;
-    const Plan plan = make_plan(MT, C, RC, a.row_bytes, nb, sizeof(S));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    float4* A4 = reinterpret_cast<float4*>(smem + 128);
-    float* Asum = reinterpret_cast<float*>(smem + 128 + plan.a4_bytes);
-    uint8_t* Wst = smem + 128 + plan.a4_bytes + plan.asum_bytes;
-    uint8_t* Sst = Wst + kStages * plan.w_stage;
+    const int C = a.chunks, nb = a.nb;
+    const Plan plan = make_plan(MT, C, RC, a.row_bytes, nb, sizeof(S), a.stages);
+    const int NST = plan.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMaxStages;
+    float4* A4 = reinterpret_cast<float4*>(smem + 256);
+    float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
+    uint8_t* Wst = smem + plan.fixed;
+    uint8_t* Sst = Wst + NST * plan.w_stage;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = int64_t(blockIdx.y) * MT;
-
+    const int nblk = a.n_blocks;
     auto block_rows = [&](int blk) -> int {
-        const int64_t n0 = int64_t(blk) * RC;
-        return static_cast<int>(a.N - n0 < RC ? a.N - n0 : int64_t(RC));
-    };
-    auto issue = [&](int blk, int st) {
-        const int64_t n0 = int64_t(blk) * RC;
-        const int rc = block_rows(blk);
-        const uint32_t wb = static_cast<uint32_t>(rc * a.row_bytes) & ~15u;
-        const uint32_t sb = static_cast<uint32_t>(int64_t(rc) * nb * sizeof(S)) & ~15u;
-        mbar_arrive_expect_tx(&bars[st], wb + sb);
-        if (wb) bulk_g2s(Wst + st * plan.w_stage, a.B + n0 * a.row_bytes, wb, &bars[st]);
-        if (sb)
-            bulk_g2s(Sst + st * plan.s_stage, static_cast<const S*>(a.scales) + n0 * nb, sb, &bars[st]);
+        const int64_t left = a.N - int64_t(blk) * RC;
+        return static_cast<int>(left < RC ? left : int64_t(RC));
     };
 
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    if (tid == kConsumerWarps * 32) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
         fence_barrier_init();
-        // Warm L2 with this CTA's first blocks while the previous kernel drains.
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < NST; ++i) {
             const int blk = blockIdx.x + i * gridDim.x;
-            if (blk >= a.n_blocks) break;
+            if (blk >= nblk) break;
             const uint32_t wb = static_cast<uint32_t>(block_rows(blk) * a.row_bytes) & ~15u;
             if (wb) bulk_prefetch_l2(a.B + int64_t(blk) * RC * a.row_bytes, wb);
         }
     }
     grid_dependency_wait();
     __syncthreads();
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            const int blk = blockIdx.x + i * gridDim.x;
-            if (blk < a.n_blocks) issue(blk, i);
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
+        int it = 0;
+        for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+            const int st = it % NST;
+            if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1)) {
+                for (int j = 0; j < NST; ++j) mbar_wait(&full[j], 0);  // give in-flight copies a bounded chance
+                return;
+            }
+            const int64_t n0 = int64_t(blk) * RC;
+            const int rc = block_rows(blk);
+            uint8_t* W = Wst + st * plan.w_stage;
+            uint8_t* Sd = Sst + st * plan.s_stage;
+            const int64_t wtot = rc * a.row_bytes, stot = int64_t(rc) * nb * sizeof(S);
+            const uint32_t wb = static_cast<uint32_t>(wtot) & ~15u, sb = static_cast<uint32_t>(stot) & ~15u;
+            const uint8_t* wsrc = a.B + n0 * a.row_bytes;
+            const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
+            // bytes past the last 16-byte multiple of a partial block: plain copies, published by the arrive below
+            for (int64_t i = wb; i < wtot; ++i) W[i] = wsrc[i];
+            for (int64_t i = sb; i < stot; ++i) Sd[i] = ssrc[i];
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&full[st], wb + sb);
+            if (wb) bulk_g2s(W, wsrc, wb, &full[st]);
+            if (sb) bulk_g2s(Sd, ssrc, sb, &full[st]);
         }
+        return;
     }
 
-    // Stage A' = 256 A (zero beyond K and beyond M) and the per-chunk sums.
-    stage_activations<MT>(
-        A4, Asum, C,
-        [&](int m, int64_t k) -> float {
-            return (m0 + m < a.M && k < a.K) ? load_as_f32(a.A, a.a_dtype, (m0 + m) * a.K + k) : 0.f;
+    // ------------------------------------------------------------ consumers
+    stage_chunks<BITS, MT>(
+        A4, Corr, C, a.K, a.a_dtype, a.a_vec != 0,
+        [&](int m) -> const void* {
+            return m0 + m < a.M ? static_cast<const char*>(a.A) + (m0 + m) * a.K * (a.a_dtype == kF32 ? 4 : 2)
+                                : nullptr;
         },
-        tid, kThreads);
+        tid, kConsumerWarps * 32);
+    consumer_sync();
     grid_launch_dependents();
 
     const int bs_shift = __ffs(a.bs) - 1;
     constexpr int kZImplicit = 1 << (BITS - 1);
-
-    for (int it = 0;; ++it) {
-        const int blk = blockIdx.x + it * gridDim.x;
-        if (blk >= a.n_blocks) break;
-        const int st = it % kStages;
-        const uint32_t parity = (it / kStages) & 1;
-        const bool ok = mbar_wait(&bars[st], parity);
-        if (__syncthreads_or(!ok)) {
-            // A bulk copy never completed; leave after giving in-flight copies a bounded chance.
-            mbar_wait(&bars[st], parity);
-            return;
-        }
+    int it = 0;
+    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+        const int st = it % NST;
+        if (!warp_wait(&full[st], (it / NST) & 1)) return;
         const int64_t n0 = int64_t(blk) * RC;
         const int rc = block_rows(blk);
-        uint8_t* W = Wst + st * plan.w_stage;
+        const uint8_t* W = Wst + st * plan.w_stage;
         const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
-        {   // bytes past the last 16-byte multiple of a partial block come in with plain loads
-            const int64_t wtot = rc * a.row_bytes, stot = int64_t(rc) * nb * sizeof(S);
-            const int64_t wb = wtot & ~int64_t(15), sb = stot & ~int64_t(15);
-            if (wtot != wb || stot != sb) {
-                for (int64_t i = wb + tid; i < wtot; i += kThreads) W[i] = a.B[n0 * a.row_bytes + i];
-                const uint8_t* sg = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
-                for (int64_t i = sb + tid; i < stot; i += kThreads) Sst[st * plan.s_stage + i] = sg[i];
-                __syncthreads();
+        const int r0 = warp * R;
+        if (r0 < rc) {
+            float2 acc[R][MT];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[r][m] = make_float2(0.f, 0.f);
+            const uint8_t* wrow[R];
+            const S* srow[R];
+            const uint8_t* zrow[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int rl = min(r0 + r, rc - 1);  // rows past the block end recompute the last row
+                wrow[r] = W + int64_t(rl) * a.row_bytes;
+                srow[r] = Sc + rl * nb;
+                zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
             }
-        }
-
-        for (int g = warp; g * R < rc; g += kWarps) {
+            for (int c = lane; c < C; c += 32) {
+                const int b = (c * 32) >> bs_shift;
+                uint32_t w[R][BITS];
+                float sc[R], dz[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    load_chunk<BITS>(wrow[r], c, w[r]);
+                    sc[r] = to_f32(srow[r][b]);
+                    dz[r] = a.zp ? float(kZImplicit - zero_point_code<BITS>(zrow[r], b)) : 0.f;
+                }
+                if (a.zp)
+                    chunk_accumulate<BITS, R, MT, true>(w, sc, dz, A4, Corr, C, c, acc);
+                else
+                    chunk_accumulate<BITS, R, MT, false>(w, sc, dz, A4, Corr, C, c, acc);
+            }
             float out[R][MT];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) out[r][m] = 0.f;
-
-            for (int c = lane; c < C; c += 32) {
-                const int b = (c * 32) >> bs_shift;
-                uint32_t w[R][BITS];
-                float sc[R], zz[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int rl = min(g * R + r, rc - 1);   // rows past the block end recompute the last row
-                    load_chunk<BITS>(W + int64_t(rl) * a.row_bytes, c, w[r]);
-                    sc[r] = to_f32(Sc[rl * nb + b]);
-                    zz[r] = float(a.zp ? zero_point_code<BITS>(a.zp + (n0 + rl) * a.zp_row_bytes, b) : kZImplicit);
-                }
-                chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Asum, C, c, out);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out[r][m]);
+                for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(acc[r][m].x + acc[r][m].y);
             if (lane == 0) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int rl = g * R + r;
-                    if (rl >= rc) break;
+                    if (r0 + r >= rc) break;
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
-                        if (m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + rl, out[r][m]);
+                        if (m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, out[r][m]);
                 }
             }
         }
-        __syncthreads();  // every warp is done with stage st
-        if (tid == 0) {
-            const int nxt = blk + kStages * gridDim.x;
-            if (nxt < a.n_blocks) {
-                fence_proxy_async_smem();
-                issue(nxt, st);
-            }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
     }
 }
 
-template <int BITS, int ST, int MT>
-cudaError_t launch_typed(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t stream, int64_t smem) {
-    auto kern = gemv_kernel<BITS, ST, MT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+int ssize_of(int dt) { return dt == kF32 ? 4 : 2; }
+
+int pick_mt(int64_t M) { return M <= 1 ? 1 : (M <= 2 ? 2 : 4); }
+
+// The smallest row count for which every block's packed bytes and scales
+// start on a 16-byte boundary (a power of two).
+int64_t row_align(int64_t row_bytes, int nb, int ssize) {
+    auto g16 = [](int64_t x) { int64_t g = 16; while (x % g) g >>= 1; return 16 / g; };
+    return std::max(g16(row_bytes), g16(int64_t(nb) * ssize));
+}
+
+// Rows per warp: as many as keep at least ~1.5 blocks per SM.
+int pick_r(int64_t N, int64_t row_bytes, int nb, int ssize, int sm_count) {
+    const int64_t align = row_align(row_bytes, nb, ssize);
+    for (int R : {4, 2, 1}) {
+        const int64_t RC = int64_t(kConsumerWarps) * R;
+        if (RC % align != 0) return 4;
+        if (R == 1 || cdiv<int64_t>(N, RC) >= int64_t(sm_count) * 3 / 2) return R;
+    }
+    return 4;
+}
+
+template <int BITS, int ST, int MT, int R>
+cudaError_t launch_typed(GemvArgs a, int sm_count, bool pdl, cudaStream_t stream) {
+    constexpr int RC = kConsumerWarps * R;
+    const int ssize = ST == kF32 ? 4 : 2;
+    a.rows_per_block = RC;
+    a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, RC));
+    const Plan p1 = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, 1);
+    const int64_t stage = p1.w_stage + p1.s_stage;
+    if (p1.fixed + 2 * stage > kSmemBudget) return cudaErrorNotSupported;
+    // Enough stages for ~48 KB in flight per CTA; fewer if that keeps two CTAs per SM.
+    int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, cdiv<int64_t>(49152, stage))));
+    while (st > 2 && p1.fixed + st * stage > kSmemBudget) --st;
+    if (2 * (p1.fixed + st * stage) > kSmemBudget && 2 * (p1.fixed + 2 * stage) <= kSmemBudget)
+        while (st > 2 && 2 * (p1.fixed + st * stage) > kSmemBudget) --st;
+    a.stages = st;
+    const Plan p = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, st);
+    auto kern = gemv_kernel<BITS, ST, MT, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, static_cast<size_t>(smem));
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, static_cast<size_t>(p.total));
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
-    int64_t gx = std::min<int64_t>(a.n_blocks, std::max<int64_t>(1, int64_t(sm_count) * per_sm / mgroups));
+    const int64_t gx = std::min<int64_t>(a.n_blocks, std::max<int64_t>(1, int64_t(sm_count) * per_sm / mgroups));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(mgroups), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.total);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -217,26 +262,20 @@ cudaError_t launch_typed(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-int pick_mt(int64_t M) { return M <= 1 ? 1 : (M <= 2 ? 2 : 4); }
-
-int ssize_of(int dt) { return dt == kF32 ? 4 : 2; }
-
-// Alignment unit of a row block: the smallest row count (a multiple of the
-// warp row group) for which every block's packed bytes and scales start on a
-// 16-byte boundary.
-int64_t row_unit(int64_t row_bytes, int nb, int ssize) {
-    auto g16 = [](int64_t x) { int64_t g = 16; while (x % g) g >>= 1; return 16 / g; };
-    return std::max<int64_t>(kRowsPerWarp, std::max(g16(row_bytes), g16(int64_t(nb) * ssize)));
+template <int BITS, int ST, int MT>
+cudaError_t launch_r(const GemvArgs& a, int R, int sm_count, bool pdl, cudaStream_t stream) {
+    if (R == 4) return launch_typed<BITS, ST, MT, 4>(a, sm_count, pdl, stream);
+    if (R == 2) return launch_typed<BITS, ST, MT, 2>(a, sm_count, pdl, stream);
+    return launch_typed<BITS, ST, MT, 1>(a, sm_count, pdl, stream);
 }
 
-// Rows per stage: about 16 KB of packed weights, a multiple of the alignment
-// unit, shrunk while the grid would leave SMs idle.
-int pick_rows(int64_t N, int64_t row_bytes, int nb, int ssize, int sm_count) {
-    const int64_t unit = row_unit(row_bytes, nb, ssize);
-    int64_t rc = std::max<int64_t>(unit, (16384 / std::max<int64_t>(row_bytes, 1)) / unit * unit);
-    rc = std::max<int64_t>(unit, std::min<int64_t>(rc, 64) / unit * unit);
-    while (rc > unit && cdiv<int64_t>(N, rc) < 2 * sm_count) rc -= unit;
-    return static_cast<int>(rc);
+template <int BITS, int ST>
+cudaError_t launch_mt(const GemvArgs& a, int R, int sm_count, bool pdl, cudaStream_t stream) {
+    switch (pick_mt(a.M)) {
+        case 1: return launch_r<BITS, ST, 1>(a, R, sm_count, pdl, stream);
+        case 2: return launch_r<BITS, ST, 2>(a, R, sm_count, pdl, stream);
+        default: return launch_r<BITS, ST, 4>(a, R, sm_count, pdl, stream);
+    }
 }
 
 }  // namespace
@@ -247,41 +286,22 @@ size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype) 
     const int nb = static_cast<int>(cdiv<int64_t>(K, bs));
     const int C = nb * bs / 32;
     const int64_t row_bytes = int64_t(nb) * bs * bits / 8;
-    const Plan p = make_plan(pick_mt(M), C, static_cast<int>(row_unit(row_bytes, nb, ssize_of(scale_dtype))),
-                             row_bytes, nb, ssize_of(scale_dtype));
-    return p.total <= 227 * 1024 ? static_cast<size_t>(p.total) : 0;
+    const int ssize = ssize_of(scale_dtype);
+    const int64_t RC = std::max<int64_t>(kConsumerWarps, row_align(row_bytes, nb, ssize));
+    const Plan p = make_plan(pick_mt(M), C, static_cast<int>(RC), row_bytes, nb, ssize, 2);
+    return p.total <= kSmemBudget ? static_cast<size_t>(p.total) : 0;
 }
 
-cudaError_t launch_gemv(const GemvArgs& in, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
-    GemvArgs a = in;
-    const int ssize = ssize_of(scale_dtype);
-    const int MT = pick_mt(a.M);
-    a.rows_per_block = pick_rows(a.N, a.row_bytes, a.nb, ssize, sm_count);
-    Plan p = make_plan(MT, a.chunks, a.rows_per_block, a.row_bytes, a.nb, ssize);
-    const int unit = static_cast<int>(row_unit(a.row_bytes, a.nb, ssize));
-    while (p.total > 227 * 1024 && a.rows_per_block > unit) {
-        a.rows_per_block = std::max(unit, a.rows_per_block / 2 / unit * unit);
-        p = make_plan(MT, a.chunks, a.rows_per_block, a.row_bytes, a.nb, ssize);
-    }
-    if (p.total > 227 * 1024) return cudaErrorNotSupported;
-    a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, a.rows_per_block));
-
-#define MNB_GEMV_DISPATCH(BITS, ST)                                                   \
-    switch (MT) {                                                                     \
-        case 1: return launch_typed<BITS, ST, 1>(a, sm_count, pdl, stream, p.total); \
-        case 2: return launch_typed<BITS, ST, 2>(a, sm_count, pdl, stream, p.total); \
-        default: return launch_typed<BITS, ST, 4>(a, sm_count, pdl, stream, p.total); \
-    }
+cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
+    const int R = pick_r(a.N, a.row_bytes, a.nb, ssize_of(scale_dtype), sm_count);
     if (a.bits == 4) {
-        if (scale_dtype == kF32) { MNB_GEMV_DISPATCH(4, kF32) }
-        if (scale_dtype == kF16) { MNB_GEMV_DISPATCH(4, kF16) }
-        MNB_GEMV_DISPATCH(4, kBF16)
-    } else {
-        if (scale_dtype == kF32) { MNB_GEMV_DISPATCH(3, kF32) }
-        if (scale_dtype == kF16) { MNB_GEMV_DISPATCH(3, kF16) }
-        MNB_GEMV_DISPATCH(3, kBF16)
+        if (scale_dtype == kF32) return launch_mt<4, kF32>(a, R, sm_count, pdl, stream);
+        if (scale_dtype == kF16) return launch_mt<4, kF16>(a, R, sm_count, pdl, stream);
+        return launch_mt<4, kBF16>(a, R, sm_count, pdl, stream);
     }
-#undef MNB_GEMV_DISPATCH
+    if (scale_dtype == kF32) return launch_mt<3, kF32>(a, R, sm_count, pdl, stream);
+    if (scale_dtype == kF16) return launch_mt<3, kF16>(a, R, sm_count, pdl, stream);
+    return launch_mt<3, kBF16>(a, R, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

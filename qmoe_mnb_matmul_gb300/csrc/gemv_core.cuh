@@ -2,13 +2,19 @@
 // (dense mnb_matmul and the QMoE expert projections).
 //
 // A chunk is 32 consecutive codes of one packed row: 16 bytes of INT4 or 12
-// bytes of INT3 (3-bit codes cross byte boundaries inside the chunk).  A code q
-// becomes a float with one byte-permute (INT4) or one shift + one mask (INT3)
-// by placing it in mantissa bits 16.. under exponent 126, f = 0.5 + q/256.
-// Activations are staged pre-multiplied by 256 (exact), A' = 256 A, so
-//     A' f = 128 A + A q   and over a chunk   sum A (q - z) = sum A' f - (128 + z) sum A.
-// The scale of the chunk's block then multiplies that once.  Integer inputs
-// stay exact: every partial sum is an integer below 2^24.
+// bytes of INT3 (3-bit codes cross byte boundaries inside the chunk).  A code
+// q becomes a float by a single bit operation that drops it into mantissa
+// bits p .. p+bits-1 under exponent 126:  f = 0.5 + q * 2^(p-24).
+//   INT4: one byte-permute per code, p = 16 (even codes) and 12 (odd codes).
+//   INT3: one funnel shift per three codes, then one mask per code,
+//         p = 13, 16, 19 for codes 3i, 3i+1, 3i+2 of the chunk.
+// Activations are staged pre-multiplied by the matching power of two,
+// A'_j = A_j * 2^(24 - p_j) (exact), so A'_j f_j = A'_j / 2 + A_j q_j and
+//     sum_j A_j (q_j - z) = sum_j A'_j f_j - Csum - z * Asum
+// with Csum = sum_j A'_j / 2 and Asum = sum_j A_j per chunk, computed once
+// per staged activation row.  The block scale then multiplies the chunk
+// result once.  Integer inputs stay exact: every partial sum is an integer
+// below 2^24.
 #pragma once
 
 #include "common.cuh"
@@ -17,38 +23,57 @@ namespace mnb {
 namespace gemv {
 
 constexpr uint32_t kCodeExp = 0x3F000000u;  // exponent 126 in bits 23..30
-constexpr float kAScale = 256.0f;
 
 __host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Float images (0.5 + q/256) of the 4 codes 4g .. 4g+3 of a 32-code chunk.
+// Mantissa position of code j (0..31) of a chunk.  INT4: the even codes
+// (low nibbles) go to bits 16..19 and the odd codes (high nibbles, masked in
+// place) to bits 12..15.
+template <int BITS>
+__host__ __device__ constexpr int code_pos(int j) {
+    return BITS == 4 ? (j % 2 == 0 ? 16 : 12) : 13 + 3 * (j % 3);
+}
+
+// Power-of-two pre-scale of the activation that meets code j.
+template <int BITS>
+__host__ __device__ constexpr float code_scale(int j) {
+    return static_cast<float>(1u << (24 - code_pos<BITS>(j)));
+}
+
+// INT3: the 32-bit window of the chunk's 96-bit stream that holds code j at
+// bit code_pos(j).  j is a compile-time constant after unrolling.
+__device__ __forceinline__ uint32_t int3_window(const uint32_t (&w)[3], int j) {
+    const int first = j - j % 3;                  // first code of j's triplet
+    const int b = 3 * first - 13;                 // stream bit that lands on bit 0
+    if (b < 0) return w[0] << (-b);
+    const int i = b >> 5, o = b & 31;
+    if (o == 0) return w[i];
+    return __funnelshift_r(w[i], w[i + 1 < 3 ? i + 1 : 2], o);  // bits past the chunk are never used
+}
+
+// Float images of the 4 codes 4g .. 4g+3 of a 32-code chunk.
 template <int BITS>
 __device__ __forceinline__ void chunk_codes4(const uint32_t (&w)[BITS], int g, float2& f01, float2& f23) {
     if constexpr (BITS == 4) {
-        // word g/2 holds codes 8(g/2) .. 8(g/2)+7, low nibble first: its low
-        // nibbles are the even codes, its high nibbles the odd ones.
+        // word g/2 holds codes 8(g/2) .. 8(g/2)+7, low nibble first.  Byte b of
+        // lo is the even code 2b (placed at bits 16..19 of the image), byte b of
+        // hi is the odd code 2b+1 already shifted up by 4 (placed at bits 8..15,
+        // i.e. the code lands on bits 12..15).
         const uint32_t x = w[g >> 1];
         const uint32_t lo = x & 0x0F0F0F0Fu;
-        const uint32_t hi = (x >> 4) & 0x0F0F0F0Fu;
+        const uint32_t hi = x & 0xF0F0F0F0u;
         const uint32_t sub = (g & 1) * 2;
         f01.x = __uint_as_float(__byte_perm(lo, kCodeExp, 0x7044u | (sub << 8)));
-        f01.y = __uint_as_float(__byte_perm(hi, kCodeExp, 0x7044u | (sub << 8)));
+        f01.y = __uint_as_float(__byte_perm(hi, kCodeExp, 0x7404u | (sub << 4)));
         f23.x = __uint_as_float(__byte_perm(lo, kCodeExp, 0x7044u | ((sub + 1) << 8)));
-        f23.y = __uint_as_float(__byte_perm(hi, kCodeExp, 0x7044u | ((sub + 1) << 8)));
+        f23.y = __uint_as_float(__byte_perm(hi, kCodeExp, 0x7404u | ((sub + 1) << 4)));
     } else {
-        // 3-bit code j sits at stream bit 3j of the 96-bit chunk (w[0] first).
         uint32_t f[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int p = 3 * (4 * g + i);
-            const int wi = p >> 5, off = p & 31;
-            uint32_t x;
-            if (off >= 16)
-                x = (off + 3 <= 32) ? (w[wi] >> (off - 16))
-                                    : __funnelshift_r(w[wi], w[wi + 1 < BITS ? wi + 1 : wi], off - 16);
-            else
-                x = w[wi] << (16 - off);
-            f[i] = (x & 0x00070000u) | kCodeExp;
+            const int j = 4 * g + i;
+            const int p = code_pos<3>(j);
+            f[i] = and_or(int3_window(w, j), 7u << p, kCodeExp);
         }
         f01 = make_float2(__uint_as_float(f[0]), __uint_as_float(f[1]));
         f23 = make_float2(__uint_as_float(f[2]), __uint_as_float(f[3]));
@@ -78,34 +103,76 @@ __device__ __forceinline__ int zero_point_code(const uint8_t* zrow, int b) {
 
 // Shared-memory image of MT activation rows for the chunk loop: float4 i4 of
 // chunk c of row m (codes 32c + 4 i4 .. +3) lives at A4[(m*8 + i4)*C + c], so
-// consecutive lanes (consecutive c) read consecutive 16-byte words.
-// fetch(m, k) returns the activation (0 when out of range); the image holds
-// 256 * fetch, and Asum[m*C + c] the plain sum of the chunk's 32 activations.
-template <int MT, typename Fetch>
-__device__ __forceinline__ void stage_activations(float4* A4, float* Asum, int C, Fetch fetch, int tid, int nthreads) {
-    const int64_t Kpad = int64_t(C) * 32;
-    for (int64_t i = tid; i < int64_t(MT) * Kpad; i += nthreads) {
-        const int m = static_cast<int>(i / Kpad);
-        const int64_t k = i - int64_t(m) * Kpad;
-        const float v = kAScale * fetch(m, k);
-        const int c = static_cast<int>(k >> 5), i4 = static_cast<int>((k >> 2) & 7), e = static_cast<int>(k & 3);
-        reinterpret_cast<float*>(&A4[(int64_t(m) * 8 + i4) * C + c])[e] = v;
-    }
-    __syncthreads();
+// consecutive lanes (consecutive c) read consecutive 16-byte words.  One
+// thread stages one (row, chunk): it loads the chunk's 32 activations
+// (vectorised when `vec`), writes A'_j = A_j * code_scale(j), and the chunk's
+// correction Corr[m*C + c] = {-(Csum + z0 Asum) over even j, the same over odd
+// j, Asum over even j, Asum over odd j}, with Csum = sum A'_j / 2, Asum =
+// sum A_j and z0 = 2^(BITS-1) the implicit zero point, summed in ascending j.
+// (The f32x2 products keep even codes in .x and odd codes in .y.)
+// row(m) returns activation row m (dtype `dt`, K valid entries) or nullptr
+// for a row of zeros.
+template <int BITS, int MT, typename RowFn>
+__device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, int64_t K, int dt, bool vec, RowFn row,
+                                             int tid, int nthreads) {
+    constexpr float z0 = float(1 << (BITS - 1));
     for (int i = tid; i < MT * C; i += nthreads) {
         const int m = i / C, c = i - m * C;
-        float s = 0.f;
-        for (int j = 0; j < 32; ++j) s += reinterpret_cast<const float*>(&A4[(m * 8 + (j >> 2)) * C + c])[j & 3];
-        Asum[m * C + c] = s * (1.0f / kAScale);
+        const void* src = row(m);
+        const int64_t k0 = int64_t(c) * 32;
+        float v[32];
+        if (src != nullptr && vec && k0 + 32 <= K) {
+            if (dt == kF32) {
+                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + k0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 x = p[q];
+                    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                }
+            } else {
+                const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + k0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 x = p[q];
+                    const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (dt == kF16) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[h]));
+                            v[8 * q + 2 * h] = f.x; v[8 * q + 2 * h + 1] = f.y;
+                        } else {
+                            v[8 * q + 2 * h] = __uint_as_float(u[h] << 16);
+                            v[8 * q + 2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+                        }
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
+        }
+        float as[2] = {0.f, 0.f}, cs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            as[j & 1] += v[j];
+            v[j] *= code_scale<BITS>(j);
+            cs[j & 1] += 0.5f * v[j];
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            A4[(int64_t(m) * 8 + q) * C + c] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        Corr[m * C + c] = make_float4(-fmaf(z0, as[0], cs[0]), -fmaf(z0, as[1], cs[1]), as[0], as[1]);
     }
-    __syncthreads();
 }
 
-// One lane, chunk c of R packed rows: out[r][m] += scale[r] * sum_k A[m, k] (q[r, k] - z[r]).
-template <int BITS, int R, int MT>
-__device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], const float (&sc)[R], const float (&zz)[R],
-                                                 const float4* __restrict__ A4, const float* __restrict__ Asum, int C,
-                                                 int c, float (&out)[R][MT]) {
+// One lane, chunk c of R packed rows:
+//   out[r][m] += scale[r] * sum_k A[m, k] (q[r, k] - z[r])      (as an even/odd pair)
+// dz[r] = z0 - z[r] is the row's zero-point shift from the implicit one (used
+// only when HAS_ZP).
+template <int BITS, int R, int MT, bool HAS_ZP>
+__device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], const float (&sc)[R], const float (&dz)[R],
+                                                 const float4* __restrict__ A4, const float4* __restrict__ Corr, int C,
+                                                 int c, float2 (&out)[R][MT]) {
     float2 P[R][MT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -129,11 +196,12 @@ __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], c
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const float as = Asum[m * C + c];
+        const float4 cr = Corr[m * C + c];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float t = fmaf(-(128.0f + zz[r]), as, P[r][m].x + P[r][m].y);
-            out[r][m] = fmaf(sc[r], t, out[r][m]);
+            float2 t = __fadd2_rn(P[r][m], make_float2(cr.x, cr.y));
+            if constexpr (HAS_ZP) t = ffma2(make_float2(dz[r], dz[r]), make_float2(cr.z, cr.w), t);
+            out[r][m] = ffma2(make_float2(sc[r], sc[r]), t, out[r][m]);
         }
     }
 }

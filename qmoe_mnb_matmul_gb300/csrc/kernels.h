@@ -23,8 +23,10 @@ struct GemvArgs {
     int y_dtype;
     int64_t y_ld;          // row stride of Y in elements (N for a plain matmul)
     int rows_per_block;    // RC: rows of B staged per pipeline stage
+    int stages;            // depth of the shared-memory ring
     int n_blocks;          // ceil(N / RC)
     int chunks;            // C = nb * bs / 32 (32 codes per chunk)
+    int a_vec;             // activation rows may be read with 16-byte loads
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
@@ -35,6 +37,25 @@ cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool p
 
 // Shared memory the GEMV plan needs for (K, bits, bs, scale dtype, M); 0 if unsupported.
 size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype);
+
+// ------------------------------------------------ tensor-core GEMM (tcgen05)
+// Y[M, N] = A[M, K] . W^T, A fp16/bf16 row-major with K % 8 == 0 and a 16-byte
+// aligned base (TMA), swap-AB tiles of 128 weight rows.
+struct GemmTcArgs {
+    const void* A;
+    int a_dtype;
+    int64_t M, K;
+    const uint8_t* B;
+    const void* scales;
+    const uint8_t* zp;
+    int64_t N;
+    int bits, bs, nb;
+    int64_t row_bytes;
+    int zp_row_bytes;
+    void* Y;
+    int y_dtype;
+};
+cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream);
 
 // --------------------------------------------------------------- unpack
 cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
@@ -49,5 +70,6 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int3
 // Per-translation-unit device error words (read and cleared; 0 = none).
 cudaError_t gemv_take_error(unsigned int* out);
 cudaError_t qmoe_take_error(unsigned int* out);
+cudaError_t gemm_tc_take_error(unsigned int* out);
 
 }  // namespace mnb

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -13,6 +14,9 @@
 namespace mnb {
 
 namespace {
+
+// Smallest M routed to the tensor-core GEMM (fp16/bf16 activations only).
+constexpr int64_t kTcMinRows = 8;
 
 bool valid_dtype(int d) { return d == MNB_F32 || d == MNB_F16 || d == MNB_BF16; }
 bool valid_bits(int b) { return b == 3 || b == 4; }
@@ -40,6 +44,13 @@ int sm_count_current() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+// Programmatic dependent launch is on unless MNB_DISABLE_PDL is set in the
+// environment (for tools that replay kernels one by one).
+bool pdl_enabled() {
+    static const bool on = std::getenv("MNB_DISABLE_PDL") == nullptr;
+    return on;
 }
 
 mnb_status from_cuda(cudaError_t e) {
@@ -85,7 +96,7 @@ mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
     unsigned int first = 0;
-    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error};
+    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error};
     for (auto take : takers) {
         unsigned int v = 0;
         if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;
@@ -125,6 +136,29 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
     if (N > (int64_t(1) << 31)) return MNB_ERR_UNSUPPORTED;
     const int sms = sm_count_current();
     if (sms <= 0) return MNB_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    // Tensor-core path: fp16/bf16 activations, enough rows to fill an MMA
+    // column block, and a TMA-compatible activation matrix.
+    if (a_dtype != MNB_F32 && M >= kTcMinRows && K % 8 == 0 && aligned(A, 16)) {
+        GemmTcArgs g = {};
+        g.A = A;
+        g.a_dtype = a_dtype;
+        g.M = M;
+        g.K = K;
+        g.B = B_packed;
+        g.scales = scales;
+        g.zp = zero_points;
+        g.N = N;
+        g.bits = bits;
+        g.bs = block_size;
+        g.nb = static_cast<int>(pb.nb);
+        g.row_bytes = pb.row_bytes;
+        g.zp_row_bytes = static_cast<int>(pb.zp_row);
+        g.Y = Y;
+        g.y_dtype = y_dtype;
+        return from_cuda(launch_gemm_tc(g, scale_dtype, sms, pdl_enabled(), st));
+    }
     if (gemv_smem_bytes(M, K, bits, block_size, scale_dtype) == 0) return MNB_ERR_UNSUPPORTED;
 
     GemvArgs a = {};
@@ -145,7 +179,8 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
     a.y_dtype = y_dtype;
     a.y_ld = N;
     a.chunks = static_cast<int>(pb.nb * block_size / 32);
-    return from_cuda(launch_gemv(a, scale_dtype, sms, /*pdl=*/true, reinterpret_cast<cudaStream_t>(stream)));
+    a.a_vec = aligned(A, 16) && (K * int64_t(dsize(a_dtype))) % 16 == 0;
+    return from_cuda(launch_gemv(a, scale_dtype, sms, pdl_enabled(), st));
 }
 
 mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits, int block_size,
@@ -243,11 +278,12 @@ mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H
     q.fc2_bits = fc2_bits;
     q.bs = block_size;
     q.fc1_layout = fc1_layout;
+    q.x_vec = aligned(X, 16) && (H * 2) % 16 == 0;
     q.Y = Y;
     q.workspace = workspace;
     q.fc1 = {p1.nb, p1.row_bytes, p1.zp_row};
     q.fc2 = {p2.nb, p2.row_bytes, p2.zp_row};
-    return from_cuda(launch_qmoe(q, sms, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_qmoe(q, sms, pdl_enabled(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------ host validation

@@ -80,7 +80,7 @@ struct Fc1Plan {
 __host__ __device__ inline Fc1Plan fc1_plan(int MT, int C, int64_t row_bytes, int nb, int ssize) {
     Fc1Plan p;
     p.a4 = int64_t(MT) * 8 * C * 16;
-    p.asum = round_up(int64_t(MT) * C * 4, 128);
+    p.asum = round_up(int64_t(MT) * C * 16, 128);  // float4 corrections
     p.w = round_up(int64_t(2 * kPairsPerBlock) * row_bytes, 128);
     p.s = round_up(int64_t(2 * kPairsPerBlock) * nb * ssize, 128);
     p.total = 256 + p.a4 + p.asum + p.w + p.s;
@@ -93,7 +93,7 @@ struct Fc2Plan {
 __host__ __device__ inline Fc2Plan fc2_plan(int ACT, int C, int64_t row_bytes, int nb, int ssize) {
     Fc2Plan p;
     p.a4 = int64_t(ACT) * 8 * C * 16;
-    p.asum = round_up(int64_t(ACT) * C * 4, 128);
+    p.asum = round_up(int64_t(ACT) * C * 16, 128);  // float4 corrections
     p.w = round_up(int64_t(kRowsPerBlock2) * row_bytes, 128);  // per expert slot
     p.s = round_up(int64_t(kRowsPerBlock2) * nb * ssize, 128);
     p.total = 256 + p.a4 + p.asum + int64_t(ACT) * (p.w + p.s);
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
     float* s_w = reinterpret_cast<float*>(smem + 128);      // routing weights (decode)
     int* s_idx = reinterpret_cast<int*>(smem + 192);        // routing experts (decode)
     float4* A4 = reinterpret_cast<float4*>(smem + 256);
-    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
     uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
     const S* Sst = reinterpret_cast<const S*>(Wst + plan.w);
 
@@ -185,13 +185,14 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             bulk_g2s(Sdst + kPairsPerBlock * nb * sizeof(S), S1 + (I + pair0) * nb, pc * srow, bar);
         }
     }
-    stage_activations<MT>(
-        A4, Asum, C,
-        [&](int m, int64_t kk) -> float {
+    stage_chunks<BITS, MT>(
+        A4, Corr, C, q.H, q.act_dtype, q.x_vec != 0,
+        [&](int m) -> const void* {
             const int t = m < cnt ? s_int[4 + m] : -1;
-            return (t >= 0 && kk < q.H) ? load_as_f32(q.X, q.act_dtype, int64_t(t) * q.H + kk) : 0.f;
+            return t >= 0 ? static_cast<const char*>(q.X) + int64_t(t) * q.H * 2 : nullptr;
         },
         tid, kThreads);
+    __syncthreads();
     grid_launch_dependents();
     const bool ok = mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -204,11 +205,11 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
 
     // Warp unit: pairs 2g and 2g+1 -> logical rows (gate 2g, up 2g, gate 2g+1, up 2g+1).
     for (int g = warp; 2 * g < pc; g += kWarps) {
-        float out[R][MT];
+        float2 out2[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) out[r][m] = 0.f;
+            for (int m = 0; m < MT; ++m) out2[r][m] = make_float2(0.f, 0.f);
         int lrow[R];      // row inside the staged block
         int64_t grow[R];  // row inside the expert's FC1 weight
 #pragma unroll
@@ -226,14 +227,18 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             for (int r = 0; r < R; ++r) {
                 load_chunk<BITS>(Wst + int64_t(lrow[r]) * rb, c, w[r]);
                 sc[r] = to_f32(Sst[lrow[r] * nb + b]);
-                zz[r] = float(Z1 ? zero_point_code<BITS>(Z1 + grow[r] * q.fc1.zp_row, b) : kZImplicit);
+                zz[r] = Z1 ? float(kZImplicit - zero_point_code<BITS>(Z1 + grow[r] * q.fc1.zp_row, b)) : 0.f;
             }
-            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Asum, C, c, out);
+            if (Z1)
+                chunk_accumulate<BITS, R, MT, true>(w, sc, zz, A4, Corr, C, c, out2);
+            else
+                chunk_accumulate<BITS, R, MT, false>(w, sc, zz, A4, Corr, C, c, out2);
         }
+        float out[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out[r][m]);
+            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out2[r][m].x + out2[r][m].y);
         if (lane == 0) {
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
@@ -262,12 +267,12 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
     const int C = static_cast<int>(q.fc2.nb * q.bs / 32);
     const int nb = static_cast<int>(q.fc2.nb);
     const int64_t rb = q.fc2.row_bytes;
-    const Fc2Plan plan = fc2_plan(k, C, rb, nb, sizeof(S));
+    const Fc2Plan plan = fc2_plan(kDecodeMaxK, C, rb, nb, sizeof(S));
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     float* s_w = reinterpret_cast<float*>(smem + 128);
     int* s_idx = reinterpret_cast<int*>(smem + 192);
     float4* A4 = reinterpret_cast<float4*>(smem + 256);
-    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
     uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
     uint8_t* Sst = Wst + int64_t(k) * plan.w;
 
@@ -301,10 +306,11 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
             bulk_g2s(Sst + j * plan.s, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
         }
     }
-    for (int j = 0; j < k; ++j)
-        stage_activations<1>(
-            A4 + int64_t(j) * 8 * C, Asum + j * C, C,
-            [&](int, int64_t kk) -> float { return kk < I ? h[(t * k + j) * I + kk] : 0.f; }, tid, kThreads);
+    stage_chunks<BITS, kDecodeMaxK>(
+        A4, Corr, C, I, kF32, true,
+        [&](int j) -> const void* { return j < k ? static_cast<const void*>(h + (t * k + j) * I) : nullptr; }, tid,
+        kThreads);
+    __syncthreads();
     grid_launch_dependents();
     const bool ok = mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -321,9 +327,9 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
             const uint8_t* W = Wst + j * plan.w;
             const S* Sc = reinterpret_cast<const S*>(Sst + j * plan.s);
             const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
-            float out[R][1];
+            float2 out[R][1];
 #pragma unroll
-            for (int r = 0; r < R; ++r) out[r][0] = 0.f;
+            for (int r = 0; r < R; ++r) out[r][0] = make_float2(0.f, 0.f);
             for (int c = lane; c < C; c += 32) {
                 const int b = (c * 32) >> bs_shift;
                 uint32_t w[R][BITS];
@@ -333,13 +339,16 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
                     const int rl = min(g * R + r, rc - 1);
                     load_chunk<BITS>(W + int64_t(rl) * rb, c, w[r]);
                     sc[r] = to_f32(Sc[rl * nb + b]);
-                    zz[r] = float(Z2 ? zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b) : kZImplicit);
+                    zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
                 }
-                chunk_accumulate<BITS, R, 1>(w, sc, zz, A4 + int64_t(j) * 8 * C, Asum + j * C, C, c, out);
+                if (Z2)
+                    chunk_accumulate<BITS, R, 1, true>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
+                else
+                    chunk_accumulate<BITS, R, 1, false>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
             }
             const float wj = s_w[j];
 #pragma unroll
-            for (int r = 0; r < R; ++r) acc[r] = fmaf(wj, out[r][0], acc[r]);
+            for (int r = 0; r < R; ++r) acc[r] = fmaf(wj, out[r][0].x + out[r][0].y, acc[r]);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) acc[r] = warp_sum(acc[r]);
@@ -367,7 +376,7 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     int* s_int = reinterpret_cast<int*>(smem + 16);
     float4* A4 = reinterpret_cast<float4*>(smem + 256);
-    float* Asum = reinterpret_cast<float*>(smem + 256 + plan.a4);
+    float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
     uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
     const S* Sc = reinterpret_cast<const S*>(Wst + plan.w);
 
@@ -398,9 +407,11 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
         bulk_g2s(Wst, q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes, bar);
         bulk_g2s(Wst + plan.w, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
     }
-    stage_activations<MT>(
-        A4, Asum, C, [&](int m, int64_t kk) -> float { return (m < cnt && kk < I) ? h[(s0 + m) * I + kk] : 0.f; },
-        tid, kThreads);
+    stage_chunks<BITS, MT>(
+        A4, Corr, C, I, kF32, true,
+        [&](int m) -> const void* { return m < cnt ? static_cast<const void*>(h + (s0 + m) * I) : nullptr; }, tid,
+        kThreads);
+    __syncthreads();
     grid_launch_dependents();
     const bool ok = mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -411,11 +422,11 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
     constexpr int kZImplicit = 1 << (BITS - 1);
     const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
     for (int g = warp; g * R < rc; g += kWarps) {
-        float out[R][MT];
+        float2 out2[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) out[r][m] = 0.f;
+            for (int m = 0; m < MT; ++m) out2[r][m] = make_float2(0.f, 0.f);
         for (int c = lane; c < C; c += 32) {
             const int b = (c * 32) >> bs_shift;
             uint32_t w[R][BITS];
@@ -425,14 +436,18 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
                 const int rl = min(g * R + r, rc - 1);
                 load_chunk<BITS>(Wst + int64_t(rl) * rb, c, w[r]);
                 sc[r] = to_f32(Sc[rl * nb + b]);
-                zz[r] = float(Z2 ? zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b) : kZImplicit);
+                zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
             }
-            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Asum, C, c, out);
+            if (Z2)
+                chunk_accumulate<BITS, R, MT, true>(w, sc, zz, A4, Corr, C, c, out2);
+            else
+                chunk_accumulate<BITS, R, MT, false>(w, sc, zz, A4, Corr, C, c, out2);
         }
+        float out[R][MT];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out[r][m]);
+            for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(out2[r][m].x + out2[r][m].y);
         if (lane == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -494,7 +509,7 @@ __global__ void combine_kernel(const __grid_constant__ QmoeArgs q) {
 // ------------------------------------------------------------ launching
 
 template <typename Kern>
-cudaError_t launch(Kern kern, dim3 grid, int64_t smem, cudaStream_t stream, const QmoeArgs& q) {
+cudaError_t launch(Kern kern, dim3 grid, int64_t smem, cudaStream_t stream, const QmoeArgs& q, bool pdl) {
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -507,20 +522,20 @@ cudaError_t launch(Kern kern, dim3 grid, int64_t smem, cudaStream_t stream, cons
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 template <int BITS, int ST, int MT, bool DECODE>
-cudaError_t launch_fc1(const QmoeArgs& q, unsigned gx, cudaStream_t stream) {
+cudaError_t launch_fc1(const QmoeArgs& q, unsigned gx, cudaStream_t stream, bool pdl) {
     const int C = static_cast<int>(q.fc1.nb * q.bs / 32);
     const Fc1Plan p = fc1_plan(MT, C, q.fc1.row_bytes, static_cast<int>(q.fc1.nb), ST == kF32 ? 4 : 2);
     const unsigned gy = static_cast<unsigned>(cdiv<int64_t>(q.I, kPairsPerBlock));
-    return launch(fc1_kernel<BITS, ST, MT, DECODE>, dim3(gx, gy, 1), p.total, stream, q);
+    return launch(fc1_kernel<BITS, ST, MT, DECODE>, dim3(gx, gy, 1), p.total, stream, q, pdl);
 }
 
 template <int B1, int B2, int ST>
-cudaError_t run_typed(const QmoeArgs& q, cudaStream_t stream) {
+cudaError_t run_typed(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
     char* ws = static_cast<char*>(q.workspace);
     const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
     const int64_t P = q.T * q.k;
@@ -528,10 +543,10 @@ cudaError_t run_typed(const QmoeArgs& q, cudaStream_t stream) {
     const unsigned gy2 = static_cast<unsigned>(cdiv<int64_t>(q.H, kRowsPerBlock2));
     cudaError_t e;
     if (use_decode(q)) {
-        e = launch_fc1<B1, ST, 1, true>(q, static_cast<unsigned>(P), stream);
+        e = launch_fc1<B1, ST, 1, true>(q, static_cast<unsigned>(P), stream, pdl);
         if (e != cudaSuccess) return e;
-        const Fc2Plan p2 = fc2_plan(q.k, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
-        return launch(fc2_decode_kernel<B2, ST>, dim3(static_cast<unsigned>(q.T), gy2, 1), p2.total, stream, q);
+        const Fc2Plan p2 = fc2_plan(kDecodeMaxK, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
+        return launch(fc2_decode_kernel<B2, ST>, dim3(static_cast<unsigned>(q.T), gy2, 1), p2.total, stream, q, pdl);
     }
     int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
     float* wts = reinterpret_cast<float*>(ws + L.wts);
@@ -543,20 +558,20 @@ cudaError_t run_typed(const QmoeArgs& q, cudaStream_t stream) {
     tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
-    if ((e = launch_fc1<B1, ST, kTileM, false>(q, gx, stream)) != cudaSuccess) return e;
+    if ((e = launch_fc1<B1, ST, kTileM, false>(q, gx, stream, pdl)) != cudaSuccess) return e;
     const Fc2Plan p2 = fc2_plan(kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
-    if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q)) != cudaSuccess) return e;
+    if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q, pdl)) != cudaSuccess) return e;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), 152 * 16);
     combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
     return cudaGetLastError();
 }
 
 template <int ST>
-cudaError_t run_bits(const QmoeArgs& q, cudaStream_t stream) {
-    if (q.fc1_bits == 3 && q.fc2_bits == 3) return run_typed<3, 3, ST>(q, stream);
-    if (q.fc1_bits == 3 && q.fc2_bits == 4) return run_typed<3, 4, ST>(q, stream);
-    if (q.fc1_bits == 4 && q.fc2_bits == 3) return run_typed<4, 3, ST>(q, stream);
-    return run_typed<4, 4, ST>(q, stream);
+cudaError_t run_bits(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
+    if (q.fc1_bits == 3 && q.fc2_bits == 3) return run_typed<3, 3, ST>(q, pdl, stream);
+    if (q.fc1_bits == 3 && q.fc2_bits == 4) return run_typed<3, 4, ST>(q, pdl, stream);
+    if (q.fc1_bits == 4 && q.fc2_bits == 3) return run_typed<4, 3, ST>(q, pdl, stream);
+    return run_typed<4, 4, ST>(q, pdl, stream);
 }
 
 }  // namespace
@@ -571,9 +586,9 @@ bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
 
 cudaError_t qmoe_take_error(unsigned int* out) { return take_unit_error(out); }
 
-cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, cudaStream_t stream) {
+cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream) {
     (void)sm_count;
-    return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, stream) : run_bits<kBF16>(q, stream);
+    return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, pdl, stream) : run_bits<kBF16>(q, pdl, stream);
 }
 
 }  // namespace mnb

@@ -28,6 +28,7 @@ struct QmoeArgs {
     int fc2_bits;
     int bs;
     int fc1_layout;
+    int x_vec;  // X rows may be read with 16-byte loads
     void* Y;
     void* workspace;
     ProjGeom fc1, fc2;
@@ -36,6 +37,6 @@ struct QmoeArgs {
 // Workspace bytes for one qmoe_forward call; false on overflow.
 bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int64_t* bytes);
 
-cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, cudaStream_t stream);
+cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream);
 
 }  // namespace mnb

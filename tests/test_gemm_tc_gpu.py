@@ -1,0 +1,111 @@
+"""GPU parity of mnb_matmul's tensor-core path (tcgen05, fp16/bf16 activations,
+M >= 8) against the oracle: every output of a sample of activation rows."""
+import os
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests._util import assert_close, empty_guarded, guards_intact, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import qmoe_mnb_matmul_gb300 as mnb  # noqa: E402
+
+THREADS = os.cpu_count() or 1
+
+
+def seed(*key):
+    return zlib.crc32(repr(key).encode())
+
+
+def run(A, a_dt, packed, scales, s_dt, zp, N, K, bits, bs, y_dt):
+    A_d = to_dev(A, a_dt)
+    M = A_d.numel() // K
+    Y, full = empty_guarded(M * N, y_dt)
+    mnb.mnb_matmul(A_d, to_dev(packed), to_dev(scales, s_dt), None if zp is None else to_dev(zp), N, bits, bs, Y,
+                   K=K, M=M)
+    torch.cuda.synchronize()
+    assert guards_intact(full), "write outside Y"
+    assert mnb.mnb_get_last_device_error() == 0
+    return to_f64(Y).reshape(M, N)
+
+
+def sample_rows(M, n=12):
+    g = wl.rng(M)
+    return sorted(set([0, M - 1, M // 2] + list(g.integers(0, M, n))))
+
+
+def check(M, K, N, bits, bs, a_dt="bf16", s_dt="f32", y_dt="bf16", with_zp=False, key=()):
+    g = wl.rng(seed(M, K, N, bits, bs, a_dt, s_dt, y_dt, with_zp, *key))
+    packed, scales, zp = wl.quantized_weight(g, N, K, bits, bs, s_dt, with_zp)
+    A = wl.normal(g, (M, K), a_dt)
+    y = run(A, a_dt, packed, scales, s_dt, zp, N, K, bits, bs, y_dt)
+    rows = sample_rows(M)
+    ref = oracle.mnb_matmul(A, a_dt, packed, scales, s_dt, zp, N, K, bits, bs, mrows=rows, threads=THREADS)
+    assert_close(y[rows], ref, y_dt)
+
+
+@pytest.mark.parametrize("M", [16, 128, 512, 2048])
+@pytest.mark.parametrize("name,K,N", wl.QWEN3_1P7B_PROJECTIONS + [wl.QWEN3_1P7B_LM_HEAD])
+def test_qwen3_prefill_projection(M, name, K, N):
+    """Same INT4 weights layout as the decode suite: bf16 activations, fp32 scales, bf16 out."""
+    check(M, K, N, 4, 32, key=(name,))
+
+
+@pytest.mark.parametrize("M,K,N,bs", [(128, 2080, 512, 32), (512, 2072, 384, 32), (128, 2080, 640, 64),
+                                      (300, 2080, 256, 128), (128, 2048, 6147, 32), (512, 2048, 6147, 32)])
+def test_tails(M, K, N, bs):
+    check(M, K, N, 4, bs)
+
+
+@pytest.mark.parametrize("M", [8, 9, 17, 100, 255, 257, 1000])
+def test_row_counts(M):
+    check(M, 1024, 768, 4, 32)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("with_zp", [False, True])
+def test_formats(bits, bs, with_zp):
+    check(256, 2048, 1024, bits, bs, "f16", "f16", "f16", with_zp)
+
+
+@pytest.mark.parametrize("a_dt,s_dt,y_dt", [("bf16", "bf16", "bf16"), ("f16", "f32", "f32"), ("bf16", "f32", "f32"),
+                                            ("f16", "f16", "bf16")])
+def test_dtypes(a_dt, s_dt, y_dt):
+    check(200, 1536, 896, 3, 64, a_dt, s_dt, y_dt, with_zp=True)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_integer_data_is_bit_exact(bits):
+    """scales = 1, zero points 0, integer activations: the bf16 tile holds the codes
+    exactly and every fp32 partial sum is an integer below 2^24."""
+    g = wl.rng(seed("tc-int", bits))
+    M, N, K, bs = 200, 384, 2048, 64
+    codes = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    packed = oracle.pack_codes(codes, bits, bs)
+    zp = oracle.pack_zero_points(np.zeros((N, K // bs), np.uint8), bits)
+    Af = g.integers(-4, 5, size=(M, K)).astype(np.float32)
+    y = run(wl.cast(Af, "bf16"), "bf16", packed, np.ones((N, K // bs), np.float32), "f32", zp, N, K, bits, bs, "f32")
+    assert np.array_equal(y, (Af.astype(np.int64) @ codes.astype(np.int64).T).astype(np.float64))
+
+
+def test_deterministic_and_matches_across_paths():
+    """M = 8 (tensor cores) against M = 4 + 4 (CUDA cores) on the same rows."""
+    g = wl.rng(seed("paths"))
+    K, N = 2048, 1024
+    packed, scales, _ = wl.quantized_weight(g, N, K, 4, 32)
+    A = wl.normal(g, (8, K), "bf16")
+    y8 = run(A, "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32")
+    y8b = run(A, "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32")
+    assert np.array_equal(y8, y8b)
+    y4 = np.concatenate([run(A[:4], "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32"),
+                         run(A[4:], "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32")])
+    assert np.max(np.abs(y8 - y4)) <= 2e-2 * np.sqrt(np.mean(y4 ** 2))
