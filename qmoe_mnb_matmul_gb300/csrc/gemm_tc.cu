@@ -320,7 +320,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int64_t m = m0 + c0 + j;
-                        if (m < a.M) store_from_f32(a.Y, a.y_dtype, m * a.N + n, __uint_as_float(v[j]));
+                        // a 16-column tile loads 32 columns: the upper 16 belong to the other accumulator
+                        if (c0 + j < BN && m < a.M) store_from_f32(a.Y, a.y_dtype, m * a.N + n, __uint_as_float(v[j]));
                     }
                 }
             }

@@ -213,32 +213,51 @@ int64_t row_align(int64_t row_bytes, int nb, int ssize) {
     return std::max(g16(row_bytes), g16(int64_t(nb) * ssize));
 }
 
-// Rows per warp: as many as keep at least ~1.5 blocks per SM.
-int pick_r(int64_t N, int64_t row_bytes, int nb, int ssize, int sm_count) {
+// Launch shape: rows per warp R and ring depth.  Each CTA wants ~48 KB of
+// weights in flight; the SM wants 3 resident CTAs (27 warps) to hide the
+// latency of the dependent decode chains; and the grid wants >= 1.5 blocks per
+// SM.  The largest R meeting all three wins; otherwise the best compromise.
+struct Shape {
+    int R = 4, stages = 2;
+};
+constexpr int64_t kSmSmem = 228 * 1024, kCtaReserve = 1024;
+
+Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count) {
     const int64_t align = row_align(row_bytes, nb, ssize);
+    Shape best;
+    int64_t best_score = -1;
     for (int R : {4, 2, 1}) {
-        const int64_t RC = int64_t(kConsumerWarps) * R;
-        if (RC % align != 0) return 4;
-        if (R == 1 || cdiv<int64_t>(N, RC) >= int64_t(sm_count) * 3 / 2) return R;
+        const int RC = kConsumerWarps * R;
+        if (RC % align != 0) continue;
+        const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
+        const int64_t stage = p1.w_stage + p1.s_stage;
+        if (p1.fixed + 2 * stage > kSmemBudget) continue;
+        int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, cdiv<int64_t>(49152, stage))));
+        while (st > 2 && p1.fixed + st * stage > kSmemBudget) --st;
+        auto ctas = [&](int s) { return kSmSmem / (p1.fixed + s * stage + kCtaReserve); };
+        while (st > 2 && ctas(st) < 3 && ctas(st - 1) > ctas(st)) --st;
+        const int64_t resident = std::min<int64_t>(3, ctas(st));
+        const bool enough_blocks = cdiv<int64_t>(N, RC) >= int64_t(sm_count) * 3 / 2;
+        const int64_t score = (enough_blocks ? 100 : 0) + 10 * resident + R;
+        if (score > best_score) {
+            best_score = score;
+            best.R = R;
+            best.stages = st;
+        }
     }
-    return 4;
+    return best;
 }
 
 template <int BITS, int ST, int MT, int R>
-cudaError_t launch_typed(GemvArgs a, int sm_count, bool pdl, cudaStream_t stream) {
+cudaError_t launch_typed(GemvArgs a, int stages, int sm_count, bool pdl, cudaStream_t stream) {
     constexpr int RC = kConsumerWarps * R;
     const int ssize = ST == kF32 ? 4 : 2;
     a.rows_per_block = RC;
     a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, RC));
     const Plan p1 = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, 1);
-    const int64_t stage = p1.w_stage + p1.s_stage;
-    if (p1.fixed + 2 * stage > kSmemBudget) return cudaErrorNotSupported;
-    // Enough stages for ~48 KB in flight per CTA; fewer if that keeps two CTAs per SM.
-    int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, cdiv<int64_t>(49152, stage))));
-    while (st > 2 && p1.fixed + st * stage > kSmemBudget) --st;
-    if (2 * (p1.fixed + st * stage) > kSmemBudget && 2 * (p1.fixed + 2 * stage) <= kSmemBudget)
-        while (st > 2 && 2 * (p1.fixed + st * stage) > kSmemBudget) --st;
-    a.stages = st;
+    if (p1.fixed + int64_t(stages) * (p1.w_stage + p1.s_stage) > kSmemBudget) return cudaErrorNotSupported;
+    a.stages = stages;
+    const int st = stages;
     const Plan p = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, st);
     auto kern = gemv_kernel<BITS, ST, MT, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
@@ -263,18 +282,20 @@ cudaError_t launch_typed(GemvArgs a, int sm_count, bool pdl, cudaStream_t stream
 }
 
 template <int BITS, int ST, int MT>
-cudaError_t launch_r(const GemvArgs& a, int R, int sm_count, bool pdl, cudaStream_t stream) {
-    if (R == 4) return launch_typed<BITS, ST, MT, 4>(a, sm_count, pdl, stream);
-    if (R == 2) return launch_typed<BITS, ST, MT, 2>(a, sm_count, pdl, stream);
-    return launch_typed<BITS, ST, MT, 1>(a, sm_count, pdl, stream);
+cudaError_t launch_r(const GemvArgs& a, const Shape& sh, int sm_count, bool pdl, cudaStream_t stream) {
+    if (sh.R == 4) return launch_typed<BITS, ST, MT, 4>(a, sh.stages, sm_count, pdl, stream);
+    if (sh.R == 2) return launch_typed<BITS, ST, MT, 2>(a, sh.stages, sm_count, pdl, stream);
+    return launch_typed<BITS, ST, MT, 1>(a, sh.stages, sm_count, pdl, stream);
 }
 
 template <int BITS, int ST>
-cudaError_t launch_mt(const GemvArgs& a, int R, int sm_count, bool pdl, cudaStream_t stream) {
-    switch (pick_mt(a.M)) {
-        case 1: return launch_r<BITS, ST, 1>(a, R, sm_count, pdl, stream);
-        case 2: return launch_r<BITS, ST, 2>(a, R, sm_count, pdl, stream);
-        default: return launch_r<BITS, ST, 4>(a, R, sm_count, pdl, stream);
+cudaError_t launch_mt(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t stream) {
+    const int MT = pick_mt(a.M);
+    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count);
+    switch (MT) {
+        case 1: return launch_r<BITS, ST, 1>(a, sh, sm_count, pdl, stream);
+        case 2: return launch_r<BITS, ST, 2>(a, sh, sm_count, pdl, stream);
+        default: return launch_r<BITS, ST, 4>(a, sh, sm_count, pdl, stream);
     }
 }
 
@@ -293,15 +314,14 @@ size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype) 
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
-    const int R = pick_r(a.N, a.row_bytes, a.nb, ssize_of(scale_dtype), sm_count);
     if (a.bits == 4) {
-        if (scale_dtype == kF32) return launch_mt<4, kF32>(a, R, sm_count, pdl, stream);
-        if (scale_dtype == kF16) return launch_mt<4, kF16>(a, R, sm_count, pdl, stream);
-        return launch_mt<4, kBF16>(a, R, sm_count, pdl, stream);
+        if (scale_dtype == kF32) return launch_mt<4, kF32>(a, sm_count, pdl, stream);
+        if (scale_dtype == kF16) return launch_mt<4, kF16>(a, sm_count, pdl, stream);
+        return launch_mt<4, kBF16>(a, sm_count, pdl, stream);
     }
-    if (scale_dtype == kF32) return launch_mt<3, kF32>(a, R, sm_count, pdl, stream);
-    if (scale_dtype == kF16) return launch_mt<3, kF16>(a, R, sm_count, pdl, stream);
-    return launch_mt<3, kBF16>(a, R, sm_count, pdl, stream);
+    if (scale_dtype == kF32) return launch_mt<3, kF32>(a, sm_count, pdl, stream);
+    if (scale_dtype == kF16) return launch_mt<3, kF16>(a, sm_count, pdl, stream);
+    return launch_mt<3, kBF16>(a, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

