@@ -130,6 +130,33 @@ mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H
                         mnb_fc1_layout fc1_layout, void* Y, void* workspace,
                         size_t workspace_bytes, mnb_stream_t stream);
 
+/* qmoe_forward without a workspace argument, for callers that cannot allocate
+ * device memory: code that receives only input and output pointers (a plugin
+ * or an operator inside another runtime that owns every allocation), code
+ * running under a fixed device-memory budget that forbids new allocations,
+ * and code that must not call cudaMalloc/cudaFree on its path (they
+ * synchronise the device and cannot be recorded in a CUDA graph).  The pages
+ * have no counterpart to this entry point; it exists for those callers.
+ *
+ * Scratch: a fixed 8 MiB array inside the library, one copy on every GPU
+ * that loads the library, held until the process exits.  Problems whose
+ * qmoe_workspace_size() exceeds 8 MiB return MNB_ERR_WORKSPACE (with the
+ * Qwen3-30B-A3B layer, H 2048, I 768, E 128, k 8, that is T <= 92 tokens;
+ * T = 1 needs 91 KiB).
+ * The first call on a device looks up the array's device address on the
+ * current device; make that first call before any stream capture.  Every
+ * call uses the same array and leaves its contents behind; nothing in it has
+ * to start at zero, but calls that overlap on the GPU (other streams, other
+ * host threads) race on it and must be serialised by the caller.  Allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library call).  All other
+ * arguments, layouts and errors are those of qmoe_forward. */
+mnb_status qmoe_forward_static(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H,
+                               const float* router_logits, int64_t E, int k, int normalize_topk,
+                               const uint8_t* fc1_w, const void* fc1_scales, const uint8_t* fc1_zp,
+                               int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                               const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
+                               mnb_fc1_layout fc1_layout, void* Y, mnb_stream_t stream);
+
 /* The routing step alone: topk_idx int32 [T, k], topk_w fp32 [T, k]. */
 mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk,
                       int32_t* topk_idx, float* topk_w, mnb_stream_t stream);

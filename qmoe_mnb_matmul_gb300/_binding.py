@@ -42,6 +42,8 @@ _SIGNATURES = {
     "qmoe_workspace_size": [_I64, _I64, _I64, _I64, _I, _I, ctypes.POINTER(_SZ)],
     "qmoe_forward": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
                      _P, _P, _SZ, _P],
+    "qmoe_forward_static": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
+                            _P, _P],
     "qmoe_route": [_P, _I64, _I64, _I, _I, _P, _P, _P],
     "qmoe_permute": [_P, _I64, _I, _I64, _P, _P, _P, _P],
     "mnb_unpack_codes": [_P, _I64, _I64, _I, _I, _P, _P],
@@ -174,6 +176,26 @@ def qmoe_forward(X, router_logits, k, normalize_topk, fc1_w, fc1_scales, fc1_zp,
                                      _ptr(workspace), workspace_bytes, _stream(stream))
     if check:
         _check(st, "qmoe_forward")
+    return st
+
+
+def qmoe_forward_static(X, router_logits, k, normalize_topk, fc1_w, fc1_scales, fc1_zp, fc1_bits, fc2_w,
+                        fc2_scales, fc2_zp, fc2_bits, I, block_size, Y, stream=None, *, fc1_layout=FC1_INTERLEAVED,
+                        T=None, H=None, E=None, act_dtype=None, check=True):
+    """qmoe_forward with the library's fixed 8 MiB scratch instead of a caller workspace."""
+    if H is None:
+        H = X.shape[-1]
+    if T is None:
+        T = X.numel() // H
+    if E is None:
+        E = router_logits.shape[-1]
+    act_dtype = _dtype_code(X) if act_dtype is None else act_dtype
+    st = load_library().qmoe_forward_static(_ptr(X), act_dtype, T, H, _ptr(router_logits), E, k,
+                                            int(bool(normalize_topk)), _ptr(fc1_w), _ptr(fc1_scales), _ptr(fc1_zp),
+                                            fc1_bits, _ptr(fc2_w), _ptr(fc2_scales), _ptr(fc2_zp), fc2_bits, I,
+                                            block_size, fc1_layout, _ptr(Y), _stream(stream))
+    if check:
+        _check(st, "qmoe_forward_static")
     return st
 
 
