@@ -1,0 +1,574 @@
+// gemm_tc_impl.cuh -- weight-only matmul on the 5th-generation tensor cores
+// (tcgen05, sm_103a) with the weights dequantised tile by tile in shared
+// memory: the small-M / prefill MatMulNBits GEMM ("Qwen3 Missing-Kernel
+// Implementation Plan", row K03: small-M and prefill GEMM on the same
+// compressed weights, bounded workspace, partial blocks and output tails) and
+// the grouped per-expert FC1 (+SwiGLU) and FC2 GEMMs of the QMoE prefill (the
+// "selected-expert / tiled-dequantisation plus GEMM" prefill the QMoE CUDA
+// page names as missing).
+//
+// Tiles are 128 weight rows x BN activation rows.  The MMA is "swap-AB": the
+// dequantised weight tile is operand A (M = 128) and the activation tile
+// operand B (N = BN <= 256), so the fp32 accumulator in tensor memory holds
+// Y^T (lane = weight row, column = activation row) and small M costs no
+// padding on the weight side.  One persistent CTA per SM walks the tiles.
+//
+// Warp roles (448 threads):
+//   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle), or
+//               (FC1) cp.async gathers of the routed tokens' rows into the
+//               same swizzled layout
+//   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
+//   warps 2-9   dequant: two threads per weight row, one 32-code chunk each
+//               per K step; a private cp.async ring of packed bytes and scales;
+//               codes -> s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
+//   warps 10-13 epilogue: tcgen05.ld of the double-buffered accumulator ->
+//               output dtype (FC1: SwiGLU of lane pairs) -> masked stores
+// Stage s of the shared ring holds one K step's activation tile and
+// dequantised weight tile; a tcgen05.commit releases it when the MMAs that
+// read it complete.  Every wait is bounded.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemv_core.cuh"
+#include "kernels.h"
+
+namespace mnb {
+
+namespace {
+
+using namespace gemv;
+
+constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
+constexpr int kBW = 128;    // weight rows per tile (MMA M)
+constexpr int kPack = 4;    // depth of each dequant thread's cp.async ring
+constexpr int kDequantWarp0 = 2, kDequantWarps = 8, kEpilogueWarp0 = 10;
+constexpr int kThreadsTC = (kEpilogueWarp0 + 4) * 32;
+constexpr int kMaxStagesTC = 8;
+
+enum { kModeGemm = 0, kModeFc1 = 1 };
+
+struct TcPlan {
+    int64_t bars, act, w, pack, scl, total;
+};
+
+__host__ __device__ inline TcPlan tc_plan(int BN, int stages, int bits) {
+    TcPlan p;
+    p.bars = 1024;                                           // barriers and the TMEM address
+    p.act = int64_t(BN) * 128;                               // activations of one stage
+    p.w = int64_t(kBW) * 128;                                // dequantised weights of one stage
+    p.pack = int64_t(kPack) * 2 * kBW * (bits == 4 ? 16 : 12);
+    p.scl = int64_t(kPack) * 2 * kBW * 4;
+    p.total = p.bars + int64_t(stages) * (p.act + p.w) + p.pack + p.scl;
+    return p;
+}
+
+// Byte offset of 16-byte chunk c (k elements 8c .. 8c+7) of row r inside a
+// 128-byte-swizzled tile: atoms of 8 rows x 128 bytes, chunk index XOR row % 8.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int ST>
+__device__ __forceinline__ float scale_from_word(uint32_t word, int64_t idx) {
+    if constexpr (ST == kF32) {
+        return __uint_as_float(word);
+    } else {
+        const uint32_t h = (idx & 1) ? (word >> 16) : (word & 0xFFFFu);
+        if constexpr (ST == kF16) return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+        return __uint_as_float(h << 16);
+    }
+}
+
+template <int AT>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (AT == kBF16) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    } else {
+        const __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    }
+}
+
+// Ring position of the i-th K step of this CTA: stage index and how many
+// times the ring has wrapped, advanced without divisions.
+struct RingPos {
+    int stage = 0;
+    uint32_t round = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++stage == S) { stage = 0; ++round; }
+    }
+};
+
+// Tile t -> (expert, first activation row, rows, first weight row).
+struct Tile {
+    int e, s0, cnt, n0;
+};
+
+__device__ __forceinline__ Tile tile_of(const TcArgs& a, int t, int BN) {
+    Tile x;
+    if (a.mtiles) {
+        const int j = t / a.tiles_n;
+        const int4 mt = a.mtiles[j];
+        x.e = mt.x;
+        x.s0 = mt.y;
+        x.cnt = mt.z;
+        x.n0 = (t - j * a.tiles_n) * kBW;
+    } else {
+        const int nt = t / a.tiles_m;
+        const int mtile = t - nt * a.tiles_m;
+        x.e = 0;
+        x.s0 = mtile * BN;
+        x.cnt = static_cast<int>(a.M - x.s0 < BN ? a.M - x.s0 : int64_t(BN));
+        x.n0 = nt * kBW;
+    }
+    return x;
+}
+
+template <int BITS, int ST, int AT, int BN, int MODE>
+__global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                                const __grid_constant__ TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int S = a.stages;
+    const TcPlan plan = tc_plan(BN, S, BITS);
+    uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* full_w = full_a + kMaxStagesTC;
+    uint64_t* empty = full_a + 2 * kMaxStagesTC;
+    uint64_t* acc_full = full_a + 3 * kMaxStagesTC;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint8_t* act = smem + plan.bars;
+    uint8_t* wt = act + S * plan.act;
+    uint8_t* pack = wt + S * plan.w;
+    uint8_t* scl = pack + plan.pack;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (smem_u32(smem) & 1023) {  // the swizzled tiles need 1024-byte alignment
+        if (tid == 0) record_error(MNB_ERR_UNSUPPORTED);
+        return;
+    }
+    const int ksteps = a.k_steps;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_a[s], 1);
+            mbar_init(&full_w[s], kDequantWarps);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        fence_barrier_init();
+        if (MODE == kModeGemm) prefetch_tmap(&tmap_a);
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
+    grid_dependency_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int n_tiles = a.mtiles ? *a.n_mtiles * a.tiles_n : a.tiles_n * a.tiles_m;
+    bool failed = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------- activation producer
+        if (MODE == kModeGemm) {
+            if (lane == 0) {
+                RingPos rp;
+                for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
+                    const Tile x = tile_of(a, t, BN);
+                    for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
+                        if (rp.round && !mbar_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+                        mbar_arrive_expect_tx(&full_a[rp.stage], BN * 128);
+                        tma_load_2d(act + rp.stage * plan.act, &tmap_a, ks * kBK, x.s0, &full_a[rp.stage]);
+                    }
+                }
+            }
+        } else {
+            // FC1: gather the routed tokens' rows with cp.async; a stage is
+            // published (after a proxy fence) once its copies have landed,
+            // lagging the issue by up to S - 1 stages.  Lane l owns tile rows
+            // l, l+32, ...; their source rows are resolved once per tile.
+            constexpr int kRowsPerLane = BN >= 32 ? BN / 32 : 1;
+            const int lag = S - 1;
+            RingPos rp, pub;
+            int issued = 0, published = 0;
+            auto publish_one = [&]() {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_a[pub.stage]);
+                pub.next(S);
+                ++published;
+            };
+            for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
+                const Tile x = tile_of(a, t, BN);
+                const uint16_t* src[kRowsPerLane];
+                uint32_t rowoff[kRowsPerLane];
+                uint32_t rx[kRowsPerLane];
+#pragma unroll
+                for (int i = 0; i < kRowsPerLane; ++i) {
+                    const int j = lane + 32 * i;
+                    src[i] = (j < BN && j < x.cnt)
+                                 ? static_cast<const uint16_t*>(a.X) + int64_t(a.perm[x.s0 + j] / a.k) * a.K
+                                 : nullptr;
+                    rowoff[i] = static_cast<uint32_t>((j >> 3) * 1024 + (j & 7) * 128);
+                    rx[i] = static_cast<uint32_t>(j & 7);
+                }
+                for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
+                    if (rp.round && !warp_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+                    uint8_t* dst = act + rp.stage * plan.act;
+                    const int64_t k0 = int64_t(ks) * kBK;
+                    const int64_t rem8 = (a.K - k0) / 8;  // K % 8 == 0
+                    const int nch = rem8 < 8 ? static_cast<int>(rem8) : 8;
+#pragma unroll
+                    for (int i = 0; i < kRowsPerLane; ++i) {
+                        if (src[i] == nullptr) continue;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if (c < nch) cp_async16(dst + rowoff[i] + ((c ^ rx[i]) << 4), src[i] + k0 + 8 * c);
+                    }
+                    cp_async_commit();
+                    ++issued;
+                    if (issued - published > lag) {
+                        cp_async_wait<1>();  // all but the newest group have landed
+                        while (issued - published > 1) publish_one();
+                    }
+                }
+            }
+            cp_async_wait<0>();
+            while (published < issued) publish_one();
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kBW, BN, AT == kBF16);
+            RingPos rp;
+            int tl = 0;
+            for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
+                const int buf = tl & 1;
+                if (tl >= 2 && !mbar_wait(&acc_empty[buf], ((tl >> 1) - 1) & 1)) { failed = true; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * BN;
+                for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
+                    const uint32_t par = rp.round & 1;
+                    if (!mbar_wait(&full_a[rp.stage], par) || !mbar_wait(&full_w[rp.stage], par)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc_sw128(wt + rp.stage * plan.w);
+                    const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+                    tc_commit(&empty[rp.stage]);
+                }
+                if (failed) break;
+                tc_commit(&acc_full[buf]);
+            }
+        }
+    } else if (warp < kEpilogueWarp0) {
+        // ------------------------------------------------------------ dequant
+        const int dq = tid - kDequantWarp0 * 32;
+        const int r = dq & (kBW - 1);  // weight row of the tile
+        const int h = dq >> 7;         // which 32-code chunk of the K step
+        constexpr int kCB = BITS == 4 ? 16 : 12;  // packed bytes per 32-code chunk
+        constexpr int kStepBytes = 2 * kCB;       // packed bytes of a row per K step
+        constexpr int kZ = 1 << (BITS - 1);
+        const int nb = a.nb, bs_shift = __ffs(a.bs) - 1;
+        const int64_t kcodes = int64_t(nb) * a.bs;  // codes stored per row
+        const int64_t n_scales = a.rows * nb;
+        // K steps whose chunk h holds stored codes (later chunks read nothing)
+        const int64_t live64 = (kcodes - 32 * h + kBK - 1) / kBK;
+        const int live_steps = live64 > 0 ? static_cast<int>(live64) : 0;
+        // One tile's source stream for this thread: packed bytes of chunk h of
+        // its weight row, that expert's scales, and the row's first scale index.
+        struct RowStream {
+            const uint8_t* w;
+            const uint8_t* s;
+            int64_t si0;
+            bool ok;
+        };
+        auto stream_of = [&](const Tile& x) -> RowStream {
+            int64_t wr;
+            if (MODE == kModeFc1) {
+                const int64_t p = x.n0 / 2 + (r >> 1), up = r & 1;  // pair-interleaved tile rows
+                wr = p < a.I ? (a.inter ? 2 * p + up : up * a.I + p) : -1;
+            } else {
+                wr = x.n0 + r < a.rows ? x.n0 + r : -1;
+            }
+            RowStream st;
+            st.ok = wr >= 0;
+            st.w = a.B + x.e * a.w_expert_stride + (st.ok ? wr : 0) * a.row_bytes + h * kCB;
+            st.s = static_cast<const uint8_t*>(a.scales) + x.e * a.s_expert_stride;
+            st.si0 = (st.ok ? wr : 0) * nb;
+            return st;
+        };
+        // prefetch cursor: the (tile, K step) whose bytes go into the ring next
+        int pt = blockIdx.x, pks = 0, pslot = 0;
+        RowStream ps = pt < n_tiles ? stream_of(tile_of(a, pt, BN)) : RowStream{nullptr, nullptr, 0, false};
+        auto issue = [&]() {
+            if (pt < n_tiles && ps.ok && pks < live_steps) {
+                uint8_t* dst = pack + ((pslot * 2 + h) * kBW + r) * kCB;
+                const uint8_t* src = ps.w + int64_t(pks) * kStepBytes;
+                if constexpr (BITS == 4) {
+                    cp_async16(dst, src);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + 4 * q);
+                }
+                const int64_t si = ps.si0 + ((int64_t(pks) * kBK + 32 * h) >> bs_shift);
+                uint32_t* sdst = reinterpret_cast<uint32_t*>(scl + ((pslot * 2 + h) * kBW + r) * 4);
+                if (ST == kF32) {
+                    cp_async4(sdst, reinterpret_cast<const float*>(ps.s) + si);
+                } else if ((si | 1) < n_scales) {
+                    cp_async4(sdst, reinterpret_cast<const uint32_t*>(ps.s) + (si >> 1));
+                } else {  // the last half-precision scale: its 4-byte word would run past the array
+                    *sdst = reinterpret_cast<const uint16_t*>(ps.s)[si];
+                }
+            }
+            cp_async_commit();
+            if (++pslot == kPack) pslot = 0;
+            if (pt < n_tiles && ++pks == ksteps) {
+                pks = 0;
+                pt += gridDim.x;
+                if (pt < n_tiles) ps = stream_of(tile_of(a, pt, BN));
+            }
+        };
+        for (int i = 0; i < kPack - 1; ++i) issue();
+        RingPos rp;
+        int cslot = 0;
+        for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
+            const Tile x = tile_of(a, t, BN);
+            const RowStream cs = stream_of(x);
+            const uint8_t* zrow = nullptr;
+            if (a.zp && cs.ok) zrow = a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes;
+            for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
+                issue();
+                cp_async_wait<kPack - 1>();
+                if (rp.round && !warp_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+                const bool live = cs.ok && ks < live_steps;
+                uint32_t w[BITS];
+                float sc = 0.f, z = float(kZ);
+                if (live) {
+                    const uint8_t* src = pack + ((cslot * 2 + h) * kBW + r) * kCB;
+                    if constexpr (BITS == 4) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(src);
+                        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
+                    }
+                    const int b = (ks * kBK + 32 * h) >> bs_shift;
+                    sc = scale_from_word<ST>(*reinterpret_cast<const uint32_t*>(scl + ((cslot * 2 + h) * kBW + r) * 4),
+                                             cs.si0 + b);
+                    if (zrow) z = float(zero_point_code<BITS>(zrow, b));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < BITS; ++q) w[q] = 0;
+                }
+                if (++cslot == kPack) cslot = 0;
+                // w = s (q - z) = f * s 2^(24-p) - s (2^(23-p) + z), one fp32 rounding per value;
+                // the pre-scale depends only on the code's position class p
+                constexpr int kCls = BITS == 4 ? 2 : 3;
+                float mc[kCls], ac[kCls];
+#pragma unroll
+                for (int c = 0; c < kCls; ++c) {
+                    const int p = code_pos<BITS>(c);
+                    mc[c] = sc * float(1u << (24 - p));
+                    ac[c] = -sc * (float(1u << (23 - p)) + z);
+                }
+                uint32_t outw[16];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    float2 f01, f23;
+                    chunk_codes4<BITS>(w, g, f01, f23);
+                    const int j = 4 * g;
+                    const float2 v01 = ffma2(f01, make_float2(mc[j % kCls], mc[(j + 1) % kCls]),
+                                             make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
+                    const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
+                                             make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
+                    outw[2 * g] = pack2<AT>(v01.x, v01.y);
+                    outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
+                }
+                uint8_t* wdst = wt + rp.stage * plan.w;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(wdst + sw128(r, 4 * h + c)) =
+                        make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_w[rp.stage]);
+            }
+        }
+        cp_async_wait<0>();
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        int tl = 0;
+        for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            const Tile x = tile_of(a, t, BN);
+            if (!warp_wait(&acc_full[buf], (tl >> 1) & 1)) { failed = true; break; }
+            tc_fence_after();
+            const int rr = quarter * 32 + lane;  // tile row of this thread
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + buf * BN + c0, v);
+                tmem_ld_wait();
+                if constexpr (MODE == kModeFc1) {
+                    // rows 2p / 2p+1 hold gate / up of pair p: the even lane combines them
+                    const int64_t p = x.n0 / 2 + (rr >> 1);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float mine = __uint_as_float(v[j]);
+                        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                        if (!(lane & 1) && c0 + j < BN && c0 + j < x.cnt && p < a.I) {
+                            const float hv = mine / (1.0f + expf(-mine)) * other;
+                            store_from_f32(a.Y, a.y_dtype, (int64_t(x.s0) + c0 + j) * a.ld_y + p, hv);
+                        }
+                    }
+                } else {
+                    const int64_t n = x.n0 + rr;
+                    if (n < a.rows) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            // a 16-column tile loads 32 columns: the upper 16 belong to the other accumulator
+                            if (c0 + j < BN && c0 + j < x.cnt)
+                                store_from_f32(a.Y, a.y_dtype, (int64_t(x.s0) + c0 + j) * a.ld_y + n,
+                                               __uint_as_float(v[j]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+    }
+    if (failed) record_error(MNB_ERR_TIMEOUT);
+    grid_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int stages_for(int BN, int bits) {
+    int stages = 6;
+    while (stages > 2 && tc_plan(BN, stages, bits).total > 227 * 1024) --stages;
+    return stages;
+}
+
+template <int BITS, int ST, int AT, int BN, int MODE>
+cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
+                       bool pdl, cudaStream_t stream) {
+    TcArgs a = in;
+    CUtensorMap tmap;
+    std::memset(&tmap, 0, sizeof tmap);
+    if (MODE == kModeGemm) {
+        auto encode = encode_fn();
+        if (!encode) return cudaErrorNotSupported;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a_cols), static_cast<cuuint64_t>(a_rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a_cols * 2)};
+        const cuuint32_t box[2] = {kBK, BN};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult cr = encode(&tmap, AT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                   2, const_cast<void*>(A_rows), dims, strides, box, estr,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    uint32_t cols = 32;
+    while (cols < 2u * BN) cols <<= 1;
+    a.tmem_cols = cols;
+    a.stages = stages_for(BN, BITS);
+    const int64_t smem = tc_plan(BN, a.stages, BITS).total;
+    auto kern = gemm_tc_kernel<BITS, ST, AT, BN, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(grid, 1)), 1, 1);
+    cfg.blockDim = dim3(kThreadsTC, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+}
+
+// Activation rows per tile: fewest waves of persistent CTAs, weighing the
+// lower per-FLOP efficiency of narrow tiles.
+int pick_bn(int64_t M, int64_t N, int sm_count) {
+    int best = 256;
+    double best_cost = 1e300;
+    for (int bn : {256, 128, 64, 32, 16}) {
+        if (bn > 16 && bn / 2 >= M) continue;  // a narrower tile covers M already
+        const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, bn);
+        const double waves = double(cdiv<int64_t>(tiles, sm_count));
+        const double eff = bn >= 256 ? 1.0 : bn >= 128 ? 0.9 : bn >= 64 ? 0.7 : 0.5;
+        const double cost = waves * bn / eff;
+        if (cost < best_cost) { best_cost = cost; best = bn; }
+    }
+    return best;
+}
+
+template <int MODE, int BITS, int ST, int AT>
+cudaError_t launch_bn(int BN, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
+                      bool pdl, cudaStream_t stream) {
+    switch (BN) {
+        case 256: return launch_cfg<BITS, ST, AT, 256, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        case 128: return launch_cfg<BITS, ST, AT, 128, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        case 64: return launch_cfg<BITS, ST, AT, 64, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        case 32: return launch_cfg<BITS, ST, AT, 32, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        default: return launch_cfg<BITS, ST, AT, 16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+    }
+}
+
+}  // namespace
+
+// One (mode, bit width) slice of the instantiations; each slice lives in its own
+// translation unit so the slices compile in parallel.
+#define MNB_GEMM_TC_SLICE(NAME, MODE, BITS)                                                                   \
+    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, const TcArgs& a, const void* A_rows, int64_t a_rows, \
+                     int64_t a_cols, int grid, bool pdl, cudaStream_t stream) {                               \
+        const bool sf = scale_dtype == kF32;                                                                   \
+        if (a_dtype == kBF16)                                                                                  \
+            return sf ? launch_bn<MODE, BITS, kF32, kBF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream)   \
+                      : launch_bn<MODE, BITS, kBF16, kBF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream); \
+        return sf ? launch_bn<MODE, BITS, kF32, kF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream)        \
+                  : launch_bn<MODE, BITS, kF16, kF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream);       \
+    }                                                                                                          \
+    cudaError_t NAME##_take_error(unsigned int* out) { return take_unit_error(out); }
+
+}  // namespace mnb

@@ -238,7 +238,7 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         while (st > 2 && ctas(st) < 3 && ctas(st - 1) > ctas(st)) --st;
         const int64_t resident = std::min<int64_t>(3, ctas(st));
         const bool enough_blocks = cdiv<int64_t>(N, RC) >= int64_t(sm_count) * 3 / 2;
-        const int64_t score = (enough_blocks ? 100 : 0) + 10 * resident + R;
+        const int64_t score = (enough_blocks ? 100 : 0) + 10 * R + resident;
         if (score > best_score) {
             best_score = score;
             best.R = R;

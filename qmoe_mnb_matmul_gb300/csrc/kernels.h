@@ -57,6 +57,40 @@ struct GemmTcArgs {
 };
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream);
 
+// Kernel-side arguments of the tensor-core GEMM, shared with the grouped QMoE
+// launches.  Weight matrix of an expert: `rows` rows of K codes.
+struct TcArgs {
+    int64_t M, K, rows;
+    const uint8_t* B;
+    const void* scales;
+    const uint8_t* zp;
+    int64_t row_bytes;
+    int nb, bs, zp_row_bytes;
+    int64_t w_expert_stride, s_expert_stride, z_expert_stride;  // bytes between experts
+    void* Y;
+    int y_dtype;
+    int64_t ld_y;          // row stride of the output in elements
+    int tiles_n, tiles_m, k_steps, stages;
+    uint32_t tmem_cols;
+    // grouped (QMoE) launches: activation-row tiles {expert, first sorted row, rows, 0}
+    const int4* mtiles;
+    const int* n_mtiles;
+    const int* perm;       // FC1: sorted position -> flat (token, slot) index
+    int k;
+    int64_t I;
+    int inter;             // FC1 rows interleaved gate/up
+    const void* X;         // FC1: activations gathered by token
+};
+
+// Rows of activations per tile in the grouped launches.
+int grouped_tile_rows();
+
+// Grouped per-expert tensor-core GEMM over the m-tiles in the workspace:
+// fc1 gathers X rows by token and writes silu(gate)*up; otherwise a dense
+// tile GEMM on A_rows [a_rows, a_cols] (TMA).
+cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
+                              int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream);
+
 // --------------------------------------------------------------- unpack
 cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
                                 uint8_t* codes, cudaStream_t stream);

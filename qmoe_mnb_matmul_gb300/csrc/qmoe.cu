@@ -44,11 +44,18 @@ constexpr int kRowsPerBlock2 = 16;  // FC2 rows per CTA
 __host__ __device__ inline int64_t a256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct Ws {
-    int64_t idx, wts, counts, offsets, perm, inv, tiles, ntiles, h, o, total;
+    int64_t idx, wts, counts, offsets, perm, inv, tiles, ntiles, mtiles, nmtiles, h, o, total;
 };
 
 __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
     const int64_t t = (P + kTileM - 1) / kTileM + E;
+    return P < t ? P : t;
+}
+
+// m-tiles of the tensor-core plan: <= kTcTileM sorted pairs of one expert.
+constexpr int kTcTileM = 128;
+__host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
+    const int64_t t = (P + kTcTileM - 1) / kTcTileM + E;
     return P < t ? P : t;
 }
 
@@ -64,6 +71,8 @@ __host__ __device__ inline Ws ws_layout(int64_t T, int64_t H, int64_t I, int64_t
     w.inv = off; off += a256(P * 4);
     w.tiles = off; off += a256(max_tiles(P, E) * 8);
     w.ntiles = off; off += 256;
+    w.mtiles = off; off += a256(max_mtiles(P, E) * 16);
+    w.nmtiles = off; off += 256;
     w.h = off; off += a256(P * I * 4);
     w.o = off; off += a256(P * H * 4);
     w.total = off;
@@ -71,6 +80,9 @@ __host__ __device__ inline Ws ws_layout(int64_t T, int64_t H, int64_t I, int64_t
 }
 
 bool use_decode(const QmoeArgs& q) { return q.T <= kDecodeMaxT && q.k <= kDecodeMaxK; }
+
+// Tensor-core plan: gathered activation rows are read with 16-byte copies.
+bool use_tc(const QmoeArgs& q) { return q.x_vec != 0; }
 
 // --------------------------------------------------------- shared memory
 
@@ -506,6 +518,51 @@ __global__ void combine_kernel(const __grid_constant__ QmoeArgs q) {
     }
 }
 
+// m-tiles for the tensor-core plan: {expert, first sorted position, pairs, 0}.
+__global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64_t H, int64_t I, int64_t E, int k) {
+    const Ws L = ws_layout(T, H, I, E, k);
+    const int* counts = reinterpret_cast<const int*>(ws + L.counts);
+    const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+    int4* tiles = reinterpret_cast<int4*>(ws + L.mtiles);
+    __shared__ int scan[1024];
+    grid_dependency_wait();
+    const int e = threadIdx.x;
+    const int cnt = e < E ? counts[e] : 0;
+    const int n = (cnt + kTcTileM - 1) / kTcTileM;
+    scan[e] = n;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int v = e >= o ? scan[e - o] : 0;
+        __syncthreads();
+        scan[e] += v;
+        __syncthreads();
+    }
+    const int first = scan[e] - n;
+    for (int i = 0; i < n; ++i)
+        tiles[first + i] = make_int4(e, offsets[e] + i * kTcTileM, min(kTcTileM, cnt - i * kTcTileM), 0);
+    if (e == 1023) *reinterpret_cast<int*>(ws + L.nmtiles) = scan[1023];
+    grid_launch_dependents();
+}
+
+// Y[t, n] = sum_j w[t, j] * o[position of (t, j), n], ascending j, fp32 -> act
+// dtype, from FC2 outputs kept in the activation dtype (tensor-core plan).
+template <typename AT>
+__global__ void combine_sorted_kernel(const __grid_constant__ QmoeArgs q) {
+    const char* ws = static_cast<const char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const AT* o = reinterpret_cast<const AT*>(ws + L.o);
+    const float* wts = reinterpret_cast<const float*>(ws + L.wts);
+    const int* inv = reinterpret_cast<const int*>(ws + L.inv);
+    grid_dependency_wait();
+    const int64_t total = q.T * q.H;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t t = i / q.H, n = i - t * q.H;
+        float acc = 0.f;
+        for (int j = 0; j < q.k; ++j) acc = fmaf(wts[t * q.k + j], to_f32(o[int64_t(inv[t * q.k + j]) * q.H + n]), acc);
+        store_from_f32(q.Y, q.act_dtype, i, acc);
+    }
+}
+
 // ------------------------------------------------------------ launching
 
 template <typename Kern>
@@ -535,7 +592,7 @@ cudaError_t launch_fc1(const QmoeArgs& q, unsigned gx, cudaStream_t stream, bool
 }
 
 template <int B1, int B2, int ST>
-cudaError_t run_typed(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
+cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream) {
     char* ws = static_cast<char*>(q.workspace);
     const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
     const int64_t P = q.T * q.k;
@@ -555,6 +612,61 @@ cudaError_t run_typed(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
                             reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
                             reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
         return e;
+    if (use_tc(q)) {
+        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        TcArgs a = {};
+        a.mtiles = reinterpret_cast<const int4*>(ws + L.mtiles);
+        a.n_mtiles = reinterpret_cast<const int*>(ws + L.nmtiles);
+        a.bs = q.bs;
+        a.y_dtype = q.act_dtype;
+        // FC1: K = H, 2I rows (pair-interleaved in the tile), SwiGLU into h (act dtype, sorted order)
+        a.M = P;
+        a.K = q.H;
+        a.rows = 2 * q.I;
+        a.B = q.fc1_w;
+        a.scales = q.fc1_s;
+        a.zp = q.fc1_zp;
+        a.row_bytes = q.fc1.row_bytes;
+        a.nb = static_cast<int>(q.fc1.nb);
+        a.zp_row_bytes = static_cast<int>(q.fc1.zp_row);
+        a.w_expert_stride = 2 * q.I * q.fc1.row_bytes;
+        a.s_expert_stride = 2 * q.I * q.fc1.nb * 2;
+        a.z_expert_stride = 2 * q.I * q.fc1.zp_row;
+        a.Y = ws + L.h;
+        a.ld_y = q.I;
+        a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * q.I, 128));
+        a.k_steps = static_cast<int>(cdiv<int64_t>(q.H, 64));
+        a.perm = reinterpret_cast<const int*>(ws + L.perm);
+        a.k = q.k;
+        a.I = q.I;
+        a.inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
+        a.X = q.X;
+        if ((e = launch_grouped_tc(true, a, B1, ST, ST, nullptr, 0, 0, sm_count, pdl, stream)) != cudaSuccess)
+            return e;
+        // FC2: K = I, H rows; activations are h rows in sorted order (TMA), output o (act dtype, sorted order)
+        a.K = q.I;
+        a.rows = q.H;
+        a.B = q.fc2_w;
+        a.scales = q.fc2_s;
+        a.zp = q.fc2_zp;
+        a.row_bytes = q.fc2.row_bytes;
+        a.nb = static_cast<int>(q.fc2.nb);
+        a.zp_row_bytes = static_cast<int>(q.fc2.zp_row);
+        a.w_expert_stride = q.H * q.fc2.row_bytes;
+        a.s_expert_stride = q.H * q.fc2.nb * 2;
+        a.z_expert_stride = q.H * q.fc2.zp_row;
+        a.Y = ws + L.o;
+        a.ld_y = q.H;
+        a.tiles_n = static_cast<int>(cdiv<int64_t>(q.H, 128));
+        a.k_steps = static_cast<int>(cdiv<int64_t>(q.I, 64));
+        if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, sm_count, pdl, stream)) != cudaSuccess)
+            return e;
+        const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), int64_t(sm_count) * 16);
+        using AT = typename DType<ST>::T;
+        combine_sorted_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
+        return cudaGetLastError();
+    }
     tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
@@ -567,11 +679,11 @@ cudaError_t run_typed(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
 }
 
 template <int ST>
-cudaError_t run_bits(const QmoeArgs& q, bool pdl, cudaStream_t stream) {
-    if (q.fc1_bits == 3 && q.fc2_bits == 3) return run_typed<3, 3, ST>(q, pdl, stream);
-    if (q.fc1_bits == 3 && q.fc2_bits == 4) return run_typed<3, 4, ST>(q, pdl, stream);
-    if (q.fc1_bits == 4 && q.fc2_bits == 3) return run_typed<4, 3, ST>(q, pdl, stream);
-    return run_typed<4, 4, ST>(q, pdl, stream);
+cudaError_t run_bits(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream) {
+    if (q.fc1_bits == 3 && q.fc2_bits == 3) return run_typed<3, 3, ST>(q, sm_count, pdl, stream);
+    if (q.fc1_bits == 3 && q.fc2_bits == 4) return run_typed<3, 4, ST>(q, sm_count, pdl, stream);
+    if (q.fc1_bits == 4 && q.fc2_bits == 3) return run_typed<4, 3, ST>(q, sm_count, pdl, stream);
+    return run_typed<4, 4, ST>(q, sm_count, pdl, stream);
 }
 
 }  // namespace
@@ -587,8 +699,7 @@ bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
 cudaError_t qmoe_take_error(unsigned int* out) { return take_unit_error(out); }
 
 cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream) {
-    (void)sm_count;
-    return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, pdl, stream) : run_bits<kBF16>(q, pdl, stream);
+    return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, sm_count, pdl, stream) : run_bits<kBF16>(q, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

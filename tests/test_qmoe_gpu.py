@@ -1,5 +1,6 @@
 """GPU parity of qmoe_forward (routing, FC1 + SwiGLU, FC2, combine) against the
-oracle, through the C ABI.  Outputs are fp16 / bf16: |y - r| <= 1e-2 + 2e-2 |r|."""
+oracle, through the C ABI.  Outputs are fp16 / bf16:
+|y - r| <= 1e-2 + 2e-2 max(|r|, rms(r)) (tests/_util.py)."""
 import os
 import zlib
 
@@ -102,3 +103,17 @@ def test_prefill_shapes_sampled_tokens(T):
     y = run_qmoe(d, T, H, I, E, k, 3, 3, 64, "f16")
     toks = sorted(set([0, 1, T - 1, 10, 20] + list(wl.rng(T).integers(0, T, 11))))
     assert_half_close(y[toks], reference(d, k, 3, 3, I, 64, "f16", tokens=toks))
+
+
+@pytest.mark.parametrize("T,bits,bs,act,zp", [(2048, (3, 3), 64, "f16", False), (4096, (4, 4), 32, "bf16", True),
+                                              (4096, (3, 4), 128, "f16", True), (2048, (4, 3), 64, "bf16", False)])
+def test_prefill_sweep_full_size_sampled_tokens(T, bits, bs, act, zp):
+    """Full-size prefill sweep points (Qwen3-30B-A3B layer, 10% of tokens skewed onto
+    experts 0-7): every output of a sample of tokens against the oracle."""
+    b1, b2 = bits
+    H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
+    d = wl.moe_layer(wl.rng(seed("sweep", T, bits, bs, act, zp)), T, H, I, E, b1, b2, bs, act, with_zp=zp,
+                     skew=True)
+    y = run_qmoe(d, T, H, I, E, k, b1, b2, bs, act)
+    toks = sorted(set([0, 10, T - 1] + list(wl.rng(T + 1).integers(0, T, 7))))
+    assert_half_close(y[toks], reference(d, k, b1, b2, I, bs, act, tokens=toks))
