@@ -14,6 +14,16 @@
  * enqueue asynchronous work on it and return without synchronising, except
  * mnb_get_last_device_error(), which synchronises `stream`.
  *
+ * Overlapped launches.  Kernels are launched as programmatic dependents of the
+ * kernel ahead of them on the stream, so a call's prologue may run while the
+ * previous library call is still finishing: every call may warm L2 with its
+ * packed weights, and the QMoE decode path routes its tokens and copies the
+ * selected experts' FC2 rows.  Activations and workspace are read only after
+ * the previous call has completed.  Hence packed weights, scales, zero points
+ * and router logits must not be outputs of the immediately preceding library
+ * call on the same stream (outputs of any other kernel are fine).  Setting
+ * the environment variable MNB_DISABLE_PDL turns the overlap off.
+ *
  * Layouts (all dense, row-major, C order):
  *   bs = block_size, nb = ceil(K / bs), blob = bs * bits / 8 bytes.
  *   B_packed     uint8 [N, nb, blob].  Row n is one stream of K codes of width

@@ -170,6 +170,12 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Allow the next kernel in the stream to start its prologue.
+//
+// Every kernel of this library calls this only after its own
+// grid_dependency_wait (or not at all).  That is what lets a prologue read,
+// before its wait, inputs that the library never writes (packed weights,
+// scales, and router logits in the QMoE FC2 decode prologue): when a launch
+// starts early, everything ahead of the kernel that released it has completed.
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // ------------------------------------------------------------- misc

@@ -55,6 +55,11 @@ __host__ __device__ inline Plan make_plan(int MT, int C, int RC, int64_t row_byt
     return p;
 }
 
+// dst[i] = src[i] for i in [from, to): the sub-16-byte tail of a block, out of line.
+static __device__ __noinline__ void copy_bytes(uint8_t* dst, const uint8_t* src, int64_t from, int64_t to) {
+    for (int64_t i = from; i < to; ++i) dst[i] = src[i];
+}
+
 // Named barrier over the consumer warps only.
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -119,8 +124,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             const uint8_t* wsrc = a.B + n0 * a.row_bytes;
             const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
             // bytes past the last 16-byte multiple of a partial block: plain copies, published by the arrive below
-            for (int64_t i = wb; i < wtot; ++i) W[i] = wsrc[i];
-            for (int64_t i = sb; i < stot; ++i) Sd[i] = ssrc[i];
+            if (wb < wtot) copy_bytes(W, wsrc, wb, wtot);
+            if (sb < stot) copy_bytes(Sd, ssrc, sb, stot);
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&full[st], wb + sb);
             if (wb) bulk_g2s(W, wsrc, wb, &full[st]);
@@ -177,10 +182,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                     sc[r] = to_f32(srow[r][b]);
                     dz[r] = a.zp ? float(kZImplicit - zero_point_code<BITS>(zrow[r], b)) : 0.f;
                 }
-                if (a.zp)
-                    chunk_accumulate<BITS, R, MT, true>(w, sc, dz, A4, Corr, C, c, acc);
-                else
-                    chunk_accumulate<BITS, R, MT, false>(w, sc, dz, A4, Corr, C, c, acc);
+                chunk_accumulate<BITS, R, MT>(w, sc, dz, A4, Corr, C, c, acc);
             }
             float out[R][MT];
 #pragma unroll

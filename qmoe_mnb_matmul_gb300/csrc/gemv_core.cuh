@@ -110,11 +110,20 @@ __device__ __forceinline__ int zero_point_code(const uint8_t* zrow, int b) {
 // j, Asum over even j, Asum over odd j}, with Csum = sum A'_j / 2, Asum =
 // sum A_j and z0 = 2^(BITS-1) the implicit zero point, summed in ascending j.
 // (The f32x2 products keep even codes in .x and odd codes in .y.)
-// row(m) returns activation row m (dtype `dt`, K valid entries) or nullptr
-// for a row of zeros.
-template <int BITS, int MT, typename RowFn>
-__device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, int64_t K, int dt, bool vec, RowFn row,
+// row(m) returns activation row m (dtype `dt_arg`, or FIXED_DT when that is
+// given at compile time; K valid entries) or nullptr for a row of zeros.
+// 32 activations starting at k0 one by one (zeros past K or for a null row):
+// the path for unaligned rows and a ragged last chunk, kept out of line so the
+// vector path stays compact in the instruction cache.
+static __device__ __noinline__ void load_chunk_slow(const void* src, int dt, int64_t k0, int64_t K, float* v) {
+#pragma unroll 1
+    for (int j = 0; j < 32; ++j) v[j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
+}
+
+template <int BITS, int MT, int FIXED_DT = -1, typename RowFn>
+__device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, int64_t K, int dt_arg, bool vec, RowFn row,
                                              int tid, int nthreads) {
+    const int dt = FIXED_DT >= 0 ? FIXED_DT : dt_arg;  // a compile-time dtype drops the other paths
     constexpr float z0 = float(1 << (BITS - 1));
     for (int i = tid; i < MT * C; i += nthreads) {
         const int m = i / C, c = i - m * C;
@@ -148,8 +157,10 @@ __device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, in
                 }
             }
         } else {
+            float t[32];
+            load_chunk_slow(src, dt, k0, K, t);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
+            for (int j = 0; j < 32; ++j) v[j] = t[j];
         }
         float as[2] = {0.f, 0.f}, cs[2] = {0.f, 0.f};
 #pragma unroll
@@ -167,9 +178,10 @@ __device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, in
 
 // One lane, chunk c of R packed rows:
 //   out[r][m] += scale[r] * sum_k A[m, k] (q[r, k] - z[r])      (as an even/odd pair)
-// dz[r] = z0 - z[r] is the row's zero-point shift from the implicit one (used
-// only when HAS_ZP).
-template <int BITS, int R, int MT, bool HAS_ZP>
+// dz[r] = z0 - z[r] is the row's zero-point shift from the implicit one (0
+// without zero points: one code path serves both, which keeps the kernels
+// small).
+template <int BITS, int R, int MT>
 __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], const float (&sc)[R], const float (&dz)[R],
                                                  const float4* __restrict__ A4, const float4* __restrict__ Corr, int C,
                                                  int c, float2 (&out)[R][MT]) {
@@ -200,7 +212,7 @@ __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], c
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float2 t = __fadd2_rn(P[r][m], make_float2(cr.x, cr.y));
-            if constexpr (HAS_ZP) t = ffma2(make_float2(dz[r], dz[r]), make_float2(cr.z, cr.w), t);
+            t = ffma2(make_float2(dz[r], dz[r]), make_float2(cr.z, cr.w), t);
             out[r][m] = ffma2(make_float2(sc[r], sc[r]), t, out[r][m]);
         }
     }

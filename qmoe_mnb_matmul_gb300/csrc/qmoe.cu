@@ -39,7 +39,8 @@ constexpr int kTileM = 4;       // pairs per tile in the tiled plan
 constexpr int kDecodeMaxT = 8;
 constexpr int kDecodeMaxK = 8;
 constexpr int kPairsPerBlock = 16;  // FC1 gate/up pairs per CTA (32 rows)
-constexpr int kRowsPerBlock2 = 16;  // FC2 rows per CTA
+constexpr int kRowsPerBlock2 = 16;  // FC2 rows per CTA (tiled plan)
+constexpr int kDecodeRows2 = 8;     // FC2 rows per CTA (decode plan)
 
 __host__ __device__ inline int64_t a256(int64_t x) { return (x + 255) / 256 * 256; }
 
@@ -87,7 +88,7 @@ bool use_tc(const QmoeArgs& q) { return q.x_vec != 0; }
 // --------------------------------------------------------- shared memory
 
 struct Fc1Plan {
-    int64_t a4, asum, w, s, total;
+    int64_t a4, asum, w, s, lg, total;
 };
 __host__ __device__ inline Fc1Plan fc1_plan(int MT, int C, int64_t row_bytes, int nb, int ssize) {
     Fc1Plan p;
@@ -95,24 +96,48 @@ __host__ __device__ inline Fc1Plan fc1_plan(int MT, int C, int64_t row_bytes, in
     p.asum = round_up(int64_t(MT) * C * 16, 128);  // float4 corrections
     p.w = round_up(int64_t(2 * kPairsPerBlock) * row_bytes, 128);
     p.s = round_up(int64_t(2 * kPairsPerBlock) * nb * ssize, 128);
-    p.total = 256 + p.a4 + p.asum + p.w + p.s;
+    p.lg = round_up(int64_t(kBlockRouteMaxE) * 4, 128);  // router logits (decode)
+    p.total = 256 + p.a4 + p.asum + p.w + p.s + p.lg;
     return p;
 }
 
+// FC2 plan for `rows` output rows per CTA and ACT activation rows; the decode
+// kernel adds one fp32 partial per (slot, row) and the router logits.
 struct Fc2Plan {
-    int64_t a4, asum, w, s, total;
+    int64_t a4, asum, w, s, part, lg, total;
 };
-__host__ __device__ inline Fc2Plan fc2_plan(int ACT, int C, int64_t row_bytes, int nb, int ssize) {
+__host__ __device__ inline Fc2Plan fc2_plan(int rows, int ACT, int C, int64_t row_bytes, int nb, int ssize,
+                                            bool decode) {
     Fc2Plan p;
     p.a4 = int64_t(ACT) * 8 * C * 16;
     p.asum = round_up(int64_t(ACT) * C * 16, 128);  // float4 corrections
-    p.w = round_up(int64_t(kRowsPerBlock2) * row_bytes, 128);  // per expert slot
-    p.s = round_up(int64_t(kRowsPerBlock2) * nb * ssize, 128);
-    p.total = 256 + p.a4 + p.asum + int64_t(ACT) * (p.w + p.s);
+    p.w = round_up(int64_t(rows) * row_bytes, 128);  // per expert slot
+    p.s = round_up(int64_t(rows) * nb * ssize, 128);
+    p.part = decode ? round_up(int64_t(ACT) * rows * 4, 128) : 0;
+    p.lg = decode ? round_up(int64_t(kBlockRouteMaxE) * 4, 128) : 0;
+    p.total = 256 + p.a4 + p.asum + int64_t(ACT) * (p.w + p.s) + p.part + p.lg;
     return p;
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// One warp routes a token with more than kBlockRouteMaxE experts (rare; out of line).
+static __device__ __noinline__ void route_wide(const float* row, int E, int k, int normalize, int* s_idx, float* s_w) {
+    warp_route_pl<kMaxExpertsPerLane>(row, E, k, normalize, s_idx, s_w, 1);
+}
+
+// Decode kernels route their own token: the whole CTA ranks up to
+// kBlockRouteMaxE logits at once, larger routers fall back to one warp.
+// Ends with a block barrier; s_logit holds kBlockRouteMaxE floats.
+__device__ __forceinline__ void route_token(const QmoeArgs& q, int64_t t, int* s_idx, float* s_w, float* s_logit) {
+    const float* row = q.logits + t * q.E;
+    if (q.E <= kBlockRouteMaxE && q.E <= kThreads) {
+        block_route(row, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, s_logit);
+    } else {
+        if (threadIdx.x < 32) route_wide(row, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w);
+        __syncthreads();
+    }
+}
 
 // ------------------------------------------------------------------ FC1
 
@@ -144,11 +169,13 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
     const int64_t P = q.T * q.k;
 
     grid_dependency_wait();
+    // Dependents may start now: the FC2 decode prologue reads the router
+    // logits, which were complete before this kernel's wait returned.
+    grid_launch_dependents();
     if (DECODE) {
         const int64_t p = blockIdx.x;
         const int64_t t = p / q.k;
-        if (warp == 0) warp_route(q.logits + t * q.E, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, 1);
-        __syncthreads();
+        route_token(q, t, s_idx, s_w, reinterpret_cast<float*>(Wst + plan.w + plan.s));
         if (tid == 0) {
             s_int[0] = s_idx[p % q.k];
             s_int[1] = static_cast<int>(p);
@@ -197,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             bulk_g2s(Sdst + kPairsPerBlock * nb * sizeof(S), S1 + (I + pair0) * nb, pc * srow, bar);
         }
     }
-    stage_chunks<BITS, MT>(
+    stage_chunks<BITS, MT, ST>(
         A4, Corr, C, q.H, q.act_dtype, q.x_vec != 0,
         [&](int m) -> const void* {
             const int t = m < cnt ? s_int[4 + m] : -1;
@@ -205,7 +232,6 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
         },
         tid, kThreads);
     __syncthreads();
-    grid_launch_dependents();
     const bool ok = mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
         mbar_wait(bar, 0);
@@ -241,10 +267,7 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
                 sc[r] = to_f32(Sst[lrow[r] * nb + b]);
                 zz[r] = Z1 ? float(kZImplicit - zero_point_code<BITS>(Z1 + grow[r] * q.fc1.zp_row, b)) : 0.f;
             }
-            if (Z1)
-                chunk_accumulate<BITS, R, MT, true>(w, sc, zz, A4, Corr, C, c, out2);
-            else
-                chunk_accumulate<BITS, R, MT, false>(w, sc, zz, A4, Corr, C, c, out2);
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Corr, C, c, out2);
         }
         float out[R][MT];
 #pragma unroll
@@ -267,9 +290,10 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
 
 // ------------------------------------------------------- FC2 (decode)
 
-// FC2 + combine for token t = blockIdx.x over rows [n0, n0 + 16) of H: the
-// block's rows of all k selected experts are streamed, each multiplied with
-// that slot's h, and combined with the routing weights in slot order.
+// FC2 + combine for token t = blockIdx.x over rows [n0, n0 + kDecodeRows2) of
+// H: the block's rows of all k selected experts are staged, every warp takes
+// (slot, row group) tasks, and the k per-slot results of a row are combined
+// with the routing weights in slot order.
 template <int BITS, int ST>
 __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_constant__ QmoeArgs q) {
     using S = typename DType<ST>::T;
@@ -279,37 +303,35 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
     const int C = static_cast<int>(q.fc2.nb * q.bs / 32);
     const int nb = static_cast<int>(q.fc2.nb);
     const int64_t rb = q.fc2.row_bytes;
-    const Fc2Plan plan = fc2_plan(kDecodeMaxK, C, rb, nb, sizeof(S));
+    const Fc2Plan plan = fc2_plan(kDecodeRows2, kDecodeMaxK, C, rb, nb, sizeof(S), true);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     float* s_w = reinterpret_cast<float*>(smem + 128);
     int* s_idx = reinterpret_cast<int*>(smem + 192);
     float4* A4 = reinterpret_cast<float4*>(smem + 256);
     float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
     uint8_t* Wst = smem + 256 + plan.a4 + plan.asum;
-    uint8_t* Sst = Wst + int64_t(k) * plan.w;
+    uint8_t* Sst = Wst + int64_t(kDecodeMaxK) * plan.w;
+    float* part = reinterpret_cast<float*>(Sst + int64_t(kDecodeMaxK) * plan.s);  // [slot][row]
+    float* s_logit = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part) + plan.part);
 
     const int64_t t = blockIdx.x;
     const int64_t H = q.H, I = q.I;
-    const int64_t n0 = int64_t(blockIdx.y) * kRowsPerBlock2;
-    const int rc = static_cast<int>(std::min<int64_t>(kRowsPerBlock2, H - n0));
+    const int64_t n0 = int64_t(blockIdx.y) * kDecodeRows2;
+    const int rc = static_cast<int>(std::min<int64_t>(kDecodeRows2, H - n0));
     const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
     const float* h = reinterpret_cast<const float*>(static_cast<const char*>(q.workspace) + L.h);
 
     // Prologue, overlapping the FC1 kernel: the router logits were complete
-    // before FC1 started, so this CTA may route its token and warm L2 with the
-    // selected experts' rows before waiting for h.
-    if (warp == 0) warp_route(q.logits + t * q.E, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, 1);
+    // before FC1 released this launch (FC1 releases it after its own wait),
+    // and the expert weights are inputs that no kernel of this library
+    // writes, so this CTA routes its token and starts copying the selected
+    // experts' rows before waiting for h.
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
     }
-    __syncthreads();
+    route_token(q, t, s_idx, s_w, s_logit);
     const uint32_t wbytes = static_cast<uint32_t>(rc * rb), sbytes = static_cast<uint32_t>(rc * nb * sizeof(S));
-    if (tid < k) {
-        const int e = s_idx[tid];
-        bulk_prefetch_l2(q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes);
-    }
-    grid_dependency_wait();
     if (tid == 0) {
         mbar_arrive_expect_tx(bar, k * (wbytes + sbytes));
         for (int j = 0; j < k; ++j) {
@@ -318,12 +340,13 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
             bulk_g2s(Sst + j * plan.s, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
         }
     }
-    stage_chunks<BITS, kDecodeMaxK>(
+    grid_dependency_wait();
+    grid_launch_dependents();
+    stage_chunks<BITS, kDecodeMaxK, kF32>(
         A4, Corr, C, I, kF32, true,
         [&](int j) -> const void* { return j < k ? static_cast<const void*>(h + (t * k + j) * I) : nullptr; }, tid,
         kThreads);
     __syncthreads();
-    grid_launch_dependents();
     const bool ok = mbar_wait(bar, 0);
     if (__syncthreads_or(!ok)) {
         mbar_wait(bar, 0);
@@ -332,45 +355,40 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
     const int bs_shift = __ffs(q.bs) - 1;
     constexpr int kZImplicit = 1 << (BITS - 1);
 
-    for (int g = warp; g * R < rc; g += kWarps) {
-        float acc[R] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int e = s_idx[j];
-            const uint8_t* W = Wst + j * plan.w;
-            const S* Sc = reinterpret_cast<const S*>(Sst + j * plan.s);
-            const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
-            float2 out[R][1];
+    const int groups = (rc + R - 1) / R;
+    for (int task = warp; task < k * groups; task += kWarps) {
+        const int j = task / groups, g = task - j * groups;
+        const int e = s_idx[j];
+        const uint8_t* W = Wst + j * plan.w;
+        const S* Sc = reinterpret_cast<const S*>(Sst + j * plan.s);
+        const uint8_t* Z2 = q.fc2_zp ? q.fc2_zp + int64_t(e) * H * q.fc2.zp_row : nullptr;
+        float2 out[R][1];
 #pragma unroll
-            for (int r = 0; r < R; ++r) out[r][0] = make_float2(0.f, 0.f);
-            for (int c = lane; c < C; c += 32) {
-                const int b = (c * 32) >> bs_shift;
-                uint32_t w[R][BITS];
-                float sc[R], zz[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int rl = min(g * R + r, rc - 1);
-                    load_chunk<BITS>(W + int64_t(rl) * rb, c, w[r]);
-                    sc[r] = to_f32(Sc[rl * nb + b]);
-                    zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
-                }
-                if (Z2)
-                    chunk_accumulate<BITS, R, 1, true>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
-                else
-                    chunk_accumulate<BITS, R, 1, false>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
-            }
-            const float wj = s_w[j];
-#pragma unroll
-            for (int r = 0; r < R; ++r) acc[r] = fmaf(wj, out[r][0].x + out[r][0].y, acc[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) acc[r] = warp_sum(acc[r]);
-        if (lane == 0) {
+        for (int r = 0; r < R; ++r) out[r][0] = make_float2(0.f, 0.f);
+        for (int c = lane; c < C; c += 32) {
+            const int b = (c * 32) >> bs_shift;
+            uint32_t w[R][BITS];
+            float sc[R], zz[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int rl = g * R + r;
-                if (rl < rc) store_from_f32(q.Y, q.act_dtype, t * H + n0 + rl, acc[r]);
+                const int rl = min(g * R + r, rc - 1);
+                load_chunk<BITS>(W + int64_t(rl) * rb, c, w[r]);
+                sc[r] = to_f32(Sc[rl * nb + b]);
+                zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
             }
+            chunk_accumulate<BITS, R, 1>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float v = warp_sum(out[r][0].x + out[r][0].y);
+            if (lane == 0 && g * R + r < rc) part[j * kDecodeRows2 + g * R + r] = v;
+        }
+    }
+    __syncthreads();
+    if (tid < rc) {
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) acc = fmaf(s_w[j], part[j * kDecodeRows2 + tid], acc);
+        store_from_f32(q.Y, q.act_dtype, t * H + n0 + tid, acc);
     }
 }
 
@@ -384,7 +402,7 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
     const int C = static_cast<int>(q.fc2.nb * q.bs / 32);
     const int nb = static_cast<int>(q.fc2.nb);
     const int64_t rb = q.fc2.row_bytes;
-    const Fc2Plan plan = fc2_plan(MT, C, rb, nb, sizeof(S));
+    const Fc2Plan plan = fc2_plan(kRowsPerBlock2, MT, C, rb, nb, sizeof(S), false);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     int* s_int = reinterpret_cast<int*>(smem + 16);
     float4* A4 = reinterpret_cast<float4*>(smem + 256);
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
         bulk_g2s(Wst, q.fc2_w + (int64_t(e) * H + n0) * rb, wbytes, bar);
         bulk_g2s(Wst + plan.w, static_cast<const S*>(q.fc2_s) + (int64_t(e) * H + n0) * nb, sbytes, bar);
     }
-    stage_chunks<BITS, MT>(
+    stage_chunks<BITS, MT, kF32>(
         A4, Corr, C, I, kF32, true,
         [&](int m) -> const void* { return m < cnt ? static_cast<const void*>(h + (s0 + m) * I) : nullptr; }, tid,
         kThreads);
@@ -450,10 +468,7 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
                 sc[r] = to_f32(Sc[rl * nb + b]);
                 zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
             }
-            if (Z2)
-                chunk_accumulate<BITS, R, MT, true>(w, sc, zz, A4, Corr, C, c, out2);
-            else
-                chunk_accumulate<BITS, R, MT, false>(w, sc, zz, A4, Corr, C, c, out2);
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Corr, C, c, out2);
         }
         float out[R][MT];
 #pragma unroll
@@ -602,8 +617,9 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     if (use_decode(q)) {
         e = launch_fc1<B1, ST, 1, true>(q, static_cast<unsigned>(P), stream, pdl);
         if (e != cudaSuccess) return e;
-        const Fc2Plan p2 = fc2_plan(kDecodeMaxK, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
-        return launch(fc2_decode_kernel<B2, ST>, dim3(static_cast<unsigned>(q.T), gy2, 1), p2.total, stream, q, pdl);
+        const Fc2Plan p2 = fc2_plan(kDecodeRows2, kDecodeMaxK, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2, true);
+        const unsigned gyd = static_cast<unsigned>(cdiv<int64_t>(q.H, kDecodeRows2));
+        return launch(fc2_decode_kernel<B2, ST>, dim3(static_cast<unsigned>(q.T), gyd, 1), p2.total, stream, q, pdl);
     }
     int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
     float* wts = reinterpret_cast<float*>(ws + L.wts);
@@ -671,7 +687,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
     if ((e = launch_fc1<B1, ST, kTileM, false>(q, gx, stream, pdl)) != cudaSuccess) return e;
-    const Fc2Plan p2 = fc2_plan(kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2);
+    const Fc2Plan p2 = fc2_plan(kRowsPerBlock2, kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2, false);
     if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q, pdl)) != cudaSuccess) return e;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), 152 * 16);
     combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);

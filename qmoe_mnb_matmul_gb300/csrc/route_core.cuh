@@ -1,4 +1,4 @@
-// route_core.cuh -- one warp routes one token: fp32 softmax over E router
+// route_core.cuh -- one warp (or one CTA) routes one token: fp32 softmax over E router
 // logits, the k largest logits (ties to the lower expert index), weights
 // renormalised over the selected k or left as softmax probabilities
 // ("feat(qwen4): component kernels extracted from the brick PRs": fp32 softmax,
@@ -13,18 +13,18 @@ namespace mnb {
 constexpr int kMaxExpertsPerLane = 32;  // E <= 1024
 constexpr int kNoExpert = 0x7fffffff;
 
-// Every lane of the warp must call this.  Slot j's expert and weight are
-// written to idx[j * stride] / w[j * stride] (any address space) by lane 0.
-template <typename IdxT, typename WT>
-__device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, int normalize, IdxT* idx,
-                                           WT* w, int stride) {
+// One warp, PL logits per lane (E <= 32 PL): expert e lives in slot e / 32 of
+// lane e % 32, so the argmax scans only the PL slots a lane can hold.
+template <int PL, typename IdxT, typename WT>
+__device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int E, int k, int normalize, IdxT* idx,
+                                              WT* w, int stride) {
     const int lane = threadIdx.x & 31;
     const int per_lane = (E + 31) >> 5;
-    float v[kMaxExpertsPerLane];
+    float v[PL];
     uint32_t taken = 0;
     float lmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kMaxExpertsPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
         const int e = i * 32 + lane;
         const bool ok = i < per_lane && e < E;
         v[i] = ok ? row[e] : -INFINITY;
@@ -38,7 +38,7 @@ __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E,
         float bv = 0.f;
         int be = kNoExpert;
 #pragma unroll
-        for (int i = 0; i < kMaxExpertsPerLane; ++i) {
+        for (int i = 0; i < PL; ++i) {
             const int e = i * 32 + lane;
             if (i < per_lane && e < E && !((taken >> i) & 1u)) {
                 if (be == kNoExpert || v[i] > bv) { bv = v[i]; be = e; }
@@ -63,7 +63,7 @@ __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E,
     if (!normalize) {
         float s = 0.f;
 #pragma unroll
-        for (int i = 0; i < kMaxExpertsPerLane; ++i) {
+        for (int i = 0; i < PL; ++i) {
             const int e = i * 32 + lane;
             if (i < per_lane && e < E) s += expf(v[i] - lmax);
         }
@@ -73,6 +73,85 @@ __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E,
     if (lane == 0)
         for (int j = 0; j < k; ++j) w[j * stride] = static_cast<WT>(static_cast<float>(w[j * stride]) / denom);
     __syncwarp();
+}
+
+// Every lane of the warp must call this.  Slot j's expert and weight are
+// written to idx[j * stride] / w[j * stride] (any address space) by lane 0.
+// The scan width is fixed at compile time from E, so a 128-expert router pays
+// for four logits per lane, not for the 1024-expert maximum.
+template <typename IdxT, typename WT>
+__device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, int normalize, IdxT* idx,
+                                           WT* w, int stride) {
+    if (E <= 32) return warp_route_pl<1>(row, E, k, normalize, idx, w, stride);
+    if (E <= 64) return warp_route_pl<2>(row, E, k, normalize, idx, w, stride);
+    if (E <= 128) return warp_route_pl<4>(row, E, k, normalize, idx, w, stride);
+    if (E <= 256) return warp_route_pl<8>(row, E, k, normalize, idx, w, stride);
+    if (E <= 512) return warp_route_pl<16>(row, E, k, normalize, idx, w, stride);
+    return warp_route_pl<kMaxExpertsPerLane>(row, E, k, normalize, idx, w, stride);
+}
+
+// Routing of one token by a whole CTA (blockDim.x >= E): every thread ranks
+// one logit against all E (the number of logits that beat it, ties going to
+// the lower expert index, NaN taken as -inf), the ranks below k name the
+// selected experts in order, and one lane forms the weights exactly as
+// warp_route does (same sums in the same order).  All threads must call this;
+// it ends with a block barrier.  s_logit is shared scratch of E floats.
+constexpr int kBlockRouteMaxE = 256;
+
+template <typename WT>
+__device__ __forceinline__ void block_route(const float* __restrict__ row, int E, int k, int normalize, int* idx,
+                                            WT* w, float* s_logit) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < E) {
+        const float x = row[tid];
+        s_logit[tid] = x != x ? -INFINITY : x;
+    }
+    __syncthreads();
+    if (tid < E) {
+        const float v = s_logit[tid];
+        int r0 = 0, r1 = 0;
+        int j = 0;
+#pragma unroll 4
+        for (; j + 1 < tid; j += 2) {  // lower indices beat v on ties
+            const float u0 = s_logit[j], u1 = s_logit[j + 1];
+            r0 += u0 >= v;
+            r1 += u1 >= v;
+        }
+        if (j < tid) r0 += s_logit[j] >= v;
+#pragma unroll 4
+        for (j = tid + 1; j + 1 < E; j += 2) {  // higher indices only when strictly greater
+            const float u0 = s_logit[j], u1 = s_logit[j + 1];
+            r0 += u0 > v;
+            r1 += u1 > v;
+        }
+        if (j < E) r0 += s_logit[j] > v;
+        const int r = r0 + r1;
+        if (r < k) idx[r] = tid;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const float lmax = s_logit[idx[0]];
+        float denom = 0.f;
+        if (!normalize) {
+            float sum = 0.f;
+#pragma unroll 1
+            for (int e = lane; e < E; e += 32) sum += expf(s_logit[e] - lmax);
+            denom = warp_sum(sum);
+        }
+        if (lane == 0) {
+            float sel = 0.f;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                const float p = expf(s_logit[idx[j]] - lmax);
+                sel += p;
+                w[j] = static_cast<WT>(p);
+            }
+            if (normalize) denom = sel;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) w[j] = static_cast<WT>(static_cast<float>(w[j]) / denom);
+        }
+    }
+    __syncthreads();
 }
 
 }  // namespace mnb
