@@ -186,6 +186,41 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Sums each of N per-lane values over the warp (N a power of two, <= 32) and
+// returns, in every lane, the total of value transpose_row<N>(lane).  At each
+// of the first log2(N) steps a lane hands half of the values it still holds
+// to its partner and keeps the other half, so the warp needs N - 1 + log2(32/N)
+// shuffles instead of 5 N.  The order of the additions is fixed.
+template <int N>
+__device__ __forceinline__ float warp_sum_transpose(float (&v)[N]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int n = N, off = 16; n > 1; n >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float give = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int off = 16 / N; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    return s;
+}
+
+// The value whose total warp_sum_transpose<N> leaves in this lane; lanes whose
+// low log2(32/N) bits are zero hold one distinct value each.
+template <int N>
+__device__ __forceinline__ int transpose_row(int lane) {
+    int row = 0;
+#pragma unroll
+    for (int n = N, off = 16; n > 1; n >>= 1, off >>= 1)
+        if (lane & off) row += n / 2;
+    return row;
+}
+
 template <typename T>
 __host__ __device__ constexpr T cdiv(T a, T b) {
     return (a + b - 1) / b;

@@ -15,8 +15,9 @@
 //    The grid is persistent (<= resident CTAs).
 //  * The activations are staged once per CTA (gemv_core.cuh); each consumer
 //    warp owns R rows of a block and walks their 32-code chunks, one chunk
-//    per lane; the R x MT sums are reduced with shuffles in a fixed order, so
-//    results are deterministic.
+//    per lane; the R x MT sums are reduced together with shuffles that hand
+//    half of the values to the partner lane at each step (fixed order, so
+//    results are deterministic).
 //  * Before the grid-dependency wait each CTA only warms L2 with its first
 //    blocks (a prefetch cannot observe stale data), so a programmatic
 //    dependent launch overlaps that traffic with the previous kernel.
@@ -45,7 +46,7 @@ struct Plan {
 
 __host__ __device__ inline Plan make_plan(int MT, int C, int RC, int64_t row_bytes, int nb, int ssize, int stages) {
     Plan p;
-    p.a4 = int64_t(MT) * 8 * C * 16;
+    p.a4 = a4_bytes(MT, C);
     p.sums = round_up(int64_t(MT) * C * 16, 128);  // one float4 correction per (row, chunk)
     p.w_stage = round_up(int64_t(RC) * row_bytes, 128);
     p.s_stage = round_up(int64_t(RC) * nb * ssize, 128);
@@ -108,10 +109,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
         if (lane != 0) return;
-        int it = 0;
-        for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
-            const int st = it % NST;
-            if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1)) {
+        int st = 0;
+        uint32_t round = 0;  // times the ring has wrapped
+        for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+            if (round && !mbar_wait(&empty[st], (round - 1) & 1)) {
                 for (int j = 0; j < NST; ++j) mbar_wait(&full[j], 0);  // give in-flight copies a bounded chance
                 return;
             }
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             mbar_arrive_expect_tx(&full[st], wb + sb);
             if (wb) bulk_g2s(W, wsrc, wb, &full[st]);
             if (sb) bulk_g2s(Sd, ssrc, sb, &full[st]);
+            if (++st == NST) { st = 0; ++round; }
         }
         return;
     }
@@ -146,11 +148,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     grid_launch_dependents();
 
     const int bs_shift = __ffs(a.bs) - 1;
+    const int mstride = a4_groups(C) * 256;
     constexpr int kZImplicit = 1 << (BITS - 1);
-    int it = 0;
-    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
-        const int st = it % NST;
-        if (!warp_wait(&full[st], (it / NST) & 1)) return;
+    int st = 0;
+    uint32_t phase = 0;
+    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        if (!warp_wait(&full[st], phase)) return;
         const int64_t n0 = int64_t(blk) * RC;
         const int rc = block_rows(blk);
         const uint8_t* W = Wst + st * plan.w_stage;
@@ -172,35 +175,37 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                 srow[r] = Sc + rl * nb;
                 zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
             }
-            for (int c = lane; c < C; c += 32) {
+            auto load = [&](int c, uint32_t (&w)[R][BITS], float (&sc)[R], float (&dz)[R]) {
                 const int b = (c * 32) >> bs_shift;
-                uint32_t w[R][BITS];
-                float sc[R], dz[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     load_chunk<BITS>(wrow[r], c, w[r]);
                     sc[r] = to_f32(srow[r][b]);
                     dz[r] = a.zp ? float(kZImplicit - zero_point_code<BITS>(zrow[r], b)) : 0.f;
                 }
-                chunk_accumulate<BITS, R, MT>(w, sc, dz, A4, Corr, C, c, acc);
+            };
+            for (int c = lane; c < C; c += 32) {
+                uint32_t w[R][BITS];
+                float sc[R], dz[R];
+                load(c, w, sc, dz);
+                chunk_accumulate<BITS, R, MT>(w, sc, dz, A4 + a4_base(0, c, C), mstride, Corr + c, C, acc);
             }
-            float out[R][MT];
+            // value q = r * MT + m; each total ends in one lane
+            constexpr int N = R * MT;
+            float part[N];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) out[r][m] = warp_sum(acc[r][m].x + acc[r][m].y);
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    if (r0 + r >= rc) break;
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-                        if (m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, out[r][m]);
-                }
+                for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m].x + acc[r][m].y;
+            const float total = warp_sum_transpose<N>(part);
+            if ((lane & (32 / N - 1)) == 0) {
+                const int q = transpose_row<N>(lane), r = q / MT, m = q - r * MT;
+                if (r0 + r < rc && m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
+        if (++st == NST) { st = 0; phase ^= 1; }
     }
 }
 

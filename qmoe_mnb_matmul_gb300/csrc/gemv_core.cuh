@@ -101,17 +101,6 @@ __device__ __forceinline__ int zero_point_code(const uint8_t* zrow, int b) {
     return (v >> sh) & ((1u << BITS) - 1u);
 }
 
-// Shared-memory image of MT activation rows for the chunk loop: float4 i4 of
-// chunk c of row m (codes 32c + 4 i4 .. +3) lives at A4[(m*8 + i4)*C + c], so
-// consecutive lanes (consecutive c) read consecutive 16-byte words.  One
-// thread stages one (row, chunk): it loads the chunk's 32 activations
-// (vectorised when `vec`), writes A'_j = A_j * code_scale(j), and the chunk's
-// correction Corr[m*C + c] = {-(Csum + z0 Asum) over even j, the same over odd
-// j, Asum over even j, Asum over odd j}, with Csum = sum A'_j / 2, Asum =
-// sum A_j and z0 = 2^(BITS-1) the implicit zero point, summed in ascending j.
-// (The f32x2 products keep even codes in .x and odd codes in .y.)
-// row(m) returns activation row m (dtype `dt_arg`, or FIXED_DT when that is
-// given at compile time; K valid entries) or nullptr for a row of zeros.
 // 32 activations starting at k0 one by one (zeros past K or for a null row):
 // the path for unaligned rows and a ragged last chunk, kept out of line so the
 // vector path stays compact in the instruction cache.
@@ -120,6 +109,24 @@ static __device__ __noinline__ void load_chunk_slow(const void* src, int dt, int
     for (int j = 0; j < 32; ++j) v[j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
 }
 
+// Shared-memory image of MT activation rows for the chunk loop.  Chunks are
+// grouped by 32 (one per lane of a warp step): float4 i4 (codes 4 i4 .. +3 of
+// the chunk) of chunk c of row m lives at
+//   A4[(m * CB + c / 32) * 256 + i4 * 32 + c % 32],   CB = ceil(C / 32),
+// so a lane's eight float4 of one chunk sit at fixed 512-byte steps from one
+// base and the 32 lanes of a step read 32 consecutive 16-byte words.
+__host__ __device__ inline int a4_groups(int C) { return (C + 31) / 32; }
+__host__ __device__ inline int64_t a4_bytes(int MT, int C) { return int64_t(MT) * a4_groups(C) * 256 * 16; }
+__device__ __forceinline__ int a4_base(int m, int c, int C) { return (m * a4_groups(C) + (c >> 5)) * 256 + (c & 31); }
+
+// One thread stages one (row, chunk): it loads the chunk's 32 activations
+// (vectorised when `vec`), writes A'_j = A_j * code_scale(j), and the chunk's
+// correction Corr[m*C + c] = {-(Csum + z0 Asum) over even j, the same over odd
+// j, Asum over even j, Asum over odd j}, with Csum = sum A'_j / 2, Asum =
+// sum A_j and z0 = 2^(BITS-1) the implicit zero point, summed in ascending j.
+// (The f32x2 products keep even codes in .x and odd codes in .y.)
+// row(m) returns activation row m (dtype `dt_arg`, or FIXED_DT when that is
+// given at compile time; K valid entries) or nullptr for a row of zeros.
 template <int BITS, int MT, int FIXED_DT = -1, typename RowFn>
 __device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, int64_t K, int dt_arg, bool vec, RowFn row,
                                              int tid, int nthreads) {
@@ -169,9 +176,9 @@ __device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, in
             v[j] *= code_scale<BITS>(j);
             cs[j & 1] += 0.5f * v[j];
         }
+        float4* dst = A4 + a4_base(m, c, C);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            A4[(int64_t(m) * 8 + q) * C + c] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 8; ++q) dst[q * 32] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         Corr[m * C + c] = make_float4(-fmaf(z0, as[0], cs[0]), -fmaf(z0, as[1], cs[1]), as[0], as[1]);
     }
 }
@@ -181,10 +188,14 @@ __device__ __forceinline__ void stage_chunks(float4* A4, float4* Corr, int C, in
 // dz[r] = z0 - z[r] is the row's zero-point shift from the implicit one (0
 // without zero points: one code path serves both, which keeps the kernels
 // small).
+//
+// a4c = A4 + a4_base(0, c, C); row m's float4 i4 is a4c[m * mstride + 32 i4]
+// with mstride = a4_groups(C) * 256.  corr = Corr + c; row m's correction is
+// corr[m * C].
 template <int BITS, int R, int MT>
 __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], const float (&sc)[R], const float (&dz)[R],
-                                                 const float4* __restrict__ A4, const float4* __restrict__ Corr, int C,
-                                                 int c, float2 (&out)[R][MT]) {
+                                                 const float4* __restrict__ a4c, int mstride,
+                                                 const float4* __restrict__ corr, int C, float2 (&out)[R][MT]) {
     float2 P[R][MT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -194,7 +205,7 @@ __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], c
     for (int i4 = 0; i4 < 8; ++i4) {
         float4 av[MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) av[m] = A4[(m * 8 + i4) * C + c];
+        for (int m = 0; m < MT; ++m) av[m] = a4c[m * mstride + i4 * 32];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float2 f01, f23;
@@ -208,7 +219,7 @@ __device__ __forceinline__ void chunk_accumulate(const uint32_t (&w)[R][BITS], c
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const float4 cr = Corr[m * C + c];
+        const float4 cr = corr[m * C];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float2 t = __fadd2_rn(P[r][m], make_float2(cr.x, cr.y));

@@ -92,7 +92,7 @@ struct Fc1Plan {
 };
 __host__ __device__ inline Fc1Plan fc1_plan(int MT, int C, int64_t row_bytes, int nb, int ssize) {
     Fc1Plan p;
-    p.a4 = int64_t(MT) * 8 * C * 16;
+    p.a4 = a4_bytes(MT, C);
     p.asum = round_up(int64_t(MT) * C * 16, 128);  // float4 corrections
     p.w = round_up(int64_t(2 * kPairsPerBlock) * row_bytes, 128);
     p.s = round_up(int64_t(2 * kPairsPerBlock) * nb * ssize, 128);
@@ -109,7 +109,7 @@ struct Fc2Plan {
 __host__ __device__ inline Fc2Plan fc2_plan(int rows, int ACT, int C, int64_t row_bytes, int nb, int ssize,
                                             bool decode) {
     Fc2Plan p;
-    p.a4 = int64_t(ACT) * 8 * C * 16;
+    p.a4 = a4_bytes(ACT, C);
     p.asum = round_up(int64_t(ACT) * C * 16, 128);  // float4 corrections
     p.w = round_up(int64_t(rows) * row_bytes, 128);  // per expert slot
     p.s = round_up(int64_t(rows) * nb * ssize, 128);
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
                 sc[r] = to_f32(Sst[lrow[r] * nb + b]);
                 zz[r] = Z1 ? float(kZImplicit - zero_point_code<BITS>(Z1 + grow[r] * q.fc1.zp_row, b)) : 0.f;
             }
-            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Corr, C, c, out2);
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4 + a4_base(0, c, C), a4_groups(C) * 256, Corr + c, C, out2);
         }
         float out[R][MT];
 #pragma unroll
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
                 sc[r] = to_f32(Sc[rl * nb + b]);
                 zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
             }
-            chunk_accumulate<BITS, R, 1>(w, sc, zz, A4 + int64_t(j) * 8 * C, Corr + j * C, C, c, out);
+            chunk_accumulate<BITS, R, 1>(w, sc, zz, A4 + a4_base(j, c, C), a4_groups(C) * 256, Corr + j * C + c, C, out);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
                 sc[r] = to_f32(Sc[rl * nb + b]);
                 zz[r] = Z2 ? float(kZImplicit - zero_point_code<BITS>(Z2 + (n0 + rl) * q.fc2.zp_row, b)) : 0.f;
             }
-            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4, Corr, C, c, out2);
+            chunk_accumulate<BITS, R, MT>(w, sc, zz, A4 + a4_base(0, c, C), a4_groups(C) * 256, Corr + c, C, out2);
         }
         float out[R][MT];
 #pragma unroll
