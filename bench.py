@@ -14,8 +14,13 @@ of the GEMV kernel (timed with CUDA events inside the timed region) against the
 measured HBM copy bandwidth; `e2e` repeats the step with the activations copied
 from pinned host memory and all outputs copied back inside the timed region.
 
+`other_rows` times the rest of the hot path, each against its own roofline:
+the tensor-core prefill GEMM at M=2048 and one Qwen3-30B-A3B-shaped QMoE layer
+at decode (T=1) and prefill (T=4096).  `cpu_baseline` times the oracle.
+
 `--impl reference` times the oracle (plain fp64 C, test infrastructure) on the
-host cores over a bounded sample of the same workload.
+host cores over a bounded sample of the same workload.  `--profile-case NAME`
+runs one small fixed invocation of a kernel (for ncu captures) and exits.
 """
 from __future__ import annotations
 
@@ -128,6 +133,15 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def tc_peak():
+    try:
+        with open(PEAKS_FILE) as fh:
+            p = json.load(fh)
+        return float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def ncu_traffic(kernel_sha: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
     try:
@@ -211,6 +225,167 @@ def run_reference(args, ws, rank):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
+# ------------------------------------------------ the other rows of the path
+
+MOE = wl.QWEN3_30B_A3B_MOE
+
+
+def moe_expert_bytes(b1, b2, bs):
+    H, I = MOE["H"], MOE["I"]
+    return 2 * I * (H * b1 // 8 + H // bs * 2) + H * (I * b2 // 8 + I // bs * 2)
+
+
+def make_moe_layers(torch, dev, n, b1, b2, bs, gen):
+    H, I, E = MOE["H"], MOE["I"], MOE["E"]
+    def r8(*shape):
+        return torch.randint(0, 256, shape, dtype=torch.uint8, generator=gen).to(dev)
+    def sc(*shape):
+        return (torch.rand(shape, generator=gen) * 0.015 + 0.005).half().to(dev)
+    return [(r8(E, 2 * I, H * b1 // 8), sc(E, 2 * I, H // bs), r8(E, H, I * b2 // 8), sc(E, H, I // bs))
+            for _ in range(n)]
+
+
+def event_time_us(torch, stream, fn, reps, warmup=3):
+    """Median CUDA-event time of fn() on `stream` (µs), with the raw samples' p10/p90."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in ts)
+    return us[len(us) // 2], us[len(us) // 10], us[(len(us) * 9) // 10]
+
+
+def other_rows(torch, mnb, dev):
+    """The rest of the hot path, each against its own roofline: the tensor-core
+    prefill GEMM (M=2048, bf16) and one Qwen3-30B-A3B-shaped QMoE layer at
+    decode (T=1, CUDA graph over 16 distinct layers) and prefill (T=4096)."""
+    gen = torch.Generator().manual_seed(7)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, hbm_kind = peaks()
+    tc, tc_kind = tc_peak()
+    rows = {}
+    # a5: prefill GEMM on the tensor cores
+    for name, K, N in (("gate", 2048, 6144), ("lm_head", 2048, 151936)):
+        M = 2048
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)
+        S = (torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev)
+        A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        us, p10, p90 = event_time_us(torch, stream, lambda: mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y, stream=stream),
+                                     reps=10 if N > 100000 else 30)
+        tf = 2 * M * N * K / (us * 1e-6) / 1e12
+        rows[f"prefill_gemm_{name}_m2048"] = {
+            "kernel": "gemm_tc (tcgen05, TMEM accumulators)", "shape": f"M={M} K={K} N={N} INT4 bs32 bf16 A/Y",
+            "us": us, "us_p10_p90": [p10, p90], "achieved": tf, "unit": "TFLOP/s", "peak": tc,
+            "frac": tf / tc, "bound": "tensor", "peak_source": f"{tc_kind} bf16_tflops"}
+        del B, S, A, Y
+    # a6-a10: the QMoE layer
+    H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
+    b1 = b2 = 3
+    bs = 64
+    nl = 16
+    layers = make_moe_layers(torch, dev, nl, b1, b2, bs, gen)
+    for T in (1, 4096):
+        X = torch.randn((T, H), generator=gen).half().to(dev)
+        logits = torch.randn((T, E), generator=gen).to(dev)
+        Y = torch.empty((T, H), dtype=torch.float16, device=dev)
+        ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, mnb.F16), dtype=torch.uint8, device=dev)
+
+        def call(i):
+            w1, s1, w2, s2 = layers[i % nl]
+            mnb.qmoe_forward(X, logits, k, True, w1, s1, None, b1, w2, s2, None, b2, I, bs, Y, ws, stream=stream)
+        if T == 1:
+            with torch.cuda.stream(stream):
+                call(0)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                gr.capture_begin()
+                for i in range(nl):
+                    call(i)
+                gr.capture_end()
+            us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=50)
+            us, p10, p90 = us / nl, p10 / nl, p90 / nl
+            touched = min(E, T * k) * moe_expert_bytes(b1, b2, bs)
+            gbs = touched / (us * 1e-6) / 1e9
+            rows["qmoe_decode_t1"] = {
+                "kernel": "fc1_kernel (decode) + fc2_decode_kernel", "shape": "Qwen3-30B-A3B layer, T=1, top-8 of 128, "
+                "INT3/INT3 bs64 fp16, 16 distinct layers replayed in one graph", "us": us, "us_p10_p90": [p10, p90],
+                "achieved": gbs, "unit": "GB/s", "peak": hbm, "frac": gbs / hbm, "bound": "hbm",
+                "bytes_per_layer": touched, "peak_source": f"{hbm_kind} hbm_gbs"}
+        else:
+            it = [0]
+
+            def once():
+                call(it[0])
+                it[0] += 1
+            us, p10, p90 = event_time_us(torch, stream, once, reps=10)
+            tf = T * k * (2 * H * 2 * I + 2 * I * H) / (us * 1e-6) / 1e12
+            rows["qmoe_prefill_t4096"] = {
+                "kernel": "route + permute + grouped gemm_tc FC1 (SwiGLU epilogue) + grouped gemm_tc FC2 + combine",
+                "shape": "Qwen3-30B-A3B layer, T=4096, top-8 of 128, INT3/INT3 bs64 fp16", "us": us,
+                "us_p10_p90": [p10, p90], "achieved": tf, "unit": "TFLOP/s", "peak": tc, "frac": tf / tc,
+                "bound": "tensor", "peak_source": f"{tc_kind} bf16_tflops"}
+        del X, logits, Y, ws
+    del layers
+    torch.cuda.empty_cache()
+    if mnb.mnb_get_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set in the other rows")
+    return rows
+
+
+PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill")
+
+
+def profile_case(name):
+    """One small, fixed invocation of a kernel for an ncu capture (no timing, no JSON)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import qmoe_mnb_matmul_gb300 as mnb
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator().manual_seed(11)
+    if name == "gemv_head":  # vocabulary head 2048 -> 151936, M=1, INT4 bs32, fp32: 3 launches
+        K, N = wl.QWEN3_1P7B_LM_HEAD[1:]
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)
+        S = (torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev)
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        for _ in range(3):
+            mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y)
+    elif name == "gemm_tc_gate":  # M=2048 bf16, gate 2048 -> 6144 INT4 bs32: 3 launches
+        M, K, N = 2048, 2048, 6144
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)
+        S = (torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev)
+        A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y)
+    else:  # one Qwen3-30B-A3B-shaped QMoE layer, INT3/INT3 bs64 fp16
+        T = 1 if name == "qmoe_decode" else 4096
+        H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
+        nl = 16 if T == 1 else 2
+        layers = make_moe_layers(torch, dev, nl, 3, 3, 64, gen)
+        X = torch.randn((T, H), generator=gen).half().to(dev)
+        logits = torch.randn((T, E), generator=gen).to(dev)
+        Y = torch.empty((T, H), dtype=torch.float16, device=dev)
+        ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, mnb.F16), dtype=torch.uint8, device=dev)
+        for i in range(24 if T == 1 else 3):
+            w1, s1, w2, s2 = layers[i % nl]
+            mnb.qmoe_forward(X, logits, k, True, w1, s1, None, 3, w2, s2, None, 3, I, 64, Y, ws)
+    torch.cuda.synchronize()
+    if mnb.mnb_get_last_device_error() != 0:
+        raise RuntimeError("device error word set")
+    print("ok")
+
+
 # ------------------------------------------------------------- our arm
 
 def main():
@@ -220,7 +395,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-rows", action="store_true", help="skip the prefill GEMM and QMoE measurements")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="run one small fixed invocation for an ncu capture and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_setup()
@@ -312,7 +493,9 @@ def main():
         return ms, clocks.summary()
 
     # One step = the 140 layer projections (one graph) then the vocabulary head
-    # (a second graph); CUDA events on the launching stream bracket the head.
+    # (a second graph).  On sampled steps the head is launched directly between
+    # two CUDA events on the launching stream (the host enqueues it while the
+    # layer graph runs), so the events time the kernel, not a graph launch.
     n_ev = min(args.steps, 512)
     hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
     stride = max(1, args.steps // n_ev)
@@ -322,7 +505,7 @@ def main():
         j = i // stride
         if i % stride == 0 and j < n_ev:
             hev[j][0].record(stream)
-            g_head.replay()
+            launch([head], stream)
             hev[j][1].record(stream)
         else:
             g_head.replay()
@@ -377,6 +560,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e / e2e_steps},
     }
+    if not args.no_other_rows:
+        out["other_rows"] = other_rows(torch, mnb, dev)
     if ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample()
     print(json.dumps(out))
