@@ -561,20 +561,48 @@ __global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64
 
 // Y[t, n] = sum_j w[t, j] * o[position of (t, j), n], ascending j, fp32 -> act
 // dtype, from FC2 outputs kept in the activation dtype (tensor-core plan).
+// One thread makes 8 consecutive outputs of a token from 16-byte loads of the
+// k routed rows (H % 8 == 0; the workspace rows are 16-byte aligned).
 template <typename AT>
-__global__ void combine_sorted_kernel(const __grid_constant__ QmoeArgs q) {
+__device__ __forceinline__ uint32_t pack_pair(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__half>(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <typename AT>
+__global__ void combine_sorted_kernel(const __grid_constant__ QmoeArgs q, int y_vec) {
     const char* ws = static_cast<const char*>(q.workspace);
     const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
     const AT* o = reinterpret_cast<const AT*>(ws + L.o);
     const float* wts = reinterpret_cast<const float*>(ws + L.wts);
     const int* inv = reinterpret_cast<const int*>(ws + L.inv);
     grid_dependency_wait();
-    const int64_t total = q.T * q.H;
+    const int64_t G = q.H / 8, total = q.T * G;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t t = i / q.H, n = i - t * q.H;
-        float acc = 0.f;
-        for (int j = 0; j < q.k; ++j) acc = fmaf(wts[t * q.k + j], to_f32(o[int64_t(inv[t * q.k + j]) * q.H + n]), acc);
-        store_from_f32(q.Y, q.act_dtype, i, acc);
+        const int64_t t = i / G, n0 = (i - t * G) * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < q.k; ++j) {
+            const float wj = wts[t * q.k + j];
+            const uint4 v = *reinterpret_cast<const uint4*>(o + int64_t(inv[t * q.k + j]) * q.H + n0);
+            const AT* h = reinterpret_cast<const AT*>(&v);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] = fmaf(wj, to_f32(h[c]), acc[c]);
+        }
+        if (y_vec) {
+            *reinterpret_cast<uint4*>(static_cast<AT*>(q.Y) + t * q.H + n0) =
+                make_uint4(pack_pair<AT>(acc[0], acc[1]), pack_pair<AT>(acc[2], acc[3]), pack_pair<AT>(acc[4], acc[5]),
+                           pack_pair<AT>(acc[6], acc[7]));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) store_from_f32(q.Y, q.act_dtype, t * q.H + n0 + c, acc[c]);
+        }
     }
 }
 
@@ -678,9 +706,10 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.k_steps = static_cast<int>(cdiv<int64_t>(q.I, 64));
         if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, sm_count, pdl, stream)) != cudaSuccess)
             return e;
-        const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), int64_t(sm_count) * 16);
+        const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H / 8, 256), int64_t(sm_count) * 16);
         using AT = typename DType<ST>::T;
-        combine_sorted_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
+        const int y_vec = (reinterpret_cast<uintptr_t>(q.Y) & 15) == 0;
+        combine_sorted_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, y_vec);
         return cudaGetLastError();
     }
     tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);

@@ -34,6 +34,8 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
     for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
 
     float sel_sum = 0.f;
+    int my_e = 0;
+    float my_p = 0.f;
     for (int j = 0; j < k; ++j) {
         float bv = 0.f;
         int be = kNoExpert;
@@ -54,7 +56,12 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
         if ((be & 31) == lane) taken |= 1u << (be >> 5);
         const float p = expf(bv - lmax);
         sel_sum += p;
-        if (lane == 0) {
+        if (j < 32) {  // lane j keeps slot j until the end
+            if (lane == j) {
+                my_e = be;
+                my_p = p;
+            }
+        } else if (lane == 0) {  // k > 32: park the raw weight in the output
             idx[j * stride] = static_cast<IdxT>(be);
             w[j * stride] = static_cast<WT>(p);
         }
@@ -69,14 +76,19 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
         }
         denom = warp_sum(s);
     }
+    if (lane < k) {
+        idx[lane * stride] = static_cast<IdxT>(my_e);
+        w[lane * stride] = static_cast<WT>(my_p / denom);
+    }
     __syncwarp();
-    if (lane == 0)
-        for (int j = 0; j < k; ++j) w[j * stride] = static_cast<WT>(static_cast<float>(w[j * stride]) / denom);
+    if (k > 32 && lane == 0)
+        for (int j = 32; j < k; ++j) w[j * stride] = static_cast<WT>(static_cast<float>(w[j * stride]) / denom);
     __syncwarp();
 }
 
 // Every lane of the warp must call this.  Slot j's expert and weight are
-// written to idx[j * stride] / w[j * stride] (any address space) by lane 0.
+// written to idx[j * stride] / w[j * stride] (any address space) by lane j
+// (slots past 32 by lane 0).
 // The scan width is fixed at compile time from E, so a 128-expert router pays
 // for four logits per lane, not for the 1024-expert maximum.
 template <typename IdxT, typename WT>
