@@ -76,7 +76,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     return fn(scale_dtype, g.a_dtype, BN, a, g.A, g.M, g.K, grid, pdl, stream);
 }
 
-int grouped_tile_rows() { return 128; }
+int grouped_tile_rows() { return 256; }
 
 cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
                               int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream) {

@@ -54,7 +54,7 @@ __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
 }
 
 // m-tiles of the tensor-core plan: <= kTcTileM sorted pairs of one expert.
-constexpr int kTcTileM = 128;
+constexpr int kTcTileM = 256;  // equals grouped_tile_rows()
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
     const int64_t t = (P + kTcTileM - 1) / kTcTileM + E;
     return P < t ? P : t;
