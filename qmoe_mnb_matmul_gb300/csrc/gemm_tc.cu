@@ -7,8 +7,8 @@
 namespace mnb {
 
 #define MNB_SLICE_DECL(NAME)                                                                                      \
-    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, const TcArgs& a, const void* A_rows, int64_t a_rows, \
-                     int64_t a_cols, int grid, bool pdl, cudaStream_t stream);                                \
+    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, int G, const TcArgs& a, const void* A_rows,          \
+                     int64_t a_rows, int64_t a_cols, int grid, bool pdl, cudaStream_t stream);                 \
     cudaError_t NAME##_take_error(unsigned int* out);
 MNB_SLICE_DECL(gemm_tc_gemm_b3)
 MNB_SLICE_DECL(gemm_tc_gemm_b4)
@@ -21,18 +21,26 @@ namespace {
 constexpr int kBW = 128;  // weight rows per tile
 constexpr int kBK = 64;   // K per stage
 
-// Activation rows per tile: fewest waves of persistent CTAs, weighing the
-// lower per-FLOP efficiency of narrow tiles.
-int pick_bn(int64_t M, int64_t N, int sm_count) {
-    int best = 256;
+// Tile shape: BN activation rows per MMA and G sub-tiles per dequantised
+// weight tile.  A tile's time is modelled as max(MMA columns G*BN, the
+// dequantisation of its weight K steps, worth ~460 MMA columns per step at the
+// measured rates) over the narrow-tile MMA efficiency; the grid walks the
+// tiles in waves of one per SM.
+struct TcShape {
+    int BN, G;
+};
+TcShape pick_shape(int64_t M, int64_t N, int sm_count) {
+    TcShape best{256, 1};
     double best_cost = 1e300;
-    for (int bn : {256, 128, 64, 32, 16}) {
-        if (bn > 16 && bn / 2 >= M) continue;  // a narrower tile covers M already
-        const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, bn);
+    const TcShape cands[] = {{256, 1}, {128, 1}, {64, 1}, {32, 1}, {16, 1}};
+    for (const TcShape& c : cands) {
+        if (c.G == 1 && c.BN > 16 && c.BN / 2 >= M) continue;  // a narrower tile covers M already
+        if (c.G == 2 && M <= 256) continue;
+        const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(c.BN) * c.G);
         const double waves = double(cdiv<int64_t>(tiles, sm_count));
-        const double eff = bn >= 256 ? 1.0 : bn >= 128 ? 0.9 : bn >= 64 ? 0.7 : 0.5;
-        const double cost = waves * bn / eff;
-        if (cost < best_cost) { best_cost = cost; best = bn; }
+        const double eff = c.BN >= 256 ? 1.0 : c.BN >= 128 ? 0.9 : c.BN >= 64 ? 0.7 : 0.5;
+        const double cost = waves * std::max(double(c.BN * c.G), 460.0) / eff;
+        if (cost < best_cost) { best_cost = cost; best = c; }
     }
     return best;
 }
@@ -53,7 +61,7 @@ cudaError_t gemm_tc_take_error(unsigned int* out) {
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
-    const int BN = pick_bn(g.M, g.N, sm_count);
+    const TcShape sh = pick_shape(g.M, g.N, sm_count);
     TcArgs a = {};
     a.M = g.M;
     a.K = g.K;
@@ -69,20 +77,20 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     a.y_dtype = g.y_dtype;
     a.ld_y = g.N;
     a.tiles_n = static_cast<int>(cdiv<int64_t>(g.N, kBW));
-    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, BN));
+    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(sh.BN) * sh.G));
     a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK));
     const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m, sm_count));
     auto fn = g.bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3;
-    return fn(scale_dtype, g.a_dtype, BN, a, g.A, g.M, g.K, grid, pdl, stream);
+    return fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
 }
 
+// Grouped (QMoE) tiles: 256 routed rows of one expert.
 int grouped_tile_rows() { return 256; }
 
 cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
                               int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream) {
-    const int BN = grouped_tile_rows();
     auto fn = fc1 ? (bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3) : (bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3);
-    return fn(scale_dtype, a_dtype, BN, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
+    return fn(scale_dtype, a_dtype, grouped_tile_rows(), 1, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

@@ -7,25 +7,32 @@
 // "selected-expert / tiled-dequantisation plus GEMM" prefill the QMoE CUDA
 // page names as missing).
 //
-// Tiles are 128 weight rows x BN activation rows.  The MMA is "swap-AB": the
-// dequantised weight tile is operand A (M = 128) and the activation tile
-// operand B (N = BN <= 256), so the fp32 accumulator in tensor memory holds
-// Y^T (lane = weight row, column = activation row) and small M costs no
-// padding on the weight side.  One persistent CTA per SM walks the tiles.
+// Tiles are 128 weight rows x G*BN activation rows.  The MMA is "swap-AB":
+// the dequantised weight tile is operand A (M = 128) and each of the G
+// activation sub-tiles operand B (N = BN <= 256), so the fp32 accumulators in
+// tensor memory hold Y^T (lane = weight row, column = activation row) and small
+// M costs no padding on the weight side.  With G = 2 every dequantised weight
+// K step feeds two MMAs (512 accumulator columns), halving the dequantisation
+// per FLOP; with G = 1 the two 256-column halves of tensor memory double-buffer
+// consecutive tiles.  One persistent CTA per SM walks the tiles.
 //
-// Warp roles (448 threads):
+// Warp roles (704 threads):
 //   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle), or
 //               (FC1) cp.async gathers of the routed tokens' rows into the
 //               same swizzled layout
 //   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
-//   warps 2-9   dequant: two threads per weight row, one 32-code chunk each
-//               per K step; a private cp.async ring of packed bytes and scales;
-//               codes -> s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
-//   warps 10-13 epilogue: tcgen05.ld of the double-buffered accumulator ->
-//               output dtype (FC1: SwiGLU of lane pairs) -> masked stores
-// Stage s of the shared ring holds one K step's activation tile and
-// dequantised weight tile; a tcgen05.commit releases it when the MMAs that
-// read it complete.  Every wait is bounded.
+//   warps 2-17  dequant, two groups of 8 warps taking alternate K steps: two
+//               threads per weight row, one 32-code chunk each per K step; a
+//               private cp.async ring of packed bytes and scales; codes ->
+//               s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
+//   warps 18-21 epilogue: tcgen05.ld of the accumulators -> output dtype
+//               (FC1: SwiGLU of lane pairs) -> masked stores
+// The activation tiles and the dequantised weight tiles of the K steps sit in
+// two separate shared rings: the activation ring is deep (its tiles come from
+// L2 / HBM with the longest latency), the weight ring shallow (its tiles are
+// written by the dequantisation warps, whose own cp.async ring hides the
+// packed-byte latency).  A tcgen05.commit releases a slot of each when the MMAs
+// that read it complete.  Every wait is bounded.
 #pragma once
 
 #include <cuda.h>
@@ -48,7 +55,10 @@ using namespace gemv;
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kBW = 128;    // weight rows per tile (MMA M)
 constexpr int kPack = 4;    // depth of each dequant thread's cp.async ring
-constexpr int kDequantWarp0 = 2, kDequantWarps = 8, kEpilogueWarp0 = 10;
+// Two groups of 8 dequantisation warps take alternate K steps, so each group
+// has two MMA steps' time for its 128 x 64 weight slice.
+constexpr int kDequantWarp0 = 2, kDequantWarps = 8, kDequantGroups = 2;
+constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;
 constexpr int kThreadsTC = (kEpilogueWarp0 + 4) * 32;
 constexpr int kMaxStagesTC = 8;
 
@@ -58,14 +68,14 @@ struct TcPlan {
     int64_t bars, act, w, pack, scl, total;
 };
 
-__host__ __device__ inline TcPlan tc_plan(int BN, int stages, int bits) {
+__host__ __device__ inline TcPlan tc_plan(int BN, int G, int stages, int stages_w, int bits) {
     TcPlan p;
     p.bars = 1024;                                           // barriers and the TMEM address
-    p.act = int64_t(BN) * 128;                               // activations of one stage
+    p.act = int64_t(G) * BN * 128;                           // activations of one stage (G sub-tiles)
     p.w = int64_t(kBW) * 128;                                // dequantised weights of one stage
-    p.pack = int64_t(kPack) * 2 * kBW * (bits == 4 ? 16 : 12);
-    p.scl = int64_t(kPack) * 2 * kBW * 4;
-    p.total = p.bars + int64_t(stages) * (p.act + p.w) + p.pack + p.scl;
+    p.pack = int64_t(kDequantGroups) * kPack * 2 * kBW * (bits == 4 ? 16 : 12);
+    p.scl = int64_t(kDequantGroups) * kPack * 2 * kBW * 4;
+    p.total = p.bars + int64_t(stages) * p.act + int64_t(stages_w) * p.w + p.pack + p.scl;
     return p;
 }
 
@@ -132,21 +142,31 @@ __device__ __forceinline__ Tile tile_of(const TcArgs& a, int t, int BN) {
     return x;
 }
 
-template <int BITS, int ST, int AT, int BN, int MODE>
+// Accumulator slot s (columns s*BN ..) of sub-tile g of the tl-th tile of this
+// CTA, and how many earlier tiles used that slot.
+template <int G>
+__device__ __forceinline__ int acc_slot(int tl, int g) { return G == 1 ? (tl & 1) : g; }
+template <int G>
+__device__ __forceinline__ int acc_uses(int tl) { return G == 1 ? (tl >> 1) : tl; }
+
+template <int BITS, int ST, int AT, int BN, int G, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                 const __grid_constant__ TcArgs a) {
+    static_assert(G == 1 || G == 2, "one or two activation sub-tiles per tile");
+    constexpr int UN = G * BN;  // activation rows per tile
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int S = a.stages;
-    const TcPlan plan = tc_plan(BN, S, BITS);
+    const int S = a.stages, SW = a.stages_w;
+    const TcPlan plan = tc_plan(BN, G, S, SW, BITS);
     uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* full_w = full_a + kMaxStagesTC;
-    uint64_t* empty = full_a + 2 * kMaxStagesTC;
-    uint64_t* acc_full = full_a + 3 * kMaxStagesTC;
+    uint64_t* empty = full_a + kMaxStagesTC;
+    uint64_t* full_w = full_a + 2 * kMaxStagesTC;
+    uint64_t* empty_w = full_a + 3 * kMaxStagesTC;
+    uint64_t* acc_full = full_a + 4 * kMaxStagesTC;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
     uint8_t* act = smem + plan.bars;
     uint8_t* wt = act + S * plan.act;
-    uint8_t* pack = wt + S * plan.w;
+    uint8_t* pack = wt + SW * plan.w;
     uint8_t* scl = pack + plan.pack;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -159,8 +179,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_a[s], 1);
-            mbar_init(&full_w[s], kDequantWarps);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(&full_w[s], kDequantWarps);
+            mbar_init(&empty_w[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -184,11 +207,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             if (lane == 0) {
                 RingPos rp;
                 for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                    const Tile x = tile_of(a, t, BN);
+                    const Tile x = tile_of(a, t, UN);
                     for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
                         if (rp.round && !mbar_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
-                        mbar_arrive_expect_tx(&full_a[rp.stage], BN * 128);
-                        tma_load_2d(act + rp.stage * plan.act, &tmap_a, ks * kBK, x.s0, &full_a[rp.stage]);
+                        mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
+#pragma unroll
+                        for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
+                            tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, ks * kBK, x.s0 + g * BN,
+                                        &full_a[rp.stage]);
                     }
                 }
             }
@@ -197,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             // published (after a proxy fence) once its copies have landed,
             // lagging the issue by up to S - 1 stages.  Lane l owns tile rows
             // l, l+32, ...; their source rows are resolved once per tile.
-            constexpr int kRowsPerLane = BN >= 32 ? BN / 32 : 1;
+            constexpr int kRowsPerLane = UN >= 32 ? UN / 32 : 1;
             const int lag = S - 1;
             RingPos rp, pub;
             int issued = 0, published = 0;
@@ -209,14 +235,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 ++published;
             };
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                const Tile x = tile_of(a, t, BN);
+                const Tile x = tile_of(a, t, UN);
                 const uint16_t* src[kRowsPerLane];
                 uint32_t rowoff[kRowsPerLane];
                 uint32_t rx[kRowsPerLane];
 #pragma unroll
                 for (int i = 0; i < kRowsPerLane; ++i) {
                     const int j = lane + 32 * i;
-                    src[i] = (j < BN && j < x.cnt)
+                    src[i] = (j < UN && j < x.cnt)
                                  ? static_cast<const uint16_t*>(a.X) + int64_t(a.perm[x.s0 + j] / a.k) * a.K
                                  : nullptr;
                     rowoff[i] = static_cast<uint32_t>((j >> 3) * 1024 + (j & 7) * 128);
@@ -250,39 +276,50 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kBW, BN, AT == kBF16);
-            RingPos rp;
+            RingPos rp, rw;
             int tl = 0;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
-                const int buf = tl & 1;
-                if (tl >= 2 && !mbar_wait(&acc_empty[buf], ((tl >> 1) - 1) & 1)) { failed = true; break; }
-                tc_fence_after();
-                const uint32_t d = tmem + buf * BN;
-                for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                    const uint32_t par = rp.round & 1;
-                    if (!mbar_wait(&full_a[rp.stage], par) || !mbar_wait(&full_w[rp.stage], par)) {
+                const int uses = acc_uses<G>(tl);
+                for (int ks = 0; ks < ksteps && !failed; ++ks, rp.next(S), rw.next(SW)) {
+                    if (!mbar_wait(&full_a[rp.stage], rp.round & 1) || !mbar_wait(&full_w[rw.stage], rw.round & 1)) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t da = smem_desc_sw128(wt + rp.stage * plan.w);
-                    const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act);
+                    const uint64_t da = smem_desc_sw128(wt + rw.stage * plan.w);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+                    for (int g = 0; g < G; ++g) {
+                        const int slot = acc_slot<G>(tl, g);
+                        if (ks == 0 && uses > 0) {  // the epilogue has drained this slot's previous tile
+                            if (!mbar_wait(&acc_empty[slot], (uses - 1) & 1)) { failed = true; break; }
+                            tc_fence_after();
+                        }
+                        const uint32_t d = tmem + slot * BN;
+                        const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act + g * BN * 128);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+                    }
+                    if (failed) break;
                     tc_commit(&empty[rp.stage]);
+                    tc_commit(&empty_w[rw.stage]);
                 }
                 if (failed) break;
-                tc_commit(&acc_full[buf]);
+#pragma unroll
+                for (int g = 0; g < G; ++g) tc_commit(&acc_full[acc_slot<G>(tl, g)]);
             }
         }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequant
-        const int dq = tid - kDequantWarp0 * 32;
+        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes global K steps = group (mod 2)
+        const int dq = tid - (kDequantWarp0 + group * kDequantWarps) * 32;
         const int r = dq & (kBW - 1);  // weight row of the tile
         const int h = dq >> 7;         // which 32-code chunk of the K step
         constexpr int kCB = BITS == 4 ? 16 : 12;  // packed bytes per 32-code chunk
         constexpr int kStepBytes = 2 * kCB;       // packed bytes of a row per K step
         constexpr int kZ = 1 << (BITS - 1);
+        uint8_t* gpack = pack + int64_t(group) * (plan.pack / kDequantGroups);
+        uint8_t* gscl = scl + int64_t(group) * (plan.scl / kDequantGroups);
         const int nb = a.nb, bs_shift = __ffs(a.bs) - 1;
         const int64_t kcodes = int64_t(nb) * a.bs;  // codes stored per row
         const int64_t n_scales = a.rows * nb;
@@ -312,21 +349,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             st.si0 = (st.ok ? wr : 0) * nb;
             return st;
         };
-        // prefetch cursor: the (tile, K step) whose bytes go into the ring next
-        int pt = blockIdx.x, pks = 0, pslot = 0;
-        RowStream ps = pt < n_tiles ? stream_of(tile_of(a, pt, BN)) : RowStream{nullptr, nullptr, 0, false};
+        // This group's K steps, in order: the CTA's tiles t = blockIdx.x + j * gridDim.x,
+        // each with ksteps steps, numbered globally; the group takes every second one.
+        struct Cursor {
+            int t, ks;
+        };
+        auto advance = [&](Cursor& c) {  // two global steps on
+            c.ks += kDequantGroups;
+            while (c.ks >= ksteps && c.t < n_tiles) {
+                c.ks -= ksteps;
+                c.t += gridDim.x;
+            }
+        };
+        Cursor pc{static_cast<int>(blockIdx.x), group};  // prefetch cursor
+        while (pc.ks >= ksteps && pc.t < n_tiles) {
+            pc.ks -= ksteps;
+            pc.t += gridDim.x;
+        }
+        int pslot = 0;
+        RowStream ps = pc.t < n_tiles ? stream_of(tile_of(a, pc.t, UN)) : RowStream{nullptr, nullptr, 0, false};
         auto issue = [&]() {
-            if (pt < n_tiles && ps.ok && pks < live_steps) {
-                uint8_t* dst = pack + ((pslot * 2 + h) * kBW + r) * kCB;
-                const uint8_t* src = ps.w + int64_t(pks) * kStepBytes;
+            if (pc.t < n_tiles && ps.ok && pc.ks < live_steps) {
+                uint8_t* dst = gpack + ((pslot * 2 + h) * kBW + r) * kCB;
+                const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
                 if constexpr (BITS == 4) {
                     cp_async16(dst, src);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + 4 * q);
                 }
-                const int64_t si = ps.si0 + ((int64_t(pks) * kBK + 32 * h) >> bs_shift);
-                uint32_t* sdst = reinterpret_cast<uint32_t*>(scl + ((pslot * 2 + h) * kBW + r) * 4);
+                const int64_t si = ps.si0 + ((int64_t(pc.ks) * kBK + 32 * h) >> bs_shift);
+                uint32_t* sdst = reinterpret_cast<uint32_t*>(gscl + ((pslot * 2 + h) * kBW + r) * 4);
                 if (ST == kF32) {
                     cp_async4(sdst, reinterpret_cast<const float*>(ps.s) + si);
                 } else if ((si | 1) < n_scales) {
@@ -337,77 +390,91 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             }
             cp_async_commit();
             if (++pslot == kPack) pslot = 0;
-            if (pt < n_tiles && ++pks == ksteps) {
-                pks = 0;
-                pt += gridDim.x;
-                if (pt < n_tiles) ps = stream_of(tile_of(a, pt, BN));
+            if (pc.t < n_tiles) {
+                const int t_before = pc.t;
+                advance(pc);
+                if (pc.t != t_before && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t, UN));
             }
         };
         for (int i = 0; i < kPack - 1; ++i) issue();
+        // consumer cursor and its place in the weight ring (global step g -> slot g % SW)
+        Cursor cc = Cursor{static_cast<int>(blockIdx.x), group};
+        while (cc.ks >= ksteps && cc.t < n_tiles) {
+            cc.ks -= ksteps;
+            cc.t += gridDim.x;
+        }
         RingPos rp;
+        if (group) rp.next(SW);
         int cslot = 0;
-        for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-            const Tile x = tile_of(a, t, BN);
-            const RowStream cs = stream_of(x);
-            const uint8_t* zrow = nullptr;
-            if (a.zp && cs.ok) zrow = a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes;
-            for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                issue();
-                cp_async_wait<kPack - 1>();
-                if (rp.round && !warp_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
-                const bool live = cs.ok && ks < live_steps;
-                uint32_t w[BITS];
-                float sc = 0.f, z = float(kZ);
-                if (live) {
-                    const uint8_t* src = pack + ((cslot * 2 + h) * kBW + r) * kCB;
-                    if constexpr (BITS == 4) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(src);
-                        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
-                    }
-                    const int b = (ks * kBK + 32 * h) >> bs_shift;
-                    sc = scale_from_word<ST>(*reinterpret_cast<const uint32_t*>(scl + ((cslot * 2 + h) * kBW + r) * 4),
-                                             cs.si0 + b);
-                    if (zrow) z = float(zero_point_code<BITS>(zrow, b));
+        int cur_t = -1;
+        RowStream cs{nullptr, nullptr, 0, false};
+        const uint8_t* zrow = nullptr;
+        while (cc.t < n_tiles && !failed) {
+            if (cc.t != cur_t) {
+                cur_t = cc.t;
+                const Tile x = tile_of(a, cur_t, UN);
+                cs = stream_of(x);
+                zrow = (a.zp && cs.ok) ? a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes : nullptr;
+            }
+            const int ks = cc.ks;
+            issue();
+            cp_async_wait<kPack - 1>();
+            if (rp.round && !warp_wait(&empty_w[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+            const bool live = cs.ok && ks < live_steps;
+            uint32_t w[BITS];
+            float sc = 0.f, z = float(kZ);
+            if (live) {
+                const uint8_t* src = gpack + ((cslot * 2 + h) * kBW + r) * kCB;
+                if constexpr (BITS == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src);
+                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
                 } else {
 #pragma unroll
-                    for (int q = 0; q < BITS; ++q) w[q] = 0;
+                    for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
                 }
-                if (++cslot == kPack) cslot = 0;
-                // w = s (q - z) = f * s 2^(24-p) - s (2^(23-p) + z), one fp32 rounding per value;
-                // the pre-scale depends only on the code's position class p
-                constexpr int kCls = BITS == 4 ? 2 : 3;
-                float mc[kCls], ac[kCls];
+                const int b = (ks * kBK + 32 * h) >> bs_shift;
+                sc = scale_from_word<ST>(*reinterpret_cast<const uint32_t*>(gscl + ((cslot * 2 + h) * kBW + r) * 4),
+                                         cs.si0 + b);
+                if (zrow) z = float(zero_point_code<BITS>(zrow, b));
+            } else {
 #pragma unroll
-                for (int c = 0; c < kCls; ++c) {
-                    const int p = code_pos<BITS>(c);
-                    mc[c] = sc * float(1u << (24 - p));
-                    ac[c] = -sc * (float(1u << (23 - p)) + z);
-                }
-                uint32_t outw[16];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    float2 f01, f23;
-                    chunk_codes4<BITS>(w, g, f01, f23);
-                    const int j = 4 * g;
-                    const float2 v01 = ffma2(f01, make_float2(mc[j % kCls], mc[(j + 1) % kCls]),
-                                             make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
-                    const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
-                                             make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
-                    outw[2 * g] = pack2<AT>(v01.x, v01.y);
-                    outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
-                }
-                uint8_t* wdst = wt + rp.stage * plan.w;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(wdst + sw128(r, 4 * h + c)) =
-                        make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_w[rp.stage]);
+                for (int q = 0; q < BITS; ++q) w[q] = 0;
             }
+            if (++cslot == kPack) cslot = 0;
+            // w = s (q - z) = f * s 2^(24-p) - s (2^(23-p) + z), one fp32 rounding per value;
+            // the pre-scale depends only on the code's position class p
+            constexpr int kCls = BITS == 4 ? 2 : 3;
+            float mc[kCls], ac[kCls];
+#pragma unroll
+            for (int c = 0; c < kCls; ++c) {
+                const int p = code_pos<BITS>(c);
+                mc[c] = sc * float(1u << (24 - p));
+                ac[c] = -sc * (float(1u << (23 - p)) + z);
+            }
+            uint32_t outw[16];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float2 f01, f23;
+                chunk_codes4<BITS>(w, g, f01, f23);
+                const int j = 4 * g;
+                const float2 v01 = ffma2(f01, make_float2(mc[j % kCls], mc[(j + 1) % kCls]),
+                                         make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
+                const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
+                                         make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
+                outw[2 * g] = pack2<AT>(v01.x, v01.y);
+                outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
+            }
+            uint8_t* wdst = wt + rp.stage * plan.w;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(wdst + sw128(r, 4 * h + c)) =
+                    make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_w[rp.stage]);
+            rp.next(SW);
+            rp.next(SW);
+            advance(cc);
         }
         cp_async_wait<0>();
     } else {
@@ -415,44 +482,49 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         int tl = 0;
         for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
-            const int buf = tl & 1;
-            const Tile x = tile_of(a, t, BN);
-            if (!warp_wait(&acc_full[buf], (tl >> 1) & 1)) { failed = true; break; }
-            tc_fence_after();
+            const Tile x = tile_of(a, t, UN);
+            const int uses = acc_uses<G>(tl);
             const int rr = quarter * 32 + lane;  // tile row of this thread
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + buf * BN + c0, v);
-                tmem_ld_wait();
-                if constexpr (MODE == kModeFc1) {
-                    // rows 2p / 2p+1 hold gate / up of pair p: the even lane combines them
-                    const int64_t p = x.n0 / 2 + (rr >> 1);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float mine = __uint_as_float(v[j]);
-                        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                        if (!(lane & 1) && c0 + j < BN && c0 + j < x.cnt && p < a.I) {
-                            const float hv = mine / (1.0f + expf(-mine)) * other;
-                            store_from_f32(a.Y, a.y_dtype, (int64_t(x.s0) + c0 + j) * a.ld_y + p, hv);
-                        }
-                    }
-                } else {
-                    const int64_t n = x.n0 + rr;
-                    if (n < a.rows) {
+            for (int g = 0; g < G; ++g) {
+                const int slot = acc_slot<G>(tl, g);
+                if (!warp_wait(&acc_full[slot], uses & 1)) { failed = true; break; }
+                tc_fence_after();
+                const int cnt = x.cnt - g * BN;  // live activation rows of this sub-tile
+                const int64_t m0 = int64_t(x.s0) + g * BN;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN && c0 < cnt; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + slot * BN + c0, v);
+                    tmem_ld_wait();
+                    if constexpr (MODE == kModeFc1) {
+                        // rows 2p / 2p+1 hold gate / up of pair p: the even lane combines them
+                        const int64_t p = x.n0 / 2 + (rr >> 1);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            // a 16-column tile loads 32 columns: the upper 16 belong to the other accumulator
-                            if (c0 + j < BN && c0 + j < x.cnt)
-                                store_from_f32(a.Y, a.y_dtype, (int64_t(x.s0) + c0 + j) * a.ld_y + n,
-                                               __uint_as_float(v[j]));
+                            const float mine = __uint_as_float(v[j]);
+                            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                            if (!(lane & 1) && c0 + j < BN && c0 + j < cnt && p < a.I) {
+                                const float hv = mine / (1.0f + expf(-mine)) * other;
+                                store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + p, hv);
+                            }
+                        }
+                    } else {
+                        const int64_t n = x.n0 + rr;
+                        if (n < a.rows) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                // a 16-column tile loads 32 columns: the upper 16 belong to the other accumulator
+                                if (c0 + j < BN && c0 + j < cnt)
+                                    store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + n, __uint_as_float(v[j]));
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[slot]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
     }
     if (failed) record_error(MNB_ERR_TIMEOUT);
@@ -481,13 +553,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int stages_for(int BN, int bits) {
-    int stages = 6;
-    while (stages > 2 && tc_plan(BN, stages, bits).total > 227 * 1024) --stages;
-    return stages;
+// Ring depths: as many activation slots as fit (up to kMaxStagesTC) with three
+// weight slots, or with two when that buys one more activation slot.
+void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
+    auto deepest = [&](int sw) {
+        int s = kMaxStagesTC;
+        while (s > 2 && tc_plan(BN, G, s, sw, bits).total > 227 * 1024) --s;
+        return s;
+    };
+    const int s3 = deepest(3), s2 = deepest(2);
+    *stages_w = s2 > s3 ? 2 : 3;
+    *stages = s2 > s3 ? s2 : s3;
 }
 
-template <int BITS, int ST, int AT, int BN, int MODE>
+template <int BITS, int ST, int AT, int BN, int G, int MODE>
 cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
                        bool pdl, cudaStream_t stream) {
     TcArgs a = in;
@@ -509,9 +588,9 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     uint32_t cols = 32;
     while (cols < 2u * BN) cols <<= 1;
     a.tmem_cols = cols;
-    a.stages = stages_for(BN, BITS);
-    const int64_t smem = tc_plan(BN, a.stages, BITS).total;
-    auto kern = gemm_tc_kernel<BITS, ST, AT, BN, MODE>;
+    stages_for(BN, G, BITS, &a.stages, &a.stages_w);
+    const int64_t smem = tc_plan(BN, G, a.stages, a.stages_w, BITS).total;
+    auto kern = gemm_tc_kernel<BITS, ST, AT, BN, G, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -527,31 +606,20 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     return cudaLaunchKernelEx(&cfg, kern, tmap, a);
 }
 
-// Activation rows per tile: fewest waves of persistent CTAs, weighing the
-// lower per-FLOP efficiency of narrow tiles.
-int pick_bn(int64_t M, int64_t N, int sm_count) {
-    int best = 256;
-    double best_cost = 1e300;
-    for (int bn : {256, 128, 64, 32, 16}) {
-        if (bn > 16 && bn / 2 >= M) continue;  // a narrower tile covers M already
-        const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, bn);
-        const double waves = double(cdiv<int64_t>(tiles, sm_count));
-        const double eff = bn >= 256 ? 1.0 : bn >= 128 ? 0.9 : bn >= 64 ? 0.7 : 0.5;
-        const double cost = waves * bn / eff;
-        if (cost < best_cost) { best_cost = cost; best = bn; }
-    }
-    return best;
-}
-
 template <int MODE, int BITS, int ST, int AT>
-cudaError_t launch_bn(int BN, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
+cudaError_t launch_bn(int BN, int G, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
                       bool pdl, cudaStream_t stream) {
-    switch (BN) {
-        case 256: return launch_cfg<BITS, ST, AT, 256, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
-        case 128: return launch_cfg<BITS, ST, AT, 128, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
-        case 64: return launch_cfg<BITS, ST, AT, 64, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
-        case 32: return launch_cfg<BITS, ST, AT, 32, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
-        default: return launch_cfg<BITS, ST, AT, 16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+    if (G == 2) return launch_cfg<BITS, ST, AT, 256, 2, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+    if constexpr (MODE == kModeFc1) {
+        return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);  // grouped: 256 rows
+    } else {
+        switch (BN) {
+            case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 64: return launch_cfg<BITS, ST, AT, 64, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 32: return launch_cfg<BITS, ST, AT, 32, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            default: return launch_cfg<BITS, ST, AT, 16, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        }
     }
 }
 
@@ -559,16 +627,16 @@ cudaError_t launch_bn(int BN, const TcArgs& a, const void* A_rows, int64_t a_row
 
 // One (mode, bit width) slice of the instantiations; each slice lives in its own
 // translation unit so the slices compile in parallel.
-#define MNB_GEMM_TC_SLICE(NAME, MODE, BITS)                                                                   \
-    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, const TcArgs& a, const void* A_rows, int64_t a_rows, \
-                     int64_t a_cols, int grid, bool pdl, cudaStream_t stream) {                               \
-        const bool sf = scale_dtype == kF32;                                                                   \
-        if (a_dtype == kBF16)                                                                                  \
-            return sf ? launch_bn<MODE, BITS, kF32, kBF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream)   \
-                      : launch_bn<MODE, BITS, kBF16, kBF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream); \
-        return sf ? launch_bn<MODE, BITS, kF32, kF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream)        \
-                  : launch_bn<MODE, BITS, kF16, kF16>(BN, a, A_rows, a_rows, a_cols, grid, pdl, stream);       \
-    }                                                                                                          \
+#define MNB_GEMM_TC_SLICE(NAME, MODE, BITS)                                                                     \
+    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, int G, const TcArgs& a, const void* A_rows,          \
+                     int64_t a_rows, int64_t a_cols, int grid, bool pdl, cudaStream_t stream) {                 \
+        const bool sf = scale_dtype == kF32;                                                                     \
+        if (a_dtype == kBF16)                                                                                    \
+            return sf ? launch_bn<MODE, BITS, kF32, kBF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream)  \
+                      : launch_bn<MODE, BITS, kBF16, kBF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream); \
+        return sf ? launch_bn<MODE, BITS, kF32, kF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream)       \
+                  : launch_bn<MODE, BITS, kF16, kF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream);      \
+    }                                                                                                            \
     cudaError_t NAME##_take_error(unsigned int* out) { return take_unit_error(out); }
 
 }  // namespace mnb

@@ -70,7 +70,8 @@ struct TcArgs {
     void* Y;
     int y_dtype;
     int64_t ld_y;          // row stride of the output in elements
-    int tiles_n, tiles_m, k_steps, stages;
+    int tiles_n, tiles_m, k_steps;
+    int stages, stages_w;  // activation ring and dequantised-weight ring depths
     uint32_t tmem_cols;
     // grouped (QMoE) launches: activation-row tiles {expert, first sorted row, rows, 0}
     const int4* mtiles;
