@@ -17,9 +17,9 @@
 // consecutive tiles.  One persistent CTA per SM walks the tiles.
 //
 // Warp roles (704 threads):
-//   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle), or
-//               (FC1) cp.async gathers of the routed tokens' rows into the
-//               same swizzled layout
+//   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle); in
+//               the grouped FC1 the routed tokens' rows were first copied
+//               into expert-sorted order, so the same tile loads serve
 //   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
 //   warps 2-17  dequant, two groups of 8 warps taking alternate K steps: two
 //               threads per weight row, one 32-code chunk each per K step; a
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&acc_empty[b], 4);
         }
         fence_barrier_init();
-        if (MODE == kModeGemm) prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_a);
     }
     if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
     grid_dependency_wait();
@@ -203,74 +203,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------- activation producer
-        if (MODE == kModeGemm) {
-            if (lane == 0) {
-                RingPos rp;
-                for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                    const Tile x = tile_of(a, t, UN);
-                    for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                        if (rp.round && !mbar_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
-                        mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
-#pragma unroll
-                        for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
-                            tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, ks * kBK, x.s0 + g * BN,
-                                        &full_a[rp.stage]);
-                    }
-                }
-            }
-        } else {
-            // FC1: gather the routed tokens' rows with cp.async; a stage is
-            // published (after a proxy fence) once its copies have landed,
-            // lagging the issue by up to S - 1 stages.  Lane l owns tile rows
-            // l, l+32, ...; their source rows are resolved once per tile.
-            constexpr int kRowsPerLane = UN >= 32 ? UN / 32 : 1;
-            const int lag = S - 1;
-            RingPos rp, pub;
-            int issued = 0, published = 0;
-            auto publish_one = [&]() {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full_a[pub.stage]);
-                pub.next(S);
-                ++published;
-            };
+        // TMA tiles of the activation rows (FC1: the routed tokens' rows, already
+        // copied into expert-sorted order), G sub-tiles of BN rows per K step.
+        if (lane == 0) {
+            RingPos rp;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
                 const Tile x = tile_of(a, t, UN);
-                const uint16_t* src[kRowsPerLane];
-                uint32_t rowoff[kRowsPerLane];
-                uint32_t rx[kRowsPerLane];
-#pragma unroll
-                for (int i = 0; i < kRowsPerLane; ++i) {
-                    const int j = lane + 32 * i;
-                    src[i] = (j < UN && j < x.cnt)
-                                 ? static_cast<const uint16_t*>(a.X) + int64_t(a.perm[x.s0 + j] / a.k) * a.K
-                                 : nullptr;
-                    rowoff[i] = static_cast<uint32_t>((j >> 3) * 1024 + (j & 7) * 128);
-                    rx[i] = static_cast<uint32_t>(j & 7);
-                }
                 for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                    if (rp.round && !warp_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
-                    uint8_t* dst = act + rp.stage * plan.act;
-                    const int64_t k0 = int64_t(ks) * kBK;
-                    const int64_t rem8 = (a.K - k0) / 8;  // K % 8 == 0
-                    const int nch = rem8 < 8 ? static_cast<int>(rem8) : 8;
+                    if (rp.round && !mbar_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+                    mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
 #pragma unroll
-                    for (int i = 0; i < kRowsPerLane; ++i) {
-                        if (src[i] == nullptr) continue;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            if (c < nch) cp_async16(dst + rowoff[i] + ((c ^ rx[i]) << 4), src[i] + k0 + 8 * c);
-                    }
-                    cp_async_commit();
-                    ++issued;
-                    if (issued - published > lag) {
-                        cp_async_wait<1>();  // all but the newest group have landed
-                        while (issued - published > 1) publish_one();
-                    }
+                    for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
+                        tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, ks * kBK, x.s0 + g * BN,
+                                    &full_a[rp.stage]);
                 }
             }
-            cp_async_wait<0>();
-            while (published < issued) publish_one();
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
@@ -572,12 +519,13 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     TcArgs a = in;
     CUtensorMap tmap;
     std::memset(&tmap, 0, sizeof tmap);
-    if (MODE == kModeGemm) {
+    {
+        // activations [a_rows, a_cols] in BN-row tiles
         auto encode = encode_fn();
         if (!encode) return cudaErrorNotSupported;
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a_cols), static_cast<cuuint64_t>(a_rows)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a_cols * 2)};
-        const cuuint32_t box[2] = {kBK, BN};
+        const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
         const cuuint32_t estr[2] = {1, 1};
         const CUresult cr = encode(&tmap, AT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                                    2, const_cast<void*>(A_rows), dims, strides, box, estr,
@@ -609,10 +557,10 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
 template <int MODE, int BITS, int ST, int AT>
 cudaError_t launch_bn(int BN, int G, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
                       bool pdl, cudaStream_t stream) {
-    if (G == 2) return launch_cfg<BITS, ST, AT, 256, 2, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
     if constexpr (MODE == kModeFc1) {
         return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);  // grouped: 256 rows
     } else {
+        if (G == 2) return launch_cfg<BITS, ST, AT, 256, 2, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
         switch (BN) {
             case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
             case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
