@@ -102,6 +102,13 @@ cudaError_t launch_route(const float* logits, int64_t T, int64_t E, int k, int n
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
 
+// The same stable permutation over many CTAs: chunk histograms (n_chunks x E
+// ints of scratch in `chunkc`, n_chunks = permute_chunks(T * k)), a scan, and
+// a scatter.  E <= 1024.
+int64_t permute_chunks(int64_t P);
+cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* chunkc, int32_t* counts,
+                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
+
 // Per-translation-unit device error words (read and cleared; 0 = none).
 cudaError_t gemv_take_error(unsigned int* out);
 cudaError_t qmoe_take_error(unsigned int* out);

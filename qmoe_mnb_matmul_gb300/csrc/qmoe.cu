@@ -45,7 +45,7 @@ constexpr int kDecodeRows2 = 8;     // FC2 rows per CTA (decode plan)
 __host__ __device__ inline int64_t a256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct Ws {
-    int64_t idx, wts, counts, offsets, perm, inv, tiles, ntiles, mtiles, nmtiles, h, o, total;
+    int64_t idx, wts, counts, offsets, perm, inv, chunkc, tiles, ntiles, mtiles, nmtiles, h, o, total;
 };
 
 __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
@@ -70,6 +70,7 @@ __host__ __device__ inline Ws ws_layout(int64_t T, int64_t H, int64_t I, int64_t
     w.offsets = off; off += a256((E + 1) * 4);
     w.perm = off; off += a256(P * 4);
     w.inv = off; off += a256(P * 4);
+    w.chunkc = off; off += a256(((P + 255) / 256) * E * 4);  // chunk histograms of the permutation
     w.tiles = off; off += a256(max_tiles(P, E) * 8);
     w.ntiles = off; off += 256;
     w.mtiles = off; off += a256(max_mtiles(P, E) * 16);
@@ -671,9 +672,10 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
     float* wts = reinterpret_cast<float*>(ws + L.wts);
     if ((e = launch_route(q.logits, q.T, q.E, q.k, q.normalize, idx, wts, stream)) != cudaSuccess) return e;
-    if ((e = launch_permute(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.counts),
-                            reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
-                            reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
+    if ((e = launch_permute_chunked(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.chunkc),
+                                    reinterpret_cast<int32_t*>(ws + L.counts),
+                                    reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
+                                    reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
         return e;
     if (use_tc(q)) {
         mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);

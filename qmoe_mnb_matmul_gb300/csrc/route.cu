@@ -137,7 +137,118 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
     }
 }
 
+// ------------------------------------------- permutation over many CTAs
+// Chunks of kPermChunk consecutive pairs.  perm_count_kernel: per-chunk expert
+// histograms.  perm_scan_kernel: per expert, the exclusive scan over chunks
+// (in place) and the totals; then the exclusive scan over experts (offsets).
+// perm_scatter_kernel: each warp ranks its 32 pairs among equal experts, the
+// warps of a chunk add the counts of earlier warps, and every pair lands at
+// offsets[e] + (earlier chunks) + (earlier warps) + (earlier lanes): stable.
+constexpr int kPermChunk = 256;
+
+__global__ void __launch_bounds__(kPermChunk) perm_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                                                                int32_t* __restrict__ chunkc) {
+    extern __shared__ int32_t hist[];
+    grid_dependency_wait();
+    for (int e = threadIdx.x; e < E; e += kPermChunk) hist[e] = 0;
+    __syncthreads();
+    const int64_t p = int64_t(blockIdx.x) * kPermChunk + threadIdx.x;
+    if (p < P) atomicAdd(&hist[idx[p]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kPermChunk) chunkc[int64_t(blockIdx.x) * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunkc, int n_chunks, int E,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+    __shared__ int32_t warp_sums[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependency_wait();
+    int32_t total = 0;
+    if (tid < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            const int32_t v = chunkc[int64_t(c) * E + tid];
+            chunkc[int64_t(c) * E + tid] = total;
+            total += v;
+        }
+    }
+    int32_t x = total;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t v = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        warp_sums[lane] = v;
+    }
+    __syncthreads();
+    const int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (tid < E) {
+        counts[tid] = total;
+        offsets[tid] = incl - total;
+        if (tid == E - 1) offsets[E] = incl;
+    }
+}
+
+__global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                                                                  const int32_t* __restrict__ chunkc,
+                                                                  const int32_t* __restrict__ offsets,
+                                                                  int32_t* __restrict__ perm,
+                                                                  int32_t* __restrict__ inv_perm) {
+    constexpr int kWarps = kPermChunk / 32;
+    extern __shared__ int32_t whist[];  // [kWarps][E]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependency_wait();
+    for (int i = tid; i < kWarps * E; i += kPermChunk) whist[i] = 0;
+    __syncthreads();
+    const int64_t p = int64_t(blockIdx.x) * kPermChunk + tid;
+    const int e = p < P ? idx[p] : -1 - lane;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) whist[warp * E + e] = __popc(same);
+    __syncthreads();
+    for (int x = tid; x < E; x += kPermChunk) {  // counts of earlier warps, per expert
+        int32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t v = whist[w * E + x];
+            whist[w * E + x] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) {
+        const int32_t slot = offsets[e] + chunkc[int64_t(blockIdx.x) * E + e] + whist[warp * E + e] + rank;
+        perm[slot] = static_cast<int32_t>(p);
+        if (inv_perm) inv_perm[p] = slot;
+    }
+}
+
 }  // namespace
+
+int64_t permute_chunks(int64_t P) { return (P + kPermChunk - 1) / kPermChunk; }
+
+cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* chunkc, int32_t* counts,
+                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream) {
+    const int64_t P = T * k;
+    const int64_t n = permute_chunks(P);
+    const size_t hist = size_t(E) * sizeof(int32_t);
+    perm_count_kernel<<<static_cast<unsigned>(n), kPermChunk, hist, stream>>>(idx, P, static_cast<int>(E), chunkc);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    perm_scan_kernel<<<1, 1024, 0, stream>>>(chunkc, static_cast<int>(n), static_cast<int>(E), counts, offsets);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t whist = size_t(kPermChunk / 32) * E * sizeof(int32_t);
+    perm_scatter_kernel<<<static_cast<unsigned>(n), kPermChunk, whist, stream>>>(idx, P, static_cast<int>(E), chunkc,
+                                                                                 offsets, perm, inv_perm);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
                                 uint8_t* codes, cudaStream_t stream) {
