@@ -107,6 +107,16 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
+// Named barrier of the four epilogue warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
 // Ring position of the i-th K step of this CTA: stage index and how many
 // times the ring has wrapped, advanced without divisions.
 struct RingPos {
@@ -164,6 +174,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     uint64_t* acc_full = full_a + 4 * kMaxStagesTC;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_holder + 1);  // the epilogue's wait gave up
     uint8_t* act = smem + plan.bars;
     uint8_t* wt = act + S * plan.act;
     uint8_t* pack = wt + SW * plan.w;
@@ -189,6 +200,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
+        *epi_fail = 0;
         fence_barrier_init();
         prefetch_tmap(&tmap_a);
     }
@@ -353,6 +365,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         RingPos rp;
         if (group) rp.next(SW);
         int cslot = 0;
+        uint32_t swo[4];  // this thread's four 16-byte slots of a weight tile row
+#pragma unroll
+        for (int c = 0; c < 4; ++c) swo[c] = sw128(r, 4 * h + c);
         int cur_t = -1;
         RowStream cs{nullptr, nullptr, 0, false};
         const uint8_t* zrow = nullptr;
@@ -414,7 +429,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             uint8_t* wdst = wt + rp.stage * plan.w;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(wdst + sw128(r, 4 * h + c)) =
+                *reinterpret_cast<uint4*>(wdst + swo[c]) =
                     make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             fence_proxy_async_smem();
             __syncwarp();
@@ -426,7 +441,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         cp_async_wait<0>();
     } else {
         // ----------------------------------------------------------- epilogue
+        // One lane polls the accumulator barrier; the four epilogue warps meet
+        // on a named barrier, so the others take no issue slots while waiting.
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const bool poller = warp == kEpilogueWarp0 && lane == 0;
         int tl = 0;
         for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
             const Tile x = tile_of(a, t, UN);
@@ -435,7 +453,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll 1
             for (int g = 0; g < G; ++g) {
                 const int slot = acc_slot<G>(tl, g);
-                if (!warp_wait(&acc_full[slot], uses & 1)) { failed = true; break; }
+                if (poller && !mbar_wait(&acc_full[slot], uses & 1)) *epi_fail = 1;
+                epilogue_sync();
+                if (*epi_fail) { failed = true; break; }
                 tc_fence_after();
                 const int cnt = x.cnt - g * BN;  // live activation rows of this sub-tile
                 const int64_t m0 = int64_t(x.s0) + g * BN;
@@ -444,6 +464,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     uint32_t v[32];
                     tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + slot * BN + c0, v);
                     tmem_ld_wait();
+                    // live columns of this 32-column chunk (a 16-column tile loads 32: the
+                    // upper 16 belong to the other accumulator)
+                    const int jn = min(32, min(BN - c0, cnt - c0));
                     if constexpr (MODE == kModeFc1) {
                         // rows 2p / 2p+1 hold gate / up of pair p: the even lane combines them
                         const int64_t p = x.n0 / 2 + (rr >> 1);
@@ -451,7 +474,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         for (int j = 0; j < 32; ++j) {
                             const float mine = __uint_as_float(v[j]);
                             const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                            if (!(lane & 1) && c0 + j < BN && c0 + j < cnt && p < a.I) {
+                            if (!(lane & 1) && j < jn && p < a.I) {
                                 const float hv = mine / (1.0f + expf(-mine)) * other;
                                 store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + p, hv);
                             }
@@ -459,11 +482,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     } else {
                         const int64_t n = x.n0 + rr;
                         if (n < a.rows) {
+                            if (a.y_dtype == AT) {  // 16-bit output: one strided pointer
+                                using OT = typename DType<AT>::T;
+                                OT* yp = static_cast<OT*>(a.Y) + (m0 + c0) * a.ld_y + n;
+                                const int64_t ld = a.ld_y;
+                                if (jn == 32) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                // a 16-column tile loads 32 columns: the upper 16 belong to the other accumulator
-                                if (c0 + j < BN && c0 + j < cnt)
-                                    store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + n, __uint_as_float(v[j]));
+                                    for (int j = 0; j < 32; ++j) yp[j * ld] = from_f32<OT>(__uint_as_float(v[j]));
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j)
+                                        if (j < jn) yp[j * ld] = from_f32<OT>(__uint_as_float(v[j]));
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < jn)
+                                        store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + n, __uint_as_float(v[j]));
                             }
                         }
                     }
