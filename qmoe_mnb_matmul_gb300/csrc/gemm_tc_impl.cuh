@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                             const float mine = __uint_as_float(v[j]);
                             const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
                             if (!(lane & 1) && j < jn && p < a.I) {
-                                const float hv = mine / (1.0f + expf(-mine)) * other;
+                                // h is rounded to the 16-bit activation type next, so the fast
+                                // exponential and division (a few ulp of fp32) do not show
+                                const float hv = __fdividef(mine, 1.0f + __expf(-mine)) * other;
                                 store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + p, hv);
                             }
                         }
