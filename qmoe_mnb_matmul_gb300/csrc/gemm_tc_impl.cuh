@@ -468,17 +468,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     // upper 16 belong to the other accumulator)
                     const int jn = min(32, min(BN - c0, cnt - c0));
                     if constexpr (MODE == kModeFc1) {
-                        // rows 2p / 2p+1 hold gate / up of pair p: the even lane combines them
+                        // Lanes 2i / 2i+1 hold the gate / up rows of pair p: the even lane
+                        // makes h for the even columns, the odd lane for the odd ones,
+                        // each trading the value the other needs in one shuffle.
                         const int64_t p = x.n0 / 2 + (rr >> 1);
+                        const int odd = lane & 1;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float mine = __uint_as_float(v[j]);
-                            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                            if (!(lane & 1) && j < jn && p < a.I) {
+                        for (int j = 0; j < 32; j += 2) {
+                            const float send = __uint_as_float(v[j + 1 - odd]);  // even: gate of j+1; odd: up of j
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            const float gate = odd ? recv : __uint_as_float(v[j]);
+                            const float up = odd ? __uint_as_float(v[j + 1]) : recv;
+                            const int col = j + odd;
+                            if (col < jn && p < a.I) {
                                 // h is rounded to the 16-bit activation type next, so the fast
                                 // exponential and division (a few ulp of fp32) do not show
-                                const float hv = __fdividef(mine, 1.0f + __expf(-mine)) * other;
-                                store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + p, hv);
+                                const float hv = __fdividef(gate, 1.0f + __expf(-gate)) * up;
+                                store_from_f32(a.Y, a.y_dtype, (m0 + c0 + col) * a.ld_y + p, hv);
                             }
                         }
                     } else {
