@@ -90,8 +90,12 @@ typedef struct CUstream_st* mnb_stream_t;
 
 /* ------------------------------------------------------------ MatMulNBits */
 
-/* Bytes of device workspace mnb_matmul needs for this problem (0 = none, in
- * which case workspace may be NULL).  The bound depends only on the arguments. */
+/* Bytes of device workspace mnb_matmul can use for this problem (0 = none, in
+ * which case workspace may be NULL).  The bound depends only on the arguments.
+ * Non-zero for tensor-core problems whose output tiles cannot fill the GPU
+ * (small M, few output columns): K is then split across CTAs and the fp32
+ * partial sums go to the workspace before one reduction.  A call given less
+ * (or NULL) splits K less, or not at all: same result, slower. */
 mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, int block_size,
                                      mnb_dtype a_dtype, size_t* bytes);
 
@@ -102,7 +106,9 @@ mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, 
  * Accumulation is fp32; the dequantised weight is formed in fp32 (SIMT paths)
  * or rounded to bf16/fp16 in shared memory before a tensor-core contraction
  * (M >= 16 with f16/bf16 activations).  Y is written in y_dtype with
- * round-to-nearest-even. */
+ * round-to-nearest-even.  `workspace` (16-byte aligned, see
+ * mnb_matmul_workspace_size) holds split-K partial sums; the split changes the
+ * order of the fp32 additions, not the rounding points. */
 mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
                       const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
                       const uint8_t* zero_points, int64_t N, int bits, int block_size, void* Y,

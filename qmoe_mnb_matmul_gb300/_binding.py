@@ -141,6 +141,11 @@ def mnb_matmul(A, B_packed, scales, zero_points, N, bits, block_size, Y, workspa
     a_dtype = _dtype_code(A) if a_dtype is None else a_dtype
     scale_dtype = _dtype_code(scales) if scale_dtype is None else scale_dtype
     y_dtype = _dtype_code(Y) if y_dtype is None else y_dtype
+    if workspace is None:  # the workspace the library can use (split-K partial sums), if any
+        need = mnb_matmul_workspace_size(M, K, N, bits, block_size, a_dtype)
+        if need:
+            import torch
+            workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
     ws_bytes = 0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size()
     st = load_library().mnb_matmul(_ptr(A), a_dtype, M, K, _ptr(B_packed), _ptr(scales), scale_dtype,
                                    _ptr(zero_points), N, bits, block_size, _ptr(Y), y_dtype, _ptr(workspace),

@@ -45,7 +45,43 @@ TcShape pick_shape(int64_t M, int64_t N, int sm_count) {
     return best;
 }
 
+// K split: when the output tiles cannot give every SM a tile, the K steps of
+// each tile are divided among up to 16 CTAs (an equal share each, at least 4
+// steps), their fp32 partial sums go to the workspace, and a second kernel adds
+// them in split order.
+struct TcPlanK {
+    TcShape sh;
+    int splits;
+};
+TcPlanK plan_tc(int64_t M, int64_t K, int64_t N, int sm_count) {
+    TcPlanK p{pick_shape(M, N, sm_count), 1};
+    const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(p.sh.BN) * p.sh.G);
+    const int64_t ksteps = cdiv<int64_t>(K, kBK);
+    if (tiles * 2 > sm_count) return p;
+    for (int s = 16; s >= 2; --s) {
+        if (ksteps % s != 0 || ksteps / s < 4 || tiles * s > int64_t(sm_count) * 5 / 4) continue;
+        p.splits = s;
+        break;
+    }
+    return p;
+}
+
+// Y[i] = sum over splits s of P[s][i] (in split order), rounded once to Y's dtype.
+__global__ void splitk_reduce_kernel(const float* __restrict__ P, int splits, int64_t MN, void* Y, int y_dtype) {
+    grid_dependency_wait();
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < MN; i += int64_t(gridDim.x) * blockDim.x) {
+        float acc = P[i];
+        for (int s = 1; s < splits; ++s) acc += P[s * MN + i];
+        store_from_f32(Y, y_dtype, i, acc);
+    }
+}
+
 }  // namespace
+
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t K, int64_t N, int sm_count) {
+    const TcPlanK p = plan_tc(M, K, N, sm_count);
+    return p.splits > 1 ? size_t(p.splits) * size_t(M) * size_t(N) * sizeof(float) : 0;
+}
 
 cudaError_t gemm_tc_take_error(unsigned int* out) {
     unsigned int first = 0;
@@ -61,7 +97,14 @@ cudaError_t gemm_tc_take_error(unsigned int* out) {
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
-    const TcShape sh = pick_shape(g.M, g.N, sm_count);
+    TcPlanK plan = plan_tc(g.M, g.K, g.N, sm_count);
+    const int64_t ksteps = cdiv<int64_t>(g.K, kBK);
+    const size_t per_split = size_t(g.M) * size_t(g.N) * sizeof(float);
+    // fewer splits when the caller's workspace holds fewer partial sums (none: one CTA per tile)
+    while (plan.splits > 1 &&
+           (g.workspace == nullptr || g.workspace_bytes < per_split * plan.splits || ksteps % plan.splits != 0))
+        --plan.splits;
+    const TcShape sh = plan.sh;
     TcArgs a = {};
     a.M = g.M;
     a.K = g.K;
@@ -78,10 +121,18 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     a.ld_y = g.N;
     a.tiles_n = static_cast<int>(cdiv<int64_t>(g.N, kBW));
     a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(sh.BN) * sh.G));
-    a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK));
-    const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m, sm_count));
+    a.splits = plan.splits;
+    a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK)) / plan.splits;
+    a.partials = plan.splits > 1 ? static_cast<float*>(g.workspace) : nullptr;
+    const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m * a.splits, sm_count));
     auto fn = g.bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3;
-    return fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
+    cudaError_t e = fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    const int64_t MN = g.M * g.N;
+    const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(MN, 256), int64_t(sm_count) * 8);
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.partials, plan.splits, MN, g.Y,
+                                                                           g.y_dtype);
+    return cudaGetLastError();
 }
 
 // Grouped (QMoE) tiles: 256 routed rows of one expert.

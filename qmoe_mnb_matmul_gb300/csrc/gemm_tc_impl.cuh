@@ -127,9 +127,10 @@ struct RingPos {
     }
 };
 
-// Tile t -> (expert, first activation row, rows, first weight row).
+// Tile t -> (expert, first activation row, rows, first weight row, split of K
+// and its first K step).
 struct Tile {
-    int e, s0, cnt, n0;
+    int e, s0, cnt, n0, split, ks0;
 };
 
 __device__ __forceinline__ Tile tile_of(const TcArgs& a, int t, int BN) {
@@ -141,7 +142,12 @@ __device__ __forceinline__ Tile tile_of(const TcArgs& a, int t, int BN) {
         x.s0 = mt.y;
         x.cnt = mt.z;
         x.n0 = (t - j * a.tiles_n) * kBW;
+        x.split = 0;
+        x.ks0 = 0;
     } else {
+        x.split = t % a.splits;  // splits of one output tile run on neighbouring CTAs
+        t /= a.splits;
+        x.ks0 = x.split * a.k_steps;
         const int nt = t / a.tiles_m;
         const int mtile = t - nt * a.tiles_m;
         x.e = 0;
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const int n_tiles = a.mtiles ? *a.n_mtiles * a.tiles_n : a.tiles_n * a.tiles_m;
+    const int n_tiles = a.mtiles ? *a.n_mtiles * a.tiles_n : a.tiles_n * a.tiles_m * a.splits;
     bool failed = false;
 
     if (warp == 0) {
@@ -226,8 +232,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
 #pragma unroll
                     for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
-                        tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, ks * kBK, x.s0 + g * BN,
-                                    &full_a[rp.stage]);
+                        tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, (x.ks0 + ks) * kBK,
+                                    x.s0 + g * BN, &full_a[rp.stage]);
                 }
             }
         }
@@ -288,9 +294,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         // One tile's source stream for this thread: packed bytes of chunk h of
         // its weight row, that expert's scales, and the row's first scale index.
         struct RowStream {
-            const uint8_t* w;
+            const uint8_t* w;  // packed bytes of chunk h at the tile's first K step
             const uint8_t* s;
             int64_t si0;
+            int ks0;           // the tile's first K step (split of K)
             bool ok;
         };
         auto stream_of = [&](const Tile& x) -> RowStream {
@@ -303,9 +310,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             }
             RowStream st;
             st.ok = wr >= 0;
-            st.w = a.B + x.e * a.w_expert_stride + (st.ok ? wr : 0) * a.row_bytes + h * kCB;
+            st.w = a.B + x.e * a.w_expert_stride + (st.ok ? wr : 0) * a.row_bytes + h * kCB +
+                   int64_t(x.ks0) * kStepBytes;
             st.s = static_cast<const uint8_t*>(a.scales) + x.e * a.s_expert_stride;
             st.si0 = (st.ok ? wr : 0) * nb;
+            st.ks0 = x.ks0;
             return st;
         };
         // This group's K steps, in order: the CTA's tiles t = blockIdx.x + j * gridDim.x,
@@ -326,9 +335,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             pc.t += gridDim.x;
         }
         int pslot = 0;
-        RowStream ps = pc.t < n_tiles ? stream_of(tile_of(a, pc.t, UN)) : RowStream{nullptr, nullptr, 0, false};
+        RowStream ps = pc.t < n_tiles ? stream_of(tile_of(a, pc.t, UN)) : RowStream{nullptr, nullptr, 0, 0, false};
         auto issue = [&]() {
-            if (pc.t < n_tiles && ps.ok && pc.ks < live_steps) {
+            if (pc.t < n_tiles && ps.ok && ps.ks0 + pc.ks < live_steps) {
                 uint8_t* dst = gpack + ((pslot * 2 + h) * kBW + r) * kCB;
                 const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
                 if constexpr (BITS == 4) {
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
                     for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + 4 * q);
                 }
-                const int64_t si = ps.si0 + ((int64_t(pc.ks) * kBK + 32 * h) >> bs_shift);
+                const int64_t si = ps.si0 + ((int64_t(ps.ks0 + pc.ks) * kBK + 32 * h) >> bs_shift);
                 uint32_t* sdst = reinterpret_cast<uint32_t*>(gscl + ((pslot * 2 + h) * kBW + r) * 4);
                 if (ST == kF32) {
                     cp_async4(sdst, reinterpret_cast<const float*>(ps.s) + si);
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
         for (int c = 0; c < 4; ++c) swo[c] = sw128(r, 4 * h + c);
         int cur_t = -1;
-        RowStream cs{nullptr, nullptr, 0, false};
+        RowStream cs{nullptr, nullptr, 0, 0, false};
         const uint8_t* zrow = nullptr;
         while (cc.t < n_tiles && !failed) {
             if (cc.t != cur_t) {
@@ -378,7 +387,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 cs = stream_of(x);
                 zrow = (a.zp && cs.ok) ? a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes : nullptr;
             }
-            const int ks = cc.ks;
+            const int ks = cs.ks0 + cc.ks;  // absolute K step
             issue();
             cp_async_wait<kPack - 1>();
             if (rp.round && !warp_wait(&empty_w[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
@@ -489,7 +498,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         }
                     } else {
                         const int64_t n = x.n0 + rr;
-                        if (n < a.rows) {
+                        if (n < a.rows && a.splits > 1) {  // fp32 partial sums of this split of K
+                            float* pp = a.partials + (int64_t(x.split) * a.M + m0 + c0) * a.ld_y + n;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < jn) pp[j * a.ld_y] = __uint_as_float(v[j]);
+                        } else if (n < a.rows) {
                             if (a.y_dtype == AT) {  // 16-bit output: one strided pointer
                                 using OT = typename DType<AT>::T;
                                 OT* yp = static_cast<OT*>(a.Y) + (m0 + c0) * a.ld_y + n;

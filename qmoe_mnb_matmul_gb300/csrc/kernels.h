@@ -54,8 +54,14 @@ struct GemmTcArgs {
     int zp_row_bytes;
     void* Y;
     int y_dtype;
+    void* workspace;        // split-K partial sums (may be null: no split)
+    size_t workspace_bytes;
 };
 cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream);
+
+// Workspace the tensor-core GEMM uses for this problem: fp32 partial sums when
+// the output tiles alone cannot fill the GPU and K is split (0 otherwise).
+size_t gemm_tc_workspace_bytes(int64_t M, int64_t K, int64_t N, int sm_count);
 
 // Kernel-side arguments of the tensor-core GEMM, shared with the grouped QMoE
 // launches.  Weight matrix of an expert: `rows` rows of K codes.
@@ -70,7 +76,9 @@ struct TcArgs {
     void* Y;
     int y_dtype;
     int64_t ld_y;          // row stride of the output in elements
-    int tiles_n, tiles_m, k_steps;
+    int tiles_n, tiles_m, k_steps;  // k_steps: K steps of one tile (of one split of K)
+    int splits;                     // dense: K split in this many parts (partials, then a reduction)
+    float* partials;                // [splits][M][N] fp32 when splits > 1
     int stages, stages_w;  // activation ring and dequantised-weight ring depths
     uint32_t tmem_cols;
     // grouped (QMoE) launches: activation-row tiles {expert, first sorted row, rows, 0}

@@ -16,7 +16,7 @@ namespace mnb {
 namespace {
 
 // Smallest M routed to the tensor-core GEMM (fp16/bf16 activations only).
-constexpr int64_t kTcMinRows = 8;
+constexpr int64_t kTcMinRows = 16;
 
 bool valid_dtype(int d) { return d == MNB_F32 || d == MNB_F16 || d == MNB_BF16; }
 bool valid_bits(int b) { return b == 3 || b == 4; }
@@ -111,6 +111,10 @@ mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, 
     if (M < 1 || K < 1 || N < 1 || !valid_dtype(a_dtype)) return MNB_ERR_INVALID_ARG;
     if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     *bytes = 0;
+    // The tensor-core path splits K when its output tiles cannot fill the GPU;
+    // the size is planned for a 152-SM GB300 so that it depends only on the
+    // arguments (a call given less workspace splits less, or not at all).
+    if (a_dtype != MNB_F32 && M >= kTcMinRows && K % 8 == 0) *bytes = gemm_tc_workspace_bytes(M, K, N, 152);
     return MNB_OK;
 }
 
@@ -118,8 +122,6 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
                       const void* scales, mnb_dtype scale_dtype, const uint8_t* zero_points, int64_t N,
                       int bits, int block_size, void* Y, mnb_dtype y_dtype, void* workspace,
                       size_t workspace_bytes, mnb_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (!A || !B_packed || !scales || !Y) return MNB_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || N < 1) return MNB_ERR_INVALID_ARG;
     if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
@@ -157,6 +159,8 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
         g.zp_row_bytes = static_cast<int>(pb.zp_row);
         g.Y = Y;
         g.y_dtype = y_dtype;
+        g.workspace = aligned(workspace, 16) ? workspace : nullptr;
+        g.workspace_bytes = g.workspace ? workspace_bytes : 0;
         return from_cuda(launch_gemm_tc(g, scale_dtype, sms, pdl_enabled(), st));
     }
     if (gemv_smem_bytes(M, K, bits, block_size, scale_dtype) == 0) return MNB_ERR_UNSUPPORTED;

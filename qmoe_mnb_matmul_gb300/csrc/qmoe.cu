@@ -681,6 +681,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         TcArgs a = {};
+        a.splits = 1;
         a.mtiles = reinterpret_cast<const int4*>(ws + L.mtiles);
         a.n_mtiles = reinterpret_cast<const int*>(ws + L.nmtiles);
         a.bs = q.bs;

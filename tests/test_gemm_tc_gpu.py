@@ -1,5 +1,5 @@
 """GPU parity of mnb_matmul's tensor-core path (tcgen05, fp16/bf16 activations,
-M >= 8) against the oracle: every output of a sample of activation rows."""
+M >= 16) against the oracle: every output of a sample of activation rows."""
 import os
 import zlib
 
@@ -134,3 +134,31 @@ def test_rounding_point_is_the_16bit_weight(bits, bs):
     rel = lambda d: float(np.sqrt(np.mean(d * d)) / np.sqrt(np.mean(exact * exact)))
     assert rel(y - rne) <= 0.2 * rel(rne - exact)
     assert rel(y - rz) >= 1.0 * rel(rne - exact)
+
+
+@pytest.mark.parametrize("M,K,N,bits,bs", [(16, 2048, 4096, 4, 32), (16, 6144, 2048, 4, 32), (32, 2080, 2048, 3, 32),
+                                           (64, 2048, 1024, 3, 64), (24, 2304, 640, 4, 128)])
+def test_split_k_against_unsplit(M, K, N, bits, bs):
+    """Output tiles too few to fill the GPU: K is split across CTAs (fp32 partial sums in
+    the workspace, then a reduction).  Checked against the oracle, and against the same
+    call with no workspace (no split): equal up to the order of the fp32 additions."""
+    g = wl.rng(seed("splitk", M, K, N, bits, bs))
+    packed, scales, zp = wl.quantized_weight(g, N, K, bits, bs, "bf16", bits == 3)
+    A = wl.normal(g, (M, K), "bf16")
+    need = mnb.mnb_matmul_workspace_size(M, K, N, bits, bs, mnb.BF16)
+    assert need > 0, "these shapes leave SMs idle without a split"
+    A_d, B_d, S_d = to_dev(A, "bf16"), to_dev(packed), to_dev(scales, "bf16")
+    Z_d = None if zp is None else to_dev(zp)
+    ys = []
+    for ws in (torch.empty(need, dtype=torch.uint8, device="cuda"), torch.empty(0, dtype=torch.uint8, device="cuda")):
+        Y, full = empty_guarded(M * N, "f32")
+        mnb.mnb_matmul(A_d, B_d, S_d, Z_d, N, bits, bs, Y, ws, K=K, M=M)
+        torch.cuda.synchronize()
+        assert guards_intact(full), "write outside Y"
+        assert mnb.mnb_get_last_device_error() == 0
+        ys.append(to_f64(Y).reshape(M, N))
+    ref = oracle.mnb_matmul(A, "bf16", packed, scales, "bf16", zp, N, K, bits, bs, threads=THREADS)
+    assert_close(ys[0], ref, "bf16")
+    assert_close(ys[1], ref, "bf16")
+    rel = np.max(np.abs(ys[0] - ys[1])) / max(np.max(np.abs(ys[1])), 1e-30)
+    assert rel <= 1e-5, rel
