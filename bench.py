@@ -264,13 +264,41 @@ def event_time_us(torch, stream, fn, reps, warmup=3):
 
 def other_rows(torch, mnb, dev):
     """The rest of the hot path, each against its own roofline: the tensor-core
-    prefill GEMM (M=2048, bf16) and one Qwen3-30B-A3B-shaped QMoE layer at
-    decode (T=1, CUDA graph over 16 distinct layers) and prefill (T=4096)."""
+    GEMM at small M (M=16, HBM-bound) and prefill (M=2048, bf16), and one
+    Qwen3-30B-A3B-shaped QMoE layer at decode (T=1, CUDA graph over 16 distinct
+    layers) and prefill (T=4096)."""
     gen = torch.Generator().manual_seed(7)
     stream = torch.cuda.Stream(device=dev)
     hbm, hbm_kind = peaks()
     tc, tc_kind = tc_peak()
     rows = {}
+    # a5, small M (memory-bound): the qkv projection at M=16 through the K-split tensor-core path,
+    # 16 distinct weight copies replayed in one graph
+    M, K, N = 16, 2048, 4096
+    Bs = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev) for _ in range(16)]
+    Ss = [(torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev) for _ in range(16)]
+    A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, mnb.mnb_matmul_workspace_size(M, K, N, BITS, BS, mnb.BF16)), dtype=torch.uint8,
+                     device=dev)
+    with torch.cuda.stream(stream):
+        mnb.mnb_matmul(A, Bs[0], Ss[0], None, N, BITS, BS, Y, ws, stream=stream)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        gr.capture_begin()
+        for i in range(16):
+            mnb.mnb_matmul(A, Bs[i], Ss[i], None, N, BITS, BS, Y, ws, stream=stream)
+        gr.capture_end()
+    us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=30)
+    us, p10, p90 = us / 16, p10 / 16, p90 / 16
+    nbytes = proj_bytes(K, N) - K * 4 - N * 4 + M * K * 2 + M * N * 2
+    rows["prefill_gemm_qkv_m16"] = {
+        "kernel": "gemm_tc (tcgen05, K split across CTAs) + split-K reduction",
+        "shape": f"M={M} K={K} N={N} INT4 bs32 bf16 A/Y, fp32 scales, 16 distinct weight copies in one graph",
+        "us": us, "us_p10_p90": [p10, p90], "achieved": nbytes / (us * 1e-6) / 1e9, "unit": "GB/s", "peak": hbm,
+        "frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm", "peak_source": f"{hbm_kind} hbm_gbs"}
+    del Bs, Ss, A, Y, ws
     # a5: prefill GEMM on the tensor cores
     for name, K, N in (("gate", 2048, 6144), ("lm_head", 2048, 151936)):
         M = 2048
