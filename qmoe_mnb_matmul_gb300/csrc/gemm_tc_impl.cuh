@@ -21,9 +21,9 @@
 //               the grouped FC1 the routed tokens' rows were first copied
 //               into expert-sorted order, so the same tile loads serve
 //   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
-//   warps 2-17  dequant, two groups of 8 warps taking alternate K steps: two
-//               threads per weight row, one 32-code chunk each per K step; a
-//               private cp.async ring of packed bytes and scales; codes ->
+//   warps 2-17  dequant, four groups of 4 warps taking every fourth K step:
+//               one thread per weight row, both 32-code chunks of the K step;
+//               a private cp.async ring of packed bytes and scales; codes ->
 //               s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
 //   warps 18-21 epilogue: tcgen05.ld of the accumulators -> output dtype
 //               (FC1: SwiGLU of lane pairs) -> masked stores
@@ -54,10 +54,11 @@ using namespace gemv;
 
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kBW = 128;    // weight rows per tile (MMA M)
-constexpr int kPack = 4;    // depth of each dequant thread's cp.async ring
-// Two groups of 8 dequantisation warps take alternate K steps, so each group
-// has two MMA steps' time for its 128 x 64 weight slice.
-constexpr int kDequantWarp0 = 2, kDequantWarps = 8, kDequantGroups = 2;
+constexpr int kPack = 2;    // depth of each dequant thread's cp.async ring (own K steps)
+// Four groups of 4 dequantisation warps take every fourth K step: one thread
+// per weight row makes all 64 codes of the row's K step, and each group has
+// four MMA steps' time for its 128 x 64 weight slice.
+constexpr int kDequantWarp0 = 2, kDequantWarps = 4, kDequantGroups = 4;
 constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;
 constexpr int kThreadsTC = (kEpilogueWarp0 + 4) * 32;
 constexpr int kMaxStagesTC = 8;
@@ -73,8 +74,8 @@ __host__ __device__ inline TcPlan tc_plan(int BN, int G, int stages, int stages_
     p.bars = 1024;                                           // barriers and the TMEM address
     p.act = int64_t(G) * BN * 128;                           // activations of one stage (G sub-tiles)
     p.w = int64_t(kBW) * 128;                                // dequantised weights of one stage
-    p.pack = int64_t(kDequantGroups) * kPack * 2 * kBW * (bits == 4 ? 16 : 12);
-    p.scl = int64_t(kDequantGroups) * kPack * 2 * kBW * 4;
+    p.pack = int64_t(kDequantGroups) * kPack * 2 * kBW * (bits == 4 ? 16 : 12);  // [slot][half][row][chunk]
+    p.scl = int64_t(kDequantGroups) * kPack * kBW * 8;                          // [slot][row][2 words]
     p.total = p.bars + int64_t(stages) * p.act + int64_t(stages_w) * p.w + p.pack + p.scl;
     return p;
 }
@@ -276,10 +277,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequant
-        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes global K steps = group (mod 2)
-        const int dq = tid - (kDequantWarp0 + group * kDequantWarps) * 32;
-        const int r = dq & (kBW - 1);  // weight row of the tile
-        const int h = dq >> 7;         // which 32-code chunk of the K step
+        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes global K steps = group (mod 4)
+        const int r = tid - (kDequantWarp0 + group * kDequantWarps) * 32;  // weight row of the tile
         constexpr int kCB = BITS == 4 ? 16 : 12;  // packed bytes per 32-code chunk
         constexpr int kStepBytes = 2 * kCB;       // packed bytes of a row per K step
         constexpr int kZ = 1 << (BITS - 1);
@@ -288,13 +287,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         const int nb = a.nb, bs_shift = __ffs(a.bs) - 1;
         const int64_t kcodes = int64_t(nb) * a.bs;  // codes stored per row
         const int64_t n_scales = a.rows * nb;
-        // K steps whose chunk h holds stored codes (later chunks read nothing)
-        const int64_t live64 = (kcodes - 32 * h + kBK - 1) / kBK;
-        const int live_steps = live64 > 0 ? static_cast<int>(live64) : 0;
-        // One tile's source stream for this thread: packed bytes of chunk h of
-        // its weight row, that expert's scales, and the row's first scale index.
+        // One tile's source stream for this thread: packed bytes of its weight
+        // row, that expert's scales, and the row's first scale index.
         struct RowStream {
-            const uint8_t* w;  // packed bytes of chunk h at the tile's first K step
+            const uint8_t* w;  // packed bytes at the tile's first K step
             const uint8_t* s;
             int64_t si0;
             int ks0;           // the tile's first K step (split of K)
@@ -310,19 +306,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             }
             RowStream st;
             st.ok = wr >= 0;
-            st.w = a.B + x.e * a.w_expert_stride + (st.ok ? wr : 0) * a.row_bytes + h * kCB +
-                   int64_t(x.ks0) * kStepBytes;
+            st.w = a.B + x.e * a.w_expert_stride + (st.ok ? wr : 0) * a.row_bytes + int64_t(x.ks0) * kStepBytes;
             st.s = static_cast<const uint8_t*>(a.scales) + x.e * a.s_expert_stride;
             st.si0 = (st.ok ? wr : 0) * nb;
             st.ks0 = x.ks0;
             return st;
         };
         // This group's K steps, in order: the CTA's tiles t = blockIdx.x + j * gridDim.x,
-        // each with ksteps steps, numbered globally; the group takes every second one.
+        // each with ksteps steps, numbered globally; the group takes every fourth one.
         struct Cursor {
             int t, ks;
         };
-        auto advance = [&](Cursor& c) {  // two global steps on
+        auto advance = [&](Cursor& c) {  // kDequantGroups global steps on
             c.ks += kDequantGroups;
             while (c.ks >= ksteps && c.t < n_tiles) {
                 c.ks -= ksteps;
@@ -336,25 +331,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         }
         int pslot = 0;
         RowStream ps = pc.t < n_tiles ? stream_of(tile_of(a, pc.t, UN)) : RowStream{nullptr, nullptr, 0, 0, false};
+        // one half-precision scale: the 4-byte word that holds it (the last scale
+        // of the array alone, where its word would run past the end)
+        auto copy_scale_word = [&](uint32_t* dst, const uint8_t* base, int64_t si) {
+            if (ST == kF32) {
+                cp_async4(dst, reinterpret_cast<const float*>(base) + si);
+            } else if ((si | 1) < n_scales) {
+                cp_async4(dst, reinterpret_cast<const uint32_t*>(base) + (si >> 1));
+            } else {
+                *dst = reinterpret_cast<const uint16_t*>(base)[si];
+            }
+        };
         auto issue = [&]() {
-            if (pc.t < n_tiles && ps.ok && ps.ks0 + pc.ks < live_steps) {
-                uint8_t* dst = gpack + ((pslot * 2 + h) * kBW + r) * kCB;
+            const int64_t k0 = int64_t(ps.ks0 + pc.ks) * kBK;  // first code of this K step
+            if (pc.t < n_tiles && ps.ok && k0 < kcodes) {
                 const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
-                if constexpr (BITS == 4) {
-                    cp_async16(dst, src);
-                } else {
+                const bool two = k0 + 32 < kcodes;  // the second chunk holds stored codes
 #pragma unroll
-                    for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + 4 * q);
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (hh == 1 && !two) break;
+                    uint8_t* dst = gpack + ((pslot * 2 + hh) * kBW + r) * kCB;
+                    if constexpr (BITS == 4) {
+                        cp_async16(dst, src + hh * kCB);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + hh * kCB + 4 * q);
+                    }
                 }
-                const int64_t si = ps.si0 + ((int64_t(ps.ks0 + pc.ks) * kBK + 32 * h) >> bs_shift);
-                uint32_t* sdst = reinterpret_cast<uint32_t*>(gscl + ((pslot * 2 + h) * kBW + r) * 4);
-                if (ST == kF32) {
-                    cp_async4(sdst, reinterpret_cast<const float*>(ps.s) + si);
-                } else if ((si | 1) < n_scales) {
-                    cp_async4(sdst, reinterpret_cast<const uint32_t*>(ps.s) + (si >> 1));
-                } else {  // the last half-precision scale: its 4-byte word would run past the array
-                    *sdst = reinterpret_cast<const uint16_t*>(ps.s)[si];
-                }
+                uint32_t* sdst = reinterpret_cast<uint32_t*>(gscl + (pslot * kBW + r) * 8);
+                const int64_t i0 = ps.si0 + (k0 >> bs_shift), i1 = ps.si0 + ((k0 + 32) >> bs_shift);
+                copy_scale_word(sdst, ps.s, i0);
+                if (two && (ST == kF32 ? i1 != i0 : (i1 >> 1) != (i0 >> 1))) copy_scale_word(sdst + 1, ps.s, i1);
             }
             cp_async_commit();
             if (++pslot == kPack) pslot = 0;
@@ -372,11 +379,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             cc.t += gridDim.x;
         }
         RingPos rp;
-        if (group) rp.next(SW);
+        for (int i = 0; i < group; ++i) rp.next(SW);
         int cslot = 0;
-        uint32_t swo[4];  // this thread's four 16-byte slots of a weight tile row
+        uint32_t swo[8];  // this thread's eight 16-byte slots of a weight tile row
 #pragma unroll
-        for (int c = 0; c < 4; ++c) swo[c] = sw128(r, 4 * h + c);
+        for (int c = 0; c < 8; ++c) swo[c] = sw128(r, c);
         int cur_t = -1;
         RowStream cs{nullptr, nullptr, 0, 0, false};
         const uint8_t* zrow = nullptr;
@@ -391,60 +398,67 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             issue();
             cp_async_wait<kPack - 1>();
             if (rp.round && !warp_wait(&empty_w[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
-            const bool live = cs.ok && ks < live_steps;
-            uint32_t w[BITS];
-            float sc = 0.f, z = float(kZ);
-            if (live) {
-                const uint8_t* src = gpack + ((cslot * 2 + h) * kBW + r) * kCB;
-                if constexpr (BITS == 4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(src);
-                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            uint8_t* wdst = wt + rp.stage * plan.w;
+            const uint32_t* swd = reinterpret_cast<const uint32_t*>(gscl + (cslot * kBW + r) * 8);
+            const int64_t i0 = cs.si0 + ((int64_t(ks) * kBK) >> bs_shift);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int64_t kc = int64_t(ks) * kBK + 32 * hh;  // first code of this chunk
+                const bool live = cs.ok && kc < kcodes;
+                uint32_t w[BITS];
+                float sc = 0.f, z = float(kZ);
+                if (live) {
+                    const uint8_t* src = gpack + ((cslot * 2 + hh) * kBW + r) * kCB;
+                    if constexpr (BITS == 4) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(src);
+                        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
+                    }
+                    const int64_t si = cs.si0 + (kc >> bs_shift);
+                    // word 0 holds scale i0; scale si is either in it or in word 1
+                    const bool in0 = ST == kF32 ? si == i0 : (si >> 1) == (i0 >> 1);
+                    sc = scale_from_word<ST>(swd[in0 ? 0 : 1], si);
+                    if (zrow) z = float(zero_point_code<BITS>(zrow, static_cast<int>(kc >> bs_shift)));
                 } else {
 #pragma unroll
-                    for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
+                    for (int q = 0; q < BITS; ++q) w[q] = 0;
                 }
-                const int b = (ks * kBK + 32 * h) >> bs_shift;
-                sc = scale_from_word<ST>(*reinterpret_cast<const uint32_t*>(gscl + ((cslot * 2 + h) * kBW + r) * 4),
-                                         cs.si0 + b);
-                if (zrow) z = float(zero_point_code<BITS>(zrow, b));
-            } else {
+                // w = s (q - z) = f * s 2^(24-p) - s (2^(23-p) + z), one fp32 rounding per value;
+                // the pre-scale depends only on the code's position class p
+                constexpr int kCls = BITS == 4 ? 2 : 3;
+                float mc[kCls], ac[kCls];
 #pragma unroll
-                for (int q = 0; q < BITS; ++q) w[q] = 0;
+                for (int c = 0; c < kCls; ++c) {
+                    const int p = code_pos<BITS>(c);
+                    mc[c] = sc * float(1u << (24 - p));
+                    ac[c] = -sc * (float(1u << (23 - p)) + z);
+                }
+                uint32_t outw[16];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    float2 f01, f23;
+                    chunk_codes4<BITS>(w, g, f01, f23);
+                    const int j = 4 * g;
+                    const float2 v01 = ffma2(f01, make_float2(mc[j % kCls], mc[(j + 1) % kCls]),
+                                             make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
+                    const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
+                                             make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
+                    outw[2 * g] = pack2<AT>(v01.x, v01.y);
+                    outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(wdst + swo[4 * hh + c]) =
+                        make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             }
             if (++cslot == kPack) cslot = 0;
-            // w = s (q - z) = f * s 2^(24-p) - s (2^(23-p) + z), one fp32 rounding per value;
-            // the pre-scale depends only on the code's position class p
-            constexpr int kCls = BITS == 4 ? 2 : 3;
-            float mc[kCls], ac[kCls];
-#pragma unroll
-            for (int c = 0; c < kCls; ++c) {
-                const int p = code_pos<BITS>(c);
-                mc[c] = sc * float(1u << (24 - p));
-                ac[c] = -sc * (float(1u << (23 - p)) + z);
-            }
-            uint32_t outw[16];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                float2 f01, f23;
-                chunk_codes4<BITS>(w, g, f01, f23);
-                const int j = 4 * g;
-                const float2 v01 = ffma2(f01, make_float2(mc[j % kCls], mc[(j + 1) % kCls]),
-                                         make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
-                const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
-                                         make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
-                outw[2 * g] = pack2<AT>(v01.x, v01.y);
-                outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
-            }
-            uint8_t* wdst = wt + rp.stage * plan.w;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *reinterpret_cast<uint4*>(wdst + swo[c]) =
-                    make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_w[rp.stage]);
-            rp.next(SW);
-            rp.next(SW);
+#pragma unroll
+            for (int i = 0; i < kDequantGroups; ++i) rp.next(SW);
             advance(cc);
         }
         cp_async_wait<0>();
@@ -557,17 +571,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Ring depths: as many activation slots as fit (up to kMaxStagesTC) with three
-// weight slots, or with two when that buys one more activation slot.
+// Ring depths: one weight slot per dequantisation group, and as many
+// activation slots as fit (up to kMaxStagesTC).  A group waits on the weight
+// slot of its next K step, kDequantGroups global steps after its last one; an
+// mbarrier parity wait is only sound while the slot's barrier is at most one
+// phase behind the awaited one, which holds exactly when that slot's previous
+// use was at or before the group's last step, i.e. stages_w >= kDequantGroups.
 void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
-    auto deepest = [&](int sw) {
-        int s = kMaxStagesTC;
-        while (s > 2 && tc_plan(BN, G, s, sw, bits).total > 227 * 1024) --s;
-        return s;
-    };
-    const int s3 = deepest(3), s2 = deepest(2);
-    *stages_w = s2 > s3 ? 2 : 3;
-    *stages = s2 > s3 ? s2 : s3;
+    static_assert(kDequantGroups <= 4, "four weight slots at most fit beside the rings");
+    int s = kMaxStagesTC;
+    while (s > 2 && tc_plan(BN, G, s, kDequantGroups, bits).total > 227 * 1024) --s;
+    *stages_w = kDequantGroups;
+    *stages = s;
 }
 
 template <int BITS, int ST, int AT, int BN, int G, int MODE>
