@@ -16,23 +16,28 @@
 // per FLOP; with G = 1 the two 256-column halves of tensor memory double-buffer
 // consecutive tiles.  One persistent CTA per SM walks the tiles.
 //
-// Warp roles (704 threads):
+// Warp roles (736 threads):
 //   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle); in
 //               the grouped FC1 the routed tokens' rows were first copied
 //               into expert-sorted order, so the same tile loads serve
 //   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
-//   warps 2-17  dequant, four groups of 4 warps taking every fourth K step:
+//   warp 2      packed-weight producer: per K step one TMA tile of the 128
+//               rows' packed bytes [128 x 32 B] and one of their scales
+//               [128 x 16 B] into an 8-slot ring (where the rows are 16-byte
+//               aligned; otherwise each dequant thread copies its own row
+//               with cp.async into the same slots)
+//   warps 3-18  dequant, four groups of 4 warps taking every fourth K step:
 //               one thread per weight row, both 32-code chunks of the K step;
-//               a private cp.async ring of packed bytes and scales; codes ->
-//               s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
-//   warps 18-21 epilogue: tcgen05.ld of the accumulators -> output dtype
+//               codes -> s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
+//   warps 19-22 epilogue: tcgen05.ld of the accumulators -> output dtype
 //               (FC1: SwiGLU of lane pairs) -> masked stores
 // The activation tiles and the dequantised weight tiles of the K steps sit in
 // two separate shared rings: the activation ring is deep (its tiles come from
-// L2 / HBM with the longest latency), the weight ring shallow (its tiles are
-// written by the dequantisation warps, whose own cp.async ring hides the
-// packed-byte latency).  A tcgen05.commit releases a slot of each when the MMAs
-// that read it complete.  Every wait is bounded.
+// L2 / HBM with the longest latency), the weight ring holds one slot per
+// dequant group.  A tcgen05.commit releases a slot of each when the MMAs that
+// read it complete.  Packed rows come as tensor tiles rather than per-thread
+// copies because a 32-lane copy of 32 scattered rows costs a shared-memory
+// wavefront per lane.  Every wait is bounded.
 #pragma once
 
 #include <cuda.h>
@@ -54,11 +59,16 @@ using namespace gemv;
 
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kBW = 128;    // weight rows per tile (MMA M)
-constexpr int kPack = 2;    // depth of each dequant thread's cp.async ring (own K steps)
+constexpr int kPackWarp = 2;  // TMA producer of packed rows and scales
 // Four groups of 4 dequantisation warps take every fourth K step: one thread
 // per weight row makes all 64 codes of the row's K step, and each group has
 // four MMA steps' time for its 128 x 64 weight slice.
-constexpr int kDequantWarp0 = 2, kDequantWarps = 4, kDequantGroups = 4;
+constexpr int kDequantWarp0 = 3, kDequantWarps = 4, kDequantGroups = 4;
+// Packed ring: K step g of the CTA's sequence -> slot g % 8, so each group owns
+// two slots and has its next K step in flight while it works on the current.
+constexpr int kPackSlots = 2 * kDequantGroups;
+constexpr int kPackRow = 32;  // bytes of a row's K step in a slot (INT3: a 16-byte-aligned 32-byte window)
+constexpr int kSclRow = 16;   // bytes of a row's scale window in a slot
 constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;
 constexpr int kThreadsTC = (kEpilogueWarp0 + 4) * 32;
 constexpr int kMaxStagesTC = 8;
@@ -74,8 +84,8 @@ __host__ __device__ inline TcPlan tc_plan(int BN, int G, int stages, int stages_
     p.bars = 1024;                                           // barriers and the TMEM address
     p.act = int64_t(G) * BN * 128;                           // activations of one stage (G sub-tiles)
     p.w = int64_t(kBW) * 128;                                // dequantised weights of one stage
-    p.pack = int64_t(kDequantGroups) * kPack * 2 * kBW * (bits == 4 ? 16 : 12);  // [slot][half][row][chunk]
-    p.scl = int64_t(kDequantGroups) * kPack * kBW * 8;                          // [slot][row][2 words]
+    p.pack = int64_t(kPackSlots) * kBW * kPackRow;  // [slot][row][32 bytes]
+    p.scl = int64_t(kPackSlots) * kBW * kSclRow;    // [slot][row][16 bytes]
     p.total = p.bars + int64_t(stages) * p.act + int64_t(stages_w) * p.w + p.pack + p.scl;
     return p;
 }
@@ -168,6 +178,8 @@ __device__ __forceinline__ int acc_uses(int tl) { return G == 1 ? (tl >> 1) : tl
 
 template <int BITS, int ST, int AT, int BN, int G, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                                const __grid_constant__ CUtensorMap tmap_w,
+                                                                const __grid_constant__ CUtensorMap tmap_s,
                                                                 const __grid_constant__ TcArgs a) {
     static_assert(G == 1 || G == 2, "one or two activation sub-tiles per tile");
     constexpr int UN = G * BN;  // activation rows per tile
@@ -180,7 +192,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     uint64_t* empty_w = full_a + 3 * kMaxStagesTC;
     uint64_t* acc_full = full_a + 4 * kMaxStagesTC;
     uint64_t* acc_empty = acc_full + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* pfull = full_a + 5 * kMaxStagesTC;   // packed slot loaded (TMA)
+    uint64_t* pempty = full_a + 6 * kMaxStagesTC;  // packed slot read by its group's 4 warps
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_a + 7 * kMaxStagesTC);
     volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_holder + 1);  // the epilogue's wait gave up
     uint8_t* act = smem + plan.bars;
     uint8_t* wt = act + S * plan.act;
@@ -207,9 +221,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
+        for (int s = 0; s < kPackSlots; ++s) {
+            mbar_init(&pfull[s], 1);
+            mbar_init(&pempty[s], kDequantWarps);
+        }
         *epi_fail = 0;
         fence_barrier_init();
         prefetch_tmap(&tmap_a);
+        if (a.w_tma) prefetch_tmap(&tmap_w);
+        if (a.s_tma) prefetch_tmap(&tmap_s);
     }
     if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
     grid_dependency_wait();
@@ -275,15 +295,59 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 for (int g = 0; g < G; ++g) tc_commit(&acc_full[acc_slot<G>(tl, g)]);
             }
         }
+    } else if (warp == kPackWarp) {
+        // ----------------------------------------------- packed-row producer
+        // One TMA tile of packed bytes (and one of scales) per K step of the
+        // CTA's sequence into slot g % 8; the FC1 gate/up halves of a tile
+        // (rows p and I + p) come as two 64-row tiles.
+        if (lane == 0 && a.w_tma) {
+            constexpr int kStepBytes = BITS == 4 ? 32 : 24;
+            const int SS = ST == kF32 ? 4 : 2;
+            const bool halves = MODE == kModeFc1 && !a.inter;
+            const uint32_t tx = kBW * kPackRow + (a.s_tma ? kBW * kSclRow : 0);
+            const int bs_shift = __ffs(a.bs) - 1;
+            RingPos pp;
+            for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
+                const Tile x = tile_of(a, t, UN);
+                const int y0 = static_cast<int>(x.e * a.rows + (halves ? x.n0 / 2 : x.n0));
+                const int y1 = static_cast<int>(y0 + a.I);  // halves: the up rows
+                for (int ks = 0; ks < ksteps; ++ks, pp.next(kPackSlots)) {
+                    if (pp.round && !mbar_wait(&pempty[pp.stage], (pp.round - 1) & 1)) { failed = true; break; }
+                    mbar_arrive_expect_tx(&pfull[pp.stage], tx);
+                    const int kabs = x.ks0 + ks;
+                    const int xw = (kabs * kStepBytes) & ~15;                       // 16-byte aligned window
+                    uint8_t* dw = pack + pp.stage * (kBW * kPackRow);
+                    if (halves) {
+                        tma_load_2d(dw, &tmap_w, xw, y0, &pfull[pp.stage]);
+                        tma_load_2d(dw + 64 * kPackRow, &tmap_w, xw, y1, &pfull[pp.stage]);
+                    } else {
+                        tma_load_2d(dw, &tmap_w, xw, y0, &pfull[pp.stage]);
+                    }
+                    if (a.s_tma) {
+                        const int xs = (((kabs * kBK) >> bs_shift) * SS) & ~15;
+                        uint8_t* ds = scl + pp.stage * (kBW * kSclRow);
+                        if (halves) {
+                            tma_load_2d(ds, &tmap_s, xs, y0, &pfull[pp.stage]);
+                            tma_load_2d(ds + 64 * kSclRow, &tmap_s, xs, y1, &pfull[pp.stage]);
+                        } else {
+                            tma_load_2d(ds, &tmap_s, xs, y0, &pfull[pp.stage]);
+                        }
+                    }
+                }
+            }
+        }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequant
-        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes global K steps = group (mod 4)
-        const int r = tid - (kDequantWarp0 + group * kDequantWarps) * 32;  // weight row of the tile
+        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes K steps = group (mod 4)
+        const int r = tid - (kDequantWarp0 + group * kDequantWarps) * 32;  // row of the packed slot
+        // Tile row (MMA lane) this thread makes: FC1 gate and up rows of pair p
+        // sit in slot rows p and 64 + p, and go to tile rows 2p and 2p + 1.
+        const int orow = (MODE == kModeFc1 && !a.inter) ? 2 * (r & 63) + (r >> 6) : r;
         constexpr int kCB = BITS == 4 ? 16 : 12;  // packed bytes per 32-code chunk
         constexpr int kStepBytes = 2 * kCB;       // packed bytes of a row per K step
         constexpr int kZ = 1 << (BITS - 1);
-        uint8_t* gpack = pack + int64_t(group) * (plan.pack / kDequantGroups);
-        uint8_t* gscl = scl + int64_t(group) * (plan.scl / kDequantGroups);
+        constexpr int SS = ST == kF32 ? 4 : 2;
+        const bool w_tma = a.w_tma != 0, s_tma = a.s_tma != 0;
         const int nb = a.nb, bs_shift = __ffs(a.bs) - 1;
         const int64_t kcodes = int64_t(nb) * a.bs;  // codes stored per row
         const int64_t n_scales = a.rows * nb;
@@ -299,10 +363,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         auto stream_of = [&](const Tile& x) -> RowStream {
             int64_t wr;
             if (MODE == kModeFc1) {
-                const int64_t p = x.n0 / 2 + (r >> 1), up = r & 1;  // pair-interleaved tile rows
+                const int64_t p = x.n0 / 2 + (orow >> 1), up = orow & 1;  // pair-interleaved tile rows
                 wr = p < a.I ? (a.inter ? 2 * p + up : up * a.I + p) : -1;
             } else {
-                wr = x.n0 + r < a.rows ? x.n0 + r : -1;
+                wr = x.n0 + orow < a.rows ? x.n0 + orow : -1;
             }
             RowStream st;
             st.ok = wr >= 0;
@@ -324,13 +388,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 c.t += gridDim.x;
             }
         };
+        // Where the rows are not 16-byte aligned, each thread copies what the
+        // producer's tiles do not bring, one own K step ahead (cp.async).
+        const bool own_copies = !(w_tma && s_tma);
         Cursor pc{static_cast<int>(blockIdx.x), group};  // prefetch cursor
         while (pc.ks >= ksteps && pc.t < n_tiles) {
             pc.ks -= ksteps;
             pc.t += gridDim.x;
         }
         int pslot = 0;
-        RowStream ps = pc.t < n_tiles ? stream_of(tile_of(a, pc.t, UN)) : RowStream{nullptr, nullptr, 0, 0, false};
+        RowStream ps{nullptr, nullptr, 0, 0, false};
+        if (own_copies && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t, UN));
         // one half-precision scale: the 4-byte word that holds it (the last scale
         // of the array alone, where its word would run past the end)
         auto copy_scale_word = [&](uint32_t* dst, const uint8_t* base, int64_t si) {
@@ -345,33 +413,38 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         auto issue = [&]() {
             const int64_t k0 = int64_t(ps.ks0 + pc.ks) * kBK;  // first code of this K step
             if (pc.t < n_tiles && ps.ok && k0 < kcodes) {
-                const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
+                const int slot = group + kDequantGroups * pslot;
                 const bool two = k0 + 32 < kcodes;  // the second chunk holds stored codes
+                if (!w_tma) {
+                    const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
+                    uint8_t* dst = pack + (slot * kBW + r) * kPackRow;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (hh == 1 && !two) break;
-                    uint8_t* dst = gpack + ((pslot * 2 + hh) * kBW + r) * kCB;
-                    if constexpr (BITS == 4) {
-                        cp_async16(dst, src + hh * kCB);
-                    } else {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh == 1 && !two) break;
+                        if constexpr (BITS == 4) {
+                            cp_async16(dst + hh * kCB, src + hh * kCB);
+                        } else {
 #pragma unroll
-                        for (int q = 0; q < 3; ++q) cp_async4(dst + 4 * q, src + hh * kCB + 4 * q);
+                            for (int q = 0; q < 3; ++q) cp_async4(dst + hh * kCB + 4 * q, src + hh * kCB + 4 * q);
+                        }
                     }
                 }
-                uint32_t* sdst = reinterpret_cast<uint32_t*>(gscl + (pslot * kBW + r) * 8);
-                const int64_t i0 = ps.si0 + (k0 >> bs_shift), i1 = ps.si0 + ((k0 + 32) >> bs_shift);
-                copy_scale_word(sdst, ps.s, i0);
-                if (two && (ST == kF32 ? i1 != i0 : (i1 >> 1) != (i0 >> 1))) copy_scale_word(sdst + 1, ps.s, i1);
+                if (!s_tma) {
+                    uint32_t* sdst = reinterpret_cast<uint32_t*>(scl + (slot * kBW + r) * kSclRow);
+                    const int64_t i0 = ps.si0 + (k0 >> bs_shift), i1 = ps.si0 + ((k0 + 32) >> bs_shift);
+                    copy_scale_word(sdst, ps.s, i0);
+                    if (two && (ST == kF32 ? i1 != i0 : (i1 >> 1) != (i0 >> 1))) copy_scale_word(sdst + 1, ps.s, i1);
+                }
             }
             cp_async_commit();
-            if (++pslot == kPack) pslot = 0;
+            pslot ^= 1;
             if (pc.t < n_tiles) {
                 const int t_before = pc.t;
                 advance(pc);
                 if (pc.t != t_before && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t, UN));
             }
         };
-        for (int i = 0; i < kPack - 1; ++i) issue();
+        if (own_copies) issue();
         // consumer cursor and its place in the weight ring (global step g -> slot g % SW)
         Cursor cc = Cursor{static_cast<int>(blockIdx.x), group};
         while (cc.ks >= ksteps && cc.t < n_tiles) {
@@ -380,10 +453,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         }
         RingPos rp;
         for (int i = 0; i < group; ++i) rp.next(SW);
-        int cslot = 0;
-        uint32_t swo[8];  // this thread's eight 16-byte slots of a weight tile row
+        uint32_t own = 0;  // this group's K steps so far: packed slot group + 4 (own & 1), its use own >> 1
+        uint32_t swo[8];   // this thread's eight 16-byte slots of a weight tile row
 #pragma unroll
-        for (int c = 0; c < 8; ++c) swo[c] = sw128(r, c);
+        for (int c = 0; c < 8; ++c) swo[c] = sw128(orow, c);
         int cur_t = -1;
         RowStream cs{nullptr, nullptr, 0, 0, false};
         const uint8_t* zrow = nullptr;
@@ -395,20 +468,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 zrow = (a.zp && cs.ok) ? a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes : nullptr;
             }
             const int ks = cs.ks0 + cc.ks;  // absolute K step
-            issue();
-            cp_async_wait<kPack - 1>();
+            const int slot = group + kDequantGroups * static_cast<int>(own & 1);
+            if (own_copies) {
+                issue();
+                cp_async_wait<1>();
+            }
+            if (w_tma && !warp_wait(&pfull[slot], (own >> 1) & 1)) { failed = true; break; }
             if (rp.round && !warp_wait(&empty_w[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
             uint8_t* wdst = wt + rp.stage * plan.w;
-            const uint32_t* swd = reinterpret_cast<const uint32_t*>(gscl + (cslot * kBW + r) * 8);
-            const int64_t i0 = cs.si0 + ((int64_t(ks) * kBK) >> bs_shift);
+            const int64_t kstep0 = int64_t(ks) * kBK;
+            // packed bytes of this row's K step (the tensor tile's window starts
+            // on a 16-byte boundary: INT3 steps at odd positions sit 8 bytes in)
+            const uint8_t* prow = pack + (slot * kBW + r) * kPackRow + (w_tma ? (ks * kStepBytes) & 15 : 0);
+            // scales: the tensor tile holds the row's 16-byte window around the
+            // step's first scale; own copies hold the step's one or two words
+            const uint8_t* srow = scl + (slot * kBW + r) * kSclRow;
+            uint4 swin = make_uint4(0, 0, 0, 0);
+            if (s_tma) swin = *reinterpret_cast<const uint4*>(srow);
+            const int xs = static_cast<int>(((kstep0 >> bs_shift) * SS) & ~int64_t(15));
+            const int64_t i0 = cs.si0 + (kstep0 >> bs_shift);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int64_t kc = int64_t(ks) * kBK + 32 * hh;  // first code of this chunk
+                const int64_t kc = kstep0 + 32 * hh;  // first code of this chunk
                 const bool live = cs.ok && kc < kcodes;
                 uint32_t w[BITS];
                 float sc = 0.f, z = float(kZ);
                 if (live) {
-                    const uint8_t* src = gpack + ((cslot * 2 + hh) * kBW + r) * kCB;
+                    const uint8_t* src = prow + hh * kCB;
                     if constexpr (BITS == 4) {
                         const uint4 v = *reinterpret_cast<const uint4*>(src);
                         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
@@ -417,9 +503,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         for (int q = 0; q < BITS; ++q) w[q] = reinterpret_cast<const uint32_t*>(src)[q];
                     }
                     const int64_t si = cs.si0 + (kc >> bs_shift);
-                    // word 0 holds scale i0; scale si is either in it or in word 1
-                    const bool in0 = ST == kF32 ? si == i0 : (si >> 1) == (i0 >> 1);
-                    sc = scale_from_word<ST>(swd[in0 ? 0 : 1], si);
+                    if (s_tma) {
+                        const int b = static_cast<int>((kc >> bs_shift) * SS) - xs;  // byte in the window
+                        const int wi = b >> 2;
+                        const uint32_t word = wi == 0 ? swin.x : wi == 1 ? swin.y : wi == 2 ? swin.z : swin.w;
+                        sc = scale_from_word<ST>(word, b >> 1);
+                    } else {
+                        // word 0 holds scale i0; scale si is either in it or in word 1
+                        const bool in0 = ST == kF32 ? si == i0 : (si >> 1) == (i0 >> 1);
+                        sc = scale_from_word<ST>(reinterpret_cast<const uint32_t*>(srow)[in0 ? 0 : 1], si);
+                    }
                     if (zrow) z = float(zero_point_code<BITS>(zrow, static_cast<int>(kc >> bs_shift)));
                 } else {
 #pragma unroll
@@ -453,10 +546,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     *reinterpret_cast<uint4*>(wdst + swo[4 * hh + c]) =
                         make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             }
-            if (++cslot == kPack) cslot = 0;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_w[rp.stage]);
+            if (lane == 0) {
+                mbar_arrive(&full_w[rp.stage]);
+                if (w_tma) mbar_arrive(&pempty[slot]);
+            }
+            ++own;
 #pragma unroll
             for (int i = 0; i < kDequantGroups; ++i) rp.next(SW);
             advance(cc);
@@ -605,6 +701,42 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
+    // Packed rows and scales as [rows x bytes] tensors of all stacked matrices,
+    // read in tiles of 128 rows (FC1 with separate gate/up halves: 64) by 32
+    // (scales: 16) bytes; only where every row starts on a 16-byte boundary.
+    CUtensorMap tmap_w, tmap_s;
+    std::memset(&tmap_w, 0, sizeof tmap_w);
+    std::memset(&tmap_s, 0, sizeof tmap_s);
+    {
+        auto encode = encode_fn();
+        const int64_t ex = a.experts > 1 ? a.experts : 1;
+        const int64_t all_rows = ex * a.rows;
+        const cuuint32_t box_rows = (MODE == kModeFc1 && !a.inter) ? 64 : kBW;
+        const int ss = ST == kF32 ? 4 : 2;
+        const int64_t s_row = int64_t(a.nb) * ss;
+        auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+        a.w_tma = 0;
+        a.s_tma = 0;
+        if (all_rows < (int64_t(1) << 31) && aligned(a.B) && a.row_bytes % 16 == 0 &&
+            (ex == 1 || a.w_expert_stride == a.rows * a.row_bytes)) {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.row_bytes), static_cast<cuuint64_t>(all_rows)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.row_bytes)};
+            const cuuint32_t box[2] = {kPackRow, box_rows};
+            const cuuint32_t estr[2] = {1, 1};
+            a.w_tma = encode(&tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.B), dims, strides,
+                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        if (a.w_tma && aligned(a.scales) && s_row % 16 == 0 && (ex == 1 || a.s_expert_stride == a.rows * s_row)) {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(s_row), static_cast<cuuint64_t>(all_rows)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(s_row)};
+            const cuuint32_t box[2] = {kSclRow, box_rows};
+            const cuuint32_t estr[2] = {1, 1};
+            a.s_tma = encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.scales), dims, strides,
+                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+    }
     uint32_t cols = 32;
     while (cols < 2u * BN) cols <<= 1;
     a.tmem_cols = cols;
@@ -623,7 +755,7 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, tmap, a);
+    return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, tmap_s, a);
 }
 
 template <int MODE, int BITS, int ST, int AT>

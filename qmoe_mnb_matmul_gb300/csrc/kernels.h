@@ -89,6 +89,8 @@ struct TcArgs {
     int64_t I;
     int inter;             // FC1 rows interleaved gate/up
     const void* X;         // FC1: activations gathered by token
+    int64_t experts;       // matrices stacked in B / scales (grouped launches; 0 or 1 otherwise)
+    int w_tma, s_tma;      // set by the launcher: packed rows / scales come as tensor tiles
 };
 
 // Rows of activations per tile in the grouped launches.

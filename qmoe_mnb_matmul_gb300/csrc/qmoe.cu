@@ -686,6 +686,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.n_mtiles = reinterpret_cast<const int*>(ws + L.nmtiles);
         a.bs = q.bs;
         a.y_dtype = q.act_dtype;
+        a.experts = q.E;
         // FC1: K = H, 2I rows (pair-interleaved in the tile), SwiGLU into h (act dtype, sorted order)
         a.M = P;
         a.K = q.H;
