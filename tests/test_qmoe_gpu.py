@@ -88,11 +88,16 @@ def test_tiled_plan(T, E, k, skew, bits):
 
 
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
-def test_tiled_plan_layouts(layout):
-    H, I, E, k, T, bs = 256, 128, 16, 4, 50, 32
-    d = wl.moe_layer(wl.rng(seed("tiled-layout", layout)), T, H, I, E, 4, 4, bs, "f16", with_zp=True, skew=True)
-    y = run_qmoe(d, T, H, I, E, k, 4, 4, bs, "f16", layout)
-    assert_half_close(y, reference(d, k, 4, 4, I, bs, "f16", layout))
+@pytest.mark.parametrize("I,bits", [(128, 4), (96, 4), (96, 3)])
+def test_tiled_plan_layouts(layout, I, bits):
+    """Both FC1 row layouts; I = 96 leaves the last weight tile of each expert
+    half empty (its gate and up rows are read as two 64-row tiles in the
+    concatenated layout)."""
+    H, E, k, T, bs = 256, 16, 4, 50, 32
+    d = wl.moe_layer(wl.rng(seed("tiled-layout", layout, I, bits)), T, H, I, E, bits, bits, bs, "f16", with_zp=True,
+                     skew=True)
+    y = run_qmoe(d, T, H, I, E, k, bits, bits, bs, "f16", layout)
+    assert_half_close(y, reference(d, k, bits, bits, I, bs, "f16", layout))
 
 
 @pytest.mark.parametrize("T", [128, 512])
