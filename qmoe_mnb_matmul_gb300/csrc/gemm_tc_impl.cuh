@@ -63,7 +63,10 @@ constexpr int kPackWarp = 2;  // TMA producer of packed rows and scales
 // Four groups of 4 dequantisation warps take every fourth K step: one thread
 // per weight row makes all 64 codes of the row's K step, and each group has
 // four MMA steps' time for its 128 x 64 weight slice.
-constexpr int kDequantWarp0 = 3, kDequantWarps = 4, kDequantGroups = 4;
+constexpr int kDequantWarp0 = 3, kDequantGroups = 4;
+constexpr int kDequantWarps = 16 / kDequantGroups;            // warps per group
+constexpr int kChunksPerThread = kDequantGroups == 4 ? 2 : 1;  // 32-code chunks of a row's K step per thread
+constexpr int kWeightSlots = 4;                                // dequantised-weight ring depth (>= groups)
 // Packed ring: K step g of the CTA's sequence -> slot g % 8, so each group owns
 // two slots and has its next K step in flight while it works on the current.
 constexpr int kPackSlots = 2 * kDequantGroups;
@@ -338,8 +341,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------------ dequant
-        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes K steps = group (mod 4)
-        const int r = tid - (kDequantWarp0 + group * kDequantWarps) * 32;  // row of the packed slot
+        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes K steps = group (mod groups)
+        const int dq = tid - (kDequantWarp0 + group * kDequantWarps) * 32;
+        const int r = dq & (kBW - 1);                               // row of the packed slot
+        const int h0 = kChunksPerThread == 2 ? 0 : dq >> 7;         // this thread's first chunk
         // Tile row (MMA lane) this thread makes: FC1 gate and up rows of pair p
         // sit in slot rows p and 64 + p, and go to tile rows 2p and 2p + 1.
         const int orow = (MODE == kModeFc1 && !a.inter) ? 2 * (r & 63) + (r >> 6) : r;
@@ -419,7 +424,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     const uint8_t* src = ps.w + int64_t(pc.ks) * kStepBytes;
                     uint8_t* dst = pack + (slot * kBW + r) * kPackRow;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int i = 0; i < kChunksPerThread; ++i) {
+                        const int hh = h0 + i;
                         if (hh == 1 && !two) break;
                         if constexpr (BITS == 4) {
                             cp_async16(dst + hh * kCB, src + hh * kCB);
@@ -429,11 +435,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         }
                     }
                 }
-                if (!s_tma) {
+                if (!s_tma) {  // word hh: the word holding chunk hh's scale
                     uint32_t* sdst = reinterpret_cast<uint32_t*>(scl + (slot * kBW + r) * kSclRow);
-                    const int64_t i0 = ps.si0 + (k0 >> bs_shift), i1 = ps.si0 + ((k0 + 32) >> bs_shift);
-                    copy_scale_word(sdst, ps.s, i0);
-                    if (two && (ST == kF32 ? i1 != i0 : (i1 >> 1) != (i0 >> 1))) copy_scale_word(sdst + 1, ps.s, i1);
+#pragma unroll
+                    for (int i = 0; i < kChunksPerThread; ++i) {
+                        const int hh = h0 + i;
+                        if (hh == 1 && !two) break;
+                        copy_scale_word(sdst + hh, ps.s, ps.si0 + ((k0 + 32 * hh) >> bs_shift));
+                    }
                 }
             }
             cp_async_commit();
@@ -454,9 +463,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         RingPos rp;
         for (int i = 0; i < group; ++i) rp.next(SW);
         uint32_t own = 0;  // this group's K steps so far: packed slot group + 4 (own & 1), its use own >> 1
-        uint32_t swo[8];   // this thread's eight 16-byte slots of a weight tile row
+        uint32_t swo[4 * kChunksPerThread];  // this thread's 16-byte slots of a weight tile row
 #pragma unroll
-        for (int c = 0; c < 8; ++c) swo[c] = sw128(orow, c);
+        for (int c = 0; c < 4 * kChunksPerThread; ++c) swo[c] = sw128(orow, 4 * h0 + c);
         int cur_t = -1;
         RowStream cs{nullptr, nullptr, 0, 0, false};
         const uint8_t* zrow = nullptr;
@@ -486,9 +495,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             uint4 swin = make_uint4(0, 0, 0, 0);
             if (s_tma) swin = *reinterpret_cast<const uint4*>(srow);
             const int xs = static_cast<int>(((kstep0 >> bs_shift) * SS) & ~int64_t(15));
-            const int64_t i0 = cs.si0 + (kstep0 >> bs_shift);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int i = 0; i < kChunksPerThread; ++i) {
+                const int hh = h0 + i;
                 const int64_t kc = kstep0 + 32 * hh;  // first code of this chunk
                 const bool live = cs.ok && kc < kcodes;
                 uint32_t w[BITS];
@@ -509,9 +518,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         const uint32_t word = wi == 0 ? swin.x : wi == 1 ? swin.y : wi == 2 ? swin.z : swin.w;
                         sc = scale_from_word<ST>(word, b >> 1);
                     } else {
-                        // word 0 holds scale i0; scale si is either in it or in word 1
-                        const bool in0 = ST == kF32 ? si == i0 : (si >> 1) == (i0 >> 1);
-                        sc = scale_from_word<ST>(reinterpret_cast<const uint32_t*>(srow)[in0 ? 0 : 1], si);
+                        sc = scale_from_word<ST>(reinterpret_cast<const uint32_t*>(srow)[hh], si);
                     }
                     if (zrow) z = float(zero_point_code<BITS>(zrow, static_cast<int>(kc >> bs_shift)));
                 } else {
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(wdst + swo[4 * hh + c]) =
+                    *reinterpret_cast<uint4*>(wdst + swo[4 * i + c]) =
                         make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             }
             fence_proxy_async_smem();
@@ -674,10 +681,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // phase behind the awaited one, which holds exactly when that slot's previous
 // use was at or before the group's last step, i.e. stages_w >= kDequantGroups.
 void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
-    static_assert(kDequantGroups <= 4, "four weight slots at most fit beside the rings");
+    static_assert(kWeightSlots >= kDequantGroups, "a parity wait needs a weight slot per group");
     int s = kMaxStagesTC;
-    while (s > 2 && tc_plan(BN, G, s, kDequantGroups, bits).total > 227 * 1024) --s;
-    *stages_w = kDequantGroups;
+    while (s > 2 && tc_plan(BN, G, s, kWeightSlots, bits).total > 227 * 1024) --s;
+    *stages_w = kWeightSlots;
     *stages = s;
 }
 
