@@ -158,20 +158,57 @@ __global__ void __launch_bounds__(kPermChunk) perm_count_kernel(const int32_t* _
     for (int e = threadIdx.x; e < E; e += kPermChunk) chunkc[int64_t(blockIdx.x) * E + e] = hist[e];
 }
 
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunkc, int n_chunks, int E,
-                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+// The chunks of each expert are split into `parts` consecutive ranges, one
+// thread per (range, expert): a first pass sums the range, the ranges' sums
+// are scanned in shared memory, and a second pass writes the exclusive
+// prefixes.  Loads go out kScanBatch at a time, so a range costs a few memory
+// round trips rather than one per chunk.
+constexpr int kScanThreads = 1024, kScanBatch = 16;
+
+__global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* __restrict__ chunkc, int n_chunks, int E,
+                                                                 int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ offsets) {
+    __shared__ int32_t part_sums[kScanThreads];  // [part][E]
     __shared__ int32_t warp_sums[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int parts = E <= kScanThreads ? kScanThreads / E : 1;
+    const int e = tid % E, part = tid / E;
+    const bool active = part < parts;
+    const int per = (n_chunks + parts - 1) / parts;
+    const int c0 = part * per, c1 = min(n_chunks, c0 + per);
     grid_dependency_wait();
-    int32_t total = 0;
-    if (tid < E) {
-        for (int c = 0; c < n_chunks; ++c) {
-            const int32_t v = chunkc[int64_t(c) * E + tid];
-            chunkc[int64_t(c) * E + tid] = total;
-            total += v;
+    int32_t sum = 0;
+    if (active) {
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) v[j] = c + j < c1 ? chunkc[int64_t(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) sum += v[j];
+        }
+        part_sums[part * E + e] = sum;
+    }
+    __syncthreads();
+    int32_t run = 0, total = 0;
+    if (active) {
+        for (int q = 0; q < parts; ++q) {
+            const int32_t ps = part_sums[q * E + e];
+            run += q < part ? ps : 0;
+            total += ps;
+        }
+        for (int c = c0; c < c1; c += kScanBatch) {
+            int32_t v[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) v[j] = c + j < c1 ? chunkc[int64_t(c + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) {
+                if (c + j < c1) chunkc[int64_t(c + j) * E + e] = run;
+                run += v[j];
+            }
         }
     }
-    int32_t x = total;
+    // exclusive scan of the expert totals (threads 0 .. E-1 hold expert tid's total)
+    int32_t x = tid < E ? total : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
@@ -242,7 +279,7 @@ cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t
     perm_count_kernel<<<static_cast<unsigned>(n), kPermChunk, hist, stream>>>(idx, P, static_cast<int>(E), chunkc);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    perm_scan_kernel<<<1, 1024, 0, stream>>>(chunkc, static_cast<int>(n), static_cast<int>(E), counts, offsets);
+    perm_scan_kernel<<<1, kScanThreads, 0, stream>>>(chunkc, static_cast<int>(n), static_cast<int>(E), counts, offsets);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t whist = size_t(kPermChunk / 32) * E * sizeof(int32_t);
     perm_scatter_kernel<<<static_cast<unsigned>(n), kPermChunk, whist, stream>>>(idx, P, static_cast<int>(E), chunkc,
