@@ -34,7 +34,7 @@
 // The activation tiles and the dequantised weight tiles of the K steps sit in
 // two separate shared rings: the activation ring is deep (its tiles come from
 // L2 / HBM with the longest latency), the weight ring holds one slot per
-// dequant group.  A tcgen05.commit releases a slot of each when the MMAs that
+// dequant group plus one.  A tcgen05.commit releases a slot of each when the MMAs that
 // read it complete.  Packed rows come as tensor tiles rather than per-thread
 // copies because a 32-lane copy of 32 scattered rows costs a shared-memory
 // wavefront per lane.  Every wait is bounded.
@@ -66,7 +66,10 @@ constexpr int kPackWarp = 2;  // TMA producer of packed rows and scales
 constexpr int kDequantWarp0 = 3, kDequantGroups = 4;
 constexpr int kDequantWarps = 16 / kDequantGroups;            // warps per group
 constexpr int kChunksPerThread = kDequantGroups == 4 ? 2 : 1;  // 32-code chunks of a row's K step per thread
-constexpr int kWeightSlots = 4;                                // dequantised-weight ring depth (>= groups)
+// Dequantised-weight ring depth: at least one slot per group (a group's parity
+// wait needs it), plus one so that a group may start its next K step one MMA
+// step before the slot it last wrote has been read.
+constexpr int kWeightSlots = kDequantGroups + 1;
 // Packed ring: K step g of the CTA's sequence -> slot g % 8, so each group owns
 // two slots and has its next K step in flight while it works on the current.
 constexpr int kPackSlots = 2 * kDequantGroups;
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         const int odd = lane & 1;
 #pragma unroll
                         for (int j = 0; j < 32; j += 2) {
-                            const float send = __uint_as_float(v[j + 1 - odd]);  // even: gate of j+1; odd: up of j
+                            const float send = __uint_as_float(odd ? v[j] : v[j + 1]);  // even: gate of j+1; odd: up of j
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
                             const float gate = odd ? recv : __uint_as_float(v[j]);
                             const float up = odd ? __uint_as_float(v[j + 1]) : recv;
@@ -674,12 +677,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Ring depths: one weight slot per dequantisation group, and as many
-// activation slots as fit (up to kMaxStagesTC).  A group waits on the weight
-// slot of its next K step, kDequantGroups global steps after its last one; an
-// mbarrier parity wait is only sound while the slot's barrier is at most one
-// phase behind the awaited one, which holds exactly when that slot's previous
-// use was at or before the group's last step, i.e. stages_w >= kDequantGroups.
+// Ring depths: kWeightSlots dequantised-weight slots, and as many activation
+// slots as fit (up to kMaxStagesTC).  A group waits on the weight slot of its
+// next K step, kDequantGroups global steps after its last one; an mbarrier
+// parity wait is only sound while the slot's barrier is at most one phase
+// behind the awaited one, which holds exactly when that slot's previous use
+// was at or before the group's last step, i.e. stages_w >= kDequantGroups.
 void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
     static_assert(kWeightSlots >= kDequantGroups, "a parity wait needs a weight slot per group");
     int s = kMaxStagesTC;
