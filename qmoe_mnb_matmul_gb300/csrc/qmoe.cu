@@ -169,48 +169,18 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
     float* h = reinterpret_cast<float*>(ws + L.h);
     const int64_t P = q.T * q.k;
 
-    grid_dependency_wait();
-    // Dependents may start now: the FC2 decode prologue reads the router
-    // logits, which were complete before this kernel's wait returned.
-    grid_launch_dependents();
-    if (DECODE) {
-        const int64_t p = blockIdx.x;
-        const int64_t t = p / q.k;
-        route_token(q, t, s_idx, s_w, reinterpret_cast<float*>(Wst + plan.w + plan.s));
-        if (tid == 0) {
-            s_int[0] = s_idx[p % q.k];
-            s_int[1] = static_cast<int>(p);
-            s_int[2] = 1;
-            s_int[4] = static_cast<int>(t);
-        }
-    } else {
-        const int tile = blockIdx.x;
-        const int ntiles = *reinterpret_cast<const int*>(ws + L.ntiles);
-        if (tile >= ntiles) return;
-        if (tid == 0) {
-            const int2 ti = reinterpret_cast<const int2*>(ws + L.tiles)[tile];
-            const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
-            const int* perm = reinterpret_cast<const int*>(ws + L.perm);
-            const int cnt = min(MT, offsets[ti.x + 1] - ti.y);
-            s_int[0] = ti.x;
-            s_int[1] = ti.y;
-            s_int[2] = cnt;
-            for (int m = 0; m < MT; ++m) s_int[4 + m] = m < cnt ? perm[ti.y + m] / q.k : -1;
-        }
-    }
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
     }
-    __syncthreads();
-    const int e = s_int[0], s0 = s_int[1], cnt = s_int[2];
     const int64_t I = q.I;
     const int64_t pair0 = int64_t(blockIdx.y) * kPairsPerBlock;
     const int pc = static_cast<int>(std::min<int64_t>(kPairsPerBlock, I - pair0));
-    const uint8_t* W1 = q.fc1_w + int64_t(e) * 2 * I * rb;
-    const S* S1 = static_cast<const S*>(q.fc1_s) + int64_t(e) * 2 * I * nb;
     const bool inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
-    if (tid == 0) {
+    // The block of gate/up rows of expert e (and their scales) into shared memory.
+    auto copy_rows = [&](int e) {
+        const uint8_t* W1 = q.fc1_w + int64_t(e) * 2 * I * rb;
+        const S* S1 = static_cast<const S*>(q.fc1_s) + int64_t(e) * 2 * I * nb;
         const uint32_t wrow = static_cast<uint32_t>(rb), srow = static_cast<uint32_t>(nb * sizeof(S));
         const uint32_t total = 2u * pc * (wrow + srow);
         mbar_arrive_expect_tx(bar, total);
@@ -224,7 +194,44 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             bulk_g2s(Sdst, S1 + pair0 * nb, pc * srow, bar);
             bulk_g2s(Sdst + kPairsPerBlock * nb * sizeof(S), S1 + (I + pair0) * nb, pc * srow, bar);
         }
+    };
+    if (DECODE) {
+        // Prologue, overlapping the kernel ahead: router logits and expert
+        // weights are never outputs of the immediately preceding library call,
+        // so the CTA routes its token and starts copying the selected expert's
+        // rows before waiting; activations and workspace are read after.
+        const int64_t p = blockIdx.x;
+        const int64_t t = p / q.k;
+        route_token(q, t, s_idx, s_w, reinterpret_cast<float*>(Wst + plan.w + plan.s));
+        if (tid == 0) {
+            s_int[0] = s_idx[p % q.k];
+            s_int[1] = static_cast<int>(p);
+            s_int[2] = 1;
+            s_int[4] = static_cast<int>(t);
+            copy_rows(s_int[0]);
+        }
+        grid_dependency_wait();
+        grid_launch_dependents();
+    } else {
+        grid_dependency_wait();
+        grid_launch_dependents();
+        const int tile = blockIdx.x;
+        const int ntiles = *reinterpret_cast<const int*>(ws + L.ntiles);
+        if (tile >= ntiles) return;
+        if (tid == 0) {
+            const int2 ti = reinterpret_cast<const int2*>(ws + L.tiles)[tile];
+            const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
+            const int* perm = reinterpret_cast<const int*>(ws + L.perm);
+            const int cnt = min(MT, offsets[ti.x + 1] - ti.y);
+            s_int[0] = ti.x;
+            s_int[1] = ti.y;
+            s_int[2] = cnt;
+            for (int m = 0; m < MT; ++m) s_int[4 + m] = m < cnt ? perm[ti.y + m] / q.k : -1;
+            copy_rows(ti.x);
+        }
     }
+    __syncthreads();
+    const int e = s_int[0], s0 = s_int[1], cnt = s_int[2];
     stage_chunks<BITS, MT, ST>(
         A4, Corr, C, q.H, q.act_dtype, q.x_vec != 0,
         [&](int m) -> const void* {
