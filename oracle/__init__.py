@@ -72,6 +72,7 @@ def _lib():
                 "orc_permute": [P, I64, C, I64, P, P, P],
                 "orc_qmoe": [P, C, I64, I64, P, I64, C, C, P, P, P, C, P, P, P, C, I64, C, C, P,
                              I64, P, C],
+                "orc_quantize_int3": [P, C, I64, I64, C, C, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -218,3 +219,21 @@ def qmoe(X, act_dtype: str, logits, k: int, normalize: bool, fc1_w, fc1_scales, 
             0 if toks is None else toks.size, _ptr(out), threads)
     _check(_lib().orc_qmoe(*args), "qmoe")
     return out
+
+
+def quantize_int3(W, w_dtype: str, bs: int, s_dtype: str):
+    """Symmetric grouped INT3 round-to-nearest of W [N, K] (K % bs == 0).
+
+    Returns (packed uint8 [N, K/bs * 3*bs/8], scales [N, K/bs], bad bool [N, K/bs]):
+    scales are float32 for "f32" and raw uint16 bit patterns for "f16" / "bf16";
+    bad marks the rejected blocks (non-finite weight or stored scale, or a
+    nonzero block whose stored scale rounds to zero)."""
+    W = _elem(W, w_dtype)
+    N, K = W.shape
+    nb = K // bs
+    packed = np.zeros((N, nb * bs * 3 // 8), np.uint8)
+    scales = np.zeros((N, nb), np.float32 if s_dtype == "f32" else np.uint16)
+    bad = np.zeros((N, nb), np.uint8)
+    _check(_lib().orc_quantize_int3(_ptr(W), DTYPES[w_dtype], N, K, bs, DTYPES[s_dtype], _ptr(packed),
+                                    _ptr(scales), _ptr(bad)), "quantize_int3")
+    return packed, scales, bad.astype(bool)

@@ -24,6 +24,11 @@
  *  - "feat(qwen4): component kernels extracted from the brick PRs"
  *    (pegainfer PR 1242): MoE routing is an fp32 softmax, a canonical top-k and
  *    an optional renormalisation of the selected probabilities.
+ *  - The same page's quoted Olive producer summary (symmetric grouped INT3
+ *    round-to-nearest): scale max|w| / 3.5, implicit zero point 4, all-zero
+ *    block scale 1/3.5 with code 4, stored-scale rounding, rejection of
+ *    non-finite weights or scales and of nonzero blocks whose stored scale
+ *    rounds to zero, subnormal stored scales kept.
  *
  * Readings taken where the pages are silent (each one is listed in the design
  * notes): nibble order low-first (even k in the low nibble); implicit zero point
@@ -376,4 +381,104 @@ int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* lo
         free(x); free(wg); free(wu); free(h); free(w2); free(idx); free(rw); free(taken);
     }
     return bad;
+}
+
+/* --------------------------------------------- INT3 producer (quantizer) */
+
+/* binary32 -> binary16 bit pattern, rounded to nearest with ties to even (the
+ * IEEE 754 default): normal values 2^-14 .. 65504 keep 10 fraction bits,
+ * smaller ones become subnormals m * 2^-24, values that round past 65504
+ * become infinity.  A subnormal that rounds up to m = 1024 is exactly the
+ * smallest normal, whose encoding is the same integer. */
+static uint16_t float_to_f16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    const double a = fabs((double)f);
+    if (f != f) return (uint16_t)(sign | 0x7E00u);
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+    if (a < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)nearbyint(ldexp(a, 24)));
+    int e;
+    frexp(a, &e); /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    double m = nearbyint(ldexp(a, 10 - E)); /* 1024 .. 2048 */
+    if (m == 2048.0) {
+        m = 1024.0;
+        ++E;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(m - 1024.0));
+}
+
+/* binary32 -> bfloat16 bit pattern: the upper 16 bits, the dropped 16 rounded
+ * to nearest with ties to even (a carry may reach the exponent, and past the
+ * largest finite value gives infinity); NaN stays NaN. */
+static uint16_t float_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (f != f) return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t hi = u >> 16;
+    const uint32_t low = u & 0xFFFFu;
+    if (low > 0x8000u || (low == 0x8000u && (hi & 1u))) ++hi;
+    return (uint16_t)hi;
+}
+
+/* Symmetric grouped INT3 round-to-nearest, as the Olive producer summary
+ * quoted in "INT3 QMoE CUDA correctness baseline and Qwen experimental
+ * results" states it: for each block of bs weights of a row, scale = max|w| / 3.5,
+ * rounded to the stored scale dtype; code = round(w / stored scale) + 4,
+ * clamped to 0..7, so that (code - 4) * scale reconstructs w; an all-zero
+ * block stores scale 1/3.5 and code 4.  A block with a non-finite weight, a
+ * non-finite stored scale, or a nonzero block whose stored scale rounds to
+ * zero is rejected: bad[n * nb + b] = 1, its codes are then 4.  Subnormal
+ * stored scales are kept.  The arithmetic is binary32 (max|w| exact, each
+ * division correctly rounded, rounding to an integer with ties to even).
+ * Requires K % bs == 0; W is [N, K] in w_dtype, packed [N, nb, 3*bs/8],
+ * scales [N, nb] in s_dtype. */
+int orc_quantize_int3(const void* W, int w_dtype, int64_t N, int64_t K, int bs, int s_dtype,
+                      uint8_t* packed, void* scales, uint8_t* bad) {
+    if (check_format(3, bs) || K % bs != 0) return 1;
+    const int64_t nb = K / bs, blob = blob_bytes(3, bs), rb = nb * blob;
+    memset(packed, 0, (size_t)(N * rb));
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const int64_t w0 = n * K + b * bs;
+            float amax = 0.0f;
+            int nonfinite = 0;
+            for (int i = 0; i < bs; ++i) {
+                const float w = (float)load_elem(W, w_dtype, w0 + i);
+                if (!isfinite(w))
+                    nonfinite = 1;
+                else if (fabsf(w) > amax)
+                    amax = fabsf(w);
+            }
+            const float s = amax > 0.0f ? amax / 3.5f : 1.0f / 3.5f;
+            float stored;
+            if (s_dtype == ORC_F32) {
+                ((float*)scales)[n * nb + b] = s;
+                stored = s;
+            } else if (s_dtype == ORC_F16) {
+                const uint16_t h = float_to_f16_bits(s);
+                ((uint16_t*)scales)[n * nb + b] = h;
+                stored = (float)f16_to_double(h);
+            } else {
+                const uint16_t h = float_to_bf16_bits(s);
+                ((uint16_t*)scales)[n * nb + b] = h;
+                stored = (float)bf16_to_double(h);
+            }
+            const int rejected = nonfinite || !isfinite(stored) || (amax > 0.0f && stored == 0.0f);
+            bad[n * nb + b] = (uint8_t)rejected;
+            uint8_t* blk = packed + n * rb + b * blob;
+            for (int i = 0; i < bs; ++i) {
+                int q = 4;
+                if (!rejected) {
+                    const float w = (float)load_elem(W, w_dtype, w0 + i);
+                    const float r = rintf(w / stored);
+                    q = r < -4.0f ? 0 : r > 3.0f ? 7 : (int)r + 4;
+                }
+                stream_put(blk, i, 3, q);
+            }
+        }
+    }
+    return 0;
 }

@@ -363,3 +363,116 @@ def test_qmoe_unnormalised_weights_are_softmax_probabilities():
     # with k = E and no renormalisation the weights are the full softmax, which sums to one,
     # so the result equals the renormalised one up to rounding
     assert np.allclose(one(E, False), one(E, True), rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------- INT3 quantizer (producer)
+# The symmetric grouped INT3 round-to-nearest policy quoted in "INT3 QMoE CUDA
+# correctness baseline and Qwen experimental results" (Olive producer summary).
+
+def _f16_bits(x32):
+    with np.errstate(over="ignore"):  # values past 65504 become infinity, as they should
+        return np.asarray(x32, np.float32).astype(np.float16).view(np.uint16)
+
+
+def _bf16_bits(x32):
+    return torch.from_numpy(np.asarray(x32, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_int3_worked_example():
+    """max|w| = 3.5 gives scale 1: codes are round(w) + 4 with ties to even, +3.5
+    saturating at 7 and -3.5 landing on 0."""
+    w = np.zeros((1, 32), np.float32)
+    w[0, :8] = [3.5, -3.5, 1.0, 1.5, 2.5, -0.5, 0.0, -2.5]
+    packed, scales, bad = oracle.quantize_int3(w, "f32", 32, "f16")
+    assert not bad.any() and scales[0, 0] == 0x3C00  # binary16 1.0
+    codes = oracle.unpack_codes(packed, 1, 32, 3, 32)[0]
+    assert list(codes[:8]) == [7, 0, 5, 6, 6, 4, 4, 2]
+    assert (codes[8:] == 4).all()
+
+
+def test_quantize_int3_all_zero_block_stores_one_over_three_and_a_half():
+    w = np.zeros((2, 64), np.float32)
+    w[1, 40] = 1.0  # second row: the first block is zero, the second is not
+    for s_dtype, bits_of in (("f16", _f16_bits), ("bf16", _bf16_bits)):
+        packed, scales, bad = oracle.quantize_int3(w, "f32", 32, s_dtype)
+        assert not bad.any()
+        one_over = bits_of(np.float32(1.0) / np.float32(3.5))
+        assert scales[0, 0] == one_over and scales[0, 1] == one_over and scales[1, 0] == one_over
+        assert scales[1, 1] == bits_of(np.float32(1.0) / np.float32(3.5))  # max|w| = 1 as well
+        codes = oracle.unpack_codes(packed, 2, 64, 3, 32)
+        assert (codes[0] == 4).all() and (codes[1, :32] == 4).all()
+        assert codes[1, 40] == 7  # 1 / (1/3.5) = 3.5 saturates
+
+
+@pytest.mark.parametrize("s_dtype", ["f16", "bf16"])
+def test_quantize_int3_stored_scale_rounding_matches_library_casts(s_dtype):
+    """Per-block scales over many magnitudes (subnormal, normal, overflowing
+    binary16) equal numpy's / torch's round-to-nearest-even casts of the binary32
+    quotient max|w| / 3.5."""
+    g = np.random.default_rng(31)
+    N, bs = 400, 32
+    mag = np.float32(10.0) ** g.uniform(-9, 6, size=N).astype(np.float32)
+    w = (g.standard_normal((N, bs)).astype(np.float32) * mag[:, None]).astype(np.float32)
+    packed, scales, bad = oracle.quantize_int3(w, "f32", bs, s_dtype)
+    q = np.abs(w).max(axis=1).astype(np.float32) / np.float32(3.5)
+    ref = _f16_bits(q) if s_dtype == "f16" else _bf16_bits(q)
+    assert np.array_equal(scales[:, 0], ref)
+    stored = (ref.view(np.float16).astype(np.float64) if s_dtype == "f16" else as_f64(ref, "bf16"))
+    assert np.array_equal(bad[:, 0], ~np.isfinite(stored) | (stored == 0))
+    if s_dtype == "f16":
+        assert (stored[~bad[:, 0]] < 2.0 ** -14).any() and bad[:, 0].any()  # subnormals kept, some rejected
+
+
+@pytest.mark.parametrize("s_dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_quantize_int3_codes_are_the_nearest_levels(s_dtype, bs):
+    """Every code picks, among the eight levels (q - 4) * scale, the one nearest
+    to w in units of the binary32 quotient w / scale; an exact half goes to the
+    even level; the reconstruction error is at most half a scale step except at
+    the saturated top."""
+    g = np.random.default_rng(bs * 7 + len(s_dtype))
+    N, K = 9, 4 * bs
+    w = g.standard_normal((N, K)).astype(np.float32)
+    packed, scales, bad = oracle.quantize_int3(w, "f32", bs, s_dtype)
+    assert not bad.any()
+    codes = oracle.unpack_codes(packed, N, K, 3, bs).astype(np.int64)
+    s = scales.astype(np.float64) if s_dtype == "f32" else (
+        scales.view(np.float16).astype(np.float64) if s_dtype == "f16" else as_f64(scales, "bf16"))
+    s32 = np.repeat(s, bs, axis=1).astype(np.float32)
+    r = (w / s32).astype(np.float64)
+    levels = np.arange(-4, 4, dtype=np.float64)
+    dist = np.abs(r[..., None] - levels)
+    best = dist.min(axis=-1)
+    chosen = dist[np.arange(N)[:, None], np.arange(K)[None, :], codes]
+    assert np.array_equal(chosen, best)
+    ties = (dist == best[..., None]).sum(axis=-1) > 1
+    assert ((codes[ties] - 4) % 2 == 0).all()
+    err = np.abs(w - np.repeat(s, bs, axis=1) * (codes - 4))
+    top = codes == 7
+    assert (err[~top] <= 0.5 * np.repeat(s, bs, axis=1)[~top] * (1 + 1e-6)).all()
+
+
+def test_quantize_int3_rejects_non_finite_and_zero_rounded_blocks():
+    w = np.ones((4, 64), np.float32)
+    w[0, 3] = np.nan
+    w[1, 40] = np.inf
+    w[2, :32] = 1e-9  # binary16 scale 2.9e-10 rounds to zero
+    w[3, :32] = 3.5e-6  # scale 1e-6: a binary16 subnormal, kept
+    packed, scales, bad = oracle.quantize_int3(w, "f32", 32, "f16")
+    assert bad.tolist() == [[True, False], [False, True], [True, False], [False, False]]
+    assert scales[3, 0] < 0x0400  # subnormal binary16 pattern
+    codes = oracle.unpack_codes(packed, 4, 64, 3, 32)
+    assert (codes[0, :32] == 4).all() and (codes[2, :32] == 4).all()
+    # the same tiny block is representable with a bfloat16 scale
+    _, _, bad_bf = oracle.quantize_int3(w[2:3], "f32", 32, "bf16")
+    assert not bad_bf.any()
+
+
+@pytest.mark.parametrize("w_dtype", ["f16", "bf16"])
+def test_quantize_int3_half_inputs_equal_their_binary32_values(w_dtype):
+    g = np.random.default_rng(5)
+    w16 = wl.normal(g, (5, 128), w_dtype)
+    a = oracle.quantize_int3(w16, w_dtype, 64, "f16")
+    b = oracle.quantize_int3(as_f64(w16, w_dtype).astype(np.float32).reshape(5, 128), "f32", 64, "f16")
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
