@@ -264,9 +264,10 @@ def event_time_us(torch, stream, fn, reps, warmup=3):
 
 def other_rows(torch, mnb, dev):
     """The rest of the hot path, each against its own roofline: the tensor-core
-    GEMM at small M (M=16, HBM-bound) and prefill (M=2048, bf16), and one
+    GEMM at small M (M=16, HBM-bound) and prefill (M=2048, bf16), one
     Qwen3-30B-A3B-shaped QMoE layer at decode (T=1, CUDA graph over 16 distinct
-    layers) and prefill (T=4096)."""
+    layers) and prefill (T=4096), and the INT3 quantizer over one layer's FC1
+    expert weights."""
     gen = torch.Generator().manual_seed(7)
     stream = torch.cuda.Stream(device=dev)
     hbm, hbm_kind = peaks()
@@ -363,6 +364,24 @@ def other_rows(torch, mnb, dev):
                 "bound": "tensor", "peak_source": f"{tc_kind} bf16_tflops"}
         del X, logits, Y, ws
     del layers
+    torch.cuda.empty_cache()
+    # the INT3 producer: every expert's FC1 weights of one layer (128 x 1536 x 2048 fp16,
+    # 805 MB, larger than L2) quantised to packed INT3 codes and fp16 scales, bs 64
+    E, H, I = MOE["E"], MOE["H"], MOE["I"]
+    N = E * 2 * I
+    gq = torch.Generator(device=dev).manual_seed(17)
+    Wq = (torch.randn((N, H), generator=gq, device=dev, dtype=torch.float16) * 0.02)
+    Bq = torch.empty((N, H // 64, 24), dtype=torch.uint8, device=dev)
+    Sq = torch.empty((N, H // 64), dtype=torch.float16, device=dev)
+    us, p10, p90 = event_time_us(torch, stream,
+                                 lambda: mnb.mnb_quantize_int3(Wq, 64, mnb.F16, Bq, Sq, stream=stream), reps=10)
+    qbytes = N * H * 2 + Bq.numel() + Sq.numel() * 2
+    rows["quantize_int3_fc1_layer"] = {
+        "kernel": "quantize_int3_kernel (symmetric grouped INT3 round-to-nearest)",
+        "shape": f"{E} experts x {2 * I} rows x K={H}, fp16 weights -> INT3 bs64 + fp16 scales", "us": us,
+        "us_p10_p90": [p10, p90], "achieved": qbytes / (us * 1e-6) / 1e9, "unit": "GB/s", "peak": hbm,
+        "frac": qbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm", "peak_source": f"{hbm_kind} hbm_gbs"}
+    del Wq, Bq, Sq
     torch.cuda.empty_cache()
     if mnb.mnb_get_last_device_error(stream) != 0:
         raise RuntimeError("device error word set in the other rows")

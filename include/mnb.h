@@ -74,7 +74,8 @@ typedef enum {
     MNB_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
     MNB_ERR_CUDA = 5,          /* a CUDA runtime call failed */
     MNB_ERR_TIMEOUT = 6,       /* a bounded on-device wait gave up */
-    MNB_ERR_CONTENT = 7        /* mnb_validate_host found malformed content */
+    MNB_ERR_CONTENT = 7        /* malformed content: mnb_validate_host, or a block
+                                  mnb_quantize_int3 rejected (device error word) */
 } mnb_status;
 
 typedef enum { MNB_F32 = 0, MNB_F16 = 1, MNB_BF16 = 2 } mnb_dtype;
@@ -188,6 +189,28 @@ mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, in
 /* codes uint8 [rows, K] = the raw codes of B_packed (layout above), bit-exact. */
 mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits,
                             int block_size, uint8_t* codes, mnb_stream_t stream);
+
+/* Symmetric grouped INT3 round-to-nearest quantisation, the producer policy
+ * quoted in "INT3 QMoE CUDA correctness baseline and Qwen experimental
+ * results" (Olive summary): for every block of block_size weights of a row,
+ * scale = max|w| / 3.5 (binary32) rounded to scale_dtype (nearest, ties to
+ * even), code = round(w / stored scale) + 4 (binary32 quotient, ties to even)
+ * clamped to 0..7, packed like B_packed above (implicit zero point 4, so
+ * (code - 4) * scale reconstructs w); an all-zero block stores scale 1/3.5
+ * and code 4.
+ *   W          device, [N, K] in w_dtype (f32, f16 or bf16), 16-byte aligned.
+ *   B_packed   device, out, [N, K/block_size, 3*block_size/8], 4-byte aligned.
+ *   scales     device, out, [N, K/block_size] in scale_dtype, aligned to its
+ *              element size.
+ * K must be a multiple of block_size (32, 64 or 128), else
+ * MNB_ERR_UNSUPPORTED.  Content errors are found on the device: a block with
+ * a non-finite weight or stored scale, or a nonzero block whose stored scale
+ * rounds to zero (subnormal stored scales are kept), gets codes 4 and sets
+ * the device error word to MNB_ERR_CONTENT (read it with
+ * mnb_get_last_device_error); the other blocks are unaffected.  Asynchronous
+ * on `stream`; the caller owns every buffer. */
+mnb_status mnb_quantize_int3(const void* W, mnb_dtype w_dtype, int64_t N, int64_t K, int block_size,
+                             uint8_t* B_packed, void* scales, mnb_dtype scale_dtype, mnb_stream_t stream);
 
 /* Host-side content check of one packed projection (host buffers): exact
  * sizes are implied by the arguments; scales must be finite and >= 0; every

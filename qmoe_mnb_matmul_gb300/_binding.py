@@ -47,6 +47,7 @@ _SIGNATURES = {
     "qmoe_route": [_P, _I64, _I64, _I, _I, _P, _P, _P],
     "qmoe_permute": [_P, _I64, _I, _I64, _P, _P, _P, _P],
     "mnb_unpack_codes": [_P, _I64, _I64, _I, _I, _P, _P],
+    "mnb_quantize_int3": [_P, _I, _I64, _I64, _I, _P, _P, _I, _P],
     "mnb_validate_host": [_P, _P, _I, _P, _I64, _I64, _I, _I],
     "mnb_get_last_device_error": [_P],
     "mnb_status_string": [_I],
@@ -233,6 +234,25 @@ def mnb_unpack_codes(B_packed, rows, K, bits, block_size, codes, stream=None, *,
     if check:
         _check(st, "mnb_unpack_codes")
     return st
+
+
+def mnb_quantize_int3(W, block_size, scale_dtype, B_packed=None, scales=None, stream=None, *, check=True):
+    """INT3 quantisation of the 2-D tensor W [N, K] (f32/f16/bf16); returns
+    (B_packed uint8 [N, K/bs, 3*bs/8], scales [N, K/bs] in scale_dtype), allocating
+    the outputs with torch when they are not given."""
+    import torch
+    N, K = W.shape
+    nb = K // block_size
+    sdt = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[scale_dtype]
+    if B_packed is None:
+        B_packed = torch.empty((N, nb, 3 * block_size // 8), dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((N, nb), dtype=sdt, device=W.device)
+    st = load_library().mnb_quantize_int3(_ptr(W), _dtype_code(W), N, K, block_size, _ptr(B_packed), _ptr(scales),
+                                          scale_dtype, _stream(stream))
+    if check:
+        _check(st, "mnb_quantize_int3")
+    return B_packed, scales
 
 
 def mnb_validate_host(B_packed, scales, scale_dtype, zero_points, N, K, bits, block_size) -> int:

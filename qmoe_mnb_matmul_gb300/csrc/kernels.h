@@ -123,5 +123,12 @@ cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t
 cudaError_t gemv_take_error(unsigned int* out);
 cudaError_t qmoe_take_error(unsigned int* out);
 cudaError_t gemm_tc_take_error(unsigned int* out);
+cudaError_t quant_take_error(unsigned int* out);
+
+// --------------------------------------------------------------- quantizer
+// Symmetric grouped INT3 round-to-nearest of W [N, K] (K % bs == 0) into
+// packed codes B [N, K/bs, 3*bs/8] and scales S [N, K/bs].
+cudaError_t launch_quantize_int3(const void* W, int w_dtype, int64_t N, int64_t K, int bs, uint8_t* B, void* S,
+                                 int s_dtype, int sm_count, cudaStream_t stream);
 
 }  // namespace mnb

@@ -96,7 +96,8 @@ mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
     unsigned int first = 0;
-    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error};
+    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error,
+                                              quant_take_error};
     for (auto take : takers) {
         unsigned int v = 0;
         if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;
@@ -197,6 +198,20 @@ mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, in
         return MNB_ERR_SIZE_OVERFLOW;
     return from_cuda(launch_unpack_codes(B_packed, rows, K, bits, block_size, codes,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status mnb_quantize_int3(const void* W, mnb_dtype w_dtype, int64_t N, int64_t K, int block_size,
+                             uint8_t* B_packed, void* scales, mnb_dtype scale_dtype, mnb_stream_t stream) {
+    if (!W || !B_packed || !scales || N < 1 || K < 1) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(w_dtype) || !valid_dtype(scale_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bs(block_size) || K % block_size != 0) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(W, 16) || !aligned(B_packed, 4) || !aligned(scales, dsize(scale_dtype))) return MNB_ERR_INVALID_ARG;
+    int64_t wbytes;
+    if (!mul_ok(N, K, &wbytes) || !mul_ok(wbytes, int64_t(dsize(w_dtype)), &wbytes)) return MNB_ERR_SIZE_OVERFLOW;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+    return from_cuda(launch_quantize_int3(W, w_dtype, N, K, block_size, B_packed, scales, scale_dtype, sms,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk, int32_t* topk_idx,

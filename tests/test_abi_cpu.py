@@ -113,6 +113,19 @@ def test_route_permute_unpack_metadata_errors(lib):
     assert lib.mnb_unpack_codes(None, 4, 64, 4, 32, FAKE, None) == INVALID
 
 
+def test_quantize_int3_metadata_errors(lib):
+    q = lib.mnb_quantize_int3
+    assert q(None, 0, 4, 64, 32, FAKE, FAKE, 1, None) == INVALID
+    assert q(FAKE, 0, 4, 64, 32, None, FAKE, 1, None) == INVALID
+    assert q(FAKE, 0, 0, 64, 32, FAKE, FAKE, 1, None) == INVALID
+    assert q(FAKE, 3, 4, 64, 32, FAKE, FAKE, 1, None) == INVALID       # no such dtype
+    assert q(FAKE, 0, 4, 64, 48, FAKE, FAKE, 1, None) == UNSUPPORTED   # block size
+    assert q(FAKE, 0, 4, 80, 32, FAKE, FAKE, 1, None) == UNSUPPORTED   # K not a multiple of the block
+    assert q(FAKE + 4, 0, 4, 64, 32, FAKE, FAKE, 1, None) == INVALID   # W not 16-byte aligned
+    assert q(FAKE, 0, 4, 64, 32, FAKE + 2, FAKE, 1, None) == INVALID   # B_packed not 4-byte aligned
+    assert q(FAKE, 0, 1 << 40, 1 << 30, 32, FAKE, FAKE, 1, None) == OVERFLOW
+
+
 # ------------------------------------------------------- host validator
 
 @pytest.mark.parametrize("bits", [3, 4])
