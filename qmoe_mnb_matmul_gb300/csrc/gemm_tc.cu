@@ -35,7 +35,6 @@ TcShape pick_shape(int64_t M, int64_t N, int sm_count) {
     const TcShape cands[] = {{256, 1}, {128, 1}, {64, 1}, {32, 1}, {16, 1}};
     for (const TcShape& c : cands) {
         if (c.G == 1 && c.BN > 16 && c.BN / 2 >= M) continue;  // a narrower tile covers M already
-        if (c.G == 2 && M <= 256) continue;
         const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(c.BN) * c.G);
         const double waves = double(cdiv<int64_t>(tiles, sm_count));
         const double eff = c.BN >= 256 ? 1.0 : c.BN >= 128 ? 0.9 : c.BN >= 64 ? 0.7 : 0.5;

@@ -11,10 +11,12 @@
 // the dequantised weight tile is operand A (M = 128) and each of the G
 // activation sub-tiles operand B (N = BN <= 256), so the fp32 accumulators in
 // tensor memory hold Y^T (lane = weight row, column = activation row) and small
-// M costs no padding on the weight side.  With G = 2 every dequantised weight
-// K step feeds two MMAs (512 accumulator columns), halving the dequantisation
-// per FLOP; with G = 1 the two 256-column halves of tensor memory double-buffer
-// consecutive tiles.  One persistent CTA per SM walks the tiles.
+// M costs no padding on the weight side.  The kernel supports G = 2 (every
+// dequantised weight K step feeding two MMAs, 512 accumulator columns), but
+// the launcher always takes G = 1, whose two 256-column halves of tensor
+// memory double-buffer consecutive tiles: with only two activation stages
+// beside G = 2's tiles it measured slower.  One persistent CTA per SM walks
+// the tiles.
 //
 // Warp roles (736 threads):
 //   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle); in
@@ -774,7 +776,6 @@ cudaError_t launch_bn(int BN, int G, const TcArgs& a, const void* A_rows, int64_
     if constexpr (MODE == kModeFc1) {
         return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);  // grouped: 256 rows
     } else {
-        if (G == 2) return launch_cfg<BITS, ST, AT, 256, 2, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
         switch (BN) {
             case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
             case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
