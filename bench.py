@@ -388,7 +388,7 @@ def other_rows(torch, mnb, dev):
     return rows
 
 
-PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill")
+PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "quantize_int3")
 
 
 def profile_case(name):
@@ -415,6 +415,13 @@ def profile_case(name):
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         for _ in range(3):
             mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y)
+    elif name == "quantize_int3":  # 65536 x 2048 weights, fp16 then fp32, INT3 bs64, fp16 scales: 2 launches
+        gq = torch.Generator(device=dev).manual_seed(17)
+        for wdt in (torch.float16, torch.float32):
+            W = torch.randn((65536, 2048), generator=gq, device=dev, dtype=wdt) * 0.02
+            mnb.mnb_quantize_int3(W, 64, mnb.F16)
+            torch.cuda.synchronize()
+            del W
     else:  # one Qwen3-30B-A3B-shaped QMoE layer, INT3/INT3 bs64 fp16
         T = 1 if name == "qmoe_decode" else 4096
         H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
