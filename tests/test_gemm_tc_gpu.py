@@ -67,6 +67,14 @@ def test_tails(M, K, N, bs):
     check(M, K, N, 4, bs)
 
 
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("N", [1, 48, 127])
+def test_fewer_weight_rows_than_a_tile(bits, N):
+    """N < 128: the packed-row and scale tiles of the single weight tile run past
+    the matrix and read zeros there; all N outputs of the sampled rows are checked."""
+    check(64, 1024, N, bits, 64, "bf16", "bf16", "bf16", with_zp=bits == 3)
+
+
 @pytest.mark.parametrize("M", [8, 9, 17, 100, 255, 257, 1000])
 def test_row_counts(M):
     check(M, 1024, 768, 4, 32)
