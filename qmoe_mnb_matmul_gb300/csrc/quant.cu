@@ -150,13 +150,15 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_int3_kernel(const void
         // formed without a division by Markstein's correction step (Markstein,
         // "Computation of elementary functions on the IBM RISC System/6000
         // processor", 1990; Muller et al., "Handbook of Floating-Point
-        // Arithmetic", division by an fma): with y = RN(1/stored), q0 =
-        // RN(w y) and the exact residual r = w - stored * q0 (one fma),
-        // RN(q0 + r y) is the correctly rounded quotient.  Scales whose
-        // reciprocal is not a normal number, or whose significand is all ones,
-        // keep the IEEE division.  Adding 1.5 * 2^23 then rounds the quotient
-        // (|q| < 6 for an accepted block) to an integer in the low mantissa
-        // bits, ties to even.
+        // Arithmetic", division with an fma): when y = RN(1/stored) and q is
+        // within one ulp of w / stored, the residual r = w - stored * q is
+        // exact in one fma and RN(q + r y) is the correctly rounded quotient.
+        // q0 = RN(w y) can be up to two ulps off near the top of a binade, so
+        // the step is applied twice: the first brings q within one ulp, the
+        // second rounds correctly.  Scales whose reciprocal is not a normal
+        // number, or whose significand is all ones, keep the IEEE division.
+        // Adding 1.5 * 2^23 then rounds the quotient (|q| < 6 for an accepted
+        // block) to an integer in the low mantissa bits, ties to even.
         constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
         const float y = 1.0f / stored;
         const bool direct = rejected || !(fabsf(y) < 0x1p100f && fabsf(y) > 0x1p-100f) ||
@@ -168,7 +170,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_int3_kernel(const void
             for (int j = 0; j < 32; ++j) {
                 const float w = weight_at<WD>(raw, j);
                 const float q0 = w * y;
-                const float q = fmaf(fmaf(-q0, stored, w), y, q0);
+                const float q1 = fmaf(fmaf(-q0, stored, w), y, q0);
+                const float q = fmaf(fmaf(-q1, stored, w), y, q1);
                 const float m = q + kMagic;
                 put_code(word, j, static_cast<uint32_t>(min(max(__float_as_int(m) - kBias, 0), 7)));
             }
