@@ -18,7 +18,7 @@
  * kernel ahead of them on the stream, so a call's prologue may run while the
  * previous library call is still finishing: every call may warm L2 with its
  * packed weights, and the QMoE decode path routes its tokens and copies the
- * selected experts' FC2 rows.  Activations and workspace are read only after
+ * selected experts' FC1 and FC2 rows.  Activations and workspace are read only after
  * the previous call has completed.  Hence packed weights, scales, zero points
  * and router logits must not be outputs of the immediately preceding library
  * call on the same stream (outputs of any other kernel are fine).  Setting

@@ -6,18 +6,24 @@
 // ever written to global memory ("prohibit all-expert floating-weight
 // materialization").
 //
-// Two SIMT plans share the packed-row machinery of gemv_core.cuh:
-//  * decode (T <= 8, k <= 8): two kernels.  Every CTA routes its own token
-//    (one warp, a few hundred logits), so no routing kernel sits on the
+// Three plans:
+//  * decode (T <= 8, k <= 8), SIMT, on the packed-row machinery of
+//    gemv_core.cuh: two kernels.  Every CTA routes its own token (the whole
+//    CTA ranks up to 256 logits at once), so no routing kernel sits on the
 //    critical path.  FC1 runs over (token, slot) x row blocks of the selected
 //    expert and writes h = silu(gate) * up in fp32.  FC2 runs over tokens x
-//    row blocks, streams the block's rows of all k selected experts and folds
-//    the weighted combine into its epilogue (fixed slot order).  FC2 is
-//    launched as a programmatic dependent: its prologue routes and pulls its
-//    experts' rows into L2 while FC1 is still running.
-//  * tiled (any T): route -> expert-sorted permutation -> tiles of <= 4 pairs
-//    of one expert -> FC1 tiles (gathered activations) -> FC2 tiles -> combine
-//    by token in fixed slot order.
+//    row blocks, stages the block's rows of all k selected experts and folds
+//    the weighted combine into its epilogue (fixed slot order).  Both are
+//    launched as programmatic dependents: before its dependency wait each CTA
+//    routes and starts the bulk copies of its expert rows into shared memory.
+//  * tensor-core (T > 8, 16-byte-aligned fp16/bf16 activation rows): route ->
+//    expert-sorted permutation over many CTAs -> m-tiles of <= 256 routed rows
+//    of one expert -> the routed rows copied into sorted order -> grouped
+//    tcgen05 FC1 (SwiGLU in the epilogue) -> grouped FC2 -> combine by token
+//    in fixed slot order.
+//  * tiled SIMT (any T, the remaining cases): route -> permutation -> tiles of
+//    <= 4 pairs of one expert -> FC1 tiles (gathered activations) -> FC2 tiles
+//    -> combine by token in fixed slot order.
 #include <algorithm>
 
 #include "common.cuh"
