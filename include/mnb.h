@@ -186,9 +186,18 @@ mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, in
 
 /* ------------------------------------------------------ diagnostics, tools */
 
-/* codes uint8 [rows, K] = the raw codes of B_packed (layout above), bit-exact. */
+/* Row-local LSB-first packing for any width 1..8 ("INT3 QMoE CUDA correctness
+ * baseline and Qwen experimental results", "P0: Portable Format and Numerical
+ * References": generic pack/unpack for widths 1..8).  Device buffers, caller
+ * owned; bits in 1..8 and block_size in {32, 64, 128}, else MNB_ERR_UNSUPPORTED.
+ * mnb_unpack_codes: codes uint8 [rows, K] = the raw codes of B_packed [rows,
+ * nb, block_size*bits/8] (layout above), bit-exact.
+ * mnb_pack_codes: B_packed from codes uint8 [rows, K], each code's low `bits`
+ * bits; the padding bits of a partial last block are written as zeros. */
 mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits,
                             int block_size, uint8_t* codes, mnb_stream_t stream);
+mnb_status mnb_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int bits, int block_size,
+                          uint8_t* B_packed, mnb_stream_t stream);
 
 /* Symmetric grouped INT3 round-to-nearest quantisation, the producer policy
  * quoted in "INT3 QMoE CUDA correctness baseline and Qwen experimental

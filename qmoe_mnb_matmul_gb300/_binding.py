@@ -47,6 +47,7 @@ _SIGNATURES = {
     "qmoe_route": [_P, _I64, _I64, _I, _I, _P, _P, _P],
     "qmoe_permute": [_P, _I64, _I, _I64, _P, _P, _P, _P],
     "mnb_unpack_codes": [_P, _I64, _I64, _I, _I, _P, _P],
+    "mnb_pack_codes": [_P, _I64, _I64, _I, _I, _P, _P],
     "mnb_quantize_int3": [_P, _I, _I64, _I64, _I, _P, _P, _I, _P],
     "mnb_validate_host": [_P, _P, _I, _P, _I64, _I64, _I, _I],
     "mnb_get_last_device_error": [_P],
@@ -233,6 +234,13 @@ def mnb_unpack_codes(B_packed, rows, K, bits, block_size, codes, stream=None, *,
     st = load_library().mnb_unpack_codes(_ptr(B_packed), rows, K, bits, block_size, _ptr(codes), _stream(stream))
     if check:
         _check(st, "mnb_unpack_codes")
+    return st
+
+
+def mnb_pack_codes(codes, rows, K, bits, block_size, B_packed, stream=None, *, check=True):
+    st = load_library().mnb_pack_codes(_ptr(codes), rows, K, bits, block_size, _ptr(B_packed), _stream(stream))
+    if check:
+        _check(st, "mnb_pack_codes")
     return st
 
 

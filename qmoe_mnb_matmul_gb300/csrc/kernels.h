@@ -103,6 +103,8 @@ cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dty
                               int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream);
 
 // --------------------------------------------------------------- unpack
+cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int bits, int bs, uint8_t* packed,
+                              cudaStream_t stream);
 cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
                                 uint8_t* codes, cudaStream_t stream);
 

@@ -191,7 +191,7 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
 mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits, int block_size,
                             uint8_t* codes, mnb_stream_t stream) {
     if (!B_packed || !codes || rows < 1 || K < 1) return MNB_ERR_INVALID_ARG;
-    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (bits < 1 || bits > 8 || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     ProjBytes pb;
     int64_t tmp;
     if (!proj_bytes(rows, K, bits, block_size, MNB_F32, &pb) || !mul_ok(rows, K, &tmp))
@@ -212,6 +212,18 @@ mnb_status mnb_quantize_int3(const void* W, mnb_dtype w_dtype, int64_t N, int64_
     if (sms <= 0) return MNB_ERR_CUDA;
     return from_cuda(launch_quantize_int3(W, w_dtype, N, K, block_size, B_packed, scales, scale_dtype, sms,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status mnb_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int bits, int block_size,
+                          uint8_t* B_packed, mnb_stream_t stream) {
+    if (!codes || !B_packed || rows < 1 || K < 1) return MNB_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 8 || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    ProjBytes pb;
+    int64_t tmp;
+    if (!proj_bytes(rows, K, bits, block_size, MNB_F32, &pb) || !mul_ok(rows, K, &tmp))
+        return MNB_ERR_SIZE_OVERFLOW;
+    return from_cuda(launch_pack_codes(codes, rows, K, bits, block_size, B_packed,
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk, int32_t* topk_idx,

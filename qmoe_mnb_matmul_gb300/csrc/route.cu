@@ -35,6 +35,27 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ packed, int64_t rows, 
     }
 }
 
+// Output byte b of a packed row holds stream bits 8b .. 8b+7, i.e. parts of the
+// codes k with bits*k in [8b - bits + 1, 8b + 7]; codes past K (the padding of a
+// partial last block) contribute zeros, so the padding is canonical.
+__global__ void pack_kernel(const uint8_t* __restrict__ codes, int64_t rows, int64_t K, int bits,
+                            int64_t row_bytes, uint8_t* __restrict__ packed) {
+    const int64_t total = rows * row_bytes;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t n = i / row_bytes, b = i - n * row_bytes;
+        const int64_t k_lo = (8 * b) / bits, k_hi = min((8 * b + 7) / bits, K - 1);
+        uint32_t out = 0;
+        for (int64_t k = k_lo; k <= k_hi; ++k) {
+            const uint32_t q = codes[n * K + k] & mask;
+            const int64_t off = k * bits - 8 * b;  // the code's first bit relative to the byte
+            out |= off >= 0 ? (q << off) : (q >> -off);
+        }
+        packed[i] = static_cast<uint8_t>(out & 0xFFu);
+    }
+}
+
 // ----------------------------------------------------------------- routing
 
 // One warp per token (see route_core.cuh).
@@ -296,6 +317,17 @@ cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, 
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(total, threads), 65535 * 16);
     unpack_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(
         packed, rows, K, bits, row_bytes, codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int bits, int bs, uint8_t* packed,
+                              cudaStream_t stream) {
+    const int64_t nb = cdiv<int64_t>(K, bs);
+    const int64_t row_bytes = nb * bs * bits / 8;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(rows * row_bytes, threads), 65535 * 16);
+    pack_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(codes, rows, K, bits,
+                                                                                           row_bytes, packed);
     return cudaGetLastError();
 }
 

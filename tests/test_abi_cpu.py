@@ -109,8 +109,15 @@ def test_route_permute_unpack_metadata_errors(lib):
     assert lib.qmoe_route(FAKE, 1, 2048, 8, 1, FAKE, FAKE, None) == UNSUPPORTED
     assert lib.qmoe_permute(FAKE, 0, 8, 128, FAKE, FAKE, FAKE, None) == INVALID
     assert lib.qmoe_permute(FAKE, 1 << 30, 8, 128, FAKE, FAKE, FAKE, None) == OVERFLOW
-    assert lib.mnb_unpack_codes(FAKE, 4, 64, 7, 32, FAKE, None) == UNSUPPORTED
+    assert lib.mnb_unpack_codes(FAKE, 4, 64, 9, 32, FAKE, None) == UNSUPPORTED   # widths 1..8
+    assert lib.mnb_unpack_codes(FAKE, 4, 64, 0, 32, FAKE, None) == UNSUPPORTED
+    assert lib.mnb_unpack_codes(FAKE, 4, 64, 5, 16, FAKE, None) == UNSUPPORTED
     assert lib.mnb_unpack_codes(None, 4, 64, 4, 32, FAKE, None) == INVALID
+    assert lib.mnb_pack_codes(None, 4, 64, 4, 32, FAKE, None) == INVALID
+    assert lib.mnb_pack_codes(FAKE, 0, 64, 4, 32, FAKE, None) == INVALID
+    assert lib.mnb_pack_codes(FAKE, 4, 64, 9, 32, FAKE, None) == UNSUPPORTED
+    assert lib.mnb_pack_codes(FAKE, 4, 64, 6, 48, FAKE, None) == UNSUPPORTED
+    assert lib.mnb_pack_codes(FAKE, 1 << 40, 1 << 30, 8, 32, FAKE, None) == OVERFLOW
 
 
 def test_quantize_int3_metadata_errors(lib):

@@ -86,3 +86,23 @@ def test_unpack_codes_bit_exact(bits, bs, K):
     codes = torch.zeros((rows, K), dtype=torch.uint8, device="cuda")
     mnb.mnb_unpack_codes(to_dev(packed), rows, K, bits, bs, codes)
     assert np.array_equal(codes.cpu().numpy(), oracle.unpack_codes(packed, rows, K, bits, bs))
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_pack_and_unpack_every_width(bits, bs):
+    """Row-local LSB-first packing for widths 1..8 ("P0: Portable Format"):
+    the GPU pack equals the oracle's bytes (zero padding in a partial last
+    block, code bits above the width ignored) and the GPU unpack returns the
+    codes."""
+    g = wl.rng(zlib.crc32(repr(("pack", bits, bs)).encode()))
+    rows, K = 37, 3 * bs + 11
+    codes = g.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    ref = oracle.pack_codes(codes & ((1 << bits) - 1), bits, bs)
+    packed = torch.empty(ref.shape, dtype=torch.uint8, device="cuda")
+    mnb.mnb_pack_codes(to_dev(codes), rows, K, bits, bs, packed)
+    got = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+    mnb.mnb_unpack_codes(packed, rows, K, bits, bs, got)
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), ref)
+    assert np.array_equal(got.cpu().numpy(), codes & ((1 << bits) - 1))
