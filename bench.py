@@ -171,6 +171,22 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(pg, x: float, device) -> float:
+    """The largest of every rank's x, on every rank (x itself without a process group)."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(bytes_per_step: int, steps: int, ws: int, ms_max: float) -> float:
+    """Whole-job GB/s of ws replicas that each ran `steps` steps: every rank's
+    bytes over the slowest rank's time (weak scaling)."""
+    return bytes_per_step * steps * ws / (ms_max / 1e3) / 1e9
+
+
 # ------------------------------------------------------------ the oracle arm
 
 def oracle_sample(seconds: float = 12.0):
@@ -540,11 +556,7 @@ def main():
         barrier()
         clocks.stop()
         ms = e0.elapsed_time(e1)
-        if pg is not None:
-            t = torch.tensor([ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms, clocks.summary()
+        return max_over_ranks(pg, ms, dev), clocks.summary()
 
     # One step = the 140 layer projections (one graph) then the vocabulary head
     # (a second graph).  On sampled steps the head is launched directly between
@@ -572,7 +584,7 @@ def main():
     used = [a.elapsed_time(b) * 1e3 for a, b in hev[:min(n_ev, (args.steps + stride - 1) // stride)]]
     head_us = statistics.mean(used)
 
-    value = bytes_step * args.steps * ws / (ms / 1e3) / 1e9
+    value = replica_throughput(bytes_step, args.steps, ws, ms)
     peak, peak_kind = peaks()
     achieved = head_bytes / (head_us * 1e-6) / 1e9
 
@@ -591,7 +603,7 @@ def main():
             g_e2e.replay()
         e2e_steps = max(3, args.steps // 4)
         ms_e2e, _ = timed(lambda i: g_e2e.replay(), e2e_steps)
-    e2e_value = bytes_step * e2e_steps * ws / (ms_e2e / 1e3) / 1e9
+    e2e_value = replica_throughput(bytes_step, e2e_steps, ws, ms_e2e)
 
     if mnb.mnb_get_last_device_error(stream) != 0:
         raise RuntimeError("device error word set during the timed region")
