@@ -73,6 +73,7 @@ def _lib():
                 "orc_qmoe": [P, C, I64, I64, P, I64, C, C, P, P, P, C, P, P, P, C, I64, C, C, P,
                              I64, P, C],
                 "orc_quantize_int3": [P, C, I64, I64, C, C, P, P, P],
+                "orc_round_to_half_bits": [P, I64, C, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -237,3 +238,12 @@ def quantize_int3(W, w_dtype: str, bs: int, s_dtype: str):
     _check(_lib().orc_quantize_int3(_ptr(W), DTYPES[w_dtype], N, K, bs, DTYPES[s_dtype], _ptr(packed),
                                     _ptr(scales), _ptr(bad)), "quantize_int3")
     return packed, scales, bad.astype(bool)
+
+
+def round_to_half_bits(x, dtype: str) -> np.ndarray:
+    """binary32 values -> the bit patterns the quantizer stores for dtype
+    "f16" or "bf16" (round to nearest, ties to even)."""
+    x = _c(np.asarray(x, np.float32).reshape(-1), np.float32)
+    out = np.zeros(x.size, np.uint16)
+    _check(_lib().orc_round_to_half_bits(_ptr(x), x.size, 1 if dtype == "bf16" else 0, _ptr(out)), "round")
+    return out

@@ -423,6 +423,12 @@ static uint16_t float_to_bf16_bits(float f) {
     return (uint16_t)hi;
 }
 
+/* Exported for the pins: the rounding helpers above over arrays. */
+int orc_round_to_half_bits(const float* x, int64_t n, int bf16, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bf16 ? float_to_bf16_bits(x[i]) : float_to_f16_bits(x[i]);
+    return 0;
+}
+
 /* Symmetric grouped INT3 round-to-nearest, as the Olive producer summary
  * quoted in "INT3 QMoE CUDA correctness baseline and Qwen experimental
  * results" states it: for each block of bs weights of a row, scale = max|w| / 3.5,

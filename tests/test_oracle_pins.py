@@ -476,3 +476,30 @@ def test_quantize_int3_half_inputs_equal_their_binary32_values(w_dtype):
     b = oracle.quantize_int3(as_f64(w16, w_dtype).astype(np.float32).reshape(5, 128), "f32", 64, "f16")
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def _boundary_cases(patterns_f64):
+    """Every midpoint between adjacent representable values and its binary32
+    neighbours one ulp below and above, plus the values themselves."""
+    v = np.sort(np.unique(patterns_f64[np.isfinite(patterns_f64)]))
+    mids = ((v[:-1] + v[1:]) / 2).astype(np.float32)
+    xs = np.concatenate([v.astype(np.float32), mids, np.nextafter(mids, np.float32(-np.inf)),
+                         np.nextafter(mids, np.float32(np.inf))])
+    return xs[np.isfinite(xs)]
+
+
+def test_half_rounding_at_every_boundary_matches_numpy():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    xs = _boundary_cases(pats.view(np.float16).astype(np.float64))
+    xs = np.concatenate([xs, np.float32([65519.996, 65520.0, 65536.0, 1e30, -1e30, np.inf, -np.inf])])
+    with np.errstate(over="ignore"):
+        ref = xs.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.round_to_half_bits(xs, "f16"), ref)
+
+
+def test_bfloat16_rounding_at_every_boundary_matches_torch():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    xs = _boundary_cases(as_f64(pats, "bf16"))
+    xs = np.concatenate([xs, np.float32([3.4e38, -3.4e38, np.inf, -np.inf])])
+    ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_to_half_bits(xs, "bf16"), ref)
