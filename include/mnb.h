@@ -15,14 +15,14 @@
  * mnb_get_last_device_error(), which synchronises `stream`.
  *
  * Overlapped launches.  Kernels are launched as programmatic dependents of the
- * kernel ahead of them on the stream, so a call's prologue may run while the
- * previous library call is still finishing: every call may warm L2 with its
- * packed weights, and the QMoE decode path routes its tokens and copies the
- * selected experts' FC1 and FC2 rows.  Activations and workspace are read only after
- * the previous call has completed.  Hence packed weights, scales, zero points
- * and router logits must not be outputs of the immediately preceding library
- * call on the same stream (outputs of any other kernel are fine).  Setting
- * the environment variable MNB_DISABLE_PDL turns the overlap off.
+ * kernel ahead of them on the stream, so a call's prologue (barrier set-up,
+ * tensor-memory allocation, L2 prefetches of its packed weights) may run while
+ * the kernel ahead is still finishing.  No call reads any of its inputs before
+ * the work ahead of it on the stream has completed (an L2 prefetch reads
+ * nothing the call uses: L2 is coherent with every later write), so any
+ * tensor may be the output of the immediately preceding kernel, whether it
+ * belongs to this library or not.  Setting the environment variable
+ * MNB_DISABLE_PDL turns the overlap off.
  *
  * Layouts (all dense, row-major, C order):
  *   bs = block_size, nb = ceil(K / bs), blob = bs * bits / 8 bytes.
@@ -45,10 +45,12 @@
  *
  * Supported set.  bits in {3, 4}; block_size in {32, 64, 128}; activation and
  * output dtypes f32 / f16 / bf16 for mnb_matmul (f16 / bf16 for QMoE); scale
- * dtype f32 or equal to the activation dtype (QMoE: equal).  B_packed must be
- * 16-byte aligned, the other tensors aligned to their element size.  Anything
- * else returns MNB_ERR_UNSUPPORTED before any work is enqueued; no call ever
- * falls back to a CPU path or to a different kernel family silently.
+ * dtype f32 or equal to the activation dtype (QMoE: equal).  Alignment:
+ * B_packed and the scales (mnb_matmul; QMoE: fc1_w, fc2_w, fc1_scales and
+ * fc2_scales) must be 16-byte aligned, the QMoE workspace 256-byte aligned,
+ * every other tensor aligned to its element size.  Anything else returns
+ * MNB_ERR_UNSUPPORTED before any work is enqueued; no call ever falls back to
+ * a CPU path or to a different kernel family silently.
  *
  * Errors.  Metadata is validated on the host before any launch (payloads are
  * never read on the host, except by mnb_validate_host).  Launch failures return
@@ -92,7 +94,8 @@ typedef struct CUstream_st* mnb_stream_t;
 /* ------------------------------------------------------------ MatMulNBits */
 
 /* Bytes of device workspace mnb_matmul can use for this problem (0 = none, in
- * which case workspace may be NULL).  The bound depends only on the arguments.
+ * which case workspace may be NULL): the bounded workspace of "Qwen3
+ * Missing-Kernel Implementation Plan", row K03.  The bound depends only on the arguments.
  * Non-zero for tensor-core problems whose output tiles cannot fill the GPU
  * (small M, few output columns): K is then split across CTAs and the fp32
  * partial sums go to the workspace before one reduction.  A call given less
@@ -106,8 +109,10 @@ mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, 
  * with partial blocks and output tails).  Any M >= 1, K >= 1, N >= 1.
  * Accumulation is fp32; the dequantised weight is formed in fp32 (SIMT paths)
  * or rounded to bf16/fp16 in shared memory before a tensor-core contraction
- * (M >= 16 with f16/bf16 activations).  Y is written in y_dtype with
- * round-to-nearest-even.  `workspace` (16-byte aligned, see
+ * (M >= 16 with f16/bf16 activations); an fp32 Y from f16/bf16 activations
+ * adds, in a second tensor-core pass, the product with what that rounding
+ * left (itself rounded to 16 bits), so its weights carry ~16 significant
+ * bits.  Y is written in y_dtype with round-to-nearest-even.  `workspace` (16-byte aligned, see
  * mnb_matmul_workspace_size) holds split-K partial sums; the split changes the
  * order of the fp32 additions, not the rounding points. */
 mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
@@ -118,8 +123,11 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
 
 /* ------------------------------------------------------------------- QMoE */
 
-/* Bytes of device workspace qmoe_forward needs (routing tables, the SwiGLU
- * activations between FC1 and FC2, the FC2 outputs before the combine). */
+/* Bytes of device workspace qmoe_forward needs: the routing tables, the
+ * SwiGLU activations between FC1 and FC2 and the FC2 outputs before the
+ * combine (the bounded activation tiling of "INT3 QMoE CUDA correctness
+ * baseline and Qwen experimental results", Summary).  Depends only on the
+ * arguments; writes *bytes, touches no device memory. */
 mnb_status qmoe_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int k,
                                mnb_dtype act_dtype, size_t* bytes);
 
@@ -174,13 +182,26 @@ mnb_status qmoe_forward_static(const void* X, mnb_dtype act_dtype, int64_t T, in
                                const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
                                mnb_fc1_layout fc1_layout, void* Y, mnb_stream_t stream);
 
-/* The routing step alone: topk_idx int32 [T, k], topk_w fp32 [T, k]. */
+/* The routing step alone ("feat(qwen4): component kernels extracted from the
+ * brick PRs", MoE routing: softmax over the router logits in fp32, canonical
+ * top-k, optional renormalisation; the top-k of QMoE's Summary in "INT3 QMoE
+ * CUDA correctness baseline and Qwen experimental results"): logits fp32
+ * [T, E] in, topk_idx int32 [T, k] and topk_w fp32 [T, k] out, all device
+ * buffers owned by the caller.  Indices are the k largest logits in
+ * descending order, ties to the lower expert index; weights as in
+ * qmoe_forward.  1 <= k <= E, E <= 1024 (else MNB_ERR_UNSUPPORTED); NaN
+ * logits are not supported. */
 mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int normalize_topk,
                       int32_t* topk_idx, float* topk_w, mnb_stream_t stream);
 
-/* Expert-sorted order of routed (token, slot) pairs: counts int32 [E];
- * offsets int32 [E+1] = exclusive prefix sum of counts; perm int32 [T*k] lists
- * the flat pair index t*k + j grouped by expert, ascending inside an expert. */
+/* Expert-sorted order of routed (token, slot) pairs, the step that lets the
+ * prefill run one grouped GEMM per selected expert ("INT3 QMoE CUDA
+ * correctness baseline and Qwen experimental results", Not PR2-PR4
+ * Completion: the selected-expert prefill): topk_idx int32 [T, k] in (values
+ * in [0, E)); counts int32 [E]; offsets int32 [E+1] = exclusive prefix sum of
+ * counts; perm int32 [T*k] lists the flat pair index t*k + j grouped by
+ * expert, ascending inside an expert (a stable sort).  Device buffers owned by
+ * the caller; E <= 1024, T*k < 2^31. */
 mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, int32_t* counts,
                         int32_t* offsets, int32_t* perm, mnb_stream_t stream);
 
@@ -233,6 +254,16 @@ mnb_status mnb_validate_host(const uint8_t* B_packed, const void* scales, mnb_dt
 /* Synchronises `stream`, then returns and clears the device error word
  * (MNB_OK when no kernel recorded an error). */
 mnb_status mnb_get_last_device_error(mnb_stream_t stream);
+
+/* Diagnostic: enqueues one small kernel that runs the library's bounded
+ * on-chip wait on a barrier nothing ever completes, giving up after limit_ns
+ * nanoseconds (1e3 .. 1e9, else MNB_ERR_INVALID_ARG).  No copy, tensor-core
+ * operation or tensor-memory allocation is in flight while it waits.  The
+ * kernel records MNB_ERR_TIMEOUT in the device error word and returns
+ * normally, so the context stays usable: it exercises the failure path every
+ * pipelined kernel takes when a wait runs out.  The pages have no
+ * counterpart; this entry point exists for failure-detection tests. */
+mnb_status mnb_diag_wait_timeout(uint64_t limit_ns, mnb_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* mnb_status_string(mnb_status s);

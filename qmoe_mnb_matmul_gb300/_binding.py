@@ -51,6 +51,7 @@ _SIGNATURES = {
     "mnb_quantize_int3": [_P, _I, _I64, _I64, _I, _P, _P, _I, _P],
     "mnb_validate_host": [_P, _P, _I, _P, _I64, _I64, _I, _I],
     "mnb_get_last_device_error": [_P],
+    "mnb_diag_wait_timeout": [ctypes.c_uint64, _P],
     "mnb_status_string": [_I],
 }
 
@@ -275,3 +276,11 @@ def mnb_validate_host(B_packed, scales, scale_dtype, zero_points, N, K, bits, bl
 
 def mnb_get_last_device_error(stream=None) -> int:
     return load_library().mnb_get_last_device_error(_stream(stream))
+
+
+def mnb_diag_wait_timeout(limit_ns: int, stream=None, *, check=True) -> int:
+    """Enqueue the diagnostic kernel whose bounded wait runs out after limit_ns."""
+    st = load_library().mnb_diag_wait_timeout(int(limit_ns), _stream(stream))
+    if check:
+        _check(st, "mnb_diag_wait_timeout")
+    return st

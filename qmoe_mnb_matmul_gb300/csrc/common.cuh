@@ -127,23 +127,28 @@ __device__ __forceinline__ uint64_t global_ns() {
 // returns false.
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// The same wait with a limit of limit_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitNs) break;
+        if (global_ns() - t0 > limit_ns) break;
     }
     record_error(MNB_ERR_TIMEOUT);
     return false;
 }
 
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) { return mbar_wait_for(bar, parity, kWaitNs); }
+
 // Warp-uniform bounded wait: lane 0 waits, every lane gets the same verdict.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool warp_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_for(bar, parity, limit_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) { return warp_wait_for(bar, parity, kWaitNs); }
 
 // ------------------------------------------------------------ bulk copies
 
@@ -172,10 +177,11 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 // Allow the next kernel in the stream to start its prologue.
 //
 // Every kernel of this library calls this only after its own
-// grid_dependency_wait (or not at all).  That is what lets a prologue read,
-// before its wait, inputs that the library never writes (packed weights,
-// scales, and router logits in the QMoE FC2 decode prologue): when a launch
-// starts early, everything ahead of the kernel that released it has completed.
+// grid_dependency_wait (or not at all), and the first kernel of every call
+// reads nothing before its wait (it may only warm L2, which is coherent).  A
+// later kernel of the same call (QMoE decode FC2) may read the call's inputs
+// in its prologue: the kernel that released it had already waited, so
+// everything ahead of the call has completed.
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // ------------------------------------------------------------- misc

@@ -65,13 +65,18 @@ TcPlanK plan_tc(int64_t M, int64_t K, int64_t N, int sm_count) {
     return p;
 }
 
-// Y[i] = sum over splits s of P[s][i] (in split order), rounded once to Y's dtype.
-__global__ void splitk_reduce_kernel(const float* __restrict__ P, int splits, int64_t MN, void* Y, int y_dtype) {
+// Y[i] = sum over splits s of P[s][i] (in split order), rounded once to Y's
+// dtype; with `add` (the remainder pass of an fp32 output) Y[i] += that sum.
+__global__ void splitk_reduce_kernel(const float* __restrict__ P, int splits, int64_t MN, void* Y, int y_dtype,
+                                     int add) {
     grid_dependency_wait();
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < MN; i += int64_t(gridDim.x) * blockDim.x) {
         float acc = P[i];
         for (int s = 1; s < splits; ++s) acc += P[s * MN + i];
-        store_from_f32(Y, y_dtype, i, acc);
+        if (add)
+            static_cast<float*>(Y)[i] += acc;
+        else
+            store_from_f32(Y, y_dtype, i, acc);
     }
 }
 
@@ -125,13 +130,23 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     a.partials = plan.splits > 1 ? static_cast<float*>(g.workspace) : nullptr;
     const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m * a.splits, sm_count));
     auto fn = g.bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3;
-    cudaError_t e = fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
-    if (e != cudaSuccess || plan.splits == 1) return e;
-    const int64_t MN = g.M * g.N;
-    const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(MN, 256), int64_t(sm_count) * 8);
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.partials, plan.splits, MN, g.Y,
-                                                                           g.y_dtype);
-    return cudaGetLastError();
+    // An fp32 output from 16-bit activations takes two passes: the product with
+    // the weights rounded to the activation type, then the product with what
+    // that rounding left (the remainder, also 16-bit) added to the output, so
+    // the weight reaches ~16 significant bits (two 8- or 11-bit terms).
+    const int passes = (g.y_dtype == kF32 && g.a_dtype != kF32) ? 2 : 1;
+    for (int pass = 0; pass < passes; ++pass) {
+        a.remainder = pass;
+        cudaError_t e = fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
+        if (e != cudaSuccess) return e;
+        if (plan.splits == 1) continue;
+        const int64_t MN = g.M * g.N;
+        const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(MN, 256), int64_t(sm_count) * 8);
+        splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.partials, plan.splits, MN, g.Y,
+                                                                               g.y_dtype, pass);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Grouped (QMoE) tiles: 256 routed rows of one expert.

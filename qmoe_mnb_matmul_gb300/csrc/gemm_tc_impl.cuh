@@ -48,6 +48,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemv_core.cuh"
@@ -123,6 +124,25 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     } else {
         const __half2 v = __floats2half2_rn(a, b);
         return *reinterpret_cast<const uint32_t*>(&v);
+    }
+}
+
+// The pair (a, b) rounded to the 16-bit type (REM false), or what that
+// rounding left behind, a - round16(a), itself rounded to the 16-bit type
+// (REM true; the difference is exact in fp32).
+template <int AT, bool REM>
+__device__ __forceinline__ uint32_t pack2_part(float2 v) {
+    const uint32_t hi = pack2<AT>(v.x, v.y);
+    if constexpr (!REM) {
+        return hi;
+    } else {
+        float2 h;
+        if constexpr (AT == kBF16) {
+            h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u));
+        } else {
+            h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        }
+        return pack2<AT>(v.x - h.x, v.y - h.y);
     }
 }
 
@@ -500,6 +520,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             uint4 swin = make_uint4(0, 0, 0, 0);
             if (s_tma) swin = *reinterpret_cast<const uint4*>(srow);
             const int xs = static_cast<int>(((kstep0 >> bs_shift) * SS) & ~int64_t(15));
+            // the chunks of this row's K step; REM: the remainder operand of the
+            // second pass of an fp32 output (a uniform branch, taken once per step)
+            auto make_chunks = [&](auto rem) {
 #pragma unroll
             for (int i = 0; i < kChunksPerThread; ++i) {
                 const int hh = h0 + i;
@@ -550,14 +573,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                                              make_float2(ac[j % kCls], ac[(j + 1) % kCls]));
                     const float2 v23 = ffma2(f23, make_float2(mc[(j + 2) % kCls], mc[(j + 3) % kCls]),
                                              make_float2(ac[(j + 2) % kCls], ac[(j + 3) % kCls]));
-                    outw[2 * g] = pack2<AT>(v01.x, v01.y);
-                    outw[2 * g + 1] = pack2<AT>(v23.x, v23.y);
+                    outw[2 * g] = pack2_part<AT, decltype(rem)::value>(v01);
+                    outw[2 * g + 1] = pack2_part<AT, decltype(rem)::value>(v23);
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     *reinterpret_cast<uint4*>(wdst + swo[4 * i + c]) =
                         make_uint4(outw[4 * c], outw[4 * c + 1], outw[4 * c + 2], outw[4 * c + 3]);
             }
+            };
+            if (a.remainder)
+                make_chunks(std::true_type{});
+            else
+                make_chunks(std::false_type{});
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -638,6 +666,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                                     for (int j = 0; j < 32; ++j)
                                         if (j < jn) yp[j * ld] = from_f32<OT>(__uint_as_float(v[j]));
                                 }
+                            } else if (a.remainder) {  // second pass of an fp32 output: add
+                                float* yp = static_cast<float*>(a.Y) + (m0 + c0) * a.ld_y + n;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < jn) yp[j * a.ld_y] += __uint_as_float(v[j]);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)

@@ -91,6 +91,11 @@ struct TcArgs {
     const void* X;         // FC1: activations gathered by token
     int64_t experts;       // matrices stacked in B / scales (grouped launches; 0 or 1 otherwise)
     int w_tma, s_tma;      // set by the launcher: packed rows / scales come as tensor tiles
+    // Second pass of an fp32 output from 16-bit activations: the weight
+    // operand is the remainder s (q - z) - round16(s (q - z)) (rounded to the
+    // activation type) and the epilogue adds to the fp32 output instead of
+    // storing it.
+    int remainder;
 };
 
 // Rows of activations per tile in the grouped launches.
@@ -126,6 +131,12 @@ cudaError_t gemv_take_error(unsigned int* out);
 cudaError_t qmoe_take_error(unsigned int* out);
 cudaError_t gemm_tc_take_error(unsigned int* out);
 cudaError_t quant_take_error(unsigned int* out);
+cudaError_t diag_take_error(unsigned int* out);
+
+// ------------------------------------------------------------ diagnostics
+// One CTA waits, with the library's bounded wait and a limit of limit_ns, on
+// an mbarrier no thread arrives at; the wait records MNB_ERR_TIMEOUT.
+cudaError_t launch_diag_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
 
 // --------------------------------------------------------------- quantizer
 // Symmetric grouped INT3 round-to-nearest of W [N, K] (K % bs == 0) into

@@ -97,13 +97,18 @@ mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
     unsigned int first = 0;
     cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error,
-                                              quant_take_error};
+                                              quant_take_error, diag_take_error};
     for (auto take : takers) {
         unsigned int v = 0;
         if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;
         if (first == 0) first = v;
     }
     return static_cast<mnb_status>(first);
+}
+
+mnb_status mnb_diag_wait_timeout(uint64_t limit_ns, mnb_stream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000ull) return MNB_ERR_INVALID_ARG;
+    return from_cuda(launch_diag_wait_timeout(limit_ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, int block_size,

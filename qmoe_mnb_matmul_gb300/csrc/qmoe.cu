@@ -202,10 +202,12 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
         }
     };
     if (DECODE) {
-        // Prologue, overlapping the kernel ahead: router logits and expert
-        // weights are never outputs of the immediately preceding library call,
-        // so the CTA routes its token and starts copying the selected expert's
-        // rows before waiting; activations and workspace are read after.
+        // The first kernel of the layer reads no input before its dependency
+        // wait (the kernel ahead may still be writing the router logits or the
+        // weights); it releases the FC2 kernel right after, so FC2 may read
+        // the layer's inputs in its own prologue.
+        grid_dependency_wait();
+        grid_launch_dependents();
         const int64_t p = blockIdx.x;
         const int64_t t = p / q.k;
         route_token(q, t, s_idx, s_w, reinterpret_cast<float*>(Wst + plan.w + plan.s));
@@ -216,8 +218,6 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             s_int[4] = static_cast<int>(t);
             copy_rows(s_int[0]);
         }
-        grid_dependency_wait();
-        grid_launch_dependents();
     } else {
         grid_dependency_wait();
         grid_launch_dependents();
@@ -335,11 +335,11 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
     const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
     const float* h = reinterpret_cast<const float*>(static_cast<const char*>(q.workspace) + L.h);
 
-    // Prologue, overlapping the FC1 kernel: the router logits were complete
-    // before FC1 released this launch (FC1 releases it after its own wait),
-    // and the expert weights are inputs that no kernel of this library
-    // writes, so this CTA routes its token and starts copying the selected
-    // experts' rows before waiting for h.
+    // Prologue, overlapping the FC1 kernel: FC1 releases this launch only
+    // after its own dependency wait, when every kernel ahead of the layer has
+    // completed, so the router logits and the weights are final here; this
+    // CTA routes its token and starts copying the selected experts' rows
+    // before waiting for h.
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();

@@ -6,7 +6,13 @@ import numpy as np
 
 # Tolerances of the parity contract:
 #  - fp32 outputs: max_i |y_i - r_i| / max(|r_i|, rms(r)) <= 1e-3
-#  - fp16 / bf16 outputs: |y - r| <= 1e-2 + 2e-2 max(|r|, rms(r)) elementwise
+#  - fp16 / bf16 outputs: |y_i - r_i| <= 1e-2 + 2e-2 |r_i| elementwise
+#  - bf16 outputs of the tensor-core paths only (bf16 activations, so the
+#    dequantised weight is a bf16 MMA operand): |y_i - r_i| <= 1e-2 + 2e-2
+#    max(|r_i|, rms(r)), and the number of outputs outside the elementwise
+#    rule is printed.  An exact product of bf16-rounded weights already
+#    misses the elementwise rule on a fraction of a percent of the near-zero
+#    outputs at K = 2048.
 F32_TOL = 1e-3
 HALF_ATOL, HALF_RTOL = 1e-2, 2e-2
 TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
@@ -28,23 +34,44 @@ def assert_f32_close(y, ref, tol=F32_TOL):
     assert err <= tol, f"fp32 relative error {err:.3g} > {tol}"
 
 
+def half_violations(y, ref) -> int:
+    """Outputs outside the elementwise 16-bit rule |y - r| <= 1e-2 + 2e-2 |r|."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return int(np.sum(np.abs(y - ref) > HALF_ATOL + HALF_RTOL * np.abs(ref)))
+
+
 def assert_half_close(y, ref):
-    """|y - r| <= 1e-2 + 2e-2 * max(|r|, rms(r)) elementwise.  The relative part is
-    measured against max(|r_i|, rms(r)), as in the fp32 rule: rounding a dequantised
-    weight to a 16-bit tensor-core operand gives errors that scale with the output's
-    rms, so an exact product of bf16-rounded weights already exceeds 2e-2 |r_i| on
-    near-zero outputs at K = 2048."""
+    """|y - r| <= 1e-2 + 2e-2 |r|, every output."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    bad = half_violations(y, ref)
+    assert bad == 0, (f"{bad} of {y.size} half-precision outputs out of tolerance; "
+                      f"worst |y-r| = {np.max(np.abs(y - ref)):.3g}")
+
+
+def assert_bf16_tc_close(y, ref, label: str = ""):
+    """bf16 tensor-core outputs: |y - r| <= 1e-2 + 2e-2 max(|r|, rms(r)) every
+    output; prints how many outputs miss the elementwise rule."""
     y = np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    elementwise = half_violations(y, ref)
+    print(f"[bf16 tensor-core rule] {label}: {elementwise} of {y.size} outputs outside the elementwise rule "
+          f"({100.0 * elementwise / max(y.size, 1):.3f} %)")
     bad = np.abs(y - ref) > HALF_ATOL + HALF_RTOL * np.maximum(np.abs(ref), rms)
-    assert not bad.any(), (f"{int(bad.sum())} of {bad.size} half-precision outputs out of tolerance; "
+    assert not bad.any(), (f"{int(bad.sum())} of {bad.size} bf16 outputs out of tolerance; "
                            f"worst |y-r| = {np.max(np.abs(y - ref)):.3g}")
 
 
-def assert_close(y, ref, dtype: str):
-    if dtype == "f32":
+def assert_close(y, ref, y_dtype: str, a_dtype: str | None = None, tensor_cores: bool = False, label: str = ""):
+    """The rule of the output dtype: fp32 for fp32 outputs, the elementwise 16-bit
+    rule for fp16 / bf16 outputs, and the bf16 tensor-core rule for bf16 outputs
+    of a tensor-core path fed bf16 activations."""
+    if y_dtype == "f32":
         assert_f32_close(y, ref)
+    elif tensor_cores and a_dtype == "bf16" and y_dtype == "bf16":
+        assert_bf16_tc_close(y, ref, label)
     else:
         assert_half_close(y, ref)
 

@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests._util import (CODE, assert_close, assert_f32_close, empty_guarded, guards_intact, to_dev, to_f64)
+from tests._util import (CODE, assert_close, assert_f32_close, empty_guarded, f32_error, guards_intact, to_dev,
+                         to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +59,9 @@ def test_qwen3_decode_projection(name, K, N):
     A, packed, scales, _ = case(g, 1, K, N, 4, 32)
     y = run(A, "f32", packed, scales, "f32", None, N, K, 4, 32)
     ref = oracle.mnb_matmul(A, "f32", packed, scales, "f32", None, N, K, 4, 32, threads=THREADS)
+    # the margin of the float-image dequantisation (sums of pre-scaled activations
+    # cancel before the block scale is applied) against the 1e-3 rule
+    print(f"[decode {name} K={K} N={N}] fp32 relative error {f32_error(y, ref):.3g} (rule 1e-3)")
     assert_f32_close(y, ref)
     if name == "qkv":  # the fused QKV output splits by column offset [2048, 1024, 1024]
         o = 0
@@ -106,7 +110,8 @@ def test_small_m(M, a_dt):
     y_dt = "f32" if a_dt == "f32" else "bf16"
     A, packed, scales, zp = case(g, M, K, N, 4, bs, a_dt)
     y = run(A, a_dt, packed, scales, "f32", None, N, K, 4, bs, y_dt)
-    assert_close(y, oracle.mnb_matmul(A, a_dt, packed, scales, "f32", None, N, K, 4, bs, threads=THREADS), y_dt)
+    assert_close(y, oracle.mnb_matmul(A, a_dt, packed, scales, "f32", None, N, K, 4, bs, threads=THREADS), y_dt,
+                 a_dt, tensor_cores=M >= 16 and a_dt != "f32", label=f"small M={M}")
 
 
 @pytest.mark.parametrize("bits", [3, 4])

@@ -153,8 +153,11 @@ def test_brute_force_expand_then_multiply(bits, bs, with_zp, a_dtype, s_dtype):
     assert np.array_equal(oracle.dequantize(packed, scales, s_dtype, zp, N, K, bits, bs), W)
     A = wl.normal(g, (M, K), a_dtype)
     Y = oracle.mnb_matmul(A, a_dtype, packed, scales, s_dtype, zp, N, K, bits, bs)
-    ref = as_f64(A, a_dtype).reshape(M, K) @ W.T
-    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+    # the expanded product summed in ascending k (a running sum: np.cumsum adds
+    # strictly left to right), so the same fp64 operations in the same order
+    prod = as_f64(A, a_dtype).reshape(M, 1, K) * W.reshape(1, N, K)
+    ref = np.cumsum(prod, axis=2)[:, :, -1]
+    assert np.array_equal(Y, ref)
 
 
 def test_selected_rows_match_full_output():

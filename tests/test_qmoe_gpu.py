@@ -1,6 +1,8 @@
 """GPU parity of qmoe_forward (routing, FC1 + SwiGLU, FC2, combine) against the
-oracle, through the C ABI.  Outputs are fp16 / bf16:
-|y - r| <= 1e-2 + 2e-2 max(|r|, rms(r)) (tests/_util.py)."""
+oracle, through the C ABI.  Outputs are fp16 / bf16: the elementwise rule
+|y - r| <= 1e-2 + 2e-2 |r|, except bf16 layers on the tensor-core plan (T > 8),
+which take the bf16 tensor-core rule and print their elementwise misses
+(tests/_util.py).  Sampled prefill checks cover at least 64 tokens."""
 import os
 import zlib
 
@@ -9,7 +11,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests._util import assert_half_close, empty_guarded, guards_intact, to_dev, to_f64
+from tests._util import assert_close, empty_guarded, guards_intact, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +44,22 @@ def run_qmoe(d, T, H, I, E, k, b1, b2, bs, act, layout="interleaved", normalize=
     return to_f64(Y).reshape(T, H)
 
 
+def check(y, ref, act, T, label=""):
+    """The rule of the plan that ran: T > 8 is the tensor-core plan."""
+    assert_close(y, ref, act, act, tensor_cores=T > 8, label=label)
+
+
+def sample_tokens(T, key, n=64):
+    """Every token up to n, else the first, last and tenth plus random distinct ones, n in all."""
+    if T <= n:
+        return list(range(T))
+    g = wl.rng(key)
+    toks = {0, 10, T - 1}
+    while len(toks) < n:
+        toks.add(int(g.integers(0, T)))
+    return sorted(toks)
+
+
 def reference(d, k, b1, b2, I, bs, act, layout="interleaved", normalize=True, tokens=None):
     return oracle.qmoe(d["X"], act, d["logits"], k, normalize, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], b1,
                        d["fc2_w"], d["fc2_scales"], d["fc2_zp"], b2, I, bs, layout, tokens=tokens, threads=THREADS)
@@ -52,7 +70,7 @@ def test_int3_decode_layer():
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
     d = wl.moe_layer(wl.rng(seed("c3")), 1, H, I, E, 3, 3, 64, "f16")
     y = run_qmoe(d, 1, H, I, E, k, 3, 3, 64, "f16")
-    assert_half_close(y, reference(d, k, 3, 3, I, 64, "f16"))
+    check(y, reference(d, k, 3, 3, I, 64, "f16"), "f16", 1)
 
 
 @pytest.mark.parametrize("T", [1, 2, 5, 8])
@@ -63,7 +81,7 @@ def test_decode_plan(T, bits):
     act = "bf16" if T % 2 else "f16"
     d = wl.moe_layer(wl.rng(seed("dec", T, bits)), T, H, I, E, b1, b2, bs, act, with_zp=(T == 2))
     y = run_qmoe(d, T, H, I, E, k, b1, b2, bs, act)
-    assert_half_close(y, reference(d, k, b1, b2, I, bs, act))
+    check(y, reference(d, k, b1, b2, I, bs, act), act, T)
 
 
 @pytest.mark.parametrize("bs", [32, 64, 128])
@@ -73,7 +91,7 @@ def test_decode_layouts_and_blocks(bs, layout, normalize):
     H, I, E, k, T = 512, 256, 32, 4, 3
     d = wl.moe_layer(wl.rng(seed("lay", bs, layout, normalize)), T, H, I, E, 3, 4, bs, "f16", with_zp=True)
     y = run_qmoe(d, T, H, I, E, k, 3, 4, bs, "f16", layout, normalize)
-    assert_half_close(y, reference(d, k, 3, 4, I, bs, "f16", layout, normalize))
+    check(y, reference(d, k, 3, 4, I, bs, "f16", layout, normalize), "f16", T)
 
 
 @pytest.mark.parametrize("T,E,k,skew", [(9, 64, 8, True), (64, 128, 8, True), (33, 16, 2, False), (40, 8, 8, False),
@@ -84,7 +102,7 @@ def test_tiled_plan(T, E, k, skew, bits):
     H, I, bs = 512, 256, 64
     d = wl.moe_layer(wl.rng(seed("tiled", T, E, k, bits)), T, H, I, E, b1, b2, bs, "bf16", with_zp=skew, skew=skew)
     y = run_qmoe(d, T, H, I, E, k, b1, b2, bs, "bf16")
-    assert_half_close(y, reference(d, k, b1, b2, I, bs, "bf16"))
+    check(y, reference(d, k, b1, b2, I, bs, "bf16"), "bf16", T, f"T={T} E={E} k={k} bits={bits}")
 
 
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
@@ -97,7 +115,7 @@ def test_tiled_plan_layouts(layout, I, bits):
     d = wl.moe_layer(wl.rng(seed("tiled-layout", layout, I, bits)), T, H, I, E, bits, bits, bs, "f16", with_zp=True,
                      skew=True)
     y = run_qmoe(d, T, H, I, E, k, bits, bits, bs, "f16", layout)
-    assert_half_close(y, reference(d, k, bits, bits, I, bs, "f16", layout))
+    check(y, reference(d, k, bits, bits, I, bs, "f16", layout), "f16", T)
 
 
 @pytest.mark.parametrize("T", [128, 512])
@@ -106,8 +124,8 @@ def test_prefill_shapes_sampled_tokens(T):
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
     d = wl.moe_layer(wl.rng(seed("prefill", T)), T, H, I, E, 3, 3, 64, "f16", skew=True)
     y = run_qmoe(d, T, H, I, E, k, 3, 3, 64, "f16")
-    toks = sorted(set([0, 1, T - 1, 10, 20] + list(wl.rng(T).integers(0, T, 11))))
-    assert_half_close(y[toks], reference(d, k, 3, 3, I, 64, "f16", tokens=toks))
+    toks = sample_tokens(T, ("prefill", T))
+    check(y[toks], reference(d, k, 3, 3, I, 64, "f16", tokens=toks), "f16", T)
 
 
 @pytest.mark.parametrize("T,bits,bs,act,zp", [(2048, (3, 3), 64, "f16", False), (4096, (4, 4), 32, "bf16", True),
@@ -120,5 +138,54 @@ def test_prefill_sweep_full_size_sampled_tokens(T, bits, bs, act, zp):
     d = wl.moe_layer(wl.rng(seed("sweep", T, bits, bs, act, zp)), T, H, I, E, b1, b2, bs, act, with_zp=zp,
                      skew=True)
     y = run_qmoe(d, T, H, I, E, k, b1, b2, bs, act)
-    toks = sorted(set([0, 10, T - 1] + list(wl.rng(T + 1).integers(0, T, 7))))
-    assert_half_close(y[toks], reference(d, k, b1, b2, I, bs, act, tokens=toks))
+    toks = sample_tokens(T, ("sweep", T, bits, bs, act, zp))
+    check(y[toks], reference(d, k, b1, b2, I, bs, act, tokens=toks), act, T, f"T={T} bits={bits} bs={bs} zp={zp}")
+
+
+# ------------------------------------------------ producers right ahead of a layer
+
+def test_router_logits_written_by_the_kernel_right_ahead():
+    """The router projection (mnb_matmul, M=1, fp32 logits) runs immediately before
+    the decode layer on the same stream; the GEMV releases its dependents before it
+    writes the logits, so the layer must not read them before its dependency wait."""
+    H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
+    g = wl.rng(seed("chain-router"))
+    d = wl.moe_layer(g, 1, H, I, E, 3, 3, 64, "f16")
+    rw, rs, _ = wl.quantized_weight(g, E, H, 4, 32)          # router weights: INT4 [E, H]
+    Xf = torch.from_numpy(d["X"].view(np.int16)).view(torch.float16).float().numpy()
+    ws = torch.empty(mnb.qmoe_workspace_size(1, H, I, E, k, mnb.F16), dtype=torch.uint8, device="cuda")
+    X_d, X32 = to_dev(d["X"], "f16"), to_dev(Xf)
+    W1, S1, W2, S2 = to_dev(d["fc1_w"]), to_dev(d["fc1_scales"], "f16"), to_dev(d["fc2_w"]), to_dev(d["fc2_scales"], "f16")
+    RW, RS = to_dev(rw), to_dev(rs)
+    logits = torch.full((1, E), float("nan"), device="cuda")   # stale contents would route on NaN
+    Y = torch.empty((1, H), dtype=torch.float16, device="cuda")
+    for _ in range(3):
+        logits.fill_(float("nan"))
+        mnb.mnb_matmul(X32, RW, RS, None, E, 4, 32, logits, K=H, M=1)
+        mnb.qmoe_forward(X_d, logits, k, True, W1, S1, None, 3, W2, S2, None, 3, I, 64, Y, ws)
+        torch.cuda.synchronize()
+        assert mnb.mnb_get_last_device_error() == 0
+        lg = logits.cpu().numpy()
+        d2 = dict(d, logits=lg)
+        check(to_f64(Y), reference(d2, k, 3, 3, I, 64, "f16"), "f16", 1)
+
+
+def test_expert_weights_written_by_the_quantizer_right_ahead():
+    """mnb_quantize_int3 writes FC1's packed weights and scales immediately before the
+    decode layer that consumes them, on the same stream."""
+    H, I, E, k, bs = 1024, 256, 16, 4, 64
+    g = wl.rng(seed("chain-quant"))
+    d = wl.moe_layer(g, 1, H, I, E, 3, 3, bs, "f16")
+    Wd = torch.from_numpy((g.standard_normal((E * 2 * I, H)) * 0.02).astype(np.float16)).cuda()
+    W1 = torch.full((E * 2 * I, H // bs, 3 * bs // 8), 0xFF, dtype=torch.uint8, device="cuda")
+    S1 = torch.full((E * 2 * I, H // bs), float("nan"), dtype=torch.float16, device="cuda")
+    ws = torch.empty(mnb.qmoe_workspace_size(1, H, I, E, k, mnb.F16), dtype=torch.uint8, device="cuda")
+    Y = torch.empty((1, H), dtype=torch.float16, device="cuda")
+    mnb.mnb_quantize_int3(Wd, bs, mnb.F16, W1, S1)
+    mnb.qmoe_forward(to_dev(d["X"], "f16"), to_dev(d["logits"]), k, True, W1, S1, None, 3, to_dev(d["fc2_w"]),
+                     to_dev(d["fc2_scales"], "f16"), None, 3, I, bs, Y, ws)
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_last_device_error() == 0
+    d2 = dict(d, fc1_w=W1.cpu().numpy().reshape(E, 2 * I, -1),
+              fc1_scales=S1.cpu().view(torch.int16).numpy().view(np.uint16).reshape(E, 2 * I, -1))
+    check(to_f64(Y), reference(d2, k, 3, 3, I, bs, "f16"), "f16", 1)
