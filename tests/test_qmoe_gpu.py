@@ -53,7 +53,7 @@ def sample_tokens(T, key, n=64):
     """Every token up to n, else the first, last and tenth plus random distinct ones, n in all."""
     if T <= n:
         return list(range(T))
-    g = wl.rng(key)
+    g = wl.rng(seed(*key))
     toks = {0, 10, T - 1}
     while len(toks) < n:
         toks.add(int(g.integers(0, T)))
