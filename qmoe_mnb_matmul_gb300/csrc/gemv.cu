@@ -6,51 +6,57 @@
 // consumed; no dequantised weight matrix is ever written to global memory.
 //
 // Design (HBM-bound: the packed weights and scales are the traffic):
-//  * A CTA owns contiguous blocks of RC = 8 * R weight rows.  Rows are
-//    contiguous in the [N, nb, blob] layout, so a block's packed bytes and its
-//    scales are two contiguous ranges, each moved by one bulk (TMA) copy.
-//  * Warp 8 is the producer: one lane keeps a ring of NST stages filled,
-//    waiting on per-stage "empty" mbarriers; the 8 consumer warps wait on the
-//    per-stage "full" mbarriers.  There is no block-wide barrier in the loop.
-//    The grid is persistent (<= resident CTAs).
-//  * The activations are staged once per CTA (gemv_core.cuh); each consumer
-//    warp owns R rows of a block and walks their 32-code chunks, one chunk
-//    per lane; the R x MT sums are reduced together with shuffles that hand
-//    half of the values to the partner lane at each step (fixed order, so
-//    results are deterministic).
-//  * Before the grid-dependency wait each CTA only warms L2 with its first
-//    blocks (a prefetch cannot observe stale data), so a programmatic
-//    dependent launch overlaps that traffic with the previous kernel.
+//  * A CTA owns one contiguous range of row blocks (RC = 8 * R rows each).
+//    Rows are contiguous in the [N, nb, blob] layout, so the range's packed
+//    bytes and scales are two contiguous byte ranges: before its grid
+//    dependency wait the CTA asks L2 to prefetch them (the whole range when
+//    the matrix is small enough to sit in L2 beside its neighbours, else the
+//    first ring-full) and lets the next kernel on the stream launch, so a
+//    chain of projections keeps HBM busy across kernel boundaries.  Nothing
+//    the CTA reads is read before the wait (a prefetch only warms L2, which
+//    stays coherent with any later write).
+//  * Warp 8 is the producer: one lane keeps a ring of NST stages filled with
+//    bulk (TMA) copies of whole row blocks, waiting on per-stage "empty"
+//    mbarriers; the 8 consumer warps wait on the per-stage "full" mbarriers.
+//  * The activations are staged once per CTA as a fixed-point image
+//    (gemv_int.cuh); each consumer warp owns R rows of a block and walks
+//    their 32-code chunks, one chunk per lane, with exact dp4a integer dot
+//    products per chunk; the R x MT sums are reduced together with shuffles
+//    that hand half of the values to the partner lane at each step (fixed
+//    order, so results are deterministic).
 #include <algorithm>
 
 #include "common.cuh"
 #include "gemv_core.cuh"
+#include "gemv_int.cuh"
 #include "kernels.h"
 
 namespace mnb {
 
 namespace {
 
-using namespace gemv;
+using namespace gemv_int;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
 constexpr int64_t kSmemBudget = 227 * 1024;
 
+__host__ __device__ constexpr int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
 struct Plan {
-    int64_t a4, sums, w_stage, s_stage, fixed;
+    int64_t qimg, corr, w_stage, s_stage, fixed;
     int stages;
     int64_t total;
 };
 
 __host__ __device__ inline Plan make_plan(int MT, int C, int RC, int64_t row_bytes, int nb, int ssize, int stages) {
     Plan p;
-    p.a4 = a4_bytes(MT, C);
-    p.sums = round_up(int64_t(MT) * C * 16, 128);  // one float4 correction per (row, chunk)
+    p.qimg = qimg_bytes(MT, C);
+    p.corr = corr_bytes(MT, C);
     p.w_stage = round_up(int64_t(RC) * row_bytes, 128);
     p.s_stage = round_up(int64_t(RC) * nb * ssize, 128);
-    p.fixed = 256 + p.a4 + p.sums;
+    p.fixed = 256 + p.qimg + p.corr;
     p.stages = stages;
     p.total = p.fixed + int64_t(stages) * (p.w_stage + p.s_stage);
     return p;
@@ -66,6 +72,13 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Blocks [first, last) of CTA x among gx CTAs: contiguous, sizes differing by at most one.
+__device__ __forceinline__ void cta_blocks(int nblk, int x, int gx, int& first, int& last) {
+    const int q = nblk / gx, r = nblk - q * gx;
+    first = x * q + min(x, r);
+    last = first + q + (x < r ? 1 : 0);
+}
+
 template <int BITS, int ST, int MT, int R>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using S = typename DType<ST>::T;
@@ -77,14 +90,15 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     const int NST = plan.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kMaxStages;
-    float4* A4 = reinterpret_cast<float4*>(smem + 256);
-    float4* Corr = reinterpret_cast<float4*>(smem + 256 + plan.a4);
+    uint4* Q = reinterpret_cast<uint4*>(smem + 256);
+    int2* Corr = reinterpret_cast<int2*>(smem + 256 + plan.qimg);
     uint8_t* Wst = smem + plan.fixed;
     uint8_t* Sst = Wst + NST * plan.w_stage;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = int64_t(blockIdx.y) * MT;
-    const int nblk = a.n_blocks;
+    int b_first, b_last;
+    cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
     auto block_rows = [&](int blk) -> int {
         const int64_t left = a.N - int64_t(blk) * RC;
         return static_cast<int>(left < RC ? left : int64_t(RC));
@@ -96,13 +110,26 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             mbar_init(&empty[s], kConsumerWarps);
         }
         fence_barrier_init();
-        for (int i = 0; i < NST; ++i) {
-            const int blk = blockIdx.x + i * gridDim.x;
-            if (blk >= nblk) break;
-            const uint32_t wb = static_cast<uint32_t>(block_rows(blk) * a.row_bytes) & ~15u;
-            if (wb) bulk_prefetch_l2(a.B + int64_t(blk) * RC * a.row_bytes, wb);
+        // L2 prefetch of this CTA's rows (a hint that reads nothing we use)
+        if (b_first < b_last) {
+            const int pf_last = a.prefetch_all ? b_last : min(b_last, b_first + NST);
+            const int64_t r0 = int64_t(b_first) * RC, r1 = min(int64_t(pf_last) * RC, a.N);
+            const int64_t ss = sizeof(S);
+            auto prefetch = [](const uint8_t* p, int64_t bytes) {
+                const uintptr_t start = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
+                int64_t n = int64_t(reinterpret_cast<uintptr_t>(p) + bytes - start) & ~int64_t(15);
+                for (int64_t off = 0; off < n; off += int64_t(1) << 30) {
+                    const int64_t len = min(n - off, int64_t(1) << 30);
+                    bulk_prefetch_l2(reinterpret_cast<const void*>(start + off), static_cast<uint32_t>(len));
+                }
+            };
+            prefetch(a.B + r0 * a.row_bytes, (r1 - r0) * a.row_bytes);
+            prefetch(static_cast<const uint8_t*>(a.scales) + r0 * nb * ss, (r1 - r0) * nb * ss);
         }
     }
+    // The next kernel on the stream may start its own prologue now; it reads
+    // nothing before its dependency wait either.
+    grid_launch_dependents();
     grid_dependency_wait();
     __syncthreads();
 
@@ -111,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         if (lane != 0) return;
         int st = 0;
         uint32_t round = 0;  // times the ring has wrapped
-        for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        for (int blk = b_first; blk < b_last; ++blk) {
             if (round && !mbar_wait(&empty[st], (round - 1) & 1)) {
                 for (int j = 0; j < NST; ++j) mbar_wait(&full[j], 0);  // give in-flight copies a bounded chance
                 return;
@@ -137,22 +164,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     }
 
     // ------------------------------------------------------------ consumers
-    stage_chunks<BITS, MT>(
-        A4, Corr, C, a.K, a.a_dtype, a.a_vec != 0,
+    const int esz = a.a_dtype == kF32 ? 4 : 2;
+    stage_image(
+        Q, Corr, MT, C, a.K, a.a_dtype, a.a_vec != 0,
         [&](int m) -> const void* {
-            return m0 + m < a.M ? static_cast<const char*>(a.A) + (m0 + m) * a.K * (a.a_dtype == kF32 ? 4 : 2)
-                                : nullptr;
+            return m0 + m < a.M ? static_cast<const char*>(a.A) + (m0 + m) * a.K * esz : nullptr;
         },
         tid, kConsumerWarps * 32);
     consumer_sync();
-    grid_launch_dependents();
 
     const int bs_shift = __ffs(a.bs) - 1;
-    const int mstride = a4_groups(C) * 256;
     constexpr int kZImplicit = 1 << (BITS - 1);
     int st = 0;
     uint32_t phase = 0;
-    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    for (int blk = b_first; blk < b_last; ++blk) {
         if (!warp_wait(&full[st], phase)) return;
         const int64_t n0 = int64_t(blk) * RC;
         const int rc = block_rows(blk);
@@ -160,11 +185,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
         const int r0 = warp * R;
         if (r0 < rc) {
-            float2 acc[R][MT];
+            float acc[R][MT];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[r][m] = make_float2(0.f, 0.f);
+                for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
             const uint8_t* wrow[R];
             const S* srow[R];
             const uint8_t* zrow[R];
@@ -175,20 +200,32 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                 srow[r] = Sc + rl * nb;
                 zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
             }
-            auto load = [&](int c, uint32_t (&w)[R][BITS], float (&sc)[R], float (&dz)[R]) {
+            for (int c = lane; c < C; c += 32) {
                 const int b = (c * 32) >> bs_shift;
+                uint4 q[MT][4];
+                float p2[MT];
+                int V[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const uint4* qp = Q + qbase(m, c, C);
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) q[m][qq] = qp[qq * 32];
+                    const int2 cr = Corr[m * C + c];
+                    V[m] = cr.x;
+                    p2[m] = __int_as_float(cr.y);
+                }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    load_chunk<BITS>(wrow[r], c, w[r]);
-                    sc[r] = to_f32(srow[r][b]);
-                    dz[r] = a.zp ? float(kZImplicit - zero_point_code<BITS>(zrow[r], b)) : 0.f;
+                    uint32_t w[BITS];
+                    gemv::load_chunk<BITS>(wrow[r], c, w);
+                    const float sc = to_f32(srow[r][b]);
+                    const int z = a.zp ? gemv::zero_point_code<BITS>(zrow[r], b) : kZImplicit;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const int T = chunk_dot<BITS>(w, q[m]) - z * V[m];
+                        acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                    }
                 }
-            };
-            for (int c = lane; c < C; c += 32) {
-                uint32_t w[R][BITS];
-                float sc[R], dz[R];
-                load(c, w, sc, dz);
-                chunk_accumulate<BITS, R, MT>(w, sc, dz, A4 + a4_base(0, c, C), mstride, Corr + c, C, acc);
             }
             // value q = r * MT + m; each total ends in one lane
             constexpr int N = R * MT;
@@ -196,10 +233,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m].x + acc[r][m].y;
+                for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m];
             const float total = warp_sum_transpose<N>(part);
             if ((lane & (32 / N - 1)) == 0) {
-                const int q = transpose_row<N>(lane), r = q / MT, m = q - r * MT;
+                const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
                 if (r0 + r < rc && m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
             }
         }
@@ -220,65 +257,73 @@ int64_t row_align(int64_t row_bytes, int nb, int ssize) {
     return std::max(g16(row_bytes), g16(int64_t(nb) * ssize));
 }
 
-// Launch shape: rows per warp R and ring depth.  Each CTA wants ~48 KB of
-// weights in flight and the SM wants up to 3 resident CTAs; the largest R
-// that still gives >= 0.8 blocks per SM wins.  Measured on the decode
-// projections: fewer, larger blocks beat more CTAs per SM there (every CTA
-// stages the whole activation row), e.g. 2048 -> 4096 in 3.8 us with 128
-// 32-row blocks against 4.9 us with 256 16-row blocks.
-struct Shape {
-    int R = 4, stages = 2;
-};
-constexpr int64_t kSmSmem = 228 * 1024, kCtaReserve = 1024;
+// Matrices up to this many bytes are prefetched into L2 whole before the
+// dependency wait: a few of them fit in the 129 MB L2 beside the kernels
+// still running, so a chain of decode projections streams without gaps.
+constexpr int64_t kPrefetchAllBytes = int64_t(32) << 20;
 
-Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count) {
+// Launch shape: rows per warp R, ring depth and grid.  Small matrices (whole
+// L2 prefetch) keep each CTA's shared memory modest so that the next
+// kernel's CTAs fit beside it (~72 KB); large ones get a deep ring (~144 KB
+// in flight per SM) to cover HBM latency.  Among the R that fit, the one
+// whose busiest CTA has the fewest rows wins, with a small handicap for
+// fewer rows per warp (more activation-image reads per code).
+struct Shape {
+    int R = 4, stages = 2, grid = 1;
+    bool prefetch_all = false;
+};
+
+Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups) {
     const int64_t align = row_align(row_bytes, nb, ssize);
+    const int64_t bytes = N * (row_bytes + int64_t(nb) * ssize);
+    const bool small = bytes <= kPrefetchAllBytes;
+    const int64_t ring_target = small ? 64 * 1024 : 144 * 1024;
+    const int64_t cta_cap = small ? 80 * 1024 : kSmemBudget;
     Shape best;
-    int64_t best_score = -1;
+    double best_cost = -1;
     for (int R : {4, 2, 1}) {
+        if (MT == 4 && R == 4) continue;  // keeps the four rows' activation images in registers
         const int RC = kConsumerWarps * R;
         if (RC % align != 0) continue;
         const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
         const int64_t stage = p1.w_stage + p1.s_stage;
+        const int64_t cap = std::max<int64_t>(cta_cap, p1.fixed + 2 * stage);
         if (p1.fixed + 2 * stage > kSmemBudget) continue;
-        int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, cdiv<int64_t>(49152, stage))));
-        while (st > 2 && p1.fixed + st * stage > kSmemBudget) --st;
-        auto ctas = [&](int s) { return kSmSmem / (p1.fixed + s * stage + kCtaReserve); };
-        while (st > 2 && ctas(st) < 3 && ctas(st - 1) > ctas(st)) --st;
-        const int64_t resident = std::min<int64_t>(3, ctas(st));
-        const bool enough_blocks = cdiv<int64_t>(N, RC) * 5 >= int64_t(sm_count) * 4;
-        const int64_t score = (enough_blocks ? 100 : 0) + 10 * R + resident;
-        if (score > best_score) {
-            best_score = score;
+        int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, ring_target / stage)));
+        while (st > 2 && p1.fixed + st * stage > cap) --st;
+        const int64_t nblk = cdiv<int64_t>(N, RC);
+        const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(nblk, std::max<int64_t>(1, sm_count / mgroups)));
+        const int64_t share = cdiv<int64_t>(nblk, ctas) * RC;  // rows of the busiest CTA
+        // fewer rows per warp re-read the activation image more often per code
+        const double cost = double(share) * (R == 4 ? 1.0 : R == 2 ? 1.03 : 1.08);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
             best.R = R;
             best.stages = st;
+            // as few CTAs as give every CTA the busiest CTA's share
+            best.grid = static_cast<int>(cdiv<int64_t>(nblk, cdiv<int64_t>(nblk, ctas)));
         }
     }
+    best.prefetch_all = small;
     return best;
 }
 
 template <int BITS, int ST, int MT, int R>
-cudaError_t launch_typed(GemvArgs a, int stages, int sm_count, bool pdl, cudaStream_t stream) {
+cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t stream) {
     constexpr int RC = kConsumerWarps * R;
     const int ssize = ST == kF32 ? 4 : 2;
     a.rows_per_block = RC;
     a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, RC));
-    const Plan p1 = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, 1);
-    if (p1.fixed + int64_t(stages) * (p1.w_stage + p1.s_stage) > kSmemBudget) return cudaErrorNotSupported;
-    a.stages = stages;
-    const int st = stages;
-    const Plan p = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, st);
+    a.stages = sh.stages;
+    a.prefetch_all = sh.prefetch_all ? 1 : 0;
+    const Plan p = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, sh.stages);
+    if (p.total > kSmemBudget) return cudaErrorNotSupported;
     auto kern = gemv_kernel<BITS, ST, MT, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, static_cast<size_t>(p.total));
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorNotSupported;
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
-    const int64_t gx = std::min<int64_t>(a.n_blocks, std::max<int64_t>(1, int64_t(sm_count) * per_sm / mgroups));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(mgroups), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(sh.grid, a.n_blocks)), static_cast<unsigned>(mgroups), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(p.total);
     cfg.stream = stream;
@@ -291,20 +336,23 @@ cudaError_t launch_typed(GemvArgs a, int stages, int sm_count, bool pdl, cudaStr
 }
 
 template <int BITS, int ST, int MT>
-cudaError_t launch_r(const GemvArgs& a, const Shape& sh, int sm_count, bool pdl, cudaStream_t stream) {
-    if (sh.R == 4) return launch_typed<BITS, ST, MT, 4>(a, sh.stages, sm_count, pdl, stream);
-    if (sh.R == 2) return launch_typed<BITS, ST, MT, 2>(a, sh.stages, sm_count, pdl, stream);
-    return launch_typed<BITS, ST, MT, 1>(a, sh.stages, sm_count, pdl, stream);
+cudaError_t launch_r(const GemvArgs& a, const Shape& sh, bool pdl, cudaStream_t stream) {
+    if constexpr (MT < 4) {
+        if (sh.R == 4) return launch_typed<BITS, ST, MT, 4>(a, sh, pdl, stream);
+    }
+    if (sh.R == 2) return launch_typed<BITS, ST, MT, 2>(a, sh, pdl, stream);
+    return launch_typed<BITS, ST, MT, 1>(a, sh, pdl, stream);
 }
 
 template <int BITS, int ST>
 cudaError_t launch_mt(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t stream) {
     const int MT = pick_mt(a.M);
-    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count);
+    const int64_t mgroups = cdiv<int64_t>(a.M, MT);
+    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups);
     switch (MT) {
-        case 1: return launch_r<BITS, ST, 1>(a, sh, sm_count, pdl, stream);
-        case 2: return launch_r<BITS, ST, 2>(a, sh, sm_count, pdl, stream);
-        default: return launch_r<BITS, ST, 4>(a, sh, sm_count, pdl, stream);
+        case 1: return launch_r<BITS, ST, 1>(a, sh, pdl, stream);
+        case 2: return launch_r<BITS, ST, 2>(a, sh, pdl, stream);
+        default: return launch_r<BITS, ST, 4>(a, sh, pdl, stream);
     }
 }
 

@@ -27,6 +27,7 @@ struct GemvArgs {
     int n_blocks;          // ceil(N / RC)
     int chunks;            // C = nb * bs / 32 (32 codes per chunk)
     int a_vec;             // activation rows may be read with 16-byte loads
+    int prefetch_all;      // prefetch the CTA's whole row range into L2 before the dependency wait
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
