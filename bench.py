@@ -404,7 +404,45 @@ def other_rows(torch, mnb, dev):
     return rows
 
 
-PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "quantize_int3")
+PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "quantize_int3", "decode_chain")
+
+
+def decode_chain(torch, mnb, dev):
+    """Kernel-chain microbenchmark of the decode GEMV: for each Qwen3-1.7B
+    projection shape, one CUDA graph of 140 dependent mnb_matmul launches (M=1,
+    INT4 bs32, fp32) over 64 distinct weight copies (>= 4x L2, so the weights
+    stream from HBM), and the same chain on one weight copy (L2-resident for the
+    layer shapes: what is left is the chain's latency).  Prints one line per case."""
+    gen = torch.Generator().manual_seed(5)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, _ = peaks()
+    lines = []
+    for name, K, N in wl.QWEN3_1P7B_PROJECTIONS[:3] + [wl.QWEN3_1P7B_PROJECTIONS[4]]:
+        copies = 64
+        Bs = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev) for _ in range(copies)]
+        Ss = [(torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev) for _ in range(copies)]
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        for label, idx in (("distinct weights", lambda i: i % copies), ("one weight copy", lambda i: 0)):
+            with torch.cuda.stream(stream):
+                mnb.mnb_matmul(A, Bs[0], Ss[0], None, N, BITS, BS, Y, stream=stream)
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                gr.capture_begin()
+                for i in range(140):
+                    j = idx(i)
+                    mnb.mnb_matmul(A, Bs[j], Ss[j], None, N, BITS, BS, Y, stream=stream)
+                gr.capture_end()
+            us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=20)
+            per = us / 140
+            gbs = proj_bytes(K, N) / (per * 1e-6) / 1e9
+            lines.append(f"{name:7s} K={K:5d} N={N:6d} {proj_bytes(K, N) / 1e6:6.2f} MB  {label:16s} "
+                         f"{per:6.2f} us/launch  {gbs:7.1f} GB/s  {gbs / hbm * 100:5.1f} % of HBM")
+            del gr
+        del Bs, Ss
+    torch.cuda.empty_cache()
+    print("\n".join(lines))
 
 
 def profile_case(name):
@@ -415,6 +453,9 @@ def profile_case(name):
     import qmoe_mnb_matmul_gb300 as mnb
     dev = torch.device("cuda", 0)
     gen = torch.Generator().manual_seed(11)
+    if name == "decode_chain":
+        decode_chain(torch, mnb, dev)
+        return
     if name == "gemv_head":  # vocabulary head 2048 -> 151936, M=1, INT4 bs32, fp32: 3 launches
         K, N = wl.QWEN3_1P7B_LM_HEAD[1:]
         B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)

@@ -25,6 +25,7 @@
 //    that hand half of the values to the partner lane at each step (fixed
 //    order, so results are deterministic).
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemv_core.cuh"
@@ -200,33 +201,41 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                 srow[r] = Sc + rl * nb;
                 zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
             }
-            for (int c = lane; c < C; c += 32) {
-                const int b = (c * 32) >> bs_shift;
-                uint4 q[MT][4];
-                float p2[MT];
-                int V[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const uint4* qp = Q + qbase(m, c, C);
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) q[m][qq] = qp[qq * 32];
-                    const int2 cr = Corr[m * C + c];
-                    V[m] = cr.x;
-                    p2[m] = __int_as_float(cr.y);
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    uint32_t w[BITS];
-                    gemv::load_chunk<BITS>(wrow[r], c, w);
-                    const float sc = to_f32(srow[r][b]);
-                    const int z = a.zp ? gemv::zero_point_code<BITS>(zrow[r], b) : kZImplicit;
+            // the chunk loop; HAS_ZP: explicit zero points (a uniform branch, taken once per block)
+            auto chunks = [&](auto has_zp) {
+                for (int c = lane; c < C; c += 32) {
+                    const int b = (c * 32) >> bs_shift;
+                    uint4 q[MT][4];
+                    float p2[MT];
+                    int V[MT];
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        const int T = chunk_dot<BITS>(w, q[m]) - z * V[m];
-                        acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                        const uint4* qp = Q + qbase(m, c, C);
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) q[m][qq] = qp[qq * 32];
+                        const int2 cr = Corr[m * C + c];
+                        V[m] = cr.x;
+                        p2[m] = __int_as_float(cr.y);
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        uint32_t w[BITS];
+                        gemv::load_chunk<BITS>(wrow[r], c, w);
+                        const float sc = to_f32(srow[r][b]);
+                        int z = kZImplicit;
+                        if constexpr (decltype(has_zp)::value) z = gemv::zero_point_code<BITS>(zrow[r], b);
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const int T = chunk_dot<BITS>(w, q[m]) - z * V[m];
+                            acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                        }
                     }
                 }
-            }
+            };
+            if (a.zp)
+                chunks(std::true_type{});
+            else
+                chunks(std::false_type{});
             // value q = r * MT + m; each total ends in one lane
             constexpr int N = R * MT;
             float part[N];
@@ -277,8 +286,11 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     const int64_t align = row_align(row_bytes, nb, ssize);
     const int64_t bytes = N * (row_bytes + int64_t(nb) * ssize);
     const bool small = bytes <= kPrefetchAllBytes;
-    const int64_t ring_target = small ? 64 * 1024 : 144 * 1024;
-    const int64_t cta_cap = small ? 80 * 1024 : kSmemBudget;
+    // large matrices: two CTAs per SM, each with ~80 KB of ring (twice the
+    // warps to cover the instruction latencies, ~120 KB in flight per SM)
+    const int per_sm = small ? 1 : 2;
+    const int64_t ring_target = small ? 64 * 1024 : 80 * 1024;
+    const int64_t cta_cap = small ? 80 * 1024 : 112 * 1024;
     Shape best;
     double best_cost = -1;
     for (int R : {4, 2, 1}) {
@@ -292,7 +304,8 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, ring_target / stage)));
         while (st > 2 && p1.fixed + st * stage > cap) --st;
         const int64_t nblk = cdiv<int64_t>(N, RC);
-        const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(nblk, std::max<int64_t>(1, sm_count / mgroups)));
+        const int64_t ctas =
+            std::max<int64_t>(1, std::min<int64_t>(nblk, std::max<int64_t>(1, int64_t(sm_count) * per_sm / mgroups)));
         const int64_t share = cdiv<int64_t>(nblk, ctas) * RC;  // rows of the busiest CTA
         // fewer rows per warp re-read the activation image more often per code
         const double cost = double(share) * (R == 4 ? 1.0 : R == 2 ? 1.03 : 1.08);
