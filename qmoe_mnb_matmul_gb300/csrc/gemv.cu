@@ -83,7 +83,10 @@ __device__ __forceinline__ void cta_blocks(int nblk, int x, int gx, int& first, 
 template <int BITS, int ST, int MT, int R>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using S = typename DType<ST>::T;
-    constexpr int RC = kConsumerWarps * R;
+    // ring mode: blocks of 8 R rows, every warp takes R rows of every block;
+    // task mode: blocks of R rows, warp w takes blocks w, w + 8, ... of the CTA
+    const bool tasks = a.task_mode != 0;
+    const int RC = a.rows_per_block;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int C = a.chunks, nb = a.nb;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         // ------------------------------------------------------- producer
         if (lane != 0) return;
         int st = 0;
-        uint32_t round = 0;  // times the ring has wrapped
+        uint32_t round = 0;  // times the ring has wrapped (never, in task mode: one slot per block)
         for (int blk = b_first; blk < b_last; ++blk) {
             if (round && !mbar_wait(&empty[st], (round - 1) & 1)) {
                 for (int j = 0; j < NST; ++j) mbar_wait(&full[j], 0);  // give in-flight copies a bounded chance
@@ -176,15 +179,15 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 
     const int bs_shift = __ffs(a.bs) - 1;
     constexpr int kZImplicit = 1 << (BITS - 1);
-    int st = 0;
+    int st = tasks ? warp : 0;
     uint32_t phase = 0;
-    for (int blk = b_first; blk < b_last; ++blk) {
+    for (int blk = b_first + (tasks ? warp : 0); blk < b_last; blk += tasks ? kConsumerWarps : 1) {
         if (!warp_wait(&full[st], phase)) return;
         const int64_t n0 = int64_t(blk) * RC;
         const int rc = block_rows(blk);
         const uint8_t* W = Wst + st * plan.w_stage;
         const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
-        const int r0 = warp * R;
+        const int r0 = tasks ? 0 : warp * R;
         if (r0 < rc) {
             float acc[R][MT];
 #pragma unroll
@@ -250,6 +253,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             }
         }
         __syncwarp();
+        if (tasks) {
+            st += kConsumerWarps;  // every block has its own slot; nothing is refilled
+            continue;
+        }
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == NST) { st = 0; phase ^= 1; }
     }
@@ -271,47 +278,67 @@ int64_t row_align(int64_t row_bytes, int nb, int ssize) {
 // still running, so a chain of decode projections streams without gaps.
 constexpr int64_t kPrefetchAllBytes = int64_t(32) << 20;
 
-// Launch shape: rows per warp R, ring depth and grid.  Small matrices (whole
-// L2 prefetch) keep each CTA's shared memory modest so that the next
-// kernel's CTAs fit beside it (~72 KB); large ones get a deep ring (~144 KB
-// in flight per SM) to cover HBM latency.  Among the R that fit, the one
-// whose busiest CTA has the fewest rows wins, with a small handicap for
-// fewer rows per warp (more activation-image reads per code).
+// Launch shape.
+//  * Small matrices (prefetched into L2 whole; the layer projections of a
+//    decode step): task mode.  Work is cut into tasks of R rows, spread over
+//    two CTAs per SM so that every warp has at most one task; each CTA copies
+//    all its tasks at once (one barrier per task), so no warp waits on
+//    another warp's rows.  The time of such a launch is mostly latency (the
+//    dependency release, one L2 round trip for the activations and the rows,
+//    the stores); this keeps the compute part to one short pass per warp.
+//  * Large matrices (the vocabulary head): ring mode with two CTAs per SM and
+//    ~80 KB of ring each, so that ~120 KB per SM are in flight (bulk copies
+//    need well over 64 KB in flight per SM to reach HBM bandwidth).
 struct Shape {
-    int R = 4, stages = 2, grid = 1;
-    bool prefetch_all = false;
+    int R = 4, stages = 2, grid = 1, rows_per_block = 32;
+    bool prefetch_all = false, task_mode = false;
 };
 
 Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups) {
     const int64_t align = row_align(row_bytes, nb, ssize);
-    const int64_t bytes = N * (row_bytes + int64_t(nb) * ssize);
-    const bool small = bytes <= kPrefetchAllBytes;
-    // large matrices: two CTAs per SM, each with ~80 KB of ring (twice the
-    // warps to cover the instruction latencies, ~120 KB in flight per SM)
-    const int per_sm = small ? 1 : 2;
-    const int64_t ring_target = small ? 64 * 1024 : 80 * 1024;
-    const int64_t cta_cap = small ? 80 * 1024 : 112 * 1024;
+    const int64_t row_total = row_bytes + int64_t(nb) * ssize;
+    const bool small = N * row_total <= kPrefetchAllBytes;
+    const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
     Shape best;
+    if (small) {
+        for (int R : {4, 2, 1}) {
+            if (MT == 4 && R == 4) continue;  // keeps the four rows' activation images in registers
+            if (R % align != 0) continue;
+            const int64_t nblk = cdiv<int64_t>(N, R);
+            const int64_t grid = std::min<int64_t>(nblk, per_group);
+            const int64_t bpc = cdiv<int64_t>(nblk, grid);  // blocks (tasks) of the busiest CTA
+            if (bpc > kMaxStages) continue;
+            const Plan p = make_plan(MT, C, R, row_bytes, nb, ssize, static_cast<int>(bpc));
+            if (p.total > 100 * 1024) continue;
+            best.R = R;
+            best.rows_per_block = R;
+            best.stages = static_cast<int>(bpc);
+            best.grid = static_cast<int>(cdiv<int64_t>(nblk, bpc));
+            best.task_mode = true;
+            best.prefetch_all = true;
+            return best;
+        }
+    }
     double best_cost = -1;
     for (int R : {4, 2, 1}) {
-        if (MT == 4 && R == 4) continue;  // keeps the four rows' activation images in registers
+        if (MT == 4 && R == 4) continue;
         const int RC = kConsumerWarps * R;
         if (RC % align != 0) continue;
         const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
         const int64_t stage = p1.w_stage + p1.s_stage;
-        const int64_t cap = std::max<int64_t>(cta_cap, p1.fixed + 2 * stage);
+        const int64_t cap = std::max<int64_t>(112 * 1024, p1.fixed + 2 * stage);
         if (p1.fixed + 2 * stage > kSmemBudget) continue;
-        int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, ring_target / stage)));
+        int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, (80 * 1024) / stage)));
         while (st > 2 && p1.fixed + st * stage > cap) --st;
         const int64_t nblk = cdiv<int64_t>(N, RC);
-        const int64_t ctas =
-            std::max<int64_t>(1, std::min<int64_t>(nblk, std::max<int64_t>(1, int64_t(sm_count) * per_sm / mgroups)));
+        const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(nblk, per_group));
         const int64_t share = cdiv<int64_t>(nblk, ctas) * RC;  // rows of the busiest CTA
         // fewer rows per warp re-read the activation image more often per code
         const double cost = double(share) * (R == 4 ? 1.0 : R == 2 ? 1.03 : 1.08);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best.R = R;
+            best.rows_per_block = RC;
             best.stages = st;
             // as few CTAs as give every CTA the busiest CTA's share
             best.grid = static_cast<int>(cdiv<int64_t>(nblk, cdiv<int64_t>(nblk, ctas)));
@@ -323,13 +350,13 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
 
 template <int BITS, int ST, int MT, int R>
 cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t stream) {
-    constexpr int RC = kConsumerWarps * R;
     const int ssize = ST == kF32 ? 4 : 2;
-    a.rows_per_block = RC;
-    a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, RC));
+    a.rows_per_block = sh.rows_per_block;
+    a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, sh.rows_per_block));
     a.stages = sh.stages;
     a.prefetch_all = sh.prefetch_all ? 1 : 0;
-    const Plan p = make_plan(MT, a.chunks, RC, a.row_bytes, a.nb, ssize, sh.stages);
+    a.task_mode = sh.task_mode ? 1 : 0;
+    const Plan p = make_plan(MT, a.chunks, sh.rows_per_block, a.row_bytes, a.nb, ssize, sh.stages);
     if (p.total > kSmemBudget) return cudaErrorNotSupported;
     auto kern = gemv_kernel<BITS, ST, MT, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
