@@ -84,7 +84,9 @@ template <int BITS, int ST, int MT, int R>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using S = typename DType<ST>::T;
     // ring mode: blocks of 8 R rows, every warp takes R rows of every block;
-    // task mode: blocks of R rows, warp w takes blocks w, w + 8, ... of the CTA
+    // slice mode: CTA x owns blocks 8x .. 8x+7 (one per warp, a block being
+    // the warp's slice of rows), all copied at once; a warp walks its slice R
+    // rows at a time
     const bool tasks = a.task_mode != 0;
     const int RC = a.rows_per_block;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -102,7 +104,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = int64_t(blockIdx.y) * MT;
     int b_first, b_last;
-    cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
+    if (tasks) {
+        b_first = blockIdx.x * kConsumerWarps;
+        b_last = min(b_first + kConsumerWarps, a.n_blocks);
+    } else {
+        cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
+    }
     auto block_rows = [&](int blk) -> int {
         const int64_t left = a.N - int64_t(blk) * RC;
         return static_cast<int>(left < RC ? left : int64_t(RC));
@@ -187,8 +194,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         const int rc = block_rows(blk);
         const uint8_t* W = Wst + st * plan.w_stage;
         const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
-        const int r0 = tasks ? 0 : warp * R;
-        if (r0 < rc) {
+        // ring mode: this warp's R rows of the block; slice mode: every R rows of it
+        for (int r0 = tasks ? 0 : warp * R; r0 < rc; r0 += tasks ? R : rc) {
             float acc[R][MT];
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -301,19 +308,16 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
     Shape best;
     if (small) {
-        for (int R : {4, 2, 1}) {
-            if (MT == 4 && R == 4) continue;  // keeps the four rows' activation images in registers
-            if (R % align != 0) continue;
-            const int64_t nblk = cdiv<int64_t>(N, R);
-            const int64_t grid = std::min<int64_t>(nblk, per_group);
-            const int64_t bpc = cdiv<int64_t>(nblk, grid);  // blocks (tasks) of the busiest CTA
-            if (bpc > kMaxStages) continue;
-            const Plan p = make_plan(MT, C, R, row_bytes, nb, ssize, static_cast<int>(bpc));
-            if (p.total > 100 * 1024) continue;
+        // rows per warp: the matrix spread over every warp of two CTAs per SM
+        int64_t rpw = cdiv<int64_t>(N, per_group * kConsumerWarps);
+        rpw = cdiv<int64_t>(rpw, align) * align;
+        const int R = rpw >= 3 ? 4 : static_cast<int>(rpw);
+        const Plan p = make_plan(MT, C, static_cast<int>(rpw), row_bytes, nb, ssize, kConsumerWarps);
+        if (rpw <= 64 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
             best.R = R;
-            best.rows_per_block = R;
-            best.stages = static_cast<int>(bpc);
-            best.grid = static_cast<int>(cdiv<int64_t>(nblk, bpc));
+            best.rows_per_block = static_cast<int>(rpw);
+            best.stages = kConsumerWarps;
+            best.grid = static_cast<int>(cdiv<int64_t>(N, rpw * kConsumerWarps));
             best.task_mode = true;
             best.prefetch_all = true;
             return best;

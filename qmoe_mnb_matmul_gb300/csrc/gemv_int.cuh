@@ -102,71 +102,87 @@ __device__ __forceinline__ uint32_t digit_byte(int d, int lane) { return (static
 
 // One thread per (row m, chunk c, code word i): the eight activations of codes
 // 32c + 8i .. +7 of row m -> the image words and, from lane i == 0 of the four
-// adjacent lanes that share the chunk, the chunk's {V, 2^-s}.  Every lane of a
-// warp runs the same number of iterations (the shuffles need all of them);
-// row(m) returns activation row m (K valid entries, dtype `dt`) or nullptr for
-// a row of zeros; `vec`: rows may be read with 16-byte loads.
+// adjacent lanes that share the chunk, the chunk's {V, 2^-s}.  A thread loads
+// up to kStageBatch items before it converts any (one memory round trip per
+// batch, not per item).  Every lane of a warp runs the same number of
+// iterations (the shuffles need all of them); row(m) returns activation row m
+// (K valid entries, dtype `dt`) or nullptr for a row of zeros; `vec`: rows may
+// be read with 16-byte loads.
+constexpr int kStageBatch = 4;
+
 template <typename RowFn>
 __device__ __forceinline__ void stage_image(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec, RowFn row,
                                             int tid, int nthreads) {
     const int total = MT * C * 4;
-    for (int base = 0; base < total; base += nthreads) {
-        const int item = base + tid;
-        const bool live = item < total;
-        const int i = item & 3, mc = item >> 2;
-        const int m = live ? mc / C : 0, c = live ? mc - m * C : 0;
-        const void* src = live ? row(m) : nullptr;
-        const int64_t k0 = int64_t(c) * 32 + 8 * i;
-        float a[8];
-        if (src != nullptr && vec && k0 + 8 <= K) {
-            if (dt == kF32) {
-                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + k0);
-                const float4 x = p[0], y = p[1];
-                a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w; a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
-            } else {
-                const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + k0);
-                const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+    for (int base = 0; base < total; base += nthreads * kStageBatch) {
+        float a[kStageBatch][8];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    if (dt == kF16) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[h]));
-                        a[2 * h] = f.x; a[2 * h + 1] = f.y;
-                    } else {
-                        a[2 * h] = __uint_as_float(u[h] << 16);
-                        a[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+        for (int u = 0; u < kStageBatch; ++u) {
+            const int item = base + u * nthreads + tid;
+            const bool live = item < total;
+            const int i = item & 3, mc = item >> 2;
+            const int m = live ? mc / C : 0, c = live ? mc - m * C : 0;
+            const void* src = live ? row(m) : nullptr;
+            const int64_t k0 = int64_t(c) * 32 + 8 * i;
+            if (src != nullptr && vec && k0 + 8 <= K) {
+                if (dt == kF32) {
+                    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + k0);
+                    const float4 x = p[0], y = p[1];
+                    a[u][0] = x.x; a[u][1] = x.y; a[u][2] = x.z; a[u][3] = x.w;
+                    a[u][4] = y.x; a[u][5] = y.y; a[u][6] = y.z; a[u][7] = y.w;
+                } else {
+                    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + k0);
+                    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (dt == kF16) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[h]));
+                            a[u][2 * h] = f.x; a[u][2 * h + 1] = f.y;
+                        } else {
+                            a[u][2 * h] = __uint_as_float(w4[h] << 16);
+                            a[u][2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+                        }
                     }
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a[u][j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) a[j] = (src != nullptr && k0 + j < K) ? load_as_f32(src, dt, k0 + j) : 0.f;
         }
-        uint32_t mx = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mx = max(mx, __float_as_uint(a[j]) & 0x7FFFFFFFu);
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const int s = min(140 - static_cast<int>(mx >> 23), 126);  // |a| 2^s < 2^14 for the whole chunk
-        const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-        uint32_t wd[4] = {0u, 0u, 0u, 0u};  // even low, even high, odd low, odd high
-        int vsum = 0;
+        for (int u = 0; u < kStageBatch; ++u) {
+            if (base + u * nthreads >= total) break;  // uniform: no lane of the CTA has items from here on
+            const int item = base + u * nthreads + tid;
+            const bool live = item < total;
+            const int i = item & 3, mc = item >> 2;
+            const int m = live ? mc / C : 0, c = live ? mc - m * C : 0;
+            uint32_t mx = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int v = __float2int_rn(a[j] * up);  // exact scaling, one rounding
-            const int d1 = (v + 128) >> 8;
-            const int d0 = v - d1 * 256;
-            const int odd = j & 1, lane = j >> 1;
-            wd[2 * odd] |= digit_byte(d0, lane);
-            wd[2 * odd + 1] |= digit_byte(d1, lane);
-            vsum += v;
-        }
-        vsum += __shfl_xor_sync(0xffffffffu, vsum, 1);
-        vsum += __shfl_xor_sync(0xffffffffu, vsum, 2);
-        if (live) {
-            uint32_t* q = reinterpret_cast<uint32_t*>(Q + qbase(m, c, C));
+            for (int j = 0; j < 8; ++j) mx = max(mx, __float_as_uint(a[u][j]) & 0x7FFFFFFFu);
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const int s = min(140 - static_cast<int>(mx >> 23), 126);  // |a| 2^s < 2^14 for the whole chunk
+            const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};  // even low, even high, odd low, odd high
+            int vsum = 0;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) q[qq * 32 * 4 + i] = wd[qq];
-            if (i == 0) Corr[m * C + c] = make_int2(vsum, static_cast<int>(static_cast<uint32_t>(127 - s) << 23));
+            for (int j = 0; j < 8; ++j) {
+                const int v = __float2int_rn(a[u][j] * up);  // exact scaling, one rounding
+                const int d1 = (v + 128) >> 8;
+                const int d0 = v - d1 * 256;
+                const int odd = j & 1, lane = j >> 1;
+                wd[2 * odd] |= digit_byte(d0, lane);
+                wd[2 * odd + 1] |= digit_byte(d1, lane);
+                vsum += v;
+            }
+            vsum += __shfl_xor_sync(0xffffffffu, vsum, 1);
+            vsum += __shfl_xor_sync(0xffffffffu, vsum, 2);
+            if (live) {
+                uint32_t* q = reinterpret_cast<uint32_t*>(Q + qbase(m, c, C));
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) q[qq * 32 * 4 + i] = wd[qq];
+                if (i == 0) Corr[m * C + c] = make_int2(vsum, static_cast<int>(static_cast<uint32_t>(127 - s) << 23));
+            }
         }
     }
 }
