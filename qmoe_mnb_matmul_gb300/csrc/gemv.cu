@@ -6,7 +6,7 @@
 // consumed; no dequantised weight matrix is ever written to global memory.
 //
 // Design (HBM-bound: the packed weights and scales are the traffic):
-//  * A CTA owns one contiguous range of row blocks (RC = 8 * R rows each).
+//  * A CTA owns one contiguous range of row blocks (RC = 8 warps x rpw rows).
 //    Rows are contiguous in the [N, nb, blob] layout, so the range's packed
 //    bytes and scales are two contiguous byte ranges: before its grid
 //    dependency wait the CTA asks L2 to prefetch them (the whole range when
@@ -19,8 +19,9 @@
 //    bulk (TMA) copies of whole row blocks, waiting on per-stage "empty"
 //    mbarriers; the 8 consumer warps wait on the per-stage "full" mbarriers.
 //  * The activations are staged once per CTA as a fixed-point image
-//    (gemv_int.cuh); each consumer warp owns R rows of a block and walks
-//    their 32-code chunks, one chunk per lane, with exact dp4a integer dot
+//    (gemv_int.cuh); each consumer warp owns a slice of rpw rows of a block
+//    and walks their 32-code chunks R rows at a time, one chunk per lane,
+//    with exact dp4a integer dot
 //    products per chunk; the R x MT sums are reduced together with shuffles
 //    that hand half of the values to the partner lane at each step (fixed
 //    order, so results are deterministic).
@@ -83,12 +84,11 @@ __device__ __forceinline__ void cta_blocks(int nblk, int x, int gx, int& first, 
 template <int BITS, int ST, int MT, int R>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
     using S = typename DType<ST>::T;
-    // ring mode: blocks of 8 R rows, every warp takes R rows of every block;
-    // slice mode: CTA x owns blocks 8x .. 8x+7 (one per warp, a block being
-    // the warp's slice of rows), all copied at once; a warp walks its slice R
-    // rows at a time
-    const bool tasks = a.task_mode != 0;
+    // Blocks of RC = 8 * rpw rows: warp w takes rows [w rpw, (w+1) rpw) of
+    // every block, R rows at a time (rpw = R for the large matrices; small
+    // matrices have one block per CTA and rpw of 1..4).
     const int RC = a.rows_per_block;
+    const int rpw = RC / kConsumerWarps;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int C = a.chunks, nb = a.nb;
@@ -104,12 +104,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t m0 = int64_t(blockIdx.y) * MT;
     int b_first, b_last;
-    if (tasks) {
-        b_first = blockIdx.x * kConsumerWarps;
-        b_last = min(b_first + kConsumerWarps, a.n_blocks);
-    } else {
-        cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
-    }
+    cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
     auto block_rows = [&](int blk) -> int {
         const int64_t left = a.N - int64_t(blk) * RC;
         return static_cast<int>(left < RC ? left : int64_t(RC));
@@ -148,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         // ------------------------------------------------------- producer
         if (lane != 0) return;
         int st = 0;
-        uint32_t round = 0;  // times the ring has wrapped (never, in task mode: one slot per block)
+        uint32_t round = 0;  // times the ring has wrapped
         for (int blk = b_first; blk < b_last; ++blk) {
             if (round && !mbar_wait(&empty[st], (round - 1) & 1)) {
                 for (int j = 0; j < NST; ++j) mbar_wait(&full[j], 0);  // give in-flight copies a bounded chance
@@ -186,16 +181,17 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 
     const int bs_shift = __ffs(a.bs) - 1;
     constexpr int kZImplicit = 1 << (BITS - 1);
-    int st = tasks ? warp : 0;
+    int st = 0;
     uint32_t phase = 0;
-    for (int blk = b_first + (tasks ? warp : 0); blk < b_last; blk += tasks ? kConsumerWarps : 1) {
+    for (int blk = b_first; blk < b_last; ++blk) {
         if (!warp_wait(&full[st], phase)) return;
         const int64_t n0 = int64_t(blk) * RC;
         const int rc = block_rows(blk);
         const uint8_t* W = Wst + st * plan.w_stage;
         const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
-        // ring mode: this warp's R rows of the block; slice mode: every R rows of it
-        for (int r0 = tasks ? 0 : warp * R; r0 < rc; r0 += tasks ? R : rc) {
+        // this warp's slice of the block, R rows at a time
+        const int w_end = min(rc, (warp + 1) * rpw);
+        for (int r0 = warp * rpw; r0 < w_end; r0 += R) {
             float acc[R][MT];
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -206,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             const uint8_t* zrow[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int rl = min(r0 + r, rc - 1);  // rows past the block end recompute the last row
+                const int rl = min(r0 + r, w_end - 1);  // rows past the slice end recompute its last row
                 wrow[r] = W + int64_t(rl) * a.row_bytes;
                 srow[r] = Sc + rl * nb;
                 zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
@@ -256,14 +252,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             const float total = warp_sum_transpose<N>(part);
             if ((lane & (32 / N - 1)) == 0) {
                 const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
-                if (r0 + r < rc && m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
+                if (r0 + r < w_end && m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
             }
         }
         __syncwarp();
-        if (tasks) {
-            st += kConsumerWarps;  // every block has its own slot; nothing is refilled
-            continue;
-        }
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == NST) { st = 0; phase ^= 1; }
     }
@@ -287,18 +279,18 @@ constexpr int64_t kPrefetchAllBytes = int64_t(32) << 20;
 
 // Launch shape.
 //  * Small matrices (prefetched into L2 whole; the layer projections of a
-//    decode step): task mode.  Work is cut into tasks of R rows, spread over
-//    two CTAs per SM so that every warp has at most one task; each CTA copies
-//    all its tasks at once (one barrier per task), so no warp waits on
-//    another warp's rows.  The time of such a launch is mostly latency (the
-//    dependency release, one L2 round trip for the activations and the rows,
-//    the stores); this keeps the compute part to one short pass per warp.
-//  * Large matrices (the vocabulary head): ring mode with two CTAs per SM and
+//    decode step): one block per CTA, two CTAs per SM, every warp a slice of
+//    1..4 rows, the block's rows and scales moved by two bulk copies.  Such a
+//    launch is mostly latency (the dependency release, one L2 round trip for
+//    the activations and the rows, the stores); this keeps the compute part to
+//    one short pass per warp and the copies few and large.
+//  * Large matrices (the vocabulary head): a ring with two CTAs per SM and
 //    ~80 KB of ring each, so that ~120 KB per SM are in flight (bulk copies
-//    need well over 64 KB in flight per SM to reach HBM bandwidth).
+//    need well over 64 KB in flight per SM to reach HBM bandwidth); each warp
+//    takes R rows of every block.
 struct Shape {
     int R = 4, stages = 2, grid = 1, rows_per_block = 32;
-    bool prefetch_all = false, task_mode = false;
+    bool prefetch_all = false;
 };
 
 Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups) {
@@ -308,17 +300,18 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
     Shape best;
     if (small) {
-        // rows per warp: the matrix spread over every warp of two CTAs per SM
+        // one block per CTA: the matrix spread over every warp of two CTAs
+        // per SM, each warp a slice of rpw rows (two bulk copies per CTA)
         int64_t rpw = cdiv<int64_t>(N, per_group * kConsumerWarps);
-        rpw = cdiv<int64_t>(rpw, align) * align;
+        while ((rpw * kConsumerWarps) % align != 0) ++rpw;
         const int R = rpw >= 3 ? 4 : static_cast<int>(rpw);
-        const Plan p = make_plan(MT, C, static_cast<int>(rpw), row_bytes, nb, ssize, kConsumerWarps);
-        if (rpw <= 64 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
+        const int64_t RC = rpw * kConsumerWarps;
+        const Plan p = make_plan(MT, C, static_cast<int>(RC), row_bytes, nb, ssize, 1);
+        if (rpw <= 8 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
             best.R = R;
-            best.rows_per_block = static_cast<int>(rpw);
-            best.stages = kConsumerWarps;
-            best.grid = static_cast<int>(cdiv<int64_t>(N, rpw * kConsumerWarps));
-            best.task_mode = true;
+            best.rows_per_block = static_cast<int>(RC);
+            best.stages = 1;
+            best.grid = static_cast<int>(cdiv<int64_t>(N, RC));
             best.prefetch_all = true;
             return best;
         }
@@ -359,7 +352,6 @@ cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t str
     a.n_blocks = static_cast<int>(cdiv<int64_t>(a.N, sh.rows_per_block));
     a.stages = sh.stages;
     a.prefetch_all = sh.prefetch_all ? 1 : 0;
-    a.task_mode = sh.task_mode ? 1 : 0;
     const Plan p = make_plan(MT, a.chunks, sh.rows_per_block, a.row_bytes, a.nb, ssize, sh.stages);
     if (p.total > kSmemBudget) return cudaErrorNotSupported;
     auto kern = gemv_kernel<BITS, ST, MT, R>;

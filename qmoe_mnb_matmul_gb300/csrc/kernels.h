@@ -22,13 +22,12 @@ struct GemvArgs {
     void* Y;
     int y_dtype;
     int64_t y_ld;          // row stride of Y in elements (N for a plain matmul)
-    int rows_per_block;    // RC: rows of B staged per pipeline stage
+    int rows_per_block;    // RC: rows of B staged per pipeline stage (8 warps x rows per warp)
     int stages;            // depth of the shared-memory ring
     int n_blocks;          // ceil(N / RC)
     int chunks;            // C = nb * bs / 32 (32 codes per chunk)
     int a_vec;             // activation rows may be read with 16-byte loads
     int prefetch_all;      // prefetch the CTA's whole row range into L2 before the dependency wait
-    int task_mode;         // blocks of R rows, one per warp, all copied at once (no ring)
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
