@@ -279,8 +279,8 @@ constexpr int64_t kPrefetchAllBytes = int64_t(32) << 20;
 
 // Launch shape.
 //  * Small matrices (prefetched into L2 whole; the layer projections of a
-//    decode step): one block per CTA, two CTAs per SM, every warp a slice of
-//    1..4 rows, the block's rows and scales moved by two bulk copies.  Such a
+//    decode step): one block per CTA, one CTA per SM, every warp a slice of
+//    rows, the block's rows and scales moved by two bulk copies.  Such a
 //    launch is mostly latency (the dependency release, one L2 round trip for
 //    the activations and the rows, the stores); this keeps the compute part to
 //    one short pass per warp and the copies few and large.
@@ -297,14 +297,17 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     const int64_t align = row_align(row_bytes, nb, ssize);
     const int64_t row_total = row_bytes + int64_t(nb) * ssize;
     const bool small = N * row_total <= kPrefetchAllBytes;
-    const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
     Shape best;
     if (small) {
-        // one block per CTA: the matrix spread over every warp of two CTAs
-        // per SM, each warp a slice of rpw rows (two bulk copies per CTA)
-        int64_t rpw = cdiv<int64_t>(N, per_group * kConsumerWarps);
+        // one block per CTA and one CTA per SM (at ~70 registers a thread an
+        // SM holds three such CTAs: this kernel's, and the next two kernels'
+        // of a chain, which prefetch their rows meanwhile), each warp a slice
+        // of rpw rows of the block (two bulk copies per CTA)
+        const int64_t ctas = std::max<int64_t>(1, sm_count / mgroups);
+        int64_t rpw = cdiv<int64_t>(N, ctas * kConsumerWarps);
+        rpw = rpw <= 2 ? rpw : rpw <= 4 ? 4 : cdiv<int64_t>(rpw, 2) * 2;  // 1, 2, 4, then even
         while ((rpw * kConsumerWarps) % align != 0) ++rpw;
-        const int R = rpw >= 3 ? 4 : static_cast<int>(rpw);
+        const int R = rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
         const int64_t RC = rpw * kConsumerWarps;
         const Plan p = make_plan(MT, C, static_cast<int>(RC), row_bytes, nb, ssize, 1);
         if (rpw <= 8 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
@@ -316,6 +319,7 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
             return best;
         }
     }
+    const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
     double best_cost = -1;
     for (int R : {4, 2, 1}) {
         if (MT == 4 && R == 4) continue;
