@@ -11,10 +11,10 @@
 //    bytes and scales are two contiguous byte ranges: before its grid
 //    dependency wait the CTA asks L2 to prefetch them (the whole range when
 //    the matrix is small enough to sit in L2 beside its neighbours, else the
-//    first ring-full) and lets the next kernel on the stream launch, so a
-//    chain of projections keeps HBM busy across kernel boundaries.  Nothing
-//    the CTA reads is read before the wait (a prefetch only warms L2, which
-//    stays coherent with any later write).
+//    first ring-full); right after the wait it lets the next kernel on the
+//    stream launch, whose CTAs then prefetch their own rows while this one
+//    computes.  Nothing the CTA reads is read before the wait (a prefetch
+//    only warms L2, which stays coherent with any later write).
 //  * Warp 8 is the producer: one lane keeps a ring of NST stages filled with
 //    bulk (TMA) copies of whole row blocks, waiting on per-stage "empty"
 //    mbarriers; the 8 consumer warps wait on the per-stage "full" mbarriers.
@@ -133,10 +133,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             prefetch(static_cast<const uint8_t*>(a.scales) + r0 * nb * ss, (r1 - r0) * nb * ss);
         }
     }
-    // The next kernel on the stream may start its own prologue now; it reads
-    // nothing before its dependency wait either.
-    grid_launch_dependents();
+    // The next kernel on the stream may start its prologue (its own L2
+    // prefetch) once this one has passed its dependency wait: one kernel of a
+    // chain runs ahead, no more (letting several run ahead measured slower).
     grid_dependency_wait();
+    grid_launch_dependents();
     __syncthreads();
 
     if (warp == kConsumerWarps) {

@@ -102,17 +102,18 @@ __device__ __forceinline__ uint32_t digit_byte(int d, int lane) { return (static
 
 // One thread per (row m, chunk c, code word i): the eight activations of codes
 // 32c + 8i .. +7 of row m -> the image words and, from lane i == 0 of the four
-// adjacent lanes that share the chunk, the chunk's {V, 2^-s}.  A thread loads
-// up to kStageBatch items before it converts any (one memory round trip per
-// batch, not per item).  Every lane of a warp runs the same number of
-// iterations (the shuffles need all of them); row(m) returns activation row m
-// (K valid entries, dtype `dt`) or nullptr for a row of zeros; `vec`: rows may
-// be read with 16-byte loads.
+// adjacent lanes that share the chunk, the chunk's {V, 2^-s}.  With more items
+// than threads, a thread loads kStageBatch items before it converts any (one
+// memory round trip per batch, not per item).  Every lane of a warp runs the
+// same number of iterations (the shuffles need all of them); row(m) returns
+// activation row m (K valid entries, dtype `dt`) or nullptr for a row of
+// zeros; `vec`: rows may be read with 16-byte loads.
 constexpr int kStageBatch = 4;
 
-template <typename RowFn>
-__device__ __forceinline__ void stage_image(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec, RowFn row,
-                                            int tid, int nthreads) {
+template <int BATCH, typename RowFn>
+__device__ __forceinline__ void stage_image_b(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec,
+                                              RowFn row, int tid, int nthreads) {
+    constexpr int kStageBatch = BATCH;
     const int total = MT * C * 4;
     for (int base = 0; base < total; base += nthreads * kStageBatch) {
         float a[kStageBatch][8];
@@ -185,6 +186,17 @@ __device__ __forceinline__ void stage_image(uint4* Q, int2* Corr, int MT, int C,
             }
         }
     }
+}
+
+// One item per thread when they all fit (the common decode case: a batch
+// would only add dead slots), else batches of kStageBatch.
+template <typename RowFn>
+__device__ __forceinline__ void stage_image(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec, RowFn row,
+                                            int tid, int nthreads) {
+    if (MT * C * 4 <= nthreads)
+        stage_image_b<1>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads);
+    else
+        stage_image_b<kStageBatch>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads);
 }
 
 }  // namespace gemv_int
