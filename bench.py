@@ -246,19 +246,31 @@ def run_reference(args, ws, rank):
 MOE = wl.QWEN3_30B_A3B_MOE
 
 
-def moe_expert_bytes(b1, b2, bs):
+def moe_expert_bytes(b1, b2, bs, zp=False):
+    """Packed weights + 16-bit scales (+ packed zero points) of one expert."""
     H, I = MOE["H"], MOE["I"]
-    return 2 * I * (H * b1 // 8 + H // bs * 2) + H * (I * b2 // 8 + I // bs * 2)
+    b = 2 * I * (H * b1 // 8 + H // bs * 2) + H * (I * b2 // 8 + I // bs * 2)
+    if zp:
+        b += 2 * I * (((H // bs) * b1 + 7) // 8) + H * (((I // bs) * b2 + 7) // 8)
+    return b
 
 
-def make_moe_layers(torch, dev, n, b1, b2, bs, gen):
+def make_moe_layers(torch, dev, n, b1, b2, bs, gen, act=None, zp=False):
+    """n distinct QMoE layers: (fc1_w, fc1_s, fc1_zp, fc2_w, fc2_s, fc2_zp), scales in `act` (fp16 default)."""
     H, I, E = MOE["H"], MOE["I"], MOE["E"]
+    act = torch.float16 if act is None else act
+
     def r8(*shape):
         return torch.randint(0, 256, shape, dtype=torch.uint8, generator=gen).to(dev)
+
     def sc(*shape):
-        return (torch.rand(shape, generator=gen) * 0.015 + 0.005).half().to(dev)
-    return [(r8(E, 2 * I, H * b1 // 8), sc(E, 2 * I, H // bs), r8(E, H, I * b2 // 8), sc(E, H, I // bs))
-            for _ in range(n)]
+        return (torch.rand(shape, generator=gen) * 0.015 + 0.005).to(act).to(dev)
+    out = []
+    for _ in range(n):
+        z1 = r8(E, 2 * I, ((H // bs) * b1 + 7) // 8) if zp else None
+        z2 = r8(E, H, ((I // bs) * b2 + 7) // 8) if zp else None
+        out.append((r8(E, 2 * I, H * b1 // 8), sc(E, 2 * I, H // bs), z1, r8(E, H, I * b2 // 8), sc(E, H, I // bs), z2))
+    return out
 
 
 def event_time_us(torch, stream, fn, reps, warmup=3):
@@ -278,112 +290,157 @@ def event_time_us(torch, stream, fn, reps, warmup=3):
     return us[len(us) // 2], us[len(us) // 10], us[(len(us) * 9) // 10]
 
 
-def other_rows(torch, mnb, dev):
-    """The rest of the hot path, each against its own roofline: the tensor-core
-    GEMM at small M (M=16, HBM-bound) and prefill (M=2048, bf16), one
-    Qwen3-30B-A3B-shaped QMoE layer at decode (T=1, CUDA graph over 16 distinct
-    layers) and prefill (T=4096), and the INT3 quantizer over one layer's FC1
-    expert weights."""
-    gen = torch.Generator().manual_seed(7)
-    stream = torch.cuda.Stream(device=dev)
-    hbm, hbm_kind = peaks()
-    tc, tc_kind = tc_peak()
-    rows = {}
-    # a5, small M (memory-bound): the qkv projection at M=16 through the K-split tensor-core path,
-    # 16 distinct weight copies replayed in one graph
-    M, K, N = 16, 2048, 4096
-    Bs = [torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev) for _ in range(16)]
-    Ss = [(torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev) for _ in range(16)]
-    A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(1, mnb.mnb_matmul_workspace_size(M, K, N, BITS, BS, mnb.BF16)), dtype=torch.uint8,
-                     device=dev)
+def _row(kernel, shape, us, p10, p90, achieved, unit, peak, bound, peak_src, **extra):
+    r = {"kernel": kernel, "shape": shape, "us": us, "us_p10_p90": [p10, p90], "achieved": achieved, "unit": unit,
+         "peak": peak, "frac": achieved / peak, "bound": bound, "peak_source": peak_src}
+    r.update(extra)
+    return r
+
+
+def graph_time(torch, stream, calls, reps=30):
+    """Median per-call time (us) of the calls captured in one CUDA graph."""
     with torch.cuda.stream(stream):
-        mnb.mnb_matmul(A, Bs[0], Ss[0], None, N, BITS, BS, Y, ws, stream=stream)
+        calls[0]()
     torch.cuda.synchronize()
     gr = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         gr.capture_begin()
-        for i in range(16):
-            mnb.mnb_matmul(A, Bs[i], Ss[i], None, N, BITS, BS, Y, ws, stream=stream)
+        for c in calls:
+            c()
         gr.capture_end()
-    us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=30)
-    us, p10, p90 = us / 16, p10 / 16, p90 / 16
-    nbytes = proj_bytes(K, N) - K * 4 - N * 4 + M * K * 2 + M * N * 2
-    rows["prefill_gemm_qkv_m16"] = {
-        "kernel": "gemm_tc (tcgen05, K split across CTAs) + split-K reduction",
-        "shape": f"M={M} K={K} N={N} INT4 bs32 bf16 A/Y, fp32 scales, 16 distinct weight copies in one graph",
-        "us": us, "us_p10_p90": [p10, p90], "achieved": nbytes / (us * 1e-6) / 1e9, "unit": "GB/s", "peak": hbm,
-        "frac": nbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm", "peak_source": f"{hbm_kind} hbm_gbs"}
-    del Bs, Ss, A, Y, ws
-    # a5: prefill GEMM on the tensor cores
-    for name, K, N in (("gate", 2048, 6144), ("lm_head", 2048, 151936)):
-        M = 2048
-        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)
-        S = (torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev)
-        A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        us, p10, p90 = event_time_us(torch, stream, lambda: mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y, stream=stream),
-                                     reps=10 if N > 100000 else 30)
-        tf = 2 * M * N * K / (us * 1e-6) / 1e12
-        rows[f"prefill_gemm_{name}_m2048"] = {
-            "kernel": "gemm_tc (tcgen05, TMEM accumulators)", "shape": f"M={M} K={K} N={N} INT4 bs32 bf16 A/Y",
-            "us": us, "us_p10_p90": [p10, p90], "achieved": tf, "unit": "TFLOP/s", "peak": tc,
-            "frac": tf / tc, "bound": "tensor", "peak_source": f"{tc_kind} bf16_tflops"}
-        del B, S, A, Y
+    us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=reps)
+    n = len(calls)
+    return us / n, p10 / n, p90 / n
+
+
+def matmul_bytes(M, K, N, bits, bs, sbytes, abytes, ybytes, zp=False):
+    nb = (K + bs - 1) // bs
+    return N * nb * bs * bits // 8 + N * nb * sbytes + (N * ((nb * bits + 7) // 8) if zp else 0) + M * K * abytes + \
+        M * N * ybytes
+
+
+def other_rows(torch, mnb, dev):
+    """The rest of the hot path, each against its own roofline:
+      * the decode GEMV chain per projection shape (140 dependent launches,
+        distinct weights), and the INT3 decode GEMV (vocabulary head and gate);
+      * the small-M / prefill GEMM on the same INT4 weights, bf16 activations,
+        M in {4, 16, 128, 512, 2048} (HBM-bound below M ~ 100, tensor-bound above);
+      * one Qwen3-30B-A3B-shaped QMoE layer: decode T=1 and prefill T in
+        {128, 512} (all experts touched: HBM) and {2048, 4096} (tensor cores),
+        INT3/INT3 bs64 fp16, plus one bf16 layer with zero points (4,4) bs32;
+      * the INT3 quantizer over one layer's FC1 expert weights."""
+    gen = torch.Generator().manual_seed(7)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, hbm_kind = peaks()
+    tc, tc_kind = tc_peak()
+    hsrc, tsrc = f"{hbm_kind} hbm_gbs", f"{tc_kind} bf16_tflops"
+    rows = {}
+
+    def rnd_w(N, K, bits, copies):
+        return [torch.randint(0, 256, (N, (K * bits) // 8), dtype=torch.uint8, generator=gen).to(dev)
+                for _ in range(copies)]
+
+    def rnd_s(N, K, bs, copies, dt=torch.float32):
+        return [(torch.rand((N, K // bs), generator=gen) * 0.015 + 0.005).to(dt).to(dev) for _ in range(copies)]
+
+    # a4: the decode chain per projection shape (140 launches over 64 weight copies)
+    for name, K, N in (wl.QWEN3_1P7B_PROJECTIONS[0], wl.QWEN3_1P7B_PROJECTIONS[1], wl.QWEN3_1P7B_PROJECTIONS[2],
+                       wl.QWEN3_1P7B_PROJECTIONS[4]):
+        copies = 64
+        Bs, Ss = rnd_w(N, K, 4, copies), rnd_s(N, K, BS, copies)
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        calls = [lambda i=i: mnb.mnb_matmul(A, Bs[i % copies], Ss[i % copies], None, N, 4, BS, Y, stream=stream)
+                 for i in range(140)]
+        us, p10, p90 = graph_time(torch, stream, calls, reps=20)
+        nbytes = proj_bytes(K, N)
+        rows[f"decode_chain_{name}"] = _row(
+            "gemv_kernel (chain of 140 dependent launches)", f"M=1 K={K} N={N} INT4 bs32 fp32, 64 weight copies",
+            us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc)
+        del Bs, Ss
+    # a2/a4: INT3 decode GEMV (fp32 activations and scales, implicit zero point 4)
+    for name, K, N, bs, copies in (("lm_head", 2048, 151936, 32, 2), ("lm_head", 2048, 151936, 64, 2),
+                                   ("gate", 2048, 6144, 64, 32)):
+        Bs, Ss = rnd_w(N, K, 3, copies), rnd_s(N, K, bs, copies)
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        calls = [lambda i=i: mnb.mnb_matmul(A, Bs[i % copies], Ss[i % copies], None, N, 3, bs, Y, stream=stream)
+                 for i in range(16 if N > 100000 else 64)]
+        us, p10, p90 = graph_time(torch, stream, calls, reps=10 if N > 100000 else 20)
+        nbytes = matmul_bytes(1, K, N, 3, bs, 4, 4, 4)
+        rows[f"decode_int3_{name}_bs{bs}"] = _row(
+            "gemv_kernel<INT3>", f"M=1 K={K} N={N} INT3 bs{bs} fp32, {copies} weight copies", us, p10, p90,
+            nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc)
+        del Bs, Ss
+    torch.cuda.empty_cache()
+    # a5: small-M and prefill GEMM (INT4 bs32, fp32 scales, bf16 activations and outputs)
+    for name, K, N in (("qkv", 2048, 4096), ("gate", 2048, 6144), ("lm_head", 2048, 151936)):
+        for M in (4, 16, 128, 512, 2048):
+            if name == "lm_head" and M not in (16, 2048):
+                continue
+            copies = max(1, min(16, (512 << 20) // (N * K // 2 + N * K // BS * 4)))
+            Bs, Ss = rnd_w(N, K, 4, copies), rnd_s(N, K, BS, copies)
+            A = torch.randn((M, K), generator=gen).bfloat16().to(dev)
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(1, mnb.mnb_matmul_workspace_size(M, K, N, 4, BS, mnb.BF16)), dtype=torch.uint8,
+                             device=dev)
+            calls = [lambda i=i: mnb.mnb_matmul(A, Bs[i % copies], Ss[i % copies], None, N, 4, BS, Y, ws,
+                                                stream=stream) for i in range(copies if copies > 1 else 4)]
+            us, p10, p90 = graph_time(torch, stream, calls, reps=10 if N > 100000 else 20)
+            flops = 2 * M * N * K
+            nbytes = matmul_bytes(M, K, N, 4, BS, 4, 2, 2)
+            path = "gemv_kernel (CUDA cores)" if M < 16 else "gemm_tc (tcgen05" + (
+                ", K split across CTAs)" if mnb.mnb_matmul_workspace_size(M, K, N, 4, BS, mnb.BF16) else ")")
+            shape = f"M={M} K={K} N={N} INT4 bs32 bf16 A/Y, fp32 scales, {copies} weight copies"
+            if M <= 16:
+                rows[f"gemm_{name}_m{M}"] = _row(path, shape, us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s", hbm,
+                                                 "hbm", hsrc, tflops=flops / (us * 1e-6) / 1e12)
+            else:
+                rows[f"gemm_{name}_m{M}"] = _row(path, shape, us, p10, p90, flops / (us * 1e-6) / 1e12, "TFLOP/s",
+                                                 tc, "tensor", tsrc, gbs=nbytes / (us * 1e-6) / 1e9)
+            del Bs, Ss, A, Y, ws
+    torch.cuda.empty_cache()
     # a6-a10: the QMoE layer
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
-    b1 = b2 = 3
-    bs = 64
-    nl = 16
-    layers = make_moe_layers(torch, dev, nl, b1, b2, bs, gen)
-    for T in (1, 4096):
-        X = torch.randn((T, H), generator=gen).half().to(dev)
-        logits = torch.randn((T, E), generator=gen).to(dev)
-        Y = torch.empty((T, H), dtype=torch.float16, device=dev)
-        ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, mnb.F16), dtype=torch.uint8, device=dev)
+    for b1, b2, bs, act, zp, Ts in ((3, 3, 64, torch.float16, False, (1, 128, 512, 2048, 4096)),
+                                    (4, 4, 32, torch.bfloat16, True, (4096,))):
+        code = mnb.F16 if act == torch.float16 else mnb.BF16
+        nl = 16
+        layers = make_moe_layers(torch, dev, nl, b1, b2, bs, gen, act=act, zp=zp)
+        per_expert = moe_expert_bytes(b1, b2, bs, zp=zp)
+        for T in Ts:
+            X = torch.randn((T, H), generator=gen).to(act).to(dev)
+            logits = torch.randn((T, E), generator=gen)
+            logits[::10, :8] += 3.0  # the skewed tenth of the tokens
+            logits = logits.to(dev)
+            Y = torch.empty((T, H), dtype=act, device=dev)
+            ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, code), dtype=torch.uint8, device=dev)
+            touched = int(torch.unique(torch.topk(logits, k, dim=1).indices).numel())
 
-        def call(i):
-            w1, s1, w2, s2 = layers[i % nl]
-            mnb.qmoe_forward(X, logits, k, True, w1, s1, None, b1, w2, s2, None, b2, I, bs, Y, ws, stream=stream)
-        if T == 1:
-            with torch.cuda.stream(stream):
-                call(0)
-            torch.cuda.synchronize()
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                gr.capture_begin()
-                for i in range(nl):
-                    call(i)
-                gr.capture_end()
-            us, p10, p90 = event_time_us(torch, stream, gr.replay, reps=50)
-            us, p10, p90 = us / nl, p10 / nl, p90 / nl
-            touched = min(E, T * k) * moe_expert_bytes(b1, b2, bs)
-            gbs = touched / (us * 1e-6) / 1e9
-            rows["qmoe_decode_t1"] = {
-                "kernel": "fc1_kernel (decode) + fc2_decode_kernel", "shape": "Qwen3-30B-A3B layer, T=1, top-8 of 128, "
-                "INT3/INT3 bs64 fp16, 16 distinct layers replayed in one graph", "us": us, "us_p10_p90": [p10, p90],
-                "achieved": gbs, "unit": "GB/s", "peak": hbm, "frac": gbs / hbm, "bound": "hbm",
-                "bytes_per_layer": touched, "peak_source": f"{hbm_kind} hbm_gbs"}
-        else:
-            it = [0]
-
-            def once():
-                call(it[0])
-                it[0] += 1
-            us, p10, p90 = event_time_us(torch, stream, once, reps=10)
-            tf = T * k * (2 * H * 2 * I + 2 * I * H) / (us * 1e-6) / 1e12
-            rows["qmoe_prefill_t4096"] = {
-                "kernel": "route + permute + grouped gemm_tc FC1 (SwiGLU epilogue) + grouped gemm_tc FC2 + combine",
-                "shape": "Qwen3-30B-A3B layer, T=4096, top-8 of 128, INT3/INT3 bs64 fp16", "us": us,
-                "us_p10_p90": [p10, p90], "achieved": tf, "unit": "TFLOP/s", "peak": tc, "frac": tf / tc,
-                "bound": "tensor", "peak_source": f"{tc_kind} bf16_tflops"}
-        del X, logits, Y, ws
-    del layers
-    torch.cuda.empty_cache()
+            def call(i):
+                w1, s1, z1, w2, s2, z2 = layers[i % nl]
+                mnb.qmoe_forward(X, logits, k, True, w1, s1, z1, b1, w2, s2, z2, b2, I, bs, Y, ws, stream=stream)
+            calls = [lambda i=i: call(i) for i in range(nl if T <= 512 else 4)]
+            us, p10, p90 = graph_time(torch, stream, calls, reps=30 if T <= 512 else 5)
+            flops = T * k * (2 * H * 2 * I + 2 * I * H)
+            nbytes = touched * per_expert + T * H * 2 * 2 + T * E * 4
+            tag = f"qmoe_{'decode' if T == 1 else 'prefill'}_t{T}" + ("" if act == torch.float16 else "_bf16_zp44")
+            shape = (f"Qwen3-30B-A3B layer, T={T}, top-{k} of {E} ({touched} experts touched), INT{b1}/INT{b2} "
+                     f"bs{bs} {'fp16' if act == torch.float16 else 'bf16'}{' + zero points' if zp else ''}, "
+                     f"{nl} distinct layers")
+            kern = ("fc1_kernel (decode) + fc2_decode_kernel" if T <= 8 else
+                    "route + permute + grouped gemm_tc FC1 (SwiGLU epilogue) + grouped gemm_tc FC2 + combine")
+            if T <= 512:
+                rows[tag] = _row(kern, shape, us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc,
+                                 bytes_per_layer=nbytes, tflops=flops / (us * 1e-6) / 1e12)
+            else:
+                rows[tag] = _row(kern, shape, us, p10, p90, flops / (us * 1e-6) / 1e12, "TFLOP/s", tc, "tensor", tsrc,
+                                 gbs=nbytes / (us * 1e-6) / 1e9)
+            del X, logits, Y, ws
+        del layers
+        torch.cuda.empty_cache()
     # the INT3 producer: every expert's FC1 weights of one layer (128 x 1536 x 2048 fp16,
     # 805 MB, larger than L2) quantised to packed INT3 codes and fp16 scales, bs 64
-    E, H, I = MOE["E"], MOE["H"], MOE["I"]
     N = E * 2 * I
     gq = torch.Generator(device=dev).manual_seed(17)
     Wq = (torch.randn((N, H), generator=gq, device=dev, dtype=torch.float16) * 0.02)
@@ -392,11 +449,10 @@ def other_rows(torch, mnb, dev):
     us, p10, p90 = event_time_us(torch, stream,
                                  lambda: mnb.mnb_quantize_int3(Wq, 64, mnb.F16, Bq, Sq, stream=stream), reps=10)
     qbytes = N * H * 2 + Bq.numel() + Sq.numel() * 2
-    rows["quantize_int3_fc1_layer"] = {
-        "kernel": "quantize_int3_kernel (symmetric grouped INT3 round-to-nearest)",
-        "shape": f"{E} experts x {2 * I} rows x K={H}, fp16 weights -> INT3 bs64 + fp16 scales", "us": us,
-        "us_p10_p90": [p10, p90], "achieved": qbytes / (us * 1e-6) / 1e9, "unit": "GB/s", "peak": hbm,
-        "frac": qbytes / (us * 1e-6) / 1e9 / hbm, "bound": "hbm", "peak_source": f"{hbm_kind} hbm_gbs"}
+    rows["quantize_int3_fc1_layer"] = _row(
+        "quantize_int3_kernel (symmetric grouped INT3 round-to-nearest)",
+        f"{E} experts x {2 * I} rows x K={H}, fp16 weights -> INT3 bs64 + fp16 scales", us, p10, p90,
+        qbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc)
     del Wq, Bq, Sq
     torch.cuda.empty_cache()
     if mnb.mnb_get_last_device_error(stream) != 0:
@@ -489,8 +545,8 @@ def profile_case(name):
         Y = torch.empty((T, H), dtype=torch.float16, device=dev)
         ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, mnb.F16), dtype=torch.uint8, device=dev)
         for i in range(24 if T == 1 else 3):
-            w1, s1, w2, s2 = layers[i % nl]
-            mnb.qmoe_forward(X, logits, k, True, w1, s1, None, 3, w2, s2, None, 3, I, 64, Y, ws)
+            w1, s1, z1, w2, s2, z2 = layers[i % nl]
+            mnb.qmoe_forward(X, logits, k, True, w1, s1, z1, 3, w2, s2, z2, 3, I, 64, Y, ws)
     torch.cuda.synchronize()
     if mnb.mnb_get_last_device_error() != 0:
         raise RuntimeError("device error word set")
