@@ -158,7 +158,7 @@ def ncu_traffic(kernel_sha: str):
 def kernel_source_sha():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemv.cu", "gemv_core.cuh", "common.cuh"):
+    for f in ("gemv.cu", "gemv_core.cuh", "gemv_int.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "qmoe_mnb_matmul_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
