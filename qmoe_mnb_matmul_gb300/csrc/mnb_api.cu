@@ -97,7 +97,7 @@ mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
     unsigned int first = 0;
     cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error,
-                                              quant_take_error, diag_take_error};
+                                              quant_take_error, diag_take_error, qmoe_decode_take_error};
     for (auto take : takers) {
         unsigned int v = 0;
         if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;

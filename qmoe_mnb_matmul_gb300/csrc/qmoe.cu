@@ -51,7 +51,7 @@ constexpr int kDecodeRows2 = 8;     // FC2 rows per CTA (decode plan)
 __host__ __device__ inline int64_t a256(int64_t x) { return (x + 255) / 256 * 256; }
 
 struct Ws {
-    int64_t idx, wts, counts, offsets, perm, inv, chunkc, tiles, ntiles, mtiles, nmtiles, h, o, total;
+    int64_t idx, wts, counts, offsets, perm, inv, chunkc, tiles, ntiles, mtiles, nmtiles, h, o, sync, total;
 };
 
 __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
@@ -83,6 +83,7 @@ __host__ __device__ inline Ws ws_layout(int64_t T, int64_t H, int64_t I, int64_t
     w.nmtiles = off; off += 256;
     w.h = off; off += a256(P * I * 4);
     w.o = off; off += a256(P * H * 4);
+    w.sync = off; off += 256;  // the fused decode kernel's grid barrier counter
     w.total = off;
     return w;
 }
@@ -676,6 +677,11 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     const unsigned gy2 = static_cast<unsigned>(cdiv<int64_t>(q.H, kRowsPerBlock2));
     cudaError_t e;
     if (use_decode(q)) {
+        // one token: the fused single-pass kernel (qmoe_decode.cu) where its shape rules allow
+        if (q.T == 1) {
+            e = launch_qmoe_decode_fused(q, sm_count, pdl, stream);
+            if (e != cudaErrorNotSupported) return e;
+        }
         e = launch_fc1<B1, ST, 1, true>(q, static_cast<unsigned>(P), stream, pdl);
         if (e != cudaSuccess) return e;
         const Fc2Plan p2 = fc2_plan(kDecodeRows2, kDecodeMaxK, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2, true);
@@ -786,6 +792,12 @@ bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
 }
 
 cudaError_t qmoe_take_error(unsigned int* out) { return take_unit_error(out); }
+
+void qmoe_ws_decode_regions(int64_t T, int64_t H, int64_t I, int64_t E, int k, int64_t* h_off, int64_t* sync_off) {
+    const Ws L = ws_layout(T, H, I, E, k);
+    *h_off = L.h;
+    *sync_off = L.sync;
+}
 
 cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream) {
     return q.act_dtype == MNB_F16 ? run_bits<kF16>(q, sm_count, pdl, stream) : run_bits<kBF16>(q, sm_count, pdl, stream);

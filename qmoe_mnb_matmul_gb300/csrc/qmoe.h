@@ -39,4 +39,14 @@ bool qmoe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
 
 cudaError_t launch_qmoe(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream);
 
+// Workspace offsets of the SwiGLU activations h [T*k, I] (fp32) and of the
+// 256-byte region the fused decode kernel uses for its grid barrier counter.
+void qmoe_ws_decode_regions(int64_t T, int64_t H, int64_t I, int64_t E, int k, int64_t* h_off, int64_t* sync_off);
+
+// One token (T = 1), k <= 8: the fused decode layer (qmoe_decode.cu).
+// cudaErrorNotSupported when the shape is outside its rules (the caller then
+// runs the two-kernel decode plan).
+cudaError_t launch_qmoe_decode_fused(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t stream);
+cudaError_t qmoe_decode_take_error(unsigned int* out);
+
 }  // namespace mnb

@@ -94,6 +94,20 @@ def test_decode_layouts_and_blocks(bs, layout, normalize):
     check(y, reference(d, k, 3, 4, I, bs, "f16", layout, normalize), "f16", T)
 
 
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+@pytest.mark.parametrize("bs,bits,E,k", [(32, (3, 4), 64, 8), (64, (4, 3), 300, 6), (128, (4, 4), 16, 2),
+                                        (64, (3, 3), 128, 8)])
+def test_one_token_single_pass(layout, bs, bits, E, k):
+    """T = 1 runs the single-pass layer kernel (every CTA's FC1 and FC2 rows copied
+    before the dependency wait, a grid barrier between FC1 and FC2): both FC1 layouts,
+    explicit zero points, routers wider than one CTA's ranking (E = 300)."""
+    b1, b2 = bits
+    H, I = 1024, 256 if bs != 128 else 512
+    d = wl.moe_layer(wl.rng(seed("one", layout, bs, bits, E, k)), 1, H, I, E, b1, b2, bs, "bf16", with_zp=True)
+    y = run_qmoe(d, 1, H, I, E, k, b1, b2, bs, "bf16", layout)
+    check(y, reference(d, k, b1, b2, I, bs, "bf16", layout), "bf16", 1)
+
+
 @pytest.mark.parametrize("T,E,k,skew", [(9, 64, 8, True), (64, 128, 8, True), (33, 16, 2, False), (40, 8, 8, False),
                                         (12, 1, 1, False), (20, 256, 10, True)])
 @pytest.mark.parametrize("bits", [(3, 3), (4, 3)])
