@@ -319,7 +319,7 @@ def matmul_bytes(M, K, N, bits, bs, sbytes, abytes, ybytes, zp=False):
         M * N * ybytes
 
 
-def other_rows(torch, mnb, dev):
+def other_rows(torch, mnb, dev, groups=()):
     """The rest of the hot path, each against its own roofline:
       * the decode GEMV chain per projection shape (140 dependent launches,
         distinct weights), and the INT3 decode GEMV (vocabulary head and gate);
@@ -343,8 +343,9 @@ def other_rows(torch, mnb, dev):
     def rnd_s(N, K, bs, copies, dt=torch.float32):
         return [(torch.rand((N, K // bs), generator=gen) * 0.015 + 0.005).to(dt).to(dev) for _ in range(copies)]
 
+    want = lambda g: not groups or g in groups
     # a4: the decode chain per projection shape (140 launches over 64 weight copies)
-    for name, K, N in (wl.QWEN3_1P7B_PROJECTIONS[0], wl.QWEN3_1P7B_PROJECTIONS[1], wl.QWEN3_1P7B_PROJECTIONS[2],
+    for name, K, N in () if not want("decode") else (wl.QWEN3_1P7B_PROJECTIONS[0], wl.QWEN3_1P7B_PROJECTIONS[1], wl.QWEN3_1P7B_PROJECTIONS[2],
                        wl.QWEN3_1P7B_PROJECTIONS[4]):
         copies = 64
         Bs, Ss = rnd_w(N, K, 4, copies), rnd_s(N, K, BS, copies)
@@ -359,8 +360,8 @@ def other_rows(torch, mnb, dev):
             us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc)
         del Bs, Ss
     # a2/a4: INT3 decode GEMV (fp32 activations and scales, implicit zero point 4)
-    for name, K, N, bs, copies in (("lm_head", 2048, 151936, 32, 2), ("lm_head", 2048, 151936, 64, 2),
-                                   ("gate", 2048, 6144, 64, 32)):
+    for name, K, N, bs, copies in () if not want("int3") else (("lm_head", 2048, 151936, 32, 2),
+                                                               ("lm_head", 2048, 151936, 64, 2), ("gate", 2048, 6144, 64, 32)):
         Bs, Ss = rnd_w(N, K, 3, copies), rnd_s(N, K, bs, copies)
         A = torch.randn((1, K), generator=gen).to(dev)
         Y = torch.empty((1, N), device=dev)
@@ -374,7 +375,7 @@ def other_rows(torch, mnb, dev):
         del Bs, Ss
     torch.cuda.empty_cache()
     # a5: small-M and prefill GEMM (INT4 bs32, fp32 scales, bf16 activations and outputs)
-    for name, K, N in (("qkv", 2048, 4096), ("gate", 2048, 6144), ("lm_head", 2048, 151936)):
+    for name, K, N in () if not want("gemm") else (("qkv", 2048, 4096), ("gate", 2048, 6144), ("lm_head", 2048, 151936)):
         for M in (4, 16, 128, 512, 2048):
             if name == "lm_head" and M not in (16, 2048):
                 continue
@@ -402,8 +403,8 @@ def other_rows(torch, mnb, dev):
     torch.cuda.empty_cache()
     # a6-a10: the QMoE layer
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
-    for b1, b2, bs, act, zp, Ts in ((3, 3, 64, torch.float16, False, (1, 128, 512, 2048, 4096)),
-                                    (4, 4, 32, torch.bfloat16, True, (4096,))):
+    for b1, b2, bs, act, zp, Ts in () if not want("qmoe") else ((3, 3, 64, torch.float16, False, (1, 128, 512, 2048, 4096)),
+                                                                (4, 4, 32, torch.bfloat16, True, (4096,))):
         code = mnb.F16 if act == torch.float16 else mnb.BF16
         nl = 16
         layers = make_moe_layers(torch, dev, nl, b1, b2, bs, gen, act=act, zp=zp)
@@ -441,6 +442,8 @@ def other_rows(torch, mnb, dev):
         torch.cuda.empty_cache()
     # the INT3 producer: every expert's FC1 weights of one layer (128 x 1536 x 2048 fp16,
     # 805 MB, larger than L2) quantised to packed INT3 codes and fp16 scales, bs 64
+    if not want("quant"):
+        return rows
     N = E * 2 * I
     gq = torch.Generator(device=dev).manual_seed(17)
     Wq = (torch.randn((N, H), generator=gq, device=dev, dtype=torch.float16) * 0.02)
@@ -563,6 +566,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true", help="skip the prefill GEMM and QMoE measurements")
+    ap.add_argument("--rows", default="", help="comma-separated groups of other rows to run (decode, int3, gemm, "
+                    "qmoe, quant); default all")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run one small fixed invocation for an ncu capture and exit")
     args = ap.parse_args()
@@ -724,7 +729,7 @@ def main():
                 "ms_per_step": ms_e2e / e2e_steps},
     }
     if not args.no_other_rows:
-        out["other_rows"] = other_rows(torch, mnb, dev)
+        out["other_rows"] = other_rows(torch, mnb, dev, tuple(g for g in args.rows.split(",") if g))
     if ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample()
     print(json.dumps(out))

@@ -66,11 +66,21 @@ __host__ __device__ inline DecPlan dec_plan(int C1, int C2, int k, int64_t rb1, 
     return p;
 }
 
-// Items [first, last) of CTA x among g CTAs: contiguous, sizes differing by at most one.
-__host__ __device__ inline void split(int64_t n, int x, int g, int64_t& first, int64_t& last) {
-    const int64_t q = n / g, r = n - q * g;
-    first = x * q + (x < r ? x : r);
-    last = first + q + (x < r ? 1 : 0);
+// Items [first, last) of CTA x among g CTAs, in units of u items: contiguous,
+// unit counts differing by at most one.
+__host__ __device__ inline void split(int64_t n, int64_t u, int x, int g, int64_t& first, int64_t& last) {
+    const int64_t units = n / u, q = units / g, r = units - q * g;
+    first = (x * q + (x < r ? x : r)) * u;
+    last = first + (q + (x < r ? 1 : 0)) * u;
+}
+
+// The smallest count of rows (FC2) or gate/up pairs (FC1, two rows each)
+// whose packed bytes and 16-bit scales are whole 16-byte units, so that every
+// CTA's bulk copies start and end on 16-byte boundaries.
+__host__ __device__ inline int64_t copy_unit(int64_t row_bytes, int64_t scale_bytes, int rows_per_item) {
+    int64_t u = 1;
+    while ((u * rows_per_item * row_bytes) % 16 || (u * rows_per_item * scale_bytes) % 16) u *= 2;
+    return u;
 }
 
 __global__ void qmoe_decode_prep_kernel(unsigned int* counter) {
@@ -128,8 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
 
     // this CTA's FC1 pairs (flat over the k slots) and FC2 output rows
     int64_t pr0, pr1, n0, n1;
-    split(int64_t(k) * I, blockIdx.x, gridDim.x, pr0, pr1);
-    split(H, blockIdx.x, gridDim.x, n0, n1);
+    const int64_t ss_ = sizeof(S);
+    split(int64_t(k) * I, copy_unit(rb1, nb1 * ss_, inter ? 2 : 1), blockIdx.x, gridDim.x, pr0, pr1);
+    split(H, copy_unit(rb2, nb2 * ss_, 1), blockIdx.x, gridDim.x, n0, n1);
     const int np = static_cast<int>(pr1 - pr0), nr = static_cast<int>(n1 - n0);
 
     // ------------------------------------------------------ prologue
@@ -400,13 +411,21 @@ cudaError_t launch_qmoe_decode_fused(const QmoeArgs& q, int sm_count, bool pdl, 
     const int ssize = 2;
     const int nb1 = static_cast<int>(q.fc1.nb), nb2 = static_cast<int>(q.fc2.nb);
     const int64_t rb1 = q.fc1.row_bytes, rb2 = q.fc2.row_bytes;
-    // every bulk copy must be a whole number of 16-byte units at 16-byte offsets
-    if (rb1 % 16 || rb2 % 16 || (int64_t(nb1) * ssize) % 16 || (int64_t(nb2) * ssize) % 16) return cudaErrorNotSupported;
+    // every bulk copy must be a whole number of 16-byte units at 16-byte
+    // offsets: CTAs take pairs and rows in copy units, which must tile an
+    // expert (I pairs) and the output (H rows)
+    const bool inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
+    const int64_t u1 = copy_unit(rb1, int64_t(nb1) * ssize, inter ? 2 : 1), u2 = copy_unit(rb2, int64_t(nb2) * ssize, 1);
+    if (u1 > 8 || u2 > 8 || q.I % u1 || q.H % u2) return cudaErrorNotSupported;
+    // bases of the expert matrices (16-byte aligned pointers, whole-unit expert strides)
+    if ((2 * q.I * rb1) % 16 || (2 * q.I * nb1 * ssize) % 16 || (q.H * rb2) % 16 || (q.H * nb2 * ssize) % 16)
+        return cudaErrorNotSupported;
     const int64_t pairs = int64_t(q.k) * q.I;
-    int grid = static_cast<int>(std::min<int64_t>(sm_count, std::min<int64_t>(pairs, q.H)));
+    int grid = static_cast<int>(std::min<int64_t>(sm_count, std::min<int64_t>(pairs / u1, q.H / u2)));
     if (grid < 1) return cudaErrorNotSupported;
-    if (cdiv<int64_t>(pairs, grid) > kMaxPairs || cdiv<int64_t>(q.H, grid) > kMaxRows2) return cudaErrorNotSupported;
-    if (cdiv<int64_t>(pairs, grid) > q.I) return cudaErrorNotSupported;  // a CTA's pairs span at most two slots
+    if (cdiv<int64_t>(pairs / u1, grid) * u1 > kMaxPairs || cdiv<int64_t>(q.H / u2, grid) * u2 > kMaxRows2)
+        return cudaErrorNotSupported;
+    if (cdiv<int64_t>(pairs / u1, grid) * u1 > q.I) return cudaErrorNotSupported;  // a CTA's pairs span <= 2 slots
     const int C1 = static_cast<int>(q.fc1.nb * q.bs / 32), C2 = static_cast<int>(q.fc2.nb * q.bs / 32);
     const DecPlan p = dec_plan(C1, C2, q.k, rb1, nb1, rb2, nb2, ssize);
     if (p.total > kSmemCap) return cudaErrorNotSupported;
