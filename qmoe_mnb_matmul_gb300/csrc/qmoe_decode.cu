@@ -36,7 +36,7 @@ namespace {
 
 using namespace gemv_int;
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;  // alone on its SM: 16 warps to hide the instruction latencies
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxK = 8;
 constexpr int kMaxPairs = 48;      // FC1 gate/up pairs per CTA
@@ -299,13 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
         Hq, Hc, k, C2, I, kF32, true, [&](int j) -> const void* { return h + int64_t(j) * I; }, tid, kThreads);
     __syncthreads();
     ok = warp_wait(bar2, 0);
-    if (ok && warp < k) {
+    // tasks: (slot j, rows r0 .. r0+3 of the CTA's output rows), spread over the warps
+    const int groups2 = (nr + 3) / 4;
+    for (int task = warp; ok && task < k * groups2; task += kWarps) {
         constexpr int Z2 = 1 << (B2 - 1);
-        const int j = warp;
+        const int j = task / groups2, r0 = (task - j * groups2) * 4;
         const int64_t e = s_idx[j];
         const uint8_t* Wj = W2 + int64_t(j) * kMaxRows2 * rb2;
         const S* Sj = reinterpret_cast<const S*>(S2 + int64_t(j) * kMaxRows2 * nb2 * sizeof(S));
-        for (int r0 = 0; r0 < nr; r0 += 4) {
+        {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             const uint8_t* wr[4];
             const S* sr[4];
