@@ -151,47 +151,57 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
         fence_barrier_init();
     }
     if (q.E <= kBlockRouteMaxE && q.E <= kThreads) {
-        block_route(q.logits, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, s_logit);
+        block_route_fast(q.logits, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, s_logit);
     } else {
         if (tid < 32) warp_route(q.logits, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, 1);
         __syncthreads();
     }
     // local FC1 pair lp: gate row at lrow(lp, 0), up row at lrow(lp, 1) of the staged rows
     auto lrow = [&](int lp, int up) { return inter ? 2 * lp + up : up * kMaxPairs + lp; };
-    if (tid == 0) {
-        const uint32_t ss = sizeof(S);
-        const uint32_t tx = static_cast<uint32_t>(2 * int64_t(np) * (rb1 + int64_t(nb1) * ss));
-        mbar_arrive_expect_tx(bar1, tx);
-        for (int64_t p = pr0; p < pr1;) {
-            const int j = static_cast<int>(p / I);
-            const int64_t pe = min(pr1, int64_t(j + 1) * I);
-            const int64_t a0 = p - int64_t(j) * I, cnt = pe - p;
-            const int lp = static_cast<int>(p - pr0);
-            const int64_t e = s_idx[j];
-            const uint8_t* wexp = q.fc1_w + e * 2 * I * rb1;
-            const uint8_t* sexp = static_cast<const uint8_t*>(q.fc1_s) + e * 2 * I * nb1 * ss;
-            if (inter) {
-                bulk_g2s(W1 + lrow(lp, 0) * rb1, wexp + 2 * a0 * rb1, static_cast<uint32_t>(2 * cnt * rb1), bar1);
-                bulk_g2s(S1 + lrow(lp, 0) * nb1 * ss, sexp + 2 * a0 * nb1 * ss, static_cast<uint32_t>(2 * cnt * nb1 * ss),
-                         bar1);
-            } else {
-                for (int up = 0; up < 2; ++up) {
-                    bulk_g2s(W1 + lrow(lp, up) * rb1, wexp + (up * I + a0) * rb1, static_cast<uint32_t>(cnt * rb1),
-                             bar1);
-                    bulk_g2s(S1 + lrow(lp, up) * nb1 * ss, sexp + (up * I + a0) * nb1 * ss,
-                             static_cast<uint32_t>(cnt * nb1 * ss), bar1);
+    // The copies, issued by the lanes of warp 0 at once (lane 0 arms both
+    // barriers first): FC1 pairs [pr0, pr1) fall into at most two slots (two
+    // segments, lanes 0-3 and 4-7: packed rows and scales, of the gate and
+    // up halves when those are separate); FC2 rows [n0, n1) of slot j on
+    // lanes 8 + 2j (packed rows) and 9 + 2j (scales).
+    if (warp == 0) {
+        const int64_t ss = sizeof(S);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar1, static_cast<uint32_t>(2 * int64_t(np) * (rb1 + nb1 * ss)));
+            mbar_arrive_expect_tx(bar2, static_cast<uint32_t>(int64_t(k) * nr * (rb2 + nb2 * ss)));
+        }
+        __syncwarp();
+        if (lane < 8) {
+            const int seg = lane >> 2, sub = lane & 3;
+            const int j0 = static_cast<int>(pr0 / I);
+            const int64_t split_at = min(pr1, int64_t(j0 + 1) * I);
+            const int64_t p = seg == 0 ? pr0 : split_at, pe = seg == 0 ? split_at : pr1;
+            const bool scales = sub & 1;
+            const int up = sub >> 1;
+            if (p < pe && (!inter || up == 0)) {
+                const int j = j0 + seg;
+                const int64_t a0 = p - int64_t(j) * I, cnt = pe - p;
+                const int lp = static_cast<int>(p - pr0);
+                const int64_t e = s_idx[j];
+                // rows: interleaved 2 a0 .. (gate and up together), else up * I + a0 ..
+                const int64_t r0 = inter ? 2 * a0 : up * I + a0, nrows = inter ? 2 * cnt : cnt;
+                if (scales) {
+                    const uint8_t* src = static_cast<const uint8_t*>(q.fc1_s) + (e * 2 * I + r0) * nb1 * ss;
+                    bulk_g2s(S1 + lrow(lp, up) * nb1 * ss, src, static_cast<uint32_t>(nrows * nb1 * ss), bar1);
+                } else {
+                    bulk_g2s(W1 + lrow(lp, up) * rb1, q.fc1_w + (e * 2 * I + r0) * rb1,
+                             static_cast<uint32_t>(nrows * rb1), bar1);
                 }
             }
-            p = pe;
-        }
-        // FC2: rows [n0, n1) of every selected expert
-        const uint32_t wb = static_cast<uint32_t>(nr * rb2), sb = static_cast<uint32_t>(nr * nb2 * ss);
-        mbar_arrive_expect_tx(bar2, static_cast<uint32_t>(k) * (wb + sb));
-        for (int j = 0; j < k; ++j) {
+        } else if (lane < 8 + 2 * k) {
+            const int j = (lane - 8) >> 1;
             const int64_t e = s_idx[j];
-            bulk_g2s(W2 + int64_t(j) * kMaxRows2 * rb2, q.fc2_w + (e * H + n0) * rb2, wb, bar2);
-            bulk_g2s(S2 + int64_t(j) * kMaxRows2 * nb2 * ss,
-                     static_cast<const uint8_t*>(q.fc2_s) + (e * H + n0) * nb2 * ss, sb, bar2);
+            if (lane & 1)
+                bulk_g2s(S2 + int64_t(j) * kMaxRows2 * nb2 * ss,
+                         static_cast<const uint8_t*>(q.fc2_s) + (e * H + n0) * nb2 * ss,
+                         static_cast<uint32_t>(nr * nb2 * ss), bar2);
+            else
+                bulk_g2s(W2 + int64_t(j) * kMaxRows2 * rb2, q.fc2_w + (e * H + n0) * rb2, static_cast<uint32_t>(nr * rb2),
+                         bar2);
         }
     }
     grid_dependency_wait();

@@ -166,4 +166,54 @@ __device__ __forceinline__ void block_route(const float* __restrict__ row, int E
     __syncthreads();
 }
 
+// block_route with the ranking split over `tpl` adjacent lanes per logit
+// (tpl = the largest power of two <= min(8, blockDim.x / E)) and the k
+// selected probabilities formed by k lanes at once; the k selected
+// probabilities are summed by a fixed shuffle tree.  Same selection (ties to
+// the lower index, NaN as -inf) and the same weights up to the order of that
+// sum.  Needs blockDim.x >= E, a multiple of 32; all threads must call it; it
+// ends with a block barrier.  s_logit is shared scratch of E floats.
+template <typename WT>
+__device__ __forceinline__ void block_route_fast(const float* __restrict__ row, int E, int k, int normalize, int* idx,
+                                                 WT* w, float* s_logit) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    int tpl = 1;
+    while (tpl < 8 && E * tpl * 2 <= int(blockDim.x)) tpl *= 2;
+    if (tid < E) {
+        const float x = row[tid];
+        s_logit[tid] = x != x ? -INFINITY : x;
+    }
+    __syncthreads();
+    const int e = tid / tpl, part = tid - e * tpl;
+    if (e < E) {
+        const float v = s_logit[e];
+        int r = 0;
+        for (int j = part; j < E; j += tpl) {  // lower indices beat v on ties, higher ones only when greater
+            const float u = s_logit[j];
+            r += j < e ? (u >= v) : (u > v);
+        }
+        for (int o = 1; o < tpl; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+        if (part == 0 && r < k) idx[r] = e;
+    } else if (tpl > 1) {
+        int r = 0;  // lanes past E still take part in the shuffles of their warp
+        for (int o = 1; o < tpl; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const float lmax = s_logit[idx[0]];
+        const float p = lane < k ? expf(s_logit[idx[lane]] - lmax) : 0.f;
+        float denom;
+        if (normalize) {
+            denom = warp_sum(p);
+        } else {
+            float sum = 0.f;
+#pragma unroll 1
+            for (int x = lane; x < E; x += 32) sum += expf(s_logit[x] - lmax);
+            denom = warp_sum(sum);
+        }
+        if (lane < k) w[lane] = static_cast<WT>(p / denom);
+    }
+    __syncthreads();
+}
+
 }  // namespace mnb
