@@ -72,6 +72,8 @@ def _lib():
                 "orc_permute": [P, I64, C, I64, P, P, P],
                 "orc_qmoe": [P, C, I64, I64, P, I64, C, C, P, P, P, C, P, P, P, C, I64, C, C, P,
                              I64, P, C],
+                "orc_qmoe_ex": [P, C, I64, I64, P, C, I64, C, C, P, P, P, P, C, P, P, P, P, C, P, C, I64, C, C,
+                                P, I64, P, C],
                 "orc_quantize_int3": [P, C, I64, I64, C, C, P, P, P],
                 "orc_round_to_half_bits": [P, I64, C, P],
             }
@@ -219,6 +221,33 @@ def qmoe(X, act_dtype: str, logits, k: int, normalize: bool, fc1_w, fc1_scales, 
             _ptr(keep[5]), fc2_bits, I, bs, FC1_LAYOUTS[fc1_layout], _ptr(toks),
             0 if toks is None else toks.size, _ptr(out), threads)
     _check(_lib().orc_qmoe(*args), "qmoe")
+    return out
+
+
+def qmoe_ex(X, act_dtype: str, logits, logits_dtype: str, k: int, normalize: bool, fc1_w, fc1_scales, fc1_zp,
+            fc1_bias, fc1_bits: int, fc2_w, fc2_scales, fc2_zp, fc2_bias, fc2_bits: int, I: int, bs: int,
+            fc1_layout: str = "interleaved", agg=None, agg_dtype: str = "f32", tokens=None,
+            threads: int = 1) -> np.ndarray:
+    """fp64 Y[len(tokens) or T, H] with the optional inputs: logits [T, E] in
+    logits_dtype, fc1_bias [E, 2I] and fc2_bias [E, H] in act_dtype (or None),
+    agg [T, E] aggregation weights in agg_dtype (or None)."""
+    L = _elem(logits, logits_dtype)
+    T, E = np.asarray(logits).shape
+    X = _elem(X, act_dtype)
+    H = X.size // T
+    toks = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    rows = T if toks is None else toks.size
+    out = np.zeros((rows, H), np.float64)
+    keep = [_c(fc1_w, np.uint8), _elem(fc1_scales, act_dtype), _c(fc1_zp, np.uint8),
+            None if fc1_bias is None else _elem(fc1_bias, act_dtype),
+            _c(fc2_w, np.uint8), _elem(fc2_scales, act_dtype), _c(fc2_zp, np.uint8),
+            None if fc2_bias is None else _elem(fc2_bias, act_dtype),
+            None if agg is None else _elem(agg, agg_dtype)]
+    args = (_ptr(X), DTYPES[act_dtype], T, H, _ptr(L), DTYPES[logits_dtype], E, k, int(bool(normalize)),
+            _ptr(keep[0]), _ptr(keep[1]), _ptr(keep[2]), _ptr(keep[3]), fc1_bits, _ptr(keep[4]), _ptr(keep[5]),
+            _ptr(keep[6]), _ptr(keep[7]), fc2_bits, _ptr(keep[8]), DTYPES[agg_dtype], I, bs,
+            FC1_LAYOUTS[fc1_layout], _ptr(toks), 0 if toks is None else toks.size, _ptr(out), threads)
+    _check(_lib().orc_qmoe_ex(*args), "qmoe_ex")
     return out
 
 

@@ -309,11 +309,20 @@ static double swiglu(double g, double u) { return g / (1.0 + exp(-g)) * u; }
  * gate_i at row 2i and up_i at row 2i+1; the concatenated layout puts gate_i at
  * row i and up_i at row I+i.  Y[t] = sum_j w[t,j] * FC2_e(swiglu(FC1_e(x_t))),
  * ascending slot j, everything in fp64. */
-int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* logits, int64_t E,
-             int k, int normalize, const uint8_t* fc1_w, const void* fc1_s, const uint8_t* fc1_zp,
-             int fc1_bits, const uint8_t* fc2_w, const void* fc2_s, const uint8_t* fc2_zp,
-             int fc2_bits, int64_t I, int bs, int fc1_layout, const int64_t* tokens, int64_t n_tokens,
-             double* Y, int threads) {
+/* One QMoE layer with the optional inputs of the QMoE contract ("INT3 QMoE CUDA
+ * correctness baseline and Qwen experimental results", Summary: routing, fused
+ * gate/up SwiGLU, the down projection, optional biases / zero points /
+ * aggregation weights).  logits [T, E] in logits_dtype, widened exactly;
+ * fc1_bias [E, 2I] (rows in the FC1 layout) and fc2_bias [E, H] in act_dtype,
+ * added to the projections before SwiGLU and before the combine; agg [T, E] in
+ * agg_dtype: when given, the combine weight of slot j is agg[t, idx[j]]
+ * (selection still by the logits), else the routing weight.  Every NULL
+ * optional input is absent. */
+int orc_qmoe_ex(const void* X, int act_dtype, int64_t T, int64_t H, const void* logits, int logits_dtype,
+                int64_t E, int k, int normalize, const uint8_t* fc1_w, const void* fc1_s, const uint8_t* fc1_zp,
+                const void* fc1_bias, int fc1_bits, const uint8_t* fc2_w, const void* fc2_s, const uint8_t* fc2_zp,
+                const void* fc2_bias, int fc2_bits, const void* agg, int agg_dtype, int64_t I, int bs,
+                int fc1_layout, const int64_t* tokens, int64_t n_tokens, double* Y, int threads) {
     if (check_format(fc1_bits, bs) || check_format(fc2_bits, bs)) return 1;
     if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return 1;
     if (fc1_layout != ORC_FC1_INTERLEAVED && fc1_layout != ORC_FC1_CONCAT) return 1;
@@ -335,10 +344,11 @@ int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* lo
         double* wu = (double*)malloc(sizeof(double) * (size_t)H);
         double* h = (double*)malloc(sizeof(double) * (size_t)I);
         double* w2 = (double*)malloc(sizeof(double) * (size_t)I);
+        float* lrow = (float*)malloc(sizeof(float) * (size_t)E);
         int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
         double* rw = (double*)malloc(sizeof(double) * (size_t)k);
         unsigned char* taken = (unsigned char*)malloc((size_t)E);
-        if (!x || !wg || !wu || !h || !w2 || !idx || !rw || !taken) {
+        if (!x || !wg || !wu || !h || !w2 || !lrow || !idx || !rw || !taken) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -350,7 +360,10 @@ int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* lo
                     x[c] = load_elem(X, act_dtype, t * H + c);
                     y[c] = 0.0;
                 }
-                route_token(logits + t * E, E, k, normalize, idx, rw, taken);
+                for (int64_t e = 0; e < E; ++e) lrow[e] = (float)load_elem(logits, logits_dtype, t * E + e);
+                route_token(lrow, E, k, normalize, idx, rw, taken);
+                if (agg)
+                    for (int j = 0; j < k; ++j) rw[j] = load_elem(agg, agg_dtype, t * E + idx[j]);
                 for (int j = 0; j < k; ++j) {
                     int64_t e = idx[j];
                     const uint8_t* W1 = fc1_w + e * w1_stride;
@@ -367,20 +380,35 @@ int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* lo
                         double g = 0.0, u = 0.0;
                         for (int64_t q = 0; q < H; ++q) g += x[q] * wg[q];
                         for (int64_t q = 0; q < H; ++q) u += x[q] * wu[q];
+                        if (fc1_bias) {
+                            g += load_elem(fc1_bias, act_dtype, e * 2 * I + rg);
+                            u += load_elem(fc1_bias, act_dtype, e * 2 * I + ru);
+                        }
                         h[c] = swiglu(g, u);
                     }
                     for (int64_t r = 0; r < H; ++r) {
                         dequant_row(W2, S2, act_dtype, Z2, r, I, fc2_bits, bs, w2);
                         double o = 0.0;
                         for (int64_t q = 0; q < I; ++q) o += h[q] * w2[q];
+                        if (fc2_bias) o += load_elem(fc2_bias, act_dtype, e * H + r);
                         y[r] += rw[j] * o;
                     }
                 }
             }
         }
-        free(x); free(wg); free(wu); free(h); free(w2); free(idx); free(rw); free(taken);
+        free(x); free(wg); free(wu); free(h); free(w2); free(lrow); free(idx); free(rw); free(taken);
     }
     return bad;
+}
+
+int orc_qmoe(const void* X, int act_dtype, int64_t T, int64_t H, const float* logits, int64_t E,
+             int k, int normalize, const uint8_t* fc1_w, const void* fc1_s, const uint8_t* fc1_zp,
+             int fc1_bits, const uint8_t* fc2_w, const void* fc2_s, const uint8_t* fc2_zp,
+             int fc2_bits, int64_t I, int bs, int fc1_layout, const int64_t* tokens, int64_t n_tokens,
+             double* Y, int threads) {
+    return orc_qmoe_ex(X, act_dtype, T, H, logits, ORC_F32, E, k, normalize, fc1_w, fc1_s, fc1_zp, NULL,
+                       fc1_bits, fc2_w, fc2_s, fc2_zp, NULL, fc2_bits, NULL, ORC_F32, I, bs, fc1_layout, tokens,
+                       n_tokens, Y, threads);
 }
 
 /* --------------------------------------------- INT3 producer (quantizer) */

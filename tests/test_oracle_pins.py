@@ -368,6 +368,104 @@ def test_qmoe_unnormalised_weights_are_softmax_probabilities():
     assert np.allclose(one(E, False), one(E, True), rtol=1e-13, atol=1e-13)
 
 
+# ------------------------------------------- QMoE optional inputs (biases, aggregation)
+
+def _zero_weight_layer(g, E, H, I, bits, bs, act):
+    """Experts whose dequantised weights are all zero (unit scales, every code equal to
+    the implicit zero point): each projection is its bias alone."""
+    z = 1 << (bits - 1)
+    fc1 = np.stack([oracle.pack_codes(np.full((2 * I, H), z, np.uint8), bits, bs) for _ in range(E)])
+    fc2 = np.stack([oracle.pack_codes(np.full((H, I), z, np.uint8), bits, bs) for _ in range(E)])
+    s1 = wl.cast(np.ones((E, 2 * I, H // bs)), act)
+    s2 = wl.cast(np.ones((E, H, I // bs)), act)
+    return fc1, s1, fc2, s2
+
+
+def _topk_softmax(logits, k):
+    """Top-k by value, ties to the lower index (a stable sort of -logit), weights
+    renormalised over the selected probabilities."""
+    idx = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
+    sel = np.take_along_axis(logits.astype(np.float64), idx, axis=1)
+    p = np.exp(sel - sel[:, :1])
+    return idx, p / p.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("with_agg", [False, True])
+def test_qmoe_fc2_bias_and_aggregation_weights_closed_form(with_agg):
+    """All weights zero: FC1 gives its bias alone, FC2 gives its bias alone, so
+    Y[t] = sum_j c_j fc2_bias[e_j], c_j the routing weight of slot j, or with
+    aggregation weights c_j = agg[t, e_j] (the selection still follows the logits)."""
+    g = wl.rng(21)
+    T, H, I, E, k, bs, bits = 4, 64, 32, 6, 3, 32, 4
+    fc1, s1, fc2, s2 = _zero_weight_layer(g, E, H, I, bits, bs, "f16")
+    X = wl.normal(g, (T, H), "f16")
+    logits = wl.router_logits(g, T, E)
+    b1 = wl.normal(g, (E, 2 * I), "f16")
+    b2 = wl.normal(g, (E, H), "f16")
+    agg = wl.uniform(g, (T, E), 0.0, 1.0) if with_agg else None
+    Y = oracle.qmoe_ex(X, "f16", logits, "f32", k, True, fc1, s1, None, b1, bits, fc2, s2, None, b2, bits, I, bs,
+                       agg=agg)
+    idx, w = _topk_softmax(logits, k)
+    if with_agg:
+        w = np.take_along_axis(agg.astype(np.float64), idx, axis=1)
+    b2v = b2.view(np.float16).astype(np.float64)
+    ref = np.einsum("tj,tjh->th", w, b2v[idx])
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+def test_qmoe_fc1_bias_closed_form(layout):
+    """FC1 weights zero, FC2 the identity (H = I, explicit zero point 0, codes 1 on the
+    diagonal, unit scales): Y[t, n] = sum_j w_j silu(bg[e_j, n]) bu[e_j, n] with bg and bu
+    the FC1 bias entries of gate and up rows of pair n in the layout's row order."""
+    g = wl.rng(22)
+    T, H, I, E, k, bs, bits = 3, 32, 32, 5, 2, 32, 4
+    z = 1 << (bits - 1)
+    fc1 = np.stack([oracle.pack_codes(np.full((2 * I, H), z, np.uint8), bits, bs) for _ in range(E)])
+    eye = np.eye(H, I, dtype=np.uint8)
+    fc2 = np.stack([oracle.pack_codes(eye, bits, bs) for _ in range(E)])
+    z2 = np.stack([oracle.pack_zero_points(np.zeros((H, I // bs), np.uint8), bits) for _ in range(E)])
+    s1 = wl.cast(np.ones((E, 2 * I, H // bs)), "bf16")
+    s2 = wl.cast(np.ones((E, H, I // bs)), "bf16")
+    X = wl.normal(g, (T, H), "bf16")
+    logits = wl.router_logits(g, T, E)
+    b1 = wl.normal(g, (E, 2 * I), "bf16")
+    Y = oracle.qmoe_ex(X, "bf16", logits, "f32", k, True, fc1, s1, None, b1, bits, fc2, s2, z2, None, bits, I, bs,
+                       layout)
+    idx, w = _topk_softmax(logits, k)
+    b = torch.from_numpy(b1.view(np.int16)).view(torch.bfloat16).double().numpy()
+    bg = b[:, 0::2] if layout == "interleaved" else b[:, :I]
+    bu = b[:, 1::2] if layout == "interleaved" else b[:, I:]
+    h = bg / (1 + np.exp(-bg)) * bu  # [E, I]
+    ref = np.einsum("tj,tjn->tn", w, h[idx])
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("ldt", ["f16", "bf16"])
+def test_qmoe_half_logits_equal_their_widened_values(ldt):
+    """Router logits in a 16-bit type select and weigh exactly like fp32 logits that
+    hold the widened values."""
+    g = wl.rng(23)
+    T, H, I, E, k, bs = 3, 64, 32, 8, 3, 32
+    d = wl.moe_layer(g, T, H, I, E, 4, 3, bs, "f16")
+    lh = wl.cast(np.round(d["logits"] * 4) / 4, ldt)  # coarse values: ties in the selection too
+    lf = as_f64(lh, ldt).astype(np.float32).reshape(T, E)
+    args = lambda L, dt: oracle.qmoe_ex(d["X"], "f16", L, dt, k, True, d["fc1_w"], d["fc1_scales"], None, None, 4,
+                                        d["fc2_w"], d["fc2_scales"], None, None, 3, I, bs)
+    assert np.array_equal(args(lh.reshape(T, E), ldt), args(lf, "f32"))
+
+
+def test_qmoe_ex_without_options_is_qmoe():
+    g = wl.rng(24)
+    T, H, I, E, k, bs = 2, 64, 64, 4, 2, 64
+    d = wl.moe_layer(g, T, H, I, E, 3, 3, bs, "bf16", with_zp=True)
+    a = oracle.qmoe(d["X"], "bf16", d["logits"], k, False, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], 3, d["fc2_w"],
+                    d["fc2_scales"], d["fc2_zp"], 3, I, bs)
+    b = oracle.qmoe_ex(d["X"], "bf16", d["logits"], "f32", k, False, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], None,
+                       3, d["fc2_w"], d["fc2_scales"], d["fc2_zp"], None, 3, I, bs)
+    assert np.array_equal(a, b)
+
+
 # ------------------------------------------------- INT3 quantizer (producer)
 # The symmetric grouped INT3 round-to-nearest policy quoted in "INT3 QMoE CUDA
 # correctness baseline and Qwen experimental results" (Olive producer summary).
