@@ -155,6 +155,38 @@ mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H
                         mnb_fc1_layout fc1_layout, void* Y, void* workspace,
                         size_t workspace_bytes, mnb_stream_t stream);
 
+/* Optional inputs of a QMoE layer ("INT3 QMoE CUDA correctness baseline and
+ * Qwen experimental results", Summary: optional biases / zero points /
+ * aggregation weights).  Every NULL pointer is an absent input.
+ *   fc1_bias     [E, 2I] in act_dtype, rows in the FC1 layout; added to the
+ *                gate and up projections before SwiGLU.
+ *   fc2_bias     [E, H] in act_dtype; added to each expert's FC2 output
+ *                before the combine.
+ *   agg_weights  [T, E] in agg_dtype: the combine weight of slot j becomes
+ *                agg_weights[t, idx[j]] (the experts are still selected by the
+ *                router logits; normalize_topk then has no effect).
+ *   logits_dtype dtype of router_logits: MNB_F32, MNB_F16 or MNB_BF16 (the
+ *                selection and the softmax use the exactly widened values). */
+typedef struct {
+    const void* fc1_bias;
+    const void* fc2_bias;
+    const void* agg_weights;
+    mnb_dtype agg_dtype;
+    mnb_dtype logits_dtype;
+} qmoe_options;
+
+/* qmoe_forward with the optional inputs above (options == NULL: none, fp32
+ * logits; the result is then that of qmoe_forward).  router_logits is
+ * [T, E] in options->logits_dtype, aligned to its element size; the biases
+ * are aligned to 2 bytes, agg_weights to its element size.  Same workspace,
+ * layouts, errors and asynchrony as qmoe_forward. */
+mnb_status qmoe_forward_ex(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H, const void* router_logits,
+                           int64_t E, int k, int normalize_topk, const uint8_t* fc1_w, const void* fc1_scales,
+                           const uint8_t* fc1_zp, int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                           const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
+                           mnb_fc1_layout fc1_layout, void* Y, void* workspace, size_t workspace_bytes,
+                           const qmoe_options* options, mnb_stream_t stream);
+
 /* qmoe_forward without a workspace argument, for callers that cannot allocate
  * device memory: code that receives only input and output pointers (a plugin
  * or an operator inside another runtime that owns every allocation), code

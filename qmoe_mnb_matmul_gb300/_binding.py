@@ -42,6 +42,8 @@ _SIGNATURES = {
     "qmoe_workspace_size": [_I64, _I64, _I64, _I64, _I, _I, ctypes.POINTER(_SZ)],
     "qmoe_forward": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
                      _P, _P, _SZ, _P],
+    "qmoe_forward_ex": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
+                        _P, _P, _SZ, _P, _P],
     "qmoe_forward_static": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
                             _P, _P],
     "qmoe_route": [_P, _I64, _I64, _I, _I, _P, _P, _P],
@@ -184,6 +186,38 @@ def qmoe_forward(X, router_logits, k, normalize_topk, fc1_w, fc1_scales, fc1_zp,
                                      _ptr(workspace), workspace_bytes, _stream(stream))
     if check:
         _check(st, "qmoe_forward")
+    return st
+
+
+class QmoeOptions(ctypes.Structure):
+    """The qmoe_options struct of include/mnb.h (device pointers as ints)."""
+    _fields_ = [("fc1_bias", ctypes.c_void_p), ("fc2_bias", ctypes.c_void_p), ("agg_weights", ctypes.c_void_p),
+                ("agg_dtype", ctypes.c_int), ("logits_dtype", ctypes.c_int)]
+
+
+def qmoe_forward_ex(X, router_logits, k, normalize_topk, fc1_w, fc1_scales, fc1_zp, fc1_bits, fc2_w, fc2_scales,
+                    fc2_zp, fc2_bits, I, block_size, Y, workspace, stream=None, *, fc1_bias=None, fc2_bias=None,
+                    agg_weights=None, fc1_layout=FC1_INTERLEAVED, T=None, H=None, E=None, act_dtype=None,
+                    workspace_bytes=None, check=True):
+    """qmoe_forward with the optional inputs: FC1/FC2 biases, aggregation weights
+    [T, E], router logits of any float dtype (taken from the tensor)."""
+    if H is None:
+        H = X.shape[-1]
+    if T is None:
+        T = X.numel() // H
+    if E is None:
+        E = router_logits.shape[-1]
+    act_dtype = _dtype_code(X) if act_dtype is None else act_dtype
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    opts = QmoeOptions(_ptr(fc1_bias), _ptr(fc2_bias), _ptr(agg_weights),
+                       _dtype_code(agg_weights) if agg_weights is not None else F32, _dtype_code(router_logits))
+    st = load_library().qmoe_forward_ex(_ptr(X), act_dtype, T, H, _ptr(router_logits), E, k, int(bool(normalize_topk)),
+                                        _ptr(fc1_w), _ptr(fc1_scales), _ptr(fc1_zp), fc1_bits, _ptr(fc2_w),
+                                        _ptr(fc2_scales), _ptr(fc2_zp), fc2_bits, I, block_size, fc1_layout, _ptr(Y),
+                                        _ptr(workspace), workspace_bytes, ctypes.byref(opts), _stream(stream))
+    if check:
+        _check(st, "qmoe_forward_ex")
     return st
 
 

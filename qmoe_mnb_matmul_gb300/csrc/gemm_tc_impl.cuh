@@ -632,12 +632,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         // each trading the value the other needs in one shuffle.
                         const int64_t p = x.n0 / 2 + (rr >> 1);
                         const int odd = lane & 1;
+                        float bg = 0.f, bu = 0.f;  // biases of the pair's gate and up rows
+                        if (a.bias && p < a.I) {
+                            const auto* bp = static_cast<const typename DType<AT>::T*>(a.bias) + x.e * a.rows;
+                            bg = to_f32(bp[a.inter ? 2 * p : p]);
+                            bu = to_f32(bp[a.inter ? 2 * p + 1 : a.I + p]);
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; j += 2) {
                             const float send = __uint_as_float(odd ? v[j] : v[j + 1]);  // even: gate of j+1; odd: up of j
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                            const float gate = odd ? recv : __uint_as_float(v[j]);
-                            const float up = odd ? __uint_as_float(v[j + 1]) : recv;
+                            const float gate = (odd ? recv : __uint_as_float(v[j])) + bg;
+                            const float up = (odd ? __uint_as_float(v[j + 1]) : recv) + bu;
                             const int col = j + odd;
                             if (col < jn && p < a.I) {
                                 // h is rounded to the 16-bit activation type next, so the fast
@@ -648,6 +654,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         }
                     } else {
                         const int64_t n = x.n0 + rr;
+                        if (a.bias && n < a.rows) {  // grouped FC2: the expert's bias of row n
+                            const float b = to_f32(static_cast<const typename DType<AT>::T*>(a.bias)[x.e * a.rows + n]);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + b);
+                        }
                         if (n < a.rows && a.splits > 1) {  // fp32 partial sums of this split of K
                             float* pp = a.partials + (int64_t(x.split) * a.M + m0 + c0) * a.ld_y + n;
 #pragma unroll

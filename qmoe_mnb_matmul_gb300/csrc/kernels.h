@@ -97,6 +97,9 @@ struct TcArgs {
     // activation type) and the epilogue adds to the fp32 output instead of
     // storing it.
     int remainder;
+    // grouped (QMoE) launches: bias [experts, rows] in the activation dtype
+    // added to each output row (FC1: to the gate and up rows before SwiGLU), or null
+    const void* bias;
 };
 
 // Rows of activations per tile in the grouped launches.
@@ -115,8 +118,10 @@ cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, 
                                 uint8_t* codes, cudaStream_t stream);
 
 // ------------------------------------------------------------- routing
-cudaError_t launch_route(const float* logits, int64_t T, int64_t E, int k, int normalize,
-                         int32_t* idx, float* w, cudaStream_t stream);
+// logits [T, E] in dtype ldt; agg (or null): [T, E] aggregation weights in dtype
+// adt, which replace the routing weights of the selected experts.
+cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int normalize,
+                         int32_t* idx, float* w, const void* agg, int adt, cudaStream_t stream);
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
 

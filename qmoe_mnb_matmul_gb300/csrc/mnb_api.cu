@@ -238,8 +238,8 @@ mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int norm
     if (E > 1024) return MNB_ERR_UNSUPPORTED;
     int64_t tmp;
     if (!mul_ok(T, E * 4, &tmp) || T > (int64_t(1) << 31)) return MNB_ERR_SIZE_OVERFLOW;
-    return from_cuda(launch_route(logits, T, E, k, normalize_topk ? 1 : 0, topk_idx, topk_w,
-                                  reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_route(logits, MNB_F32, T, E, k, normalize_topk ? 1 : 0, topk_idx, topk_w, nullptr,
+                                  MNB_F32, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
@@ -266,20 +266,24 @@ mnb_status qmoe_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int k
     return MNB_OK;
 }
 
-mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H, const float* router_logits,
-                        int64_t E, int k, int normalize_topk, const uint8_t* fc1_w, const void* fc1_scales,
-                        const uint8_t* fc1_zp, int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
-                        const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
-                        mnb_fc1_layout fc1_layout, void* Y, void* workspace, size_t workspace_bytes,
-                        mnb_stream_t stream) {
+mnb_status qmoe_forward_ex(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H, const void* router_logits,
+                           int64_t E, int k, int normalize_topk, const uint8_t* fc1_w, const void* fc1_scales,
+                           const uint8_t* fc1_zp, int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                           const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size, mnb_fc1_layout fc1_layout,
+                           void* Y, void* workspace, size_t workspace_bytes, const qmoe_options* options,
+                           mnb_stream_t stream) {
+    const qmoe_options none = {nullptr, nullptr, nullptr, MNB_F32, MNB_F32};
+    const qmoe_options& op = options ? *options : none;
     if (!X || !router_logits || !fc1_w || !fc1_scales || !fc2_w || !fc2_scales || !Y) return MNB_ERR_INVALID_ARG;
     if (T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return MNB_ERR_INVALID_ARG;
     if (fc1_layout != MNB_FC1_INTERLEAVED && fc1_layout != MNB_FC1_CONCAT) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(op.logits_dtype) || !valid_dtype(op.agg_dtype)) return MNB_ERR_INVALID_ARG;
     if (act_dtype != MNB_F16 && act_dtype != MNB_BF16) return MNB_ERR_UNSUPPORTED;
     if (!valid_bits(fc1_bits) || !valid_bits(fc2_bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     if (H % block_size != 0 || I % block_size != 0 || E > 1024) return MNB_ERR_UNSUPPORTED;
     if (!aligned(fc1_w, 16) || !aligned(fc2_w, 16) || !aligned(fc1_scales, 16) || !aligned(fc2_scales, 16) ||
-        !aligned(X, 2) || !aligned(Y, 2) || !aligned(router_logits, 4))
+        !aligned(X, 2) || !aligned(Y, 2) || !aligned(router_logits, dsize(op.logits_dtype)) ||
+        !aligned(op.fc1_bias, 2) || !aligned(op.fc2_bias, 2) || !aligned(op.agg_weights, dsize(op.agg_dtype)))
         return MNB_ERR_UNSUPPORTED;
     ProjBytes p1, p2;
     int64_t w1, w2, tmp;
@@ -304,6 +308,11 @@ mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H
     q.k = k;
     q.normalize = normalize_topk ? 1 : 0;
     q.logits = router_logits;
+    q.logits_dtype = op.logits_dtype;
+    q.fc1_bias = op.fc1_bias;
+    q.fc2_bias = op.fc2_bias;
+    q.agg = op.agg_weights;
+    q.agg_dtype = op.agg_dtype;
     q.fc1_w = fc1_w;
     q.fc1_s = fc1_scales;
     q.fc1_zp = fc1_zp;
@@ -320,6 +329,17 @@ mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H
     q.fc1 = {p1.nb, p1.row_bytes, p1.zp_row};
     q.fc2 = {p2.nb, p2.row_bytes, p2.zp_row};
     return from_cuda(launch_qmoe(q, sms, pdl_enabled(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status qmoe_forward(const void* X, mnb_dtype act_dtype, int64_t T, int64_t H, const float* router_logits,
+                        int64_t E, int k, int normalize_topk, const uint8_t* fc1_w, const void* fc1_scales,
+                        const uint8_t* fc1_zp, int fc1_bits, const uint8_t* fc2_w, const void* fc2_scales,
+                        const uint8_t* fc2_zp, int fc2_bits, int64_t I, int block_size,
+                        mnb_fc1_layout fc1_layout, void* Y, void* workspace, size_t workspace_bytes,
+                        mnb_stream_t stream) {
+    return qmoe_forward_ex(X, act_dtype, T, H, router_logits, E, k, normalize_topk, fc1_w, fc1_scales, fc1_zp,
+                           fc1_bits, fc2_w, fc2_scales, fc2_zp, fc2_bits, I, block_size, fc1_layout, Y, workspace,
+                           workspace_bytes, nullptr, stream);
 }
 
 // ------------------------------------------------------ host validation

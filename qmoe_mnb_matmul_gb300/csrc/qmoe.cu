@@ -130,21 +130,38 @@ __host__ __device__ inline Fc2Plan fc2_plan(int rows, int ACT, int C, int64_t ro
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // One warp routes a token with more than kBlockRouteMaxE experts (rare; out of line).
-static __device__ __noinline__ void route_wide(const float* row, int E, int k, int normalize, int* s_idx, float* s_w) {
-    warp_route_pl<kMaxExpertsPerLane>(row, E, k, normalize, s_idx, s_w, 1);
+static __device__ __noinline__ void route_wide(const void* row, int ldt, int E, int k, int normalize, int* s_idx,
+                                              float* s_w, const void* agg, int adt) {
+    warp_route_pl<kMaxExpertsPerLane>(row, ldt, E, k, normalize, s_idx, s_w, 1, agg, adt);
+}
+
+// Router row and aggregation-weight row of token t.
+__device__ __forceinline__ const void* logits_row(const QmoeArgs& q, int64_t t) {
+    return static_cast<const char*>(q.logits) + t * q.E * (q.logits_dtype == kF32 ? 4 : 2);
+}
+__device__ __forceinline__ const void* agg_row(const QmoeArgs& q, int64_t t) {
+    return q.agg ? static_cast<const char*>(q.agg) + t * q.E * (q.agg_dtype == kF32 ? 4 : 2) : nullptr;
 }
 
 // Decode kernels route their own token: the whole CTA ranks up to
 // kBlockRouteMaxE logits at once, larger routers fall back to one warp.
 // Ends with a block barrier; s_logit holds kBlockRouteMaxE floats.
 __device__ __forceinline__ void route_token(const QmoeArgs& q, int64_t t, int* s_idx, float* s_w, float* s_logit) {
-    const float* row = q.logits + t * q.E;
+    const void* row = logits_row(q, t);
     if (q.E <= kBlockRouteMaxE && q.E <= kThreads) {
-        block_route(row, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, s_logit);
+        block_route(row, q.logits_dtype, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, s_logit, agg_row(q, t),
+                    q.agg_dtype);
     } else {
-        if (threadIdx.x < 32) route_wide(row, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w);
+        if (threadIdx.x < 32)
+            route_wide(row, q.logits_dtype, static_cast<int>(q.E), q.k, q.normalize, s_idx, s_w, agg_row(q, t),
+                       q.agg_dtype);
         __syncthreads();
     }
+}
+
+// Bias entry i of a bias tensor in the activation dtype (0 without a bias).
+__device__ __forceinline__ float bias_at(const void* bias, int dt, int64_t i) {
+    return bias ? load_as_f32(bias, dt, i) : 0.f;
 }
 
 // ------------------------------------------------------------------ FC1
@@ -295,8 +312,13 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
                 const int pq = 2 * g + pp;
                 if (pq >= pc) break;
 #pragma unroll
+                const int64_t pa = pair0 + pq;  // bias rows of the gate and up halves of pair pa
+                const float bg = bias_at(q.fc1_bias, q.act_dtype, int64_t(e) * 2 * I + (inter ? 2 * pa : pa));
+                const float bu = bias_at(q.fc1_bias, q.act_dtype, int64_t(e) * 2 * I + (inter ? 2 * pa + 1 : I + pa));
+#pragma unroll
                 for (int m = 0; m < MT; ++m)
-                    if (m < cnt) h[int64_t(s0 + m) * I + pair0 + pq] = silu_mul(out[2 * pp][m], out[2 * pp + 1][m]);
+                    if (m < cnt)
+                        h[int64_t(s0 + m) * I + pair0 + pq] = silu_mul(out[2 * pp][m] + bg, out[2 * pp + 1][m] + bu);
             }
         }
     }
@@ -396,7 +418,8 @@ __global__ void __launch_bounds__(kThreads) fc2_decode_kernel(const __grid_const
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const float v = warp_sum(out[r][0].x + out[r][0].y);
-            if (lane == 0 && g * R + r < rc) part[j * kDecodeRows2 + g * R + r] = v;
+            if (lane == 0 && g * R + r < rc)
+                part[j * kDecodeRows2 + g * R + r] = v + bias_at(q.fc2_bias, q.act_dtype, e * H + n0 + g * R + r);
         }
     }
     __syncthreads();
@@ -496,8 +519,10 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
                 const int rl = g * R + r;
                 if (rl >= rc) break;
 #pragma unroll
+                const float b2 = bias_at(q.fc2_bias, q.act_dtype, int64_t(e) * H + n0 + rl);
+#pragma unroll
                 for (int m = 0; m < MT; ++m)
-                    if (m < cnt) o[int64_t(s0 + m) * H + n0 + rl] = out[r][m];
+                    if (m < cnt) o[int64_t(s0 + m) * H + n0 + rl] = out[r][m] + b2;
             }
         }
     }
@@ -690,7 +715,9 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     }
     int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
     float* wts = reinterpret_cast<float*>(ws + L.wts);
-    if ((e = launch_route(q.logits, q.T, q.E, q.k, q.normalize, idx, wts, stream)) != cudaSuccess) return e;
+    if ((e = launch_route(q.logits, q.logits_dtype, q.T, q.E, q.k, q.normalize, idx, wts, q.agg, q.agg_dtype,
+                          stream)) != cudaSuccess)
+        return e;
     if ((e = launch_permute_chunked(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.chunkc),
                                     reinterpret_cast<int32_t*>(ws + L.counts),
                                     reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
@@ -728,6 +755,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.I = q.I;
         a.inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
         a.X = q.X;
+        a.bias = q.fc1_bias;
         // The routed tokens' rows in expert-sorted order go into the FC2-output
         // region (free until FC2 runs), so FC1 loads them as plain TMA tiles.
         {
@@ -752,6 +780,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.z_expert_stride = q.H * q.fc2.zp_row;
         a.Y = ws + L.o;
         a.ld_y = q.H;
+        a.bias = q.fc2_bias;
         a.tiles_n = static_cast<int>(cdiv<int64_t>(q.H, 128));
         a.k_steps = static_cast<int>(cdiv<int64_t>(q.I, 64));
         if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, sm_count, pdl, stream)) != cudaSuccess)

@@ -17,7 +17,12 @@ struct QmoeArgs {
     int act_dtype;
     int64_t T, H, I, E;
     int k, normalize;
-    const float* logits;
+    const void* logits;
+    int logits_dtype;        // fp32, fp16 or bf16 router logits
+    const void* fc1_bias;    // [E, 2I] in the activation dtype (rows in the FC1 layout) or null
+    const void* fc2_bias;    // [E, H] in the activation dtype or null
+    const void* agg;         // [T, E] aggregation weights (combine weights) or null
+    int agg_dtype;
     const uint8_t* fc1_w;
     const void* fc1_s;
     const uint8_t* fc1_zp;

@@ -151,9 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
         fence_barrier_init();
     }
     if (q.E <= kBlockRouteMaxE && q.E <= kThreads) {
-        block_route_fast(q.logits, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, s_logit);
+        block_route_fast(q.logits, q.logits_dtype, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, s_logit, q.agg,
+                         q.agg_dtype);
     } else {
-        if (tid < 32) warp_route(q.logits, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, 1);
+        if (tid < 32) warp_route(q.logits, q.logits_dtype, static_cast<int>(q.E), k, q.normalize, s_idx, s_w, 1, q.agg,
+                                 q.agg_dtype);
         __syncthreads();
     }
     // local FC1 pair lp: gate row at lrow(lp, 0), up row at lrow(lp, 1) of the staged rows
@@ -263,7 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
                     if (lp >= np) break;
                     const int64_t p = pr0 + lp;
                     const int j = static_cast<int>(p / I);
-                    h[int64_t(j) * I + (p - int64_t(j) * I)] = silu_mul(acc[2 * pp], acc[2 * pp + 1]);
+                    const int64_t a = p - int64_t(j) * I;
+                    float bg = 0.f, bu = 0.f;  // biases of the gate and up rows of pair a
+                    if (q.fc1_bias) {
+                        const int64_t base = int64_t(s_idx[j]) * 2 * I;
+                        bg = load_as_f32(q.fc1_bias, q.act_dtype, base + (inter ? 2 * a : a));
+                        bu = load_as_f32(q.fc1_bias, q.act_dtype, base + (inter ? 2 * a + 1 : I + a));
+                    }
+                    h[int64_t(j) * I + a] = silu_mul(acc[2 * pp] + bg, acc[2 * pp + 1] + bu);
                 }
             }
         }
@@ -357,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmoe_decode_fused_kernel(const __
             if (lane == 0) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    if (r0 + r < nr) part[j * kMaxRows2 + r0 + r] = acc[r];
+                    if (r0 + r < nr)
+                        part[j * kMaxRows2 + r0 + r] =
+                            acc[r] + (q.fc2_bias ? load_as_f32(q.fc2_bias, q.act_dtype, e * H + n0 + r0 + r) : 0.f);
             }
         }
     }

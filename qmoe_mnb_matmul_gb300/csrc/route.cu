@@ -59,12 +59,14 @@ __global__ void pack_kernel(const uint8_t* __restrict__ codes, int64_t rows, int
 // ----------------------------------------------------------------- routing
 
 // One warp per token (see route_core.cuh).
-__global__ void route_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int normalize,
-                             int32_t* __restrict__ idx, float* __restrict__ wout) {
+__global__ void route_kernel(const void* __restrict__ logits, int ldt, int64_t T, int E, int k, int normalize,
+                             int32_t* __restrict__ idx, float* __restrict__ wout, const void* agg, int adt) {
     const int64_t t = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5);
     grid_dependency_wait();
     if (t >= T) return;
-    warp_route(logits + t * E, E, k, normalize, idx + t * k, wout + t * k, 1);
+    const int esz = ldt == kF32 ? 4 : 2, asz = adt == kF32 ? 4 : 2;
+    warp_route(static_cast<const char*>(logits) + t * E * esz, ldt, E, k, normalize, idx + t * k, wout + t * k, 1,
+               agg ? static_cast<const char*>(agg) + t * E * asz : nullptr, adt);
 }
 
 // ------------------------------------------------------------- permutation
@@ -331,12 +333,12 @@ cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_route(const float* logits, int64_t T, int64_t E, int k, int normalize, int32_t* idx,
-                         float* w, cudaStream_t stream) {
+cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int normalize, int32_t* idx,
+                         float* w, const void* agg, int adt, cudaStream_t stream) {
     const int warps = 8;
     const int64_t blocks = cdiv<int64_t>(T, warps);
-    route_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(logits, T, static_cast<int>(E), k,
-                                                                            normalize, idx, w);
+    route_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(logits, ldt, T, static_cast<int>(E), k,
+                                                                            normalize, idx, w, agg, adt);
     return cudaGetLastError();
 }
 

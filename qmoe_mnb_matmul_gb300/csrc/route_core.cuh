@@ -15,9 +15,18 @@ constexpr int kNoExpert = 0x7fffffff;
 
 // One warp, PL logits per lane (E <= 32 PL): expert e lives in slot e / 32 of
 // lane e % 32, so the argmax scans only the PL slots a lane can hold.
+// Logit e of a router row stored in dtype dt (fp32, fp16 or bf16; widened exactly).
+__device__ __forceinline__ float logit_at(const void* row, int dt, int e) { return load_as_f32(row, dt, e); }
+
+// With aggregation weights, slot j's combine weight is agg[idx[j]] (dtype adt)
+// instead of the routing probability; called by the lane that owns slot j.
+__device__ __forceinline__ float agg_or(const void* agg, int adt, int e, float p) {
+    return agg ? load_as_f32(agg, adt, e) : p;
+}
+
 template <int PL, typename IdxT, typename WT>
-__device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int E, int k, int normalize, IdxT* idx,
-                                              WT* w, int stride) {
+__device__ __forceinline__ void warp_route_pl(const void* __restrict__ row, int ldt, int E, int k, int normalize,
+                                              IdxT* idx, WT* w, int stride, const void* agg = nullptr, int adt = 0) {
     const int lane = threadIdx.x & 31;
     const int per_lane = (E + 31) >> 5;
     float v[PL];
@@ -27,7 +36,7 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
     for (int i = 0; i < PL; ++i) {
         const int e = i * 32 + lane;
         const bool ok = i < per_lane && e < E;
-        v[i] = ok ? row[e] : -INFINITY;
+        v[i] = ok ? logit_at(row, ldt, e) : -INFINITY;
         if (ok) lmax = fmaxf(lmax, v[i]);
     }
 #pragma unroll
@@ -63,7 +72,7 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
             }
         } else if (lane == 0) {  // k > 32: park the raw weight in the output
             idx[j * stride] = static_cast<IdxT>(be);
-            w[j * stride] = static_cast<WT>(p);
+            w[j * stride] = static_cast<WT>(agg ? agg_or(agg, adt, be, p) : p);
         }
     }
     float denom = sel_sum;
@@ -78,10 +87,10 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
     }
     if (lane < k) {
         idx[lane * stride] = static_cast<IdxT>(my_e);
-        w[lane * stride] = static_cast<WT>(my_p / denom);
+        w[lane * stride] = static_cast<WT>(agg ? agg_or(agg, adt, my_e, 0.f) : my_p / denom);
     }
     __syncwarp();
-    if (k > 32 && lane == 0)
+    if (k > 32 && lane == 0 && !agg)
         for (int j = 32; j < k; ++j) w[j * stride] = static_cast<WT>(static_cast<float>(w[j * stride]) / denom);
     __syncwarp();
 }
@@ -92,14 +101,14 @@ __device__ __forceinline__ void warp_route_pl(const float* __restrict__ row, int
 // The scan width is fixed at compile time from E, so a 128-expert router pays
 // for four logits per lane, not for the 1024-expert maximum.
 template <typename IdxT, typename WT>
-__device__ __forceinline__ void warp_route(const float* __restrict__ row, int E, int k, int normalize, IdxT* idx,
-                                           WT* w, int stride) {
-    if (E <= 32) return warp_route_pl<1>(row, E, k, normalize, idx, w, stride);
-    if (E <= 64) return warp_route_pl<2>(row, E, k, normalize, idx, w, stride);
-    if (E <= 128) return warp_route_pl<4>(row, E, k, normalize, idx, w, stride);
-    if (E <= 256) return warp_route_pl<8>(row, E, k, normalize, idx, w, stride);
-    if (E <= 512) return warp_route_pl<16>(row, E, k, normalize, idx, w, stride);
-    return warp_route_pl<kMaxExpertsPerLane>(row, E, k, normalize, idx, w, stride);
+__device__ __forceinline__ void warp_route(const void* __restrict__ row, int ldt, int E, int k, int normalize,
+                                           IdxT* idx, WT* w, int stride, const void* agg = nullptr, int adt = 0) {
+    if (E <= 32) return warp_route_pl<1>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
+    if (E <= 64) return warp_route_pl<2>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
+    if (E <= 128) return warp_route_pl<4>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
+    if (E <= 256) return warp_route_pl<8>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
+    if (E <= 512) return warp_route_pl<16>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
+    return warp_route_pl<kMaxExpertsPerLane>(row, ldt, E, k, normalize, idx, w, stride, agg, adt);
 }
 
 // Routing of one token by a whole CTA (blockDim.x >= E): every thread ranks
@@ -111,11 +120,11 @@ __device__ __forceinline__ void warp_route(const float* __restrict__ row, int E,
 constexpr int kBlockRouteMaxE = 256;
 
 template <typename WT>
-__device__ __forceinline__ void block_route(const float* __restrict__ row, int E, int k, int normalize, int* idx,
-                                            WT* w, float* s_logit) {
+__device__ __forceinline__ void block_route(const void* __restrict__ row, int ldt, int E, int k, int normalize,
+                                            int* idx, WT* w, float* s_logit, const void* agg = nullptr, int adt = 0) {
     const int tid = threadIdx.x, lane = tid & 31;
     if (tid < E) {
-        const float x = row[tid];
+        const float x = logit_at(row, ldt, tid);
         s_logit[tid] = x != x ? -INFINITY : x;
     }
     __syncthreads();
@@ -160,7 +169,8 @@ __device__ __forceinline__ void block_route(const float* __restrict__ row, int E
             }
             if (normalize) denom = sel;
 #pragma unroll 1
-            for (int j = 0; j < k; ++j) w[j] = static_cast<WT>(static_cast<float>(w[j]) / denom);
+            for (int j = 0; j < k; ++j)
+                w[j] = static_cast<WT>(agg ? agg_or(agg, adt, idx[j], 0.f) : static_cast<float>(w[j]) / denom);
         }
     }
     __syncthreads();
@@ -174,13 +184,14 @@ __device__ __forceinline__ void block_route(const float* __restrict__ row, int E
 // sum.  Needs blockDim.x >= E, a multiple of 32; all threads must call it; it
 // ends with a block barrier.  s_logit is shared scratch of E floats.
 template <typename WT>
-__device__ __forceinline__ void block_route_fast(const float* __restrict__ row, int E, int k, int normalize, int* idx,
-                                                 WT* w, float* s_logit) {
+__device__ __forceinline__ void block_route_fast(const void* __restrict__ row, int ldt, int E, int k, int normalize,
+                                                 int* idx, WT* w, float* s_logit, const void* agg = nullptr,
+                                                 int adt = 0) {
     const int tid = threadIdx.x, lane = tid & 31;
     int tpl = 1;
     while (tpl < 8 && E * tpl * 2 <= int(blockDim.x)) tpl *= 2;
     if (tid < E) {
-        const float x = row[tid];
+        const float x = logit_at(row, ldt, tid);
         s_logit[tid] = x != x ? -INFINITY : x;
     }
     __syncthreads();
@@ -211,7 +222,7 @@ __device__ __forceinline__ void block_route_fast(const float* __restrict__ row, 
             for (int x = lane; x < E; x += 32) sum += expf(s_logit[x] - lmax);
             denom = warp_sum(sum);
         }
-        if (lane < k) w[lane] = static_cast<WT>(p / denom);
+        if (lane < k) w[lane] = static_cast<WT>(agg ? agg_or(agg, adt, idx[lane], 0.f) : p / denom);
     }
     __syncthreads();
 }

@@ -203,3 +203,51 @@ def test_expert_weights_written_by_the_quantizer_right_ahead():
     d2 = dict(d, fc1_w=W1.cpu().numpy().reshape(E, 2 * I, -1),
               fc1_scales=S1.cpu().view(torch.int16).numpy().view(np.uint16).reshape(E, 2 * I, -1))
     check(to_f64(Y), reference(d2, k, 3, 3, I, bs, "f16"), "f16", 1)
+
+
+# ----------------------------------------------------------- optional inputs
+
+def run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x_offset=0):
+    """qmoe_forward_ex; x_offset = 1 places X one element past a 16-byte boundary
+    (its rows then cannot be read with 16-byte loads: the tiled CUDA-core plan)."""
+    code = {"f16": mnb.F16, "bf16": mnb.BF16}[act]
+    ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, code), dtype=torch.uint8, device="cuda")
+    Y, full = empty_guarded(T * H, act)
+    Xbuf = torch.zeros(T * H + 8, dtype=torch.float16 if act == "f16" else torch.bfloat16, device="cuda")
+    Xbuf[x_offset:x_offset + T * H] = to_dev(d["X"], act).reshape(-1)
+    X = Xbuf[x_offset:x_offset + T * H]
+    z = lambda a: None if a is None else to_dev(a)
+    lay = mnb.FC1_INTERLEAVED if layout == "interleaved" else mnb.FC1_CONCAT
+    mnb.qmoe_forward_ex(X, to_dev(d["logits"], ldt if ldt != "f32" else None), k, True, to_dev(d["fc1_w"]),
+                        to_dev(d["fc1_scales"], act), z(d["fc1_zp"]), b1, to_dev(d["fc2_w"]), to_dev(d["fc2_scales"], act),
+                        z(d["fc2_zp"]), b2, I, bs, Y, ws, fc1_bias=None if b1v is None else to_dev(b1v, act),
+                        fc2_bias=None if b2v is None else to_dev(b2v, act), agg_weights=None if agg is None else to_dev(agg),
+                        fc1_layout=lay, T=T, H=H, E=E, act_dtype=code)
+    torch.cuda.synchronize()
+    assert guards_intact(full), "write outside Y"
+    assert mnb.mnb_get_last_device_error() == 0
+    return to_f64(Y).reshape(T, H)
+
+
+@pytest.mark.parametrize("T,x_offset", [(1, 0), (3, 0), (40, 0), (20, 1)])
+@pytest.mark.parametrize("opts", ["biases", "agg", "half_logits", "all"])
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+def test_optional_inputs_every_plan(T, x_offset, opts, layout):
+    """FC1/FC2 biases, aggregation weights and 16-bit router logits on every plan: the
+    single-pass layer (T = 1), the two-kernel decode (T = 3), the tensor-core plan
+    (T = 40) and the tiled CUDA-core plan (X rows off a 16-byte boundary)."""
+    H, I, E, k, bs, b1, b2 = 512, 256, 32, 4, 64, 3, 4
+    act = "bf16" if T % 2 else "f16"
+    g = wl.rng(seed("opts", T, x_offset, opts, layout))
+    d = wl.moe_layer(g, T, H, I, E, b1, b2, bs, act, with_zp=True, skew=True)
+    want_b = opts in ("biases", "all")
+    b1v = wl.normal(g, (E, 2 * I), act) if want_b else None
+    b2v = wl.normal(g, (E, H), act) if want_b else None
+    agg = wl.uniform(g, (T, E), 0.0, 1.0) if opts in ("agg", "all") else None
+    ldt = "bf16" if opts in ("half_logits", "all") else "f32"
+    if ldt != "f32":
+        d = dict(d, logits=wl.cast(d["logits"], ldt))
+    y = run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x_offset)
+    ref = oracle.qmoe_ex(d["X"], act, d["logits"], ldt, k, True, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], b1v, b1,
+                         d["fc2_w"], d["fc2_scales"], d["fc2_zp"], b2v, b2, I, bs, layout, agg=agg, threads=THREADS)
+    check(y, ref, act, T if x_offset == 0 else 1, f"opts={opts} T={T} layout={layout}")
