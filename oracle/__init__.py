@@ -75,6 +75,8 @@ def _lib():
                 "orc_qmoe_ex": [P, C, I64, I64, P, C, I64, C, C, P, P, P, P, C, P, P, P, P, C, P, C, I64, C, C,
                                 P, I64, P, C],
                 "orc_quantize_int3": [P, C, I64, I64, C, C, P, P, P],
+                "orc_quantize_a_int8": [P, C, I64, I64, C, P, P],
+                "orc_mnb_matmul_int8a": [P, C, I64, I64, P, P, C, P, I64, C, C, P, C],
                 "orc_round_to_half_bits": [P, I64, C, P],
             }
             for name, args in sig.items():
@@ -180,6 +182,32 @@ def mnb_matmul(A, a_dtype: str, packed, scales, s_dtype: str, zp, N: int, K: int
     _check(_lib().orc_mnb_matmul(_ptr(A), DTYPES[a_dtype], M, K, _ptr(packed), _ptr(scales),
                                  DTYPES[s_dtype], _ptr(zp), N, bits, bs, _ptr(rows),
                                  0 if rows is None else rows.size, _ptr(out), threads), "matmul")
+    return out
+
+
+def quantize_a_int8(A, a_dtype: str, K: int, bs: int):
+    """Per-(row, block) symmetric int8 quantisation of activations A [M, K]:
+    (aq int8 [M, K], sa float32 [M, nb]) -- the accuracy_level=4 activation step."""
+    A = _elem(A, a_dtype)
+    M = A.size // K
+    nb = n_blocks(K, bs)
+    aq = np.zeros((M, K), np.int8)
+    sa = np.zeros((M, nb), np.float32)
+    _lib().orc_quantize_a_int8(_ptr(A), DTYPES[a_dtype], M, K, bs, _ptr(aq), _ptr(sa))
+    return aq, sa
+
+
+def mnb_matmul_int8a(A, a_dtype: str, packed, scales, s_dtype: str, zp, N: int, K: int, bits: int, bs: int,
+                     threads: int = 1) -> np.ndarray:
+    """fp64 Y[M, N] of MatMulNBits with int8 activation compute (accuracy_level=4)."""
+    A = _elem(A, a_dtype)
+    M = A.size // K if K else 0
+    packed = _c(packed, np.uint8)
+    scales = _elem(scales, s_dtype)
+    zp = _c(zp, np.uint8)
+    out = np.zeros((M, N), np.float64)
+    _check(_lib().orc_mnb_matmul_int8a(_ptr(A), DTYPES[a_dtype], M, K, _ptr(packed), _ptr(scales),
+                                       DTYPES[s_dtype], _ptr(zp), N, bits, bs, _ptr(out), threads), "matmul_int8a")
     return out
 
 

@@ -235,6 +235,72 @@ int orc_mnb_matmul(const void* A, int a_dtype, int64_t M, int64_t K,
     return bad;
 }
 
+/* MatMulNBits with accuracy_level=4 ("Qwen3 Missing-Kernel Implementation
+ * Plan", row K01: the audited contract carries accuracy_level=4, which ONNX
+ * Runtime takes as int8 activation compute).  Each block of bs activations of
+ * a row (the weight's K blocks) is quantised symmetrically:
+ *   amax = max |a| over the block's K entries (binary32),
+ *   sa   = amax / 127 (binary32 division; 0 when amax is 0),
+ *   aq   = rint(a / sa) clamped to [-127, 127] (binary32 quotient, ties to
+ *          even; 0 when sa is 0),
+ * and Y[m, n] = sum_b sa_b * sw_b * sum_{k in b} aq_k (q_k - z_b), the inner
+ * sums exact integers, the rest in fp64, ascending b. */
+void orc_quantize_a_int8(const void* A, int a_dtype, int64_t M, int64_t K, int bs, int8_t* aq, float* sa) {
+    int64_t nb = n_blocks(K, bs);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int64_t k = b * bs; k < (b + 1) * bs && k < K; ++k) {
+                float v = (float)load_elem(A, a_dtype, m * K + k);
+                float av = v < 0.0f ? -v : v;
+                if (av > amax) amax = av;
+            }
+            float s = amax / 127.0f;
+            sa[m * nb + b] = s;
+            for (int64_t k = b * bs; k < (b + 1) * bs; ++k) {
+                int8_t q = 0;
+                if (k < K && s != 0.0f) {
+                    float r = rintf((float)load_elem(A, a_dtype, m * K + k) / s);
+                    if (r > 127.0f) r = 127.0f;
+                    if (r < -127.0f) r = -127.0f;
+                    q = (int8_t)r;
+                }
+                if (k < K) aq[m * K + k] = q;
+            }
+        }
+}
+
+int orc_mnb_matmul_int8a(const void* A, int a_dtype, int64_t M, int64_t K, const uint8_t* packed,
+                         const void* scales, int s_dtype, const uint8_t* zp, int64_t N, int bits, int bs,
+                         double* Y, int threads) {
+    if (check_format(bits, bs) || M < 0 || K < 0 || N < 0) return 1;
+    int64_t nb = n_blocks(K, bs);
+    int8_t* aq = (int8_t*)malloc((size_t)(M * K > 0 ? M * K : 1));
+    float* sa = (float*)malloc(sizeof(float) * (size_t)(M * nb > 0 ? M * nb : 1));
+    if (!aq || !sa) { free(aq); free(sa); return 1; }
+    orc_quantize_a_int8(A, a_dtype, M, K, bs, aq, sa);
+    int64_t rb = nb * blob_bytes(bits, bs), zr = zp_row_bytes(nb, bits);
+    if (threads < 1) threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* row = packed + n * rb;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                int64_t z = zp ? stream_code(zp + n * zr, b, bits) : (1 << (bits - 1));
+                int64_t isum = 0;
+                for (int64_t k = b * bs; k < (b + 1) * bs && k < K; ++k)
+                    isum += (int64_t)aq[m * K + k] * (stream_code(row, k, bits) - z);
+                acc += (double)sa[m * nb + b] * load_elem(scales, s_dtype, n * nb + b) * (double)isum;
+            }
+            Y[m * N + n] = acc;
+        }
+    }
+    free(aq);
+    free(sa);
+    return 0;
+}
+
 /* ------------------------------------------------------------ routing */
 
 /* Top-k by fp32 logit value: repeatedly take the largest unselected logit; a

@@ -223,6 +223,64 @@ def test_partial_block_equals_zero_padded_k(K, Kpad, bs):
     assert np.array_equal(a, b)
 
 
+# ------------------------------------------- int8 activation compute (accuracy_level=4)
+
+@pytest.mark.parametrize("a_dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_int8_activation_quantisation_matches_binary32_numpy(a_dtype, bs):
+    """aq = rint(a / (amax / 127)) in binary32 per (row, block), clamped to +-127; a
+    zero block gives scale 0 and codes 0; a partial last block uses its K entries."""
+    g = wl.rng(zlib.crc32(repr(("q8", a_dtype, bs)).encode()))
+    M, K = 5, 3 * bs + 17
+    A = wl.normal(g, (M, K), a_dtype)
+    Af = as_f64(A, a_dtype).reshape(M, K).astype(np.float32)
+    Af[2, :bs] = 0.0
+    A = wl.cast(Af, a_dtype)
+    Af = as_f64(A, a_dtype).reshape(M, K).astype(np.float32)
+    aq, sa = oracle.quantize_a_int8(A, a_dtype, K, bs)
+    nb = oracle.n_blocks(K, bs)
+    for b in range(nb):
+        blk = Af[:, b * bs:(b + 1) * bs]
+        amax = np.max(np.abs(blk), axis=1).astype(np.float32)
+        s = (amax / np.float32(127.0)).astype(np.float32)
+        assert np.array_equal(sa[:, b], s)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.where(s[:, None] != 0, np.rint(blk / s[:, None]), 0).astype(np.float32)
+        assert np.array_equal(aq[:, b * bs:(b + 1) * bs], np.clip(q, -127, 127).astype(np.int8))
+    assert np.all(sa[2, 0] == 0) and np.all(aq[2, :bs] == 0)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_int8_activation_matmul_is_exact_for_127_scaled_integers(bits):
+    """Activations that are integers with a block maximum of exactly 127 quantise to
+    themselves (scale 1), so the int8 mode equals the exact matmul."""
+    g = wl.rng(31 + bits)
+    M, N, K, bs = 3, 20, 256, 64
+    A = g.integers(-127, 128, size=(M, K)).astype(np.float32)
+    A[:, ::bs] = 127.0
+    packed, scales, zp = wl.quantized_weight(g, N, K, bits, bs, with_zp=True)
+    exact = oracle.mnb_matmul(A, "f32", packed, scales, "f32", zp, N, K, bits, bs)
+    q8 = oracle.mnb_matmul_int8a(A, "f32", packed, scales, "f32", zp, N, K, bits, bs)
+    assert np.allclose(q8, exact, rtol=1e-13, atol=1e-12)
+
+
+def test_int8_activation_matmul_against_quantise_then_expand():
+    """Brute force: quantise A (the pinned step above), expand both operands to fp64 and
+    multiply; equal to the blockwise-integer formula up to fp64 rounding."""
+    g = wl.rng(33)
+    M, N, K, bs, bits = 4, 9, 200, 32, 3
+    A = wl.normal(g, (M, K), "bf16")
+    packed, scales, _ = wl.quantized_weight(g, N, K, bits, bs, "bf16")
+    aq, sa = oracle.quantize_a_int8(A, "bf16", K, bs)
+    Adq = aq.astype(np.float64) * np.repeat(sa.astype(np.float64), bs, axis=1)[:, :K]
+    W = oracle.dequantize(packed, scales, "bf16", None, N, K, bits, bs)
+    q8 = oracle.mnb_matmul_int8a(A, "bf16", packed, scales, "bf16", None, N, K, bits, bs)
+    assert np.allclose(q8, Adq @ W.T, rtol=1e-12, atol=1e-12)
+    # and it stays within int8 quantisation distance of the exact result
+    exact = oracle.mnb_matmul(A, "bf16", packed, scales, "bf16", None, N, K, bits, bs)
+    assert np.max(np.abs(q8 - exact)) < 0.05 * np.sqrt(np.mean(exact ** 2))
+
+
 # ---------------------------------------------------------------- routing
 
 def test_route_equal_logits():
