@@ -121,6 +121,20 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
                       mnb_dtype y_dtype, void* workspace, size_t workspace_bytes,
                       mnb_stream_t stream);
 
+/* MatMulNBits with int8 activation compute, the accuracy_level=4 mode of the
+ * K01 contract ("Qwen3 Missing-Kernel Implementation Plan", row K01), as an
+ * explicitly selected entry point (mnb_matmul never quantises activations).
+ * Each block of block_size activations of a row of A is quantised
+ * symmetrically: sa = max|a| / 127 (binary32 division; 0 for an all-zero
+ * block), aq = rint(a / sa) (binary32 quotient, ties to even) clamped to
+ * [-127, 127]; then Y[m, n] = sum_b sa_b * scale_b * sum_{k in b} aq_k
+ * (code_k - zp_b), the inner sums exact in integers.  Same arguments, layouts
+ * and errors as mnb_matmul (no workspace); runs on CUDA cores for any M. */
+mnb_status mnb_matmul_int8a(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
+                            const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                            const uint8_t* zero_points, int64_t N, int bits, int block_size, void* Y,
+                            mnb_dtype y_dtype, mnb_stream_t stream);
+
 /* ------------------------------------------------------------------- QMoE */
 
 /* Bytes of device workspace qmoe_forward needs: the routing tables, the

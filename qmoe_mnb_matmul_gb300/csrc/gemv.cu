@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         [&](int m) -> const void* {
             return m0 + m < a.M ? static_cast<const char*>(a.A) + (m0 + m) * a.K * esz : nullptr;
         },
-        tid, kConsumerWarps * 32);
+        tid, kConsumerWarps * 32, a.int8a ? 4 * a.bs / 32 : 0);
     consumer_sync();
 
     const int bs_shift = __ffs(a.bs) - 1;

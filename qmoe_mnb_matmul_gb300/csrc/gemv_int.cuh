@@ -110,9 +110,32 @@ __device__ __forceinline__ uint32_t digit_byte(int d, int lane) { return (static
 // zeros; `vec`: rows may be read with 16-byte loads.
 constexpr int kStageBatch = 4;
 
+// int8 activation image (the int8-activation compute mode): lanes of one
+// weight block (4 * bs / 32 adjacent items) share the block's amax; the
+// quantised codes rint(a / (amax / 127)) (binary32 division) go to the low
+// digits, the high digits stay zero, and the chunk factor is amax / 127.
+__device__ __forceinline__ void int8a_item(const float (&a)[8], int block_lanes, uint32_t (&wd)[4], int& vsum,
+                                           float& factor) {
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx = max(mx, __float_as_uint(a[j]) & 0x7FFFFFFFu);
+    for (int o = 1; o < block_lanes; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float sa = __uint_as_float(mx) / 127.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) wd[q] = 0u;
+    vsum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int v = sa != 0.0f ? static_cast<int>(fminf(fmaxf(rintf(a[j] / sa), -127.0f), 127.0f)) : 0;
+        wd[2 * (j & 1)] |= digit_byte(v, j >> 1);
+        vsum += v;
+    }
+    factor = sa;
+}
+
 template <int BATCH, typename RowFn>
 __device__ __forceinline__ void stage_image_b(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec,
-                                              RowFn row, int tid, int nthreads) {
+                                              RowFn row, int tid, int nthreads, int int8a_block_lanes = 0) {
     constexpr int kStageBatch = BATCH;
     const int total = MT * C * 4;
     for (int base = 0; base < total; base += nthreads * kStageBatch) {
@@ -157,24 +180,30 @@ __device__ __forceinline__ void stage_image_b(uint4* Q, int2* Corr, int MT, int 
             const bool live = item < total;
             const int i = item & 3, mc = item >> 2;
             const int m = live ? mc / C : 0, c = live ? mc - m * C : 0;
-            uint32_t mx = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mx = max(mx, __float_as_uint(a[u][j]) & 0x7FFFFFFFu);
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const int s = min(140 - static_cast<int>(mx >> 23), 126);  // |a| 2^s < 2^14 for the whole chunk
-            const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
             uint32_t wd[4] = {0u, 0u, 0u, 0u};  // even low, even high, odd low, odd high
             int vsum = 0;
+            float factor;
+            if (int8a_block_lanes) {
+                int8a_item(a[u], int8a_block_lanes, wd, vsum, factor);
+            } else {
+                uint32_t mx = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int v = __float2int_rn(a[u][j] * up);  // exact scaling, one rounding
-                const int d1 = (v + 128) >> 8;
-                const int d0 = v - d1 * 256;
-                const int odd = j & 1, lane = j >> 1;
-                wd[2 * odd] |= digit_byte(d0, lane);
-                wd[2 * odd + 1] |= digit_byte(d1, lane);
-                vsum += v;
+                for (int j = 0; j < 8; ++j) mx = max(mx, __float_as_uint(a[u][j]) & 0x7FFFFFFFu);
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const int s = min(140 - static_cast<int>(mx >> 23), 126);  // |a| 2^s < 2^14 for the whole chunk
+                const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int v = __float2int_rn(a[u][j] * up);  // exact scaling, one rounding
+                    const int d1 = (v + 128) >> 8;
+                    const int d0 = v - d1 * 256;
+                    const int odd = j & 1, lane = j >> 1;
+                    wd[2 * odd] |= digit_byte(d0, lane);
+                    wd[2 * odd + 1] |= digit_byte(d1, lane);
+                    vsum += v;
+                }
+                factor = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
             }
             vsum += __shfl_xor_sync(0xffffffffu, vsum, 1);
             vsum += __shfl_xor_sync(0xffffffffu, vsum, 2);
@@ -182,7 +211,7 @@ __device__ __forceinline__ void stage_image_b(uint4* Q, int2* Corr, int MT, int 
                 uint32_t* q = reinterpret_cast<uint32_t*>(Q + qbase(m, c, C));
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) q[qq * 32 * 4 + i] = wd[qq];
-                if (i == 0) Corr[m * C + c] = make_int2(vsum, static_cast<int>(static_cast<uint32_t>(127 - s) << 23));
+                if (i == 0) Corr[m * C + c] = make_int2(vsum, __float_as_int(factor));
             }
         }
     }
@@ -190,13 +219,15 @@ __device__ __forceinline__ void stage_image_b(uint4* Q, int2* Corr, int MT, int 
 
 // One item per thread when they all fit (the common decode case: a batch
 // would only add dead slots), else batches of kStageBatch.
+// int8a_block_lanes: 0 for the exact 15-bit image, else 4 * block_size / 32
+// (the int8 activation compute mode).
 template <typename RowFn>
 __device__ __forceinline__ void stage_image(uint4* Q, int2* Corr, int MT, int C, int64_t K, int dt, bool vec, RowFn row,
-                                            int tid, int nthreads) {
+                                            int tid, int nthreads, int int8a_block_lanes = 0) {
     if (MT * C * 4 <= nthreads)
-        stage_image_b<1>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads);
+        stage_image_b<1>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads, int8a_block_lanes);
     else
-        stage_image_b<kStageBatch>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads);
+        stage_image_b<kStageBatch>(Q, Corr, MT, C, K, dt, vec, row, tid, nthreads, int8a_block_lanes);
 }
 
 }  // namespace gemv_int

@@ -28,6 +28,7 @@ struct GemvArgs {
     int chunks;            // C = nb * bs / 32 (32 codes per chunk)
     int a_vec;             // activation rows may be read with 16-byte loads
     int prefetch_all;      // prefetch the CTA's whole row range into L2 before the dependency wait
+    int int8a;             // int8 activation compute: A quantised per (row, block) to int8
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the

@@ -182,3 +182,53 @@ def test_non_canonical_padding_is_ignored():
     A = wl.normal(g, (1, K))
     assert np.array_equal(run(A, "f32", canon, scales, "f32", None, N, K, 4, bs),
                           run(A, "f32", noisy, scales, "f32", None, N, K, 4, bs))
+
+
+# ------------------------------------------- int8 activation compute (accuracy_level=4)
+
+def run_int8a(A, a_dt, packed, scales, s_dt, zp, N, K, bits, bs, y_dt="f32"):
+    A_d = to_dev(A, a_dt)
+    M = A_d.numel() // K
+    Y, full = empty_guarded(M * N, y_dt)
+    mnb.mnb_matmul_int8a(A_d, to_dev(packed), to_dev(scales, s_dt), None if zp is None else to_dev(zp), N, bits, bs, Y,
+                         K=K, M=M)
+    torch.cuda.synchronize()
+    assert guards_intact(full), "write outside Y"
+    assert mnb.mnb_get_last_device_error() == 0
+    return to_f64(Y).reshape(M, N)
+
+
+@pytest.mark.parametrize("name,K,N", wl.QWEN3_1P7B_PROJECTIONS)
+def test_int8a_decode_projection(name, K, N):
+    g = wl.rng(seed("int8a", name))
+    A, packed, scales, _ = case(g, 1, K, N, 4, 32)
+    y = run_int8a(A, "f32", packed, scales, "f32", None, N, K, 4, 32)
+    assert_f32_close(y, oracle.mnb_matmul_int8a(A, "f32", packed, scales, "f32", None, N, K, 4, 32, threads=THREADS))
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("a_dt,M", [("f16", 1), ("bf16", 3), ("f32", 16), ("bf16", 33)])
+def test_int8a_formats_and_rows(bits, bs, a_dt, M):
+    """Every width and block size, 16-bit and fp32 activations, M up to 33 (the mode
+    runs on CUDA cores for any M), zero points, a partial last block."""
+    g = wl.rng(seed("int8a-fmt", bits, bs, a_dt, M))
+    K, N = 1000, 300
+    A, packed, scales, zp = case(g, M, K, N, bits, bs, a_dt, "f32", with_zp=True)
+    y = run_int8a(A, a_dt, packed, scales, "f32", zp, N, K, bits, bs)
+    assert_f32_close(y, oracle.mnb_matmul_int8a(A, a_dt, packed, scales, "f32", zp, N, K, bits, bs, threads=THREADS))
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_int8a_integer_data_is_bit_exact(bits):
+    """Integer activations whose every block reaches 127 quantise to themselves; with unit
+    scales and zero points 0 every partial sum is an integer below 2^24."""
+    g = wl.rng(seed("int8a-exact", bits))
+    N, K, bs, M = 200, 2048, 64, 2
+    codes = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    packed = oracle.pack_codes(codes, bits, bs)
+    zp = oracle.pack_zero_points(np.zeros((N, K // bs), np.uint8), bits)
+    Af = g.integers(-127, 128, size=(M, K)).astype(np.float32)
+    Af[:, ::bs] = 127.0
+    y = run_int8a(Af, "f32", packed, np.ones((N, K // bs), np.float32), "f32", zp, N, K, bits, bs)
+    assert np.array_equal(y, (Af.astype(np.int64) @ codes.astype(np.int64).T).astype(np.float64))
