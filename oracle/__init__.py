@@ -76,6 +76,7 @@ def _lib():
                                 P, I64, P, C],
                 "orc_quantize_int3": [P, C, I64, I64, C, C, P, P, P],
                 "orc_quantize_a_int8": [P, C, I64, I64, C, P, P],
+                "orc_gate_up_swiglu": [P, C, I64, I64, P, P, C, P, I64, C, C, C, P, C],
                 "orc_mnb_matmul_int8a": [P, C, I64, I64, P, P, C, P, I64, C, C, P, C],
                 "orc_round_to_half_bits": [P, I64, C, P],
             }
@@ -208,6 +209,20 @@ def mnb_matmul_int8a(A, a_dtype: str, packed, scales, s_dtype: str, zp, N: int, 
     out = np.zeros((M, N), np.float64)
     _check(_lib().orc_mnb_matmul_int8a(_ptr(A), DTYPES[a_dtype], M, K, _ptr(packed), _ptr(scales),
                                        DTYPES[s_dtype], _ptr(zp), N, bits, bs, _ptr(out), threads), "matmul_int8a")
+    return out
+
+
+def gate_up_swiglu(A, a_dtype: str, packed, scales, s_dtype: str, zp, I: int, K: int, bits: int, bs: int,
+                   layout: str = "interleaved", threads: int = 1) -> np.ndarray:
+    """fp64 H[M, I] = silu(A . Wg^T) * (A . Wu^T), gate/up rows of packed [2I, ...] in `layout`."""
+    A = _elem(A, a_dtype)
+    M = A.size // K if K else 0
+    packed = _c(packed, np.uint8)
+    scales = _elem(scales, s_dtype)
+    zp = _c(zp, np.uint8)
+    out = np.zeros((M, I), np.float64)
+    _check(_lib().orc_gate_up_swiglu(_ptr(A), DTYPES[a_dtype], M, K, _ptr(packed), _ptr(scales), DTYPES[s_dtype],
+                                     _ptr(zp), I, bits, bs, FC1_LAYOUTS[layout], _ptr(out), threads), "gate_up_swiglu")
     return out
 
 

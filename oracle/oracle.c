@@ -367,6 +367,46 @@ int orc_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts
 /* silu(g) * u = g * sigmoid(g) * u */
 static double swiglu(double g, double u) { return g / (1.0 + exp(-g)) * u; }
 
+/* The dense FFN's fused gate/up projection with SwiGLU (the gate+up GEMV of a
+ * Qwen3 decoder layer, the dense counterpart of the QMoE FC1): packed
+ * [2I, K] with the gate and up rows of pair p at rows 2p / 2p+1 (interleaved)
+ * or p / I+p (concatenated); Y[m, p] = swiglu(g, u) with g, u the two rows'
+ * products with A[m] (steps 1-4 of the matmul above, fp64, ascending k). */
+int orc_gate_up_swiglu(const void* A, int a_dtype, int64_t M, int64_t K, const uint8_t* packed,
+                       const void* scales, int s_dtype, const uint8_t* zp, int64_t I, int bits, int bs,
+                       int layout, double* Y, int threads) {
+    if (check_format(bits, bs) || M < 0 || K < 0 || I < 1) return 1;
+    if (layout != ORC_FC1_INTERLEAVED && layout != ORC_FC1_CONCAT) return 1;
+    int bad = 0;
+    if (threads < 1) threads = 1;
+#pragma omp parallel num_threads(threads)
+    {
+        double* wg = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        double* wu = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!wg || !wu) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t p = 0; p < I; ++p) {
+                int64_t rg = layout == ORC_FC1_INTERLEAVED ? 2 * p : p;
+                int64_t ru = layout == ORC_FC1_INTERLEAVED ? 2 * p + 1 : I + p;
+                dequant_row(packed, scales, s_dtype, zp, rg, K, bits, bs, wg);
+                dequant_row(packed, scales, s_dtype, zp, ru, K, bits, bs, wu);
+                for (int64_t m = 0; m < M; ++m) {
+                    double g = 0.0, u = 0.0;
+                    for (int64_t k = 0; k < K; ++k) g += load_elem(A, a_dtype, m * K + k) * wg[k];
+                    for (int64_t k = 0; k < K; ++k) u += load_elem(A, a_dtype, m * K + k) * wu[k];
+                    Y[m * I + p] = g / (1.0 + exp(-g)) * u;
+                }
+            }
+        }
+        free(wg);
+        free(wu);
+    }
+    return bad;
+}
+
 /* One QMoE FFN layer for the listed tokens (all T when tokens == NULL).
  * Expert tensors are stacked on a leading expert axis:
  *   fc1_w [E, 2I, H/bs, bs*fc1_bits/8], fc1_scales [E, 2I, H/bs], fc1_zp [E, 2I, ceil((H/bs)*fc1_bits/8)]

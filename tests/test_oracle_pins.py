@@ -223,6 +223,54 @@ def test_partial_block_equals_zero_padded_k(K, Kpad, bs):
     assert np.array_equal(a, b)
 
 
+# ----------------------------------------------- dense FFN gate/up with SwiGLU
+
+@pytest.mark.parametrize("layout", ["interleaved", "concat"])
+def test_gate_up_swiglu_is_swiglu_of_the_two_matmuls(layout):
+    """The fused projection equals silu(gate) * up of the plain matmul's gate and up
+    columns (the same fp64 sums; the exponential of libm against numpy's)."""
+    g = wl.rng(41)
+    M, K, I, bs, bits = 3, 160, 24, 32, 3
+    packed, scales, zp = wl.quantized_weight(g, 2 * I, K, bits, bs, "bf16", with_zp=True)
+    A = wl.normal(g, (M, K), "bf16")
+    Hh = oracle.gate_up_swiglu(A, "bf16", packed, scales, "bf16", zp, I, K, bits, bs, layout)
+    GU = oracle.mnb_matmul(A, "bf16", packed, scales, "bf16", zp, 2 * I, K, bits, bs)
+    gate = GU[:, 0::2] if layout == "interleaved" else GU[:, :I]
+    up = GU[:, 1::2] if layout == "interleaved" else GU[:, I:]
+    assert np.allclose(Hh, gate / (1 + np.exp(-gate)) * up, rtol=1e-14, atol=1e-14)
+
+
+def test_gate_up_swiglu_unit_rows_closed_form():
+    """Gate row p = unit vector e_p, up row p = 2 e_p (interleaved, unit scales): the
+    output is silu(a_p) * 2 a_p."""
+    K = I = 32
+    bits, bs = 4, 32
+    z = 1 << (bits - 1)
+    codes = np.full((2 * I, K), z, np.uint8)
+    for p in range(I):
+        codes[2 * p, p] = z + 1
+        codes[2 * p + 1, p] = z + 2
+    packed = oracle.pack_codes(codes, bits, bs)
+    a = np.linspace(-2, 2, K).astype(np.float32).reshape(1, K)
+    Hh = oracle.gate_up_swiglu(a, "f32", packed, np.ones((2 * I, 1), np.float32), "f32", None, I, K, bits, bs)
+    x = a.astype(np.float64)[0]
+    assert np.allclose(Hh[0], x / (1 + np.exp(-x)) * 2 * x, rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 5, 6, 7, 8])
+def test_brute_force_other_widths(bits):
+    """The matmul at the widths the row-local LSB-first format allows beyond 3 and 4."""
+    g = wl.rng(42 + bits)
+    N, M, bs = 5, 2, 32
+    K = bs + 11
+    packed, scales, zp, W = _case(g, N, K, bits, bs, True, "f32")
+    assert np.array_equal(oracle.dequantize(packed, scales, "f32", zp, N, K, bits, bs), W)
+    A = wl.normal(g, (M, K))
+    Y = oracle.mnb_matmul(A, "f32", packed, scales, "f32", zp, N, K, bits, bs)
+    prod = A.astype(np.float64).reshape(M, 1, K) * W.reshape(1, N, K)
+    assert np.array_equal(Y, np.cumsum(prod, axis=2)[:, :, -1])
+
+
 # ------------------------------------------- int8 activation compute (accuracy_level=4)
 
 @pytest.mark.parametrize("a_dtype", ["f32", "f16", "bf16"])
