@@ -181,7 +181,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     consumer_sync();
 
     const int bs_shift = __ffs(a.bs) - 1;
-    constexpr int kZImplicit = 1 << (BITS - 1);
+    // BITS == 0: any width 1..8 given at run time (codes read straight from shared memory)
+    const int bits_rt = BITS ? BITS : a.bits;
+    const int kZImplicit = 1 << (bits_rt - 1);
     int st = 0;
     uint32_t phase = 0;
     for (int blk = b_first; blk < b_last; ++blk) {
@@ -226,15 +228,26 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                     }
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        uint32_t w[BITS];
-                        gemv::load_chunk<BITS>(wrow[r], c, w);
                         const float sc = to_f32(srow[r][b]);
                         int z = kZImplicit;
-                        if constexpr (decltype(has_zp)::value) z = gemv::zero_point_code<BITS>(zrow[r], b);
+                        if constexpr (BITS == 0) {
+                            if constexpr (decltype(has_zp)::value) z = zero_point_any(zrow[r], b, bits_rt);
+                            uint32_t lo[4], hi[4];
+                            codes_any(wrow[r] + c * 4 * bits_rt, bits_rt, lo, hi);
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const int T = chunk_dot<BITS>(w, q[m]) - z * V[m];
-                            acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                            for (int m = 0; m < MT; ++m) {
+                                const int T = chunk_dot_bytes(lo, hi, q[m]) - z * V[m];
+                                acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                            }
+                        } else {
+                            uint32_t w[BITS];
+                            gemv::load_chunk<BITS>(wrow[r], c, w);
+                            if constexpr (decltype(has_zp)::value) z = gemv::zero_point_code<BITS>(zrow[r], b);
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                const int T = chunk_dot<BITS>(w, q[m]) - z * V[m];
+                                acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                            }
                         }
                     }
                 }
@@ -294,7 +307,8 @@ struct Shape {
     bool prefetch_all = false;
 };
 
-Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups) {
+Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups,
+                 int force_r = 0) {
     const int64_t align = row_align(row_bytes, nb, ssize);
     const int64_t row_total = row_bytes + int64_t(nb) * ssize;
     const bool small = N * row_total <= kPrefetchAllBytes;
@@ -308,7 +322,7 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         int64_t rpw = cdiv<int64_t>(N, ctas * kConsumerWarps);
         rpw = rpw <= 2 ? rpw : rpw <= 4 ? 4 : cdiv<int64_t>(rpw, 2) * 2;  // 1, 2, 4, then even
         while ((rpw * kConsumerWarps) % align != 0) ++rpw;
-        const int R = rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
+        const int R = force_r ? force_r : rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
         const int64_t RC = rpw * kConsumerWarps;
         const Plan p = make_plan(MT, C, static_cast<int>(RC), row_bytes, nb, ssize, 1);
         if (rpw <= 8 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
@@ -324,6 +338,7 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     double best_cost = -1;
     for (int R : {4, 2, 1}) {
         if (MT == 4 && R == 4) continue;
+        if (force_r && R != force_r) continue;
         const int RC = kConsumerWarps * R;
         if (RC % align != 0) continue;
         const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
@@ -378,22 +393,32 @@ cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t str
 
 template <int BITS, int ST, int MT>
 cudaError_t launch_r(const GemvArgs& a, const Shape& sh, bool pdl, cudaStream_t stream) {
-    if constexpr (MT < 4) {
-        if (sh.R == 4) return launch_typed<BITS, ST, MT, 4>(a, sh, pdl, stream);
+    if constexpr (BITS == 0) {  // any width: one register tile (the shape picks R = 2)
+        return launch_typed<0, ST, MT, 2>(a, sh, pdl, stream);
+    } else {
+        if constexpr (MT < 4) {
+            if (sh.R == 4) return launch_typed<BITS, ST, MT, 4>(a, sh, pdl, stream);
+        }
+        if (sh.R == 2) return launch_typed<BITS, ST, MT, 2>(a, sh, pdl, stream);
+        return launch_typed<BITS, ST, MT, 1>(a, sh, pdl, stream);
     }
-    if (sh.R == 2) return launch_typed<BITS, ST, MT, 2>(a, sh, pdl, stream);
-    return launch_typed<BITS, ST, MT, 1>(a, sh, pdl, stream);
 }
 
 template <int BITS, int ST>
 cudaError_t launch_mt(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t stream) {
-    const int MT = pick_mt(a.M);
+    // any width: at most two activation rows per pass (the code extraction takes the registers)
+    const int MT = BITS == 0 ? std::min(pick_mt(a.M), 2) : pick_mt(a.M);
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
-    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups);
-    switch (MT) {
-        case 1: return launch_r<BITS, ST, 1>(a, sh, pdl, stream);
-        case 2: return launch_r<BITS, ST, 2>(a, sh, pdl, stream);
-        default: return launch_r<BITS, ST, 4>(a, sh, pdl, stream);
+    const Shape sh =
+        pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups, BITS == 0 ? 2 : 0);
+    if constexpr (BITS == 0) {
+        return MT == 1 ? launch_r<0, ST, 1>(a, sh, pdl, stream) : launch_r<0, ST, 2>(a, sh, pdl, stream);
+    } else {
+        switch (MT) {
+            case 1: return launch_r<BITS, ST, 1>(a, sh, pdl, stream);
+            case 2: return launch_r<BITS, ST, 2>(a, sh, pdl, stream);
+            default: return launch_r<BITS, ST, 4>(a, sh, pdl, stream);
+        }
     }
 }
 
@@ -412,6 +437,11 @@ size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype) 
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream) {
+    if (a.bits != 3 && a.bits != 4) {  // widths 1, 2, 5..8
+        if (scale_dtype == kF32) return launch_mt<0, kF32>(a, sm_count, pdl, stream);
+        if (scale_dtype == kF16) return launch_mt<0, kF16>(a, sm_count, pdl, stream);
+        return launch_mt<0, kBF16>(a, sm_count, pdl, stream);
+    }
     if (a.bits == 4) {
         if (scale_dtype == kF32) return launch_mt<4, kF32>(a, sm_count, pdl, stream);
         if (scale_dtype == kF16) return launch_mt<4, kF16>(a, sm_count, pdl, stream);

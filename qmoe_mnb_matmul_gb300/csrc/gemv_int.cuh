@@ -97,6 +97,57 @@ __device__ __forceinline__ int chunk_dot(const uint32_t (&w)[BITS], const uint4 
     return (se1 * 256 + se0) + ((so1 * 256 + so0) >> (BITS == 4 ? 4 : 3));
 }
 
+// Any width 1..8 (the row-local LSB-first format beyond 3 and 4 bits): code j
+// of the chunk whose 4 * bits bytes start at `chunk` (4-byte aligned, shared
+// memory), read through at most two aligned words.
+__device__ __forceinline__ uint32_t code_any(const uint8_t* chunk, int j, int bits) {
+    const uint32_t bit = static_cast<uint32_t>(j * bits);
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(chunk) + (bit >> 5);
+    const uint32_t off = bit & 31;
+    const uint32_t hi = off + bits > 32 ? wp[1] : 0u;  // only a code that crosses a word reads the next one
+    return __funnelshift_r(wp[0], hi, off) & ((1u << bits) - 1u);
+}
+
+// Any width: the chunk's codes as plain bytes, code word g's even codes in
+// lo[g] and its odd codes in hi[g] (no position factor).
+__device__ __forceinline__ void codes_any(const uint8_t* chunk, int bits, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        lo[g] = 0;
+        hi[g] = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            lo[g] |= code_any(chunk, 8 * g + 2 * b, bits) << (8 * b);
+            hi[g] |= code_any(chunk, 8 * g + 2 * b + 1, bits) << (8 * b);
+        }
+    }
+}
+
+// chunk_dot on code bytes from codes_any.
+__device__ __forceinline__ int chunk_dot_bytes(const uint32_t (&lo)[4], const uint32_t (&hi)[4], const uint4 (&q)[4]) {
+    const uint32_t q0[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+    const uint32_t q1[4] = {q[1].x, q[1].y, q[1].z, q[1].w};
+    const uint32_t q2[4] = {q[2].x, q[2].y, q[2].z, q[2].w};
+    const uint32_t q3[4] = {q[3].x, q[3].y, q[3].z, q[3].w};
+    int se0 = 0, se1 = 0, so0 = 0, so1 = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        se0 = dp4a_su(q0[g], lo[g], se0);
+        se1 = dp4a_su(q1[g], lo[g], se1);
+        so0 = dp4a_su(q2[g], hi[g], so0);
+        so1 = dp4a_su(q3[g], hi[g], so1);
+    }
+    return (se1 * 256 + se0) + (so1 * 256 + so0);
+}
+
+// Zero-point code of block b in a packed zero-point row of any width.
+__device__ __forceinline__ int zero_point_any(const uint8_t* zrow, int b, int bits) {
+    const int bit = b * bits, byte = bit >> 3, sh = bit & 7;
+    uint32_t v = zrow[byte];
+    if (sh + bits > 8) v |= static_cast<uint32_t>(zrow[byte + 1]) << 8;
+    return static_cast<int>((v >> sh) & ((1u << bits) - 1u));
+}
+
 // Signed 8-bit digit d as the byte of lane `lane` (0..3).
 __device__ __forceinline__ uint32_t digit_byte(int d, int lane) { return (static_cast<uint32_t>(d) & 0xFFu) << (8 * lane); }
 

@@ -20,6 +20,9 @@ constexpr int64_t kTcMinRows = 16;
 
 bool valid_dtype(int d) { return d == MNB_F32 || d == MNB_F16 || d == MNB_BF16; }
 bool valid_bits(int b) { return b == 3 || b == 4; }
+// mnb_matmul / mnb_matmul_int8a: every width of the row-local LSB-first format
+// (3 and 4 on every path; 1, 2 and 5..8 on the CUDA-core path for any M)
+bool valid_bits_any(int b) { return b >= 1 && b <= 8; }
 bool valid_bs(int bs) { return bs == 32 || bs == 64 || bs == 128; }
 size_t dsize(int d) { return d == MNB_F32 ? 4 : 2; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -115,8 +118,9 @@ mnb_status mnb_matmul_workspace_size(int64_t M, int64_t K, int64_t N, int bits, 
                                      mnb_dtype a_dtype, size_t* bytes) {
     if (!bytes) return MNB_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || N < 1 || !valid_dtype(a_dtype)) return MNB_ERR_INVALID_ARG;
-    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (!valid_bits_any(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     *bytes = 0;
+    if (!valid_bits(bits)) return MNB_OK;  // other widths run on CUDA cores without a workspace
     // The tensor-core path splits K when its output tiles cannot fill the GPU;
     // the size is planned for a 152-SM GB300 so that it depends only on the
     // arguments (a call given less workspace splits less, or not at all).
@@ -131,7 +135,7 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
     if (!A || !B_packed || !scales || !Y) return MNB_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || N < 1) return MNB_ERR_INVALID_ARG;
     if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
-    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (!valid_bits_any(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     if (scale_dtype != MNB_F32 && scale_dtype != a_dtype) return MNB_ERR_UNSUPPORTED;
     if (!aligned(B_packed, 16) || !aligned(scales, 16) || !aligned(A, dsize(a_dtype)) ||
         !aligned(Y, dsize(y_dtype)))
@@ -146,9 +150,9 @@ mnb_status mnb_matmul(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, co
     if (sms <= 0) return MNB_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    // Tensor-core path: fp16/bf16 activations, enough rows to fill an MMA
-    // column block, and a TMA-compatible activation matrix.
-    if (a_dtype != MNB_F32 && M >= kTcMinRows && K % 8 == 0 && aligned(A, 16)) {
+    // Tensor-core path: 3- and 4-bit weights, fp16/bf16 activations, enough
+    // rows to fill an MMA column block, and a TMA-compatible activation matrix.
+    if (valid_bits(bits) && a_dtype != MNB_F32 && M >= kTcMinRows && K % 8 == 0 && aligned(A, 16)) {
         GemmTcArgs g = {};
         g.A = A;
         g.a_dtype = a_dtype;
@@ -199,7 +203,7 @@ mnb_status mnb_matmul_int8a(const void* A, mnb_dtype a_dtype, int64_t M, int64_t
     if (!A || !B_packed || !scales || !Y) return MNB_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || N < 1) return MNB_ERR_INVALID_ARG;
     if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
-    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (!valid_bits_any(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     if (scale_dtype != MNB_F32 && scale_dtype != a_dtype) return MNB_ERR_UNSUPPORTED;
     if (!aligned(B_packed, 16) || !aligned(scales, 16) || !aligned(A, dsize(a_dtype)) ||
         !aligned(Y, dsize(y_dtype)))
@@ -412,7 +416,7 @@ mnb_status mnb_validate_host(const uint8_t* B_packed, const void* scales, mnb_dt
                              const uint8_t* zero_points, int64_t N, int64_t K, int bits, int block_size) {
     if (!B_packed || !scales || N < 1 || K < 1) return MNB_ERR_INVALID_ARG;
     if (!valid_dtype(scale_dtype)) return MNB_ERR_INVALID_ARG;
-    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (!valid_bits_any(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
     ProjBytes pb;
     if (!proj_bytes(N, K, bits, block_size, scale_dtype, &pb)) return MNB_ERR_SIZE_OVERFLOW;
     for (int64_t i = 0; i < N * pb.nb; ++i) {

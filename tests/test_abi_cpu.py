@@ -55,8 +55,8 @@ def test_matmul_metadata_errors(lib):
     assert call_matmul(lib, K=0) == INVALID
     assert call_matmul(lib, N=-1) == INVALID
     assert call_matmul(lib, a_dt=7) == INVALID
-    assert call_matmul(lib, bits=5) == UNSUPPORTED
-    assert call_matmul(lib, bits=2) == UNSUPPORTED
+    assert call_matmul(lib, bits=9) == UNSUPPORTED   # widths 1..8 only
+    assert call_matmul(lib, bits=0) == UNSUPPORTED
     assert call_matmul(lib, bs=16) == UNSUPPORTED
     assert call_matmul(lib, bs=256) == UNSUPPORTED
     assert call_matmul(lib, a_dt=1, s_dt=2) == UNSUPPORTED  # scale dtype must be f32 or the activation dtype
@@ -71,7 +71,9 @@ def test_workspace_size_queries(lib):
     assert lib.mnb_matmul_workspace_size(1, 2048, 4096, 4, 32, 0, ctypes.byref(n)) == OK
     assert n.value == 0
     assert lib.mnb_matmul_workspace_size(1, 2048, 4096, 4, 32, 0, None) == INVALID
-    assert lib.mnb_matmul_workspace_size(1, 2048, 4096, 6, 32, 0, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.mnb_matmul_workspace_size(1, 2048, 4096, 9, 32, 0, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.mnb_matmul_workspace_size(64, 2048, 4096, 6, 32, 1, ctypes.byref(n)) == OK  # CUDA cores: none
+    assert n.value == 0
     assert lib.qmoe_workspace_size(1, 2048, 768, 128, 8, 1, ctypes.byref(n)) == OK
     assert n.value > 0
     small = n.value

@@ -232,3 +232,26 @@ def test_int8a_integer_data_is_bit_exact(bits):
     Af[:, ::bs] = 127.0
     y = run_int8a(Af, "f32", packed, np.ones((N, K // bs), np.float32), "f32", zp, N, K, bits, bs)
     assert np.array_equal(y, (Af.astype(np.int64) @ codes.astype(np.int64).T).astype(np.float64))
+
+
+# ---------------------------------------- widths beyond 3 and 4 (row-local LSB-first)
+
+@pytest.mark.parametrize("bits", [1, 2, 5, 6, 7, 8])
+@pytest.mark.parametrize("bs,with_zp,a_dt,M", [(32, False, "f32", 1), (64, True, "bf16", 3), (128, True, "f16", 20)])
+def test_other_widths(bits, bs, with_zp, a_dt, M):
+    """mnb_matmul at widths 1, 2, 5..8 (the CUDA-core path for any M; M = 20 with 16-bit
+    activations would take the tensor cores at widths 3 and 4)."""
+    g = wl.rng(seed("widths", bits, bs, with_zp, a_dt, M))
+    K, N = 1000, 257
+    A, packed, scales, zp = case(g, M, K, N, bits, bs, a_dt, "f32", with_zp=with_zp)
+    y = run(A, a_dt, packed, scales, "f32", zp, N, K, bits, bs)
+    assert_f32_close(y, oracle.mnb_matmul(A, a_dt, packed, scales, "f32", zp, N, K, bits, bs, threads=THREADS))
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_other_widths_int8a(bits):
+    g = wl.rng(seed("widths-int8a", bits))
+    K, N, bs = 2048, 512, 64
+    A, packed, scales, zp = case(g, 2, K, N, bits, bs, "bf16", "f32", with_zp=True)
+    y = run_int8a(A, "bf16", packed, scales, "f32", zp, N, K, bits, bs)
+    assert_f32_close(y, oracle.mnb_matmul_int8a(A, "bf16", packed, scales, "f32", zp, N, K, bits, bs, threads=THREADS))
