@@ -43,8 +43,9 @@
  *                offset-4 decoding (code - 4) * scale).
  *   Dequantised weight: w[n, k] = scale[n, k/bs] * (code[n, k] - zp[n, k/bs]).
  *
- * Supported set.  bits in {3, 4}; block_size in {32, 64, 128}; activation and
- * output dtypes f32 / f16 / bf16 for mnb_matmul (f16 / bf16 for QMoE); scale
+ * Supported set.  bits in {3, 4} (mnb_matmul and mnb_matmul_int8a: 1..8, the
+ * widths other than 3 and 4 on CUDA cores); block_size in {32, 64, 128};
+ * activation and output dtypes f32 / f16 / bf16 for mnb_matmul (f16 / bf16 for QMoE); scale
  * dtype f32 or equal to the activation dtype (QMoE: equal).  Alignment:
  * B_packed and the scales (mnb_matmul; QMoE: fc1_w, fc2_w, fc1_scales and
  * fc2_scales) must be 16-byte aligned, the QMoE workspace 256-byte aligned,
@@ -134,6 +135,23 @@ mnb_status mnb_matmul_int8a(const void* A, mnb_dtype a_dtype, int64_t M, int64_t
                             const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
                             const uint8_t* zero_points, int64_t N, int bits, int block_size, void* Y,
                             mnb_dtype y_dtype, mnb_stream_t stream);
+
+/* The dense FFN's fused gate/up projection with SwiGLU, the dense
+ * counterpart of the QMoE FC1 (the Qwen3 decoder MLP's gate and up
+ * projections share their input): B_packed holds 2I rows [2I, nb, blob]
+ * (scales [2I, nb], zero_points [2I, ...] or NULL, layouts as above), the gate
+ * and up rows of pair i at rows 2i / 2i+1 (MNB_FC1_INTERLEAVED) or i / I+i
+ * (MNB_FC1_CONCAT);
+ *   Y[m, i] = silu(g) * up,  g = A[m] . Wgate_i^T,  up = A[m] . Wup_i^T,
+ * Y [M, I] in y_dtype.  bits 3 or 4.  One launch: tensor cores for M >= 16
+ * with f16/bf16 activations and y_dtype == a_dtype (K a multiple of 8, A
+ * 16-byte aligned), CUDA cores otherwise (there the concatenated
+ * layout needs rows and scale rows of whole 16-byte units, else
+ * MNB_ERR_UNSUPPORTED).  Other arguments, alignment and errors as mnb_matmul. */
+mnb_status mnb_gate_up_swiglu(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
+                              const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                              const uint8_t* zero_points, int64_t I, int bits, int block_size,
+                              mnb_fc1_layout layout, void* Y, mnb_dtype y_dtype, mnb_stream_t stream);
 
 /* ------------------------------------------------------------------- QMoE */
 

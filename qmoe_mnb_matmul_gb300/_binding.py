@@ -40,6 +40,7 @@ _SIGNATURES = {
     "mnb_matmul_workspace_size": [_I64, _I64, _I64, _I, _I, _I, ctypes.POINTER(_SZ)],
     "mnb_matmul": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _P, _I, _P, _SZ, _P],
     "mnb_matmul_int8a": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _P, _I, _P],
+    "mnb_gate_up_swiglu": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _I, _P, _I, _P],
     "qmoe_workspace_size": [_I64, _I64, _I64, _I64, _I, _I, ctypes.POINTER(_SZ)],
     "qmoe_forward": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
                      _P, _P, _SZ, _P],
@@ -175,6 +176,25 @@ def mnb_matmul_int8a(A, B_packed, scales, zero_points, N, bits, block_size, Y, s
                                          _ptr(zero_points), N, bits, block_size, _ptr(Y), y_dtype, _stream(stream))
     if check:
         _check(st, "mnb_matmul_int8a")
+    return st
+
+
+def mnb_gate_up_swiglu(A, B_packed, scales, zero_points, I, bits, block_size, Y, stream=None, *,
+                       layout=FC1_INTERLEAVED, K=None, M=None, a_dtype=None, scale_dtype=None, y_dtype=None,
+                       check=True):
+    """Y[M, I] = silu(A . Wgate^T) * (A . Wup^T) from the fused gate/up weight [2I, K]."""
+    if K is None:
+        K = A.shape[-1]
+    if M is None:
+        M = A.numel() // K
+    a_dtype = _dtype_code(A) if a_dtype is None else a_dtype
+    scale_dtype = _dtype_code(scales) if scale_dtype is None else scale_dtype
+    y_dtype = _dtype_code(Y) if y_dtype is None else y_dtype
+    st = load_library().mnb_gate_up_swiglu(_ptr(A), a_dtype, M, K, _ptr(B_packed), _ptr(scales), scale_dtype,
+                                           _ptr(zero_points), I, bits, block_size, layout, _ptr(Y), y_dtype,
+                                           _stream(stream))
+    if check:
+        _check(st, "mnb_gate_up_swiglu")
     return st
 
 

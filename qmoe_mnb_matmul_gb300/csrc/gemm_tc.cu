@@ -16,6 +16,8 @@ MNB_SLICE_DECL(gemm_tc_fc1_b3)
 MNB_SLICE_DECL(gemm_tc_fc1_b4)
 #undef MNB_SLICE_DECL
 
+int grouped_tile_rows();
+
 namespace {
 
 constexpr int kBW = 128;  // weight rows per tile
@@ -147,6 +149,36 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Dense gate/up with SwiGLU on the tensor cores: the FC1 mode of the grouped
+// kernel over one "expert" (the whole matrix), plain activation-row tiles.
+cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int scale_dtype, int sm_count, bool pdl,
+                              cudaStream_t stream) {
+    TcArgs a = {};
+    a.M = g.M;
+    a.K = g.K;
+    a.rows = 2 * I;
+    a.B = g.B;
+    a.scales = g.scales;
+    a.zp = g.zp;
+    a.row_bytes = g.row_bytes;
+    a.nb = g.nb;
+    a.bs = g.bs;
+    a.zp_row_bytes = g.zp_row_bytes;
+    a.Y = g.Y;
+    a.y_dtype = g.y_dtype;
+    a.ld_y = I;
+    a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * I, kBW));
+    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(grouped_tile_rows())));
+    a.splits = 1;
+    a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK));
+    a.I = I;
+    a.inter = inter ? 1 : 0;
+    a.experts = 1;
+    const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m, sm_count));
+    auto fn = g.bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3;
+    return fn(scale_dtype, g.a_dtype, grouped_tile_rows(), 1, a, g.A, g.M, g.K, grid, pdl, stream);
 }
 
 // Grouped (QMoE) tiles: 256 routed rows of one expert.

@@ -154,17 +154,31 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             const int rc = block_rows(blk);
             uint8_t* W = Wst + st * plan.w_stage;
             uint8_t* Sd = Sst + st * plan.s_stage;
-            const int64_t wtot = rc * a.row_bytes, stot = int64_t(rc) * nb * sizeof(S);
-            const uint32_t wb = static_cast<uint32_t>(wtot) & ~15u, sb = static_cast<uint32_t>(stot) & ~15u;
-            const uint8_t* wsrc = a.B + n0 * a.row_bytes;
-            const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
-            // bytes past the last 16-byte multiple of a partial block: plain copies, published by the arrive below
-            if (wb < wtot) copy_bytes(W, wsrc, wb, wtot);
-            if (sb < stot) copy_bytes(Sd, ssrc, sb, stot);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&full[st], wb + sb);
-            if (wb) bulk_g2s(W, wsrc, wb, &full[st]);
-            if (sb) bulk_g2s(Sd, ssrc, sb, &full[st]);
+            if (a.swiglu && !a.fc1_inter) {
+                // concatenated gate/up halves: the block's pairs [n0/2, n0/2 + rc/2) of
+                // the gate rows, then the same pairs of the up rows (every copy whole
+                // 16-byte units: the launcher checks the row alignment)
+                const int64_t p0 = n0 / 2, np = rc / 2, ss = int64_t(nb) * sizeof(S);
+                const uint32_t wb = static_cast<uint32_t>(np * a.row_bytes), sb = static_cast<uint32_t>(np * ss);
+                mbar_arrive_expect_tx(&full[st], 2 * (wb + sb));
+                for (int up = 0; up < 2; ++up) {
+                    const int64_t r = up * a.pairs + p0;
+                    bulk_g2s(W + up * (RC / 2) * a.row_bytes, a.B + r * a.row_bytes, wb, &full[st]);
+                    bulk_g2s(Sd + up * (RC / 2) * ss, static_cast<const uint8_t*>(a.scales) + r * ss, sb, &full[st]);
+                }
+            } else {
+                const int64_t wtot = rc * a.row_bytes, stot = int64_t(rc) * nb * sizeof(S);
+                const uint32_t wb = static_cast<uint32_t>(wtot) & ~15u, sb = static_cast<uint32_t>(stot) & ~15u;
+                const uint8_t* wsrc = a.B + n0 * a.row_bytes;
+                const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
+                // bytes past the last 16-byte multiple of a partial block: plain copies, published by the arrive below
+                if (wb < wtot) copy_bytes(W, wsrc, wb, wtot);
+                if (sb < stot) copy_bytes(Sd, ssrc, sb, stot);
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&full[st], wb + sb);
+                if (wb) bulk_g2s(W, wsrc, wb, &full[st]);
+                if (sb) bulk_g2s(Sd, ssrc, sb, &full[st]);
+            }
             if (++st == NST) { st = 0; ++round; }
         }
         return;
@@ -206,9 +220,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int rl = min(r0 + r, w_end - 1);  // rows past the slice end recompute its last row
-                wrow[r] = W + int64_t(rl) * a.row_bytes;
-                srow[r] = Sc + rl * nb;
-                zrow[r] = a.zp ? a.zp + (n0 + rl) * a.zp_row_bytes : nullptr;
+                // concatenated gate/up: logical row 2i / 2i+1 sits in the gate / up half of the stage
+                const int sl = (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? RC / 2 + (rl >> 1) : (rl >> 1)) : rl;
+                wrow[r] = W + int64_t(sl) * a.row_bytes;
+                srow[r] = Sc + sl * nb;
+                const int64_t phys = (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? a.pairs : 0) + (n0 + rl) / 2 : n0 + rl;
+                zrow[r] = a.zp ? a.zp + phys * a.zp_row_bytes : nullptr;
             }
             // the chunk loop; HAS_ZP: explicit zero points (a uniform branch, taken once per block)
             auto chunks = [&](auto has_zp) {
@@ -257,16 +274,41 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             else
                 chunks(std::false_type{});
             // value q = r * MT + m; each total ends in one lane
-            constexpr int N = R * MT;
-            float part[N];
+            if (a.swiglu) {
+                // rows 2i, 2i+1 of the group are the gate and up rows of one pair:
+                // every lane gets every total, lane 0 stores silu(gate) * up
+                if constexpr (R % 2 == 0) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                    for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m];
-            const float total = warp_sum_transpose<N>(part);
-            if ((lane & (32 / N - 1)) == 0) {
-                const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
-                if (r0 + r < w_end && m0 + m < a.M) store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
+                        for (int m = 0; m < MT; ++m) acc[r][m] = warp_sum(acc[r][m]);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int pp = 0; pp < R / 2; ++pp) {
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                if (r0 + 2 * pp + 1 < w_end && m0 + m < a.M) {
+                                    const float gt = acc[2 * pp][m], up = acc[2 * pp + 1][m];
+                                    store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + (n0 + r0) / 2 + pp,
+                                                   gt / (1.0f + expf(-gt)) * up);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else {
+                constexpr int N = R * MT;
+                float part[N];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m];
+                const float total = warp_sum_transpose<N>(part);
+                if ((lane & (32 / N - 1)) == 0) {
+                    const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
+                    if (r0 + r < w_end && m0 + m < a.M)
+                        store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
+                }
             }
         }
         __syncwarp();
@@ -308,7 +350,7 @@ struct Shape {
 };
 
 Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups,
-                 int force_r = 0) {
+                 int force_r = 0, bool pairs = false) {
     const int64_t align = row_align(row_bytes, nb, ssize);
     const int64_t row_total = row_bytes + int64_t(nb) * ssize;
     const bool small = N * row_total <= kPrefetchAllBytes;
@@ -321,7 +363,8 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         const int64_t ctas = std::max<int64_t>(1, sm_count / mgroups);
         int64_t rpw = cdiv<int64_t>(N, ctas * kConsumerWarps);
         rpw = rpw <= 2 ? rpw : rpw <= 4 ? 4 : cdiv<int64_t>(rpw, 2) * 2;  // 1, 2, 4, then even
-        while ((rpw * kConsumerWarps) % align != 0) ++rpw;
+        if (pairs && rpw % 2) ++rpw;  // SwiGLU: every warp slice holds whole gate/up pairs
+        while ((rpw * kConsumerWarps) % (pairs ? 2 * align : align) != 0) ++rpw;
         const int R = force_r ? force_r : rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
         const int64_t RC = rpw * kConsumerWarps;
         const Plan p = make_plan(MT, C, static_cast<int>(RC), row_bytes, nb, ssize, 1);
@@ -339,8 +382,9 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
     for (int R : {4, 2, 1}) {
         if (MT == 4 && R == 4) continue;
         if (force_r && R != force_r) continue;
+        if (pairs && R == 1) continue;
         const int RC = kConsumerWarps * R;
-        if (RC % align != 0) continue;
+        if (RC % (pairs ? 2 * align : align) != 0) continue;
         const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
         const int64_t stage = p1.w_stage + p1.s_stage;
         const int64_t cap = std::max<int64_t>(112 * 1024, p1.fixed + 2 * stage);
@@ -409,8 +453,8 @@ cudaError_t launch_mt(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t st
     // any width: at most two activation rows per pass (the code extraction takes the registers)
     const int MT = BITS == 0 ? std::min(pick_mt(a.M), 2) : pick_mt(a.M);
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
-    const Shape sh =
-        pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups, BITS == 0 ? 2 : 0);
+    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups,
+                                BITS == 0 ? 2 : 0, a.swiglu != 0);
     if constexpr (BITS == 0) {
         return MT == 1 ? launch_r<0, ST, 1>(a, sh, pdl, stream) : launch_r<0, ST, 2>(a, sh, pdl, stream);
     } else {

@@ -29,6 +29,11 @@ struct GemvArgs {
     int a_vec;             // activation rows may be read with 16-byte loads
     int prefetch_all;      // prefetch the CTA's whole row range into L2 before the dependency wait
     int int8a;             // int8 activation compute: A quantised per (row, block) to int8
+    // dense gate/up with SwiGLU: N = 2 * pairs logical rows (gate i = 2i, up i =
+    // 2i + 1), stored in B interleaved (fc1_inter) or as gate rows then up rows;
+    // Y[m, i] = silu(gate_i) * up_i, y_ld = pairs
+    int swiglu, fc1_inter;
+    int64_t pairs;
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
@@ -105,6 +110,11 @@ struct TcArgs {
 
 // Rows of activations per tile in the grouped launches.
 int grouped_tile_rows();
+
+// Dense H[M, I] = silu(A . Wg^T) * (A . Wu^T) on the tensor cores (B holds the
+// 2I gate/up rows, interleaved or gate half then up half).
+cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int scale_dtype, int sm_count, bool pdl,
+                              cudaStream_t stream);
 
 // Grouped per-expert tensor-core GEMM over the m-tiles in the workspace:
 // fc1 gathers X rows by token and writes silu(gate)*up; otherwise a dense

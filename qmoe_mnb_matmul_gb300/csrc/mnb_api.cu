@@ -240,6 +240,79 @@ mnb_status mnb_matmul_int8a(const void* A, mnb_dtype a_dtype, int64_t M, int64_t
     return from_cuda(launch_gemv(a, scale_dtype, sms, pdl_enabled(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mnb_status mnb_gate_up_swiglu(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, const uint8_t* B_packed,
+                              const void* scales, mnb_dtype scale_dtype, const uint8_t* zero_points, int64_t I,
+                              int bits, int block_size, mnb_fc1_layout layout, void* Y, mnb_dtype y_dtype,
+                              mnb_stream_t stream) {
+    if (!A || !B_packed || !scales || !Y) return MNB_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || I < 1) return MNB_ERR_INVALID_ARG;
+    if (layout != MNB_FC1_INTERLEAVED && layout != MNB_FC1_CONCAT) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(a_dtype) || !valid_dtype(scale_dtype) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (scale_dtype != MNB_F32 && scale_dtype != a_dtype) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(B_packed, 16) || !aligned(scales, 16) || !aligned(A, dsize(a_dtype)) ||
+        !aligned(Y, dsize(y_dtype)))
+        return MNB_ERR_UNSUPPORTED;
+    ProjBytes pb;
+    int64_t tmp;
+    if (!proj_bytes(2 * I, K, bits, block_size, scale_dtype, &pb) || !mul_ok(M, K * 4, &tmp) ||
+        !mul_ok(M, I * 4, &tmp))
+        return MNB_ERR_SIZE_OVERFLOW;
+    if (2 * I > (int64_t(1) << 31)) return MNB_ERR_UNSUPPORTED;
+    const bool inter = layout == MNB_FC1_INTERLEAVED;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // tensor cores: 16-bit activations and output (the SwiGLU of two 16-bit
+    // products has no exact fp32 second pass)
+    if (a_dtype != MNB_F32 && y_dtype == a_dtype && M >= kTcMinRows && K % 8 == 0 && aligned(A, 16)) {
+        GemmTcArgs g = {};
+        g.A = A;
+        g.a_dtype = a_dtype;
+        g.M = M;
+        g.K = K;
+        g.B = B_packed;
+        g.scales = scales;
+        g.zp = zero_points;
+        g.N = 2 * I;
+        g.bits = bits;
+        g.bs = block_size;
+        g.nb = static_cast<int>(pb.nb);
+        g.row_bytes = pb.row_bytes;
+        g.zp_row_bytes = static_cast<int>(pb.zp_row);
+        g.Y = Y;
+        g.y_dtype = y_dtype;
+        return from_cuda(launch_gate_up_tc(g, I, inter, scale_dtype, sms, pdl_enabled(), st));
+    }
+    // CUDA cores: the gate and up halves of the concatenated layout are staged
+    // by separate bulk copies, which need whole 16-byte rows
+    if (!inter && (pb.row_bytes % 16 || (pb.nb * int64_t(dsize(scale_dtype))) % 16)) return MNB_ERR_UNSUPPORTED;
+    if (gemv_smem_bytes(M, K, bits, block_size, scale_dtype) == 0) return MNB_ERR_UNSUPPORTED;
+    GemvArgs a = {};
+    a.A = A;
+    a.a_dtype = a_dtype;
+    a.M = M;
+    a.K = K;
+    a.B = B_packed;
+    a.scales = scales;
+    a.zp = zero_points;
+    a.N = 2 * I;
+    a.bits = bits;
+    a.bs = block_size;
+    a.nb = static_cast<int>(pb.nb);
+    a.row_bytes = pb.row_bytes;
+    a.zp_row_bytes = static_cast<int>(pb.zp_row);
+    a.Y = Y;
+    a.y_dtype = y_dtype;
+    a.y_ld = I;
+    a.chunks = static_cast<int>(pb.nb * block_size / 32);
+    a.a_vec = aligned(A, 16) && (K * int64_t(dsize(a_dtype))) % 16 == 0;
+    a.swiglu = 1;
+    a.fc1_inter = inter ? 1 : 0;
+    a.pairs = I;
+    return from_cuda(launch_gemv(a, scale_dtype, sms, pdl_enabled(), st));
+}
+
 mnb_status mnb_unpack_codes(const uint8_t* B_packed, int64_t rows, int64_t K, int bits, int block_size,
                             uint8_t* codes, mnb_stream_t stream) {
     if (!B_packed || !codes || rows < 1 || K < 1) return MNB_ERR_INVALID_ARG;
