@@ -64,6 +64,56 @@ def assert_bf16_tc_close(y, ref, label: str = ""):
                            f"worst |y-r| = {np.max(np.abs(y - ref)):.3g}")
 
 
+def _swiglu_parts(g, u):
+    """h = silu(g) u, silu'(g), and the rms of g and u."""
+    g = np.asarray(g, np.float64)
+    u = np.asarray(u, np.float64)
+    sig = 1.0 / (1.0 + np.exp(-g))
+    h = g * sig * u
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    return g, u, h, dsilu, float(np.sqrt(np.mean(g * g))), float(np.sqrt(np.mean(u * u)))
+
+
+def swiglu_f32_error(y, g, u) -> float:
+    """The fp32 rule carried through h = silu(g) * u: the gate and up products may
+    each miss by F32_TOL of max(|value|, its rms), so h may miss by
+    |silu'(g)| |u| dg + |silu(g)| du to first order.  Returns max |y - h| over
+    that allowance (at 1x the rule); the floor keeps outputs where every term
+    vanishes from dividing by zero."""
+    y = np.asarray(y, np.float64)
+    if y.size == 0:
+        return 0.0
+    g, u, h, dsilu, rg, ru = _swiglu_parts(g, u)
+    allow = np.abs(dsilu * u) * np.maximum(np.abs(g), rg) + np.abs(g / (1.0 + np.exp(-g))) * np.maximum(np.abs(u), ru)
+    allow = allow + 1e-2 * rg * ru
+    return float(np.max(np.abs(y - h) / allow))
+
+
+def assert_swiglu_bf16_tc_close(y, g, u, label: str = ""):
+    """bf16 tensor-core SwiGLU outputs: the bf16 tensor-core rule on the gate and up
+    products (|d| <= 1e-2 + 2e-2 max(|value|, rms)) carried through silu(g) * u to
+    first order, plus the rounding of h to bf16 (2^-8 |h|).  Prints how many
+    outputs miss the plain elementwise 16-bit rule on h."""
+    y = np.asarray(y, np.float64)
+    g, u, h, dsilu, rg, ru = _swiglu_parts(g, u)
+    eg = HALF_ATOL + HALF_RTOL * np.maximum(np.abs(g), rg)
+    eu = HALF_ATOL + HALF_RTOL * np.maximum(np.abs(u), ru)
+    allow = np.abs(dsilu * u) * eg + np.abs(g / (1.0 + np.exp(-g))) * eu + 2.0 ** -8 * np.abs(h)
+    elementwise = half_violations(y, h)
+    print(f"[bf16 tensor-core SwiGLU rule] {label}: {elementwise} of {y.size} outputs outside the elementwise "
+          f"rule ({100.0 * elementwise / max(y.size, 1):.3f} %), worst fraction of the allowance "
+          f"{float(np.max(np.abs(y - h) / allow)) if y.size else 0.0:.3g}")
+    bad = np.abs(y - h) > allow
+    assert not bad.any(), f"{int(bad.sum())} of {bad.size} bf16 SwiGLU outputs out of tolerance"
+
+
+def assert_swiglu_f32_close(y, g, u, tol=F32_TOL, label: str = ""):
+    err = swiglu_f32_error(y, g, u) * tol
+    if label:
+        print(f"[{label}] SwiGLU-propagated fp32 error {err:.3g} (rule {tol})")
+    assert err <= tol, f"fp32 error through SwiGLU {err:.3g} > {tol}"
+
+
 def assert_close(y, ref, y_dtype: str, a_dtype: str | None = None, tensor_cores: bool = False, label: str = ""):
     """The rule of the output dtype: fp32 for fp32 outputs, the elementwise 16-bit
     rule for fp16 / bf16 outputs, and the bf16 tensor-core rule for bf16 outputs
