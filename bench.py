@@ -158,7 +158,7 @@ def ncu_traffic(kernel_sha: str):
 def kernel_source_sha():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemv.cu", "gemv_core.cuh", "gemv_int.cuh", "common.cuh"):
+    for f in ("gemv.cu", "gemv_impl.cuh", "gemv_core.cuh", "gemv_int.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "qmoe_mnb_matmul_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -374,6 +374,34 @@ def other_rows(torch, mnb, dev, groups=()):
             nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc)
         del Bs, Ss
     torch.cuda.empty_cache()
+    # f-1: the same decode GEMVs over the version-1 prepacked layout, and the prepack's own cost
+    for name, K, N, bits, bs, copies in () if not want("prepack") else (
+            ("lm_head", 2048, 151936, 3, 32, 2), ("lm_head", 2048, 151936, 3, 64, 2),
+            ("lm_head", 2048, 151936, 4, 32, 2), ("gate", 2048, 6144, 3, 64, 32)):
+        Bs, Ss = rnd_w(N, K, bits, copies), rnd_s(N, K, bs, copies)
+        n = mnb.mnb_prepack_size(N, K, bits, bs, mnb.F32, False)
+        bufs = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(copies)]
+        descs = [mnb.mnb_prepack(Bs[i], Ss[i], None, N, K, bits, bs, bufs[i], identity=i, stream=stream)
+                 for i in range(copies)]
+        torch.cuda.synchronize()
+        pus, pp10, pp90 = event_time_us(
+            torch, stream, lambda: mnb.mnb_prepack(Bs[0], Ss[0], None, N, K, bits, bs, bufs[0], identity=0,
+                                                   stream=stream), reps=5)
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        calls = [lambda i=i: mnb.mnb_matmul_prepacked(A, descs[i % copies], bufs[i % copies], Y, stream=stream)
+                 for i in range(16 if N > 100000 else 64)]
+        us, p10, p90 = graph_time(torch, stream, calls, reps=10 if N > 100000 else 20)
+        nbytes = (n - 128) + K * 4 + N * 4
+        src_bytes = matmul_bytes(1, K, N, bits, bs, 4, 4, 4) - K * 4 - N * 4
+        rows[f"decode_prepacked_int{bits}_{name}_bs{bs}"] = _row(
+            f"gemv_kernel<INT{bits}, prepacked>", f"M=1 K={K} N={N} INT{bits} bs{bs} fp32, version-1 prepacked "
+            f"({(n - 128) / 1e6:.1f} MB), {copies} weight copies", us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s",
+            hbm, "hbm", hsrc,
+            prepack_us=pus, prepack_gbs=(src_bytes + n) / (pus * 1e-6) / 1e9,
+            prepack_note="one mnb_prepack of one weight copy (reads the row-local weight, writes the layout)")
+        del Bs, Ss, bufs
+    torch.cuda.empty_cache()
     # a5: small-M and prefill GEMM (INT4 bs32, fp32 scales, bf16 activations and outputs)
     for name, K, N in () if not want("gemm") else (("qkv", 2048, 4096), ("gate", 2048, 6144), ("lm_head", 2048, 151936)):
         for M in (4, 16, 128, 512, 2048):
@@ -566,7 +594,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true", help="skip the prefill GEMM and QMoE measurements")
-    ap.add_argument("--rows", default="", help="comma-separated groups of other rows to run (decode, int3, gemm, "
+    ap.add_argument("--rows", default="", help="comma-separated groups of other rows to run (decode, int3, prepack, gemm, "
                     "qmoe, quant); default all")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run one small fixed invocation for an ncu capture and exit")

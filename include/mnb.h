@@ -153,6 +153,75 @@ mnb_status mnb_gate_up_swiglu(const void* A, mnb_dtype a_dtype, int64_t M, int64
                               const uint8_t* zero_points, int64_t I, int bits, int block_size,
                               mnb_fc1_layout layout, void* Y, mnb_dtype y_dtype, mnb_stream_t stream);
 
+/* ------------------------------------------------------ private prepack */
+
+/* A versioned private layout of one MatMulNBits weight (the "versioned
+ * private prepack, cache identity/lifetime and prepack-cost qualification"
+ * of "INT3 QMoE CUDA correctness baseline and Qwen experimental results", Not
+ * PR2-PR4 Completion; a vectorised private layout, which the same page's
+ * Review Fixes and Padding Experiment leaves open).  Version 1:
+ *   bytes [0, 128): the header, this struct (the rest zero);
+ *   row n at 128 + n * row_stride: the row's codes (C = nb * bs / 32 chunks of
+ *   4 * bits bytes), its nb scales, its packed zero points (if any), zeros up
+ *   to row_stride, a multiple of 16 bytes.
+ * INT4 chunks are stored as in the row-local layout.  An INT3 chunk's 96 bits
+ * are regrouped into three little-endian 32-bit words W0, W1, W2: byte b
+ * (b = 0..3) of word g < 3 holds code 8g+2b in bits 0-2 and code 8g+2b+1 in
+ * bits 3-5; bits 6-7 of byte b of W0 / W1 hold the low two bits of code 24+2b
+ * / 25+2b, and bit 6 / 7 of byte b of W2 their third bits.  Scales keep their
+ * dtype; zero points keep the row-local LSB-first packing.  Rows are then
+ * whole 16-byte units whatever K is: one bulk copy moves a block of rows with
+ * its scales and zero points.
+ * identity is the caller's key for the source weight (an initializer id, a
+ * content hash): mnb_matmul_prepacked checks the device copy of the header
+ * against the descriptor it is given (magic, version, identity and shape), so
+ * a buffer re-prepacked for another weight, or overwritten, is refused on the
+ * device (MNB_ERR_INVALID_ARG in the device error word, Y left untouched)
+ * instead of being read as codes.  The buffer stays valid while the caller
+ * keeps it; nothing is cached inside the library. */
+#define MNB_PREPACK_MAGIC 0x50424E4Du /* "MNBP" little-endian */
+#define MNB_PREPACK_VERSION 1u
+#define MNB_PREPACK_HEADER_BYTES 128
+
+typedef struct {
+    uint32_t magic;      /* MNB_PREPACK_MAGIC */
+    uint32_t version;    /* MNB_PREPACK_VERSION */
+    int64_t N, K;        /* weight rows and columns */
+    int32_t bits;        /* 3 or 4 */
+    int32_t block_size;  /* 32, 64 or 128 */
+    int32_t scale_dtype; /* mnb_dtype of the scales */
+    int32_t has_zp;      /* 1: packed zero points follow the scales */
+    int64_t row_stride;  /* bytes per prepacked row, a multiple of 16 */
+    int64_t scale_offset; /* bytes from a row's start to its scales */
+    int64_t zp_offset;   /* bytes from a row's start to its zero points (-1: none) */
+    int64_t bytes;       /* the whole buffer: header + N * row_stride */
+    uint64_t identity;   /* the caller's key for the source weight */
+} mnb_prepacked_desc;
+
+/* Bytes of a version-1 prepacked buffer for these arguments. */
+mnb_status mnb_prepack_size(int64_t N, int64_t K, int bits, int block_size, mnb_dtype scale_dtype,
+                            int has_zero_points, size_t* bytes);
+
+/* Rewrites a row-local weight (B_packed, scales, zero_points as in
+ * mnb_matmul) into the version-1 layout at `dst` (device memory, 16-byte
+ * aligned, dst_bytes >= mnb_prepack_size) with one kernel on `stream`, and
+ * fills *desc (host memory) with the header it writes.  bits 3 or 4.  The
+ * source is read, not changed; dst must not overlap it. */
+mnb_status mnb_prepack(const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                       const uint8_t* zero_points, int64_t N, int64_t K, int bits, int block_size,
+                       uint64_t identity, void* dst, size_t dst_bytes, mnb_prepacked_desc* desc,
+                       mnb_stream_t stream);
+
+/* Y[M, N] = A[M, K] . W^T as mnb_matmul, W read from a prepacked buffer
+ * described by *desc (host memory, as mnb_prepack filled it).  Runs the
+ * CUDA-core GEMV for any M (the decode and small-M shapes the layout is made
+ * for); fp32 accumulation, the same exact integer chunk sums as mnb_matmul's
+ * CUDA-core path.  MNB_ERR_INVALID_ARG for a descriptor that is not version 1
+ * or does not match K. */
+mnb_status mnb_matmul_prepacked(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
+                                const mnb_prepacked_desc* desc, const void* prepacked, void* Y,
+                                mnb_dtype y_dtype, mnb_stream_t stream);
+
 /* ------------------------------------------------------------------- QMoE */
 
 /* Bytes of device workspace qmoe_forward needs: the routing tables, the

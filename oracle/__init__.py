@@ -79,11 +79,14 @@ def _lib():
                 "orc_gate_up_swiglu": [P, C, I64, I64, P, P, C, P, I64, C, C, C, P, C],
                 "orc_mnb_matmul_int8a": [P, C, I64, I64, P, P, C, P, I64, C, C, P, C],
                 "orc_round_to_half_bits": [P, I64, C, P],
+                "orc_prepack": [P, P, C, P, I64, I64, C, C, ctypes.c_uint64, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = C
+            lib.orc_prepack_size.argtypes = [I64, I64, C, C, C, C]
+            lib.orc_prepack_size.restype = I64
             _LIB = lib
     return _LIB
 
@@ -223,6 +226,18 @@ def gate_up_swiglu(A, a_dtype: str, packed, scales, s_dtype: str, zp, I: int, K:
     out = np.zeros((M, I), np.float64)
     _check(_lib().orc_gate_up_swiglu(_ptr(A), DTYPES[a_dtype], M, K, _ptr(packed), _ptr(scales), DTYPES[s_dtype],
                                      _ptr(zp), I, bits, bs, FC1_LAYOUTS[layout], _ptr(out), threads), "gate_up_swiglu")
+    return out
+
+
+def prepack(packed, scales, s_dtype: str, zp, N: int, K: int, bits: int, bs: int, identity: int = 0) -> np.ndarray:
+    """The library's version-1 prepacked bytes (header + rows) of a row-local weight."""
+    packed = _c(packed, np.uint8)
+    scales = _elem(scales, s_dtype)
+    zp = _c(zp, np.uint8)
+    n = _lib().orc_prepack_size(N, K, bits, bs, DTYPES[s_dtype], int(zp is not None))
+    out = np.zeros(n, np.uint8)
+    _check(_lib().orc_prepack(_ptr(packed), _ptr(scales), DTYPES[s_dtype], _ptr(zp), N, K, bits, bs,
+                              ctypes.c_uint64(identity), _ptr(out)), "prepack")
     return out
 
 

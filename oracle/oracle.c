@@ -622,3 +622,83 @@ int orc_quantize_int3(const void* W, int w_dtype, int64_t N, int64_t K, int bs, 
     }
     return 0;
 }
+
+/* ------------------------------------------------- version-1 prepacked layout
+ *
+ * The library's private prepacked form of a weight (its own format, restated
+ * here from its definition so the tests can check the bytes the library
+ * writes): a 128-byte little-endian header {u32 magic "MNBP", u32 version 1,
+ * i64 N, i64 K, i32 bits, i32 block_size, i32 scale dtype, i32 has_zp,
+ * i64 row_stride, i64 scale_offset, i64 zp_offset (-1: none), i64 bytes,
+ * u64 identity, zeros}, then N rows of row_stride bytes: the row's 32-code
+ * chunks (INT4: the stored bytes; INT3: regrouped, below), its scale bytes,
+ * its zero-point bytes, zeros up to a multiple of 16 bytes.
+ * INT3 chunk (codes c_0 .. c_31), three 32-bit little-endian words W_0..W_2:
+ * in byte b of W_g (g < 3), bits 0-2 = c_{8g+2b}, bits 3-5 = c_{8g+2b+1};
+ * bits 6-7 of byte b of W_0 = low two bits of c_{24+2b}, of W_1 = low two bits
+ * of c_{25+2b}; bit 6 of byte b of W_2 = bit 2 of c_{24+2b}, bit 7 = bit 2 of
+ * c_{25+2b}.  Parity unpinned against the pages: the layout is the library's
+ * own; the tests pin it by decoding it back to the row-local codes. */
+static void put_le(uint8_t* p, uint64_t v, int n) {
+    for (int i = 0; i < n; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+
+int64_t orc_prepack_size(int64_t N, int64_t K, int bits, int bs, int s_dtype, int has_zp) {
+    const int64_t nb = n_blocks(K, bs);
+    const int64_t raw = nb * blob_bytes(bits, bs) + nb * (s_dtype == ORC_F32 ? 4 : 2) +
+                        (has_zp ? zp_row_bytes(nb, bits) : 0);
+    const int64_t stride = (raw + 15) / 16 * 16;
+    return 128 + N * stride;
+}
+
+int orc_prepack(const uint8_t* packed, const void* scales, int s_dtype, const uint8_t* zp, int64_t N,
+                int64_t K, int bits, int bs, uint64_t identity, uint8_t* out) {
+    if ((bits != 3 && bits != 4) || (bs != 32 && bs != 64 && bs != 128)) return 1;
+    const int64_t nb = n_blocks(K, bs);
+    const int64_t rb = nb * blob_bytes(bits, bs);
+    const int64_t ss = s_dtype == ORC_F32 ? 4 : 2;
+    const int64_t zr = zp_row_bytes(nb, bits);
+    const int64_t total = orc_prepack_size(N, K, bits, bs, s_dtype, zp != NULL);
+    const int64_t stride = (total - 128) / N;
+    const int64_t scale_off = rb;
+    const int64_t zp_off = zp ? scale_off + nb * ss : -1;
+    memset(out, 0, (size_t)total);
+    put_le(out + 0, 0x50424E4Du, 4);
+    put_le(out + 4, 1, 4);
+    put_le(out + 8, (uint64_t)N, 8);
+    put_le(out + 16, (uint64_t)K, 8);
+    put_le(out + 24, (uint64_t)bits, 4);
+    put_le(out + 28, (uint64_t)bs, 4);
+    put_le(out + 32, (uint64_t)s_dtype, 4);
+    put_le(out + 36, zp != NULL, 4);
+    put_le(out + 40, (uint64_t)stride, 8);
+    put_le(out + 48, (uint64_t)scale_off, 8);
+    put_le(out + 56, (uint64_t)zp_off, 8);
+    put_le(out + 64, (uint64_t)total, 8);
+    put_le(out + 72, identity, 8);
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* src = packed + n * rb;
+        uint8_t* row = out + 128 + n * stride;
+        for (int64_t c = 0; c < nb * bs / 32; ++c) {
+            uint8_t* ch = row + c * 4 * bits;
+            if (bits == 4) {
+                memcpy(ch, src + c * 16, 16);
+                continue;
+            }
+            /* code j of the chunk: stream position 32c + j of the row */
+            int q[32];
+            for (int j = 0; j < 32; ++j) q[j] = stream_code(src, 32 * c + j, 3);
+            for (int g = 0; g < 3; ++g)
+                for (int b = 0; b < 4; ++b) ch[4 * g + b] = (uint8_t)(q[8 * g + 2 * b] | (q[8 * g + 2 * b + 1] << 3));
+            for (int b = 0; b < 4; ++b) {
+                const int e = q[24 + 2 * b], d = q[25 + 2 * b];
+                ch[0 + b] |= (uint8_t)((e & 3) << 6);
+                ch[4 + b] |= (uint8_t)((d & 3) << 6);
+                ch[8 + b] |= (uint8_t)(((e >> 2) & 1) << 6 | ((d >> 2) & 1) << 7);
+            }
+        }
+        memcpy(row + scale_off, (const uint8_t*)scales + n * nb * ss, (size_t)(nb * ss));
+        if (zp) memcpy(row + zp_off, zp + n * zr, (size_t)zr);
+    }
+    return 0;
+}

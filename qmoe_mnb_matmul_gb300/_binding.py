@@ -24,6 +24,15 @@ F32, F16, BF16 = 0, 1, 2
 FC1_INTERLEAVED, FC1_CONCAT = 0, 1
 
 
+class PrepackedDesc(ctypes.Structure):
+    """mnb_prepacked_desc: the host copy of a prepacked buffer's header."""
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("bits", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("scale_dtype", ctypes.c_int32), ("has_zp", ctypes.c_int32), ("row_stride", ctypes.c_int64),
+                ("scale_offset", ctypes.c_int64), ("zp_offset", ctypes.c_int64), ("bytes", ctypes.c_int64),
+                ("identity", ctypes.c_uint64)]
+
+
 class MnbError(RuntimeError):
     def __init__(self, status: int, call: str):
         super().__init__(f"{call} failed: {STATUS.get(status, status)}")
@@ -41,6 +50,9 @@ _SIGNATURES = {
     "mnb_matmul": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _P, _I, _P, _SZ, _P],
     "mnb_matmul_int8a": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _P, _I, _P],
     "mnb_gate_up_swiglu": [_P, _I, _I64, _I64, _P, _P, _I, _P, _I64, _I, _I, _I, _P, _I, _P],
+    "mnb_prepack_size": [_I64, _I64, _I, _I, _I, _I, ctypes.POINTER(_SZ)],
+    "mnb_prepack": [_P, _P, _I, _P, _I64, _I64, _I, _I, ctypes.c_uint64, _P, _SZ, _P, _P],
+    "mnb_matmul_prepacked": [_P, _I, _I64, _I64, _P, _P, _P, _I, _P],
     "qmoe_workspace_size": [_I64, _I64, _I64, _I64, _I, _I, ctypes.POINTER(_SZ)],
     "qmoe_forward": [_P, _I, _I64, _I64, _P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I64, _I, _I,
                      _P, _P, _SZ, _P],
@@ -195,6 +207,46 @@ def mnb_gate_up_swiglu(A, B_packed, scales, zero_points, I, bits, block_size, Y,
                                            _stream(stream))
     if check:
         _check(st, "mnb_gate_up_swiglu")
+    return st
+
+
+def mnb_prepack_size(N, K, bits, block_size, scale_dtype=F32, has_zero_points=False) -> int:
+    out = _SZ(0)
+    _check(load_library().mnb_prepack_size(N, K, bits, block_size, scale_dtype, int(bool(has_zero_points)),
+                                           ctypes.byref(out)), "mnb_prepack_size")
+    return out.value
+
+
+def mnb_prepack(B_packed, scales, zero_points, N, K, bits, block_size, dst, identity=0, stream=None, *,
+                scale_dtype=None, dst_bytes=None, check=True):
+    """Writes the version-1 prepacked form of a row-local weight into `dst`; returns its
+    PrepackedDesc (with check=False: (status, desc))."""
+    scale_dtype = _dtype_code(scales) if scale_dtype is None else scale_dtype
+    if dst_bytes is None:
+        dst_bytes = dst.numel() * dst.element_size()
+    desc = PrepackedDesc()
+    st = load_library().mnb_prepack(_ptr(B_packed), _ptr(scales), scale_dtype, _ptr(zero_points), N, K, bits,
+                                    block_size, ctypes.c_uint64(identity), _ptr(dst), dst_bytes, ctypes.byref(desc),
+                                    _stream(stream))
+    if not check:
+        return st, desc
+    _check(st, "mnb_prepack")
+    return desc
+
+
+def mnb_matmul_prepacked(A, desc, prepacked, Y, stream=None, *, K=None, M=None, a_dtype=None, y_dtype=None,
+                         check=True):
+    """Y[M, N] = A . W^T with W read from a prepacked buffer and its descriptor."""
+    if K is None:
+        K = A.shape[-1]
+    if M is None:
+        M = A.numel() // K
+    a_dtype = _dtype_code(A) if a_dtype is None else a_dtype
+    y_dtype = _dtype_code(Y) if y_dtype is None else y_dtype
+    st = load_library().mnb_matmul_prepacked(_ptr(A), a_dtype, M, K, ctypes.byref(desc), _ptr(prepacked), _ptr(Y),
+                                             y_dtype, _stream(stream))
+    if check:
+        _check(st, "mnb_matmul_prepacked")
     return st
 
 

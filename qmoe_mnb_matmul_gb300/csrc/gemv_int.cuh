@@ -18,6 +18,13 @@
 // bits 3-5; the masks 0x07070707 and 0x38383838 then give the even codes and
 // 8 x the odd codes.
 //
+// Regrouped INT3 (the prepacked layout): the chunk's three words hold codes
+// 0-7, 8-15 and 16-23 already spread (byte b: code 8g+2b in bits 0-2, code
+// 8g+2b+1 in bits 3-5), and codes 24-31 in the spare top two bits of each
+// byte: bits 6-7 of word 0 / word 1 byte b hold the low two bits of code
+// 24+2b / 25+2b, bits 6 / 7 of word 2 byte b their third bits.  Groups 0-2
+// then need only the two masks, and group 3 two shifts and a mask per half.
+//
 // A chunk's result T = sum_k v_k (q_k - z) = S_even + S_odd / 16 (INT4; / 8
 // for INT3) - z V with V = sum_k v_k is an exact int32 (|T| < 2^23), and the
 // chunk contributes block_scale * 2^-s * T (one conversion, one multiply and
@@ -57,10 +64,19 @@ __device__ __forceinline__ uint32_t bit_select(uint32_t m, uint32_t a, uint32_t 
     return d;
 }
 
-// Even / odd code bytes of code word g of a chunk (see the file comment).
-template <int BITS>
+// Even / odd code bytes of code word g of a chunk (see the file comment);
+// RG: the chunk is in the regrouped INT3 form.
+template <int BITS, bool RG = false>
 __device__ __forceinline__ void code_bytes(const uint32_t (&w)[BITS], int g, uint32_t& lo, uint32_t& hi) {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 3 && RG) {
+        if (g < 3) {
+            lo = w[g] & 0x07070707u;
+            hi = w[g] & 0x38383838u;
+        } else {
+            lo = ((w[0] >> 6) & 0x03030303u) | ((w[2] >> 4) & 0x04040404u);
+            hi = ((w[1] >> 3) & 0x18181818u) | ((w[2] >> 2) & 0x20202020u);
+        }
+    } else if constexpr (BITS == 4) {
         lo = w[g] & 0x0F0F0F0Fu;
         hi = w[g] & 0xF0F0F0F0u;
     } else {
@@ -77,7 +93,7 @@ __device__ __forceinline__ void code_bytes(const uint32_t (&w)[BITS], int g, uin
 }
 
 // sum over the chunk of v_k q_k for one code chunk w and one activation image q.
-template <int BITS>
+template <int BITS, bool RG = false>
 __device__ __forceinline__ int chunk_dot(const uint32_t (&w)[BITS], const uint4 (&q)[4]) {
     const uint32_t q0[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
     const uint32_t q1[4] = {q[1].x, q[1].y, q[1].z, q[1].w};
@@ -87,7 +103,7 @@ __device__ __forceinline__ int chunk_dot(const uint32_t (&w)[BITS], const uint4 
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         uint32_t lo, hi;
-        code_bytes<BITS>(w, g, lo, hi);
+        code_bytes<BITS, RG>(w, g, lo, hi);
         se0 = dp4a_su(q0[g], lo, se0);
         se1 = dp4a_su(q1[g], lo, se1);
         so0 = dp4a_su(q2[g], hi, so0);

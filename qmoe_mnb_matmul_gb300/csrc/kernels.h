@@ -34,6 +34,12 @@ struct GemvArgs {
     // Y[m, i] = silu(gate_i) * up_i, y_ld = pairs
     int swiglu, fc1_inter;
     int64_t pairs;
+    // prepacked weight (gemv_pp.cu): B = the first row, row_bytes = the row
+    // stride; the header and the identity the kernel checks it against;
+    // scales / zero points at these offsets within a row (zero points: -1 = none)
+    const void* pp_header;
+    uint64_t pp_identity;
+    int64_t pp_scale_off, pp_zp_off;
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
@@ -41,6 +47,16 @@ struct GemvArgs {
 // when the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl,
                         cudaStream_t stream);
+
+// The GEMV over a prepacked weight (a.B, a.row_bytes, a.pp_* set from its
+// descriptor); bits 3 or 4.
+cudaError_t launch_gemv_prepacked(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl, cudaStream_t stream);
+cudaError_t gemv_pp_take_error(unsigned int* out);
+
+// The prepack kernel: the version-1 layout of a row-local weight (header included).
+cudaError_t launch_prepack(const uint8_t* B, const void* scales, int scale_dtype, const uint8_t* zp, int64_t N,
+                           int64_t K, int bits, int bs, const void* header, size_t header_bytes, uint8_t* dst,
+                           int64_t row_stride, int64_t scale_off, int64_t zp_off, int sm_count, cudaStream_t stream);
 
 // Shared memory the GEMV plan needs for (K, bits, bs, scale dtype, M); 0 if unsupported.
 size_t gemv_smem_bytes(int64_t M, int64_t K, int bits, int bs, int scale_dtype);

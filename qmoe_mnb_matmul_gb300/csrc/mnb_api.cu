@@ -74,6 +74,25 @@ bool proj_bytes(int64_t N, int64_t K, int bits, int bs, int sdt, ProjBytes* p) {
            mul_ok(N, p->zp_row, &p->zp);
 }
 
+// The version-1 prepacked row of a weight: code bytes, scale bytes, zero-point
+// bytes, and the row stride rounded up to 16 bytes.
+struct PpLayout {
+    int64_t nb, code_bytes, scale_off, zp_off, stride, bytes;
+};
+bool pp_layout(int64_t N, int64_t K, int bits, int bs, int sdt, bool has_zp, PpLayout* l) {
+    l->nb = (K + bs - 1) / bs;
+    l->code_bytes = l->nb * bs * bits / 8;
+    l->scale_off = l->code_bytes;
+    const int64_t s_row = l->nb * dsize(sdt);
+    const int64_t z_row = (l->nb * bits + 7) / 8;
+    l->zp_off = has_zp ? l->scale_off + s_row : -1;
+    l->stride = (l->code_bytes + s_row + (has_zp ? z_row : 0) + 15) / 16 * 16;
+    int64_t rows;
+    if (!mul_ok(N, l->stride, &rows)) return false;
+    l->bytes = rows + MNB_PREPACK_HEADER_BYTES;
+    return l->bytes > rows;
+}
+
 }  // namespace
 }  // namespace mnb
 
@@ -99,8 +118,9 @@ mnb_status mnb_get_last_device_error(mnb_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return MNB_ERR_CUDA;
     unsigned int first = 0;
-    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, qmoe_take_error, gemm_tc_take_error,
-                                              quant_take_error, diag_take_error, qmoe_decode_take_error};
+    cudaError_t (*takers[])(unsigned int*) = {gemv_take_error, gemv_pp_take_error, qmoe_take_error,
+                                              gemm_tc_take_error, quant_take_error, diag_take_error,
+                                              qmoe_decode_take_error};
     for (auto take : takers) {
         unsigned int v = 0;
         if (take(&v) != cudaSuccess) return MNB_ERR_CUDA;
@@ -238,6 +258,112 @@ mnb_status mnb_matmul_int8a(const void* A, mnb_dtype a_dtype, int64_t M, int64_t
     a.a_vec = aligned(A, 16) && (K * int64_t(dsize(a_dtype))) % 16 == 0;
     a.int8a = 1;
     return from_cuda(launch_gemv(a, scale_dtype, sms, pdl_enabled(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mnb_status mnb_prepack_size(int64_t N, int64_t K, int bits, int block_size, mnb_dtype scale_dtype,
+                            int has_zero_points, size_t* bytes) {
+    if (!bytes) return MNB_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (N < 1 || K < 1 || !valid_dtype(scale_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    PpLayout l;
+    if (!pp_layout(N, K, bits, block_size, scale_dtype, has_zero_points != 0, &l)) return MNB_ERR_SIZE_OVERFLOW;
+    *bytes = static_cast<size_t>(l.bytes);
+    return MNB_OK;
+}
+
+mnb_status mnb_prepack(const uint8_t* B_packed, const void* scales, mnb_dtype scale_dtype,
+                       const uint8_t* zero_points, int64_t N, int64_t K, int bits, int block_size, uint64_t identity,
+                       void* dst, size_t dst_bytes, mnb_prepacked_desc* desc, mnb_stream_t stream) {
+    if (!B_packed || !scales || !dst || !desc) return MNB_ERR_INVALID_ARG;
+    if (N < 1 || K < 1 || !valid_dtype(scale_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(block_size)) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(B_packed, 16) || !aligned(scales, dsize(scale_dtype)) || !aligned(dst, 16))
+        return MNB_ERR_UNSUPPORTED;
+    if (N > (int64_t(1) << 31)) return MNB_ERR_UNSUPPORTED;
+    PpLayout l;
+    ProjBytes pb;
+    if (!pp_layout(N, K, bits, block_size, scale_dtype, zero_points != nullptr, &l) ||
+        !proj_bytes(N, K, bits, block_size, scale_dtype, &pb))
+        return MNB_ERR_SIZE_OVERFLOW;
+    if (dst_bytes < static_cast<size_t>(l.bytes)) return MNB_ERR_WORKSPACE;
+    // the destination must not overlap any source
+    auto overlaps = [&](const void* p, int64_t n) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), d0 = reinterpret_cast<uintptr_t>(dst);
+        return a0 < d0 + static_cast<uintptr_t>(l.bytes) && d0 < a0 + static_cast<uintptr_t>(n);
+    };
+    if (overlaps(B_packed, pb.weight) || overlaps(scales, pb.scales) || (zero_points && overlaps(zero_points, pb.zp)))
+        return MNB_ERR_INVALID_ARG;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+    mnb_prepacked_desc d = {};
+    d.magic = MNB_PREPACK_MAGIC;
+    d.version = MNB_PREPACK_VERSION;
+    d.N = N;
+    d.K = K;
+    d.bits = bits;
+    d.block_size = block_size;
+    d.scale_dtype = scale_dtype;
+    d.has_zp = zero_points != nullptr;
+    d.row_stride = l.stride;
+    d.scale_offset = l.scale_off;
+    d.zp_offset = l.zp_off;
+    d.bytes = l.bytes;
+    d.identity = identity;
+    const cudaError_t e = launch_prepack(B_packed, scales, scale_dtype, zero_points, N, K, bits, block_size, &d,
+                                         sizeof d, static_cast<uint8_t*>(dst), l.stride, l.scale_off, l.zp_off, sms,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    *desc = d;
+    return MNB_OK;
+}
+
+mnb_status mnb_matmul_prepacked(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K,
+                                const mnb_prepacked_desc* desc, const void* prepacked, void* Y, mnb_dtype y_dtype,
+                                mnb_stream_t stream) {
+    if (!A || !desc || !prepacked || !Y) return MNB_ERR_INVALID_ARG;
+    if (desc->magic != MNB_PREPACK_MAGIC || desc->version != MNB_PREPACK_VERSION || desc->K != K)
+        return MNB_ERR_INVALID_ARG;
+    const int64_t N = desc->N;
+    const int bits = desc->bits, bs = desc->block_size;
+    const mnb_dtype sdt = static_cast<mnb_dtype>(desc->scale_dtype);
+    if (M < 1 || K < 1 || N < 1) return MNB_ERR_INVALID_ARG;
+    if (!valid_dtype(a_dtype) || !valid_dtype(sdt) || !valid_dtype(y_dtype)) return MNB_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_bs(bs)) return MNB_ERR_INVALID_ARG;
+    PpLayout l;
+    if (!pp_layout(N, K, bits, bs, sdt, desc->has_zp != 0, &l)) return MNB_ERR_SIZE_OVERFLOW;
+    if (l.stride != desc->row_stride || l.scale_off != desc->scale_offset || l.zp_off != desc->zp_offset ||
+        l.bytes != desc->bytes)
+        return MNB_ERR_INVALID_ARG;
+    if (sdt != MNB_F32 && sdt != a_dtype) return MNB_ERR_UNSUPPORTED;
+    if (!aligned(prepacked, 16) || !aligned(A, dsize(a_dtype)) || !aligned(Y, dsize(y_dtype)))
+        return MNB_ERR_UNSUPPORTED;
+    int64_t tmp;
+    if (!mul_ok(M, K * 4, &tmp) || !mul_ok(M, N * 4, &tmp)) return MNB_ERR_SIZE_OVERFLOW;
+    if (N > (int64_t(1) << 31)) return MNB_ERR_UNSUPPORTED;
+    const int sms = sm_count_current();
+    if (sms <= 0) return MNB_ERR_CUDA;
+    GemvArgs a = {};
+    a.A = A;
+    a.a_dtype = a_dtype;
+    a.M = M;
+    a.K = K;
+    a.B = static_cast<const uint8_t*>(prepacked) + MNB_PREPACK_HEADER_BYTES;
+    a.N = N;
+    a.bits = bits;
+    a.bs = bs;
+    a.nb = static_cast<int>(l.nb);
+    a.row_bytes = l.stride;
+    a.Y = Y;
+    a.y_dtype = y_dtype;
+    a.y_ld = N;
+    a.chunks = static_cast<int>(l.nb * bs / 32);
+    a.a_vec = aligned(A, 16) && (K * int64_t(dsize(a_dtype))) % 16 == 0;
+    a.pp_header = prepacked;
+    a.pp_identity = desc->identity;
+    a.pp_scale_off = l.scale_off;
+    a.pp_zp_off = l.zp_off;
+    return from_cuda(launch_gemv_prepacked(a, sdt, sms, pdl_enabled(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mnb_status mnb_gate_up_swiglu(const void* A, mnb_dtype a_dtype, int64_t M, int64_t K, const uint8_t* B_packed,

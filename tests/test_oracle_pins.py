@@ -13,6 +13,7 @@
 import json
 import math
 import os
+import struct
 import zlib
 
 import numpy as np
@@ -710,3 +711,88 @@ def test_bfloat16_rounding_at_every_boundary_matches_torch():
     xs = np.concatenate([xs, np.float32([3.4e38, -3.4e38, np.inf, -np.inf])])
     ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(oracle.round_to_half_bits(xs, "bf16"), ref)
+
+
+# ---------------------------------------------------------------- prepacked layout
+
+PREPACK_HEADER = struct.Struct("<IIqqiiiiqqqqQ")
+
+
+def _lsb_first_codes(row: np.ndarray, n: int, bits: int) -> list[int]:
+    """Codes 0 .. n-1 of a row-local LSB-first stream, bit by bit."""
+    bitv = np.unpackbits(row, bitorder="little")
+    return [int(sum(int(bitv[bits * j + t]) << t for t in range(bits))) for j in range(n)]
+
+
+def _decode_prepacked_chunk(ch: bytes, bits: int) -> list[int]:
+    """The 32 codes of one prepacked chunk, read back from the layout's definition."""
+    if bits == 4:
+        return [(ch[j // 2] >> (4 * (j % 2))) & 15 for j in range(32)]
+    q = [0] * 32
+    for g in range(3):
+        for b in range(4):
+            byte = ch[4 * g + b]
+            q[8 * g + 2 * b] = byte & 7
+            q[8 * g + 2 * b + 1] = (byte >> 3) & 7
+    for b in range(4):
+        q[24 + 2 * b] = (ch[b] >> 6) | (((ch[8 + b] >> 6) & 1) << 2)
+        q[25 + 2 * b] = (ch[4 + b] >> 6) | (((ch[8 + b] >> 7) & 1) << 2)
+    return q
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("s_dtype,with_zp", [("f32", False), ("f16", True), ("bf16", True)])
+def test_prepack_decodes_back_to_the_row_local_weight(bits, bs, s_dtype, with_zp):
+    """The oracle's prepacked bytes, decoded field by field from the layout's
+    definition: header values, every stored code (padding codes included), the
+    scale and zero-point bytes, zero padding, rows of whole 16-byte units."""
+    N, K = 5, 200
+    g = wl.rng(0xB0 + bits + bs)
+    packed, scales, zp = wl.quantized_weight(g, N, K, bits, bs, s_dtype, with_zp)
+    out = oracle.prepack(packed, scales, s_dtype, zp, N, K, bits, bs, identity=0x1234_5678_9ABC_DEF0)
+    (magic, version, n_, k_, bits_, bs_, sdt, has_zp, stride, s_off, z_off, total,
+     ident) = PREPACK_HEADER.unpack_from(out.tobytes(), 0)
+    nb = -(-K // bs)
+    ss = 4 if s_dtype == "f32" else 2
+    zr = (nb * bits + 7) // 8
+    assert (magic, version, n_, k_, bits_, bs_) == (0x50424E4D, 1, N, K, bits, bs)
+    assert out[:4].tobytes() == b"MNBP"
+    assert (sdt, has_zp, ident) == (oracle.DTYPES[s_dtype], int(with_zp), 0x1234_5678_9ABC_DEF0)
+    code_bytes = nb * bs * bits // 8
+    raw = code_bytes + nb * ss + (zr if with_zp else 0)
+    assert stride % 16 == 0 and raw <= stride < raw + 16
+    assert (s_off, z_off) == (code_bytes, code_bytes + nb * ss if with_zp else -1)
+    assert total == out.size == 128 + N * stride
+    assert not out[PREPACK_HEADER.size:128].any()
+    sb = np.ascontiguousarray(scales).view(np.uint8).reshape(N, nb * ss)
+    for n in range(N):
+        row = out[128 + n * stride:128 + (n + 1) * stride]
+        want = _lsb_first_codes(packed[n], nb * bs, bits)
+        got = []
+        for c in range(nb * bs // 32):
+            got += _decode_prepacked_chunk(row[c * 4 * bits:(c + 1) * 4 * bits].tobytes(), bits)
+        assert got == want
+        assert np.array_equal(row[s_off:s_off + nb * ss], sb[n])
+        end = s_off + nb * ss
+        if with_zp:
+            assert np.array_equal(row[z_off:z_off + zr], zp[n])
+            end = z_off + zr
+        assert not row[end:].any()
+
+
+def test_prepack_int3_chunk_worked_example():
+    """Codes c_j = j mod 8 in one chunk: the regrouped words worked out by hand from
+    the layout (bytes of W0: 8, 26, 44, 62 plus the low bits of c_24, c_26, c_28,
+    c_30 = 0, 2, 4, 6 in bits 6-7; W2 carries their third bits)."""
+    codes = np.array([[j % 8 for j in range(32)]], np.uint8)
+    packed = oracle.pack_codes(codes, 3, 32)
+    out = oracle.prepack(packed, np.ones((1, 1), np.float32), "f32", None, 1, 32, 3, 32)
+    ch = list(out[128:140])
+    # W0 byte b: c_{2b} | c_{2b+1} << 3 | (c_{24+2b} & 3) << 6, c_{24+2b} = 0, 2, 4, 6
+    assert ch[0:4] == [0 | 1 << 3 | 0 << 6, 2 | 3 << 3 | 2 << 6, 4 | 5 << 3 | 0 << 6, 6 | 7 << 3 | 2 << 6]
+    # W1 byte b: c_{8+2b} | c_{9+2b} << 3 | (c_{25+2b} & 3) << 6, c_{25+2b} = 1, 3, 5, 7
+    assert ch[4:8] == [0 | 1 << 3 | 1 << 6, 2 | 3 << 3 | 3 << 6, 4 | 5 << 3 | 1 << 6, 6 | 7 << 3 | 3 << 6]
+    # W2 byte b: c_{16+2b} | c_{17+2b} << 3 | bit2(c_{24+2b}) << 6 | bit2(c_{25+2b}) << 7
+    assert ch[8:12] == [0 | 1 << 3 | 0 << 6 | 0 << 7, 2 | 3 << 3 | 0 << 6 | 0 << 7,
+                        4 | 5 << 3 | 1 << 6 | 1 << 7, 6 | 7 << 3 | 1 << 6 | 1 << 7]
