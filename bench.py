@@ -491,7 +491,8 @@ def other_rows(torch, mnb, dev, groups=()):
     return rows
 
 
-PROFILE_CASES = ("gemv_head", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "quantize_int3", "decode_chain")
+PROFILE_CASES = ("gemv_head", "gemv_head_int3", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "qmoe_prefill_t128",
+                 "quantize_int3", "decode_chain")
 
 
 def decode_chain(torch, mnb, dev):
@@ -551,6 +552,18 @@ def profile_case(name):
         Y = torch.empty((1, N), device=dev)
         for _ in range(3):
             mnb.mnb_matmul(A, B, S, None, N, BITS, BS, Y)
+    elif name == "gemv_head_int3":  # the head in INT3 bs32 fp32: 2 row-local launches, then 2 prepacked
+        K, N = wl.QWEN3_1P7B_LM_HEAD[1:]
+        B = torch.randint(0, 256, (N, K * 3 // 8), dtype=torch.uint8, generator=gen).to(dev)
+        S = (torch.rand((N, K // BS), generator=gen) * 0.015 + 0.005).to(dev)
+        A = torch.randn((1, K), generator=gen).to(dev)
+        Y = torch.empty((1, N), device=dev)
+        for _ in range(2):
+            mnb.mnb_matmul(A, B, S, None, N, 3, BS, Y)
+        buf = torch.empty(mnb.mnb_prepack_size(N, K, 3, BS, mnb.F32, False), dtype=torch.uint8, device=dev)
+        desc = mnb.mnb_prepack(B, S, None, N, K, 3, BS, buf)
+        for _ in range(2):
+            mnb.mnb_matmul_prepacked(A, desc, buf, Y)
     elif name == "gemm_tc_gate":  # M=2048 bf16, gate 2048 -> 6144 INT4 bs32: 3 launches
         M, K, N = 2048, 2048, 6144
         B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=gen).to(dev)
@@ -567,7 +580,7 @@ def profile_case(name):
             torch.cuda.synchronize()
             del W
     else:  # one Qwen3-30B-A3B-shaped QMoE layer, INT3/INT3 bs64 fp16
-        T = 1 if name == "qmoe_decode" else 4096
+        T = 1 if name == "qmoe_decode" else 128 if name == "qmoe_prefill_t128" else 4096
         H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
         nl = 16 if T == 1 else 2
         layers = make_moe_layers(torch, dev, nl, 3, 3, 64, gen)

@@ -16,8 +16,6 @@ MNB_SLICE_DECL(gemm_tc_fc1_b3)
 MNB_SLICE_DECL(gemm_tc_fc1_b4)
 #undef MNB_SLICE_DECL
 
-int grouped_tile_rows();
-
 namespace {
 
 constexpr int kBW = 128;  // weight rows per tile
@@ -170,7 +168,8 @@ cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int sc
     a.y_dtype = g.y_dtype;
     a.ld_y = I;
     a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * I, kBW));
-    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(grouped_tile_rows())));
+    const int bn = grouped_tile_m(g.M, 1);
+    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(bn)));
     a.splits = 1;
     a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK));
     a.I = I;
@@ -178,16 +177,26 @@ cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int sc
     a.experts = 1;
     const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m, sm_count));
     auto fn = g.bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3;
-    return fn(scale_dtype, g.a_dtype, grouped_tile_rows(), 1, a, g.A, g.M, g.K, grid, pdl, stream);
+    return fn(scale_dtype, g.a_dtype, bn, 1, a, g.A, g.M, g.K, grid, pdl, stream);
 }
 
-// Grouped (QMoE) tiles: 256 routed rows of one expert.
-int grouped_tile_rows() { return 256; }
+// Activation rows per grouped tile: the power of two in [32, 256] at or above
+// four times the mean rows per matrix.  Every tile dequantises its expert's
+// weights again, which costs more than the tensor-core work of a tile, so a
+// tile should hold all of an expert's rows (routing is uneven: four times the
+// mean); only where even that leaves most of a 256-row tile empty does a
+// shorter tile save MMA work.
+int grouped_tile_m(int64_t rows, int64_t matrices) {
+    const int64_t mean = (rows + matrices - 1) / std::max<int64_t>(matrices, 1);
+    int bn = 32;
+    while (bn < 256 && bn < 4 * mean) bn <<= 1;
+    return bn;
+}
 
 cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
-                              int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream) {
+                              int64_t a_rows, int64_t a_cols, int tile_m, int sm_count, bool pdl, cudaStream_t stream) {
     auto fn = fc1 ? (bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3) : (bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3);
-    return fn(scale_dtype, a_dtype, grouped_tile_rows(), 1, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
+    return fn(scale_dtype, a_dtype, tile_m, 1, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

@@ -817,8 +817,13 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
 template <int MODE, int BITS, int ST, int AT>
 cudaError_t launch_bn(int BN, int G, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
                       bool pdl, cudaStream_t stream) {
-    if constexpr (MODE == kModeFc1) {
-        return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);  // grouped: 256 rows
+    if constexpr (MODE == kModeFc1) {  // grouped / dense gate-up: 32 .. 256 activation rows per tile
+        switch (BN) {
+            case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 64: return launch_cfg<BITS, ST, AT, 64, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            default: return launch_cfg<BITS, ST, AT, 32, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        }
     } else {
         switch (BN) {
             case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);

@@ -30,7 +30,9 @@
 #pragma once
 
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "gemv_core.cuh"
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             };
             prefetch(a.B + r0 * a.row_bytes, (r1 - r0) * a.row_bytes);
             if (!PP) prefetch(static_cast<const uint8_t*>(a.scales) + r0 * nb * ss, (r1 - r0) * nb * ss);
+            if (PP) bulk_prefetch_l2(a.pp_header, MNB_PREPACK_HEADER_BYTES);  // read right after the wait
         }
     }
     // The next kernel on the stream may start its prologue (its own L2
@@ -374,17 +377,18 @@ constexpr int64_t kPrefetchAllBytes = int64_t(32) << 20;
 //    launch is mostly latency (the dependency release, one L2 round trip for
 //    the activations and the rows, the stores); this keeps the compute part to
 //    one short pass per warp and the copies few and large.
-//  * Large matrices (the vocabulary head): a ring with two CTAs per SM and
-//    ~80 KB of ring each, so that ~120 KB per SM are in flight (bulk copies
-//    need well over 64 KB in flight per SM to reach HBM bandwidth); each warp
-//    takes R rows of every block.
+//  * Large matrices (the vocabulary head): a ring with `cps` CTAs per SM (three
+//    where the kernel's registers allow, else two) and up to ~80 KB of ring
+//    each, so that 120-190 KB per SM are in flight (bulk copies need well over
+//    64 KB in flight per SM to reach HBM bandwidth); each warp takes R rows of
+//    every block.
 struct Shape {
     int R = 4, stages = 2, grid = 1, rows_per_block = 32;
     bool prefetch_all = false;
 };
 
 Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C, int sm_count, int64_t mgroups,
-                 int force_r = 0, bool pairs = false) {
+                 int force_r = 0, bool pairs = false, int cps = 2) {
     const int64_t align = row_align(row_bytes, nb, ssize);
     const int64_t row_total = row_bytes + int64_t(nb) * ssize;
     const bool small = N * row_total <= kPrefetchAllBytes;
@@ -411,7 +415,8 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
             return best;
         }
     }
-    const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * 2 / mgroups);  // CTAs per activation group
+    const int64_t per_group = std::max<int64_t>(1, int64_t(sm_count) * cps / mgroups);  // CTAs per activation group
+    const int64_t per_cta = (kSmemBudget / cps) & ~int64_t(1023);  // shared memory of one of cps CTAs
     double best_cost = -1;
     for (int R : {4, 2, 1}) {
         if (MT == 4 && R == 4) continue;
@@ -421,8 +426,8 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         if (RC % (pairs ? 2 * align : align) != 0) continue;
         const Plan p1 = make_plan(MT, C, RC, row_bytes, nb, ssize, 1);
         const int64_t stage = p1.w_stage + p1.s_stage;
-        const int64_t cap = std::max<int64_t>(112 * 1024, p1.fixed + 2 * stage);
-        if (p1.fixed + 2 * stage > kSmemBudget) continue;
+        const int64_t cap = cps == 2 ? std::max<int64_t>(112 * 1024, p1.fixed + 2 * stage) : per_cta;
+        if (p1.fixed + 2 * stage > (cps == 2 ? kSmemBudget : per_cta)) continue;
         int st = static_cast<int>(std::min<int64_t>(kMaxStages, std::max<int64_t>(2, (80 * 1024) / stage)));
         while (st > 2 && p1.fixed + st * stage > cap) --st;
         const int64_t nblk = cdiv<int64_t>(N, RC);
@@ -469,6 +474,51 @@ cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t str
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// CTAs of this instantiation an SM holds with `smem` bytes of dynamic shared
+// memory (registers, shared memory and threads), cached per (kernel, smem).
+template <int BITS, int ST, int MT, int R, bool PP>
+int resident_ctas(int64_t smem) {
+    static std::mutex mu;
+    static std::unordered_map<int64_t, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(smem);
+    if (it != cache.end()) return it->second;
+    auto kern = gemv_kernel<BITS, ST, MT, R, PP>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, static_cast<size_t>(smem)) != cudaSuccess)
+        n = 0;
+    cache.emplace(smem, n);
+    return n;
+}
+
+template <int BITS, int ST, int MT, bool PP>
+int resident_ctas_r(int R, int64_t smem) {
+    if constexpr (BITS == 0) {
+        return resident_ctas<0, ST, MT, 2, PP>(smem);
+    } else {
+        if constexpr (MT < 4) {
+            if (R == 4) return resident_ctas<BITS, ST, MT, 4, PP>(smem);
+        }
+        if (R == 2) return resident_ctas<BITS, ST, MT, 2, PP>(smem);
+        return resident_ctas<BITS, ST, MT, 1, PP>(smem);
+    }
+}
+
+// The launch shape of the large-matrix ring: three CTAs per SM where that
+// instantiation's registers and shared memory let three be resident (the
+// rows are split evenly over co-resident CTAs, so a CTA that had to wait for
+// a free slot would double the time), else two.
+template <int BITS, int ST, int MT, bool PP>
+Shape pick_shape_resident(const GemvArgs& a, int ssize, int sm_count, int64_t mgroups, int force_r) {
+    Shape sh = pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, force_r, a.swiglu != 0, 3);
+    if (sh.prefetch_all) return sh;  // the small-matrix shape: one CTA per SM
+    const Plan p = make_plan(MT, a.chunks, sh.rows_per_block, a.row_bytes, a.nb, ssize, sh.stages);
+    if (resident_ctas_r<BITS, ST, MT, PP>(sh.R, p.total) >= 3) return sh;
+    return pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, force_r, a.swiglu != 0, 2);
+}
+
 template <int BITS, int ST, int MT, bool PP = false>
 cudaError_t launch_r(const GemvArgs& a, const Shape& sh, bool pdl, cudaStream_t stream) {
     if constexpr (BITS == 0) {  // any width: one register tile (the shape picks R = 2)
@@ -487,15 +537,23 @@ cudaError_t launch_mt(const GemvArgs& a, int sm_count, bool pdl, cudaStream_t st
     // any width: at most two activation rows per pass (the code extraction takes the registers)
     const int MT = BITS == 0 ? std::min(pick_mt(a.M), 2) : pick_mt(a.M);
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
-    const Shape sh = pick_shape(a.N, a.row_bytes, a.nb, PP ? 0 : ST == kF32 ? 4 : 2, MT, a.chunks, sm_count, mgroups,
-                                BITS == 0 ? 2 : 0, a.swiglu != 0);
+    const int ssize = PP ? 0 : ST == kF32 ? 4 : 2;
     if constexpr (BITS == 0) {
-        return MT == 1 ? launch_r<0, ST, 1>(a, sh, pdl, stream) : launch_r<0, ST, 2>(a, sh, pdl, stream);
+        if (MT == 1) return launch_r<0, ST, 1>(a, pick_shape_resident<0, ST, 1, false>(a, ssize, sm_count, mgroups, 2),
+                                               pdl, stream);
+        return launch_r<0, ST, 2>(a, pick_shape_resident<0, ST, 2, false>(a, ssize, sm_count, mgroups, 2), pdl,
+                                  stream);
     } else {
         switch (MT) {
-            case 1: return launch_r<BITS, ST, 1, PP>(a, sh, pdl, stream);
-            case 2: return launch_r<BITS, ST, 2, PP>(a, sh, pdl, stream);
-            default: return launch_r<BITS, ST, 4, PP>(a, sh, pdl, stream);
+            case 1:
+                return launch_r<BITS, ST, 1, PP>(a, pick_shape_resident<BITS, ST, 1, PP>(a, ssize, sm_count, mgroups, 0),
+                                                 pdl, stream);
+            case 2:
+                return launch_r<BITS, ST, 2, PP>(a, pick_shape_resident<BITS, ST, 2, PP>(a, ssize, sm_count, mgroups, 0),
+                                                 pdl, stream);
+            default:
+                return launch_r<BITS, ST, 4, PP>(a, pick_shape_resident<BITS, ST, 4, PP>(a, ssize, sm_count, mgroups, 0),
+                                                 pdl, stream);
         }
     }
 }

@@ -124,8 +124,9 @@ struct TcArgs {
     const void* bias;
 };
 
-// Rows of activations per tile in the grouped launches.
-int grouped_tile_rows();
+// Rows of activations per tile (32 .. 256) for `rows` activation rows spread
+// over `matrices` weight matrices (experts) in a grouped launch.
+int grouped_tile_m(int64_t rows, int64_t matrices);
 
 // Dense H[M, I] = silu(A . Wg^T) * (A . Wu^T) on the tensor cores (B holds the
 // 2I gate/up rows, interleaved or gate half then up half).
@@ -136,7 +137,7 @@ cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int sc
 // fc1 gathers X rows by token and writes silu(gate)*up; otherwise a dense
 // tile GEMM on A_rows [a_rows, a_cols] (TMA).
 cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
-                              int64_t a_rows, int64_t a_cols, int sm_count, bool pdl, cudaStream_t stream);
+                              int64_t a_rows, int64_t a_cols, int tile_m, int sm_count, bool pdl, cudaStream_t stream);
 
 // --------------------------------------------------------------- unpack
 cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int bits, int bs, uint8_t* packed,

@@ -59,10 +59,11 @@ __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
     return P < t ? P : t;
 }
 
-// m-tiles of the tensor-core plan: <= kTcTileM sorted pairs of one expert.
-constexpr int kTcTileM = 256;  // equals grouped_tile_rows()
+// m-tiles of the tensor-core plan: <= tile_m sorted pairs of one expert, tile_m
+// in [32, 256] (grouped_tile_m); the workspace holds enough for the shortest.
+constexpr int kTcTileMin = 32;
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
-    const int64_t t = (P + kTcTileM - 1) / kTcTileM + E;
+    const int64_t t = (P + kTcTileMin - 1) / kTcTileMin + E;
     return P < t ? P : t;
 }
 
@@ -574,7 +575,8 @@ __global__ void combine_kernel(const __grid_constant__ QmoeArgs q) {
 }
 
 // m-tiles for the tensor-core plan: {expert, first sorted position, pairs, 0}.
-__global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64_t H, int64_t I, int64_t E, int k) {
+__global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64_t H, int64_t I, int64_t E, int k,
+                                                      int tile_m) {
     const Ws L = ws_layout(T, H, I, E, k);
     const int* counts = reinterpret_cast<const int*>(ws + L.counts);
     const int* offsets = reinterpret_cast<const int*>(ws + L.offsets);
@@ -583,7 +585,7 @@ __global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64
     grid_dependency_wait();
     const int e = threadIdx.x;
     const int cnt = e < E ? counts[e] : 0;
-    const int n = (cnt + kTcTileM - 1) / kTcTileM;
+    const int n = (cnt + tile_m - 1) / tile_m;
     scan[e] = n;
     __syncthreads();
     for (int o = 1; o < 1024; o <<= 1) {
@@ -594,7 +596,7 @@ __global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64
     }
     const int first = scan[e] - n;
     for (int i = 0; i < n; ++i)
-        tiles[first + i] = make_int4(e, offsets[e] + i * kTcTileM, min(kTcTileM, cnt - i * kTcTileM), 0);
+        tiles[first + i] = make_int4(e, offsets[e] + i * tile_m, min(tile_m, cnt - i * tile_m), 0);
     if (e == 1023) *reinterpret_cast<int*>(ws + L.nmtiles) = scan[1023];
     grid_launch_dependents();
 }
@@ -724,7 +726,9 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
                                     reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
         return e;
     if (use_tc(q)) {
-        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
+        // tile height from the mean routed rows per expert (FC1 and FC2 alike)
+        const int tile_m = grouped_tile_m(P, q.E);
+        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         TcArgs a = {};
         a.splits = 1;
@@ -764,7 +768,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
             gather_rows_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        if ((e = launch_grouped_tc(true, a, B1, ST, ST, ws + L.o, P, q.H, sm_count, pdl, stream)) != cudaSuccess)
+        if ((e = launch_grouped_tc(true, a, B1, ST, ST, ws + L.o, P, q.H, tile_m, sm_count, pdl, stream)) != cudaSuccess)
             return e;
         // FC2: K = I, H rows; activations are h rows in sorted order (TMA), output o (act dtype, sorted order)
         a.K = q.I;
@@ -783,7 +787,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.bias = q.fc2_bias;
         a.tiles_n = static_cast<int>(cdiv<int64_t>(q.H, 128));
         a.k_steps = static_cast<int>(cdiv<int64_t>(q.I, 64));
-        if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, sm_count, pdl, stream)) != cudaSuccess)
+        if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, tile_m, sm_count, pdl, stream)) != cudaSuccess)
             return e;
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H / 8, 256), int64_t(sm_count) * 16);
         using AT = typename DType<ST>::T;
