@@ -18,21 +18,28 @@
 // beside G = 2's tiles it measured slower.  One persistent CTA per SM walks
 // the tiles.
 //
-// Warp roles (736 threads):
-//   warp 0      activation producer: TMA tiles [BN x 64] (128-byte swizzle); in
+// Warp roles (768 threads, 24 warps; warp w issues from SM sub-partition
+// w % 4).  The three single-lane roles share sub-partition 1 with one epilogue
+// warp and one dequant warp: the dequant warps' long ALU streams on the other
+// three sub-partitions would otherwise take the issue slots that the MMA
+// issuer needs every K step (measured: with them mixed in, issuing a K step's
+// four MMAs and two commits took ~500 cycles).
+//   warp 9      activation producer: TMA tiles [BN x 64] (128-byte swizzle); in
 //               the grouped FC1 the routed tokens' rows were first copied
 //               into expert-sorted order, so the same tile loads serve
 //   warp 1      TMEM owner; one lane issues tcgen05.mma (K = 16, 4 per stage)
-//   warp 2      packed-weight producer: per K step one TMA tile of the 128
+//   warp 5      packed-weight producer: per K step one TMA tile of the 128
 //               rows' packed bytes [128 x 32 B] and one of their scales
 //               [128 x 16 B] into an 8-slot ring (where the rows are 16-byte
 //               aligned; otherwise each dequant thread copies its own row
 //               with cp.async into the same slots)
-//   warps 3-18  dequant, four groups of 4 warps taking every fourth K step:
-//               one thread per weight row, both 32-code chunks of the K step;
-//               codes -> s (q - z) -> fp16/bf16 -> swizzled 16-byte stores
-//   warps 19-22 epilogue: tcgen05.ld of the accumulators -> output dtype
-//               (FC1: SwiGLU of lane pairs) -> masked stores
+//   16 warps    dequant (all the others but warp 21, which idles), four groups
+//               of 4 warps taking every fourth K step: one thread per weight
+//               row, both 32-code chunks of the K step; codes -> s (q - z) ->
+//               fp16/bf16 -> swizzled 16-byte stores
+//   warps 12-15 epilogue (TMEM lane quarter = warp % 4): tcgen05.ld of the
+//               accumulators -> output dtype (FC1: SwiGLU of lane pairs) ->
+//               masked stores
 // The activation tiles and the dequantised weight tiles of the K steps sit in
 // two separate shared rings: the activation ring is deep (its tiles come from
 // L2 / HBM with the longest latency), the weight ring holds one slot per
@@ -62,11 +69,22 @@ using namespace gemv;
 
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kBW = 128;    // weight rows per tile (MMA M)
-constexpr int kPackWarp = 2;  // TMA producer of packed rows and scales
+constexpr int kMmaWarp = 1;   // TMEM owner and MMA issuer
+constexpr int kPackWarp = 5;  // TMA producer of packed rows and scales
+constexpr int kActWarp = 9;   // TMA producer of activation tiles
+constexpr int kEpilogueWarp0 = 12;  // warps 12..15
+constexpr int kWarpsTC = 24;
+// Warps with a role other than dequantisation (warp 21 idles).
+constexpr uint32_t kNonDequantWarps = (1u << kMmaWarp) | (1u << kPackWarp) | (1u << kActWarp) |
+                                      (0xFu << kEpilogueWarp0) | (1u << 21);
+// Rank of warp w among the dequant warps, or -1.
+__device__ __forceinline__ int dequant_rank(int w) {
+    return ((kNonDequantWarps >> w) & 1u) ? -1 : w - __popc(kNonDequantWarps & ((1u << w) - 1u));
+}
 // Four groups of 4 dequantisation warps take every fourth K step: one thread
 // per weight row makes all 64 codes of the row's K step, and each group has
 // four MMA steps' time for its 128 x 64 weight slice.
-constexpr int kDequantWarp0 = 3, kDequantGroups = 4;
+constexpr int kDequantGroups = 4;
 constexpr int kDequantWarps = 16 / kDequantGroups;            // warps per group
 constexpr int kChunksPerThread = kDequantGroups == 4 ? 2 : 1;  // 32-code chunks of a row's K step per thread
 // Dequantised-weight ring depth: at least one slot per group (a group's parity
@@ -78,8 +96,9 @@ constexpr int kWeightSlots = kDequantGroups + 1;
 constexpr int kPackSlots = 2 * kDequantGroups;
 constexpr int kPackRow = 32;  // bytes of a row's K step in a slot (INT3: a 16-byte-aligned 32-byte window)
 constexpr int kSclRow = 16;   // bytes of a row's scale window in a slot
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kDequantGroups * kDequantWarps;
-constexpr int kThreadsTC = (kEpilogueWarp0 + 4) * 32;
+static_assert(kWarpsTC - __builtin_popcount(kNonDequantWarps) == kDequantGroups * kDequantWarps,
+              "every dequant group needs its warps");
+constexpr int kThreadsTC = kWarpsTC * 32;
 constexpr int kMaxStagesTC = 8;
 
 enum { kModeGemm = 0, kModeFc1 = 1 };
@@ -215,7 +234,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     const int S = a.stages, SW = a.stages_w;
     const TcPlan plan = tc_plan(BN, G, S, SW, BITS);
     uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full_a + kMaxStagesTC;
+    // (full_a + kMaxStagesTC: unused; the activation stages are released
+    // through empty_w, the barrier of the K step that last read them)
     uint64_t* full_w = full_a + 2 * kMaxStagesTC;
     uint64_t* empty_w = full_a + 3 * kMaxStagesTC;
     uint64_t* acc_full = full_a + 4 * kMaxStagesTC;
@@ -237,10 +257,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     const int ksteps = a.k_steps;
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full_a[s], 1);
-            mbar_init(&empty[s], 1);
-        }
+        for (int s = 0; s < S; ++s) mbar_init(&full_a[s], 1);
         for (int s = 0; s < SW; ++s) {
             mbar_init(&full_w[s], kDequantWarps);
             mbar_init(&empty_w[s], 1);
@@ -259,7 +276,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         if (a.w_tma) prefetch_tmap(&tmap_w);
         if (a.s_tma) prefetch_tmap(&tmap_s);
     }
-    if (warp == 1) tmem_alloc(tmem_holder, a.tmem_cols);
+    if (warp == kMmaWarp) tmem_alloc(tmem_holder, a.tmem_cols);
     grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
@@ -268,16 +285,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     const int n_tiles = a.mtiles ? *a.n_mtiles * a.tiles_n : a.tiles_n * a.tiles_m * a.splits;
     bool failed = false;
 
-    if (warp == 0) {
+    const int dq_rank = dequant_rank(warp);
+    if (warp == kActWarp) {
         // ------------------------------------------------- activation producer
         // TMA tiles of the activation rows (FC1: the routed tokens' rows, already
         // copied into expert-sorted order), G sub-tiles of BN rows per K step.
+        // A stage is free again once the MMAs of the K step that last used it
+        // have completed: the one commit per K step goes to the weight ring's
+        // barrier of that step (`done` walks the weight ring S steps behind).
+        // With S <= SW that barrier cannot have moved a phase past the step.
         if (lane == 0) {
-            RingPos rp;
+            RingPos rp, done;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
                 const Tile x = tile_of(a, t, UN);
                 for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                    if (rp.round && !mbar_wait(&empty[rp.stage], (rp.round - 1) & 1)) { failed = true; break; }
+                    if (rp.round) {
+                        if (!mbar_wait(&empty_w[done.stage], done.round & 1)) { failed = true; break; }
+                        done.next(SW);
+                    }
                     mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
 #pragma unroll
                     for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
@@ -286,7 +311,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kBW, BN, AT == kBF16);
@@ -315,8 +340,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                             tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
                     }
                     if (failed) break;
-                    tc_commit(&empty[rp.stage]);
-                    tc_commit(&empty_w[rw.stage]);
+                    tc_commit(&empty_w[rw.stage]);  // frees the step's weight slot and activation stage
                 }
                 if (failed) break;
 #pragma unroll
@@ -364,10 +388,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 }
             }
         }
-    } else if (warp < kEpilogueWarp0) {
+    } else if (dq_rank >= 0) {
         // ------------------------------------------------------------ dequant
-        const int group = (warp - kDequantWarp0) / kDequantWarps;  // takes K steps = group (mod groups)
-        const int dq = tid - (kDequantWarp0 + group * kDequantWarps) * 32;
+        const int group = dq_rank / kDequantWarps;  // takes K steps = group (mod groups)
+        const int dq = (dq_rank - group * kDequantWarps) * 32 + lane;
         const int r = dq & (kBW - 1);                               // row of the packed slot
         const int h0 = kChunksPerThread == 2 ? 0 : dq >> 7;         // this thread's first chunk
         // Tile row (MMA lane) this thread makes: FC1 gate and up rows of pair p
@@ -598,7 +622,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             advance(cc);
         }
         cp_async_wait<0>();
-    } else {
+    } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ----------------------------------------------------------- epilogue
         // One lane polls the accumulator barrier; the four epilogue warps meet
         // on a named barrier, so the others take no issue slots while waiting.
@@ -701,7 +725,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     grid_launch_dependents();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
     }
@@ -731,7 +755,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // was at or before the group's last step, i.e. stages_w >= kDequantGroups.
 void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
     static_assert(kWeightSlots >= kDequantGroups, "a parity wait needs a weight slot per group");
-    int s = kMaxStagesTC;
+    int s = std::min(kMaxStagesTC, kWeightSlots);  // activation stages share the weight ring's barriers
     while (s > 2 && tc_plan(BN, G, s, kWeightSlots, bits).total > 227 * 1024) --s;
     *stages_w = kWeightSlots;
     *stages = s;
