@@ -7,8 +7,8 @@
 namespace mnb {
 
 #define MNB_SLICE_DECL(NAME)                                                                                      \
-    cudaError_t NAME(int scale_dtype, int a_dtype, const TcArgs& a, const void* A_rows, int64_t a_rows,         \
-                     int64_t a_cols, int grid, bool pdl, cudaStream_t stream);                                  \
+    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, int G, const TcArgs& a, const void* A_rows,          \
+                     int64_t a_rows, int64_t a_cols, int grid, bool pdl, cudaStream_t stream);                 \
     cudaError_t NAME##_take_error(unsigned int* out);
 MNB_SLICE_DECL(gemm_tc_gemm_b3)
 MNB_SLICE_DECL(gemm_tc_gemm_b4)
@@ -18,20 +18,43 @@ MNB_SLICE_DECL(gemm_tc_fc1_b4)
 
 namespace {
 
-constexpr int kBM = 128;  // activation rows per tile (MMA M)
-constexpr int kBW = 256;  // weight rows per tile (MMA N)
+constexpr int kBW = 128;  // weight rows per tile
 constexpr int kBK = 64;   // K per stage
+
+// Tile shape: BN activation rows per MMA and G sub-tiles per dequantised
+// weight tile.  A tile's time is modelled as max(MMA columns G*BN, the
+// dequantisation of its weight K steps, worth ~460 MMA columns per step at the
+// measured rates) over the narrow-tile MMA efficiency; the grid walks the
+// tiles in waves of one per SM.
+struct TcShape {
+    int BN, G;
+};
+TcShape pick_shape(int64_t M, int64_t N, int sm_count) {
+    TcShape best{256, 1};
+    double best_cost = 1e300;
+    const TcShape cands[] = {{256, 1}, {128, 1}, {64, 1}, {32, 1}, {16, 1}};
+    for (const TcShape& c : cands) {
+        if (c.G == 1 && c.BN > 16 && c.BN / 2 >= M) continue;  // a narrower tile covers M already
+        const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(c.BN) * c.G);
+        const double waves = double(cdiv<int64_t>(tiles, sm_count));
+        const double eff = c.BN >= 256 ? 1.0 : c.BN >= 128 ? 0.9 : c.BN >= 64 ? 0.7 : 0.5;
+        const double cost = waves * std::max(double(c.BN * c.G), 460.0) / eff;
+        if (cost < best_cost) { best_cost = cost; best = c; }
+    }
+    return best;
+}
 
 // K split: when the output tiles cannot give every SM a tile, the K steps of
 // each tile are divided among up to 16 CTAs (an equal share each, at least 4
 // steps), their fp32 partial sums go to the workspace, and a second kernel adds
 // them in split order.
 struct TcPlanK {
+    TcShape sh;
     int splits;
 };
 TcPlanK plan_tc(int64_t M, int64_t K, int64_t N, int sm_count) {
-    TcPlanK p{1};
-    const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(kBM));
+    TcPlanK p{pick_shape(M, N, sm_count), 1};
+    const int64_t tiles = cdiv<int64_t>(N, kBW) * cdiv<int64_t>(M, int64_t(p.sh.BN) * p.sh.G);
     const int64_t ksteps = cdiv<int64_t>(K, kBK);
     if (tiles * 2 > sm_count) return p;
     for (int s = 16; s >= 2; --s) {
@@ -85,6 +108,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     while (plan.splits > 1 &&
            (g.workspace == nullptr || g.workspace_bytes < per_split * plan.splits || ksteps % plan.splits != 0))
         --plan.splits;
+    const TcShape sh = plan.sh;
     TcArgs a = {};
     a.M = g.M;
     a.K = g.K;
@@ -100,7 +124,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     a.y_dtype = g.y_dtype;
     a.ld_y = g.N;
     a.tiles_n = static_cast<int>(cdiv<int64_t>(g.N, kBW));
-    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(kBM)));
+    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(sh.BN) * sh.G));
     a.splits = plan.splits;
     a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK)) / plan.splits;
     a.partials = plan.splits > 1 ? static_cast<float*>(g.workspace) : nullptr;
@@ -113,7 +137,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
     const int passes = (g.y_dtype == kF32 && g.a_dtype != kF32) ? 2 : 1;
     for (int pass = 0; pass < passes; ++pass) {
         a.remainder = pass;
-        cudaError_t e = fn(scale_dtype, g.a_dtype, a, g.A, g.M, g.K, grid, pdl, stream);
+        cudaError_t e = fn(scale_dtype, g.a_dtype, sh.BN, sh.G, a, g.A, g.M, g.K, grid, pdl, stream);
         if (e != cudaSuccess) return e;
         if (plan.splits == 1) continue;
         const int64_t MN = g.M * g.N;
@@ -144,7 +168,8 @@ cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int sc
     a.y_dtype = g.y_dtype;
     a.ld_y = I;
     a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * I, kBW));
-    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(kBM)));
+    const int bn = grouped_tile_m(g.M, 1);
+    a.tiles_m = static_cast<int>(cdiv<int64_t>(g.M, int64_t(bn)));
     a.splits = 1;
     a.k_steps = static_cast<int>(cdiv<int64_t>(g.K, kBK));
     a.I = I;
@@ -152,19 +177,26 @@ cudaError_t launch_gate_up_tc(const GemmTcArgs& g, int64_t I, bool inter, int sc
     a.experts = 1;
     const int grid = static_cast<int>(std::min<int64_t>(int64_t(a.tiles_n) * a.tiles_m, sm_count));
     auto fn = g.bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3;
-    return fn(scale_dtype, g.a_dtype, a, g.A, g.M, g.K, grid, pdl, stream);
+    return fn(scale_dtype, g.a_dtype, bn, 1, a, g.A, g.M, g.K, grid, pdl, stream);
 }
 
-// Activation rows per grouped tile: the MMA's M, 128 whatever the routing.
-// A tile's cost is set by its weights (dequantisation and one MMA instruction
-// per 256 x 16 weight slice), not by how many of its 128 rows are live.
-int grouped_tile_m(int64_t, int64_t) { return kBM; }
+// Activation rows per grouped tile: the power of two in [32, 256] at or above
+// four times the mean rows per matrix.  Every tile dequantises its expert's
+// weights again, which costs more than the tensor-core work of a tile, so a
+// tile should hold all of an expert's rows (routing is uneven: four times the
+// mean); only where even that leaves most of a 256-row tile empty does a
+// shorter tile save MMA work.
+int grouped_tile_m(int64_t rows, int64_t matrices) {
+    const int64_t mean = (rows + matrices - 1) / std::max<int64_t>(matrices, 1);
+    int bn = 32;
+    while (bn < 256 && bn < 4 * mean) bn <<= 1;
+    return bn;
+}
 
 cudaError_t launch_grouped_tc(bool fc1, const TcArgs& a, int bits, int scale_dtype, int a_dtype, const void* A_rows,
                               int64_t a_rows, int64_t a_cols, int tile_m, int sm_count, bool pdl, cudaStream_t stream) {
     auto fn = fc1 ? (bits == 4 ? gemm_tc_fc1_b4 : gemm_tc_fc1_b3) : (bits == 4 ? gemm_tc_gemm_b4 : gemm_tc_gemm_b3);
-    (void)tile_m;  // the m-tiles were built with grouped_tile_m rows
-    return fn(scale_dtype, a_dtype, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
+    return fn(scale_dtype, a_dtype, tile_m, 1, a, A_rows, a_rows, a_cols, sm_count, pdl, stream);
 }
 
 }  // namespace mnb

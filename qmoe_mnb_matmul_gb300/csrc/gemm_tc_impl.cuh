@@ -68,8 +68,7 @@ namespace {
 using namespace gemv;
 
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
-constexpr int kBM = 128;    // activation rows per tile (MMA M)
-constexpr int kBW = 256;    // weight rows per tile (MMA N)
+constexpr int kBW = 128;    // weight rows per tile (MMA M)
 constexpr int kMmaWarp = 1;   // TMEM owner and MMA issuer
 constexpr int kPackWarp = 5;  // TMA producer of packed rows and scales
 constexpr int kActWarp = 9;   // TMA producer of activation tiles
@@ -82,20 +81,17 @@ constexpr uint32_t kNonDequantWarps = (1u << kMmaWarp) | (1u << kPackWarp) | (1u
 __device__ __forceinline__ int dequant_rank(int w) {
     return ((kNonDequantWarps >> w) & 1u) ? -1 : w - __popc(kNonDequantWarps & ((1u << w) - 1u));
 }
-// Two groups of 8 dequantisation warps take alternate K steps: one thread per
-// weight row makes all 64 codes of the row's K step, and each group has two
-// MMA steps' time for its 256 x 64 weight slice.
-constexpr int kDequantGroups = 2;
-constexpr int kDequantWarps = 16 / kDequantGroups;  // warps per group: 32 x 8 = kBW threads
-constexpr int kChunksPerThread = 2;                 // 32-code chunks of a row's K step per thread
+// Four groups of 4 dequantisation warps take every fourth K step: one thread
+// per weight row makes all 64 codes of the row's K step, and each group has
+// four MMA steps' time for its 128 x 64 weight slice.
+constexpr int kDequantGroups = 4;
+constexpr int kDequantWarps = 16 / kDequantGroups;            // warps per group
+constexpr int kChunksPerThread = kDequantGroups == 4 ? 2 : 1;  // 32-code chunks of a row's K step per thread
 // Dequantised-weight ring depth: at least one slot per group (a group's parity
-// wait needs it), plus two so that a group may start its next K step while the
-// MMAs of the two before it are still reading their slots.
-constexpr int kWeightSlots = kDequantGroups + 2;
-// Activation ring depth (<= kWeightSlots: the stages are released through the
-// weight ring's barriers).
-constexpr int kActStages = 3;
-// Packed ring: K step g of the CTA's sequence -> slot g % 4, so each group owns
+// wait needs it), plus one so that a group may start its next K step one MMA
+// step before the slot it last wrote has been read.
+constexpr int kWeightSlots = kDequantGroups + 1;
+// Packed ring: K step g of the CTA's sequence -> slot g % 8, so each group owns
 // two slots and has its next K step in flight while it works on the current.
 constexpr int kPackSlots = 2 * kDequantGroups;
 constexpr int kPackRow = 32;  // bytes of a row's K step in a slot (INT3: a 16-byte-aligned 32-byte window)
@@ -104,7 +100,6 @@ static_assert(kWarpsTC - __builtin_popcount(kNonDequantWarps) == kDequantGroups 
               "every dequant group needs its warps");
 constexpr int kThreadsTC = kWarpsTC * 32;
 constexpr int kMaxStagesTC = 8;
-constexpr uint32_t kTmemCols = 2 * kBW;  // two accumulators (double-buffered tiles)
 
 enum { kModeGemm = 0, kModeFc1 = 1 };
 
@@ -112,10 +107,10 @@ struct TcPlan {
     int64_t bars, act, w, pack, scl, total;
 };
 
-__host__ __device__ inline TcPlan tc_plan(int stages, int stages_w) {
+__host__ __device__ inline TcPlan tc_plan(int BN, int G, int stages, int stages_w, int bits) {
     TcPlan p;
     p.bars = 1024;                                           // barriers and the TMEM address
-    p.act = int64_t(kBM) * 128;                              // activations of one stage
+    p.act = int64_t(G) * BN * 128;                           // activations of one stage (G sub-tiles)
     p.w = int64_t(kBW) * 128;                                // dequantised weights of one stage
     p.pack = int64_t(kPackSlots) * kBW * kPackRow;  // [slot][row][32 bytes]
     p.scl = int64_t(kPackSlots) * kBW * kSclRow;    // [slot][row][16 bytes]
@@ -196,7 +191,7 @@ struct Tile {
     int e, s0, cnt, n0, split, ks0;
 };
 
-__device__ __forceinline__ Tile tile_of(const TcArgs& a, int t) {
+__device__ __forceinline__ Tile tile_of(const TcArgs& a, int t, int BN) {
     Tile x;
     if (a.mtiles) {
         const int j = t / a.tiles_n;
@@ -214,52 +209,30 @@ __device__ __forceinline__ Tile tile_of(const TcArgs& a, int t) {
         const int nt = t / a.tiles_m;
         const int mtile = t - nt * a.tiles_m;
         x.e = 0;
-        x.s0 = mtile * kBM;
-        x.cnt = static_cast<int>(a.M - x.s0 < kBM ? a.M - x.s0 : int64_t(kBM));
+        x.s0 = mtile * BN;
+        x.cnt = static_cast<int>(a.M - x.s0 < BN ? a.M - x.s0 : int64_t(BN));
         x.n0 = nt * kBW;
     }
     return x;
 }
 
-// Eight consecutive outputs of one row: one 16-byte store where the row
-// segment is aligned and whole, else element by element.
-template <typename OT>
-__device__ __forceinline__ void store8(OT* dst, const float (&v)[8], int live, bool vec) {
-    if (vec && live == 8) {
-        if constexpr (sizeof(OT) == 4) {
-            reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
-        } else {
-            uint4 q;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&q);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const OT lo = from_f32<OT>(v[2 * i]), hi = from_f32<OT>(v[2 * i + 1]);
-                w[i] = uint32_t(*reinterpret_cast<const uint16_t*>(&lo)) |
-                       (uint32_t(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
-            }
-            *reinterpret_cast<uint4*>(dst) = q;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < live) {
-                if constexpr (sizeof(OT) == 4)
-                    dst[i] = v[i];
-                else
-                    dst[i] = from_f32<OT>(v[i]);
-            }
-    }
-}
+// Accumulator slot s (columns s*BN ..) of sub-tile g of the tl-th tile of this
+// CTA, and how many earlier tiles used that slot.
+template <int G>
+__device__ __forceinline__ int acc_slot(int tl, int g) { return G == 1 ? (tl & 1) : g; }
+template <int G>
+__device__ __forceinline__ int acc_uses(int tl) { return G == 1 ? (tl >> 1) : tl; }
 
-template <int BITS, int ST, int AT, int MODE>
+template <int BITS, int ST, int AT, int BN, int G, int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                 const __grid_constant__ CUtensorMap tmap_w,
                                                                 const __grid_constant__ CUtensorMap tmap_s,
                                                                 const __grid_constant__ TcArgs a) {
+    static_assert(G == 1 || G == 2, "one or two activation sub-tiles per tile");
+    constexpr int UN = G * BN;  // activation rows per tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = a.stages, SW = a.stages_w;
-    const TcPlan plan = tc_plan(S, SW);
+    const TcPlan plan = tc_plan(BN, G, S, SW, BITS);
     uint64_t* full_a = reinterpret_cast<uint64_t*>(smem);
     // (full_a + kMaxStagesTC: unused; the activation stages are released
     // through empty_w, the barrier of the K step that last read them)
@@ -268,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     uint64_t* acc_full = full_a + 4 * kMaxStagesTC;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* pfull = full_a + 5 * kMaxStagesTC;   // packed slot loaded (TMA)
-    uint64_t* pempty = full_a + 6 * kMaxStagesTC;  // packed slot read by its group's warps
+    uint64_t* pempty = full_a + 6 * kMaxStagesTC;  // packed slot read by its group's 4 warps
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full_a + 7 * kMaxStagesTC);
     volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_holder + 1);  // the epilogue's wait gave up
     uint8_t* act = smem + plan.bars;
@@ -303,7 +276,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         if (a.w_tma) prefetch_tmap(&tmap_w);
         if (a.s_tma) prefetch_tmap(&tmap_s);
     }
-    if (warp == kMmaWarp) tmem_alloc(tmem_holder, kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(tmem_holder, a.tmem_cols);
     grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
@@ -315,64 +288,70 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     const int dq_rank = dequant_rank(warp);
     if (warp == kActWarp) {
         // ------------------------------------------------- activation producer
-        // TMA tiles [128 rows x 64] of the activation rows (FC1: the routed
-        // tokens' rows, already copied into expert-sorted order).  A stage is
-        // free again once the MMAs of the K step that last used it have
-        // completed: the one commit per K step goes to the weight ring's barrier
-        // of that step (`done` walks the weight ring S steps behind).  With
-        // S <= SW that barrier cannot have moved a phase past the step.
+        // TMA tiles of the activation rows (FC1: the routed tokens' rows, already
+        // copied into expert-sorted order), G sub-tiles of BN rows per K step.
+        // A stage is free again once the MMAs of the K step that last used it
+        // have completed: the one commit per K step goes to the weight ring's
+        // barrier of that step (`done` walks the weight ring S steps behind).
+        // With S <= SW that barrier cannot have moved a phase past the step.
         if (lane == 0) {
             RingPos rp, done;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                const Tile x = tile_of(a, t);
+                const Tile x = tile_of(a, t, UN);
                 for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
                     if (rp.round) {
                         if (!mbar_wait(&empty_w[done.stage], done.round & 1)) { failed = true; break; }
                         done.next(SW);
                     }
-                    mbar_arrive_expect_tx(&full_a[rp.stage], kBM * 128);
-                    // rows past the matrix read as zeros
-                    tma_load_2d(act + rp.stage * plan.act, &tmap_a, (x.ks0 + ks) * kBK, x.s0, &full_a[rp.stage]);
+                    mbar_arrive_expect_tx(&full_a[rp.stage], UN * 128);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)  // rows past the matrix read as zeros
+                        tma_load_2d(act + rp.stage * plan.act + g * BN * 128, &tmap_a, (x.ks0 + ks) * kBK,
+                                    x.s0 + g * BN, &full_a[rp.stage]);
                 }
             }
         }
     } else if (warp == kMmaWarp) {
         // --------------------------------------------------------- MMA issuer
-        // D[activation row, weight row] += A[128 x 16] . B[256 x 16]^T, four
-        // MMAs per K step into one of two 256-column accumulators.
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBM, kBW, AT == kBF16);
+            constexpr uint32_t idesc = idesc_f16(kBW, BN, AT == kBF16);
             RingPos rp, rw;
             int tl = 0;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
-                const int slot = tl & 1, uses = tl >> 1;
-                if (uses > 0) {  // the epilogue has drained this slot's previous tile
-                    if (!mbar_wait(&acc_empty[slot], (uses - 1) & 1)) { failed = true; break; }
-                    tc_fence_after();
-                }
-                const uint32_t d = tmem + slot * kBW;
+                const int uses = acc_uses<G>(tl);
                 for (int ks = 0; ks < ksteps && !failed; ++ks, rp.next(S), rw.next(SW)) {
                     if (!mbar_wait(&full_a[rp.stage], rp.round & 1) || !mbar_wait(&full_w[rw.stage], rw.round & 1)) {
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t da = smem_desc_sw128(act + rp.stage * plan.act);
-                    const uint64_t db = smem_desc_sw128(wt + rw.stage * plan.w);
+                    const uint64_t da = smem_desc_sw128(wt + rw.stage * plan.w);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+                    for (int g = 0; g < G; ++g) {
+                        const int slot = acc_slot<G>(tl, g);
+                        if (ks == 0 && uses > 0) {  // the epilogue has drained this slot's previous tile
+                            if (!mbar_wait(&acc_empty[slot], (uses - 1) & 1)) { failed = true; break; }
+                            tc_fence_after();
+                        }
+                        const uint32_t d = tmem + slot * BN;
+                        const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act + g * BN * 128);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
+                    }
+                    if (failed) break;
                     tc_commit(&empty_w[rw.stage]);  // frees the step's weight slot and activation stage
                 }
                 if (failed) break;
-                tc_commit(&acc_full[slot]);
+#pragma unroll
+                for (int g = 0; g < G; ++g) tc_commit(&acc_full[acc_slot<G>(tl, g)]);
             }
         }
     } else if (warp == kPackWarp) {
         // ----------------------------------------------- packed-row producer
         // One TMA tile of packed bytes (and one of scales) per K step of the
-        // CTA's sequence into slot g % 4; the FC1 gate/up halves of a tile
-        // (rows p and I + p) come as two 128-row tiles.
+        // CTA's sequence into slot g % 8; the FC1 gate/up halves of a tile
+        // (rows p and I + p) come as two 64-row tiles.
         if (lane == 0 && a.w_tma) {
             constexpr int kStepBytes = BITS == 4 ? 32 : 24;
             const int SS = ST == kF32 ? 4 : 2;
@@ -381,18 +360,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             const int bs_shift = __ffs(a.bs) - 1;
             RingPos pp;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                const Tile x = tile_of(a, t);
+                const Tile x = tile_of(a, t, UN);
                 const int y0 = static_cast<int>(x.e * a.rows + (halves ? x.n0 / 2 : x.n0));
                 const int y1 = static_cast<int>(y0 + a.I);  // halves: the up rows
                 for (int ks = 0; ks < ksteps; ++ks, pp.next(kPackSlots)) {
                     if (pp.round && !mbar_wait(&pempty[pp.stage], (pp.round - 1) & 1)) { failed = true; break; }
                     mbar_arrive_expect_tx(&pfull[pp.stage], tx);
                     const int kabs = x.ks0 + ks;
-                    const int xw = (kabs * kStepBytes) & ~15;  // 16-byte aligned window
+                    const int xw = (kabs * kStepBytes) & ~15;                       // 16-byte aligned window
                     uint8_t* dw = pack + pp.stage * (kBW * kPackRow);
                     if (halves) {
                         tma_load_2d(dw, &tmap_w, xw, y0, &pfull[pp.stage]);
-                        tma_load_2d(dw + (kBW / 2) * kPackRow, &tmap_w, xw, y1, &pfull[pp.stage]);
+                        tma_load_2d(dw + 64 * kPackRow, &tmap_w, xw, y1, &pfull[pp.stage]);
                     } else {
                         tma_load_2d(dw, &tmap_w, xw, y0, &pfull[pp.stage]);
                     }
@@ -401,7 +380,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         uint8_t* ds = scl + pp.stage * (kBW * kSclRow);
                         if (halves) {
                             tma_load_2d(ds, &tmap_s, xs, y0, &pfull[pp.stage]);
-                            tma_load_2d(ds + (kBW / 2) * kSclRow, &tmap_s, xs, y1, &pfull[pp.stage]);
+                            tma_load_2d(ds + 64 * kSclRow, &tmap_s, xs, y1, &pfull[pp.stage]);
                         } else {
                             tma_load_2d(ds, &tmap_s, xs, y0, &pfull[pp.stage]);
                         }
@@ -413,11 +392,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         // ------------------------------------------------------------ dequant
         const int group = dq_rank / kDequantWarps;  // takes K steps = group (mod groups)
         const int dq = (dq_rank - group * kDequantWarps) * 32 + lane;
-        const int r = dq;   // row of the packed slot (one thread per weight row of the tile)
-        const int h0 = 0;   // this thread's first chunk
-        // Tile row (MMA N index) this thread makes: FC1 gate and up rows of pair
-        // p sit in slot rows p and 128 + p, and go to tile rows 2p and 2p + 1.
-        const int orow = (MODE == kModeFc1 && !a.inter) ? 2 * (r & 127) + (r >> 7) : r;
+        const int r = dq & (kBW - 1);                               // row of the packed slot
+        const int h0 = kChunksPerThread == 2 ? 0 : dq >> 7;         // this thread's first chunk
+        // Tile row (MMA lane) this thread makes: FC1 gate and up rows of pair p
+        // sit in slot rows p and 64 + p, and go to tile rows 2p and 2p + 1.
+        const int orow = (MODE == kModeFc1 && !a.inter) ? 2 * (r & 63) + (r >> 6) : r;
         constexpr int kCB = BITS == 4 ? 16 : 12;  // packed bytes per 32-code chunk
         constexpr int kStepBytes = 2 * kCB;       // packed bytes of a row per K step
         constexpr int kZ = 1 << (BITS - 1);
@@ -473,7 +452,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         }
         int pslot = 0;
         RowStream ps{nullptr, nullptr, 0, 0, false};
-        if (own_copies && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t));
+        if (own_copies && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t, UN));
         // one half-precision scale: the 4-byte word that holds it (the last scale
         // of the array alone, where its word would run past the end)
         auto copy_scale_word = [&](uint32_t* dst, const uint8_t* base, int64_t si) {
@@ -520,7 +499,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             if (pc.t < n_tiles) {
                 const int t_before = pc.t;
                 advance(pc);
-                if (pc.t != t_before && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t));
+                if (pc.t != t_before && pc.t < n_tiles) ps = stream_of(tile_of(a, pc.t, UN));
             }
         };
         if (own_copies) issue();
@@ -542,7 +521,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         while (cc.t < n_tiles && !failed) {
             if (cc.t != cur_t) {
                 cur_t = cc.t;
-                const Tile x = tile_of(a, cur_t);
+                const Tile x = tile_of(a, cur_t, UN);
                 cs = stream_of(x);
                 zrow = (a.zp && cs.ok) ? a.zp + x.e * a.z_expert_stride + (cs.si0 / nb) * a.zp_row_bytes : nullptr;
             }
@@ -645,116 +624,101 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         cp_async_wait<0>();
     } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ----------------------------------------------------------- epilogue
-        // Warp q reads TMEM lanes 32q .. 32q+31, i.e. activation rows 32q + lane
-        // of the tile, 32 weight-row columns per tcgen05.ld; each thread then
-        // owns a contiguous run of one output row.  One lane polls the
-        // accumulator barrier; the four warps meet on a named barrier.
+        // One lane polls the accumulator barrier; the four epilogue warps meet
+        // on a named barrier, so the others take no issue slots while waiting.
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const bool poller = warp == kEpilogueWarp0 && lane == 0;
         int tl = 0;
         for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
-            const Tile x = tile_of(a, t);
-            const int slot = tl & 1, uses = tl >> 1;
-            if (poller && !mbar_wait(&acc_full[slot], uses & 1)) *epi_fail = 1;
-            epilogue_sync();
-            if (*epi_fail) { failed = true; break; }
-            tc_fence_after();
-            const int row = quarter * 32 + lane;  // tile row of this thread
-            const bool live = row < x.cnt;
-            const int64_t m = int64_t(x.s0) + row;
-            if (quarter * 32 < x.cnt) {  // a warp with no live row loads nothing (warp-uniform)
+            const Tile x = tile_of(a, t, UN);
+            const int uses = acc_uses<G>(tl);
+            const int rr = quarter * 32 + lane;  // tile row of this thread
 #pragma unroll 1
-                for (int c0 = 0; c0 < kBW; c0 += 32) {
-                    const int64_t n0 = int64_t(x.n0) + c0;  // first weight row of the chunk
-                    if (MODE == kModeFc1 ? n0 / 2 >= a.I : n0 >= a.rows) break;  // warp-uniform
+            for (int g = 0; g < G; ++g) {
+                const int slot = acc_slot<G>(tl, g);
+                if (poller && !mbar_wait(&acc_full[slot], uses & 1)) *epi_fail = 1;
+                epilogue_sync();
+                if (*epi_fail) { failed = true; break; }
+                tc_fence_after();
+                const int cnt = x.cnt - g * BN;  // live activation rows of this sub-tile
+                const int64_t m0 = int64_t(x.s0) + g * BN;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN && c0 < cnt; c0 += 32) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + slot * kBW + c0, v);
+                    tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + slot * BN + c0, v);
                     tmem_ld_wait();
-                    if (!live) continue;
+                    // live columns of this 32-column chunk (a 16-column tile loads 32: the
+                    // upper 16 belong to the other accumulator)
+                    const int jn = min(32, min(BN - c0, cnt - c0));
                     if constexpr (MODE == kModeFc1) {
-                        // columns 2i / 2i+1: the gate / up rows of pair p0 + i
-                        const int64_t p0 = n0 / 2;
-                        const int np = static_cast<int>(min(int64_t(16), a.I - p0));
-                        using OT = typename DType<AT>::T;
-                        const auto* bp = a.bias ? static_cast<const OT*>(a.bias) + x.e * a.rows : nullptr;
-                        float h[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float gate = __uint_as_float(v[2 * i]), up = __uint_as_float(v[2 * i + 1]);
-                            if (bp && i < np) {
-                                const int64_t p = p0 + i;
-                                gate += to_f32(bp[a.inter ? 2 * p : p]);
-                                up += to_f32(bp[a.inter ? 2 * p + 1 : a.I + p]);
-                            }
-                            // h is rounded to the 16-bit activation type next, so the fast
-                            // exponential and division (a few ulp of fp32) do not show
-                            h[i] = __fdividef(gate, 1.0f + __expf(-gate)) * up;
+                        // Lanes 2i / 2i+1 hold the gate / up rows of pair p: the even lane
+                        // makes h for the even columns, the odd lane for the odd ones,
+                        // each trading the value the other needs in one shuffle.
+                        const int64_t p = x.n0 / 2 + (rr >> 1);
+                        const int odd = lane & 1;
+                        float bg = 0.f, bu = 0.f;  // biases of the pair's gate and up rows
+                        if (a.bias && p < a.I) {
+                            const auto* bp = static_cast<const typename DType<AT>::T*>(a.bias) + x.e * a.rows;
+                            bg = to_f32(bp[a.inter ? 2 * p : p]);
+                            bu = to_f32(bp[a.inter ? 2 * p + 1 : a.I + p]);
                         }
-                        void* yrow = static_cast<char*>(a.Y) + (m * a.ld_y + p0) * (a.y_dtype == kF32 ? 4 : 2);
-                        const bool vec = ((reinterpret_cast<uintptr_t>(yrow)) & 15) == 0;
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            float q8[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) q8[i] = h[8 * hh + i];
-                            const int lv = max(0, min(8, np - 8 * hh));
-                            if (a.y_dtype == kF32)
-                                store8(static_cast<float*>(yrow) + 8 * hh, q8, lv, vec);
-                            else if (a.y_dtype == kBF16)
-                                store8(static_cast<__nv_bfloat16*>(yrow) + 8 * hh, q8, lv, vec);
-                            else
-                                store8(static_cast<__half*>(yrow) + 8 * hh, q8, lv, vec);
+                        for (int j = 0; j < 32; j += 2) {
+                            const float send = __uint_as_float(odd ? v[j] : v[j + 1]);  // even: gate of j+1; odd: up of j
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            const float gate = (odd ? recv : __uint_as_float(v[j])) + bg;
+                            const float up = (odd ? __uint_as_float(v[j + 1]) : recv) + bu;
+                            const int col = j + odd;
+                            if (col < jn && p < a.I) {
+                                // h is rounded to the 16-bit activation type next, so the fast
+                                // exponential and division (a few ulp of fp32) do not show
+                                const float hv = __fdividef(gate, 1.0f + __expf(-gate)) * up;
+                                store_from_f32(a.Y, a.y_dtype, (m0 + c0 + col) * a.ld_y + p, hv);
+                            }
                         }
                     } else {
-                        const int nlive = static_cast<int>(min(int64_t(32), a.rows - n0));
-                        float f[32];
+                        const int64_t n = x.n0 + rr;
+                        if (a.bias && n < a.rows) {  // grouped FC2: the expert's bias of row n
+                            const float b = to_f32(static_cast<const typename DType<AT>::T*>(a.bias)[x.e * a.rows + n]);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                        if (a.bias) {  // grouped FC2: the expert's bias of each output row
-                            using OT = typename DType<AT>::T;
-                            const OT* bp = static_cast<const OT*>(a.bias) + x.e * a.rows + n0;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (j < nlive) f[j] += to_f32(bp[j]);
+                            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + b);
                         }
-                        if (a.splits > 1) {  // fp32 partial sums of this split of K
-                            float* pp = a.partials + (int64_t(x.split) * a.M + m) * a.ld_y + n0;
-                            const bool vec = (reinterpret_cast<uintptr_t>(pp) & 15) == 0;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                float q8[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) q8[i] = f[8 * q + i];
-                                store8(pp + 8 * q, q8, max(0, min(8, nlive - 8 * q)), vec);
-                            }
-                        } else if (a.remainder) {  // second pass of an fp32 output: add
-                            float* yp = static_cast<float*>(a.Y) + m * a.ld_y + n0;
+                        if (n < a.rows && a.splits > 1) {  // fp32 partial sums of this split of K
+                            float* pp = a.partials + (int64_t(x.split) * a.M + m0 + c0) * a.ld_y + n;
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
-                                if (j < nlive) yp[j] += f[j];
-                        } else {
-                            void* yrow = static_cast<char*>(a.Y) + (m * a.ld_y + n0) * (a.y_dtype == kF32 ? 4 : 2);
-                            const bool vec = (reinterpret_cast<uintptr_t>(yrow) & 15) == 0;
+                                if (j < jn) pp[j * a.ld_y] = __uint_as_float(v[j]);
+                        } else if (n < a.rows) {
+                            if (a.y_dtype == AT) {  // 16-bit output: one strided pointer
+                                using OT = typename DType<AT>::T;
+                                OT* yp = static_cast<OT*>(a.Y) + (m0 + c0) * a.ld_y + n;
+                                const int64_t ld = a.ld_y;
+                                if (jn == 32) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                float q8[8];
+                                    for (int j = 0; j < 32; ++j) yp[j * ld] = from_f32<OT>(__uint_as_float(v[j]));
+                                } else {
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) q8[i] = f[8 * q + i];
-                                const int lv = max(0, min(8, nlive - 8 * q));
-                                if (a.y_dtype == kF32)
-                                    store8(static_cast<float*>(yrow) + 8 * q, q8, lv, vec);
-                                else if (a.y_dtype == kBF16)
-                                    store8(static_cast<__nv_bfloat16*>(yrow) + 8 * q, q8, lv, vec);
-                                else
-                                    store8(static_cast<__half*>(yrow) + 8 * q, q8, lv, vec);
+                                    for (int j = 0; j < 32; ++j)
+                                        if (j < jn) yp[j * ld] = from_f32<OT>(__uint_as_float(v[j]));
+                                }
+                            } else if (a.remainder) {  // second pass of an fp32 output: add
+                                float* yp = static_cast<float*>(a.Y) + (m0 + c0) * a.ld_y + n;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < jn) yp[j * a.ld_y] += __uint_as_float(v[j]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < jn)
+                                        store_from_f32(a.Y, a.y_dtype, (m0 + c0 + j) * a.ld_y + n, __uint_as_float(v[j]));
                             }
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[slot]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[slot]);
         }
     }
     if (failed) record_error(MNB_ERR_TIMEOUT);
@@ -763,7 +727,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, a.tmem_cols);
     }
 }
 
@@ -789,28 +753,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // parity wait is only sound while the slot's barrier is at most one phase
 // behind the awaited one, which holds exactly when that slot's previous use
 // was at or before the group's last step, i.e. stages_w >= kDequantGroups.
-void stages_for(int* stages, int* stages_w) {
+void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
     static_assert(kWeightSlots >= kDequantGroups, "a parity wait needs a weight slot per group");
-    static_assert(kActStages <= kWeightSlots, "activation stages are released through the weight ring");
-    static_assert(kActStages <= kMaxStagesTC && kWeightSlots <= kMaxStagesTC && kPackSlots <= kMaxStagesTC,
-                  "barrier arrays");
+    int s = std::min(kMaxStagesTC, kWeightSlots);  // activation stages share the weight ring's barriers
+    while (s > 2 && tc_plan(BN, G, s, kWeightSlots, bits).total > 227 * 1024) --s;
     *stages_w = kWeightSlots;
-    *stages = kActStages;
+    *stages = s;
 }
 
-template <int BITS, int ST, int AT, int MODE>
+template <int BITS, int ST, int AT, int BN, int G, int MODE>
 cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
                        bool pdl, cudaStream_t stream) {
     TcArgs a = in;
     CUtensorMap tmap;
     std::memset(&tmap, 0, sizeof tmap);
     {
-        // activations [a_rows, a_cols] in 128-row tiles
+        // activations [a_rows, a_cols] in BN-row tiles
         auto encode = encode_fn();
         if (!encode) return cudaErrorNotSupported;
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a_cols), static_cast<cuuint64_t>(a_rows)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a_cols * 2)};
-        const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(kBM)};
+        const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
         const cuuint32_t estr[2] = {1, 1};
         const CUresult cr = encode(&tmap, AT == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                                    2, const_cast<void*>(A_rows), dims, strides, box, estr,
@@ -819,7 +782,7 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     // Packed rows and scales as [rows x bytes] tensors of all stacked matrices,
-    // read in tiles of 256 rows (FC1 with separate gate/up halves: 128) by 32
+    // read in tiles of 128 rows (FC1 with separate gate/up halves: 64) by 32
     // (scales: 16) bytes; only where every row starts on a 16-byte boundary.
     CUtensorMap tmap_w, tmap_s;
     std::memset(&tmap_w, 0, sizeof tmap_w);
@@ -828,7 +791,7 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
         auto encode = encode_fn();
         const int64_t ex = a.experts > 1 ? a.experts : 1;
         const int64_t all_rows = ex * a.rows;
-        const cuuint32_t box_rows = (MODE == kModeFc1 && !a.inter) ? kBW / 2 : kBW;
+        const cuuint32_t box_rows = (MODE == kModeFc1 && !a.inter) ? 64 : kBW;
         const int ss = ST == kF32 ? 4 : 2;
         const int64_t s_row = int64_t(a.nb) * ss;
         auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
@@ -854,11 +817,12 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
-    a.tmem_cols = kTmemCols;
-    stages_for(&a.stages, &a.stages_w);
-    const int64_t smem = tc_plan(a.stages, a.stages_w).total;
-    if (smem > 227 * 1024) return cudaErrorNotSupported;
-    auto kern = gemm_tc_kernel<BITS, ST, AT, MODE>;
+    uint32_t cols = 32;
+    while (cols < 2u * BN) cols <<= 1;
+    a.tmem_cols = cols;
+    stages_for(BN, G, BITS, &a.stages, &a.stages_w);
+    const int64_t smem = tc_plan(BN, G, a.stages, a.stages_w, BITS).total;
+    auto kern = gemm_tc_kernel<BITS, ST, AT, BN, G, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -874,19 +838,40 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_w, tmap_s, a);
 }
 
+template <int MODE, int BITS, int ST, int AT>
+cudaError_t launch_bn(int BN, int G, const TcArgs& a, const void* A_rows, int64_t a_rows, int64_t a_cols, int grid,
+                      bool pdl, cudaStream_t stream) {
+    if constexpr (MODE == kModeFc1) {  // grouped / dense gate-up: 32 .. 256 activation rows per tile
+        switch (BN) {
+            case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 64: return launch_cfg<BITS, ST, AT, 64, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            default: return launch_cfg<BITS, ST, AT, 32, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        }
+    } else {
+        switch (BN) {
+            case 256: return launch_cfg<BITS, ST, AT, 256, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 128: return launch_cfg<BITS, ST, AT, 128, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 64: return launch_cfg<BITS, ST, AT, 64, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            case 32: return launch_cfg<BITS, ST, AT, 32, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+            default: return launch_cfg<BITS, ST, AT, 16, 1, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);
+        }
+    }
+}
+
 }  // namespace
 
 // One (mode, bit width) slice of the instantiations; each slice lives in its own
 // translation unit so the slices compile in parallel.
 #define MNB_GEMM_TC_SLICE(NAME, MODE, BITS)                                                                     \
-    cudaError_t NAME(int scale_dtype, int a_dtype, const TcArgs& a, const void* A_rows, int64_t a_rows,         \
-                     int64_t a_cols, int grid, bool pdl, cudaStream_t stream) {                                  \
+    cudaError_t NAME(int scale_dtype, int a_dtype, int BN, int G, const TcArgs& a, const void* A_rows,          \
+                     int64_t a_rows, int64_t a_cols, int grid, bool pdl, cudaStream_t stream) {                 \
         const bool sf = scale_dtype == kF32;                                                                     \
         if (a_dtype == kBF16)                                                                                    \
-            return sf ? launch_cfg<BITS, kF32, kBF16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream)        \
-                      : launch_cfg<BITS, kBF16, kBF16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);      \
-        return sf ? launch_cfg<BITS, kF32, kF16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream)             \
-                  : launch_cfg<BITS, kF16, kF16, MODE>(a, A_rows, a_rows, a_cols, grid, pdl, stream);            \
+            return sf ? launch_bn<MODE, BITS, kF32, kBF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream)  \
+                      : launch_bn<MODE, BITS, kBF16, kBF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream); \
+        return sf ? launch_bn<MODE, BITS, kF32, kF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream)       \
+                  : launch_bn<MODE, BITS, kF16, kF16>(BN, G, a, A_rows, a_rows, a_cols, grid, pdl, stream);      \
     }                                                                                                            \
     cudaError_t NAME##_take_error(unsigned int* out) { return take_unit_error(out); }
 

@@ -59,11 +59,9 @@ __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
     return P < t ? P : t;
 }
 
-// m-tiles of the tensor-core plan: <= tile_m sorted pairs of one expert
-// (grouped_tile_m: 128); the workspace holds enough for tiles of 32 rows.
-// Each tile covers kTcTileW weight rows (the MMA's N).
+// m-tiles of the tensor-core plan: <= tile_m sorted pairs of one expert, tile_m
+// in [32, 256] (grouped_tile_m); the workspace holds enough for the shortest.
 constexpr int kTcTileMin = 32;
-constexpr int kTcTileW = 256;
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
     const int64_t t = (P + kTcTileMin - 1) / kTcTileMin + E;
     return P < t ? P : t;
@@ -754,7 +752,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.z_expert_stride = 2 * q.I * q.fc1.zp_row;
         a.Y = ws + L.h;
         a.ld_y = q.I;
-        a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * q.I, kTcTileW));
+        a.tiles_n = static_cast<int>(cdiv<int64_t>(2 * q.I, 128));
         a.k_steps = static_cast<int>(cdiv<int64_t>(q.H, 64));
         a.perm = reinterpret_cast<const int*>(ws + L.perm);
         a.k = q.k;
@@ -787,7 +785,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.Y = ws + L.o;
         a.ld_y = q.H;
         a.bias = q.fc2_bias;
-        a.tiles_n = static_cast<int>(cdiv<int64_t>(q.H, kTcTileW));
+        a.tiles_n = static_cast<int>(cdiv<int64_t>(q.H, 128));
         a.k_steps = static_cast<int>(cdiv<int64_t>(q.I, 64));
         if ((e = launch_grouped_tc(false, a, B2, ST, ST, ws + L.h, P, q.I, tile_m, sm_count, pdl, stream)) != cudaSuccess)
             return e;
