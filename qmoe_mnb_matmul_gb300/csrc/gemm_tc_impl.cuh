@@ -69,22 +69,14 @@ using namespace gemv;
 
 constexpr int kBK = 64;     // K elements per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kBW = 128;    // weight rows per tile (MMA M)
-constexpr int kMmaWarp = 1;   // TMEM owner and MMA issuer (even K steps where there are two issuers)
-constexpr int kMmaWarp2 = 21;  // second MMA issuer (odd K steps), tiles of <= 128 activation rows
+constexpr int kMmaWarp = 1;   // TMEM owner and MMA issuer
 constexpr int kPackWarp = 5;  // TMA producer of packed rows and scales
 constexpr int kActWarp = 9;   // TMA producer of activation tiles
 constexpr int kEpilogueWarp0 = 12;  // warps 12..15
 constexpr int kWarpsTC = 24;
-// Warps with a role other than dequantisation.
+// Warps with a role other than dequantisation (warp 21 idles).
 constexpr uint32_t kNonDequantWarps = (1u << kMmaWarp) | (1u << kPackWarp) | (1u << kActWarp) |
-                                      (0xFu << kEpilogueWarp0) | (1u << kMmaWarp2);
-// Accumulator parts per tile.  One thread can issue a tcgen05.mma about every
-// 120 cycles (measured), while a 128 x N x 16 MMA with N <= 128 takes the
-// tensor core 70 cycles or less; so for such tiles two warps issue the MMAs,
-// alternate K steps each into their own accumulator, and the epilogue adds the
-// two.  256-column tiles keep the tensor core busy from one issuer.
-template <int BN, int G>
-__host__ __device__ constexpr int acc_parts() { return (G == 1 && BN <= 128) ? 2 : 1; }
+                                      (0xFu << kEpilogueWarp0) | (1u << 21);
 // Rank of warp w among the dequant warps, or -1.
 __device__ __forceinline__ int dequant_rank(int w) {
     return ((kNonDequantWarps >> w) & 1u) ? -1 : w - __popc(kNonDequantWarps & ((1u << w) - 1u));
@@ -96,14 +88,9 @@ constexpr int kDequantGroups = 4;
 constexpr int kDequantWarps = 16 / kDequantGroups;            // warps per group
 constexpr int kChunksPerThread = kDequantGroups == 4 ? 2 : 1;  // 32-code chunks of a row's K step per thread
 // Dequantised-weight ring depth: at least one slot per group (a group's parity
-// wait needs it), plus two so that a group may start its next K step while
-// the MMAs of the two before it are still reading their slots.  Even: with two
-// MMA issuers taking alternate K steps, every use of a slot (and of an
-// activation stage, whose count is even too) falls to the same issuer, so an
-// issuer's parity wait on a slot always follows its own wait on the slot's
-// previous use.
-constexpr int kWeightSlots = kDequantGroups + 2;
-static_assert(kWeightSlots % 2 == 0, "alternating issuers need an even ring");
+// wait needs it), plus one so that a group may start its next K step one MMA
+// step before the slot it last wrote has been read.
+constexpr int kWeightSlots = kDequantGroups + 1;
 // Packed ring: K step g of the CTA's sequence -> slot g % 8, so each group owns
 // two slots and has its next K step in flight while it works on the current.
 constexpr int kPackSlots = 2 * kDequantGroups;
@@ -276,7 +263,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
             mbar_init(&empty_w[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], acc_parts<BN, G>());  // one commit per issuer
+            mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
         for (int s = 0; s < kPackSlots; ++s) {
@@ -324,22 +311,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 }
             }
         }
-    } else if (warp == kMmaWarp || (acc_parts<BN, G>() == 2 && warp == kMmaWarp2)) {
+    } else if (warp == kMmaWarp) {
         // --------------------------------------------------------- MMA issuer
-        // Issuer `part` takes the K steps g (numbered across the CTA's tiles)
-        // with g % parts == part, into accumulator part `part` of the tile's slot.
         if (lane == 0) {
-            constexpr int P = acc_parts<BN, G>();
-            const int part = warp == kMmaWarp ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16(kBW, BN, AT == kBF16);
             RingPos rp, rw;
             int tl = 0;
-            uint32_t g = 0;  // K steps of this CTA so far
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x, ++tl) {
                 const int uses = acc_uses<G>(tl);
-                bool first = true;  // this issuer's first K step of the tile starts its accumulator
-                for (int ks = 0; ks < ksteps && !failed; ++ks, ++g, rp.next(S), rw.next(SW)) {
-                    if (P == 2 && int(g & 1u) != part) continue;
+                for (int ks = 0; ks < ksteps && !failed; ++ks, rp.next(S), rw.next(SW)) {
                     if (!mbar_wait(&full_a[rp.stage], rp.round & 1) || !mbar_wait(&full_w[rw.stage], rw.round & 1)) {
                         failed = true;
                         break;
@@ -347,26 +327,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(wt + rw.stage * plan.w);
 #pragma unroll
-                    for (int gg = 0; gg < G; ++gg) {
-                        const int slot = acc_slot<G>(tl, gg);
-                        if (first && uses > 0) {  // the epilogue has drained this slot's previous tile
+                    for (int g = 0; g < G; ++g) {
+                        const int slot = acc_slot<G>(tl, g);
+                        if (ks == 0 && uses > 0) {  // the epilogue has drained this slot's previous tile
                             if (!mbar_wait(&acc_empty[slot], (uses - 1) & 1)) { failed = true; break; }
                             tc_fence_after();
                         }
-                        const uint32_t d = tmem + (slot * P + part) * BN;
-                        const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act + gg * BN * 128);
+                        const uint32_t d = tmem + slot * BN;
+                        const uint64_t db = smem_desc_sw128(act + rp.stage * plan.act + g * BN * 128);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
-                            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (!first || kk != 0) ? 1u : 0u);
+                            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (ks | kk) != 0);
                     }
                     if (failed) break;
-                    first = false;
                     tc_commit(&empty_w[rw.stage]);  // frees the step's weight slot and activation stage
                 }
                 if (failed) break;
-                // (an issuer with no K step in this tile arrives at once: nothing is pending)
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg) tc_commit(&acc_full[acc_slot<G>(tl, gg)]);
+                for (int g = 0; g < G; ++g) tc_commit(&acc_full[acc_slot<G>(tl, g)]);
             }
         }
     } else if (warp == kPackWarp) {
@@ -666,22 +644,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                 const int64_t m0 = int64_t(x.s0) + g * BN;
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN && c0 < cnt; c0 += 32) {
-                    constexpr int P = acc_parts<BN, G>();
                     uint32_t v[32];
-                    tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + (slot * P) * BN + c0, v);
-                    // part 1 holds the odd K steps of the CTA's sequence: present
-                    // unless the tile has a single K step, an even-numbered one
-                    if (P == 2 && (ksteps > 1 || ((uint32_t(tl) * uint32_t(ksteps)) & 1u) == 1u)) {
-                        uint32_t v1[32];
-                        tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + (slot * P + 1) * BN + c0, v1);
-                        tmem_ld_wait();
-                        const bool only1 = ksteps == 1;  // the single K step went to part 1
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = only1 ? v1[j] : __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
-                    } else {
-                        tmem_ld_wait();
-                    }
+                    tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + slot * BN + c0, v);
+                    tmem_ld_wait();
                     // live columns of this 32-column chunk (a 16-column tile loads 32: the
                     // upper 16 belong to the other accumulator)
                     const int jn = min(32, min(BN - c0, cnt - c0));
@@ -790,10 +755,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // was at or before the group's last step, i.e. stages_w >= kDequantGroups.
 void stages_for(int BN, int G, int bits, int* stages, int* stages_w) {
     static_assert(kWeightSlots >= kDequantGroups, "a parity wait needs a weight slot per group");
-    // activation stages share the weight ring's barriers (<= kWeightSlots), and
-    // their count is even (alternating issuers: see kWeightSlots)
-    int s = std::min(kMaxStagesTC, kWeightSlots) & ~1;
-    while (s > 2 && tc_plan(BN, G, s, kWeightSlots, bits).total > 227 * 1024) s -= 2;
+    int s = std::min(kMaxStagesTC, kWeightSlots);  // activation stages share the weight ring's barriers
+    while (s > 2 && tc_plan(BN, G, s, kWeightSlots, bits).total > 227 * 1024) --s;
     *stages_w = kWeightSlots;
     *stages = s;
 }
@@ -854,10 +817,8 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
-    // two slots of acc_parts accumulators of BN columns; the epilogue reads 32
-    // columns at a time, so a 16-column accumulator needs 16 more behind it
     uint32_t cols = 32;
-    while (cols < 2u * acc_parts<BN, G>() * BN + (BN < 32 ? 32u - BN : 0u)) cols <<= 1;
+    while (cols < 2u * BN) cols <<= 1;
     a.tmem_cols = cols;
     stages_for(BN, G, BITS, &a.stages, &a.stages_w);
     const int64_t smem = tc_plan(BN, G, a.stages, a.stages_w, BITS).total;
