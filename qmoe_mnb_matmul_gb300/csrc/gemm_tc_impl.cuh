@@ -817,8 +817,10 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
+    // two accumulators of BN columns; the epilogue reads 32 columns at a time,
+    // so a 16-column accumulator needs 16 more behind it
     uint32_t cols = 32;
-    while (cols < 2u * BN) cols <<= 1;
+    while (cols < 2u * BN + (BN < 32 ? 32u - BN : 0u)) cols <<= 1;
     a.tmem_cols = cols;
     stages_for(BN, G, BITS, &a.stages, &a.stages_w);
     const int64_t smem = tc_plan(BN, G, a.stages, a.stages_w, BITS).total;
