@@ -403,10 +403,11 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         rpw = rpw <= 2 ? rpw : rpw <= 4 ? 4 : cdiv<int64_t>(rpw, 2) * 2;  // 1, 2, 4, then even
         if (pairs && rpw % 2) ++rpw;  // SwiGLU: every warp slice holds whole gate/up pairs
         while ((rpw * kConsumerWarps) % (pairs ? 2 * align : align) != 0) ++rpw;
-        const int R = force_r ? force_r : rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
+        int R = force_r ? force_r : rpw % 4 == 0 ? 4 : rpw % 2 == 0 ? 2 : 1;
+        if (MT == 4 && R == 4) R = 2;  // four activation rows: at most two weight rows per pass (registers)
         const int64_t RC = rpw * kConsumerWarps;
         const Plan p = make_plan(MT, C, static_cast<int>(RC), row_bytes, nb, ssize, 1);
-        if (rpw <= 8 && !(MT == 4 && R == 4) && p.total <= 100 * 1024) {
+        if (rpw <= 8 && p.total <= 100 * 1024) {
             best.R = R;
             best.rows_per_block = static_cast<int>(RC);
             best.stages = 1;

@@ -4,10 +4,8 @@
 // Its scratch is a file-scope device array of kStaticScratchBytes.  Every GPU
 // that loads this library holds one copy until the process exits.  Host code
 // must not pass the array's name to a kernel (on the host it is only a
-// stand-in for the symbol), so the first call on each device looks up the
-// device address with cudaGetSymbolAddress while that device is current and
-// caches it; every later call on that device reuses the cached address.
-#include <mutex>
+// stand-in for the symbol), so every call looks up the current device's
+// address with cudaGetSymbolAddress.
 
 #include "common.cuh"
 
@@ -15,27 +13,17 @@ namespace mnb {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_qmoe_scratch[kStaticScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of this device's copy of the scratch array (looked up once per device).
+// Device address of the current device's copy of the scratch array.  Looked
+// up on every call (a host-side symbol query, no allocation): a cached address
+// would dangle after a device reset reloads the module.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_qmoe_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorNotSupported;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_qmoe_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
