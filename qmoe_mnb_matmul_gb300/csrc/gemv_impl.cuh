@@ -516,11 +516,11 @@ Shape pick_shape_resident(const GemvArgs& a, int ssize, int sm_count, int64_t mg
     const Shape sh2 = pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, force_r,
                                  a.swiglu != 0, 2);
     if (sh2.prefetch_all) return sh2;  // the small-matrix shape: one CTA per SM
-    // a third CTA only where it keeps the rows per pass (fewer rows per pass
-    // re-read the activation image more often: measured slower than two CTAs)
-    const Shape sh3 = pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, force_r,
+    // a third CTA with the same rows per pass (fewer rows per pass re-read the
+    // activation image more often: measured slower than two CTAs)
+    const Shape sh3 = pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, sh2.R,
                                  a.swiglu != 0, 3);
-    if (sh3.R < sh2.R) return sh2;
+    if (sh3.R != sh2.R) return sh2;
     const Plan p = make_plan(MT, a.chunks, sh3.rows_per_block, a.row_bytes, a.nb, ssize, sh3.stages);
     return resident_ctas_r<BITS, ST, MT, PP>(sh3.R, p.total) >= 3 ? sh3 : sh2;
 }
