@@ -607,7 +607,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-rows", action="store_true", help="skip the prefill GEMM and QMoE measurements")
-    ap.add_argument("--rows", default="", help="comma-separated groups of other rows to run (decode, int3, prepack, gemm, "
+    ap.add_argument("--rows", default="", help="comma-separated groups of other rows to run (step, decode, int3, prepack, gemm, "
                     "qmoe, quant); default all")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run one small fixed invocation for an ncu capture and exit")
@@ -751,6 +751,64 @@ def main():
     if mnb.mnb_get_last_device_error(stream) != 0:
         raise RuntimeError("device error word set during the timed region")
 
+    # ---- the same decode step over the library's other layouts (rows, not the headline):
+    # every weight prepacked once (version-1 layout, prepack not timed), and the
+    # row-local step with each layer's gate and up projections fused with SwiGLU.
+    step_rows = {}
+    if not args.no_other_rows and (not args.rows or "step" in args.rows.split(",")):
+        pp = []
+        for c in calls:
+            n = mnb.mnb_prepack_size(c["N"], c["K"], BITS, BS, mnb.F32, False)
+            buf = torch.empty(n, dtype=torch.uint8, device=dev)
+            pp.append((buf, mnb.mnb_prepack(c["B"], c["S"], None, c["N"], c["K"], BITS, BS, buf, stream=stream)))
+        torch.cuda.synchronize(dev)
+
+        def launch_pp():
+            for c, (buf, desc) in zip(calls, pp):
+                mnb.mnb_matmul_prepacked(c["A"], desc, buf, c["Y"], stream, K=c["K"], M=1)
+        fused = []  # per layer: qkv, o_proj, (gate|up concatenated), down
+        for l in range(wl.QWEN3_1P7B_LAYERS):
+            q, o, gt, up, dn = calls[5 * l:5 * l + 5]
+            Bgu = torch.cat([gt["B"], up["B"]])
+            Sgu = torch.cat([gt["S"], up["S"]])
+            H = torch.empty(gt["N"], dtype=torch.float32, device=dev)
+            fused.append((q, o, dict(A=gt["A"], B=Bgu, S=Sgu, I=gt["N"], K=gt["K"], Y=H), dn))
+
+        def launch_fused():
+            for q, o, gu, dn in fused:
+                launch([q, o], stream)
+                mnb.mnb_gate_up_swiglu(gu["A"], gu["B"], gu["S"], None, gu["I"], BITS, BS, gu["Y"], stream,
+                                       layout=mnb.FC1_CONCAT, K=gu["K"], M=1)
+                launch([dn], stream)
+            launch([head], stream)
+        fused_bytes = sum(proj_bytes(q["K"], q["N"]) + proj_bytes(o["K"], o["N"]) + proj_bytes(dn["K"], dn["N"])
+                          + proj_bytes(gu["K"], 2 * gu["I"]) - gu["I"] * 4 for q, o, gu, dn in fused) + head_bytes
+        for label, fn, nbytes, launches in (("decode_step_prepacked", launch_pp, bytes_step, len(calls)),
+                                            ("decode_step_fused_gate_up", launch_fused, fused_bytes,
+                                             len(calls) - wl.QWEN3_1P7B_LAYERS)):
+            with torch.cuda.stream(stream):
+                fn()
+            torch.cuda.synchronize(dev)
+            gr = capture(fn)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    gr.replay()
+                nst = max(3, min(args.steps, 500))
+                ms_v, clk_v = timed(lambda i: gr.replay(), nst)
+            v = replica_throughput(nbytes, nst, ws, ms_v)
+            step_rows[label] = {
+                "kernel": ("gemv_kernel over the version-1 prepacked layout, " if label.endswith("prepacked")
+                           else "gemv_kernel + gemv_kernel with the SwiGLU epilogue (gate|up fused), ")
+                + f"{launches} launches per step",
+                "shape": "the headline decode step (28 Qwen3-1.7B layers + head, INT4 bs32 fp32, M=1)",
+                "us": ms_v / nst * 1e3, "achieved": v, "unit": UNIT, "peak": peak, "frac": v / ws / peak,
+                "bound": "hbm", "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_step": nbytes,
+                "steps": nst, "clocks": clk_v}
+            del gr
+        if mnb.mnb_get_last_device_error(stream) != 0:
+            raise RuntimeError("device error word set during the layout variants")
+        del pp, fused
+
     if rank != 0:
         return
     out = {
@@ -770,7 +828,8 @@ def main():
                 "ms_per_step": ms_e2e / e2e_steps},
     }
     if not args.no_other_rows:
-        out["other_rows"] = other_rows(torch, mnb, dev, tuple(g for g in args.rows.split(",") if g))
+        out["other_rows"] = dict(step_rows)
+        out["other_rows"].update(other_rows(torch, mnb, dev, tuple(g for g in args.rows.split(",") if g)))
     if ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_sample()
     print(json.dumps(out))
