@@ -176,10 +176,9 @@ mnb_status mnb_gate_up_swiglu(const void* A, mnb_dtype a_dtype, int64_t M, int64
  * content hash): mnb_matmul_prepacked checks the device copy of the header
  * against the descriptor it is given (magic, version, identity and shape), so
  * a buffer re-prepacked for another weight, or overwritten, is refused on the
- * device (MNB_ERR_INVALID_ARG in the device error word, Y left untouched).
- * The check runs beside the row copies (it adds no latency), so the buffer
- * must stay allocated, at least desc->bytes long, while its descriptor is in
- * use; nothing is cached inside the library. */
+ * device (MNB_ERR_INVALID_ARG in the device error word, Y left untouched)
+ * instead of being read as codes.  The buffer stays valid while the caller
+ * keeps it; nothing is cached inside the library. */
 #define MNB_PREPACK_MAGIC 0x50424E4Du /* "MNBP" little-endian */
 #define MNB_PREPACK_VERSION 1u
 #define MNB_PREPACK_HEADER_BYTES 128

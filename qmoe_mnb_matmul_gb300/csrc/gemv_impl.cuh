@@ -119,11 +119,16 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         return static_cast<int>(left < RC ? left : int64_t(RC));
     };
 
+    // prepacked: the producer's verdict on the device header (flag, and a barrier
+    // the consumers wait on once, after staging the activations)
+    volatile int* pp_ok = reinterpret_cast<volatile int*>(smem + 2 * kMaxStages * 8);
+    uint64_t* pp_checked = full + 2 * kMaxStages + 1;
     if (tid == kConsumerWarps * 32) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        if (PP) mbar_init(pp_checked, 1);
         fence_barrier_init();
         // L2 prefetch of this CTA's rows (a hint that reads nothing we use)
         if (b_first < b_last) {
@@ -153,6 +158,19 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
         if (lane != 0) return;
+        if constexpr (PP) {
+            // the device header must describe this weight: a buffer re-prepacked for
+            // another weight, or overwritten, is refused before any code is read
+            // (the consumers stage the activations meanwhile)
+            const mnb_prepacked_desc* h = static_cast<const mnb_prepacked_desc*>(a.pp_header);
+            const bool good = h->magic == MNB_PREPACK_MAGIC && h->version == MNB_PREPACK_VERSION &&
+                              h->identity == a.pp_identity && h->N == a.N && h->K == a.K && h->bits == a.bits &&
+                              h->block_size == a.bs && h->row_stride == a.row_bytes;
+            *pp_ok = good ? 1 : 0;
+            if (!good && blockIdx.x == 0 && blockIdx.y == 0) record_error(MNB_ERR_INVALID_ARG);
+            mbar_arrive(pp_checked);  // releases the flag write
+            if (!good) return;  // no copy issued
+        }
         int st = 0;
         uint32_t round = 0;  // times the ring has wrapped
         for (int blk = b_first; blk < b_last; ++blk) {
@@ -200,17 +218,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     }
 
     // ------------------------------------------------------------ consumers
-    // Prepacked: every consumer warp reads the device header itself (its loads
-    // overlap the staging and the dot products; the verdict is needed only at
-    // the stores).  A header that does not describe this weight (a buffer
-    // re-prepacked for another weight, or overwritten) stores nothing.
-    bool pp_good = true;
-    if constexpr (PP) {
-        const mnb_prepacked_desc* h = static_cast<const mnb_prepacked_desc*>(a.pp_header);
-        pp_good = h->magic == MNB_PREPACK_MAGIC && h->version == MNB_PREPACK_VERSION &&
-                  h->identity == a.pp_identity && h->N == a.N && h->K == a.K && h->bits == a.bits &&
-                  h->block_size == a.bs && h->row_stride == a.row_bytes;
-    }
     const int esz = a.a_dtype == kF32 ? 4 : 2;
     stage_image(
         Q, Corr, MT, C, a.K, a.a_dtype, a.a_vec != 0,
@@ -219,6 +226,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         },
         tid, kConsumerWarps * 32, a.int8a ? 4 * a.bs / 32 : 0);
     consumer_sync();
+    if constexpr (PP) {
+        if (!warp_wait(pp_checked, 0) || !*pp_ok) return;  // refused: nothing was copied, nothing is stored
+    }
 
     const int bs_shift = __ffs(a.bs) - 1;
     // BITS == 0: any width 1..8 given at run time (codes read straight from shared memory)
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                 const float total = warp_sum_transpose<N>(part);
                 if ((lane & (32 / N - 1)) == 0) {
                     const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
-                    if (r0 + r < w_end && m0 + m < a.M && pp_good)
+                    if (r0 + r < w_end && m0 + m < a.M)
                         store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
                 }
             }
@@ -347,7 +357,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         if (lane == 0) mbar_arrive(&empty[st]);
         if (++st == NST) { st = 0; phase ^= 1; }
     }
-    if (PP && !pp_good && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) record_error(MNB_ERR_INVALID_ARG);
 }
 
 int ssize_of(int dt) { return dt == kF32 ? 4 : 2; }
