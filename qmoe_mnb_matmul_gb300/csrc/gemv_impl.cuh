@@ -119,16 +119,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         return static_cast<int>(left < RC ? left : int64_t(RC));
     };
 
-    // prepacked: the producer's verdict on the device header (flag, and a barrier
-    // the consumers wait on once, after staging the activations)
-    volatile int* pp_ok = reinterpret_cast<volatile int*>(smem + 2 * kMaxStages * 8);
-    uint64_t* pp_checked = full + 2 * kMaxStages + 1;
     if (tid == kConsumerWarps * 32) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
-        if (PP) mbar_init(pp_checked, 1);
         fence_barrier_init();
         // L2 prefetch of this CTA's rows (a hint that reads nothing we use)
         if (b_first < b_last) {
@@ -153,24 +148,27 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     // chain runs ahead, no more (letting several run ahead measured slower).
     grid_dependency_wait();
     grid_launch_dependents();
-    __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------- producer
-        if (lane != 0) return;
-        if constexpr (PP) {
-            // the device header must describe this weight: a buffer re-prepacked for
-            // another weight, or overwritten, is refused before any code is read
-            // (the consumers stage the activations meanwhile)
+    if constexpr (PP) {
+        // the device header must describe this weight: a buffer re-prepacked
+        // for another weight, or overwritten, is refused before any code is read
+        volatile int* ok = reinterpret_cast<volatile int*>(smem + 2 * kMaxStages * 8);
+        if (tid == 0) {
             const mnb_prepacked_desc* h = static_cast<const mnb_prepacked_desc*>(a.pp_header);
             const bool good = h->magic == MNB_PREPACK_MAGIC && h->version == MNB_PREPACK_VERSION &&
                               h->identity == a.pp_identity && h->N == a.N && h->K == a.K && h->bits == a.bits &&
                               h->block_size == a.bs && h->row_stride == a.row_bytes;
-            *pp_ok = good ? 1 : 0;
+            *ok = good ? 1 : 0;
             if (!good && blockIdx.x == 0 && blockIdx.y == 0) record_error(MNB_ERR_INVALID_ARG);
-            mbar_arrive(pp_checked);  // releases the flag write
-            if (!good) return;  // no copy issued
         }
+        __syncthreads();
+        if (!*ok) return;  // nothing in flight yet: no copy has been issued
+    } else {
+        __syncthreads();
+    }
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------- producer
+        if (lane != 0) return;
         int st = 0;
         uint32_t round = 0;  // times the ring has wrapped
         for (int blk = b_first; blk < b_last; ++blk) {
@@ -226,9 +224,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         },
         tid, kConsumerWarps * 32, a.int8a ? 4 * a.bs / 32 : 0);
     consumer_sync();
-    if constexpr (PP) {
-        if (!warp_wait(pp_checked, 0) || !*pp_ok) return;  // refused: nothing was copied, nothing is stored
-    }
 
     const int bs_shift = __ffs(a.bs) - 1;
     // BITS == 0: any width 1..8 given at run time (codes read straight from shared memory)
