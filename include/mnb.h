@@ -6,9 +6,11 @@
  * ------------------
  * Pointers.  Every tensor argument is a device pointer owned by the caller,
  * except mnb_validate_host(), which reads host buffers.  The library keeps no
- * state between calls and never repacks weights: packed weights are consumed
- * in the layout below on every call ("Qwen3 Missing-Kernel Implementation
- * Plan", PR sequence rows K01/K02: reuse constant packed weights, no repacking).
+ * state between calls that affects results and never repacks weights on its
+ * own: packed weights are consumed in the layout below on every call ("Qwen3
+ * Missing-Kernel Implementation Plan", PR sequence rows K01/K02: reuse constant
+ * packed weights, no repacking), unless the caller prepacks a weight once into
+ * the opt-in private layout (mnb_prepack, below).
  *
  * Streams.  `stream` is a cudaStream_t (0 = the legacy default stream).  Calls
  * enqueue asynchronous work on it and return without synchronising, except
