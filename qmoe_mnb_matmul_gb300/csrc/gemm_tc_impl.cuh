@@ -256,12 +256,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
     }
     const int ksteps = a.k_steps;
 
-    // FC1 of a QMoE layer: the activation tiles are gathered straight from the
-    // token rows (X[perm[s] / k]) by the whole producer warp with cp.async, each
-    // lane arriving on the stage's barrier when its copies land
-    const bool gather = MODE == kModeFc1 && a.perm != nullptr;
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full_a[s], gather ? 32 : 1);
+        for (int s = 0; s < S; ++s) mbar_init(&full_a[s], 1);
         for (int s = 0; s < SW; ++s) {
             mbar_init(&full_w[s], kDequantWarps);
             mbar_init(&empty_w[s], 1);
@@ -298,48 +294,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
         // have completed: the one commit per K step goes to the weight ring's
         // barrier of that step (`done` walks the weight ring S steps behind).
         // With S <= SW that barrier cannot have moved a phase past the step.
-        if (gather) {
-            // Lane l copies tile rows l, l + 32, ...: row r is routed pair s0 + r,
-            // token perm[s0 + r] / k, and lands in the 128-byte-swizzled layout the
-            // tensor map would have written (16-byte chunk c of row r at sw128(r, c));
-            // rows past the tile and columns past K are zero-filled.
-            constexpr int kRowsPerLane = UN >= 32 ? UN / 32 : 1;
-            const char* X = static_cast<const char*>(a.X);
-            const int64_t row_bytes_x = a.K * 2;
-            RingPos rp, done;
-            for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
-                const Tile x = tile_of(a, t, UN);
-                const char* src[kRowsPerLane];
-                bool live[kRowsPerLane];
-#pragma unroll
-                for (int j = 0; j < kRowsPerLane; ++j) {
-                    const int r = lane + 32 * j;
-                    live[j] = r < UN && r < x.cnt;
-                    src[j] = live[j] ? X + int64_t(a.perm[x.s0 + r] / a.k) * row_bytes_x : X;
-                }
-                for (int ks = 0; ks < ksteps; ++ks, rp.next(S)) {
-                    if (rp.round) {
-                        if (!warp_wait(&empty_w[done.stage], done.round & 1)) { failed = true; break; }
-                        done.next(SW);
-                    }
-                    uint8_t* stage = act + rp.stage * plan.act;
-                    const int64_t k0 = int64_t(x.ks0 + ks) * kBK;  // first column of the step
-#pragma unroll
-                    for (int j = 0; j < kRowsPerLane; ++j) {
-                        const int r = lane + 32 * j;
-                        if (r >= UN) continue;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int64_t col = k0 + 8 * c;
-                            const bool ok = live[j] && col < a.K;
-                            cp_async16_zfill(stage + sw128(r, c), ok ? src[j] + col * 2 : X, ok ? 16u : 0u);
-                        }
-                    }
-                    cp_async_arrive_noinc(&full_a[rp.stage]);
-                }
-            }
-            cp_async_wait<0>();
-        } else if (lane == 0) {
+        if (lane == 0) {
             RingPos rp, done;
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
                 const Tile x = tile_of(a, t, UN);
@@ -369,9 +324,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) gemm_tc_kernel(const __grid_con
                         failed = true;
                         break;
                     }
-                    // gathered activations were written by cp.async (generic proxy): order
-                    // them before the MMA's shared-memory reads (async proxy)
-                    if (gather) fence_proxy_async_smem();
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(wt + rw.stage * plan.w);
 #pragma unroll

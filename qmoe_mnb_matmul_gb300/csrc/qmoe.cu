@@ -601,6 +601,25 @@ __global__ void __launch_bounds__(1024) mtiles_kernel(char* ws, int64_t T, int64
     grid_launch_dependents();
 }
 
+// Xs[s, :] = X[perm[s] / k, :]: the routed tokens' rows in expert-sorted
+// order (tensor-core plan), 16 bytes per thread step (H % 8 == 0, X rows
+// 16-byte aligned), written into the FC2-output region.
+template <typename AT>
+__global__ void gather_rows_kernel(const __grid_constant__ QmoeArgs q) {
+    char* ws = static_cast<char*>(q.workspace);
+    const Ws L = ws_layout(q.T, q.H, q.I, q.E, q.k);
+    const int* perm = reinterpret_cast<const int*>(ws + L.perm);
+    AT* xs = reinterpret_cast<AT*>(ws + L.o);
+    grid_dependency_wait();
+    const int64_t G = q.H / 8, total = q.T * q.k * G;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t srow = i / G, c = (i - srow * G) * 8;
+        const int64_t t = perm[srow] / q.k;
+        *reinterpret_cast<uint4*>(xs + srow * q.H + c) =
+            *reinterpret_cast<const uint4*>(static_cast<const AT*>(q.X) + t * q.H + c);
+    }
+}
+
 // Y[t, n] = sum_j w[t, j] * o[position of (t, j), n], ascending j, fp32 -> act
 // dtype, from FC2 outputs kept in the activation dtype (tensor-core plan).
 // One thread makes 8 consecutive outputs of a token from 16-byte loads of the
@@ -741,9 +760,14 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         a.inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
         a.X = q.X;
         a.bias = q.fc1_bias;
-        // FC1's producer warp gathers the routed tokens' rows straight from X
-        // (a.perm, a.k) into its activation tiles; the tensor map over the
-        // (unused) FC2-output region only satisfies the launcher.
+        // The routed tokens' rows in expert-sorted order go into the FC2-output
+        // region (free until FC2 runs), so FC1 loads them as plain TMA tiles.
+        {
+            using AT = typename DType<ST>::T;
+            const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(P * (q.H / 8), 256), int64_t(sm_count) * 16);
+            gather_rows_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
         if ((e = launch_grouped_tc(true, a, B1, ST, ST, ws + L.o, P, q.H, tile_m, sm_count, pdl, stream)) != cudaSuccess)
             return e;
         // FC2: K = I, H rows; activations are h rows in sorted order (TMA), output o (act dtype, sorted order)
