@@ -155,6 +155,15 @@ def empty_guarded(n: int, dtype: str, guard: int = 64):
     return inner, full
 
 
+def guarded_workspace(nbytes: int, guard: int = 256):
+    """A device workspace of nbytes (256-byte aligned inside) with `guard` sentinel
+    bytes on both sides.  Returns (inner view, full byte buffer); check the sentinels
+    with guards_intact(full, guard)."""
+    import torch
+    full = torch.full((nbytes + 2 * guard,), SENTINEL, dtype=torch.uint8, device="cuda")
+    return full[guard:guard + nbytes], full
+
+
 def guards_intact(full, guard: int = 64) -> bool:
     h = full.cpu().numpy()
     return bool((h[:guard] == SENTINEL).all() and (h[-guard:] == SENTINEL).all())

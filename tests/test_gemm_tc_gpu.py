@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests._util import assert_close, empty_guarded, guards_intact, to_dev, to_f64
+from tests._util import assert_close, empty_guarded, guarded_workspace, guards_intact, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -171,11 +171,13 @@ def test_split_k_against_unsplit(M, K, N, bits, bs):
     A_d, B_d, S_d = to_dev(A, "bf16"), to_dev(packed), to_dev(scales, "bf16")
     Z_d = None if zp is None else to_dev(zp)
     ys = []
-    for ws in (torch.empty(need, dtype=torch.uint8, device="cuda"), torch.empty(0, dtype=torch.uint8, device="cuda")):
+    for nbytes in (need, 0):
+        ws, ws_full = guarded_workspace(nbytes)
         Y, full = empty_guarded(M * N, "f32")
-        mnb.mnb_matmul(A_d, B_d, S_d, Z_d, N, bits, bs, Y, ws, K=K, M=M)
+        mnb.mnb_matmul(A_d, B_d, S_d, Z_d, N, bits, bs, Y, ws, K=K, M=M)  # 0 bytes: no split
         torch.cuda.synchronize()
         assert guards_intact(full), "write outside Y"
+        assert guards_intact(ws_full, 256), "write outside the split-K workspace"
         assert mnb.mnb_get_last_device_error() == 0
         ys.append(to_f64(Y).reshape(M, N))
     ref = oracle.mnb_matmul(A, "bf16", packed, scales, "bf16", zp, N, K, bits, bs, threads=THREADS)

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests._util import assert_close, empty_guarded, guards_intact, to_dev, to_f64
+from tests._util import assert_close, empty_guarded, guarded_workspace, guards_intact, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ def seed(*key):
 
 def run_qmoe(d, T, H, I, E, k, b1, b2, bs, act, layout="interleaved", normalize=True):
     code = {"f16": mnb.F16, "bf16": mnb.BF16}[act]
-    ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, code), dtype=torch.uint8, device="cuda")
+    ws, ws_full = guarded_workspace(mnb.qmoe_workspace_size(T, H, I, E, k, code))
     Y, full = empty_guarded(T * H, act)
     lay = mnb.FC1_INTERLEAVED if layout == "interleaved" else mnb.FC1_CONCAT
     z = lambda a: None if a is None else to_dev(a)
@@ -40,6 +40,7 @@ def run_qmoe(d, T, H, I, E, k, b1, b2, bs, act, layout="interleaved", normalize=
                      z(d["fc2_zp"]), b2, I, bs, Y, ws, fc1_layout=lay)
     torch.cuda.synchronize()
     assert guards_intact(full), "write outside Y"
+    assert guards_intact(ws_full, 256), "write outside the workspace"
     assert mnb.mnb_get_last_device_error() == 0
     return to_f64(Y).reshape(T, H)
 
@@ -211,7 +212,7 @@ def run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x
     """qmoe_forward_ex; x_offset = 1 places X one element past a 16-byte boundary
     (its rows then cannot be read with 16-byte loads: the tiled CUDA-core plan)."""
     code = {"f16": mnb.F16, "bf16": mnb.BF16}[act]
-    ws = torch.empty(mnb.qmoe_workspace_size(T, H, I, E, k, code), dtype=torch.uint8, device="cuda")
+    ws, ws_full = guarded_workspace(mnb.qmoe_workspace_size(T, H, I, E, k, code))
     Y, full = empty_guarded(T * H, act)
     Xbuf = torch.zeros(T * H + 8, dtype=torch.float16 if act == "f16" else torch.bfloat16, device="cuda")
     Xbuf[x_offset:x_offset + T * H] = to_dev(d["X"], act).reshape(-1)
@@ -225,6 +226,7 @@ def run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x
                         fc1_layout=lay, T=T, H=H, E=E, act_dtype=code)
     torch.cuda.synchronize()
     assert guards_intact(full), "write outside Y"
+    assert guards_intact(ws_full, 256), "write outside the workspace"
     assert mnb.mnb_get_last_device_error() == 0
     return to_f64(Y).reshape(T, H)
 
