@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads as wl
-from tests._util import to_dev
+from tests._util import assert_f32_close, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -104,14 +104,15 @@ def test_full_size_expert_stack_sampled_rows():
     assert not bad.any()
     assert np.array_equal(B.reshape(N, -1)[torch.from_numpy(rows).cuda()].cpu().numpy(), P)
     assert np.array_equal(S[torch.from_numpy(rows).cuda()].cpu().view(torch.int16).numpy(), Rs.view(np.int16))
-    # the produced tensors are a valid INT3 projection for the matmul path
-    A = torch.randn((1, K), device="cuda")
+    # the produced tensors are a valid INT3 projection for the matmul path (seeded
+    # activations; the fp32 rule against the oracle's product of the sampled rows)
+    a = wl.normal(g, (1, K), "f32")
+    A = to_dev(a)
     Y = torch.empty((1, N), device="cuda")
     mnb.mnb_matmul(A, B, S.float(), None, N, 3, bs, Y)
     assert mnb.mnb_get_last_device_error() == 0
-    Wd = oracle.dequantize(P, Rs.view(np.uint16), "f16", None, rows.size, K, 3, bs)
-    y_ref = Wd @ A.cpu().double().numpy()[0]
-    assert np.allclose(Y[0, torch.from_numpy(rows).cuda()].cpu().double().numpy(), y_ref, rtol=1e-4, atol=1e-4)
+    y_ref = oracle.mnb_matmul(a, "f32", P, Rs, "f16", None, rows.size, K, 3, bs)
+    assert_f32_close(Y[0, torch.from_numpy(rows).cuda()].cpu().double().numpy()[None, :], y_ref)
 
 
 @pytest.mark.parametrize("w_dtype,s_dtype", [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16"), ("f32", "f16")])
