@@ -150,8 +150,11 @@ cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, 
 // adt, which replace the routing weights of the selected experts.
 cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int normalize,
                          int32_t* idx, float* w, const void* agg, int adt, cudaStream_t stream);
+// One CTA; with mtiles set it also writes the grouped plan's m-tiles of <= tile_m
+// sorted pairs per expert and their count.
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts,
-                           int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
+                           int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream,
+                           int4* mtiles = nullptr, int* n_mtiles = nullptr, int tile_m = 0);
 
 // The same stable permutation over many CTAs: chunk histograms (n_chunks x E
 // ints of scratch in `chunkc`, n_chunks = permute_chunks(T * k)), a scan, and

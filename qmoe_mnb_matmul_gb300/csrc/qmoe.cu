@@ -62,6 +62,8 @@ __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
 // m-tiles of the tensor-core plan: <= tile_m sorted pairs of one expert, tile_m
 // in [32, 256] (grouped_tile_m); the workspace holds enough for the shortest.
 constexpr int kTcTileMin = 32;
+// Routed pairs up to which one CTA sorts the pairs and builds the m-tiles.
+constexpr int64_t kOneCtaPlanPairs = 8192;
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
     const int64_t t = (P + kTcTileMin - 1) / kTcTileMin + E;
     return P < t ? P : t;
@@ -720,16 +722,30 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     if ((e = launch_route(q.logits, q.logits_dtype, q.T, q.E, q.k, q.normalize, idx, wts, q.agg, q.agg_dtype,
                           stream)) != cudaSuccess)
         return e;
-    if ((e = launch_permute_chunked(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.chunkc),
-                                    reinterpret_cast<int32_t*>(ws + L.counts),
-                                    reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
-                                    reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess)
+    // tensor-core plan: tile height from the mean routed rows per expert (FC1 and
+    // FC2 alike); up to kOneCtaPlanPairs routed pairs one CTA sorts them and
+    // writes the m-tiles in one launch (faster than four launches there)
+    const bool tc = use_tc(q);
+    const int tile_m = tc ? grouped_tile_m(P, q.E) : 0;
+    const bool one_cta = tc && P <= kOneCtaPlanPairs && q.E <= 1024;
+    if (one_cta) {
+        if ((e = launch_permute(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.counts),
+                                reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
+                                reinterpret_cast<int32_t*>(ws + L.inv), stream, reinterpret_cast<int4*>(ws + L.mtiles),
+                                reinterpret_cast<int*>(ws + L.nmtiles), tile_m)) != cudaSuccess)
+            return e;
+    } else if ((e = launch_permute_chunked(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.chunkc),
+                                           reinterpret_cast<int32_t*>(ws + L.counts),
+                                           reinterpret_cast<int32_t*>(ws + L.offsets),
+                                           reinterpret_cast<int32_t*>(ws + L.perm),
+                                           reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess) {
         return e;
-    if (use_tc(q)) {
-        // tile height from the mean routed rows per expert (FC1 and FC2 alike)
-        const int tile_m = grouped_tile_m(P, q.E);
-        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (tc) {
+        if (!one_cta) {
+            mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
         TcArgs a = {};
         a.splits = 1;
         a.mtiles = reinterpret_cast<const int4*>(ws + L.mtiles);

@@ -79,11 +79,18 @@ __global__ void route_kernel(const void* __restrict__ logits, int ldt, int64_t T
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
+// With `mtiles` set it also writes the grouped tensor-core plan's m-tiles
+// {expert, first sorted position, rows, 0} of <= tile_m rows per expert and
+// their count (one launch in place of the count / scan / scatter / m-tile
+// kernels, for the pair counts where one CTA is the faster plan).
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ idx, int64_t P,
                                                                int E, int32_t* __restrict__ counts,
                                                                int32_t* __restrict__ offsets,
                                                                int32_t* __restrict__ perm,
-                                                               int32_t* __restrict__ inv_perm) {
+                                                               int32_t* __restrict__ inv_perm,
+                                                               int4* __restrict__ mtiles = nullptr,
+                                                               int* __restrict__ n_mtiles = nullptr,
+                                                               int tile_m = 0) {
     extern __shared__ int32_t cnt[];  // [kPermWarps][E], then tot[E+1]
     int32_t* tot = cnt + kPermWarps * E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -158,6 +165,36 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
             if (inv_perm) inv_perm[p] = slot;
         }
     }
+    if (mtiles == nullptr) return;
+    // m-tiles: expert tid's ceil(count / tile_m) tiles after the tiles of the
+    // experts before it (the same block-wide scan as above)
+    const int ntile = tid < E ? (my_total + tile_m - 1) / tile_m : 0;
+    int32_t y = ntile;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += v;
+    }
+    __syncthreads();  // warp_sums is reused
+    if (lane == 31) warp_sums[warp] = y;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += v;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int32_t tincl = y + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (tid < E) {
+        const int32_t first = tincl - ntile, base = incl - my_total;
+        for (int i = 0; i < ntile; ++i)
+            mtiles[first + i] = make_int4(tid, base + i * tile_m, min(tile_m, my_total - i * tile_m), 0);
+    }
+    if (tid == kPermThreads - 1) *n_mtiles = warp_sums[kPermWarps - 1];
 }
 
 // ------------------------------------------- permutation over many CTAs
@@ -343,13 +380,14 @@ cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int 
 }
 
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
-                           int32_t* perm, int32_t* inv_perm, cudaStream_t stream) {
+                           int32_t* perm, int32_t* inv_perm, cudaStream_t stream, int4* mtiles, int* n_mtiles,
+                           int tile_m) {
     const size_t smem = (size_t(kPermWarps) * E + E + 1) * sizeof(int32_t);
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     permute_kernel<<<1, kPermThreads, smem, stream>>>(idx, T * k, static_cast<int>(E), counts, offsets, perm,
-                                                     inv_perm);
+                                                     inv_perm, mtiles, n_mtiles, tile_m);
     return cudaGetLastError();
 }
 
