@@ -431,7 +431,8 @@ def other_rows(torch, mnb, dev, groups=()):
     torch.cuda.empty_cache()
     # a6-a10: the QMoE layer
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
-    for b1, b2, bs, act, zp, Ts in () if not want("qmoe") else ((3, 3, 64, torch.float16, False, (1, 128, 512, 2048, 4096)),
+    for b1, b2, bs, act, zp, Ts in () if not want("qmoe") else ((3, 3, 64, torch.float16, False,
+                                                                 (1, 16, 128, 512, 2048, 4096)),
                                                                 (4, 4, 32, torch.bfloat16, True, (4096,))):
         code = mnb.F16 if act == torch.float16 else mnb.BF16
         nl = 16
@@ -457,8 +458,15 @@ def other_rows(torch, mnb, dev, groups=()):
             shape = (f"Qwen3-30B-A3B layer, T={T}, top-{k} of {E} ({touched} experts touched), INT{b1}/INT{b2} "
                      f"bs{bs} {'fp16' if act == torch.float16 else 'bf16'}{' + zero points' if zp else ''}, "
                      f"{nl} distinct layers")
-            kern = ("fc1_kernel (decode) + fc2_decode_kernel" if T <= 8 else
-                    "route + permute + grouped gemm_tc FC1 (SwiGLU epilogue) + grouped gemm_tc FC2 + combine")
+            if T == 1:
+                kern = "qmoe_decode_prep_kernel + qmoe_decode_fused_kernel (route, FC1, FC2, combine in one pass)"
+            elif T <= 8:
+                kern = "fc1_kernel (decode) + fc2_decode_kernel"
+            elif 2 * T * k <= 3 * E:  # <= 1.5 routed rows per expert: the grouped CUDA-core plan
+                kern = ("route + permute (m-tiles of <= 4 rows) + gemv_grouped_kernel FC1 (SwiGLU) + "
+                        "gemv_grouped_kernel FC2 + combine")
+            else:
+                kern = "route + permute + grouped gemm_tc FC1 (SwiGLU epilogue) + grouped gemm_tc FC2 + combine"
             if T <= 512:
                 rows[tag] = _row(kern, shape, us, p10, p90, nbytes / (us * 1e-6) / 1e9, "GB/s", hbm, "hbm", hsrc,
                                  bytes_per_layer=nbytes, tflops=flops / (us * 1e-6) / 1e12)

@@ -90,8 +90,13 @@ __device__ __forceinline__ void cta_blocks(int nblk, int x, int gx, int& first, 
 // PP: the weight comes in the prepacked layout (rows of codes, scales and zero
 // points, whole 16-byte units; INT3 chunks regrouped), checked against its
 // device header after the dependency wait.
-template <int BITS, int ST, int MT, int R, bool PP = false>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
+// GR: one projection of a grouped QMoE layer: blockIdx.y is an m-tile of <= MT
+// expert-sorted rows of one expert (read after the dependency wait), whose
+// weight starts e * stride bytes into B, scales and zero points; activation
+// rows come through the routing permutation (FC1) or in sorted order (FC2),
+// output rows are sorted positions, and an optional per-expert bias is added.
+template <int BITS, int ST, int MT, int R, bool PP, bool GR>
+__device__ __forceinline__ void gemv_body(const GemvArgs& a) {
     using S = typename DType<ST>::T;
     // Blocks of RC = 8 * rpw rows: warp w takes rows [w rpw, (w+1) rpw) of
     // every block, R rows at a time (rpw = R for the large matrices; small
@@ -111,7 +116,14 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     uint8_t* Sst = Wst + NST * plan.w_stage;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t m0 = int64_t(blockIdx.y) * MT;
+    // activation / output rows [mbase, mbase + mcnt) (GR: set from the m-tile)
+    int64_t mbase = int64_t(blockIdx.y) * MT;
+    int mcnt = static_cast<int>(min(int64_t(MT), a.M - mbase));
+    // the weight, its scales and zero points (GR: the m-tile's expert)
+    const uint8_t* Bw = a.B;
+    const uint8_t* Sw = static_cast<const uint8_t*>(a.scales);
+    const uint8_t* Zw = a.zp;
+    int ge = 0;
     int b_first, b_last;
     cta_blocks(a.n_blocks, blockIdx.x, gridDim.x, b_first, b_last);
     auto block_rows = [&](int blk) -> int {
@@ -125,8 +137,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             mbar_init(&empty[s], kConsumerWarps);
         }
         fence_barrier_init();
-        // L2 prefetch of this CTA's rows (a hint that reads nothing we use)
-        if (b_first < b_last) {
+        // L2 prefetch of this CTA's rows (a hint that reads nothing we use;
+        // a grouped CTA learns its expert only after the wait)
+        if (!GR && b_first < b_last) {
             const int pf_last = a.prefetch_all ? b_last : min(b_last, b_first + NST);
             const int64_t r0 = int64_t(b_first) * RC, r1 = min(int64_t(pf_last) * RC, a.N);
             const int64_t ss = sizeof(S);
@@ -162,6 +175,28 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
         }
         __syncthreads();
         if (!*ok) return;  // nothing in flight yet: no copy has been issued
+    } else if constexpr (GR) {
+        // [0] expert (-1: no tile), [1] first sorted row, [2] rows, [4 + m] activation row of row m
+        volatile int* gt = reinterpret_cast<volatile int*>(smem + 2 * kMaxStages * 8);
+        if (tid == 0) {
+            int4 t = make_int4(-1, 0, 0, 0);
+            if (static_cast<int>(blockIdx.y) < *a.g_ntiles) t = a.g_tiles[blockIdx.y];
+            gt[0] = t.x;
+            gt[1] = t.y;
+            gt[2] = t.z;
+            for (int m = 0; m < MT; ++m) {
+                const int srow = t.y + (m < t.z ? m : 0);
+                gt[4 + m] = (t.x >= 0 && a.g_perm) ? a.g_perm[srow] / a.g_k : srow;
+            }
+        }
+        __syncthreads();
+        if (gt[0] < 0) return;  // past the device's tile count: nothing issued
+        ge = gt[0];
+        mbase = gt[1];
+        mcnt = gt[2];
+        Bw += int64_t(ge) * a.w_estride;
+        Sw += int64_t(ge) * a.s_estride;
+        if (Zw) Zw += int64_t(ge) * a.z_estride;
     } else {
         __syncthreads();
     }
@@ -194,14 +229,14 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
                 mbar_arrive_expect_tx(&full[st], 2 * (wb + sb));
                 for (int up = 0; up < 2; ++up) {
                     const int64_t r = up * a.pairs + p0;
-                    bulk_g2s(W + up * (RC / 2) * a.row_bytes, a.B + r * a.row_bytes, wb, &full[st]);
-                    bulk_g2s(Sd + up * (RC / 2) * ss, static_cast<const uint8_t*>(a.scales) + r * ss, sb, &full[st]);
+                    bulk_g2s(W + up * (RC / 2) * a.row_bytes, Bw + r * a.row_bytes, wb, &full[st]);
+                    bulk_g2s(Sd + up * (RC / 2) * ss, Sw + r * ss, sb, &full[st]);
                 }
             } else {
                 const int64_t wtot = rc * a.row_bytes, stot = int64_t(rc) * nb * sizeof(S);
                 const uint32_t wb = static_cast<uint32_t>(wtot) & ~15u, sb = static_cast<uint32_t>(stot) & ~15u;
-                const uint8_t* wsrc = a.B + n0 * a.row_bytes;
-                const uint8_t* ssrc = reinterpret_cast<const uint8_t*>(static_cast<const S*>(a.scales) + n0 * nb);
+                const uint8_t* wsrc = Bw + n0 * a.row_bytes;
+                const uint8_t* ssrc = Sw + n0 * nb * int64_t(sizeof(S));
                 // bytes past the last 16-byte multiple of a partial block: plain copies, published by the arrive below
                 if (wb < wtot) copy_bytes(W, wsrc, wb, wtot);
                 if (sb < stot) copy_bytes(Sd, ssrc, sb, stot);
@@ -220,7 +255,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     stage_image(
         Q, Corr, MT, C, a.K, a.a_dtype, a.a_vec != 0,
         [&](int m) -> const void* {
-            return m0 + m < a.M ? static_cast<const char*>(a.A) + (m0 + m) * a.K * esz : nullptr;
+            if constexpr (GR) {
+                if (m >= mcnt) return nullptr;
+                const int64_t row = reinterpret_cast<volatile const int*>(smem + 2 * kMaxStages * 8)[4 + m];
+                return static_cast<const char*>(a.A) + row * a.K * esz;
+            } else {
+                return mbase + m < a.M ? static_cast<const char*>(a.A) + (mbase + m) * a.K * esz : nullptr;
+            }
         },
         tid, kConsumerWarps * 32, a.int8a ? 4 * a.bs / 32 : 0);
     consumer_sync();
@@ -229,129 +270,172 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
     // BITS == 0: any width 1..8 given at run time (codes read straight from shared memory)
     const int bits_rt = BITS ? BITS : a.bits;
     const int kZImplicit = 1 << (bits_rt - 1);
-    int st = 0;
-    uint32_t phase = 0;
-    for (int blk = b_first; blk < b_last; ++blk) {
-        if (!warp_wait(&full[st], phase)) return;
-        const int64_t n0 = int64_t(blk) * RC;
-        const int rc = block_rows(blk);
-        const uint8_t* W = Wst + st * plan.w_stage;
-        const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
-        // this warp's slice of the block, R rows at a time
-        const int w_end = min(rc, (warp + 1) * rpw);
-        for (int r0 = warp * rpw; r0 < w_end; r0 += R) {
-            float acc[R][MT];
+    // The block loop over MTE activation rows of the image (MTE <= MT), RE
+    // weight rows per pass: a grouped CTA runs it at its m-tile's row count, so
+    // a short tile costs no more than its rows.
+    auto consume = [&](auto mte) {
+        constexpr int MTE = decltype(mte)::value;
+        // grouped: four weight rows per pass for short m-tiles (the launch's
+        // blocks hold four rows per warp), two for full ones (registers)
+        constexpr int RE = (GR && MTE <= 2) ? 4 : R;
+        int st = 0;
+        uint32_t phase = 0;
+        for (int blk = b_first; blk < b_last; ++blk) {
+            if (!warp_wait(&full[st], phase)) return;
+            const int64_t n0 = int64_t(blk) * RC;
+            const int rc = block_rows(blk);
+            const uint8_t* W = Wst + st * plan.w_stage;
+            const S* Sc = reinterpret_cast<const S*>(Sst + st * plan.s_stage);
+            // this warp's slice of the block, RE rows at a time
+            const int w_end = min(rc, (warp + 1) * rpw);
+            for (int r0 = warp * rpw; r0 < w_end; r0 += RE) {
+                float acc[RE][MTE];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+                for (int r = 0; r < RE; ++r)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-            const uint8_t* wrow[R];
-            const S* srow[R];
-            const uint8_t* zrow[R];
+                    for (int m = 0; m < MTE; ++m) acc[r][m] = 0.f;
+                const uint8_t* wrow[RE];
+                const S* srow[RE];
+                const uint8_t* zrow[RE];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int rl = min(r0 + r, w_end - 1);  // rows past the slice end recompute its last row
-                // concatenated gate/up: logical row 2i / 2i+1 sits in the gate / up half of the stage
-                const int sl = (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? RC / 2 + (rl >> 1) : (rl >> 1)) : rl;
-                wrow[r] = W + int64_t(sl) * a.row_bytes;
-                if constexpr (PP) {  // the row's scales and zero points follow its codes in the stage
-                    srow[r] = reinterpret_cast<const S*>(wrow[r] + a.pp_scale_off);
-                    zrow[r] = a.pp_zp_off >= 0 ? wrow[r] + a.pp_zp_off : nullptr;
-                } else {
-                    srow[r] = Sc + sl * nb;
-                    const int64_t phys =
-                        (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? a.pairs : 0) + (n0 + rl) / 2 : n0 + rl;
-                    zrow[r] = a.zp ? a.zp + phys * a.zp_row_bytes : nullptr;
-                }
-            }
-            // the chunk loop; HAS_ZP: explicit zero points (a uniform branch, taken once per block)
-            auto chunks = [&](auto has_zp) {
-                for (int c = lane; c < C; c += 32) {
-                    const int b = (c * 32) >> bs_shift;
-                    uint4 q[MT][4];
-                    float p2[MT];
-                    int V[MT];
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const uint4* qp = Q + qbase(m, c, C);
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) q[m][qq] = qp[qq * 32];
-                        const int2 cr = Corr[m * C + c];
-                        V[m] = cr.x;
-                        p2[m] = __int_as_float(cr.y);
+                for (int r = 0; r < RE; ++r) {
+                    const int rl = min(r0 + r, w_end - 1);  // rows past the slice end recompute its last row
+                    // concatenated gate/up: logical row 2i / 2i+1 sits in the gate / up half of the stage
+                    const int sl = (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? RC / 2 + (rl >> 1) : (rl >> 1)) : rl;
+                    wrow[r] = W + int64_t(sl) * a.row_bytes;
+                    if constexpr (PP) {  // the row's scales and zero points follow its codes in the stage
+                        srow[r] = reinterpret_cast<const S*>(wrow[r] + a.pp_scale_off);
+                        zrow[r] = a.pp_zp_off >= 0 ? wrow[r] + a.pp_zp_off : nullptr;
+                    } else {
+                        srow[r] = Sc + sl * nb;
+                        const int64_t phys =
+                            (a.swiglu && !a.fc1_inter) ? ((rl & 1) ? a.pairs : 0) + (n0 + rl) / 2 : n0 + rl;
+                        zrow[r] = Zw ? Zw + phys * a.zp_row_bytes : nullptr;
                     }
+                }
+                // the chunk loop; HAS_ZP: explicit zero points (a uniform branch, taken once per block)
+                auto chunks = [&](auto has_zp) {
+                    for (int c = lane; c < C; c += 32) {
+                        const int b = (c * 32) >> bs_shift;
+                        uint4 q[MTE][4];
+                        float p2[MTE];
+                        int V[MTE];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float sc = to_f32(srow[r][b]);
-                        int z = kZImplicit;
-                        if constexpr (BITS == 0) {
-                            if constexpr (decltype(has_zp)::value) z = zero_point_any(zrow[r], b, bits_rt);
-                            uint32_t lo[4], hi[4];
-                            codes_any(wrow[r] + c * 4 * bits_rt, bits_rt, lo, hi);
+                        for (int m = 0; m < MTE; ++m) {
+                            const uint4* qp = Q + qbase(m, c, C);
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const int T = chunk_dot_bytes(lo, hi, q[m]) - z * V[m];
-                                acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
-                            }
-                        } else {
-                            uint32_t w[BITS];
-                            gemv::load_chunk<BITS>(wrow[r], c, w);
-                            if constexpr (decltype(has_zp)::value) z = gemv::zero_point_code<BITS>(zrow[r], b);
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const int T = chunk_dot<BITS, PP>(w, q[m]) - z * V[m];
-                                acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
-                            }
+                            for (int qq = 0; qq < 4; ++qq) q[m][qq] = qp[qq * 32];
+                            const int2 cr = Corr[m * C + c];
+                            V[m] = cr.x;
+                            p2[m] = __int_as_float(cr.y);
                         }
-                    }
-                }
-            };
-            if (PP ? a.pp_zp_off >= 0 : a.zp != nullptr)
-                chunks(std::true_type{});
-            else
-                chunks(std::false_type{});
-            // value q = r * MT + m; each total ends in one lane
-            if (a.swiglu) {
-                // rows 2i, 2i+1 of the group are the gate and up rows of one pair:
-                // every lane gets every total, lane 0 stores silu(gate) * up
-                if constexpr (R % 2 == 0) {
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
+                        for (int r = 0; r < RE; ++r) {
+                            const float sc = to_f32(srow[r][b]);
+                            int z = kZImplicit;
+                            if constexpr (BITS == 0) {
+                                if constexpr (decltype(has_zp)::value) z = zero_point_any(zrow[r], b, bits_rt);
+                                uint32_t lo[4], hi[4];
+                                codes_any(wrow[r] + c * 4 * bits_rt, bits_rt, lo, hi);
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) acc[r][m] = warp_sum(acc[r][m]);
-                    if (lane == 0) {
+                                for (int m = 0; m < MTE; ++m) {
+                                    const int T = chunk_dot_bytes(lo, hi, q[m]) - z * V[m];
+                                    acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
+                                }
+                            } else {
+                                uint32_t w[BITS];
+                                gemv::load_chunk<BITS>(wrow[r], c, w);
+                                if constexpr (decltype(has_zp)::value) z = gemv::zero_point_code<BITS>(zrow[r], b);
 #pragma unroll
-                        for (int pp = 0; pp < R / 2; ++pp) {
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                if (r0 + 2 * pp + 1 < w_end && m0 + m < a.M) {
-                                    const float gt = acc[2 * pp][m], up = acc[2 * pp + 1][m];
-                                    store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + (n0 + r0) / 2 + pp,
-                                                   gt / (1.0f + expf(-gt)) * up);
+                                for (int m = 0; m < MTE; ++m) {
+                                    const int T = chunk_dot<BITS, PP>(w, q[m]) - z * V[m];
+                                    acc[r][m] = fmaf(sc * p2[m], static_cast<float>(T), acc[r][m]);
                                 }
                             }
                         }
                     }
-                }
-            } else {
-                constexpr int N = R * MT;
-                float part[N];
+                };
+                if (PP ? a.pp_zp_off >= 0 : a.zp != nullptr)
+                    chunks(std::true_type{});
+                else
+                    chunks(std::false_type{});
+                // value q = r * MTE + m; each total ends in one lane
+                if (a.swiglu) {
+                    // rows 2i, 2i+1 of the group are the gate and up rows of one pair:
+                    // every lane gets every total, lane 0 stores silu(gate) * up
+                    if constexpr (RE % 2 == 0) {
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                        for (int r = 0; r < RE; ++r)
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) part[r * MT + m] = acc[r][m];
-                const float total = warp_sum_transpose<N>(part);
-                if ((lane & (32 / N - 1)) == 0) {
-                    const int qv = transpose_row<N>(lane), r = qv / MT, m = qv - r * MT;
-                    if (r0 + r < w_end && m0 + m < a.M)
-                        store_from_f32(a.Y, a.y_dtype, (m0 + m) * a.y_ld + n0 + r0 + r, total);
+                            for (int m = 0; m < MTE; ++m) acc[r][m] = warp_sum(acc[r][m]);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int pp = 0; pp < RE / 2; ++pp) {
+#pragma unroll
+                                for (int m = 0; m < MTE; ++m) {
+                                    if (r0 + 2 * pp + 1 < w_end && (GR ? m < mcnt : mbase + m < a.M)) {
+                                        float gt = acc[2 * pp][m], up = acc[2 * pp + 1][m];
+                                        if constexpr (GR) {
+                                            if (a.bias) {  // rows in the weight's layout, per expert
+                                                const int64_t i = (n0 + r0) / 2 + pp, b0 = int64_t(ge) * 2 * a.pairs;
+                                                gt += load_as_f32(a.bias, a.bias_dtype, b0 + (a.fc1_inter ? 2 * i : i));
+                                                up += load_as_f32(a.bias, a.bias_dtype,
+                                                                  b0 + (a.fc1_inter ? 2 * i + 1 : a.pairs + i));
+                                            }
+                                        }
+                                        store_from_f32(a.Y, a.y_dtype, (mbase + m) * a.y_ld + (n0 + r0) / 2 + pp,
+                                                       gt / (1.0f + expf(-gt)) * up);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    constexpr int N = RE * MTE;
+                    float part[N];
+#pragma unroll
+                    for (int r = 0; r < RE; ++r)
+#pragma unroll
+                        for (int m = 0; m < MTE; ++m) part[r * MTE + m] = acc[r][m];
+                    const float total = warp_sum_transpose<N>(part);
+                    if ((lane & (32 / N - 1)) == 0) {
+                        const int qv = transpose_row<N>(lane), r = qv / MTE, m = qv - r * MTE;
+                        if (r0 + r < w_end && (GR ? m < mcnt : mbase + m < a.M)) {
+                            float y = total;
+                            if constexpr (GR) {
+                                if (a.bias) y += load_as_f32(a.bias, a.bias_dtype, int64_t(ge) * a.N + n0 + r0 + r);
+                            }
+                            store_from_f32(a.Y, a.y_dtype, (mbase + m) * a.y_ld + n0 + r0 + r, y);
+                        }
+                    }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (++st == NST) { st = 0; phase ^= 1; }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (++st == NST) { st = 0; phase ^= 1; }
+    };
+    if constexpr (GR) {
+        if (mcnt == 1)
+            consume(std::integral_constant<int, 1>{});
+        else if (mcnt == 2 && MT > 2)
+            consume(std::integral_constant<int, (MT > 2 ? 2 : MT)>{});
+        else
+            consume(std::integral_constant<int, MT>{});
+    } else {
+        consume(std::integral_constant<int, MT>{});
     }
+}
+
+template <int BITS, int ST, int MT, int R, bool PP = false>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ GemvArgs a) {
+    gemv_body<BITS, ST, MT, R, PP, false>(a);
+}
+
+// The grouped form, held to two CTAs per SM (registers).
+template <int BITS, int ST, int MT, int R>
+__global__ void __launch_bounds__(kThreads, 2) gemv_grouped_kernel(const __grid_constant__ GemvArgs a) {
+    gemv_body<BITS, ST, MT, R, false, true>(a);
 }
 
 int ssize_of(int dt) { return dt == kF32 ? 4 : 2; }

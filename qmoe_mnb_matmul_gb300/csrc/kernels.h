@@ -40,6 +40,19 @@ struct GemvArgs {
     const void* pp_header;
     uint64_t pp_identity;
     int64_t pp_scale_off, pp_zp_off;
+    // grouped QMoE projection (gemv_grouped.cu): CTA row y takes m-tile y of
+    // g_tiles ({expert e, first sorted row, rows, 0}; *g_ntiles of them), whose
+    // weight, scales and zero points start e * w_estride / s_estride / z_estride
+    // bytes into B / scales / zp; the activation of sorted row s is A row
+    // g_perm[s] / g_k (g_perm set) or s; Y rows are sorted rows; bias [E, N]
+    // in bias_dtype (FC1: rows in the weight's gate/up layout) or null
+    const int4* g_tiles;
+    const int* g_ntiles;
+    const int* g_perm;
+    int g_k;
+    int64_t w_estride, s_estride, z_estride;
+    const void* bias;
+    int bias_dtype;
 };
 
 // Chooses the launch shape and enqueues the kernel.  scale_dtype selects the
@@ -47,6 +60,16 @@ struct GemvArgs {
 // when the shape does not fit the kernel's shared-memory plan.
 cudaError_t launch_gemv(const GemvArgs& a, int scale_dtype, int sm_count, bool pdl,
                         cudaStream_t stream);
+
+// The grouped QMoE projection (see the g_* fields): bits 3 or 4, fp16 / bf16
+// scales, up to 4 rows per m-tile; grid_y m-tile slots (CTAs past *g_ntiles
+// exit), est_tiles the expected tile count (sets the CTAs per tile).
+// cudaErrorNotSupported when the shape does not fit the plan.
+cudaError_t launch_gemv_grouped(const GemvArgs& a, int scale_dtype, int64_t grid_y, int64_t est_tiles, int sm_count,
+                                bool pdl, cudaStream_t stream);
+constexpr int kGroupedGemvRows = 4;  // rows of an m-tile of the grouped GEMV
+// Whether the grouped plan takes this projection (bits, scale dtype, shared memory).
+bool gemv_grouped_fits(const GemvArgs& a, int scale_dtype);
 
 // The GEMV over a prepacked weight (a.B, a.row_bytes, a.pp_* set from its
 // descriptor); bits 3 or 4.

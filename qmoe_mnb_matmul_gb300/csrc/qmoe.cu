@@ -59,13 +59,18 @@ __host__ __device__ inline int64_t max_tiles(int64_t P, int64_t E) {
     return P < t ? P : t;
 }
 
-// m-tiles of the tensor-core plan: <= tile_m sorted pairs of one expert, tile_m
-// in [32, 256] (grouped_tile_m); the workspace holds enough for the shortest.
-constexpr int kTcTileMin = 32;
+// m-tiles: <= tile_m sorted pairs of one expert, tile_m in [32, 256] on the
+// tensor-core plan (grouped_tile_m) and kGroupedGemvRows on the grouped CUDA-core
+// plan; the workspace holds enough for the shortest.
+constexpr int kMinTileM = kGroupedGemvRows;
 // Routed pairs up to which one CTA sorts the pairs and builds the m-tiles.
 constexpr int64_t kOneCtaPlanPairs = 8192;
+// Mean routed rows per expert up to which the grouped CUDA-core plan beats the
+// tensor-core plan: 3/2 (30B-A3B layer, INT3: 180 vs 215 us at 1 row per
+// expert, 225 vs 249 us at 1.5, 273 vs 255 us at 2).
+constexpr int64_t kGroupedMeanNum = 3, kGroupedMeanDen = 2;
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
-    const int64_t t = (P + kTcTileMin - 1) / kTcTileMin + E;
+    const int64_t t = (P + kMinTileM - 1) / kMinTileM + E;
     return P < t ? P : t;
 }
 
@@ -95,6 +100,76 @@ bool use_decode(const QmoeArgs& q) { return q.T <= kDecodeMaxT && q.k <= kDecode
 
 // Tensor-core plan: gathered activation rows are read with 16-byte copies.
 bool use_tc(const QmoeArgs& q) { return q.x_vec != 0; }
+
+// The grouped CUDA-core projections of a layer (see gemv_grouped.cu); the
+// caller completes the tile and workspace fields.
+void grouped_args(const QmoeArgs& q, GemvArgs& g1, GemvArgs& g2) {
+    const int64_t I = q.I, H = q.H;
+    g1 = {};
+    g1.A = q.X;
+    g1.a_dtype = q.act_dtype;
+    g1.K = H;
+    g1.B = q.fc1_w;
+    g1.scales = q.fc1_s;
+    g1.zp = q.fc1_zp;
+    g1.N = 2 * I;
+    g1.bits = q.fc1_bits;
+    g1.bs = q.bs;
+    g1.nb = static_cast<int>(q.fc1.nb);
+    g1.row_bytes = q.fc1.row_bytes;
+    g1.zp_row_bytes = static_cast<int>(q.fc1.zp_row);
+    g1.y_dtype = kF32;
+    g1.y_ld = I;
+    g1.chunks = static_cast<int>(q.fc1.nb * q.bs / 32);
+    g1.a_vec = q.x_vec;
+    g1.swiglu = 1;
+    g1.fc1_inter = q.fc1_layout == MNB_FC1_INTERLEAVED;
+    g1.pairs = I;
+    g1.g_k = q.k;
+    g1.w_estride = 2 * I * q.fc1.row_bytes;
+    g1.s_estride = 2 * I * q.fc1.nb * 2;
+    g1.z_estride = 2 * I * q.fc1.zp_row;
+    g1.bias = q.fc1_bias;
+    g1.bias_dtype = q.act_dtype;
+    g2 = {};
+    g2.a_dtype = kF32;  // h
+    g2.K = I;
+    g2.B = q.fc2_w;
+    g2.scales = q.fc2_s;
+    g2.zp = q.fc2_zp;
+    g2.N = H;
+    g2.bits = q.fc2_bits;
+    g2.bs = q.bs;
+    g2.nb = static_cast<int>(q.fc2.nb);
+    g2.row_bytes = q.fc2.row_bytes;
+    g2.zp_row_bytes = static_cast<int>(q.fc2.zp_row);
+    g2.y_dtype = kF32;
+    g2.y_ld = H;
+    g2.chunks = static_cast<int>(q.fc2.nb * q.bs / 32);
+    g2.a_vec = I % 4 == 0;  // h rows start on 16-byte boundaries
+    g2.w_estride = H * q.fc2.row_bytes;
+    g2.s_estride = H * q.fc2.nb * 2;
+    g2.z_estride = H * q.fc2.zp_row;
+    g2.bias = q.fc2_bias;
+    g2.bias_dtype = q.act_dtype;
+}
+
+// Grouped CUDA-core plan: few routed rows per expert (or activation rows the
+// tensor-core plan cannot load), every expert's block start on a 16-byte
+// boundary for the bulk copies, and a shared-memory plan that fits.
+bool use_grouped(const QmoeArgs& q) {
+    const int64_t P = q.T * q.k;
+    if (kGroupedMeanDen * P > kGroupedMeanNum * q.E && q.x_vec) return false;
+    if (max_mtiles(P, q.E) > 65535) return false;
+    const int64_t s1 = q.fc1.nb * 2, s2 = q.fc2.nb * 2;  // scale bytes per row
+    if ((2 * q.I * q.fc1.row_bytes) % 16 || (2 * q.I * s1) % 16 || (q.H * q.fc2.row_bytes) % 16 || (q.H * s2) % 16)
+        return false;
+    // concatenated gate/up halves are copied as separate row ranges
+    if (q.fc1_layout != MNB_FC1_INTERLEAVED && (q.fc1.row_bytes % 16 || s1 % 16)) return false;
+    GemvArgs g1, g2;
+    grouped_args(q, g1, g2);
+    return gemv_grouped_fits(g1, q.act_dtype) && gemv_grouped_fits(g2, q.act_dtype);
+}
 
 // --------------------------------------------------------- shared memory
 
@@ -314,7 +389,6 @@ __global__ void __launch_bounds__(kThreads) fc1_kernel(const __grid_constant__ Q
             for (int pp = 0; pp < 2; ++pp) {
                 const int pq = 2 * g + pp;
                 if (pq >= pc) break;
-#pragma unroll
                 const int64_t pa = pair0 + pq;  // bias rows of the gate and up halves of pair pa
                 const float bg = bias_at(q.fc1_bias, q.act_dtype, int64_t(e) * 2 * I + (inter ? 2 * pa : pa));
                 const float bu = bias_at(q.fc1_bias, q.act_dtype, int64_t(e) * 2 * I + (inter ? 2 * pa + 1 : I + pa));
@@ -521,7 +595,6 @@ __global__ void __launch_bounds__(kThreads) fc2_tile_kernel(const __grid_constan
             for (int r = 0; r < R; ++r) {
                 const int rl = g * R + r;
                 if (rl >= rc) break;
-#pragma unroll
                 const float b2 = bias_at(q.fc2_bias, q.act_dtype, int64_t(e) * H + n0 + rl);
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
@@ -722,12 +795,14 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     if ((e = launch_route(q.logits, q.logits_dtype, q.T, q.E, q.k, q.normalize, idx, wts, q.agg, q.agg_dtype,
                           stream)) != cudaSuccess)
         return e;
-    // tensor-core plan: tile height from the mean routed rows per expert (FC1 and
-    // FC2 alike); up to kOneCtaPlanPairs routed pairs one CTA sorts them and
-    // writes the m-tiles in one launch (faster than four launches there)
-    const bool tc = use_tc(q);
-    const int tile_m = tc ? grouped_tile_m(P, q.E) : 0;
-    const bool one_cta = tc && P <= kOneCtaPlanPairs && q.E <= 1024;
+    // m-tile plans (grouped CUDA-core, tensor-core): tile height kGroupedGemvRows,
+    // or from the mean routed rows per expert (FC1 and FC2 alike); up to
+    // kOneCtaPlanPairs routed pairs one CTA sorts them and writes the m-tiles in
+    // one launch (faster than four launches there)
+    const bool grouped = use_grouped(q);
+    const bool tc = !grouped && use_tc(q);
+    const int tile_m = grouped ? kGroupedGemvRows : tc ? grouped_tile_m(P, q.E) : 0;
+    const bool one_cta = (grouped || tc) && P <= kOneCtaPlanPairs && q.E <= 1024;
     if (one_cta) {
         if ((e = launch_permute(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.counts),
                                 reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
@@ -741,11 +816,30 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
                                            reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess) {
         return e;
     }
+    if ((grouped || tc) && !one_cta) {
+        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (grouped) {
+        // FC1 + SwiGLU -> h (fp32, sorted rows), FC2 -> o (fp32, sorted rows), combine
+        GemvArgs g1, g2;
+        grouped_args(q, g1, g2);
+        g1.g_tiles = g2.g_tiles = reinterpret_cast<const int4*>(ws + L.mtiles);
+        g1.g_ntiles = g2.g_ntiles = reinterpret_cast<const int*>(ws + L.nmtiles);
+        g1.g_perm = reinterpret_cast<const int*>(ws + L.perm);
+        g1.Y = ws + L.h;
+        g2.A = ws + L.h;
+        g2.Y = ws + L.o;
+        // expected m-tiles: every touched expert's last tile is partial
+        const int64_t grid_y = max_mtiles(P, q.E);
+        const int64_t est = std::min(grid_y, P / kGroupedGemvRows + std::min(P, q.E) / 2);
+        if ((e = launch_gemv_grouped(g1, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
+        if ((e = launch_gemv_grouped(g2, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
+        const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), int64_t(sm_count) * 16);
+        combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
+        return cudaGetLastError();
+    }
     if (tc) {
-        if (!one_cta) {
-            mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        }
         TcArgs a = {};
         a.splits = 1;
         a.mtiles = reinterpret_cast<const int4*>(ws + L.mtiles);

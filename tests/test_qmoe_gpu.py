@@ -1,8 +1,15 @@
 """GPU parity of qmoe_forward (routing, FC1 + SwiGLU, FC2, combine) against the
 oracle, through the C ABI.  Outputs are fp16 / bf16: the elementwise rule
-|y - r| <= 1e-2 + 2e-2 |r|, except bf16 layers on the tensor-core plan (T > 8),
-which take the bf16 tensor-core rule and print their elementwise misses
-(tests/_util.py).  Sampled prefill checks cover at least 64 tokens."""
+|y - r| <= 1e-2 + 2e-2 |r|, except bf16 layers with T > 8 (which may run on the
+tensor-core plan), which take the bf16 tensor-core rule and print their
+elementwise misses (tests/_util.py); the grouped CUDA-core plan's own tests
+hold it to the elementwise rule.  Sampled prefill checks cover at least 64
+tokens.  Plans: one token -> the single-pass layer; T <= 8 -> the two-kernel
+decode; up to 1.5 routed rows per expert on average, or X rows off a 16-byte
+boundary -> the grouped CUDA-core plan (m-tiles of <= 4 rows, one GEMV ring per
+expert block); more -> the tensor-core plan; the tiled CUDA-core plan takes
+what the grouped plan cannot (concatenated gate/up rows whose bytes or scales
+are not whole 16-byte units, with X rows off a 16-byte boundary)."""
 import os
 import zlib
 
@@ -231,13 +238,14 @@ def run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x
     return to_f64(Y).reshape(T, H)
 
 
-@pytest.mark.parametrize("T,x_offset", [(1, 0), (3, 0), (40, 0), (20, 1)])
+@pytest.mark.parametrize("T,x_offset", [(1, 0), (3, 0), (12, 0), (40, 0), (20, 1)])
 @pytest.mark.parametrize("opts", ["biases", "agg", "half_logits", "all"])
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
 def test_optional_inputs_every_plan(T, x_offset, opts, layout):
     """FC1/FC2 biases, aggregation weights and 16-bit router logits on every plan: the
-    single-pass layer (T = 1), the two-kernel decode (T = 3), the tensor-core plan
-    (T = 40) and the tiled CUDA-core plan (X rows off a 16-byte boundary)."""
+    single-pass layer (T = 1), the two-kernel decode (T = 3), the grouped CUDA-core
+    plan (T = 12: 1.5 routed rows per expert; T = 20 with X rows off a 16-byte
+    boundary) and the tensor-core plan (T = 40: 5 rows per expert)."""
     H, I, E, k, bs, b1, b2 = 512, 256, 32, 4, 64, 3, 4
     act = "bf16" if T % 2 else "f16"
     g = wl.rng(seed("opts", T, x_offset, opts, layout))
@@ -253,3 +261,42 @@ def test_optional_inputs_every_plan(T, x_offset, opts, layout):
     ref = oracle.qmoe_ex(d["X"], act, d["logits"], ldt, k, True, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], b1v, b1,
                          d["fc2_w"], d["fc2_scales"], d["fc2_zp"], b2v, b2, I, bs, layout, agg=agg, threads=THREADS)
     check(y, ref, act, T if x_offset == 0 else 1, f"opts={opts} T={T} layout={layout}")
+
+
+# ---------------------------------------------------- grouped CUDA-core plan
+
+@pytest.mark.parametrize("T,E,k,layout,bits,bs,act,zp,x_offset", [
+    (16, 128, 8, "interleaved", (3, 3), 64, "bf16", True, 0),   # 1 routed row per expert on average
+    (12, 32, 4, "concat", (4, 3), 32, "f16", False, 0),          # 1.5: the largest mean it takes
+    (24, 32, 2, "interleaved", (4, 4), 128, "bf16", True, 0),
+    (9, 1, 1, "concat", (3, 4), 64, "f16", True, 1),             # one expert: 3 m-tiles, the last of 1 row
+    (300, 8, 2, "interleaved", (3, 4), 64, "f16", True, 1),      # X off 16 bytes: any mean (75 rows per expert)
+    (50, 64, 6, "concat", (3, 3), 64, "bf16", True, 1),
+])
+def test_grouped_plan(T, E, k, layout, bits, bs, act, zp, x_offset):
+    """The grouped CUDA-core plan (exact dp4a chunk sums, fp32 accumulation) against
+    the oracle under the elementwise 16-bit rule, both FC1 layouts, zero points,
+    skewed routing (ragged m-tiles) and biases."""
+    b1, b2 = bits
+    H, I = 1024, 512
+    g = wl.rng(seed("grouped", T, E, k, layout, bits, bs, act, zp, x_offset))
+    d = wl.moe_layer(g, T, H, I, E, b1, b2, bs, act, with_zp=zp, skew=True)
+    b1v, b2v = wl.normal(g, (E, 2 * I), act), wl.normal(g, (E, H), act)
+    y = run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, None, "f32", x_offset)
+    ref = oracle.qmoe_ex(d["X"], act, d["logits"], "f32", k, True, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], b1v, b1,
+                         d["fc2_w"], d["fc2_scales"], d["fc2_zp"], b2v, b2, I, bs, layout, threads=THREADS)
+    check(y, ref, act, 1)  # CUDA cores: the elementwise rule
+
+
+@pytest.mark.parametrize("layout,H,bs", [("concat", 64, 32), ("concat", 96, 32)])
+def test_tiled_plan_fallback(layout, H, bs):
+    """Concatenated gate/up rows of less than 16 scale bytes with X rows off a
+    16-byte boundary: the grouped plan cannot copy such row ranges, the tiled
+    CUDA-core plan runs."""
+    T, E, k, I = 20, 8, 2, 64
+    g = wl.rng(seed("tiled-fallback", layout, H, bs))
+    d = wl.moe_layer(g, T, H, I, E, 4, 3, bs, "f16", with_zp=True, skew=True)
+    y = run_qmoe_ex(d, T, H, I, E, k, 4, 3, bs, "f16", layout, None, None, None, "f32", 1)
+    ref = oracle.qmoe_ex(d["X"], "f16", d["logits"], "f32", k, True, d["fc1_w"], d["fc1_scales"], d["fc1_zp"], None, 4,
+                         d["fc2_w"], d["fc2_scales"], d["fc2_zp"], None, 3, I, bs, layout, threads=THREADS)
+    check(y, ref, "f16", 1)
