@@ -432,7 +432,7 @@ def other_rows(torch, mnb, dev, groups=()):
     # a6-a10: the QMoE layer
     H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
     for b1, b2, bs, act, zp, Ts in () if not want("qmoe") else ((3, 3, 64, torch.float16, False,
-                                                                 (1, 16, 128, 512, 2048, 4096)),
+                                                                 (1, 8, 16, 128, 512, 2048, 4096)),
                                                                 (4, 4, 32, torch.bfloat16, True, (4096,))):
         code = mnb.F16 if act == torch.float16 else mnb.BF16
         nl = 16
@@ -454,13 +454,15 @@ def other_rows(torch, mnb, dev, groups=()):
             us, p10, p90 = graph_time(torch, stream, calls, reps=30 if T <= 512 else 5)
             flops = T * k * (2 * H * 2 * I + 2 * I * H)
             nbytes = touched * per_expert + T * H * 2 * 2 + T * E * 4
-            tag = f"qmoe_{'decode' if T == 1 else 'prefill'}_t{T}" + ("" if act == torch.float16 else "_bf16_zp44")
+            # one token: decode; a few (batched decode): batch; more: prefill
+            phase = "decode" if T == 1 else "batch" if T <= 16 else "prefill"
+            tag = f"qmoe_{phase}_t{T}" + ("" if act == torch.float16 else "_bf16_zp44")
             shape = (f"Qwen3-30B-A3B layer, T={T}, top-{k} of {E} ({touched} experts touched), INT{b1}/INT{b2} "
                      f"bs{bs} {'fp16' if act == torch.float16 else 'bf16'}{' + zero points' if zp else ''}, "
                      f"{nl} distinct layers")
             if T == 1:
                 kern = "qmoe_decode_prep_kernel + qmoe_decode_fused_kernel (route, FC1, FC2, combine in one pass)"
-            elif T <= 8:
+            elif T <= 2:
                 kern = "fc1_kernel (decode) + fc2_decode_kernel"
             elif 2 * T * k <= 3 * E:  # <= 1.5 routed rows per expert: the grouped CUDA-core plan
                 kern = ("route + permute (m-tiles of <= 4 rows) + gemv_grouped_kernel FC1 (SwiGLU) + "
@@ -499,8 +501,8 @@ def other_rows(torch, mnb, dev, groups=()):
     return rows
 
 
-PROFILE_CASES = ("gemv_head", "gemv_head_int3", "gemm_tc_gate", "qmoe_decode", "qmoe_prefill", "qmoe_prefill_t128",
-                 "quantize_int3", "decode_chain")
+PROFILE_CASES = ("gemv_head", "gemv_head_int3", "gemm_tc_gate", "qmoe_decode", "qmoe_batch_t16", "qmoe_prefill",
+                 "qmoe_prefill_t128", "quantize_int3", "decode_chain")
 
 
 def decode_chain(torch, mnb, dev):
@@ -588,7 +590,7 @@ def profile_case(name):
             torch.cuda.synchronize()
             del W
     else:  # one Qwen3-30B-A3B-shaped QMoE layer, INT3/INT3 bs64 fp16
-        T = 1 if name == "qmoe_decode" else 128 if name == "qmoe_prefill_t128" else 4096
+        T = {"qmoe_decode": 1, "qmoe_batch_t16": 16, "qmoe_prefill_t128": 128}.get(name, 4096)
         H, I, E, k = MOE["H"], MOE["I"], MOE["E"], MOE["k"]
         nl = 16 if T == 1 else 2
         layers = make_moe_layers(torch, dev, nl, 3, 3, 64, gen)

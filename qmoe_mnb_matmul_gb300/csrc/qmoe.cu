@@ -6,24 +6,31 @@
 // ever written to global memory ("prohibit all-expert floating-weight
 // materialization").
 //
-// Three plans:
-//  * decode (T <= 8, k <= 8), SIMT, on the packed-row machinery of
-//    gemv_core.cuh: two kernels.  Every CTA routes its own token (the whole
-//    CTA ranks up to 256 logits at once), so no routing kernel sits on the
-//    critical path.  FC1 runs over (token, slot) x row blocks of the selected
-//    expert and writes h = silu(gate) * up in fp32.  FC2 runs over tokens x
-//    row blocks, stages the block's rows of all k selected experts and folds
-//    the weighted combine into its epilogue (fixed slot order).  Both are
-//    launched as programmatic dependents: before its dependency wait each CTA
-//    routes and starts the bulk copies of its expert rows into shared memory.
-//  * tensor-core (T > 8, 16-byte-aligned fp16/bf16 activation rows): route ->
-//    expert-sorted permutation over many CTAs -> m-tiles of <= 256 routed rows
+// Plans:
+//  * decode (one token, or two; k <= 8), SIMT, on the packed-row machinery of
+//    gemv_core.cuh: one token takes the fused single-pass kernel
+//    (qmoe_decode.cu) where its shape rules allow, else two kernels.  Every CTA
+//    routes its own token (the whole CTA ranks up to 256 logits at once), so
+//    no routing kernel sits on the critical path.  FC1 runs over (token, slot)
+//    x row blocks of the selected expert and writes h = silu(gate) * up in
+//    fp32.  FC2 runs over tokens x row blocks, stages the block's rows of all k
+//    selected experts and folds the weighted combine into its epilogue (fixed
+//    slot order).  Both are launched as programmatic dependents: before its
+//    dependency wait each CTA routes and starts the bulk copies of its expert
+//    rows into shared memory.
+//  * grouped CUDA-core (3 or more tokens with at most 1.5 routed rows per
+//    expert on average, or X rows off a 16-byte boundary; gemv_grouped.cu):
+//    route -> permutation -> m-tiles of <= 4 sorted rows of one expert -> FC1
+//    (+SwiGLU) and FC2 as GEMV rings over each tile's expert -> combine by
+//    token in fixed slot order.
+//  * tensor-core (more rows per expert, 16-byte-aligned fp16/bf16 activation
+//    rows): route -> expert-sorted permutation -> m-tiles of <= 256 routed rows
 //    of one expert -> the routed rows copied into sorted order -> grouped
 //    tcgen05 FC1 (SwiGLU in the epilogue) -> grouped FC2 -> combine by token
 //    in fixed slot order.
-//  * tiled SIMT (any T, the remaining cases): route -> permutation -> tiles of
-//    <= 4 pairs of one expert -> FC1 tiles (gathered activations) -> FC2 tiles
-//    -> combine by token in fixed slot order.
+//  * tiled SIMT (what neither of the last two takes): route -> permutation ->
+//    tiles of <= 4 pairs of one expert -> FC1 tiles (gathered activations) ->
+//    FC2 tiles -> combine by token in fixed slot order.
 #include <algorithm>
 
 #include "common.cuh"
@@ -69,6 +76,7 @@ constexpr int64_t kOneCtaPlanPairs = 8192;
 // tensor-core plan: 3/2 (30B-A3B layer, INT3: 180 vs 215 us at 1 row per
 // expert, 225 vs 249 us at 1.5, 273 vs 255 us at 2).
 constexpr int64_t kGroupedMeanNum = 3, kGroupedMeanDen = 2;
+constexpr int64_t kGroupedMinT = 3;
 __host__ __device__ inline int64_t max_mtiles(int64_t P, int64_t E) {
     const int64_t t = (P + kMinTileM - 1) / kMinTileM + E;
     return P < t ? P : t;
@@ -778,7 +786,11 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     const int C2 = static_cast<int>(q.fc2.nb * q.bs / 32);
     const unsigned gy2 = static_cast<unsigned>(cdiv<int64_t>(q.H, kRowsPerBlock2));
     cudaError_t e;
-    if (use_decode(q)) {
+    // From kGroupedMinT tokens on the grouped CUDA-core plan beats the two-kernel
+    // decode plan (one copy of each touched expert per m-tile rather than per
+    // routed pair: 30B-A3B layer, INT3, T = 4: 55 vs 69 us, T = 8: 83 vs 131 us;
+    // T = 2: 42 vs 37 us).
+    if (use_decode(q) && !(q.T >= kGroupedMinT && use_grouped(q))) {
         // one token: the fused single-pass kernel (qmoe_decode.cu) where its shape rules allow
         if (q.T == 1) {
             e = launch_qmoe_decode_fused(q, sm_count, pdl, stream);

@@ -4,8 +4,9 @@ oracle, through the C ABI.  Outputs are fp16 / bf16: the elementwise rule
 tensor-core plan), which take the bf16 tensor-core rule and print their
 elementwise misses (tests/_util.py); the grouped CUDA-core plan's own tests
 hold it to the elementwise rule.  Sampled prefill checks cover at least 64
-tokens.  Plans: one token -> the single-pass layer; T <= 8 -> the two-kernel
-decode; up to 1.5 routed rows per expert on average, or X rows off a 16-byte
+tokens.  Plans: one token -> the single-pass layer; two tokens (and up to 8
+where the grouped plan does not apply) -> the two-kernel decode; from 3 tokens
+with up to 1.5 routed rows per expert on average, or X rows off a 16-byte
 boundary -> the grouped CUDA-core plan (m-tiles of <= 4 rows, one GEMV ring per
 expert block); more -> the tensor-core plan; the tiled CUDA-core plan takes
 what the grouped plan cannot (concatenated gate/up rows whose bytes or scales
@@ -84,6 +85,8 @@ def test_int3_decode_layer():
 @pytest.mark.parametrize("T", [1, 2, 5, 8])
 @pytest.mark.parametrize("bits", [(3, 3), (3, 4), (4, 3), (4, 4)])
 def test_decode_plan(T, bits):
+    """T = 1: the single-pass layer; T = 2: the two-kernel decode; T = 5, 8: the
+    grouped CUDA-core plan (under one routed row per expert)."""
     b1, b2 = bits
     H, I, E, k, bs = 1024, 512, 64, 8, 64
     act = "bf16" if T % 2 else "f16"
@@ -96,7 +99,8 @@ def test_decode_plan(T, bits):
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
 @pytest.mark.parametrize("normalize", [True, False])
 def test_decode_layouts_and_blocks(bs, layout, normalize):
-    H, I, E, k, T = 512, 256, 32, 4, 3
+    """The two-kernel decode plan (T = 2): both FC1 layouts, every block size."""
+    H, I, E, k, T = 512, 256, 32, 4, 2
     d = wl.moe_layer(wl.rng(seed("lay", bs, layout, normalize)), T, H, I, E, 3, 4, bs, "f16", with_zp=True)
     y = run_qmoe(d, T, H, I, E, k, 3, 4, bs, "f16", layout, normalize)
     check(y, reference(d, k, 3, 4, I, bs, "f16", layout, normalize), "f16", T)
@@ -238,12 +242,12 @@ def run_qmoe_ex(d, T, H, I, E, k, b1, b2, bs, act, layout, b1v, b2v, agg, ldt, x
     return to_f64(Y).reshape(T, H)
 
 
-@pytest.mark.parametrize("T,x_offset", [(1, 0), (3, 0), (12, 0), (40, 0), (20, 1)])
+@pytest.mark.parametrize("T,x_offset", [(1, 0), (2, 0), (12, 0), (40, 0), (20, 1)])
 @pytest.mark.parametrize("opts", ["biases", "agg", "half_logits", "all"])
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
 def test_optional_inputs_every_plan(T, x_offset, opts, layout):
     """FC1/FC2 biases, aggregation weights and 16-bit router logits on every plan: the
-    single-pass layer (T = 1), the two-kernel decode (T = 3), the grouped CUDA-core
+    single-pass layer (T = 1), the two-kernel decode (T = 2), the grouped CUDA-core
     plan (T = 12: 1.5 routed rows per expert; T = 20 with X rows off a 16-byte
     boundary) and the tensor-core plan (T = 40: 5 rows per expert)."""
     H, I, E, k, bs, b1, b2 = 512, 256, 32, 4, 64, 3, 4
