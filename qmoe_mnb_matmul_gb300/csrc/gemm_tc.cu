@@ -142,6 +142,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
         if (plan.splits == 1) continue;
         const int64_t MN = g.M * g.N;
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(MN, 256), int64_t(sm_count) * 8);
+        if ((e = set_max_carveout(splitk_reduce_kernel)) != cudaSuccess) return e;
         splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.partials, plan.splits, MN, g.Y,
                                                                                g.y_dtype, pass);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

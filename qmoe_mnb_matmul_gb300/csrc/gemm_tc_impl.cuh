@@ -825,7 +825,7 @@ cudaError_t launch_cfg(const TcArgs& in, const void* A_rows, int64_t a_rows, int
     stages_for(BN, G, BITS, &a.stages, &a.stages_w);
     const int64_t smem = tc_plan(BN, G, a.stages, a.stages_w, BITS).total;
     auto kern = gemm_tc_kernel<BITS, ST, AT, BN, G, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(std::max(grid, 1)), 1, 1);

@@ -51,7 +51,7 @@ cudaError_t launch_grouped_typed(GemvArgs a, int64_t grid_y, int64_t est_tiles, 
     const int64_t want = (2 * int64_t(sm_count) + std::max<int64_t>(est_tiles, 1) / 2) / std::max<int64_t>(est_tiles, 1);
     const int64_t gx = std::max<int64_t>(1, std::min<int64_t>(want, a.n_blocks));
     auto kern = gemv_grouped_kernel<BITS, ST, kGroupedGemvRows, kGroupedR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(g.smem));
+    cudaError_t e = set_kernel_smem(kern, g.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(grid_y), 1);

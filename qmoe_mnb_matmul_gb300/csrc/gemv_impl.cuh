@@ -530,6 +530,7 @@ Shape pick_shape(int64_t N, int64_t row_bytes, int nb, int ssize, int MT, int C,
         }
     }
     best.prefetch_all = small;
+    if (best_cost < 0) best.stages = 0;  // no row count fits this many CTAs per SM
     return best;
 }
 
@@ -541,9 +542,9 @@ cudaError_t launch_typed(GemvArgs a, const Shape& sh, bool pdl, cudaStream_t str
     a.stages = sh.stages;
     a.prefetch_all = sh.prefetch_all ? 1 : 0;
     const Plan p = make_plan(MT, a.chunks, sh.rows_per_block, a.row_bytes, a.nb, ssize, sh.stages);
-    if (p.total > kSmemBudget) return cudaErrorNotSupported;
+    if (sh.stages < 1 || p.total > kSmemBudget) return cudaErrorNotSupported;
     auto kern = gemv_kernel<BITS, ST, MT, R, PP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.total));
+    cudaError_t e = set_kernel_smem(kern, p.total);
     if (e != cudaSuccess) return e;
     const int64_t mgroups = cdiv<int64_t>(a.M, MT);
     cudaLaunchConfig_t cfg = {};
@@ -570,8 +571,7 @@ int resident_ctas(int64_t smem) {
     if (it != cache.end()) return it->second;
     auto kern = gemv_kernel<BITS, ST, MT, R, PP>;
     int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess ||
+    if (set_kernel_smem(kern, smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, static_cast<size_t>(smem)) != cudaSuccess)
         n = 0;
     cache.emplace(smem, n);
@@ -604,7 +604,7 @@ Shape pick_shape_resident(const GemvArgs& a, int ssize, int sm_count, int64_t mg
     // activation image more often: measured slower than two CTAs)
     const Shape sh3 = pick_shape(a.N, a.row_bytes, a.nb, ssize, MT, a.chunks, sm_count, mgroups, sh2.R,
                                  a.swiglu != 0, 3);
-    if (sh3.R != sh2.R) return sh2;
+    if (sh3.stages == 0 || sh3.R != sh2.R) return sh2;
     const Plan p = make_plan(MT, a.chunks, sh3.rows_per_block, a.row_bytes, a.nb, ssize, sh3.stages);
     return resident_ctas_r<BITS, ST, MT, PP>(sh3.R, p.total) >= 3 ? sh3 : sh2;
 }

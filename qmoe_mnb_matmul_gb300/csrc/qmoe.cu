@@ -755,7 +755,7 @@ __global__ void combine_sorted_kernel(const __grid_constant__ QmoeArgs q, int y_
 template <typename Kern>
 cudaError_t launch(Kern kern, dim3 grid, int64_t smem, cudaStream_t stream, const QmoeArgs& q, bool pdl) {
     if (smem > 227 * 1024) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -829,6 +829,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         return e;
     }
     if ((grouped || tc) && !one_cta) {
+        if ((e = set_max_carveout(mtiles_kernel)) != cudaSuccess) return e;
         mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -848,6 +849,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         if ((e = launch_gemv_grouped(g1, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
         if ((e = launch_gemv_grouped(g2, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), int64_t(sm_count) * 16);
+        if ((e = set_max_carveout(combine_kernel)) != cudaSuccess) return e;
         combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
         return cudaGetLastError();
     }
@@ -887,6 +889,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         {
             using AT = typename DType<ST>::T;
             const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(P * (q.H / 8), 256), int64_t(sm_count) * 16);
+            if ((e = set_max_carveout(gather_rows_kernel<AT>)) != cudaSuccess) return e;
             gather_rows_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
@@ -914,9 +917,11 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H / 8, 256), int64_t(sm_count) * 16);
         using AT = typename DType<ST>::T;
         const int y_vec = (reinterpret_cast<uintptr_t>(q.Y) & 15) == 0;
+        if ((e = set_max_carveout(combine_sorted_kernel<AT>)) != cudaSuccess) return e;
         combine_sorted_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, y_vec);
         return cudaGetLastError();
     }
+    if ((e = set_max_carveout(tiles_kernel)) != cudaSuccess) return e;
     tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
@@ -924,6 +929,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     const Fc2Plan p2 = fc2_plan(kRowsPerBlock2, kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2, false);
     if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q, pdl)) != cudaSuccess) return e;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), 152 * 16);
+    if ((e = set_max_carveout(combine_kernel)) != cudaSuccess) return e;
     combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
     return cudaGetLastError();
 }

@@ -397,11 +397,13 @@ cudaError_t launch_typed(const QmoeArgs& q, int grid, int64_t smem, int64_t h_of
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, qmoe_decode_prep_kernel, reinterpret_cast<unsigned int*>(ws + sync_off));
+        cudaError_t e = set_max_carveout(qmoe_decode_prep_kernel);
+        if (e != cudaSuccess) return e;
+        e = cudaLaunchKernelEx(&cfg, qmoe_decode_prep_kernel, reinterpret_cast<unsigned int*>(ws + sync_off));
         if (e != cudaSuccess) return e;
     }
     auto kern = qmoe_decode_fused_kernel<B1, B2, ST>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(kern, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // <= one CTA per SM

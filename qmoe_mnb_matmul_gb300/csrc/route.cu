@@ -336,9 +336,12 @@ cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t
     const int64_t P = T * k;
     const int64_t n = permute_chunks(P);
     const size_t hist = size_t(E) * sizeof(int32_t);
+    cudaError_t e;
+    if ((e = set_max_carveout(perm_count_kernel)) != cudaSuccess || (e = set_max_carveout(perm_scan_kernel)) != cudaSuccess ||
+        (e = set_max_carveout(perm_scatter_kernel)) != cudaSuccess)
+        return e;
     perm_count_kernel<<<static_cast<unsigned>(n), kPermChunk, hist, stream>>>(idx, P, static_cast<int>(E), chunkc);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     perm_scan_kernel<<<1, kScanThreads, 0, stream>>>(chunkc, static_cast<int>(n), static_cast<int>(E), counts, offsets);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t whist = size_t(kPermChunk / 32) * E * sizeof(int32_t);
@@ -374,6 +377,8 @@ cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int 
                          float* w, const void* agg, int adt, cudaStream_t stream) {
     const int warps = 8;
     const int64_t blocks = cdiv<int64_t>(T, warps);
+    const cudaError_t e = set_max_carveout(route_kernel);
+    if (e != cudaSuccess) return e;
     route_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(logits, ldt, T, static_cast<int>(E), k,
                                                                             normalize, idx, w, agg, adt);
     return cudaGetLastError();
@@ -383,8 +388,7 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int3
                            int32_t* perm, int32_t* inv_perm, cudaStream_t stream, int4* mtiles, int* n_mtiles,
                            int tile_m) {
     const size_t smem = (size_t(kPermWarps) * E + E + 1) * sizeof(int32_t);
-    cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_kernel_smem(permute_kernel, static_cast<int64_t>(smem));
     if (e != cudaSuccess) return e;
     permute_kernel<<<1, kPermThreads, smem, stream>>>(idx, T * k, static_cast<int>(E), counts, offsets, perm,
                                                      inv_perm, mtiles, n_mtiles, tile_m);
