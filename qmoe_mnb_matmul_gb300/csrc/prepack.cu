@@ -108,6 +108,8 @@ cudaError_t launch_prepack(const uint8_t* B, const void* scales, int scale_dtype
     const int64_t z_row = zp ? cdiv<int64_t>(nb * bits, 8) : 0;
     const int64_t items = N * (C + (row_stride - int64_t(C) * 4 * bits) / 4);
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(cdiv<int64_t>(items, 256), int64_t(sm_count) * 8));
+    const cudaError_t e = set_max_carveout(prepack_kernel);
+    if (e != cudaSuccess) return e;
     prepack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         B, static_cast<const uint8_t*>(scales), zp, N, C, bits, row_bytes, s_row, z_row, dst, row_stride, scale_off,
         zp_off, h);

@@ -195,9 +195,17 @@ cudaError_t launch_wd(const void* W, int64_t chunks, int cpb, int s_dtype, void*
                       cudaStream_t stream) {
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(chunks, kQuantThreads), int64_t(sm_count) * 8);
     const dim3 grid(static_cast<unsigned>(std::max<int64_t>(blocks, 1)));
-    if (s_dtype == kF32) quantize_int3_kernel<WD, kF32><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
-    else if (s_dtype == kF16) quantize_int3_kernel<WD, kF16><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
-    else quantize_int3_kernel<WD, kBF16><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
+    cudaError_t e;
+    if (s_dtype == kF32) {
+        if ((e = set_max_carveout(quantize_int3_kernel<WD, kF32>)) != cudaSuccess) return e;
+        quantize_int3_kernel<WD, kF32><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
+    } else if (s_dtype == kF16) {
+        if ((e = set_max_carveout(quantize_int3_kernel<WD, kF16>)) != cudaSuccess) return e;
+        quantize_int3_kernel<WD, kF16><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
+    } else {
+        if ((e = set_max_carveout(quantize_int3_kernel<WD, kBF16>)) != cudaSuccess) return e;
+        quantize_int3_kernel<WD, kBF16><<<grid, kQuantThreads, 0, stream>>>(W, chunks, cpb, S, B);
+    }
     return cudaGetLastError();
 }
 

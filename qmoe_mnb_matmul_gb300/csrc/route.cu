@@ -357,6 +357,8 @@ cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, 
     const int64_t total = rows * K;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(total, threads), 65535 * 16);
+    const cudaError_t e = set_max_carveout(unpack_kernel);
+    if (e != cudaSuccess) return e;
     unpack_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(
         packed, rows, K, bits, row_bytes, codes);
     return cudaGetLastError();
@@ -368,6 +370,8 @@ cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int
     const int64_t row_bytes = nb * bs * bits / 8;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(rows * row_bytes, threads), 65535 * 16);
+    const cudaError_t e = set_max_carveout(pack_kernel);
+    if (e != cudaSuccess) return e;
     pack_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), threads, 0, stream>>>(codes, rows, K, bits,
                                                                                            row_bytes, packed);
     return cudaGetLastError();
