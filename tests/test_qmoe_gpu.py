@@ -123,7 +123,10 @@ def test_one_token_single_pass(layout, bs, bits, E, k):
 @pytest.mark.parametrize("T,E,k,skew", [(9, 64, 8, True), (64, 128, 8, True), (33, 16, 2, False), (40, 8, 8, False),
                                         (12, 1, 1, False), (20, 256, 10, True)])
 @pytest.mark.parametrize("bits", [(3, 3), (4, 3)])
-def test_tiled_plan(T, E, k, skew, bits):
+def test_small_prefill_layers(T, E, k, skew, bits):
+    """Small layers past the decode range: the grouped CUDA-core plan where the
+    routed rows average at most 1.5 per expert (T=9 of 64 experts, T=20 of 256),
+    the tensor-core plan elsewhere (one expert, two, eight, sixteen)."""
     b1, b2 = bits
     H, I, bs = 512, 256, 64
     d = wl.moe_layer(wl.rng(seed("tiled", T, E, k, bits)), T, H, I, E, b1, b2, bs, "bf16", with_zp=skew, skew=skew)
@@ -133,8 +136,8 @@ def test_tiled_plan(T, E, k, skew, bits):
 
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
 @pytest.mark.parametrize("I,bits", [(128, 4), (96, 4), (96, 3)])
-def test_tiled_plan_layouts(layout, I, bits):
-    """Both FC1 row layouts; I = 96 leaves the last weight tile of each expert
+def test_tensor_core_plan_layouts(layout, I, bits):
+    """The tensor-core plan (12.5 routed rows per expert) in both FC1 row layouts; I = 96 leaves the last weight tile of each expert
     half empty (its gate and up rows are read as two 64-row tiles in the
     concatenated layout)."""
     H, E, k, T, bs = 256, 16, 4, 50, 32
