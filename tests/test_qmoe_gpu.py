@@ -295,6 +295,18 @@ def test_grouped_plan(T, E, k, layout, bits, bs, act, zp, x_offset):
     check(y, ref, act, 1)  # CUDA cores: the elementwise rule
 
 
+@pytest.mark.parametrize("T,E,k,layout", [(4, 1024, 8, "concat"), (5, 300, 6, "interleaved"), (3, 8, 1, "concat")])
+def test_grouped_plan_router_sizes(T, E, k, layout):
+    """The grouped CUDA-core plan from three tokens on: the largest router (E = 1024,
+    one-CTA permutation with its m-tiles), an E that is not a power of two, and a
+    single expert per token."""
+    H, I, bs = 256, 128, 32
+    g = wl.rng(seed("grouped-router", T, E, k, layout))
+    d = wl.moe_layer(g, T, H, I, E, 3, 3, bs, "bf16", with_zp=True, skew=False)
+    y = run_qmoe(d, T, H, I, E, k, 3, 3, bs, "bf16", layout)
+    check(y, reference(d, k, 3, 3, I, bs, "bf16", layout), "bf16", 1)  # CUDA cores: the elementwise rule
+
+
 @pytest.mark.parametrize("layout,H,bs", [("concat", 64, 32), ("concat", 96, 32)])
 def test_tiled_plan_fallback(layout, H, bs):
     """Concatenated gate/up rows of less than 16 scale bytes with X rows off a
