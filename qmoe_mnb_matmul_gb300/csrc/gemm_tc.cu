@@ -143,9 +143,9 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& g, int scale_dtype, int sm_count, b
         const int64_t MN = g.M * g.N;
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(MN, 256), int64_t(sm_count) * 8);
         if ((e = set_max_carveout(splitk_reduce_kernel)) != cudaSuccess) return e;
-        splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.partials, plan.splits, MN, g.Y,
-                                                                               g.y_dtype, pass);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_ex(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl,
+                           static_cast<const float*>(a.partials), plan.splits, MN, g.Y, g.y_dtype, pass)) != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }

@@ -4,7 +4,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mnb {
+
+// Enqueues kern<<<grid, block, smem, stream>>>(args...), as a programmatic
+// dependent of the work ahead on the stream when `pdl`: the kernel may then
+// start while its predecessor finishes, so it must not read anything the
+// predecessor writes before its own griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------- SIMT GEMV
 // Y[M, N] = A[M, K] . W^T for small M, streaming packed rows through shared memory.
@@ -171,20 +193,23 @@ cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, 
 // ------------------------------------------------------------- routing
 // logits [T, E] in dtype ldt; agg (or null): [T, E] aggregation weights in dtype
 // adt, which replace the routing weights of the selected experts.
+// `pdl`: these launches may start while the work ahead finishes (each kernel
+// reads its inputs only after its dependency wait).
 cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int normalize,
-                         int32_t* idx, float* w, const void* agg, int adt, cudaStream_t stream);
+                         int32_t* idx, float* w, const void* agg, int adt, cudaStream_t stream, bool pdl = false);
 // One CTA; with mtiles set it also writes the grouped plan's m-tiles of <= tile_m
 // sorted pairs per expert and their count.
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream,
-                           int4* mtiles = nullptr, int* n_mtiles = nullptr, int tile_m = 0);
+                           int4* mtiles = nullptr, int* n_mtiles = nullptr, int tile_m = 0, bool pdl = false);
 
 // The same stable permutation over many CTAs: chunk histograms (n_chunks x E
 // ints of scratch in `chunkc`, n_chunks = permute_chunks(T * k)), a scan, and
 // a scatter.  E <= 1024.
 int64_t permute_chunks(int64_t P);
 cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* chunkc, int32_t* counts,
-                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream);
+                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream,
+                                   bool pdl = false);
 
 // Per-translation-unit device error words (read and cleared; 0 = none).
 cudaError_t gemv_take_error(unsigned int* out);

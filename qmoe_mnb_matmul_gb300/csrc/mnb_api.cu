@@ -485,7 +485,7 @@ mnb_status qmoe_route(const float* logits, int64_t T, int64_t E, int k, int norm
     int64_t tmp;
     if (!mul_ok(T, E * 4, &tmp) || T > (int64_t(1) << 31)) return MNB_ERR_SIZE_OVERFLOW;
     return from_cuda(launch_route(logits, MNB_F32, T, E, k, normalize_topk ? 1 : 0, topk_idx, topk_w, nullptr,
-                                  MNB_F32, reinterpret_cast<cudaStream_t>(stream)));
+                                  MNB_F32, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
 }
 
 mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
@@ -494,8 +494,8 @@ mnb_status qmoe_permute(const int32_t* topk_idx, int64_t T, int k, int64_t E, in
     if (T < 1 || k < 1 || E < 1 || k > E) return MNB_ERR_INVALID_ARG;
     if (E > 1024) return MNB_ERR_UNSUPPORTED;
     if (T * int64_t(k) >= (int64_t(1) << 31)) return MNB_ERR_SIZE_OVERFLOW;
-    return from_cuda(
-        launch_permute(topk_idx, T, k, E, counts, offsets, perm, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_permute(topk_idx, T, k, E, counts, offsets, perm, nullptr,
+                                    reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, 0, pdl_enabled()));
 }
 
 // ------------------------------------------------------------------- QMoE

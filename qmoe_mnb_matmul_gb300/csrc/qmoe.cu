@@ -648,6 +648,7 @@ __global__ void combine_kernel(const __grid_constant__ QmoeArgs q) {
     const float* wts = reinterpret_cast<const float*>(ws + L.wts);
     const int* inv = reinterpret_cast<const int*>(ws + L.inv);
     grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t total = q.T * q.H;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = i / q.H, n = i - t * q.H;
@@ -694,6 +695,7 @@ __global__ void gather_rows_kernel(const __grid_constant__ QmoeArgs q) {
     const int* perm = reinterpret_cast<const int*>(ws + L.perm);
     AT* xs = reinterpret_cast<AT*>(ws + L.o);
     grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t G = q.H / 8, total = q.T * q.k * G;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t srow = i / G, c = (i - srow * G) * 8;
@@ -728,6 +730,7 @@ __global__ void combine_sorted_kernel(const __grid_constant__ QmoeArgs q, int y_
     const float* wts = reinterpret_cast<const float*>(ws + L.wts);
     const int* inv = reinterpret_cast<const int*>(ws + L.inv);
     grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t G = q.H / 8, total = q.T * G;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t t = i / G, n0 = (i - t * G) * 8;
@@ -805,7 +808,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
     int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
     float* wts = reinterpret_cast<float*>(ws + L.wts);
     if ((e = launch_route(q.logits, q.logits_dtype, q.T, q.E, q.k, q.normalize, idx, wts, q.agg, q.agg_dtype,
-                          stream)) != cudaSuccess)
+                          stream, pdl)) != cudaSuccess)
         return e;
     // m-tile plans (grouped CUDA-core, tensor-core): tile height kGroupedGemvRows,
     // or from the mean routed rows per expert (FC1 and FC2 alike); up to
@@ -819,19 +822,20 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         if ((e = launch_permute(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.counts),
                                 reinterpret_cast<int32_t*>(ws + L.offsets), reinterpret_cast<int32_t*>(ws + L.perm),
                                 reinterpret_cast<int32_t*>(ws + L.inv), stream, reinterpret_cast<int4*>(ws + L.mtiles),
-                                reinterpret_cast<int*>(ws + L.nmtiles), tile_m)) != cudaSuccess)
+                                reinterpret_cast<int*>(ws + L.nmtiles), tile_m, pdl)) != cudaSuccess)
             return e;
     } else if ((e = launch_permute_chunked(idx, q.T, q.k, q.E, reinterpret_cast<int32_t*>(ws + L.chunkc),
                                            reinterpret_cast<int32_t*>(ws + L.counts),
                                            reinterpret_cast<int32_t*>(ws + L.offsets),
                                            reinterpret_cast<int32_t*>(ws + L.perm),
-                                           reinterpret_cast<int32_t*>(ws + L.inv), stream)) != cudaSuccess) {
+                                           reinterpret_cast<int32_t*>(ws + L.inv), stream, pdl)) != cudaSuccess) {
         return e;
     }
     if ((grouped || tc) && !one_cta) {
         if ((e = set_max_carveout(mtiles_kernel)) != cudaSuccess) return e;
-        mtiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k, tile_m);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_ex(mtiles_kernel, dim3(1), dim3(1024), 0, stream, pdl, ws, q.T, q.H, q.I, q.E, q.k, tile_m)) !=
+            cudaSuccess)
+            return e;
     }
     if (grouped) {
         // FC1 + SwiGLU -> h (fp32, sorted rows), FC2 -> o (fp32, sorted rows), combine
@@ -850,8 +854,7 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         if ((e = launch_gemv_grouped(g2, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
         const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), int64_t(sm_count) * 16);
         if ((e = set_max_carveout(combine_kernel)) != cudaSuccess) return e;
-        combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
-        return cudaGetLastError();
+        return launch_ex(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl, q);
     }
     if (tc) {
         TcArgs a = {};
@@ -890,8 +893,9 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
             using AT = typename DType<ST>::T;
             const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(P * (q.H / 8), 256), int64_t(sm_count) * 16);
             if ((e = set_max_carveout(gather_rows_kernel<AT>)) != cudaSuccess) return e;
-            gather_rows_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if ((e = launch_ex(gather_rows_kernel<AT>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl,
+                               q)) != cudaSuccess)
+                return e;
         }
         if ((e = launch_grouped_tc(true, a, B1, ST, ST, ws + L.o, P, q.H, tile_m, sm_count, pdl, stream)) != cudaSuccess)
             return e;
@@ -918,20 +922,19 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         using AT = typename DType<ST>::T;
         const int y_vec = (reinterpret_cast<uintptr_t>(q.Y) & 15) == 0;
         if ((e = set_max_carveout(combine_sorted_kernel<AT>)) != cudaSuccess) return e;
-        combine_sorted_kernel<AT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, y_vec);
-        return cudaGetLastError();
+        return launch_ex(combine_sorted_kernel<AT>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl, q,
+                         y_vec);
     }
     if ((e = set_max_carveout(tiles_kernel)) != cudaSuccess) return e;
-    tiles_kernel<<<1, 1024, 0, stream>>>(ws, q.T, q.H, q.I, q.E, q.k);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_ex(tiles_kernel, dim3(1), dim3(1024), 0, stream, pdl, ws, q.T, q.H, q.I, q.E, q.k)) != cudaSuccess)
+        return e;
     const unsigned gx = static_cast<unsigned>(max_tiles(P, q.E));
     if ((e = launch_fc1<B1, ST, kTileM, false>(q, gx, stream, pdl)) != cudaSuccess) return e;
     const Fc2Plan p2 = fc2_plan(kRowsPerBlock2, kTileM, C2, q.fc2.row_bytes, static_cast<int>(q.fc2.nb), 2, false);
     if ((e = launch(fc2_tile_kernel<B2, ST, kTileM>, dim3(gx, gy2, 1), p2.total, stream, q, pdl)) != cudaSuccess) return e;
     const int64_t blocks = std::min<int64_t>(cdiv<int64_t>(q.T * q.H, 256), 152 * 16);
     if ((e = set_max_carveout(combine_kernel)) != cudaSuccess) return e;
-    combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q);
-    return cudaGetLastError();
+    return launch_ex(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl, q);
 }
 
 template <int ST>

@@ -63,6 +63,7 @@ __global__ void route_kernel(const void* __restrict__ logits, int ldt, int64_t T
                              int32_t* __restrict__ idx, float* __restrict__ wout, const void* agg, int adt) {
     const int64_t t = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5);
     grid_dependency_wait();
+    grid_launch_dependents();
     if (t >= T) return;
     const int esz = ldt == kF32 ? 4 : 2, asz = adt == kF32 ? 4 : 2;
     warp_route(static_cast<const char*>(logits) + t * E * esz, ldt, E, k, normalize, idx + t * k, wout + t * k, 1,
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
     int32_t* tot = cnt + kPermWarps * E;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();
+    grid_launch_dependents();
     for (int i = tid; i < kPermWarps * E; i += kPermThreads) cnt[i] = 0;
     __syncthreads();
     const int64_t seg = (P + kPermWarps - 1) / kPermWarps;
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_count_kernel(const int32_t* _
                                                                 int32_t* __restrict__ chunkc) {
     extern __shared__ int32_t hist[];
     grid_dependency_wait();
+    grid_launch_dependents();
     for (int e = threadIdx.x; e < E; e += kPermChunk) hist[e] = 0;
     __syncthreads();
     const int64_t p = int64_t(blockIdx.x) * kPermChunk + threadIdx.x;
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(kScanThreads) perm_scan_kernel(int32_t* __rest
     const int per = (n_chunks + parts - 1) / parts;
     const int c0 = part * per, c1 = min(n_chunks, c0 + per);
     grid_dependency_wait();
+    grid_launch_dependents();
     int32_t sum = 0;
     if (active) {
         for (int c = c0; c < c1; c += kScanBatch) {
@@ -303,6 +307,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
     extern __shared__ int32_t whist[];  // [kWarps][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();
+    grid_launch_dependents();
     for (int i = tid; i < kWarps * E; i += kPermChunk) whist[i] = 0;
     __syncthreads();
     const int64_t p = int64_t(blockIdx.x) * kPermChunk + tid;
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
 int64_t permute_chunks(int64_t P) { return (P + kPermChunk - 1) / kPermChunk; }
 
 cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* chunkc, int32_t* counts,
-                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream) {
+                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, cudaStream_t stream, bool pdl) {
     const int64_t P = T * k;
     const int64_t n = permute_chunks(P);
     const size_t hist = size_t(E) * sizeof(int32_t);
@@ -340,14 +345,16 @@ cudaError_t launch_permute_chunked(const int32_t* idx, int64_t T, int k, int64_t
     if ((e = set_max_carveout(perm_count_kernel)) != cudaSuccess || (e = set_max_carveout(perm_scan_kernel)) != cudaSuccess ||
         (e = set_max_carveout(perm_scatter_kernel)) != cudaSuccess)
         return e;
-    perm_count_kernel<<<static_cast<unsigned>(n), kPermChunk, hist, stream>>>(idx, P, static_cast<int>(E), chunkc);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    perm_scan_kernel<<<1, kScanThreads, 0, stream>>>(chunkc, static_cast<int>(n), static_cast<int>(E), counts, offsets);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_ex(perm_count_kernel, dim3(static_cast<unsigned>(n)), dim3(kPermChunk), hist, stream, pdl, idx, P,
+                       static_cast<int>(E), chunkc)) != cudaSuccess)
+        return e;
+    if ((e = launch_ex(perm_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, pdl, chunkc, static_cast<int>(n),
+                       static_cast<int>(E), counts, offsets)) != cudaSuccess)
+        return e;
     const size_t whist = size_t(kPermChunk / 32) * E * sizeof(int32_t);
-    perm_scatter_kernel<<<static_cast<unsigned>(n), kPermChunk, whist, stream>>>(idx, P, static_cast<int>(E), chunkc,
-                                                                                 offsets, perm, inv_perm);
-    return cudaGetLastError();
+    return launch_ex(perm_scatter_kernel, dim3(static_cast<unsigned>(n)), dim3(kPermChunk), whist, stream, pdl, idx, P,
+                     static_cast<int>(E), static_cast<const int32_t*>(chunkc), static_cast<const int32_t*>(offsets),
+                     perm, inv_perm);
 }
 
 cudaError_t launch_unpack_codes(const uint8_t* packed, int64_t rows, int64_t K, int bits, int bs,
@@ -378,25 +385,23 @@ cudaError_t launch_pack_codes(const uint8_t* codes, int64_t rows, int64_t K, int
 }
 
 cudaError_t launch_route(const void* logits, int ldt, int64_t T, int64_t E, int k, int normalize, int32_t* idx,
-                         float* w, const void* agg, int adt, cudaStream_t stream) {
+                         float* w, const void* agg, int adt, cudaStream_t stream, bool pdl) {
     const int warps = 8;
     const int64_t blocks = cdiv<int64_t>(T, warps);
     const cudaError_t e = set_max_carveout(route_kernel);
     if (e != cudaSuccess) return e;
-    route_kernel<<<static_cast<unsigned>(blocks), warps * 32, 0, stream>>>(logits, ldt, T, static_cast<int>(E), k,
-                                                                            normalize, idx, w, agg, adt);
-    return cudaGetLastError();
+    return launch_ex(route_kernel, dim3(static_cast<unsigned>(blocks)), dim3(warps * 32), 0, stream, pdl, logits, ldt, T,
+                     static_cast<int>(E), k, normalize, idx, w, agg, adt);
 }
 
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* counts, int32_t* offsets,
                            int32_t* perm, int32_t* inv_perm, cudaStream_t stream, int4* mtiles, int* n_mtiles,
-                           int tile_m) {
+                           int tile_m, bool pdl) {
     const size_t smem = (size_t(kPermWarps) * E + E + 1) * sizeof(int32_t);
     cudaError_t e = set_kernel_smem(permute_kernel, static_cast<int64_t>(smem));
     if (e != cudaSuccess) return e;
-    permute_kernel<<<1, kPermThreads, smem, stream>>>(idx, T * k, static_cast<int>(E), counts, offsets, perm,
-                                                     inv_perm, mtiles, n_mtiles, tile_m);
-    return cudaGetLastError();
+    return launch_ex(permute_kernel, dim3(1), dim3(kPermThreads), smem, stream, pdl, idx, T * k, static_cast<int>(E),
+                     counts, offsets, perm, inv_perm, mtiles, n_mtiles, tile_m);
 }
 
 }  // namespace mnb
