@@ -847,7 +847,8 @@ cudaError_t run_typed(const QmoeArgs& q, int sm_count, bool pdl, cudaStream_t st
         g1.Y = ws + L.h;
         g2.A = ws + L.h;
         g2.Y = ws + L.o;
-        // expected m-tiles: every touched expert's last tile is partial
+        // expected m-tile count (it sets the CTAs per tile): the P / 4 full tiles
+        // plus a partial last tile for about every second touched expert
         const int64_t grid_y = max_mtiles(P, q.E);
         const int64_t est = std::min(grid_y, P / kGroupedGemvRows + std::min(P, q.E) / 2);
         if ((e = launch_gemv_grouped(g1, q.act_dtype, grid_y, est, sm_count, pdl, stream)) != cudaSuccess) return e;
