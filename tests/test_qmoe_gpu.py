@@ -120,18 +120,20 @@ def test_one_token_single_pass(layout, bs, bits, E, k):
     check(y, reference(d, k, b1, b2, I, bs, "bf16", layout), "bf16", 1)
 
 
-@pytest.mark.parametrize("T,E,k,skew", [(9, 64, 8, True), (64, 128, 8, True), (33, 16, 2, False), (40, 8, 8, False),
-                                        (12, 1, 1, False), (20, 256, 10, True)])
+@pytest.mark.parametrize("T,E,k,skew,cuda_cores", [(9, 64, 8, True, True), (64, 128, 8, True, False),
+                                                   (33, 16, 2, False, False), (40, 8, 8, False, False),
+                                                   (12, 1, 1, False, False), (20, 256, 10, True, True)])
 @pytest.mark.parametrize("bits", [(3, 3), (4, 3)])
-def test_small_prefill_layers(T, E, k, skew, bits):
+def test_small_prefill_layers(T, E, k, skew, cuda_cores, bits):
     """Small layers past the decode range: the grouped CUDA-core plan where the
-    routed rows average at most 1.5 per expert (T=9 of 64 experts, T=20 of 256),
-    the tensor-core plan elsewhere (one expert, two, eight, sixteen)."""
+    routed rows average at most 1.5 per expert (T=9 of 64 experts, T=20 of 256;
+    held to the elementwise rule), the tensor-core plan elsewhere (one expert,
+    two, eight, sixteen)."""
     b1, b2 = bits
     H, I, bs = 512, 256, 64
     d = wl.moe_layer(wl.rng(seed("tiled", T, E, k, bits)), T, H, I, E, b1, b2, bs, "bf16", with_zp=skew, skew=skew)
     y = run_qmoe(d, T, H, I, E, k, b1, b2, bs, "bf16")
-    check(y, reference(d, k, b1, b2, I, bs, "bf16"), "bf16", T, f"T={T} E={E} k={k} bits={bits}")
+    check(y, reference(d, k, b1, b2, I, bs, "bf16"), "bf16", 1 if cuda_cores else T, f"T={T} E={E} k={k} bits={bits}")
 
 
 @pytest.mark.parametrize("layout", ["interleaved", "concat"])
